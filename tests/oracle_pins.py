@@ -1,0 +1,313 @@
+"""Pins that tie the fp64 oracle to facts outside itself.
+
+Each ``pin_*`` function raises AssertionError when the oracle disagrees with
+something fixed independently of its code: a library routine run on a
+contiguous copy of the cache (torch's scaled-dot-product attention, scipy's
+logsumexp), a closed form, or an invariant that any correct paged gather must
+satisfy.  ``test_oracle_pins.py`` runs them against the real oracle and
+against deliberately broken builds of it (every mutant must trip at least one
+pin).
+
+What the pins follow (the "mini-infer" pages):
+  - prajwal7-2002 docs, "Systems Architecture" and "Core Capabilities at a
+    Glance" (rows "Memory Allocation", "Batched Paged Decode", "Model
+    Architecture"): physical 16-token block pool, per-request block table,
+    direct physical gather with slot mapping, attention by SDPA.
+  - psmarter write-up, feature list items 1 and 7: block-table
+    PagedAttention, split-K flash decoding.
+  - tom-jerr "Attention Backend" table: split-KV paged decode, page_size 256.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+import torch
+
+import oracle
+from paged_kv_decode_cache_gb300 import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Widen bf16 bit patterns through torch's own bf16 type (independent of the oracle's C)."""
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+    return t.to(torch.float64).numpy()
+
+
+def f64_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.asarray(x, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def small_case(B=3, Hq=6, Hkv=2, D=32, bs=16, lens=(5, 16, 41), nb=24, seed=7, **kw):
+    return W.make_workload("pin", B=B, Hq=Hq, Hkv=Hkv, D=D, block_size=bs, seq_lens=list(lens),
+                           num_blocks=nb, seed=seed, write_new=False, **kw)
+
+
+def contiguous_kv(w: W.DecodeWorkload, b: int):
+    """Gather sequence b's K and V into contiguous [L, Hkv, D] fp64 arrays with numpy fancy indexing."""
+    L = int(w.seq_lens[b])
+    t = np.arange(L)
+    phys = w.block_tables[b][t // w.block_size]
+    off = t % w.block_size
+    k = bf16_to_f64(w.k_cache)[phys, off]
+    v = bf16_to_f64(w.v_cache)[phys, off]
+    return k, v
+
+
+def sdpa_reference(w: W.DecodeWorkload):
+    """torch.nn.functional.scaled_dot_product_attention (fp64, CPU) on contiguous copies.
+
+    The GQA group is expanded with repeat_interleave, i.e. query head h reads
+    KV head h // (Hq / Hkv).
+    """
+    out = np.zeros((w.B, w.Hq, w.D))
+    for b in range(w.B):
+        L = int(w.seq_lens[b])
+        if L == 0:
+            continue
+        k, v = contiguous_kv(w, b)
+        q = torch.from_numpy(bf16_to_f64(w.q[b]))[:, None, :]            # [Hq, 1, D]
+        kt = torch.from_numpy(k).permute(1, 0, 2).repeat_interleave(w.G, dim=0)  # [Hq, L, D]
+        vt = torch.from_numpy(v).permute(1, 0, 2).repeat_interleave(w.G, dim=0)
+        o = torch.nn.functional.scaled_dot_product_attention(q, kt, vt, scale=float(w.scale))
+        out[b] = o[:, 0, :].numpy()
+    return out
+
+
+def run_oracle(w: W.DecodeWorkload):
+    return oracle.decode(w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.scale)
+
+
+# ---------------------------------------------------------------- cache write
+def pin_cache_write_index_put():
+    """Scatter equals numpy index-put on a sentinel-filled pool; padding slots are skipped."""
+    rng = np.random.default_rng(11)
+    nb, bs, hkv, d = 8, 16, 2, 8
+    sentinel = np.uint16(0xABCD)
+    kc = np.full((nb, bs, hkv, d), sentinel, np.uint16)
+    vc = np.full((nb, bs, hkv, d), sentinel, np.uint16)
+    slots = np.array([5, -1, 127, 16, 64, -7, 3], np.int64)
+    n = slots.shape[0]
+    kn = rng.integers(0, 0xFFFF, (n, hkv, d), dtype=np.uint16)
+    vn = rng.integers(0, 0xFFFF, (n, hkv, d), dtype=np.uint16)
+    oracle.cache_write(kn, vn, slots, kc, vc)
+    ek = np.full_like(kc, sentinel).reshape(nb * bs, hkv, d)
+    ev = np.full_like(vc, sentinel).reshape(nb * bs, hkv, d)
+    ok = slots >= 0
+    ek[slots[ok]] = kn[ok]
+    ev[slots[ok]] = vn[ok]
+    assert np.array_equal(kc.reshape(nb * bs, hkv, d), ek), "K scatter differs from index-put"
+    assert np.array_equal(vc.reshape(nb * bs, hkv, d), ev), "V scatter differs from index-put"
+
+
+def pin_cache_write_then_gather():
+    """After the write, the gather through the block table returns the new token at L-1."""
+    w = W.make_workload("pin", B=3, Hq=4, Hkv=2, D=16, block_size=16, seq_lens=[1, 16, 35],
+                        num_blocks=12, seed=5)
+    kc, vc = w.k_cache.copy(), w.v_cache.copy()
+    oracle.cache_write(w.k_new, w.v_new, w.slot_mapping, kc, vc)
+    for b in range(w.B):
+        t = int(w.seq_lens[b]) - 1
+        p = w.block_tables[b, t // w.block_size]
+        assert np.array_equal(kc[p, t % w.block_size], w.k_new[b])
+        assert np.array_equal(vc[p, t % w.block_size], w.v_new[b])
+
+
+def pin_cache_write_rejects_bad_slots():
+    kc = np.zeros((2, 16, 1, 8), np.uint16)
+    vc = kc.copy()
+    kn = np.ones((2, 1, 8), np.uint16)
+    for bad in ([3, 3], [0, 32]):
+        try:
+            oracle.cache_write(kn, kn, np.array(bad, np.int64), kc, vc)
+        except oracle.OracleError:
+            continue
+        raise AssertionError(f"slots {bad} accepted")
+
+
+# ------------------------------------------------------------ gather + SDPA
+def pin_sdpa_contiguous():
+    """Oracle equals torch SDPA on a contiguous gathered cache (several shapes) to 1e-12."""
+    cases = [
+        small_case(),
+        small_case(B=2, Hq=8, Hkv=8, D=16, lens=(33, 7), nb=8, seed=3),           # MHA, G=1
+        small_case(B=2, Hq=7, Hkv=1, D=64, lens=(64, 1), nb=6, seed=4),           # G=7
+        small_case(B=2, Hq=4, Hkv=2, D=16, bs=256, lens=(300, 513), nb=6, seed=9),  # 256-token pages
+        small_case(B=1, Hq=12, Hkv=4, D=24, bs=32, lens=(95,), nb=5, seed=12),
+    ]
+    for w in cases:
+        out, _ = run_oracle(w)
+        ref = sdpa_reference(w)
+        err = np.abs(out - ref).max()
+        assert err < 1e-12, f"{w.Hq}/{w.Hkv}/{w.D}/bs{w.block_size}: oracle vs SDPA {err}"
+
+
+def pin_permutation_invariance():
+    """Relabelling physical blocks (pool permuted, tables remapped) leaves the output bit-identical."""
+    w = small_case(B=3, Hq=6, Hkv=3, D=16, lens=(20, 48, 3), nb=10, seed=21)
+    out, lse = run_oracle(w)
+    perm = np.random.default_rng(1).permutation(w.num_blocks)   # new position of old block i
+    inv = np.argsort(perm)
+    k2 = w.k_cache[inv]
+    v2 = w.v_cache[inv]
+    bt2 = np.where(w.block_tables >= 0, perm[np.maximum(w.block_tables, 0)], -1).astype(np.int32)
+    out2, lse2 = oracle.decode(w.q, k2, v2, bt2, w.seq_lens, w.scale)
+    assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
+
+
+# --------------------------------------------------------------- closed forms
+def pin_single_token_returns_v():
+    """L = 1: the softmax weight is 1, out is the V row exactly and lse is the single score."""
+    w = small_case(B=2, Hq=4, Hkv=2, D=32, lens=(1, 1), nb=4, seed=31)
+    out, lse = run_oracle(w)
+    for b in range(w.B):
+        p = w.block_tables[b, 0]
+        for h in range(w.Hq):
+            g = h // w.G
+            v = bf16_to_f64(w.v_cache[p, 0, g])
+            assert np.array_equal(out[b, h], v), "L=1 output is not the V row"
+            s = float(w.scale) * float(bf16_to_f64(w.q[b, h]) @ bf16_to_f64(w.k_cache[p, 0, g]))
+            assert abs(lse[b, h] - s) < 1e-12
+
+
+def pin_identical_keys_mean():
+    """All keys equal: uniform weights, out = mean of the V rows, lse = s + ln L."""
+    w = small_case(B=2, Hq=4, Hkv=2, D=16, lens=(23, 40), nb=8, seed=41)
+    w.k_cache[:] = w.k_cache[0, 0][None, None]
+    out, lse = run_oracle(w)
+    for b in range(w.B):
+        k, v = contiguous_kv(w, b)
+        L = int(w.seq_lens[b])
+        for h in range(w.Hq):
+            g = h // w.G
+            assert np.abs(out[b, h] - v[:, g].mean(axis=0)).max() < 1e-12
+            s = float(w.scale) * float(bf16_to_f64(w.q[b, h]) @ k[0, g])
+            assert abs(lse[b, h] - (s + math.log(L))) < 1e-12
+
+
+def pin_scale_zero_mean():
+    """scale = 0: every score is 0, out = mean of V regardless of K, lse = ln L."""
+    w = small_case(B=2, Hq=6, Hkv=3, D=8, lens=(9, 33), nb=8, seed=51, scale=0.0)
+    out, lse = run_oracle(w)
+    for b in range(w.B):
+        _, v = contiguous_kv(w, b)
+        for h in range(w.Hq):
+            assert np.abs(out[b, h] - v[:, h // w.G].mean(axis=0)).max() < 1e-12
+            assert abs(lse[b, h] - math.log(int(w.seq_lens[b]))) < 1e-12
+
+
+def pin_two_token_closed_form():
+    """Golden fixture: two keys with scores 0 and 1 give weights 1/(1+e), e/(1+e)."""
+    with open(os.path.join(GOLDEN, "two_token.json")) as f:
+        fx = json.load(f)
+    D = len(fx["q"])
+    kc = np.zeros((1, 16, 1, D), np.uint16)
+    vc = np.zeros((1, 16, 1, D), np.uint16)
+    kc[0, 0, 0] = f64_to_bf16_bits(fx["k0"])
+    kc[0, 1, 0] = f64_to_bf16_bits(fx["k1"])
+    vc[0, 0, 0] = f64_to_bf16_bits(fx["v0"])
+    vc[0, 1, 0] = f64_to_bf16_bits(fx["v1"])
+    q = f64_to_bf16_bits(fx["q"]).reshape(1, 1, D)
+    out, lse = oracle.decode(q, kc, vc, np.zeros((1, 1), np.int32), np.array([2], np.int32),
+                             fx["scale"])
+    e = math.e
+    expect = (np.array(fx["v0"]) + e * np.array(fx["v1"])) / (1 + e)
+    assert np.abs(out[0, 0] - expect).max() < 1e-14
+    assert abs(lse[0, 0] - math.log(1 + e)) < 1e-14
+
+
+def pin_linearity_pow2():
+    """Scaling V by 2 scales the output by 2 exactly (a power of two commutes with rounding)."""
+    w = small_case(seed=61)
+    out, lse = run_oracle(w)
+    vb = bf16_to_f64(w.v_cache) * 2.0
+    v2 = f64_to_bf16_bits(vb)
+    out2, lse2 = oracle.decode(w.q, w.k_cache, v2, w.block_tables, w.seq_lens, w.scale)
+    assert np.array_equal(out2, 2.0 * out) and np.array_equal(lse, lse2)
+
+
+def pin_identical_q_heads():
+    """Query heads of one group with the same q give bit-identical outputs; different groups differ."""
+    w = small_case(B=2, Hq=8, Hkv=2, D=16, lens=(30, 17), nb=8, seed=71)
+    w.q[:] = w.q[:, :1]
+    out, _ = run_oracle(w)
+    for b in range(w.B):
+        for g in range(w.Hkv):
+            grp = out[b, g * w.G:(g + 1) * w.G]
+            assert np.array_equal(grp, np.broadcast_to(grp[0], grp.shape))
+        assert not np.array_equal(out[b, 0], out[b, w.G]), "KV heads not distinguished"
+
+
+def pin_lse_logsumexp():
+    """lse equals scipy.special.logsumexp of the scores computed by numpy einsum."""
+    from scipy.special import logsumexp
+    w = small_case(B=2, Hq=4, Hkv=2, D=32, lens=(50, 3), nb=6, seed=81)
+    _, lse = run_oracle(w)
+    for b in range(w.B):
+        k, _ = contiguous_kv(w, b)
+        q = bf16_to_f64(w.q[b])
+        kk = np.repeat(k, w.G, axis=1)                      # [L, Hq, D]
+        s = float(w.scale) * np.einsum("hd,lhd->hl", q, kk)
+        assert np.abs(lse[b] - logsumexp(s, axis=1)).max() < 1e-12
+
+
+def pin_empty_sequence():
+    """L = 0 reads nothing: out = 0 and lse = -inf."""
+    w = small_case(B=2, Hq=2, Hkv=1, D=8, lens=(0, 4), nb=3, seed=91)
+    out, lse = run_oracle(w)
+    assert np.all(out[0] == 0) and np.all(np.isneginf(lse[0]))
+    assert np.all(np.isfinite(out[1]))
+
+
+def pin_poison_never_read():
+    """NaN in every pool row attention must not read leaves the output unchanged."""
+    w = small_case(B=3, Hq=4, Hkv=2, D=16, lens=(5, 17, 32), nb=9, seed=101)
+    clean, _ = run_oracle(w)
+    wp = small_case(B=3, Hq=4, Hkv=2, D=16, lens=(5, 17, 32), nb=9, seed=101, poison_unused=True)
+    out, _ = run_oracle(wp)
+    assert np.array_equal(out, clean)
+
+
+# ------------------------------------------------------------------- split-KV
+def pin_split_combine_equals_unsplit():
+    """Partials over any block-aligned (or not) partition, merged by LSE, equal unsplit to 1e-12."""
+    w = small_case(B=3, Hq=6, Hkv=2, D=16, lens=(1, 70, 129), nb=20, seed=111)
+    out, lse = run_oracle(w)
+    for P, chunk in ((1, 160), (2, 80), (3, 48), (9, 16), (19, 7), (40, 16)):
+        po, pl = oracle.decode_partial(w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens,
+                                       w.scale, P, chunk)
+        o2, l2 = oracle.combine(po, pl)
+        assert np.abs(o2 - out).max() < 1e-12, f"P={P} chunk={chunk}"
+        assert np.abs(l2 - lse).max() < 1e-12
+
+
+def pin_combine_closed_form():
+    """Two partials with lse 0 and ln 3 weigh 1/4 and 3/4; an empty (-inf) partial weighs 0."""
+    po = np.array([[[1.0, -2.0], [5.0, 6.0], [123.0, 456.0]]])
+    pl = np.array([[0.0, math.log(3.0), -math.inf]])
+    out, lse = oracle.combine(po, pl)
+    assert np.abs(out[0] - np.array([0.25 * 1 + 0.75 * 5, 0.25 * -2 + 0.75 * 6])).max() < 1e-15
+    assert abs(lse[0] - math.log(4.0)) < 1e-15
+    out, lse = oracle.combine(np.zeros((1, 2, 3)), np.full((1, 2), -math.inf))
+    assert np.all(out == 0) and np.isneginf(lse[0])
+
+
+def pin_partial_ranges():
+    """A partial covering tokens [a, b) equals SDPA over exactly those tokens."""
+    w = small_case(B=1, Hq=2, Hkv=1, D=16, lens=(45,), nb=4, seed=121)
+    po, pl = oracle.decode_partial(w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens,
+                                   w.scale, 3, 16)
+    k, v = contiguous_kv(w, 0)
+    for p, (a, bnd) in enumerate(((0, 16), (16, 32), (32, 45))):
+        q = torch.from_numpy(bf16_to_f64(w.q[0]))[:, None, :]
+        kt = torch.from_numpy(k[a:bnd]).permute(1, 0, 2)
+        vt = torch.from_numpy(v[a:bnd]).permute(1, 0, 2)
+        o = torch.nn.functional.scaled_dot_product_attention(q, kt, vt, scale=float(w.scale))
+        assert np.abs(po[0, :, p] - o[:, 0].numpy()).max() < 1e-12
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]
