@@ -1,0 +1,472 @@
+"""Benchmark of one paged-KV decode step on GB300.
+
+A step is the whole hot path for one decode layer of one batch:
+slot-mapping cache write of the batch's new K/V, split-KV decode attention
+through the block tables (partition count chosen by the library), and the
+log-sum-exp combine.  Inputs are seeded synthetic tensors shaped like the
+workload named by --workload (default: the Qwen2.5-7B-shaped layer, B=8,
+Hq=28, Hkv=4, D=128, every L=4096, 16-token blocks).
+
+Timing: W warm-up steps, then exactly K steps between a barrier and a
+device synchronise on each side, timed with CUDA events on the launching
+stream; every step is replayed from a CUDA graph (one graph per pool
+replica), and consecutive steps rotate over enough copies of the KV pool that
+the data a step reads was evicted from the 129 MB L2 before it is read again.
+The decode kernel's own duration is measured with events recorded inside the
+graphs.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "qwen2.5-7b-bs16"
+L2_BYTES = 129 * 1000 * 1000
+METRIC = "paged decode attention: achieved HBM TB/s (% of ~8 TB/s) and us/call"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--splits", type=int, default=0, help="0 = library's automatic choice")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU work for the oracle baseline sample")
+    ap.add_argument("--e2e-steps", type=int, default=0, help="0 = min(steps, 500)")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------- utilities
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def measured_peak_gbs():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def csrc_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "paged_kv_decode_cache_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernels are unchanged since."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(workload, {})
+    except Exception:
+        return None
+    if rec.get("kernel") != kernel or rec.get("csrc_hash") != csrc_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: str):
+        self.gpu = gpu
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9 and parts[1].isdigit():
+                    rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [int(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": int(rows[0][2]),
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())
+                if any(r[3].replace(".", "").isdigit() for r in rows) else None}
+
+
+def gpu_for_smi(dev) -> str:
+    """The nvidia-smi -i selector of a torch device (its UUID when torch exposes it)."""
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        first = vis.split(",")[dev.index or 0] if vis else str(dev.index or 0)
+        return first
+
+
+def algorithmic_bytes(w):
+    """(attention KV+Q+O bytes, cache-write bytes) of one step."""
+    return w.kv_bytes() + w.qo_bytes(), w.write_bytes()
+
+
+# ------------------------------------------------------------------- oracle
+def time_oracle(w, budget_s: float, max_rows: int | None = None, nthreads: int = 0):
+    """Run the fp64 oracle (cache write + attention rows) on a bounded sample.
+
+    Returns (seconds, algorithmic bytes covered, rows, threads, description).
+    Rows are taken in (b, h) order; each row is charged its share of its KV
+    head's bytes (1/G) plus its q and o rows, so all rows add up to KV+Q+O.
+    """
+    import oracle
+    threads = nthreads if nthreads > 0 else oracle.max_threads()
+    kc, vc = w.k_cache.copy(), w.v_cache.copy()
+    t0 = time.perf_counter()
+    if w.slot_mapping.size:
+        oracle.cache_write(w.k_new, w.v_new, w.slot_mapping, kc, vc)
+    t_write = time.perf_counter() - t0
+    total = w.B * w.Hq
+    rb = (np.arange(total) // w.Hq).astype(np.int32)
+    rh = (np.arange(total) % w.Hq).astype(np.int32)
+    row_bytes = (w.seq_lens[rb].astype(np.float64) * w.D * 2 * 2 / w.G + 2 * w.D * 2)
+    # calibrate on a few rows
+    n0 = min(total, max(threads, 8))
+    t0 = time.perf_counter()
+    oracle.decode_rows(w.q, kc, vc, w.block_tables, w.seq_lens, w.scale, rb[:n0], rh[:n0], threads)
+    t_cal = max(time.perf_counter() - t0, 1e-6)
+    per_row = t_cal / n0
+    n = int(min(total, max(1, budget_s / per_row)))
+    if max_rows is not None:
+        n = min(n, max_rows)
+    reps = 1
+    if n == total:
+        reps = max(1, int(budget_s / max(per_row * total, 1e-6)))
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.decode_rows(w.q, kc, vc, w.block_tables, w.seq_lens, w.scale, rb[:n], rh[:n],
+                           threads)
+    secs = time.perf_counter() - t0
+    byts = float(row_bytes[:n].sum()) * reps
+    desc = (f"{n} of {total} (b,h) rows x {reps} reps of workload {w.name}, fp64, "
+            f"write {w.write_bytes()} B in {t_write*1e3:.1f} ms excluded")
+    return secs, byts, n * reps, threads, desc
+
+
+def run_reference(args, world, rank):
+    """--impl reference: the oracle as it stands, timed on the host cores."""
+    if rank != 0:
+        return
+    from paged_kv_decode_cache_gb300 import workloads as W
+    w = W.WORKLOADS[args.workload]()
+    budget_per_step = max(0.005, 150.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        time_oracle(w, budget_per_step)
+    secs = byts = 0.0
+    rows = 0
+    threads = 1
+    desc = ""
+    for _ in range(args.steps):
+        s, b, r, threads, desc = time_oracle(w, budget_per_step)
+        secs += s
+        byts += b
+        rows += r
+    value = byts / secs / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": args.workload},
+        "cpu_baseline": {"value": value, "unit": "TB/s", "cores": threads, "kind": "oracle",
+                         "sample": f"per step: {desc}"},
+        "e2e": {"value": value, "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------- ours
+def run_ours(args, world, rank, local):
+    import torch
+
+    from paged_kv_decode_cache_gb300 import build as B
+    from paged_kv_decode_cache_gb300 import pa
+    from paged_kv_decode_cache_gb300 import workloads as W
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the library has no CPU path)")
+    B.build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = W.WORKLOADS[args.workload]()
+    attn_bytes, write_bytes = algorithmic_bytes(w)
+    step_bytes = attn_bytes + write_bytes
+
+    def to_dev(a, dtype=None):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        if a.dtype == np.uint16:
+            t = t.view(torch.int16).view(torch.bfloat16)
+        return t.to(dev)
+
+    q = to_dev(w.q)
+    bt = to_dev(w.block_tables)
+    sl = to_dev(w.seq_lens)
+    kn, vn, slots = to_dev(w.k_new), to_dev(w.v_new), to_dev(w.slot_mapping)
+    k0, v0 = to_dev(w.k_cache), to_dev(w.v_cache)
+    touched = w.kv_bytes()
+    R = max(1, min(8, math.ceil(2.5 * L2_BYTES / max(touched, 1)) + 1)) if touched < 3 * L2_BYTES else 1
+    pools = [(k0, v0)] + [(k0.clone(), v0.clone()) for _ in range(R - 1)]
+    P = args.splits or pa.pa_auto_num_splits(w.B, w.Hkv, w.max_blocks, w.block_size)
+    out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
+    po = torch.empty((w.B, w.Hq, P, w.D), dtype=torch.float32, device=dev)
+    pl = torch.empty((w.B, w.Hq, P), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    kernel_name = "decode_cc_kernel"
+
+    def step(r, ev0=None, ev1=None):
+        kc, vc = pools[r]
+        pa.pa_cache_write(kn, vn, slots, kc, vc, stream=stream)
+        if ev0 is not None:
+            ev0.record(stream)
+        if P > 1:
+            pa.pa_decode_partial(po, pl, q, kc, vc, bt, sl, w.scale, P, stream=stream)
+        else:
+            pa.pa_decode(out, lse, q, kc, vc, bt, sl, w.scale, stream=stream)
+        if ev1 is not None:
+            ev1.record(stream)
+        if P > 1:
+            pa.pa_combine(out, lse, po, pl, stream=stream)
+
+    launches_per_step = 3 if P > 1 else 2
+    # CUDA graphs of S consecutive steps (cycling over the pool replicas), NG
+    # copies, each step with its own pair of graph-recorded events around the
+    # decode kernel.  Step i of the timed loop is step i % S of graph copy
+    # (i // S) % NG, so after the loop every event pair holds a duration
+    # measured inside the timed region.
+    S = R * max(1, math.ceil(16 / R))
+    NG = 8
+    try:
+        torch.cuda.Event(enable_timing=True, external=True)
+        mk = lambda: torch.cuda.Event(enable_timing=True, external=True)  # noqa: E731
+    except TypeError:
+        mk = None
+    with torch.cuda.stream(stream):
+        for r in range(R):  # eager warm-up of every replica before capture
+            step(r)
+    stream.synchronize()
+
+    def capture(steps):
+        evs = [(mk(), mk()) if mk else (None, None) for _ in steps]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for r, (e0, e1) in zip(steps, evs):
+                step(r, e0, e1)
+        return g, evs
+
+    full = [capture([k % R for k in range(S)]) for _ in range(NG)]
+    single = [capture([r]) for r in range(R)]
+    n_full, n_rem = divmod(args.steps, S)
+
+    def run_steps(n_full_graphs, n_single, offset=0):
+        with torch.cuda.stream(stream):
+            for j in range(n_full_graphs):
+                full[(offset + j) % NG][0].replay()
+            for r in range(n_single):
+                single[r % R][0].replay()
+
+    wf, wr = divmod(args.warmup, S)
+    run_steps(wf, wr)
+    stream.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(gpu_for_smi(dev)) as clk:
+        t_start.record(stream)
+        run_steps(n_full, n_rem)
+        t_end.record(stream)
+        t_end.synchronize()
+    torch.cuda.synchronize()
+    barrier(world)
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
+    clocks = clk.summary()
+    kern_ms = []
+    if mk and n_full:
+        for g, evs in full[:min(NG, n_full)]:
+            kern_ms += [e0.elapsed_time(e1) for e0, e1 in evs]
+    kern_ms_avg = statistics.mean(kern_ms) if kern_ms else None
+
+    ms_per_step = elapsed_ms / args.steps
+    value = step_bytes * world / (ms_per_step * 1e-3) / 1e12
+
+    # ---- end to end through the public API, host buffers, copies inside the region
+    e2e_steps = args.e2e_steps or min(args.steps, 500)
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+    h_q, h_bt, h_sl = pin(w.q.view(np.int16)), pin(w.block_tables), pin(w.seq_lens)
+    h_kn, h_vn, h_slots = pin(w.k_new.view(np.int16)), pin(w.v_new.view(np.int16)), pin(w.slot_mapping)
+    h_out = torch.empty((w.B, w.Hq, w.D), dtype=torch.int16).pin_memory()
+    h_lse = torch.empty((w.B, w.Hq), dtype=torch.float32).pin_memory()
+    d_q16, d_kn16, d_vn16 = q.view(torch.int16), kn.view(torch.int16), vn.view(torch.int16)
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_bt, h_sl, h_kn, h_vn, h_slots))
+    d2h = h_out.numel() * 2 + h_lse.numel() * 4
+    ws = torch.empty(max(1, pa.pa_splitkv_workspace_bytes(w.B, w.Hq, w.D, P)), dtype=torch.uint8,
+                     device=dev)
+
+    def e2e_step(r):
+        kc, vc = pools[r]
+        with torch.cuda.stream(stream):
+            for d, h in ((d_q16, h_q), (bt, h_bt), (sl, h_sl), (d_kn16, h_kn), (d_vn16, h_vn),
+                         (slots, h_slots)):
+                d.copy_(h, non_blocking=True)
+            pa.pa_cache_write(kn, vn, slots, kc, vc, stream=stream)
+            pa.pa_decode_splitkv(out, lse, q, kc, vc, bt, sl, w.scale, num_splits=P,
+                                 workspace=ws, stream=stream)
+            h_out.copy_(out.view(torch.int16), non_blocking=True)
+            h_lse.copy_(lse, non_blocking=True)
+
+    for i in range(min(20, e2e_steps)):
+        e2e_step(i % R)
+    stream.synchronize()
+    barrier(world)
+    a0 = torch.cuda.Event(enable_timing=True)
+    a1 = torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for i in range(e2e_steps):
+        e2e_step(i % R)
+    a1.record(stream)
+    a1.synchronize()
+    e2e_ms = max_over_ranks(a0.elapsed_time(a1), world) / e2e_steps
+    e2e_value = step_bytes * world / (e2e_ms * 1e-3) / 1e12
+
+    peak, peak_kind = measured_peak_gbs()
+    kern_bytes = w.kv_bytes() + w.B * w.Hq * w.D * 2 + (w.B * w.Hq * w.D * 2 if P == 1 else 0)
+    roofline = None
+    if kern_ms_avg:
+        ach = kern_bytes / (kern_ms_avg * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
+                    "frac": round(ach / peak, 4), "traffic": recorded_traffic(args.workload, kernel_name),
+                    "peak_kind": peak_kind, "kernel": kernel_name,
+                    "kernel_us": round(kern_ms_avg * 1e3, 3), "kernel_bytes": kern_bytes}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        secs, byts, rows, threads, desc = time_oracle(w, args.cpu_seconds)
+        cpu = {"value": byts / secs / 1e12, "unit": "TB/s", "cores": threads, "kind": "oracle",
+               "sample": desc}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": args.workload, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+                       "block_size": w.block_size, "seq_lens_total": int(w.seq_lens.sum()),
+                       "splits": P, "step": "cache_write + split decode + combine",
+                       "parallelism": f"replicas x{world}",
+                       "l2": f"{R} pool replicas rotated per step ({touched/1e6:.0f} MB read per step)"},
+            "us_per_step": ms_per_step * 1e3,
+            "pct_of_8TBps": value / 8.0 * 100,
+            "step_bytes": step_bytes,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "TB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": args.steps * launches_per_step,
+            "kernel_samples": len(kern_ms),
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

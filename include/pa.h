@@ -1,0 +1,206 @@
+/*
+ * pa.h -- C ABI of libpagedattn: decode attention over a paged KV cache on
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operations are the hot path of one decode step of an LLM server, as the
+ * "mini-infer" pages describe it:
+ *   - a physical pool of fixed-size KV blocks (16 tokens per block; 256-token
+ *     pages for the FlashAttention-2 backend) and a per-sequence
+ *     virtual-to-physical block table ("mini-infer" docs by prajwal7-2002,
+ *     section "Systems Architecture"; "MiniInfer" by tom-jerr, table
+ *     "Attention Backend");
+ *   - the [B, 1] decode step that writes each sequence's new K/V through a
+ *     slot mapping and gathers physical K/V rows for attention (prajwal7-2002
+ *     docs, table "Core Capabilities at a Glance", row "Batched Paged
+ *     Decode");
+ *   - split-K "flash decoding" for long contexts, which partitions each
+ *     sequence's tokens and merges the partial results (psmarter "mini-infer"
+ *     forum write-up, feature list item 7 and benchmark list item
+ *     "Flash Decoding"; tom-jerr "Attention Backend" table, "split-KV").
+ *
+ * Layouts (all row-major, contiguous):
+ *   q          [B, Hq, D]                       bf16
+ *   k_cache    [num_blocks, block_size, Hkv, D] bf16   (v_cache identical)
+ *   block_tables [B, max_blocks_per_seq]        int32, entry j of row b is the
+ *                                               physical block holding tokens
+ *                                               [j*block_size, (j+1)*block_size)
+ *                                               of sequence b; entries past
+ *                                               ceil(L_b / block_size) are
+ *                                               never read
+ *   seq_lens   [B]                              int32, L_b = tokens attended,
+ *                                               including the one written this
+ *                                               step
+ *   slot_mapping [N]                            int64, slot = block * block_size
+ *                                               + offset; a negative slot is
+ *                                               padding and is skipped
+ *   out        [B, Hq, D]                       bf16 (round to nearest even)
+ *   lse        [B, Hq]                          fp32, natural-log log-sum-exp
+ *                                               of the scaled scores; -inf for
+ *                                               L_b = 0
+ * Query head h reads KV head h / (Hq / Hkv).  bf16 arguments are passed as
+ * untyped pointers to 16-bit storage.
+ *
+ * Conventions for every entry point:
+ *   - Pointers marked "device" are device (or managed) memory owned by the
+ *     caller; the library keeps no reference after the call returns.  It
+ *     allocates no memory and never synchronises: work is enqueued on
+ *     `stream` (NULL = the legacy default stream) and the call returns.
+ *   - Device pointers to bf16/fp32 tensors must be 16-byte aligned.
+ *   - Return value: PA_OK, or a negative PA_E* code when the arguments are
+ *     rejected on the host (nothing is enqueued then) or a launch fails.
+ *   - `status` (nullable, device int32): the kernels OR PA_STATUS_* bits
+ *     into it when they meet bad data that the host cannot see (a block id
+ *     outside the pool, a slot outside the pool, a sequence length larger
+ *     than the table allows).  The offending element is skipped, never
+ *     dereferenced.  The caller zeroes it and reads it back when convenient.
+ *   - A call writes every element of its outputs.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same handle as cudaStream_t / CUstream. */
+typedef struct CUstream_st *pa_stream_t;
+
+/* Shape of the physical K (and V) pool: [num_blocks, block_size, num_kv_heads, head_dim]. */
+typedef struct {
+    int32_t num_blocks;
+    int32_t block_size;   /* tokens per block; a multiple of 16 */
+    int32_t num_kv_heads; /* Hkv */
+    int32_t head_dim;     /* D: 64 or 128 */
+} pa_cache_desc;
+
+/* Host-side return codes. */
+enum {
+    PA_OK = 0,
+    PA_EINVAL = -1,       /* null or misaligned pointer, inconsistent sizes */
+    PA_EUNSUPPORTED = -2, /* valid request outside what the kernels implement */
+    PA_EWORKSPACE = -3,   /* workspace missing or smaller than required */
+    PA_ECUDA = -4         /* a CUDA call or kernel launch failed */
+};
+
+/* Device status bits (OR-ed into *status). */
+enum {
+    PA_STATUS_BAD_BLOCK = 1,  /* block table entry outside [0, num_blocks) */
+    PA_STATUS_BAD_SLOT = 2,   /* slot_mapping entry >= num_blocks * block_size */
+    PA_STATUS_BAD_SEQLEN = 4, /* seq_len < 0 or > max_blocks_per_seq * block_size */
+    PA_STATUS_TIMEOUT = 8     /* a bounded wait on an async copy gave up */
+};
+
+/*
+ * Slot-mapping scatter of this step's new K and V (prajwal7-2002 docs, table
+ * "Core Capabilities at a Glance", row "Batched Paged Decode": "zero-overhead
+ * slot mapping").  For every i < n_tokens with s = slot_mapping[i] >= 0:
+ *   k_cache[s / bs, s % bs, :, :] = k_new[i, :, :]   (bit copy), same for V.
+ * k_new, v_new: device [n_tokens, Hkv, D] bf16.  slot_mapping: device int64.
+ * Slots must be distinct (a repeated slot leaves one of the writers' rows;
+ * which one is unspecified).  A slot >= num_blocks * bs is skipped and
+ * reported through `status`.  n_tokens == 0 is a no-op.
+ */
+int pa_cache_write(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                   int64_t n_tokens, void *k_cache, void *v_cache, pa_cache_desc cache,
+                   int32_t *status, pa_stream_t stream);
+
+/*
+ * Batched single-token decode attention over the paged cache, one pass over
+ * each sequence's KV (psmarter write-up, feature 1: PagedAttention with
+ * block tables; prajwal7-2002 docs, row "Batched Paged Decode").  For every
+ * sequence b and query head h:
+ *   s_t = scale * <q[b,h,:], K[b, t, h / (Hq/Hkv), :]>,  t < L_b (through the table)
+ *   out[b,h,:] = sum_t softmax(s)_t V[b, t, h/(Hq/Hkv), :]
+ *   lse[b,h]   = ln sum_t exp(s_t)
+ * out: device bf16 [B, Hq, D]; lse: device fp32 [B, Hq] or NULL.
+ * q: device bf16 [B, Hq, D].  block_tables: device int32 [B, max_blocks_per_seq].
+ * seq_lens: device int32 [B].  B == 0 is a no-op.
+ * Supported: Hq % Hkv == 0 with Hq / Hkv <= 8, D in {64, 128}, block_size a
+ * multiple of 16.  One CTA per (sequence, KV head); use pa_decode_splitkv
+ * when B * Hkv is small next to the SM count.
+ */
+int pa_decode(void *out, float *lse, const void *q, const void *k_cache, const void *v_cache,
+              pa_cache_desc cache, const int32_t *block_tables, int32_t max_blocks_per_seq,
+              const int32_t *seq_lens, int32_t B, int32_t Hq, float scale, int32_t *status,
+              pa_stream_t stream);
+
+/*
+ * Split-KV partition count for a decode batch (psmarter benchmark list,
+ * "Flash Decoding": splitting lifts SM utilisation at seq 4096).  Picks P so
+ * that B * Hkv * P work units fill `sm_count` SMs while each partition keeps
+ * at least a few 16-token tiles.  Host-only, pure function of its arguments.
+ * Returns P >= 1, or PA_EINVAL.
+ */
+int pa_choose_num_splits(int32_t B, int32_t Hkv, int32_t max_blocks_per_seq,
+                         int32_t block_size, int32_t sm_count);
+
+/*
+ * Tokens per partition for P splits: ceil(ceil(max_blocks_per_seq*bs / P) / 16) * 16.
+ * Partition p of sequence b covers tokens [p * chunk, min((p + 1) * chunk, L_b)).
+ * Returns the chunk, or PA_EINVAL.
+ */
+int pa_partition_tokens(int32_t max_blocks_per_seq, int32_t block_size, int32_t num_splits);
+
+/*
+ * Bytes of workspace pa_decode_splitkv needs: fp32 partial outputs
+ * [B, Hq, P, D] followed by fp32 partial LSEs [B, Hq, P], each region
+ * 256-byte aligned.  0 when num_splits <= 1.
+ */
+size_t pa_splitkv_workspace_bytes(int32_t B, int32_t Hq, int32_t D, int32_t num_splits);
+
+/*
+ * Per-partition decode attention (the first half of split-KV decoding).
+ * part_o: device fp32 [B, Hq, P, D], each partial normalised over its own
+ * token range; part_lse: device fp32 [B, Hq, P], natural-log LSE of the
+ * range, -inf for an empty range (and then part_o = 0).  Partition ranges as
+ * in pa_partition_tokens.  num_splits >= 1.  Other arguments as pa_decode.
+ */
+int pa_decode_partial(float *part_o, float *part_lse, const void *q, const void *k_cache,
+                      const void *v_cache, pa_cache_desc cache, const int32_t *block_tables,
+                      int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t B,
+                      int32_t Hq, float scale, int32_t num_splits, int32_t *status,
+                      pa_stream_t stream);
+
+/*
+ * Log-sum-exp merge of P partials per (b, h) (the combine step that split-K
+ * flash decoding implies):
+ *   lse = M + ln sum_p exp(lse_p - M),  M = max_p lse_p
+ *   out = sum_p exp(lse_p - lse) * o_p           (bf16, round to nearest even)
+ * A partial with lse_p = -inf has weight 0; if all are -inf, out = 0 and
+ * lse = -inf.  part_o: device fp32 [B, Hq, P, D]; part_lse: device fp32
+ * [B, Hq, P]; out: device bf16 [B, Hq, D]; lse: device fp32 [B, Hq] or NULL.
+ */
+int pa_combine(void *out, float *lse, const float *part_o, const float *part_lse, int32_t B,
+               int32_t Hq, int32_t num_splits, int32_t D, pa_stream_t stream);
+
+/*
+ * Split-KV ("flash decoding") decode attention: pa_decode_partial into the
+ * caller's workspace, then pa_combine into out/lse, both on `stream`.
+ * num_splits == 0 picks P with pa_choose_num_splits for the current device;
+ * P == 1 runs pa_decode directly and needs no workspace.  workspace: device,
+ * at least pa_splitkv_workspace_bytes(B, Hq, D, P) bytes, 256-byte aligned,
+ * else PA_EWORKSPACE.  Results equal pa_decode's up to fp32 rounding order.
+ */
+int pa_decode_splitkv(void *out, float *lse, const void *q, const void *k_cache,
+                      const void *v_cache, pa_cache_desc cache, const int32_t *block_tables,
+                      int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t B,
+                      int32_t Hq, float scale, int32_t num_splits, void *workspace,
+                      size_t workspace_bytes, int32_t *status, pa_stream_t stream);
+
+/* P that pa_decode_splitkv uses for num_splits == 0 on the current device (PA_ECUDA on error). */
+int pa_auto_num_splits(int32_t B, int32_t Hkv, int32_t max_blocks_per_seq, int32_t block_size);
+
+/* Static description of a return code. */
+const char *pa_strerror(int code);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

@@ -1,0 +1,312 @@
+// C ABI of libpagedattn (declared in include/pa.h): host-side argument
+// checks, TMA descriptor encoding, split-count policy and kernel dispatch.
+// Nothing here allocates device memory or synchronises the stream.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "pa_internal.h"
+
+namespace pa {
+cudaError_t launch_decode_cc_d64(int G, const CUtensorMap &kmap, const CUtensorMap &vmap,
+                                 const DecodeParams &p, int B, cudaStream_t stream);
+cudaError_t launch_decode_cc_d128(int G, const CUtensorMap &kmap, const CUtensorMap &vmap,
+                                  const DecodeParams &p, int B, cudaStream_t stream);
+
+cudaError_t launch_decode_cc(int D, int G, const CUtensorMap &kmap, const CUtensorMap &vmap,
+                             const DecodeParams &p, int B, cudaStream_t stream) {
+    if (D == 128) return launch_decode_cc_d128(G, kmap, vmap, p, B, stream);
+    if (D == 64) return launch_decode_cc_d64(G, kmap, vmap, p, B, stream);
+    return cudaErrorInvalidValue;
+}
+}  // namespace pa
+
+namespace {
+
+constexpr int kMaxGroup = 8;      // query heads per KV head handled by one CTA
+constexpr int kMaxGridZ = 65535;  // sequences per launch (gridDim.z)
+constexpr int kCtasPerSm = 2;     // resident decode CTAs per SM (shared-memory bound)
+constexpr int kMinTilesPerSplit = 8;
+constexpr int kMaxSplits = 256;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+// K or V pool [num_blocks, bs, Hkv, D] viewed as a 4-D tensor
+// (64 elements, D/64 sub-rows, Hkv heads, num_blocks*bs token rows); one box
+// is 16 token rows of one 64-element sub-row of one head, 128-byte swizzled.
+int make_kv_map(CUtensorMap *map, const void *base, const pa_cache_desc &c) {
+    auto enc = encode_fn();
+    if (!enc) return PA_ECUDA;
+    const cuuint64_t dims[4] = {64u, static_cast<cuuint64_t>(c.head_dim / 64),
+                                static_cast<cuuint64_t>(c.num_kv_heads),
+                                static_cast<cuuint64_t>(c.num_blocks) * c.block_size};
+    const cuuint64_t strides[3] = {128u, static_cast<cuuint64_t>(c.head_dim) * 2,
+                                   static_cast<cuuint64_t>(c.num_kv_heads) * c.head_dim * 2};
+    const cuuint32_t box[4] = {64u, 1u, 1u, 16u};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ECUDA;
+}
+
+int check_cache_desc(const pa_cache_desc &c) {
+    if (c.num_blocks <= 0 || c.block_size <= 0 || c.num_kv_heads <= 0 || c.head_dim <= 0)
+        return PA_EINVAL;
+    if (c.head_dim != 64 && c.head_dim != 128) return PA_EUNSUPPORTED;
+    if (c.block_size % 16 != 0) return PA_EUNSUPPORTED;
+    if (static_cast<int64_t>(c.num_blocks) * c.block_size > INT32_MAX) return PA_EUNSUPPORTED;
+    return PA_OK;
+}
+
+int check_decode_args(const void *q, const void *k_cache, const void *v_cache,
+                      const pa_cache_desc &c, const int32_t *block_tables,
+                      int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t B, int32_t Hq,
+                      float scale) {
+    if (B < 0) return PA_EINVAL;
+    if (!q || !k_cache || !v_cache || !block_tables || !seq_lens) return PA_EINVAL;
+    int rc = check_cache_desc(c);
+    if (rc) return rc;
+    if (Hq <= 0 || Hq % c.num_kv_heads != 0) return PA_EINVAL;
+    if (Hq / c.num_kv_heads > kMaxGroup) return PA_EUNSUPPORTED;
+    if (c.num_kv_heads > 65535) return PA_EUNSUPPORTED;
+    if (B > kMaxGridZ) return PA_EUNSUPPORTED;
+    if (max_blocks_per_seq <= 0) return PA_EINVAL;
+    if (static_cast<int64_t>(max_blocks_per_seq) * c.block_size > (INT32_MAX / 2))
+        return PA_EUNSUPPORTED;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(block_tables, 4) || !aligned(seq_lens, 4))
+        return PA_EINVAL;
+    if (!std::isfinite(scale)) return PA_EINVAL;
+    return PA_OK;
+}
+
+pa::DecodeParams base_params(const void *q, const pa_cache_desc &c, const int32_t *block_tables,
+                             int32_t max_blocks, const int32_t *seq_lens, int32_t Hq, float scale,
+                             int32_t *status) {
+    pa::DecodeParams p{};
+    p.q = static_cast<const uint16_t *>(q);
+    p.block_tables = block_tables;
+    p.seq_lens = seq_lens;
+    p.status = status;
+    p.num_blocks = c.num_blocks;
+    p.block_size = c.block_size;
+    p.num_kv_heads = c.num_kv_heads;
+    p.num_q_heads = Hq;
+    p.max_blocks = max_blocks;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    return p;
+}
+
+int sm_count_current() {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    if (dev >= 0 && dev < 64) {
+        int v = cache[dev].load(std::memory_order_relaxed);
+        if (v > 0) return v;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+int run_decode(bool split, void *out, float *lse, float *part_o, float *part_lse, const void *q,
+               const void *k_cache, const void *v_cache, const pa_cache_desc &c,
+               const int32_t *block_tables, int32_t max_blocks, const int32_t *seq_lens,
+               int32_t B, int32_t Hq, float scale, int32_t P, int32_t *status,
+               cudaStream_t stream) {
+    CUtensorMap kmap, vmap;
+    int rc = make_kv_map(&kmap, k_cache, c);
+    if (rc) return rc;
+    rc = make_kv_map(&vmap, v_cache, c);
+    if (rc) return rc;
+    pa::DecodeParams p = base_params(q, c, block_tables, max_blocks, seq_lens, Hq, scale, status);
+    p.out = out;
+    p.lse = lse;
+    p.part_o = part_o;
+    p.part_lse = part_lse;
+    p.split = split ? 1 : 0;
+    p.num_splits = P;
+    p.chunk = pa_partition_tokens(max_blocks, c.block_size, P);
+    const int G = Hq / c.num_kv_heads;
+    cudaError_t e = pa::launch_decode_cc(c.head_dim, G, kmap, vmap, p, B, stream);
+    return e == cudaSuccess ? PA_OK : PA_ECUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_version(void) { return 100; }
+
+const char *pa_strerror(int code) {
+    switch (code) {
+        case PA_OK: return "success";
+        case PA_EINVAL: return "invalid argument (null or misaligned pointer, inconsistent sizes)";
+        case PA_EUNSUPPORTED: return "unsupported shape (head_dim, block_size or GQA group size)";
+        case PA_EWORKSPACE: return "split-KV workspace missing or too small";
+        case PA_ECUDA: return "CUDA call or kernel launch failed";
+        default: return "unknown error code";
+    }
+}
+
+int pa_cache_write(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                   int64_t n_tokens, void *k_cache, void *v_cache, pa_cache_desc cache,
+                   int32_t *status, pa_stream_t stream) {
+    if (n_tokens < 0) return PA_EINVAL;
+    int rc = check_cache_desc(cache);
+    if (rc) return rc;
+    if (n_tokens == 0) return PA_OK;
+    if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache) return PA_EINVAL;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) ||
+        !aligned(v_cache, 16) || !aligned(slot_mapping, 8))
+        return PA_EINVAL;
+    const int row_bytes = cache.num_kv_heads * cache.head_dim * 2;
+    cudaError_t e = pa::launch_cache_write(
+        k_new, v_new, slot_mapping, n_tokens, k_cache, v_cache,
+        static_cast<int64_t>(cache.num_blocks) * cache.block_size, row_bytes, status, stream);
+    return e == cudaSuccess ? PA_OK : PA_ECUDA;
+}
+
+int pa_decode(void *out, float *lse, const void *q, const void *k_cache, const void *v_cache,
+              pa_cache_desc cache, const int32_t *block_tables, int32_t max_blocks_per_seq,
+              const int32_t *seq_lens, int32_t B, int32_t Hq, float scale, int32_t *status,
+              pa_stream_t stream) {
+    int rc = check_decode_args(q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq,
+                               seq_lens, B, Hq, scale);
+    if (rc) return rc;
+    if (!out || !aligned(out, 16) || (lse && !aligned(lse, 4))) return PA_EINVAL;
+    if (B == 0) return PA_OK;
+    return run_decode(false, out, lse, nullptr, nullptr, q, k_cache, v_cache, cache, block_tables,
+                      max_blocks_per_seq, seq_lens, B, Hq, scale, 1, status, stream);
+}
+
+int pa_partition_tokens(int32_t max_blocks_per_seq, int32_t block_size, int32_t num_splits) {
+    if (max_blocks_per_seq <= 0 || block_size <= 0 || num_splits <= 0) return PA_EINVAL;
+    const int64_t lmax = static_cast<int64_t>(max_blocks_per_seq) * block_size;
+    const int64_t per = (lmax + num_splits - 1) / num_splits;
+    return static_cast<int>(round_up(per, 16));
+}
+
+int pa_choose_num_splits(int32_t B, int32_t Hkv, int32_t max_blocks_per_seq, int32_t block_size,
+                         int32_t sm_count) {
+    if (B < 0 || Hkv <= 0 || max_blocks_per_seq <= 0 || block_size <= 0 || sm_count <= 0)
+        return PA_EINVAL;
+    if (B == 0) return 1;
+    const int64_t units = static_cast<int64_t>(B) * Hkv;
+    const int64_t slots = static_cast<int64_t>(sm_count) * kCtasPerSm;
+    int64_t P = slots / units;  // largest P whose grid still fits one wave
+    const int64_t lmax = static_cast<int64_t>(max_blocks_per_seq) * block_size;
+    const int64_t tiles = (lmax + 15) / 16;
+    const int64_t p_by_tiles = (tiles + kMinTilesPerSplit - 1) / kMinTilesPerSplit;
+    if (P > p_by_tiles) P = p_by_tiles;
+    if (P > kMaxSplits) P = kMaxSplits;
+    if (P < 1) P = 1;
+    // Drop partitions that the rounding of the chunk to whole tiles leaves empty.
+    const int chunk = pa_partition_tokens(max_blocks_per_seq, block_size, static_cast<int>(P));
+    P = (lmax + chunk - 1) / chunk;
+    return static_cast<int>(P);
+}
+
+int pa_auto_num_splits(int32_t B, int32_t Hkv, int32_t max_blocks_per_seq, int32_t block_size) {
+    const int sms = sm_count_current();
+    if (sms <= 0) return PA_ECUDA;
+    return pa_choose_num_splits(B, Hkv, max_blocks_per_seq, block_size, sms);
+}
+
+size_t pa_splitkv_workspace_bytes(int32_t B, int32_t Hq, int32_t D, int32_t num_splits) {
+    if (B <= 0 || Hq <= 0 || D <= 0 || num_splits <= 1) return 0;
+    const int64_t rows = static_cast<int64_t>(B) * Hq * num_splits;
+    return static_cast<size_t>(round_up(rows * D * 4, 256) + round_up(rows * 4, 256));
+}
+
+int pa_decode_partial(float *part_o, float *part_lse, const void *q, const void *k_cache,
+                      const void *v_cache, pa_cache_desc cache, const int32_t *block_tables,
+                      int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t B, int32_t Hq,
+                      float scale, int32_t num_splits, int32_t *status, pa_stream_t stream) {
+    int rc = check_decode_args(q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq,
+                               seq_lens, B, Hq, scale);
+    if (rc) return rc;
+    if (num_splits <= 0) return PA_EINVAL;
+    if (num_splits > 65535) return PA_EUNSUPPORTED;
+    if (!part_o || !part_lse || !aligned(part_o, 16) || !aligned(part_lse, 4)) return PA_EINVAL;
+    if (B == 0) return PA_OK;
+    return run_decode(true, nullptr, nullptr, part_o, part_lse, q, k_cache, v_cache, cache,
+                      block_tables, max_blocks_per_seq, seq_lens, B, Hq, scale, num_splits, status,
+                      stream);
+}
+
+int pa_combine(void *out, float *lse, const float *part_o, const float *part_lse, int32_t B,
+               int32_t Hq, int32_t num_splits, int32_t D, pa_stream_t stream) {
+    if (B < 0 || Hq <= 0 || num_splits <= 0) return PA_EINVAL;
+    if (D != 64 && D != 128) return PA_EUNSUPPORTED;
+    if (B == 0) return PA_OK;
+    if (!out || !part_o || !part_lse || !aligned(out, 16) || !aligned(part_o, 16) ||
+        !aligned(part_lse, 4) || (lse && !aligned(lse, 4)))
+        return PA_EINVAL;
+    const int64_t rows = static_cast<int64_t>(B) * Hq;
+    if (rows > INT32_MAX / 2) return PA_EUNSUPPORTED;
+    cudaError_t e = pa::launch_combine(out, lse, part_o, part_lse, static_cast<int>(rows),
+                                       num_splits, D, stream);
+    return e == cudaSuccess ? PA_OK : PA_ECUDA;
+}
+
+int pa_decode_splitkv(void *out, float *lse, const void *q, const void *k_cache,
+                      const void *v_cache, pa_cache_desc cache, const int32_t *block_tables,
+                      int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t B, int32_t Hq,
+                      float scale, int32_t num_splits, void *workspace, size_t workspace_bytes,
+                      int32_t *status, pa_stream_t stream) {
+    int rc = check_decode_args(q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq,
+                               seq_lens, B, Hq, scale);
+    if (rc) return rc;
+    if (!out || !aligned(out, 16) || (lse && !aligned(lse, 4))) return PA_EINVAL;
+    if (num_splits < 0) return PA_EINVAL;
+    if (B == 0) return PA_OK;
+    int P = num_splits;
+    if (P == 0) {
+        P = pa_auto_num_splits(cache.num_kv_heads > 0 ? B : 0, cache.num_kv_heads,
+                               max_blocks_per_seq, cache.block_size);
+        if (P < 0) return P;
+    }
+    if (P > 65535) return PA_EUNSUPPORTED;
+    if (P == 1)
+        return run_decode(false, out, lse, nullptr, nullptr, q, k_cache, v_cache, cache,
+                          block_tables, max_blocks_per_seq, seq_lens, B, Hq, scale, 1, status,
+                          stream);
+    const size_t need = pa_splitkv_workspace_bytes(B, Hq, cache.head_dim, P);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return PA_EWORKSPACE;
+    const int64_t rows = static_cast<int64_t>(B) * Hq * P;
+    float *part_o = static_cast<float *>(workspace);
+    float *part_lse = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
+                                                round_up(rows * cache.head_dim * 4, 256));
+    rc = run_decode(true, nullptr, nullptr, part_o, part_lse, q, k_cache, v_cache, cache,
+                    block_tables, max_blocks_per_seq, seq_lens, B, Hq, scale, P, status, stream);
+    if (rc) return rc;
+    cudaError_t e = pa::launch_combine(out, lse, part_o, part_lse, static_cast<int>(B * Hq), P,
+                                       cache.head_dim, stream);
+    return e == cudaSuccess ? PA_OK : PA_ECUDA;
+}
+
+}  // extern "C"

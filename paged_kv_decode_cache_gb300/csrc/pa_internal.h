@@ -1,0 +1,44 @@
+// Host-side declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pa.h"
+
+namespace pa {
+
+// Everything a decode CTA needs besides the two tensor maps.
+struct DecodeParams {
+    void *out;              // bf16 [B, Hq, D]            (unsplit)
+    float *lse;             // fp32 [B, Hq] or null      (unsplit)
+    float *part_o;          // fp32 [B, Hq, P, D]         (split)
+    float *part_lse;        // fp32 [B, Hq, P]            (split)
+    const uint16_t *q;      // bf16 [B, Hq, D]
+    const int32_t *block_tables;
+    const int32_t *seq_lens;
+    int32_t *status;
+    int32_t num_blocks;
+    int32_t block_size;
+    int32_t num_kv_heads;
+    int32_t num_q_heads;
+    int32_t max_blocks;
+    int32_t num_splits;     // P (gridDim.x)
+    int32_t chunk;          // tokens per partition, multiple of 16
+    int32_t split;          // 1: write partials, 0: write out/lse
+    float scale_log2;       // scale * log2(e)
+};
+
+// CUDA-core decode kernel launch (pa_decode_cc_d*.cu).  Returns a cudaError_t.
+cudaError_t launch_decode_cc(int D, int G, const CUtensorMap &kmap, const CUtensorMap &vmap,
+                             const DecodeParams &p, int B, cudaStream_t stream);
+
+cudaError_t launch_combine(void *out, float *lse, const float *part_o, const float *part_lse,
+                           int rows, int P, int D, cudaStream_t stream);
+
+cudaError_t launch_cache_write(const void *k_new, const void *v_new, const int64_t *slots,
+                               int64_t n, void *k_cache, void *v_cache, int64_t n_slots,
+                               int row_bytes, int32_t *status, cudaStream_t stream);
+
+}  // namespace pa

@@ -1,0 +1,243 @@
+"""Thin ctypes binding of libpagedattn (include/pa.h), same entry-point names.
+
+Argument marshalling only: every function checks dtypes, shapes and
+contiguity of the torch tensors it is given, passes their device pointers to
+the C entry point of the same name, and raises ``PAError`` on a negative
+return code.  All compute happens in the CUDA kernels; there is no fallback.
+Outputs are caller-allocated, as in the C ABI.  Work is enqueued on
+``stream`` (default: torch's current stream) and nothing synchronises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+PA_OK, PA_EINVAL, PA_EUNSUPPORTED, PA_EWORKSPACE, PA_ECUDA = 0, -1, -2, -3, -4
+PA_STATUS_BAD_BLOCK, PA_STATUS_BAD_SLOT, PA_STATUS_BAD_SEQLEN, PA_STATUS_TIMEOUT = 1, 2, 4, 8
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "pa.h")
+
+
+class PAError(RuntimeError):
+    def __init__(self, fn: str, code: int, msg: str):
+        super().__init__(f"{fn}: {msg} (code {code})")
+        self.code = code
+
+
+class CacheDesc(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+_P, _I32, _I64, _F32, _SZ = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
+                             ctypes.c_size_t)
+_SIGNATURES = {
+    "pa_cache_write": ([_P, _P, _P, _I64, _P, _P, CacheDesc, _P, _P], ctypes.c_int),
+    "pa_decode": ([_P, _P, _P, _P, _P, CacheDesc, _P, _I32, _P, _I32, _I32, _F32, _P, _P],
+                  ctypes.c_int),
+    "pa_choose_num_splits": ([_I32, _I32, _I32, _I32, _I32], ctypes.c_int),
+    "pa_partition_tokens": ([_I32, _I32, _I32], ctypes.c_int),
+    "pa_splitkv_workspace_bytes": ([_I32, _I32, _I32, _I32], _SZ),
+    "pa_decode_partial": ([_P, _P, _P, _P, _P, CacheDesc, _P, _I32, _P, _I32, _I32, _F32, _I32,
+                           _P, _P], ctypes.c_int),
+    "pa_combine": ([_P, _P, _P, _P, _I32, _I32, _I32, _I32, _P], ctypes.c_int),
+    "pa_decode_splitkv": ([_P, _P, _P, _P, _P, CacheDesc, _P, _I32, _P, _I32, _I32, _F32, _I32,
+                           _P, _SZ, _P, _P], ctypes.c_int),
+    "pa_auto_num_splits": ([_I32, _I32, _I32, _I32], ctypes.c_int),
+    "pa_strerror": ([ctypes.c_int], ctypes.c_char_p),
+    "pa_version": ([], ctypes.c_int),
+}
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """Load libpagedattn.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"{path} is missing: build it with paged_kv_decode_cache_gb300.build.build() "
+                    "(needs nvcc); there is no CPU fallback")
+            L = ctypes.CDLL(path)
+            for name, (args, res) in _SIGNATURES.items():
+                fn = getattr(L, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = L
+    return _lib
+
+
+def header_functions(path: str = HEADER) -> list[str]:
+    """Names of the functions include/pa.h declares."""
+    with open(path) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text)))
+
+
+def _check(name: str, rc: int):
+    if rc != PA_OK:
+        raise PAError(name, rc, pa_strerror(rc))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype, ndim: int):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+
+
+def cache_desc(k_cache: torch.Tensor) -> CacheDesc:
+    nb, bs, hkv, d = k_cache.shape
+    return CacheDesc(nb, bs, hkv, d)
+
+
+def pa_strerror(code: int) -> str:
+    return lib().pa_strerror(code).decode()
+
+
+def pa_version() -> int:
+    return lib().pa_version()
+
+
+def pa_choose_num_splits(B: int, Hkv: int, max_blocks_per_seq: int, block_size: int,
+                         sm_count: int) -> int:
+    r = lib().pa_choose_num_splits(B, Hkv, max_blocks_per_seq, block_size, sm_count)
+    _check("pa_choose_num_splits", min(r, 0))
+    return r
+
+
+def pa_partition_tokens(max_blocks_per_seq: int, block_size: int, num_splits: int) -> int:
+    r = lib().pa_partition_tokens(max_blocks_per_seq, block_size, num_splits)
+    _check("pa_partition_tokens", min(r, 0))
+    return r
+
+
+def pa_splitkv_workspace_bytes(B: int, Hq: int, D: int, num_splits: int) -> int:
+    return int(lib().pa_splitkv_workspace_bytes(B, Hq, D, num_splits))
+
+
+def pa_auto_num_splits(B: int, Hkv: int, max_blocks_per_seq: int, block_size: int) -> int:
+    r = lib().pa_auto_num_splits(B, Hkv, max_blocks_per_seq, block_size)
+    _check("pa_auto_num_splits", min(r, 0))
+    return r
+
+
+def pa_cache_write(k_new, v_new, slot_mapping, k_cache, v_cache, status=None, stream=None):
+    _need(k_new, "k_new", torch.bfloat16, 3)
+    _need(v_new, "v_new", torch.bfloat16, 3)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    if v_cache.shape != k_cache.shape or v_new.shape != k_new.shape:
+        raise ValueError("K/V shape mismatch")
+    if k_new.shape[0] != slot_mapping.shape[0] or tuple(k_new.shape[1:]) != tuple(k_cache.shape[2:]):
+        raise ValueError("k_new must be [N, Hkv, D] matching the pool")
+    rc = lib().pa_cache_write(_ptr(k_new), _ptr(v_new), _ptr(slot_mapping), slot_mapping.shape[0],
+                              _ptr(k_cache), _ptr(v_cache), cache_desc(k_cache), _ptr(status),
+                              _stream(stream))
+    _check("pa_cache_write", rc)
+
+
+def _decode_inputs(q, k_cache, v_cache, block_tables, seq_lens):
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    if v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache and v_cache differ in shape")
+    B, Hq, D = q.shape
+    if k_cache.shape[3] != D or block_tables.shape[0] != B or seq_lens.shape[0] != B:
+        raise ValueError("inconsistent q / cache / table shapes")
+    return B, Hq, D
+
+
+def pa_decode(out, lse, q, k_cache, v_cache, block_tables, seq_lens, scale, status=None,
+              stream=None):
+    B, Hq, D = _decode_inputs(q, k_cache, v_cache, block_tables, seq_lens)
+    _need(out, "out", torch.bfloat16, 3)
+    if tuple(out.shape) != (B, Hq, D):
+        raise ValueError("out must be [B, Hq, D]")
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 2)
+    rc = lib().pa_decode(_ptr(out), _ptr(lse), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                         cache_desc(k_cache), _ptr(block_tables), block_tables.shape[1],
+                         _ptr(seq_lens), B, Hq, float(scale), _ptr(status), _stream(stream))
+    _check("pa_decode", rc)
+
+
+def pa_decode_partial(part_o, part_lse, q, k_cache, v_cache, block_tables, seq_lens, scale,
+                      num_splits, status=None, stream=None):
+    B, Hq, D = _decode_inputs(q, k_cache, v_cache, block_tables, seq_lens)
+    _need(part_o, "part_o", torch.float32, 4)
+    _need(part_lse, "part_lse", torch.float32, 3)
+    if tuple(part_o.shape) != (B, Hq, num_splits, D) or tuple(part_lse.shape) != (B, Hq, num_splits):
+        raise ValueError("partials must be [B, Hq, P, D] and [B, Hq, P]")
+    rc = lib().pa_decode_partial(_ptr(part_o), _ptr(part_lse), _ptr(q), _ptr(k_cache),
+                                 _ptr(v_cache), cache_desc(k_cache), _ptr(block_tables),
+                                 block_tables.shape[1], _ptr(seq_lens), B, Hq, float(scale),
+                                 num_splits, _ptr(status), _stream(stream))
+    _check("pa_decode_partial", rc)
+
+
+def pa_combine(out, lse, part_o, part_lse, stream=None):
+    _need(part_o, "part_o", torch.float32, 4)
+    _need(part_lse, "part_lse", torch.float32, 3)
+    _need(out, "out", torch.bfloat16, 3)
+    B, Hq, P, D = part_o.shape
+    if tuple(out.shape) != (B, Hq, D) or tuple(part_lse.shape) != (B, Hq, P):
+        raise ValueError("inconsistent combine shapes")
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 2)
+    rc = lib().pa_combine(_ptr(out), _ptr(lse), _ptr(part_o), _ptr(part_lse), B, Hq, P, D,
+                          _stream(stream))
+    _check("pa_combine", rc)
+
+
+def pa_decode_splitkv(out, lse, q, k_cache, v_cache, block_tables, seq_lens, scale,
+                      num_splits=0, workspace=None, status=None, stream=None):
+    B, Hq, D = _decode_inputs(q, k_cache, v_cache, block_tables, seq_lens)
+    _need(out, "out", torch.bfloat16, 3)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 2)
+    ws_bytes = 0
+    if workspace is not None:
+        if not (workspace.is_cuda and workspace.is_contiguous()):
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    rc = lib().pa_decode_splitkv(_ptr(out), _ptr(lse), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                 cache_desc(k_cache), _ptr(block_tables), block_tables.shape[1],
+                                 _ptr(seq_lens), B, Hq, float(scale), num_splits,
+                                 _ptr(workspace), ws_bytes, _ptr(status), _stream(stream))
+    _check("pa_decode_splitkv", rc)

@@ -1,0 +1,137 @@
+"""The C-ABI library builds, loads and exports every function include/pa.h
+declares; host-side logic (split policy, workspace sizing, argument checks
+that reject before any CUDA call) behaves as documented.  No GPU needed."""
+import ctypes
+import subprocess
+
+import pytest
+
+from paged_kv_decode_cache_gb300 import build as B
+from paged_kv_decode_cache_gb300 import pa
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return pa.lib()
+
+
+def test_header_declares_the_boundary():
+    names = set(pa.header_functions())
+    for required in ("pa_cache_write", "pa_decode", "pa_decode_splitkv", "pa_combine",
+                     "pa_decode_partial", "pa_choose_num_splits", "pa_splitkv_workspace_bytes",
+                     "pa_strerror"):
+        assert required in names
+
+
+def test_every_declared_function_is_exported(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", pa.library_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    missing = [n for n in pa.header_functions() if n not in exported]
+    assert not missing, f"declared but not exported: {missing}"
+    for n in pa.header_functions():
+        assert isinstance(getattr(lib, n), ctypes._CFuncPtr)
+
+
+def test_binding_covers_the_header():
+    assert set(pa.header_functions()) == set(pa._SIGNATURES)
+
+
+def test_version_and_strerror(lib):
+    assert pa.pa_version() >= 100
+    for code in (pa.PA_OK, pa.PA_EINVAL, pa.PA_EUNSUPPORTED, pa.PA_EWORKSPACE, pa.PA_ECUDA):
+        assert pa.pa_strerror(code) and pa.pa_strerror(code) != "unknown error code"
+    assert pa.pa_strerror(-99) == "unknown error code"
+
+
+@pytest.mark.parametrize("B,Hkv,mb,bs,sms", [
+    (8, 4, 256, 16, 152), (1, 4, 2048, 16, 152), (2, 4, 2048, 16, 152), (256, 8, 128, 16, 152),
+    (8, 2, 128, 16, 152), (1, 2, 128, 16, 152), (8, 4, 16, 256, 152), (4, 2, 7, 16, 152),
+    (1, 1, 1, 16, 152), (3, 1, 1000, 16, 132),
+])
+def test_split_policy(lib, B, Hkv, mb, bs, sms):
+    P = pa.pa_choose_num_splits(B, Hkv, mb, bs, sms)
+    lmax = mb * bs
+    assert 1 <= P <= 256
+    chunk = pa.pa_partition_tokens(mb, bs, P)
+    assert chunk % 16 == 0 and chunk * P >= lmax and chunk * (P - 1) < lmax  # no empty tail split
+    if P > 1:
+        assert B * Hkv * P <= 2 * sms          # one wave of resident CTAs
+        assert chunk >= 16 * 8 or chunk * P >= lmax
+    if B * Hkv >= 2 * sms:
+        assert P == 1
+
+
+def test_split_policy_fills_small_batches(lib):
+    # 4 work units (B=1, Hkv=4) at 32k tokens: the split fills every SM slot.
+    P = pa.pa_choose_num_splits(1, 4, 2048, 16, 152)
+    assert 4 * P >= 0.9 * 2 * 152
+
+
+def test_partition_tokens(lib):
+    assert pa.pa_partition_tokens(256, 16, 1) == 4096
+    assert pa.pa_partition_tokens(256, 16, 9) == 464
+    assert pa.pa_partition_tokens(7, 16, 3) == 48
+    assert lib.pa_partition_tokens(0, 16, 1) == pa.PA_EINVAL
+
+
+def test_workspace_bytes(lib):
+    assert pa.pa_splitkv_workspace_bytes(8, 28, 128, 1) == 0
+    n = pa.pa_splitkv_workspace_bytes(8, 28, 128, 9)
+    rows = 8 * 28 * 9
+    assert n >= rows * 128 * 4 + rows * 4 and n % 256 == 0
+
+
+def _desc(nb=64, bs=16, hkv=2, d=64):
+    return pa.CacheDesc(nb, bs, hkv, d)
+
+
+FAKE = ctypes.c_void_p(1 << 20)  # aligned, never dereferenced: these calls fail validation first
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=-1), pa.PA_EINVAL),
+    (dict(q=None), pa.PA_EINVAL),
+    (dict(Hq=5), pa.PA_EINVAL),                 # Hq % Hkv != 0
+    (dict(Hq=18), pa.PA_EUNSUPPORTED),          # G = 9 > 8
+    (dict(desc=_desc(d=96)), pa.PA_EUNSUPPORTED),
+    (dict(desc=_desc(bs=8)), pa.PA_EUNSUPPORTED),
+    (dict(desc=_desc(nb=0)), pa.PA_EINVAL),
+    (dict(max_blocks=0), pa.PA_EINVAL),
+    (dict(q=ctypes.c_void_p((1 << 20) + 2)), pa.PA_EINVAL),   # misaligned
+    (dict(scale=float("nan")), pa.PA_EINVAL),
+    (dict(B=70000), pa.PA_EUNSUPPORTED),
+])
+def test_decode_rejects_bad_arguments(lib, kw, code):
+    a = dict(out=FAKE, lse=None, q=FAKE, k=FAKE, v=FAKE, desc=_desc(), bt=FAKE, max_blocks=7,
+             sl=FAKE, B=4, Hq=4, scale=0.125, status=None, stream=None)
+    a.update(kw)
+    rc = lib.pa_decode(a["out"], a["lse"], a["q"], a["k"], a["v"], a["desc"], a["bt"],
+                       a["max_blocks"], a["sl"], a["B"], a["Hq"], a["scale"], a["status"],
+                       a["stream"])
+    assert rc == code
+
+
+def test_empty_batch_is_a_noop(lib):
+    assert lib.pa_decode(FAKE, None, FAKE, FAKE, FAKE, _desc(), FAKE, 7, FAKE, 0, 4, 0.1,
+                         None, None) == pa.PA_OK
+    assert lib.pa_cache_write(FAKE, FAKE, FAKE, 0, FAKE, FAKE, _desc(), None, None) == pa.PA_OK
+
+
+def test_splitkv_rejects_missing_workspace(lib):
+    rc = lib.pa_decode_splitkv(FAKE, None, FAKE, FAKE, FAKE, _desc(), FAKE, 7, FAKE, 4, 4, 0.1,
+                               4, None, 0, None, None)
+    assert rc == pa.PA_EWORKSPACE
+    rc = lib.pa_decode_splitkv(FAKE, None, FAKE, FAKE, FAKE, _desc(), FAKE, 7, FAKE, 4, 4, 0.1,
+                               -1, None, 0, None, None)
+    assert rc == pa.PA_EINVAL
+
+
+def test_combine_and_write_reject_bad_arguments(lib):
+    assert lib.pa_combine(FAKE, None, FAKE, FAKE, 2, 4, 0, 128, None) == pa.PA_EINVAL
+    assert lib.pa_combine(FAKE, None, FAKE, FAKE, 2, 4, 3, 80, None) == pa.PA_EUNSUPPORTED
+    assert lib.pa_cache_write(None, FAKE, FAKE, 3, FAKE, FAKE, _desc(), None, None) == pa.PA_EINVAL
+    assert lib.pa_cache_write(FAKE, FAKE, FAKE, -1, FAKE, FAKE, _desc(), None, None) == pa.PA_EINVAL
+    assert lib.pa_decode_partial(FAKE, FAKE, FAKE, FAKE, FAKE, _desc(), FAKE, 7, FAKE, 4, 4, 0.1,
+                                 0, None, None) == pa.PA_EINVAL

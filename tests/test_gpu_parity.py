@@ -1,0 +1,261 @@
+"""CUDA path vs the fp64 oracle, through the C ABI (needs a GB300)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import (Dev, assert_close, assert_lse_close, bf16_dev_to_f64, oracle_after_write,
+                      oracle_rows, sample_rows, u16_to_dev_bf16)
+from paged_kv_decode_cache_gb300 import pa
+from paged_kv_decode_cache_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from paged_kv_decode_cache_gb300 import build
+    build.build()
+
+
+# ---------------------------------------------------------------- cache write
+def test_cache_write_bit_exact_with_sentinels():
+    rng = np.random.default_rng(0)
+    nb, bs, hkv, d = 40, 16, 8, 128
+    sentinel = np.uint16(0x5A5A)
+    kc = np.full((nb, bs, hkv, d), sentinel, np.uint16)
+    vc = np.full((nb, bs, hkv, d), sentinel, np.uint16)
+    slots = rng.choice(nb * bs, 300, replace=False).astype(np.int64)
+    slots[::7] = -1                               # padding
+    kn = rng.integers(0, 0xFFFF, (300, hkv, d), dtype=np.uint16)
+    vn = rng.integers(0, 0xFFFF, (300, hkv, d), dtype=np.uint16)
+    dk, dv = u16_to_dev_bf16(kc), u16_to_dev_bf16(vc)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.pa_cache_write(u16_to_dev_bf16(kn), u16_to_dev_bf16(vn), torch.from_numpy(slots).cuda(),
+                      dk, dv, status=status)
+    oracle.cache_write(kn, vn, slots, kc, vc)
+    gk = dk.view(torch.int16).cpu().numpy().view(np.uint16)
+    gv = dv.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(gk, kc) and np.array_equal(gv, vc)
+    assert status.item() == 0
+
+
+def test_cache_write_out_of_pool_slot_is_skipped_and_reported():
+    nb, bs, hkv, d = 4, 16, 2, 64
+    kc = np.zeros((nb, bs, hkv, d), np.uint16)
+    slots = np.array([3, nb * bs + 5, 10], np.int64)
+    kn = np.full((3, hkv, d), 0x3F80, np.uint16)
+    dk, dv = u16_to_dev_bf16(kc), u16_to_dev_bf16(kc)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.pa_cache_write(u16_to_dev_bf16(kn), u16_to_dev_bf16(kn), torch.from_numpy(slots).cuda(),
+                      dk, dv, status=status)
+    assert status.item() & pa.PA_STATUS_BAD_SLOT
+    ref = kc.copy()
+    oracle.cache_write(kn[[0, 2]], kn[[0, 2]], slots[[0, 2]], ref, ref.copy())
+    assert np.array_equal(dk.view(torch.int16).cpu().numpy().view(np.uint16), ref)
+
+
+# ------------------------------------------------------- decode, small shapes
+SMALL = [
+    # (Hq, Hkv, D, bs, lens)
+    (4, 2, 64, 16, (1, 17, 33, 100)),
+    (8, 8, 128, 16, (1, 15, 16, 17, 31, 33)),       # G = 1
+    (12, 2, 128, 16, (48, 130, 7)),                 # G = 6
+    (28, 4, 128, 16, (257, 16, 1)),                 # G = 7
+    (16, 2, 128, 16, (64, 65)),                     # G = 8
+    (6, 2, 64, 16, (200, 3)),                       # G = 3
+    (10, 2, 128, 32, (95, 64, 1)),                  # G = 5, 32-token blocks
+    (16, 4, 128, 256, (300, 513, 256, 1)),          # 256-token pages
+    (4, 1, 64, 256, (1000,)),                       # G = 4, pages, long-ish
+    (2, 2, 128, 16, (0, 5)),                        # empty sequence
+]
+
+
+def _small(Hq, Hkv, D, bs, lens, seed=0, **kw):
+    nb = sum((L + bs - 1) // bs for L in lens) + 5
+    return W.make_workload("small", B=len(lens), Hq=Hq, Hkv=Hkv, D=D, block_size=bs,
+                           seq_lens=list(lens), num_blocks=nb, seed=seed, **kw)
+
+
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: f"Hq{c[0]}-Hkv{c[1]}-D{c[2]}-bs{c[3]}")
+def test_decode_small_elementwise(case):
+    w = _small(*case, seed=hash(case) % 1000, poison_unused=True)
+    dev = Dev(w)
+    dev.write()
+    out, lse = dev.decode()
+    kc, vc = oracle_after_write(w)
+    ref, ref_lse = oracle.decode(w.q, kc, vc, w.block_tables, w.seq_lens, w.scale)
+    assert_close(bf16_dev_to_f64(out), ref, "pa_decode")
+    assert_lse_close(lse.cpu().double().numpy(), ref_lse, "pa_decode")
+    for P in (2, 3, 7):
+        so, sl, _ = dev.splitkv(P)
+        assert_close(bf16_dev_to_f64(so), ref, f"splitkv P={P}")
+        assert_lse_close(sl.cpu().double().numpy(), ref_lse, f"splitkv P={P}")
+    assert dev.status_value() == 0
+
+
+@pytest.mark.parametrize("P", [1, 2, 5, 16, 40])
+def test_partials_match_oracle_partials(P):
+    w = _small(12, 2, 128, 16, (1, 70, 129, 400), seed=P)
+    dev = Dev(w)
+    dev.write()
+    kc, vc = oracle_after_write(w)
+    chunk = pa.pa_partition_tokens(w.max_blocks, w.block_size, P)
+    po, pl = dev.partial(P)
+    ro, rl = oracle.decode_partial(w.q, kc, vc, w.block_tables, w.seq_lens, w.scale, P, chunk)
+    assert_close(po.cpu().double().numpy(), ro, "partial o")
+    assert_lse_close(pl.cpu().double().numpy(), rl, "partial lse")
+
+
+def test_combine_matches_oracle():
+    g = torch.Generator().manual_seed(3)
+    B, Hq, P, D = 3, 5, 9, 128
+    po = torch.randn(B, Hq, P, D, generator=g, dtype=torch.float64).float()
+    pl = (torch.randn(B, Hq, P, generator=g, dtype=torch.float64) * 4).float()
+    pl[0, 0, :] = -math.inf                       # all partitions empty
+    pl[1, 2, 3:] = -math.inf                      # some empty
+    po[pl == -math.inf] = 0
+    out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(B, Hq, dtype=torch.float32, device="cuda")
+    pa.pa_combine(out, lse, po.cuda(), pl.cuda())
+    ro, rl = oracle.combine(po.double().numpy(), pl.double().numpy())
+    assert_close(bf16_dev_to_f64(out), ro, "combine")
+    assert_lse_close(lse.cpu().double().numpy(), rl, "combine")
+
+
+# ----------------------------------------------------- workloads at full size
+FULL = ["tiny", "qwen2.5-1.5b-B1", "qwen2.5-1.5b-B8", "qwen2.5-7b-bs16", "qwen2.5-7b-bs256",
+        "long-B1-L4096", "long-B2-L4096", "long-B1-L32768", "long-B2-L32768", "qwen3-0.6b-B256"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_workload_full_size(name):
+    """The bench's launch configuration (auto split) plus the unsplit kernel, on the
+    full-size workload; all rows for small batches, a seeded sample otherwise."""
+    w = W.WORKLOADS[name]()
+    dev = Dev(w)
+    dev.write()
+    out_s, lse_s, P = dev.splitkv(0)
+    out_u, lse_u = dev.decode()
+    assert dev.status_value() == 0
+    kc, vc = oracle_after_write(w)
+    rb, rh = sample_rows(w, 160, seed=len(name))
+    ref, ref_lse = oracle_rows(w, kc, vc, rb, rh)
+    for tag, o, l in (("splitkv", out_s, lse_s), ("decode", out_u, lse_u)):
+        assert_close(bf16_dev_to_f64(o)[rb, rh], ref, f"{name} {tag} P={P}")
+        assert_lse_close(l.cpu().double().numpy()[rb, rh], ref_lse, f"{name} {tag}")
+
+
+# ------------------------------------------------------ bit-exact invariants
+def test_block_permutation_invariance_bit_exact():
+    w = _small(28, 4, 128, 16, (300, 77, 16), seed=5)
+    dev = Dev(w)
+    out1, lse1 = dev.decode()
+    perm = np.random.default_rng(2).permutation(w.num_blocks)
+    inv = np.argsort(perm)
+    w2 = _small(28, 4, 128, 16, (300, 77, 16), seed=5)
+    w2.k_cache = w.k_cache[inv].copy()
+    w2.v_cache = w.v_cache[inv].copy()
+    w2.block_tables = np.where(w.block_tables >= 0, perm[np.maximum(w.block_tables, 0)],
+                               -1).astype(np.int32)
+    out2, lse2 = Dev(w2).decode()
+    assert torch.equal(out1, out2) and torch.equal(lse1, lse2)
+
+
+def test_single_token_returns_v_row_exactly():
+    w = _small(8, 2, 128, 16, (1, 1, 1), seed=9)
+    dev = Dev(w)
+    dev.write()
+    out, _ = dev.decode()
+    o2, _, _ = dev.splitkv(3)
+    got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+    for b in range(w.B):
+        for h in range(w.Hq):
+            assert np.array_equal(got[b, h], w.v_new[b, h // w.G])
+    assert torch.equal(out, o2)
+
+
+def test_value_scaling_by_two_is_exact():
+    w = _small(12, 2, 128, 16, (100, 33), seed=11)
+    out1, lse1 = Dev(w).decode()
+    v2 = torch.from_numpy(w.v_cache.view(np.int16)).view(torch.bfloat16).float() * 2
+    w.v_cache = v2.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    out2, lse2 = Dev(w).decode()
+    assert torch.equal(out2.float(), out1.float() * 2) and torch.equal(lse1, lse2)
+
+
+def test_identical_query_heads_give_identical_outputs():
+    w = _small(16, 2, 128, 16, (90, 40), seed=13)
+    w.q[:] = w.q[:, :1]
+    out, _ = Dev(w).decode()
+    for g in range(w.Hkv):
+        grp = out[:, g * w.G:(g + 1) * w.G]
+        assert torch.equal(grp, grp[:, :1].expand_as(grp))
+
+
+def test_poisoned_pool_rows_never_leak():
+    lens = (5, 17, 250)
+    clean = Dev(_small(12, 2, 128, 16, lens, seed=17)).decode()[0]
+    poisoned = Dev(_small(12, 2, 128, 16, lens, seed=17, poison_unused=True)).decode()[0]
+    assert torch.isfinite(poisoned.float()).all()
+    assert torch.equal(clean, poisoned)
+
+
+# ---------------------------------------------------------- bad device data
+def test_bad_block_id_is_reported_not_dereferenced():
+    w = _small(4, 2, 64, 16, (40, 20), seed=19)
+    w.block_tables[0, 1] = w.num_blocks + 1000
+    w.block_tables[1, 0] = -5
+    dev = Dev(w)
+    out, _ = dev.decode()
+    torch.cuda.synchronize()
+    assert dev.status_value() & pa.PA_STATUS_BAD_BLOCK
+
+
+def test_bad_seq_len_is_reported_and_clamped():
+    w = _small(4, 2, 64, 16, (40, 20), seed=23)
+    w.seq_lens = np.array([40, 10_000], np.int32)
+    dev = Dev(w)
+    dev.decode()
+    torch.cuda.synchronize()
+    assert dev.status_value() & pa.PA_STATUS_BAD_SEQLEN
+
+
+def test_splitkv_small_workspace_is_rejected():
+    w = _small(12, 2, 128, 16, (300,), seed=29)
+    dev = Dev(w)
+    out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(pa.PAError) as e:
+        pa.pa_decode_splitkv(out, None, dev.q, dev.k_cache, dev.v_cache, dev.block_tables,
+                             dev.seq_lens, w.scale, num_splits=4, workspace=ws)
+    assert e.value.code == pa.PA_EWORKSPACE
+
+
+# ------------------------------------------------------------ graph capture
+def test_decode_step_replays_in_a_cuda_graph():
+    w = W.qwen25_1p5b(8)
+    dev = Dev(w)
+    P = pa.pa_auto_num_splits(w.B, w.Hkv, w.max_blocks, w.block_size)
+    ws = torch.empty(pa.pa_splitkv_workspace_bytes(w.B, w.Hq, w.D, P), dtype=torch.uint8,
+                     device="cuda")
+    out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        dev.write()
+        pa.pa_decode_splitkv(out, None, dev.q, dev.k_cache, dev.v_cache, dev.block_tables,
+                             dev.seq_lens, w.scale, num_splits=P, workspace=ws)
+    torch.cuda.current_stream().wait_stream(s)
+    eager = out.clone()
+    out.zero_()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        pa.pa_cache_write(dev.k_new, dev.v_new, dev.slot_mapping, dev.k_cache, dev.v_cache)
+        pa.pa_decode_splitkv(out, None, dev.q, dev.k_cache, dev.v_cache, dev.block_tables,
+                             dev.seq_lens, w.scale, num_splits=P, workspace=ws)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager)
