@@ -328,10 +328,11 @@ decode_cc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     }
 }
 
-// Opt a kernel into more than 48 KB of dynamic shared memory, once per device.
+// Opt a kernel into more than 48 KB of dynamic shared memory, once per
+// device.  `done` must be distinct for every kernel: callers pass a static
+// that lives in their own (per-instantiation) function.
 template <typename Kernel>
-cudaError_t ensure_smem_attr(Kernel kern, int bytes) {
-    static std::atomic<uint64_t> done{0};
+cudaError_t ensure_smem_attr(std::atomic<uint64_t> &done, Kernel kern, int bytes) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -349,7 +350,8 @@ cudaError_t launch_cc_instance(const CUtensorMap &kmap, const CUtensorMap &vmap,
     constexpr int NST = (D == 128) ? 3 : 4;
     using C = CcCfg<D, G, NW, NST>;
     auto kern = decode_cc_kernel<D, G, NW, NST>;
-    cudaError_t e = ensure_smem_attr(kern, C::kSmemBytes);
+    static std::atomic<uint64_t> smem_attr_done{0};
+    cudaError_t e = ensure_smem_attr(smem_attr_done, kern, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     dim3 grid(p.num_splits, p.num_kv_heads, B);
     kern<<<grid, NW * 32, C::kSmemBytes, stream>>>(kmap, vmap, p);
