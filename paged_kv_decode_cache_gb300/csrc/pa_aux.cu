@@ -50,10 +50,13 @@ cudaError_t launch_cache_write(const void *k_new, const void *v_new, const int64
     return cudaGetLastError();
 }
 
-// One warp per output row (b, h).  Each lane owns D/32 dims.  The lanes
-// first find M = max_p lse_p and the total lse by a strided pass over the P
-// partials plus warp reductions; then every lane walks the partials in order
-// and accumulates exp(lse_p - lse) * o_p for its dims.
+// One warp per output row (b, h); each lane owns D/32 dims.  The P partial
+// LSEs are read once, coalesced (lane i holds partitions i, i+32, ...); the
+// warp reduces their max and sum, so lane i then knows the final weight
+// exp(lse_p - lse) of its partitions and hands it to the other lanes by
+// shuffle while all lanes stream the partial outputs.  The partial loads of
+// consecutive partitions are independent, so the unrolled loop keeps several
+// in flight.
 template <int D>
 __global__ void __launch_bounds__(128)
 combine_kernel(__nv_bfloat16 *__restrict__ out, float *__restrict__ lse,
@@ -79,19 +82,25 @@ combine_kernel(__nv_bfloat16 *__restrict__ out, float *__restrict__ lse,
         for (int off = 16; off; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
         total = M + logf(z);
         const float *po = part_o + static_cast<int64_t>(row) * P * D + lane * kDPL;
-        for (int i = 0; i < P; ++i) {
-            const float w = expf(pl[i] - total);
-            if (w == 0.f) continue;
-            if constexpr (kDPL == 4) {
-                const float4 v = *reinterpret_cast<const float4 *>(po + static_cast<int64_t>(i) * D);
-                acc[0] = fmaf(w, v.x, acc[0]);
-                acc[1] = fmaf(w, v.y, acc[1]);
-                acc[2] = fmaf(w, v.z, acc[2]);
-                acc[3] = fmaf(w, v.w, acc[3]);
-            } else {
-                const float2 v = *reinterpret_cast<const float2 *>(po + static_cast<int64_t>(i) * D);
-                acc[0] = fmaf(w, v.x, acc[0]);
-                acc[1] = fmaf(w, v.y, acc[1]);
+        for (int base = 0; base < P; base += 32) {
+            const int i = base + lane;
+            const float wl = i < P ? expf(pl[i] - total) : 0.f;  // weight of partition i
+            const int n = min(32, P - base);
+#pragma unroll 4
+            for (int j = 0; j < n; ++j) {
+                const float w = __shfl_sync(0xffffffffu, wl, j);
+                const float *src = po + static_cast<int64_t>(base + j) * D;
+                if constexpr (kDPL == 4) {
+                    const float4 v = *reinterpret_cast<const float4 *>(src);
+                    acc[0] = fmaf(w, v.x, acc[0]);
+                    acc[1] = fmaf(w, v.y, acc[1]);
+                    acc[2] = fmaf(w, v.z, acc[2]);
+                    acc[3] = fmaf(w, v.w, acc[3]);
+                } else {
+                    const float2 v = *reinterpret_cast<const float2 *>(src);
+                    acc[0] = fmaf(w, v.x, acc[0]);
+                    acc[1] = fmaf(w, v.y, acc[1]);
+                }
             }
         }
     }
