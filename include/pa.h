@@ -190,6 +190,35 @@ int pa_decode_splitkv(void *out, float *lse, const void *q, const void *k_cache,
                       int32_t Hq, float scale, int32_t num_splits, void *workspace,
                       size_t workspace_bytes, int32_t *status, pa_stream_t stream);
 
+/* Size of the scratch array built into the library for pa_decode_splitkv_noalloc. */
+#define PA_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
+
+/*
+ * Split-KV decode attention that needs no workspace from the caller and
+ * allocates nothing.  There is no counterpart on the pages: it exists for
+ * callers that cannot call cudaMalloc (or any allocator) where they run
+ * decode -- for instance code whose device memory is planned up front by
+ * another component, or a plugin that is handed only its inputs and outputs.
+ * Arguments and results are those of pa_decode_splitkv without the
+ * workspace.  The split's partials live in a file-scope device array of
+ * PA_NOALLOC_SCRATCH_BYTES (4 MiB) inside the library, which every GPU that
+ * loads the library holds until the process exits.
+ *   - The first call on a device looks up that array's device address
+ *     (cudaGetSymbolAddress, with the device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - Returns PA_EWORKSPACE when the split's partials,
+ *     pa_splitkv_workspace_bytes(B, Hq, D, P), exceed the array.
+ *   - Every call shares the one array: calls whose kernels overlap on the
+ *     GPU (other streams, other host threads) race on it and must be
+ *     serialised by the caller.  Nothing in it needs to start at zero; each
+ *     call writes every element it reads.
+ */
+int pa_decode_splitkv_noalloc(void *out, float *lse, const void *q, const void *k_cache,
+                              const void *v_cache, pa_cache_desc cache,
+                              const int32_t *block_tables, int32_t max_blocks_per_seq,
+                              const int32_t *seq_lens, int32_t B, int32_t Hq, float scale,
+                              int32_t num_splits, int32_t *status, pa_stream_t stream);
+
 /* P that pa_decode_splitkv uses for num_splits == 0 on the current device (PA_ECUDA on error). */
 int pa_auto_num_splits(int32_t B, int32_t Hkv, int32_t max_blocks_per_seq, int32_t block_size);
 

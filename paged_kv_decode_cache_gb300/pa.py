@@ -53,6 +53,8 @@ _SIGNATURES = {
     "pa_combine": ([_P, _P, _P, _P, _I32, _I32, _I32, _I32, _P], ctypes.c_int),
     "pa_decode_splitkv": ([_P, _P, _P, _P, _P, CacheDesc, _P, _I32, _P, _I32, _I32, _F32, _I32,
                            _P, _SZ, _P, _P], ctypes.c_int),
+    "pa_decode_splitkv_noalloc": ([_P, _P, _P, _P, _P, CacheDesc, _P, _I32, _P, _I32, _I32, _F32,
+                                   _I32, _P, _P], ctypes.c_int),
     "pa_auto_num_splits": ([_I32, _I32, _I32, _I32], ctypes.c_int),
     "pa_strerror": ([ctypes.c_int], ctypes.c_char_p),
     "pa_version": ([], ctypes.c_int),
@@ -241,3 +243,22 @@ def pa_decode_splitkv(out, lse, q, k_cache, v_cache, block_tables, seq_lens, sca
                                  _ptr(seq_lens), B, Hq, float(scale), num_splits,
                                  _ptr(workspace), ws_bytes, _ptr(status), _stream(stream))
     _check("pa_decode_splitkv", rc)
+
+
+PA_NOALLOC_SCRATCH_BYTES = 4 << 20
+
+
+def pa_decode_splitkv_noalloc(out, lse, q, k_cache, v_cache, block_tables, seq_lens, scale,
+                              num_splits=0, status=None, stream=None):
+    """Split-KV decode with the partials in the library's built-in device array
+    (no workspace argument, no allocation).  Calls that overlap on the GPU race
+    on that array; the first call on a device should precede stream capture."""
+    B, Hq, D = _decode_inputs(q, k_cache, v_cache, block_tables, seq_lens)
+    _need(out, "out", torch.bfloat16, 3)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 2)
+    rc = lib().pa_decode_splitkv_noalloc(_ptr(out), _ptr(lse), _ptr(q), _ptr(k_cache),
+                                         _ptr(v_cache), cache_desc(k_cache), _ptr(block_tables),
+                                         block_tables.shape[1], _ptr(seq_lens), B, Hq,
+                                         float(scale), num_splits, _ptr(status), _stream(stream))
+    _check("pa_decode_splitkv_noalloc", rc)
