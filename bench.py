@@ -292,13 +292,17 @@ def run_ours(args, world, rank, local):
     touched = w.kv_bytes()
     R = max(1, min(8, math.ceil(2.5 * L2_BYTES / max(touched, 1)) + 1)) if touched < 3 * L2_BYTES else 1
     pools = [(k0, v0)] + [(k0.clone(), v0.clone()) for _ in range(R - 1)]
-    P = args.splits or pa.pa_auto_num_splits(w.B, w.Hkv, w.max_blocks, w.block_size)
+    P = args.splits or pa.pa_auto_num_splits(w.B, w.Hq, w.Hkv, w.D, w.max_blocks, w.block_size)
     out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
-    po = torch.empty((w.B, w.Hq, P, w.D), dtype=torch.float32, device=dev)
-    pl = torch.empty((w.B, w.Hq, P), dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(device=dev)
-    kernel_name = "decode_cc_kernel"
+    forced = os.environ.get("PA_DECODE_KERNEL", "auto")
+    use_tc = forced == "tensor_core" or (forced != "cuda_core" and w.D == 128)
+    kernel_name = "decode_tc_kernel" if use_tc else "decode_cc_kernel"
+
+    ws = torch.zeros(max(1, pa.pa_splitkv_workspace_bytes(w.B, w.Hq, w.D, P)), dtype=torch.uint8,
+                     device=dev)
+    fused = P > 1   # the split decode kernel merges its own partials (one cooperative launch)
 
     def step(r, ev0=None, ev1=None):
         kc, vc = pools[r]
@@ -306,15 +310,14 @@ def run_ours(args, world, rank, local):
         if ev0 is not None:
             ev0.record(stream)
         if P > 1:
-            pa.pa_decode_partial(po, pl, q, kc, vc, bt, sl, w.scale, P, stream=stream)
+            pa.pa_decode_splitkv(out, lse, q, kc, vc, bt, sl, w.scale, num_splits=P, workspace=ws,
+                                 stream=stream)
         else:
             pa.pa_decode(out, lse, q, kc, vc, bt, sl, w.scale, stream=stream)
         if ev1 is not None:
             ev1.record(stream)
-        if P > 1:
-            pa.pa_combine(out, lse, po, pl, stream=stream)
 
-    launches_per_step = 3 if P > 1 else 2
+    launches_per_step = 3 if (P > 1 and not fused) else 2
     # CUDA graphs of S consecutive steps (cycling over the pool replicas), NG
     # copies, each step with its own pair of graph-recorded events around the
     # decode kernel.  Step i of the timed loop is step i % S of graph copy
@@ -386,9 +389,6 @@ def run_ours(args, world, rank, local):
     d_q16, d_kn16, d_vn16 = q.view(torch.int16), kn.view(torch.int16), vn.view(torch.int16)
     h2d = sum(t.numel() * t.element_size() for t in (h_q, h_bt, h_sl, h_kn, h_vn, h_slots))
     d2h = h_out.numel() * 2 + h_lse.numel() * 4
-    ws = torch.empty(max(1, pa.pa_splitkv_workspace_bytes(w.B, w.Hq, w.D, P)), dtype=torch.uint8,
-                     device=dev)
-
     def e2e_step(r):
         kc, vc = pools[r]
         with torch.cuda.stream(stream):
@@ -416,13 +416,17 @@ def run_ours(args, world, rank, local):
     e2e_value = step_bytes * world / (e2e_ms * 1e-3) / 1e12
 
     peak, peak_kind = measured_peak_gbs()
-    kern_bytes = w.kv_bytes() + w.B * w.Hq * w.D * 2 + (w.B * w.Hq * w.D * 2 if P == 1 else 0)
+    # the timed call reads K, V, q and writes the bf16 output (its split partials and
+    # merge are overhead on top); above 64 splits it also covers the combine launch
+    kern_bytes = w.kv_bytes() + 2 * w.B * w.Hq * w.D * 2
     roofline = None
     if kern_ms_avg:
         ach = kern_bytes / (kern_ms_avg * 1e-3) / 1e9
         roofline = {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
                     "frac": round(ach / peak, 4), "traffic": recorded_traffic(args.workload, kernel_name),
-                    "peak_kind": peak_kind, "kernel": kernel_name,
+                    "peak_kind": peak_kind,
+                    "kernel": kernel_name + (" + fused merge" if fused else
+                                             " + combine" if P > 1 else ""),
                     "kernel_us": round(kern_ms_avg * 1e3, 3), "kernel_bytes": kern_bytes}
 
     cpu = None

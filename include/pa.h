@@ -118,9 +118,15 @@ int pa_cache_write(const void *k_new, const void *v_new, const int64_t *slot_map
  * out: device bf16 [B, Hq, D]; lse: device fp32 [B, Hq] or NULL.
  * q: device bf16 [B, Hq, D].  block_tables: device int32 [B, max_blocks_per_seq].
  * seq_lens: device int32 [B].  B == 0 is a no-op.
- * Supported: Hq % Hkv == 0 with Hq / Hkv <= 8, D in {64, 128}, block_size a
- * multiple of 16.  One CTA per (sequence, KV head); use pa_decode_splitkv
- * when B * Hkv is small next to the SM count.
+ * Supported: Hq % Hkv == 0, block_size a multiple of 16, and either D = 128
+ * with G = Hq / Hkv <= 16 or D = 64 with G <= 8.  One CTA per (sequence, KV
+ * head) holds the G query heads, so each KV tile is read once; use
+ * pa_decode_splitkv when B * Hkv is small next to the SM count.
+ * Two kernels implement the step: a tensor-core one (tcgen05, D = 128,
+ * chosen for G >= 4) and a CUDA-core one (all other supported shapes).  The
+ * environment variable PA_DECODE_KERNEL=cuda_core or =tensor_core forces one
+ * of them (read on every call; a shape the forced kernel cannot run is
+ * PA_EUNSUPPORTED).  Both are checked against the same oracle.
  */
 int pa_decode(void *out, float *lse, const void *q, const void *k_cache, const void *v_cache,
               pa_cache_desc cache, const int32_t *block_tables, int32_t max_blocks_per_seq,
@@ -129,13 +135,16 @@ int pa_decode(void *out, float *lse, const void *q, const void *k_cache, const v
 
 /*
  * Split-KV partition count for a decode batch (psmarter benchmark list,
- * "Flash Decoding": splitting lifts SM utilisation at seq 4096).  Picks P so
- * that B * Hkv * P work units fill `sm_count` SMs while each partition keeps
- * at least a few 16-token tiles.  Host-only, pure function of its arguments.
- * Returns P >= 1, or PA_EINVAL.
+ * "Flash Decoding": splitting lifts SM utilisation at seq 4096).  Picks the
+ * largest P for which the B * Hkv * P CTAs fit one wave of the decode kernel
+ * that the group size Hq / Hkv and head_dim D select (2 CTAs per SM for the
+ * CUDA-core kernel, 1 for the tensor-core kernel), capped so that every
+ * partition keeps at least eight 16-token tiles.  Host-only; depends only on
+ * its arguments and the PA_DECODE_KERNEL override described at pa_decode.
+ * Returns P >= 1, or PA_EINVAL / PA_EUNSUPPORTED.
  */
-int pa_choose_num_splits(int32_t B, int32_t Hkv, int32_t max_blocks_per_seq,
-                         int32_t block_size, int32_t sm_count);
+int pa_choose_num_splits(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+                         int32_t max_blocks_per_seq, int32_t block_size, int32_t sm_count);
 
 /*
  * Tokens per partition for P splits: ceil(ceil(max_blocks_per_seq*bs / P) / 16) * 16.
@@ -146,8 +155,10 @@ int pa_partition_tokens(int32_t max_blocks_per_seq, int32_t block_size, int32_t 
 
 /*
  * Bytes of workspace pa_decode_splitkv needs: fp32 partial outputs
- * [B, Hq, P, D] followed by fp32 partial LSEs [B, Hq, P], each region
- * 256-byte aligned.  0 when num_splits <= 1.
+ * [B, Hq, P, D], fp32 partial LSEs [B, Hq, P] and two int32 merge counters
+ * per (sequence, head group) (at most 2 * B * Hq), each region 256-byte
+ * aligned.
+ * 0 when num_splits <= 1.
  */
 size_t pa_splitkv_workspace_bytes(int32_t B, int32_t Hq, int32_t D, int32_t num_splits);
 
@@ -177,12 +188,20 @@ int pa_combine(void *out, float *lse, const float *part_o, const float *part_lse
                int32_t Hq, int32_t num_splits, int32_t D, pa_stream_t stream);
 
 /*
- * Split-KV ("flash decoding") decode attention: pa_decode_partial into the
- * caller's workspace, then pa_combine into out/lse, both on `stream`.
- * num_splits == 0 picks P with pa_choose_num_splits for the current device;
- * P == 1 runs pa_decode directly and needs no workspace.  workspace: device,
- * at least pa_splitkv_workspace_bytes(B, Hq, D, P) bytes, 256-byte aligned,
- * else PA_EWORKSPACE.  Results equal pa_decode's up to fp32 rounding order.
+ * Split-KV ("flash decoding") decode attention: per-partition partials into
+ * the caller's workspace, merged by log-sum-exp into out/lse, all on
+ * `stream`.  When the split grid fits on the GPU at once the decode kernel
+ * is launched cooperatively and merges its own partials (the CTAs of each
+ * sequence and head group meet at a counter, then share the merge), so
+ * there is one launch; otherwise pa_combine runs after it.
+ * num_splits == 0 picks P with pa_auto_num_splits; P == 1 runs pa_decode
+ * directly and needs no workspace.  workspace: device, at least
+ * pa_splitkv_workspace_bytes(B, Hq, D, P) bytes, 256-byte aligned, else
+ * PA_EWORKSPACE.  It must be zero-filled before its first use (cudaMemset):
+ * the merge counters in it start at zero and every completed call leaves
+ * them at zero again, so a workspace can be reused call after call (not by
+ * calls that overlap on the GPU).  Results equal pa_decode's up to fp32
+ * rounding order.
  */
 int pa_decode_splitkv(void *out, float *lse, const void *q, const void *k_cache,
                       const void *v_cache, pa_cache_desc cache, const int32_t *block_tables,
@@ -210,8 +229,9 @@ int pa_decode_splitkv(void *out, float *lse, const void *q, const void *k_cache,
  *     pa_splitkv_workspace_bytes(B, Hq, D, P), exceed the array.
  *   - Every call shares the one array: calls whose kernels overlap on the
  *     GPU (other streams, other host threads) race on it and must be
- *     serialised by the caller.  Nothing in it needs to start at zero; each
- *     call writes every element it reads.
+ *     serialised by the caller.  Each call clears the merge counters it
+ *     uses (cudaMemsetAsync on `stream`, no allocation) and writes every
+ *     partial before reading it.
  */
 int pa_decode_splitkv_noalloc(void *out, float *lse, const void *q, const void *k_cache,
                               const void *v_cache, pa_cache_desc cache,
@@ -220,7 +240,8 @@ int pa_decode_splitkv_noalloc(void *out, float *lse, const void *q, const void *
                               int32_t num_splits, int32_t *status, pa_stream_t stream);
 
 /* P that pa_decode_splitkv uses for num_splits == 0 on the current device (PA_ECUDA on error). */
-int pa_auto_num_splits(int32_t B, int32_t Hkv, int32_t max_blocks_per_seq, int32_t block_size);
+int pa_auto_num_splits(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t max_blocks_per_seq,
+                       int32_t block_size);
 
 /* Static description of a return code. */
 const char *pa_strerror(int code);

@@ -46,10 +46,16 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
+def _extra_flags() -> list[str]:
+    """Extra nvcc flags from PA_EXTRA_NVCC_FLAGS (build-time tuning, e.g. -DPA_TC_NK=2)."""
+    return os.environ.get("PA_EXTRA_NVCC_FLAGS", "").split()
+
+
 def _compile(src: str) -> tuple[str, str]:
     obj = os.path.join(BUILD, os.path.basename(src) + ".o")
     cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
-           "-Xptxas", "-v", "--expt-relaxed-constexpr", "-I", INCLUDE, "-c", src, "-o", obj]
+           "-Xptxas", "-v", "--expt-relaxed-constexpr", *_extra_flags(), "-I", INCLUDE, "-c", src,
+           "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed on {src}:\n{r.stderr}")

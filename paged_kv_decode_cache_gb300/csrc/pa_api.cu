@@ -6,6 +6,8 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "pa_internal.h"
@@ -16,21 +18,102 @@ cudaError_t launch_decode_cc_d64(int G, const CUtensorMap &kmap, const CUtensorM
 cudaError_t launch_decode_cc_d128(int G, const CUtensorMap &kmap, const CUtensorMap &vmap,
                                   const DecodeParams &p, int B, cudaStream_t stream);
 
+cudaError_t launch_decode_tc(int HC, int GP, int G, const CUtensorMap &kmap,
+                             const CUtensorMap &vmap, const DecodeParams &p, int B,
+                             cudaStream_t stream);
+
 cudaError_t launch_decode_cc(int D, int G, const CUtensorMap &kmap, const CUtensorMap &vmap,
                              const DecodeParams &p, int B, cudaStream_t stream) {
     if (D == 128) return launch_decode_cc_d128(G, kmap, vmap, p, B, stream);
     if (D == 64) return launch_decode_cc_d64(G, kmap, vmap, p, B, stream);
     return cudaErrorInvalidValue;
 }
+
 }  // namespace pa
 
 namespace {
 
-constexpr int kMaxGroup = 8;      // query heads per KV head handled by one CTA
+constexpr int kMaxGroupCc = 8;    // query heads per KV head, CUDA-core kernel
+constexpr int kMaxGroupTc = 16;   // query heads per KV head, tensor-core kernel
 constexpr int kMaxGridZ = 65535;  // sequences per launch (gridDim.z)
-constexpr int kCtasPerSm = 2;     // resident decode CTAs per SM (shared-memory bound)
 constexpr int kMinTilesPerSplit = 8;
 constexpr int kMaxSplits = 256;
+constexpr int PA_ETOOLARGE = -100;  // internal: the cooperative grid does not fit at once
+
+
+enum class Kernel { kCudaCore, kTensorCore };
+
+// Resident decode CTAs per SM (shared memory bound): 2 for the CUDA-core
+// kernel (~104 KB each), 1 for the tensor-core kernel (~210 KB).
+int ctas_per_sm(Kernel k) { return k == Kernel::kTensorCore ? 1 : 2; }
+
+int next_pow2(int x) {
+    int p = 1;
+    while (p < x) p <<= 1;
+    return p;
+}
+
+// Shape of the tensor-core kernel for Hkv KV heads of G query heads each: HC
+// KV heads share a CTA (a power of two dividing Hkv, at most 8: a chunk is
+// 128 rows = 128 / HC tokens x HC heads) and every head's query group is
+// padded to GP columns, with HC * GP (the MMA N) between 16 and 64.
+bool tc_shape(int G, int Hkv, int *HC, int *GP) {
+    if (G < 1 || G > kMaxGroupTc || Hkv < 1) return false;
+    int hc = 1;
+    while (hc < 8 && Hkv % (hc * 2) == 0) hc *= 2;
+    int gp = 1;
+    for (;;) {
+        gp = next_pow2(G);
+        if (gp * hc < 16) gp = 16 / hc;
+        if (gp * hc <= 64) break;
+        hc /= 2;
+    }
+    *HC = hc;
+    *GP = gp;
+    return true;
+}
+
+// CTAs per split of the decode grid: one per (sequence, KV head) for the
+// CUDA-core kernel, one per (sequence, group of HC KV heads) for the
+// tensor-core kernel.
+int64_t units_per_split(Kernel k, int B, int G, int Hkv) {
+    if (k == Kernel::kTensorCore) {
+        int hc = 1, gp = 1;
+        tc_shape(G, Hkv, &hc, &gp);
+        return static_cast<int64_t>(B) * (Hkv / hc);
+    }
+    return static_cast<int64_t>(B) * Hkv;
+}
+
+// Which decode kernel runs for a GQA group of G heads of dimension D.  The
+// tensor-core kernel needs D = 128 and G <= 16; the CUDA-core kernel takes
+// D in {64, 128} and G <= 8.  By default the tensor cores take every shape
+// they can.  PA_DECODE_KERNEL=cuda_core or =tensor_core in the environment
+// forces one of them (read on every call; unsupported shapes are rejected).
+int pick_kernel(int G, int D, Kernel *k) {
+    const bool tc_ok = D == 128 && G >= 1 && G <= kMaxGroupTc;
+    const bool cc_ok = (D == 64 || D == 128) && G >= 1 && G <= kMaxGroupCc;
+    const char *env = std::getenv("PA_DECODE_KERNEL");
+    if (env && std::strcmp(env, "cuda_core") == 0) {
+        if (!cc_ok) return PA_EUNSUPPORTED;
+        *k = Kernel::kCudaCore;
+        return PA_OK;
+    }
+    if (env && std::strcmp(env, "tensor_core") == 0) {
+        if (!tc_ok) return PA_EUNSUPPORTED;
+        *k = Kernel::kTensorCore;
+        return PA_OK;
+    }
+    if (tc_ok) {
+        *k = Kernel::kTensorCore;
+        return PA_OK;
+    }
+    if (cc_ok) {
+        *k = Kernel::kCudaCore;
+        return PA_OK;
+    }
+    return PA_EUNSUPPORTED;
+}
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -70,6 +153,28 @@ int make_kv_map(CUtensorMap *map, const void *base, const pa_cache_desc &c) {
     return r == CUDA_SUCCESS ? PA_OK : PA_ECUDA;
 }
 
+// The same pool for the tensor-core kernel: a 4-D view (64 elements, token
+// rows, heads, D/64 sub-rows) whose box is 16 token rows of HC heads of one
+// 64-element sub-row; in shared memory the box is head-major, so a block's
+// rows for all HC heads arrive in one copy.  (The head stride, D * 2 bytes, is
+// smaller than the row stride: the dimensions are deliberately not in
+// increasing stride order.)
+int make_kv_map_heads(CUtensorMap *map, const void *base, const pa_cache_desc &c, int HC) {
+    auto enc = encode_fn();
+    if (!enc) return PA_ECUDA;
+    const cuuint64_t dims[4] = {64u, static_cast<cuuint64_t>(c.num_blocks) * c.block_size,
+                                static_cast<cuuint64_t>(c.num_kv_heads),
+                                static_cast<cuuint64_t>(c.head_dim / 64)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(c.num_kv_heads) * c.head_dim * 2,
+                                   static_cast<cuuint64_t>(c.head_dim) * 2, 128u};
+    const cuuint32_t box[4] = {64u, 16u, static_cast<cuuint32_t>(HC), 1u};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ECUDA;
+}
+
 int check_cache_desc(const pa_cache_desc &c) {
     if (c.num_blocks <= 0 || c.block_size <= 0 || c.num_kv_heads <= 0 || c.head_dim <= 0)
         return PA_EINVAL;
@@ -88,7 +193,9 @@ int check_decode_args(const void *q, const void *k_cache, const void *v_cache,
     int rc = check_cache_desc(c);
     if (rc) return rc;
     if (Hq <= 0 || Hq % c.num_kv_heads != 0) return PA_EINVAL;
-    if (Hq / c.num_kv_heads > kMaxGroup) return PA_EUNSUPPORTED;
+    Kernel k;
+    rc = pick_kernel(Hq / c.num_kv_heads, c.head_dim, &k);
+    if (rc) return rc;
     if (c.num_kv_heads > 65535) return PA_EUNSUPPORTED;
     if (B > kMaxGridZ) return PA_EUNSUPPORTED;
     if (max_blocks_per_seq <= 0) return PA_EINVAL;
@@ -136,11 +243,10 @@ int run_decode(bool split, void *out, float *lse, float *part_o, float *part_lse
                const void *k_cache, const void *v_cache, const pa_cache_desc &c,
                const int32_t *block_tables, int32_t max_blocks, const int32_t *seq_lens,
                int32_t B, int32_t Hq, float scale, int32_t P, int32_t *status,
-               cudaStream_t stream) {
-    CUtensorMap kmap, vmap;
-    int rc = make_kv_map(&kmap, k_cache, c);
-    if (rc) return rc;
-    rc = make_kv_map(&vmap, v_cache, c);
+               cudaStream_t stream, int32_t *counters = nullptr) {
+    const int G = Hq / c.num_kv_heads;
+    Kernel k;
+    int rc = pick_kernel(G, c.head_dim, &k);
     if (rc) return rc;
     pa::DecodeParams p = base_params(q, c, block_tables, max_blocks, seq_lens, Hq, scale, status);
     p.out = out;
@@ -150,8 +256,23 @@ int run_decode(bool split, void *out, float *lse, float *part_o, float *part_lse
     p.split = split ? 1 : 0;
     p.num_splits = P;
     p.chunk = pa_partition_tokens(max_blocks, c.block_size, P);
-    const int G = Hq / c.num_kv_heads;
-    cudaError_t e = pa::launch_decode_cc(c.head_dim, G, kmap, vmap, p, B, stream);
+    p.counters = counters;
+    CUtensorMap kmap, vmap;
+    cudaError_t e;
+    if (k == Kernel::kTensorCore) {
+        int HC = 1, GP = 1;
+        if (!tc_shape(G, c.num_kv_heads, &HC, &GP)) return PA_EUNSUPPORTED;
+        rc = make_kv_map_heads(&kmap, k_cache, c, HC);
+        if (!rc) rc = make_kv_map_heads(&vmap, v_cache, c, HC);
+        if (rc) return rc;
+        e = pa::launch_decode_tc(HC, GP, G, kmap, vmap, p, B, stream);
+    } else {
+        rc = make_kv_map(&kmap, k_cache, c);
+        if (!rc) rc = make_kv_map(&vmap, v_cache, c);
+        if (rc) return rc;
+        e = pa::launch_decode_cc(c.head_dim, G, kmap, vmap, p, B, stream);
+    }
+    if (e == cudaErrorCooperativeLaunchTooLarge && counters) return PA_ETOOLARGE;
     return e == cudaSuccess ? PA_OK : PA_ECUDA;
 }
 
@@ -210,13 +331,17 @@ int pa_partition_tokens(int32_t max_blocks_per_seq, int32_t block_size, int32_t 
     return static_cast<int>(round_up(per, 16));
 }
 
-int pa_choose_num_splits(int32_t B, int32_t Hkv, int32_t max_blocks_per_seq, int32_t block_size,
-                         int32_t sm_count) {
-    if (B < 0 || Hkv <= 0 || max_blocks_per_seq <= 0 || block_size <= 0 || sm_count <= 0)
+int pa_choose_num_splits(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+                         int32_t max_blocks_per_seq, int32_t block_size, int32_t sm_count) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || max_blocks_per_seq <= 0 ||
+        block_size <= 0 || sm_count <= 0)
         return PA_EINVAL;
     if (B == 0) return 1;
-    const int64_t units = static_cast<int64_t>(B) * Hkv;
-    const int64_t slots = static_cast<int64_t>(sm_count) * kCtasPerSm;
+    Kernel k;
+    int rc = pick_kernel(Hq / Hkv, D, &k);
+    if (rc) return rc;
+    const int64_t units = units_per_split(k, B, Hq / Hkv, Hkv);
+    const int64_t slots = static_cast<int64_t>(sm_count) * ctas_per_sm(k);
     int64_t P = slots / units;  // largest P whose grid still fits one wave
     const int64_t lmax = static_cast<int64_t>(max_blocks_per_seq) * block_size;
     const int64_t tiles = (lmax + 15) / 16;
@@ -230,16 +355,18 @@ int pa_choose_num_splits(int32_t B, int32_t Hkv, int32_t max_blocks_per_seq, int
     return static_cast<int>(P);
 }
 
-int pa_auto_num_splits(int32_t B, int32_t Hkv, int32_t max_blocks_per_seq, int32_t block_size) {
+int pa_auto_num_splits(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t max_blocks_per_seq,
+                       int32_t block_size) {
     const int sms = sm_count_current();
     if (sms <= 0) return PA_ECUDA;
-    return pa_choose_num_splits(B, Hkv, max_blocks_per_seq, block_size, sms);
+    return pa_choose_num_splits(B, Hq, Hkv, D, max_blocks_per_seq, block_size, sms);
 }
 
 size_t pa_splitkv_workspace_bytes(int32_t B, int32_t Hq, int32_t D, int32_t num_splits) {
     if (B <= 0 || Hq <= 0 || D <= 0 || num_splits <= 1) return 0;
     const int64_t rows = static_cast<int64_t>(B) * Hq * num_splits;
-    return static_cast<size_t>(round_up(rows * D * 4, 256) + round_up(rows * 4, 256));
+    return static_cast<size_t>(round_up(rows * D * 4, 256) + round_up(rows * 4, 256) +
+                               round_up(static_cast<int64_t>(B) * Hq * 8, 256));
 }
 
 int pa_decode_partial(float *part_o, float *part_lse, const void *q, const void *k_cache,
@@ -286,8 +413,8 @@ int pa_decode_splitkv(void *out, float *lse, const void *q, const void *k_cache,
     if (B == 0) return PA_OK;
     int P = num_splits;
     if (P == 0) {
-        P = pa_auto_num_splits(cache.num_kv_heads > 0 ? B : 0, cache.num_kv_heads,
-                               max_blocks_per_seq, cache.block_size);
+        P = pa_auto_num_splits(B, Hq, cache.num_kv_heads, cache.head_dim, max_blocks_per_seq,
+                               cache.block_size);
         if (P < 0) return P;
     }
     if (P > 65535) return PA_EUNSUPPORTED;
@@ -298,9 +425,16 @@ int pa_decode_splitkv(void *out, float *lse, const void *q, const void *k_cache,
     const size_t need = pa_splitkv_workspace_bytes(B, Hq, cache.head_dim, P);
     if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return PA_EWORKSPACE;
     const int64_t rows = static_cast<int64_t>(B) * Hq * P;
-    float *part_o = static_cast<float *>(workspace);
-    float *part_lse = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
-                                                round_up(rows * cache.head_dim * 4, 256));
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    float *part_o = reinterpret_cast<float *>(ws);
+    float *part_lse = reinterpret_cast<float *>(ws + round_up(rows * cache.head_dim * 4, 256));
+    int32_t *counters = reinterpret_cast<int32_t *>(ws + round_up(rows * cache.head_dim * 4, 256) +
+                                                    round_up(rows * 4, 256));
+    // One cooperative launch that merges its own partials when the whole grid
+    // fits on the GPU at once; otherwise partials, then pa_combine.
+    rc = run_decode(true, out, lse, part_o, part_lse, q, k_cache, v_cache, cache, block_tables,
+                    max_blocks_per_seq, seq_lens, B, Hq, scale, P, status, stream, counters);
+    if (rc != PA_ETOOLARGE) return rc;
     rc = run_decode(true, nullptr, nullptr, part_o, part_lse, q, k_cache, v_cache, cache,
                     block_tables, max_blocks_per_seq, seq_lens, B, Hq, scale, P, status, stream);
     if (rc) return rc;

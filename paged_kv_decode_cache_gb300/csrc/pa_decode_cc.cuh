@@ -28,6 +28,7 @@
 
 #include "pa_device.cuh"
 #include "pa_internal.h"
+#include "pa_split_merge.cuh"
 
 namespace pa {
 
@@ -47,7 +48,8 @@ struct CcCfg {
     static constexpr int kQOff = kRegion0;
     static constexpr int kPOff = kQOff + kQBytes;
     static constexpr int kBarOff = (kPOff + kPBytes + 7) / 8 * 8;
-    static constexpr int kSmemBytes = kBarOff + NW * NST * 8 + 1024;  // + alignment slack
+    static constexpr int kTicketOff = kBarOff + NW * NST * 8;
+    static constexpr int kSmemBytes = kTicketOff + 16 + 1024;  // + alignment slack
     static constexpr int kDPV = D / 32;                         // output dims per lane
 };
 
@@ -110,9 +112,7 @@ decode_cc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         const int phys = bt[tok0 / bs];
         if (phys < 0 || phys >= p.num_blocks) {
             set_status(p.status, PA_STATUS_BAD_BLOCK);
-            asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(
-                             smem_u32(&wbars[s]))
-                         : "memory");
+            mbar_arrive(&wbars[s]);
             return;
         }
         const int row0 = phys * bs + tok0 % bs;
@@ -326,6 +326,10 @@ decode_cc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             if (d == 0 && p.lse) p.lse[row] = lse_nat;
         }
     }
+    if (p.split)
+        merge_split_group<D>(p, b * gridDim.y + g, part, static_cast<int64_t>(b) * p.num_q_heads + hq0,
+                             G, reinterpret_cast<int *>(smem + C::kTicketOff), tid, NW * 32,
+                             [] { __syncthreads(); });
 }
 
 // Opt a kernel into more than 48 KB of dynamic shared memory, once per
@@ -353,9 +357,8 @@ cudaError_t launch_cc_instance(const CUtensorMap &kmap, const CUtensorMap &vmap,
     static std::atomic<uint64_t> smem_attr_done{0};
     cudaError_t e = ensure_smem_attr(smem_attr_done, kern, C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    dim3 grid(p.num_splits, p.num_kv_heads, B);
-    kern<<<grid, NW * 32, C::kSmemBytes, stream>>>(kmap, vmap, p);
-    return cudaGetLastError();
+    return launch_maybe_cooperative(kern, dim3(p.num_splits, p.num_kv_heads, B), NW * 32,
+                                    C::kSmemBytes, stream, p.counters != nullptr, kmap, vmap, p);
 }
 
 }  // namespace pa

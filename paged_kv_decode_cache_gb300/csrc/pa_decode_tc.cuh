@@ -1,0 +1,485 @@
+// Paged decode attention on the 5th-generation tensor cores (tcgen05), for
+// head_dim 128.
+//
+// One CTA per (partition p, group of HC KV heads, sequence b) streams its
+// token range in chunks of T = 128 / HC tokens, loading whole paged blocks:
+// one TMA box per 16-token tile and 64-element half-row brings that tile for
+// all HC heads (16 rows x HC heads x 128 bytes, head-major in shared memory),
+// so the HBM reads of a block are contiguous bursts.  A chunk is therefore
+// 128 rows m = (tile, head, row) of K (and of V), and both contractions are
+// dense 128-row tiles:
+//
+//   QK:  S[128 m, N] = K_chunk[128 m, 128 d] . Q^T[128 d, N]
+//        N = HC x GP columns n = (head', q): query head q of KV head head',
+//        zero-padded to GP per head.  A = the K chunk as TMA lands it
+//        (K-major, 128-byte swizzle), B = the packed queries.  Only the
+//        columns with head' = head(m) are used.
+//   PV:  O^T[128 d, N] += V_chunk^T[128 d, 128 m] . P^T[128 m, N]
+//        A = the V chunk read transposed (MN-major descriptor, no copy),
+//        B = P^T, block-diagonal by head: row m only has its own head's GP
+//        columns, the rest stay zero, so O^T[d, (h, q)] sums over head h's
+//        tokens only.
+//
+// S (NBS buffers) and O^T live in TMEM (N columns each): lane = row m for S
+// and lane = head dim d for O.  The CTA is warp-specialised:
+//   warps 0-3 (softmax): thread t owns row m = t of each chunk and output dim
+//        d = t.  It loads its S row (tcgen05.ld), keeps its head's GP scores,
+//        forms p = exp2(s - m_ref) against a per-(head, q) reference max,
+//        writes p into P^T and arrives on the chunk's "P ready" barrier.
+//        m_ref only moves when some score exceeds it by more than 2^8 (a
+//        CTA-wide vote, one barrier per chunk); then the chunk max is
+//        reduced, O^T is rescaled in TMEM and the row sums with it.  Row sums
+//        stay per thread and are reduced once at the end.
+//   warp 4 (QK issuer) and warp 7 (PV issuer): one thread each issues its
+//        MMAs as soon as their inputs are ready (QK: K landed and the S buffer
+//        released by the softmax threads; PV: P^T written and V landed) and
+//        commits to the barriers that publish S, release the K stage, release
+//        the P buffer and the V stage.
+//   warps 5, 6 (TMA): stream K and V through separate rings (NK and NV
+//        stages of 32 KB), looking every tile up in the block table; tiles
+//        past the range or with a bad block id are not loaded and their rows
+//        are masked (and their V rows zeroed).
+// Softmax threads decide row validity from the block table themselves, so
+// they never depend on a stage after its MMA has released it.  Every mbarrier
+// wait is bounded and honours a CTA-wide abort flag; the softmax warps agree
+// on an abort at their per-chunk vote.
+#pragma once
+
+#include <atomic>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+#include "pa_split_merge.cuh"
+#include "pa_tcgen05.cuh"
+
+namespace pa {
+
+constexpr int kTcRows = 128;           // rows m per chunk (M of QK)
+constexpr int kTcThreads = 256;        // 4 softmax warps + 2 MMA warps + 2 TMA warps
+constexpr int kTcQkWarp = 4;
+constexpr int kTcTmaKWarp = 5;
+constexpr int kTcTmaVWarp = 6;
+constexpr int kTcPvWarp = 7;
+constexpr int kTcNBS = 4;              // S buffers in TMEM
+constexpr int kTcNBP = 2;              // P^T buffers in shared memory
+constexpr float kTcLazyTau = 8.0f;     // log2 headroom before a reference max moves
+
+template <int HC, int GP>
+struct TcCfg {
+    static constexpr int kN = HC * GP;                          // MMA N
+    static_assert(kN % 16 == 0 && kN >= 16 && kN <= 64, "MMA N");
+    static constexpr int kT = kTcRows / HC;                     // tokens per chunk
+    static constexpr int kTiles = kT / kTile;                   // 16-token tiles per chunk
+    static_assert(kTiles >= 1 && kTiles * HC * kTile == kTcRows, "tiles");
+    static constexpr int kNK = kN <= 32 ? 3 : 2;                // K stages
+    static constexpr int kNV = 3;                               // V stages
+    static constexpr int kSubTile = kTcRows * kSubBytes;        // [128 m][64 d] bf16 = 16 KB
+    static constexpr int kTileBytes = 2 * kSubTile;             // K (or V) of one chunk: 32 KB
+    static constexpr int kBoxBytes = HC * kTile * kSubBytes;    // one TMA box: HC heads x 16 rows
+    static constexpr int kVOff = kNK * kTileBytes;
+    static constexpr int kQOff = (kNK + kNV) * kTileBytes;
+    static constexpr int kQBytes = 2 * kN * kSubBytes;          // [N][64] x 2 halves
+    static constexpr int kPOff = kQOff + kQBytes;
+    static constexpr int kPBytes = 2 * kN * kSubBytes;          // P^T: 2 atoms of [N][64 m]
+    static constexpr int kRedOff = kPOff + kTcNBP * kPBytes;
+    // red[128 rows][GP], col[N] (per-column result), m_ref[N], alpha[N], abort flag, TMEM slot
+    static constexpr int kRedBytes = (kTcRows * GP + 3 * kN) * 4 + 16;
+    static constexpr int kBarOff = (kRedOff + kRedBytes + 7) / 8 * 8;
+    static constexpr int kNumBars = 2 * kNK + 2 * kNV + 2 * kTcNBS + 2 * kTcNBP;
+    static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 1024;
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+    static constexpr uint32_t kTmemCols = (kTcNBS + 1) * kN <= 128 ? 128u
+                                          : (kTcNBS + 1) * kN <= 256 ? 256u : 512u;
+    static constexpr int kColO = kTcNBS * kN;
+};
+
+// Max (or sum) over the rows of column n's head of a [128 rows][GP] array:
+// row m = (tile * HC + head) * 16 + r holds the GP values of its own head.
+template <int HC, int GP, bool kMax>
+__device__ __forceinline__ float column_reduce(const float *red, int n) {
+    const int hh = n / GP, q = n % GP;
+    float acc = kMax ? -INFINITY : 0.f;
+#pragma unroll 1
+    for (int t = 0; t < kTcRows / (kTile * HC); ++t) {
+        const float *base = red + ((t * HC + hh) * kTile) * GP + q;
+#pragma unroll
+        for (int r = 0; r < kTile; ++r) acc = kMax ? fmaxf(acc, base[r * GP]) : acc + base[r * GP];
+    }
+    return acc;
+}
+
+template <int HC, int GP>
+__global__ void __launch_bounds__(kTcThreads, 1)
+decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                 const DecodeParams p, int G) {
+    constexpr int D = 128;
+    using C = TcCfg<HC, GP>;
+    constexpr int N = C::kN, NK = C::kNK, NV = C::kNV;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~uintptr_t(1023));
+    uint8_t *kring = smem;
+    uint8_t *vring = smem + C::kVOff;
+    uint8_t *qs = smem + C::kQOff;
+    uint8_t *ps = smem + C::kPOff;
+    float *red = reinterpret_cast<float *>(smem + C::kRedOff);      // [128 rows][GP] scratch
+    float *col = red + kTcRows * GP;                                // [N] per-column result
+    float *m_ref = col + N;                                         // [N] reference max
+    float *alpha_s = m_ref + N;                                     // [N] rescale factors
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(alpha_s + N);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(alpha_s + N + 1);
+    int *ticket = reinterpret_cast<int *>(alpha_s + N + 2);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
+    uint64_t *kfull = bars, *kempty = bars + NK, *vfull = bars + 2 * NK, *vempty = vfull + NV;
+    uint64_t *sdone = vempty + NV, *sfree = sdone + kTcNBS, *pready = sfree + kTcNBS;
+    uint64_t *pfree = pready + kTcNBP;
+
+    const int part = blockIdx.x, g0 = blockIdx.y * HC, b = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int bs = p.block_size;
+
+    int L = p.seq_lens[b];
+    const int lmax = p.max_blocks * bs;
+    if (L < 0 || L > lmax) {
+        if (tid == 0 && part == 0 && g0 == 0) set_status(p.status, PA_STATUS_BAD_SEQLEN);
+        L = L < 0 ? 0 : lmax;
+    }
+    const int t_begin = part * p.chunk;
+    const int t_end = min(t_begin + p.chunk, L);
+    const int nch = t_end > t_begin ? (t_end - t_begin + C::kT - 1) / C::kT : 0;
+    const int64_t row0 = static_cast<int64_t>(b) * p.num_q_heads + static_cast<int64_t>(g0) * G;
+
+    if (nch == 0) {  // empty range: zero output, lse = -inf
+        for (int i = tid; i < HC * G * D; i += kTcThreads) {
+            const int64_t r = row0 + i / D;
+            const int d = i % D;
+            if (p.split) p.part_o[(r * p.num_splits + part) * D + d] = 0.f;
+            else static_cast<__nv_bfloat16 *>(p.out)[r * D + d] = __float2bfloat16_rn(0.f);
+        }
+        if (tid < HC * G) {
+            if (p.split) p.part_lse[(row0 + tid) * p.num_splits + part] = -INFINITY;
+            else if (p.lse) p.lse[row0 + tid] = -INFINITY;
+        }
+        if (p.split)
+            merge_split_group<D>(p, b * gridDim.y + blockIdx.y, part, row0, HC * G, ticket, tid,
+                                 kTcThreads, [] { __syncthreads(); });
+        return;
+    }
+    const int32_t *bt = p.block_tables + static_cast<int64_t>(b) * p.max_blocks;
+
+    // ---- set-up: TMEM, barriers, the Q operand, zeroed P^T buffers ---------------------
+    if (warp == 0) tc5::tmem_alloc(tmem_slot, C::kTmemCols);
+    if (tid == 0) {
+        // every barrier completes on one arrival except "S free" and "P ready",
+        // which all 128 softmax threads arrive on
+        for (int i = 0; i < C::kNumBars; ++i)
+            mbar_init(&bars[i], (&bars[i] >= sfree && &bars[i] < pready + kTcNBP) ? 128u : 1u);
+        *abort_flag = 0;
+        prefetch_tensormap(&kmap);
+        prefetch_tensormap(&vmap);
+    }
+    if (tid < N) m_ref[tid] = -INFINITY;
+    {
+        const uint16_t *qg = p.q + row0 * D;
+        for (int i = tid; i < N * (D / 8); i += kTcThreads) {  // row n = (head', q), 16-byte chunk c
+            const int n = i / (D / 8), c = i % (D / 8);
+            const int hh = n / GP, q = n % GP;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (q < G) v = *reinterpret_cast<const uint4 *>(qg + (hh * G + q) * D + c * 8);
+            *reinterpret_cast<uint4 *>(qs + (c >> 3) * (N * kSubBytes) + swz128(n, c & 7)) = v;
+        }
+        for (int i = tid; i < kTcNBP * C::kPBytes / 16; i += kTcThreads)
+            reinterpret_cast<uint4 *>(ps)[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async_smem();
+    fence_barrier_init();
+    tc5::fence_before_sync();
+    __syncthreads();
+    tc5::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    auto wait_or_abort = [&](uint64_t *bar, uint32_t parity) -> bool {
+        for (uint32_t i = 0; i < kWaitLimit; ++i) {
+            if (mbar_try_wait(bar, parity)) return true;
+            if (*abort_flag) return false;
+        }
+        *abort_flag = 1;
+        set_status(p.status, PA_STATUS_TIMEOUT);
+        return false;
+    };
+
+    if (warp == kTcTmaKWarp || warp == kTcTmaVWarp) {
+        // ================= TMA producers: K ring (warp 5), V ring (warp 6) =================
+        const bool is_v = warp == kTcTmaVWarp;
+        const int nst = is_v ? NV : NK;
+        uint8_t *ring = is_v ? vring : kring;
+        uint64_t *full = is_v ? vfull : kfull;
+        uint64_t *empty = is_v ? vempty : kempty;
+        const CUtensorMap *map = is_v ? &vmap : &kmap;
+        const uint64_t policy = l2_evict_first_policy();
+        const int tile = lane >> 1, sub = lane & 1;   // lanes < 2 x tiles carry boxes
+        const bool carrier = lane < 2 * C::kTiles;
+        auto lookup = [&](int c) -> int {  // block of this lane's tile in chunk c (-1: none)
+            const int tok0 = t_begin + c * C::kT + tile * kTile;
+            return (carrier && tok0 < t_end) ? bt[tok0 / bs] : -1;
+        };
+        int phys_next = lookup(0);
+        int issued = 0;
+        for (int c = 0; c < nch; ++c) {
+            const int s = c % nst;
+            const int phys = phys_next;
+            if (c + 1 < nch) phys_next = lookup(c + 1);  // in flight while the stage drains
+            if (c >= nst) {
+                const bool ok = wait_or_abort(&empty[s], ((c / nst) - 1) & 1);
+                if (!__all_sync(0xffffffffu, ok)) break;
+            }
+            const int tok0 = t_begin + c * C::kT + tile * kTile;
+            bool valid = false;
+            if (carrier && tok0 < t_end) {
+                if (phys >= 0 && phys < p.num_blocks) valid = true;
+                else if (!is_v && sub == 0) set_status(p.status, PA_STATUS_BAD_BLOCK);
+            }
+            const uint32_t vm = __ballot_sync(0xffffffffu, valid);
+            if (lane == 0) mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(__popc(vm)) * C::kBoxBytes);
+            __syncwarp();
+            if (valid)
+                tma_load_4d(ring + s * C::kTileBytes + sub * C::kSubTile + tile * C::kBoxBytes, map, 0,
+                            phys * bs + tok0 % bs, g0, sub, &full[s], policy);
+            issued = c + 1;
+        }
+        if (*abort_flag && lane == 0)  // let this CTA's copies land before it leaves
+            for (int c = max(0, issued - nst); c < issued; ++c)
+                mbar_wait_bounded(&full[c % nst], (c / nst) & 1);
+    } else if (warp == kTcQkWarp) {
+        // ================= QK issuer =================
+        if (lane == 0) {
+            constexpr uint32_t kIdQK = tc5::idesc_bf16_f32(kTcRows, N, false, false);
+            int done = 0;
+            for (int c = 0; c < nch; ++c) {
+                // S buffer c % NBS is free once softmax c - NBS has read it; K c has landed
+                if (c >= kTcNBS && !wait_or_abort(&sfree[c % kTcNBS], ((c / kTcNBS) - 1) & 1)) break;
+                if (!wait_or_abort(&kfull[c % NK], (c / NK) & 1)) break;
+                tc5::fence_after_sync();
+                const uint8_t *kt = kring + (c % NK) * C::kTileBytes;
+                const uint32_t dcol = tmem + (c % kTcNBS) * N;
+#pragma unroll
+                for (int j = 0; j < D / 16; ++j) {
+                    const int half = j >> 2, off = (j & 3) * 32;
+                    tc5::mma_bf16(dcol, tc5::sw128_desc(kt + half * C::kSubTile + off, 16, 1024),
+                                  tc5::sw128_desc(qs + half * (N * kSubBytes) + off, 16, 1024),
+                                  kIdQK, j > 0);
+                }
+                tc5::commit(&sdone[c % kTcNBS]);
+                tc5::commit(&kempty[c % NK]);
+                done = c + 1;
+            }
+            if (*abort_flag && done > 0)  // let issued MMAs finish before TMEM is freed
+                mbar_wait_bounded(&sdone[(done - 1) % kTcNBS], ((done - 1) / kTcNBS) & 1);
+        }
+    } else if (warp == kTcPvWarp) {
+        // ================= PV issuer =================
+        if (lane == 0) {
+            constexpr uint32_t kIdPV = tc5::idesc_bf16_f32(kTcRows, N, true, false);
+            int done = 0;
+            for (int c = 0; c < nch; ++c) {
+                if (!wait_or_abort(&pready[c % kTcNBP], (c / kTcNBP) & 1)) break;
+                if (!wait_or_abort(&vfull[c % NV], (c / NV) & 1)) break;
+                tc5::fence_after_sync();
+                const uint8_t *vt = vring + (c % NV) * C::kTileBytes;
+                const uint8_t *pt = ps + (c % kTcNBP) * C::kPBytes;
+#pragma unroll
+                for (int j = 0; j < kTcRows / 16; ++j) {
+                    tc5::mma_bf16(tmem + C::kColO,
+                                  tc5::sw128_desc(vt + j * 16 * kSubBytes, C::kSubTile, 1024),
+                                  tc5::sw128_desc(pt + (j >> 2) * (N * kSubBytes) + (j & 3) * 32, 16, 1024),
+                                  kIdPV, c > 0 || j > 0);
+                }
+                tc5::commit(&pfree[c % kTcNBP]);
+                tc5::commit(&vempty[c % NV]);
+                done = c + 1;
+            }
+            if (*abort_flag && done > 0)
+                mbar_wait_bounded(&pfree[(done - 1) % kTcNBP], ((done - 1) / kTcNBP) & 1);
+        }
+    } else {
+        // ================= softmax warps: thread = row m of a chunk, and output dim d =================
+        const int my_head = (tid >> 4) % HC;                // head of row m = tid
+        const int my_tok = (tid / (kTile * HC)) * kTile + (tid & 15);  // token offset within a chunk
+        float l_thr[GP];
+#pragma unroll
+        for (int q = 0; q < GP; ++q) l_thr[q] = 0.f;
+        const float sl2 = p.scale_log2;
+        bool dead = false;
+        auto lookup = [&](int c) -> int {
+            const int tok = t_begin + c * C::kT + my_tok;
+            return tok < t_end ? bt[tok / bs] : -1;
+        };
+        int phys_next = lookup(0);
+        for (int c = 0; c < nch; ++c) {
+            const int sbuf = c % kTcNBS, pbuf = c % kTcNBP;
+            const int phys = phys_next;
+            if (c + 1 < nch) phys_next = lookup(c + 1);  // one chunk ahead
+            const bool in_pool = phys >= 0 && phys < p.num_blocks;
+            bool ok = wait_or_abort(&sdone[sbuf], (c / kTcNBS) & 1);
+            ok = __all_sync(0xffffffffu, ok);
+            float sv[N];
+            if (ok) {
+                tc5::fence_after_sync();
+#pragma unroll
+                for (int k = 0; k < N / 16; ++k)
+                    tc5::ld_32x32b_x16(tc5::taddr(tmem, 32 * warp, sbuf * N + 16 * k),
+                                       *reinterpret_cast<float(*)[16]>(&sv[16 * k]));
+            }
+            tc5::fence_before_sync();
+            mbar_arrive(&sfree[sbuf]);  // S buffer read: QK c + NBS may overwrite it
+            const bool valid = ok && in_pool;
+            float sc[GP], mr[GP];
+            bool over = false;
+#pragma unroll
+            for (int q = 0; q < GP; ++q) {
+                float v = sv[q];
+#pragma unroll
+                for (int hh = 1; hh < HC; ++hh)
+                    if (my_head == hh) v = sv[hh * GP + q];
+                sc[q] = (valid && q < G) ? v * sl2 : -INFINITY;
+                mr[q] = m_ref[my_head * GP + q];
+                over |= sc[q] > mr[q] + kTcLazyTau;
+            }
+            // one vote per chunk: does any reference max have to move (or is the CTA aborting)?
+            const bool bad = !ok || *abort_flag != 0;
+            if (named_sync_or(1, 128, over || bad)) {
+                if (named_sync_or(1, 128, bad)) {
+                    dead = true;
+                    break;
+                }
+                // chunk max of every column (head, q) over that head's rows, via shared memory
+#pragma unroll
+                for (int q = 0; q < GP; ++q) red[tid * GP + q] = sc[q];
+                named_sync(1, 128);
+                if (tid < N) {
+                    const float cm = column_reduce<HC, GP, true>(red, tid);
+                    const float old = m_ref[tid];
+                    const float mn = fmaxf(old, cm);
+                    alpha_s[tid] = (mn == -INFINITY) ? 1.f : fast_exp2(old - mn);
+                    m_ref[tid] = mn;
+                }
+                named_sync(1, 128);
+#pragma unroll
+                for (int q = 0; q < GP; ++q) {
+                    mr[q] = m_ref[my_head * GP + q];
+                    l_thr[q] *= alpha_s[my_head * GP + q];
+                }
+                if (c >= 1) {  // O^T (all chunks so far) is rescaled once PV c-1 is done
+                    bool ok3 = wait_or_abort(&pfree[(c - 1) % kTcNBP], ((c - 1) / kTcNBP) & 1);
+                    if (__all_sync(0xffffffffu, ok3)) {
+                        tc5::fence_after_sync();
+#pragma unroll 1
+                        for (int k = 0; k < N / 16; ++k) {
+                            float ov[16];
+                            const uint32_t ta = tc5::taddr(tmem, 32 * warp, C::kColO + 16 * k);
+                            tc5::ld_32x32b_x16(ta, ov);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) ov[i] *= alpha_s[16 * k + i];
+                            tc5::st_32x32b_x16(ta, ov);
+                        }
+                    }
+                }
+                named_sync(1, 128);  // alpha_s / red read by all before any later reuse
+            }
+            __nv_bfloat16 pb[GP];
+#pragma unroll
+            for (int q = 0; q < GP; ++q) {
+                pb[q] = __float2bfloat16_rn(valid && q < G ? fast_exp2(sc[q] - mr[q]) : 0.f);
+                l_thr[q] += __bfloat162float(pb[q]);
+            }
+            if (c >= kTcNBP) wait_or_abort(&pfree[pbuf], ((c / kTcNBP) - 1) & 1);  // PV c - NBP done
+            {
+                // P^T[n][m] for this row's own head block; the other heads' columns stay zero
+                uint8_t *pt = ps + pbuf * C::kPBytes + (tid >> 6) * (N * kSubBytes);
+                const int tt = tid & 63;
+#pragma unroll
+                for (int q = 0; q < GP; ++q) {
+                    const int n = my_head * GP + q;
+                    *reinterpret_cast<__nv_bfloat16 *>(pt + n * kSubBytes + (((tt >> 3) ^ (n & 7)) << 4) +
+                                                       (tt & 7) * 2) = pb[q];
+                }
+            }
+            // an invalid row zeroes its V row, so 0 * (stale or NaN) never reaches O^T
+            if (!valid && wait_or_abort(&vfull[c % NV], (c / NV) & 1)) {
+                uint8_t *vrow = vring + (c % NV) * C::kTileBytes + tid * kSubBytes;
+#pragma unroll
+                for (int sub = 0; sub < 2; ++sub)
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        *reinterpret_cast<uint4 *>(vrow + sub * C::kSubTile + k * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+            tc5::fence_before_sync();
+            mbar_arrive(&pready[pbuf]);
+        }
+
+        // ---- epilogue: row sums, O^T, normalise, store ----------------------------------
+        bool okf = !dead && wait_or_abort(&pfree[(nch - 1) % kTcNBP], ((nch - 1) / kTcNBP) & 1);
+        okf = named_sync_or(1, 128, !okf) ? false : true;
+        // row sums of every column (head, q) over that head's rows, via shared memory
+#pragma unroll
+        for (int q = 0; q < GP; ++q) red[tid * GP + q] = l_thr[q];
+        named_sync(1, 128);
+        if (tid < N) col[tid] = column_reduce<HC, GP, false>(red, tid);
+        named_sync(1, 128);  // col[] complete before it is read
+        if (okf) {
+            tc5::fence_after_sync();
+            // O^T row d = tid, 16 columns at a time, normalised and stored
+#pragma unroll 1
+            for (int k = 0; k < N / 16; ++k) {
+                float ov[16];
+                tc5::ld_32x32b_x16(tc5::taddr(tmem, 32 * warp, C::kColO + 16 * k), ov);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int n = 16 * k + i, hh = n / GP, q = n % GP;
+                    if (q >= G) continue;
+                    const float lsum = col[n];
+                    const float o = ov[i] / lsum;
+                    const int64_t r = row0 + hh * G + q;
+                    if (p.split) p.part_o[(r * p.num_splits + part) * D + tid] = o;
+                    else static_cast<__nv_bfloat16 *>(p.out)[r * D + tid] = __float2bfloat16_rn(o);
+                }
+            }
+            if (tid < N && tid % GP < G) {
+                const int n = tid, hh = n / GP, q = n % GP;
+                const float lse = (m_ref[n] + log2f(col[n])) * 0.69314718055994531f;
+                const int64_t r = row0 + hh * G + q;
+                if (p.split) p.part_lse[r * p.num_splits + part] = lse;
+                else if (p.lse) p.lse[r] = lse;
+            }
+        }
+        if (p.split)
+            merge_split_group<D>(p, b * gridDim.y + blockIdx.y, part, row0, HC * G, ticket, tid,
+                                 128, [] { named_sync(1, 128); });
+    }
+    tc5::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc5::tmem_free(tmem, C::kTmemCols);
+}
+
+template <int HC, int GP>
+cudaError_t launch_tc_instance(const CUtensorMap &kmap, const CUtensorMap &vmap,
+                               const DecodeParams &p, int B, int G, cudaStream_t stream) {
+    using C = TcCfg<HC, GP>;
+    auto kern = decode_tc_kernel<HC, GP>;
+    static std::atomic<uint64_t> smem_attr_done{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(smem_attr_done.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        smem_attr_done.fetch_or(bit, std::memory_order_release);
+    }
+    return launch_maybe_cooperative(kern, dim3(p.num_splits, p.num_kv_heads / HC, B), kTcThreads,
+                                    C::kSmemBytes, stream, p.counters != nullptr, kmap, vmap, p, G);
+}
+
+}  // namespace pa

@@ -112,8 +112,65 @@ __device__ __forceinline__ uint32_t swz128(int row, int chunk) {
     return static_cast<uint32_t>(row * kSubBytes + ((chunk ^ (row & 7)) << 4));
 }
 
+// Plain arrive (count 1) on an mbarrier.
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
+// Named barrier `id` over `nthreads` threads (a multiple of 32).
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Named barrier that also returns whether any participating thread passed true.
+__device__ __forceinline__ bool named_sync_or(int id, int nthreads, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred q, p;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ float ldcg(const float *p) { return __ldcg(p); }
+
 __device__ __forceinline__ void set_status(int32_t *status, int bits) {
     if (status) atomicOr(status, bits);
+}
+
+// Launch `kern` normally, or cooperatively (all CTAs resident at once, as CTAs
+// that wait for each other need) when `cooperative`; a cooperative grid larger
+// than what fits at once fails with cudaErrorCooperativeLaunchTooLarge.
+template <typename Kernel, typename... Args>
+inline cudaError_t launch_maybe_cooperative(Kernel kern, dim3 grid, int threads, int smem,
+                                            cudaStream_t stream, bool cooperative, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = cooperative ? 1 : 0;
+    if (cooperative) {
+        int per_sm = 0, dev = 0, sms = 0;
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
+        if (e == cudaSuccess) e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        if (static_cast<int64_t>(grid.x) * grid.y * grid.z > static_cast<int64_t>(per_sm) * sms)
+            return cudaErrorCooperativeLaunchTooLarge;
+    }
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
+    return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
 }  // namespace pa

@@ -28,6 +28,10 @@ struct DecodeParams {
     int32_t chunk;          // tokens per partition, multiple of 16
     int32_t split;          // 1: write partials, 0: write out/lse
     float scale_log2;       // scale * log2(e)
+    // Fused combine (split only): the last CTA of each (sequence, head group)
+    // to finish merges the group's partials into out/lse.  counters has one
+    // int per (sequence, head group), zero on entry and left zero on exit.
+    int32_t *counters;      // null: partials only
 };
 
 // CUDA-core decode kernel launch (pa_decode_cc_d*.cu).  Returns a cudaError_t.

@@ -21,9 +21,9 @@ namespace {
 
 constexpr size_t kScratchBytes = PA_NOALLOC_SCRATCH_BYTES;
 
-// Partial outputs and LSEs of the split (the same layout pa_decode_splitkv
-// uses in its caller-provided workspace).  Every call overwrites every
-// element it reads, so nothing here has to start at zero.
+// Partial outputs, LSEs and merge counters of the split (the same layout
+// pa_decode_splitkv uses in its caller-provided workspace).  Each call clears
+// the counters before its kernels run; the partials are written before read.
 __device__ __align__(256) unsigned char g_splitkv_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
@@ -60,7 +60,8 @@ int pa_decode_splitkv_noalloc(void *out, float *lse, const void *q, const void *
         return PA_EINVAL;
     int P = num_splits;
     if (P == 0) {
-        P = pa_auto_num_splits(B, cache.num_kv_heads, max_blocks_per_seq, cache.block_size);
+        P = pa_auto_num_splits(B, Hq, cache.num_kv_heads, cache.head_dim, max_blocks_per_seq,
+                               cache.block_size);
         if (P < 0) return P;
     }
     // The split's partials must fit the built-in array.
@@ -70,6 +71,16 @@ int pa_decode_splitkv_noalloc(void *out, float *lse, const void *q, const void *
     if (P > 1) {
         int rc = scratch_address(&scratch);
         if (rc) return rc;
+    }
+    if (P > 1) {
+        // The split's merge counters (after the partials) must start at zero; a
+        // completed call leaves them at zero, this also covers one that did not.
+        const int64_t rows = static_cast<int64_t>(B) * Hq * P;
+        const size_t off = static_cast<size_t>(((rows * cache.head_dim * 4 + 255) / 256) * 256 +
+                                               ((rows * 4 + 255) / 256) * 256);
+        if (cudaMemsetAsync(static_cast<uint8_t *>(scratch) + off, 0,
+                            static_cast<size_t>(B) * Hq * 8, stream) != cudaSuccess)
+            return PA_ECUDA;
     }
     return pa_decode_splitkv(out, lse, q, k_cache, v_cache, cache, block_tables,
                              max_blocks_per_seq, seq_lens, B, Hq, scale, P, scratch,

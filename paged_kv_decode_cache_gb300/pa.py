@@ -45,7 +45,7 @@ _SIGNATURES = {
     "pa_cache_write": ([_P, _P, _P, _I64, _P, _P, CacheDesc, _P, _P], ctypes.c_int),
     "pa_decode": ([_P, _P, _P, _P, _P, CacheDesc, _P, _I32, _P, _I32, _I32, _F32, _P, _P],
                   ctypes.c_int),
-    "pa_choose_num_splits": ([_I32, _I32, _I32, _I32, _I32], ctypes.c_int),
+    "pa_choose_num_splits": ([_I32, _I32, _I32, _I32, _I32, _I32, _I32], ctypes.c_int),
     "pa_partition_tokens": ([_I32, _I32, _I32], ctypes.c_int),
     "pa_splitkv_workspace_bytes": ([_I32, _I32, _I32, _I32], _SZ),
     "pa_decode_partial": ([_P, _P, _P, _P, _P, CacheDesc, _P, _I32, _P, _I32, _I32, _F32, _I32,
@@ -55,7 +55,7 @@ _SIGNATURES = {
                            _P, _SZ, _P, _P], ctypes.c_int),
     "pa_decode_splitkv_noalloc": ([_P, _P, _P, _P, _P, CacheDesc, _P, _I32, _P, _I32, _I32, _F32,
                                    _I32, _P, _P], ctypes.c_int),
-    "pa_auto_num_splits": ([_I32, _I32, _I32, _I32], ctypes.c_int),
+    "pa_auto_num_splits": ([_I32, _I32, _I32, _I32, _I32, _I32], ctypes.c_int),
     "pa_strerror": ([ctypes.c_int], ctypes.c_char_p),
     "pa_version": ([], ctypes.c_int),
 }
@@ -132,9 +132,9 @@ def pa_version() -> int:
     return lib().pa_version()
 
 
-def pa_choose_num_splits(B: int, Hkv: int, max_blocks_per_seq: int, block_size: int,
-                         sm_count: int) -> int:
-    r = lib().pa_choose_num_splits(B, Hkv, max_blocks_per_seq, block_size, sm_count)
+def pa_choose_num_splits(B: int, Hq: int, Hkv: int, D: int, max_blocks_per_seq: int,
+                         block_size: int, sm_count: int) -> int:
+    r = lib().pa_choose_num_splits(B, Hq, Hkv, D, max_blocks_per_seq, block_size, sm_count)
     _check("pa_choose_num_splits", min(r, 0))
     return r
 
@@ -149,8 +149,9 @@ def pa_splitkv_workspace_bytes(B: int, Hq: int, D: int, num_splits: int) -> int:
     return int(lib().pa_splitkv_workspace_bytes(B, Hq, D, num_splits))
 
 
-def pa_auto_num_splits(B: int, Hkv: int, max_blocks_per_seq: int, block_size: int) -> int:
-    r = lib().pa_auto_num_splits(B, Hkv, max_blocks_per_seq, block_size)
+def pa_auto_num_splits(B: int, Hq: int, Hkv: int, D: int, max_blocks_per_seq: int,
+                       block_size: int) -> int:
+    r = lib().pa_auto_num_splits(B, Hq, Hkv, D, max_blocks_per_seq, block_size)
     _check("pa_auto_num_splits", min(r, 0))
     return r
 

@@ -53,8 +53,8 @@ class Dev:
 
     def splitkv(self, num_splits=0):
         w = self.w
-        P = num_splits or pa.pa_auto_num_splits(w.B, w.Hkv, w.max_blocks, w.block_size)
-        ws = torch.empty(max(1, pa.pa_splitkv_workspace_bytes(w.B, w.Hq, w.D, P)),
+        P = num_splits or pa.pa_auto_num_splits(w.B, w.Hq, w.Hkv, w.D, w.max_blocks, w.block_size)
+        ws = torch.zeros(max(1, pa.pa_splitkv_workspace_bytes(w.B, w.Hq, w.D, P)),
                          dtype=torch.uint8, device="cuda")
         out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
         lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device="cuda")

@@ -45,28 +45,74 @@ def test_version_and_strerror(lib):
     assert pa.pa_strerror(-99) == "unknown error code"
 
 
-@pytest.mark.parametrize("B,Hkv,mb,bs,sms", [
-    (8, 4, 256, 16, 152), (1, 4, 2048, 16, 152), (2, 4, 2048, 16, 152), (256, 8, 128, 16, 152),
-    (8, 2, 128, 16, 152), (1, 2, 128, 16, 152), (8, 4, 16, 256, 152), (4, 2, 7, 16, 152),
-    (1, 1, 1, 16, 152), (3, 1, 1000, 16, 132),
-])
-def test_split_policy(lib, B, Hkv, mb, bs, sms):
-    P = pa.pa_choose_num_splits(B, Hkv, mb, bs, sms)
+# (B, Hq, Hkv, D, max_blocks, bs, sms); CTAs per SM: 1 for the tensor-core
+# kernel (D = 128, G >= 4), 2 for the CUDA-core kernel.
+SPLIT_CASES = [
+    (8, 28, 4, 128, 256, 16, 152), (1, 28, 4, 128, 2048, 16, 152), (2, 28, 4, 128, 2048, 16, 152),
+    (256, 16, 8, 128, 128, 16, 152), (8, 12, 2, 128, 128, 16, 152), (1, 12, 2, 128, 128, 16, 152),
+    (8, 28, 4, 128, 16, 256, 152), (4, 4, 2, 64, 7, 16, 152), (1, 1, 1, 64, 1, 16, 152),
+    (3, 2, 1, 128, 1000, 16, 132),
+]
+
+
+def _tc_heads_per_cta(G, Hkv):
+    """KV heads per CTA of the tensor-core kernel (mirrors the library's rule)."""
+    hc = 1
+    while hc < 8 and Hkv % (hc * 2) == 0:
+        hc *= 2
+    while True:
+        gp = 1
+        while gp < G:
+            gp *= 2
+        gp = max(gp, 16 // hc)
+        if gp * hc <= 64:
+            return hc
+        hc //= 2
+
+
+def _ctas_per_sm(Hq, Hkv, D):
+    return 1 if D == 128 else 2
+
+
+def _units(B, Hq, Hkv, D):
+    return B * (Hkv // _tc_heads_per_cta(Hq // Hkv, Hkv)) if D == 128 else B * Hkv
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,D,mb,bs,sms", SPLIT_CASES)
+def test_split_policy(lib, monkeypatch, B, Hq, Hkv, D, mb, bs, sms):
+    monkeypatch.delenv("PA_DECODE_KERNEL", raising=False)
+    P = pa.pa_choose_num_splits(B, Hq, Hkv, D, mb, bs, sms)
     lmax = mb * bs
+    slots = _ctas_per_sm(Hq, Hkv, D) * sms
     assert 1 <= P <= 256
     chunk = pa.pa_partition_tokens(mb, bs, P)
     assert chunk % 16 == 0 and chunk * P >= lmax and chunk * (P - 1) < lmax  # no empty tail split
+    units = _units(B, Hq, Hkv, D)
     if P > 1:
-        assert B * Hkv * P <= 2 * sms          # one wave of resident CTAs
+        assert units * P <= slots              # one wave of resident CTAs
         assert chunk >= 16 * 8 or chunk * P >= lmax
-    if B * Hkv >= 2 * sms:
+    if units >= slots:
         assert P == 1
 
 
-def test_split_policy_fills_small_batches(lib):
-    # 4 work units (B=1, Hkv=4) at 32k tokens: the split fills every SM slot.
-    P = pa.pa_choose_num_splits(1, 4, 2048, 16, 152)
-    assert 4 * P >= 0.9 * 2 * 152
+def test_split_policy_fills_small_batches(lib, monkeypatch):
+    monkeypatch.delenv("PA_DECODE_KERNEL", raising=False)
+    # one work unit (B=1, all 4 KV heads in one CTA) at 32k tokens: the split fills every SM
+    P = pa.pa_choose_num_splits(1, 28, 4, 128, 2048, 16, 152)
+    assert P >= 0.9 * 152
+    # the CUDA-core kernel has one CTA per KV head and two CTAs per SM
+    monkeypatch.setenv("PA_DECODE_KERNEL", "cuda_core")
+    assert 4 * pa.pa_choose_num_splits(1, 28, 4, 128, 2048, 16, 152) >= 0.9 * 2 * 152
+
+
+def test_kernel_override_rejects_what_it_cannot_run(lib, monkeypatch):
+    monkeypatch.setenv("PA_DECODE_KERNEL", "tensor_core")
+    assert lib.pa_choose_num_splits(1, 8, 2, 64, 16, 16, 152) == pa.PA_EUNSUPPORTED   # D = 64
+    monkeypatch.setenv("PA_DECODE_KERNEL", "cuda_core")
+    assert lib.pa_choose_num_splits(1, 32, 2, 128, 16, 16, 152) == pa.PA_EUNSUPPORTED  # G = 16
+    monkeypatch.delenv("PA_DECODE_KERNEL")
+    assert lib.pa_choose_num_splits(1, 32, 2, 128, 16, 16, 152) >= 1                   # tensor cores
+    assert lib.pa_choose_num_splits(1, 34, 2, 128, 16, 16, 152) == pa.PA_EUNSUPPORTED  # G = 17
 
 
 def test_partition_tokens(lib):
@@ -94,7 +140,8 @@ FAKE = ctypes.c_void_p(1 << 20)  # aligned, never dereferenced: these calls fail
     (dict(B=-1), pa.PA_EINVAL),
     (dict(q=None), pa.PA_EINVAL),
     (dict(Hq=5), pa.PA_EINVAL),                 # Hq % Hkv != 0
-    (dict(Hq=18), pa.PA_EUNSUPPORTED),          # G = 9 > 8
+    (dict(Hq=18), pa.PA_EUNSUPPORTED),          # G = 9 > 8 at D = 64
+    (dict(Hq=34, desc=_desc(d=128)), pa.PA_EUNSUPPORTED),   # G = 17 > 16
     (dict(desc=_desc(d=96)), pa.PA_EUNSUPPORTED),
     (dict(desc=_desc(bs=8)), pa.PA_EUNSUPPORTED),
     (dict(desc=_desc(nb=0)), pa.PA_EINVAL),

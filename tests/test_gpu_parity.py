@@ -20,6 +20,25 @@ def _built():
     build.build()
 
 
+def kernels_for(Hq, Hkv, D):
+    """The decode kernels that can run this shape (both are tested where both can)."""
+    G = Hq // Hkv
+    ks = []
+    if G <= 8:
+        ks.append("cuda_core")
+    if D == 128 and G <= 16:
+        ks.append("tensor_core")
+    return ks
+
+
+@pytest.fixture
+def use_kernel(monkeypatch):
+    def _set(kernel):
+        monkeypatch.setenv("PA_DECODE_KERNEL", kernel)
+    yield _set
+    monkeypatch.delenv("PA_DECODE_KERNEL", raising=False)
+
+
 # ---------------------------------------------------------------- cache write
 def test_cache_write_bit_exact_with_sentinels():
     rng = np.random.default_rng(0)
@@ -70,6 +89,9 @@ SMALL = [
     (16, 4, 128, 256, (300, 513, 256, 1)),          # 256-token pages
     (4, 1, 64, 256, (1000,)),                       # G = 4, pages, long-ish
     (2, 2, 128, 16, (0, 5)),                        # empty sequence
+    (32, 2, 128, 16, (129, 300)),                   # G = 16 (tensor cores only)
+    (24, 2, 128, 256, (700, 1)),                    # G = 12, pages (tensor cores only)
+    (8, 2, 128, 16, (127, 128, 129, 255, 256, 257)),  # chunk boundaries of 128 tokens
 ]
 
 
@@ -80,24 +102,28 @@ def _small(Hq, Hkv, D, bs, lens, seed=0, **kw):
 
 
 @pytest.mark.parametrize("case", SMALL, ids=lambda c: f"Hq{c[0]}-Hkv{c[1]}-D{c[2]}-bs{c[3]}")
-def test_decode_small_elementwise(case):
+def test_decode_small_elementwise(case, use_kernel):
     w = _small(*case, seed=hash(case) % 1000, poison_unused=True)
-    dev = Dev(w)
-    dev.write()
-    out, lse = dev.decode()
     kc, vc = oracle_after_write(w)
     ref, ref_lse = oracle.decode(w.q, kc, vc, w.block_tables, w.seq_lens, w.scale)
-    assert_close(bf16_dev_to_f64(out), ref, "pa_decode")
-    assert_lse_close(lse.cpu().double().numpy(), ref_lse, "pa_decode")
-    for P in (2, 3, 7):
-        so, sl, _ = dev.splitkv(P)
-        assert_close(bf16_dev_to_f64(so), ref, f"splitkv P={P}")
-        assert_lse_close(sl.cpu().double().numpy(), ref_lse, f"splitkv P={P}")
-    assert dev.status_value() == 0
+    for kernel in kernels_for(w.Hq, w.Hkv, w.D):
+        use_kernel(kernel)
+        dev = Dev(w)
+        dev.write()
+        out, lse = dev.decode()
+        assert_close(bf16_dev_to_f64(out), ref, f"pa_decode {kernel}")
+        assert_lse_close(lse.cpu().double().numpy(), ref_lse, f"pa_decode {kernel}")
+        for P in (2, 3, 7):
+            so, sl, _ = dev.splitkv(P)
+            assert_close(bf16_dev_to_f64(so), ref, f"splitkv P={P} {kernel}")
+            assert_lse_close(sl.cpu().double().numpy(), ref_lse, f"splitkv P={P} {kernel}")
+        assert dev.status_value() == 0
 
 
+@pytest.mark.parametrize("kernel", ["cuda_core", "tensor_core"])
 @pytest.mark.parametrize("P", [1, 2, 5, 16, 40])
-def test_partials_match_oracle_partials(P):
+def test_partials_match_oracle_partials(P, kernel, use_kernel):
+    use_kernel(kernel)
     w = _small(12, 2, 128, 16, (1, 70, 129, 400), seed=P)
     dev = Dev(w)
     dev.write()
@@ -131,25 +157,30 @@ FULL = ["tiny", "qwen2.5-1.5b-B1", "qwen2.5-1.5b-B8", "qwen2.5-7b-bs16", "qwen2.
 
 
 @pytest.mark.parametrize("name", FULL)
-def test_workload_full_size(name):
-    """The bench's launch configuration (auto split) plus the unsplit kernel, on the
-    full-size workload; all rows for small batches, a seeded sample otherwise."""
+def test_workload_full_size(name, use_kernel):
+    """The bench's launch configuration (auto kernel, auto split) plus the unsplit
+    call, then each kernel forced, on the full-size workload; all rows for small
+    batches, a seeded sample otherwise."""
     w = W.WORKLOADS[name]()
-    dev = Dev(w)
-    dev.write()
-    out_s, lse_s, P = dev.splitkv(0)
-    out_u, lse_u = dev.decode()
-    assert dev.status_value() == 0
     kc, vc = oracle_after_write(w)
     rb, rh = sample_rows(w, 160, seed=len(name))
     ref, ref_lse = oracle_rows(w, kc, vc, rb, rh)
-    for tag, o, l in (("splitkv", out_s, lse_s), ("decode", out_u, lse_u)):
-        assert_close(bf16_dev_to_f64(o)[rb, rh], ref, f"{name} {tag} P={P}")
-        assert_lse_close(l.cpu().double().numpy()[rb, rh], ref_lse, f"{name} {tag}")
+    dev = Dev(w)
+    dev.write()
+    for kernel in ["auto"] + kernels_for(w.Hq, w.Hkv, w.D):
+        use_kernel(kernel)
+        out_s, lse_s, P = dev.splitkv(0)
+        out_u, lse_u = dev.decode()
+        assert dev.status_value() == 0
+        for tag, o, l in (("splitkv", out_s, lse_s), ("decode", out_u, lse_u)):
+            assert_close(bf16_dev_to_f64(o)[rb, rh], ref, f"{name} {tag} {kernel} P={P}")
+            assert_lse_close(l.cpu().double().numpy()[rb, rh], ref_lse, f"{name} {tag} {kernel}")
 
 
 # ------------------------------------------------------ bit-exact invariants
-def test_block_permutation_invariance_bit_exact():
+@pytest.mark.parametrize("kernel", ["cuda_core", "tensor_core"])
+def test_block_permutation_invariance_bit_exact(kernel, use_kernel):
+    use_kernel(kernel)
     w = _small(28, 4, 128, 16, (300, 77, 16), seed=5)
     dev = Dev(w)
     out1, lse1 = dev.decode()
@@ -164,7 +195,9 @@ def test_block_permutation_invariance_bit_exact():
     assert torch.equal(out1, out2) and torch.equal(lse1, lse2)
 
 
-def test_single_token_returns_v_row_exactly():
+@pytest.mark.parametrize("kernel", ["cuda_core", "tensor_core"])
+def test_single_token_returns_v_row_exactly(kernel, use_kernel):
+    use_kernel(kernel)
     w = _small(8, 2, 128, 16, (1, 1, 1), seed=9)
     dev = Dev(w)
     dev.write()
@@ -177,7 +210,9 @@ def test_single_token_returns_v_row_exactly():
     assert torch.equal(out, o2)
 
 
-def test_value_scaling_by_two_is_exact():
+@pytest.mark.parametrize("kernel", ["cuda_core", "tensor_core"])
+def test_value_scaling_by_two_is_exact(kernel, use_kernel):
+    use_kernel(kernel)
     w = _small(12, 2, 128, 16, (100, 33), seed=11)
     out1, lse1 = Dev(w).decode()
     v2 = torch.from_numpy(w.v_cache.view(np.int16)).view(torch.bfloat16).float() * 2
@@ -186,7 +221,9 @@ def test_value_scaling_by_two_is_exact():
     assert torch.equal(out2.float(), out1.float() * 2) and torch.equal(lse1, lse2)
 
 
-def test_identical_query_heads_give_identical_outputs():
+@pytest.mark.parametrize("kernel", ["cuda_core", "tensor_core"])
+def test_identical_query_heads_give_identical_outputs(kernel, use_kernel):
+    use_kernel(kernel)
     w = _small(16, 2, 128, 16, (90, 40), seed=13)
     w.q[:] = w.q[:, :1]
     out, _ = Dev(w).decode()
@@ -195,7 +232,9 @@ def test_identical_query_heads_give_identical_outputs():
         assert torch.equal(grp, grp[:, :1].expand_as(grp))
 
 
-def test_poisoned_pool_rows_never_leak():
+@pytest.mark.parametrize("kernel", ["cuda_core", "tensor_core"])
+def test_poisoned_pool_rows_never_leak(kernel, use_kernel):
+    use_kernel(kernel)
     lens = (5, 17, 250)
     clean = Dev(_small(12, 2, 128, 16, lens, seed=17)).decode()[0]
     poisoned = Dev(_small(12, 2, 128, 16, lens, seed=17, poison_unused=True)).decode()[0]
@@ -204,8 +243,9 @@ def test_poisoned_pool_rows_never_leak():
 
 
 # ---------------------------------------------------------- bad device data
-def test_bad_block_id_is_reported_not_dereferenced():
-    w = _small(4, 2, 64, 16, (40, 20), seed=19)
+@pytest.mark.parametrize("shape", [(4, 2, 64), (14, 2, 128)])
+def test_bad_block_id_is_reported_not_dereferenced(shape):
+    w = _small(*shape, 16, (40, 20), seed=19)
     w.block_tables[0, 1] = w.num_blocks + 1000
     w.block_tables[1, 0] = -5
     dev = Dev(w)
@@ -214,8 +254,9 @@ def test_bad_block_id_is_reported_not_dereferenced():
     assert dev.status_value() & pa.PA_STATUS_BAD_BLOCK
 
 
-def test_bad_seq_len_is_reported_and_clamped():
-    w = _small(4, 2, 64, 16, (40, 20), seed=23)
+@pytest.mark.parametrize("shape", [(4, 2, 64), (14, 2, 128)])
+def test_bad_seq_len_is_reported_and_clamped(shape):
+    w = _small(*shape, 16, (40, 20), seed=23)
     w.seq_lens = np.array([40, 10_000], np.int32)
     dev = Dev(w)
     dev.decode()
@@ -223,11 +264,35 @@ def test_bad_seq_len_is_reported_and_clamped():
     assert dev.status_value() & pa.PA_STATUS_BAD_SEQLEN
 
 
+@pytest.mark.parametrize("kernel", ["cuda_core", "tensor_core"])
+def test_fused_merge_reuses_its_workspace(kernel, use_kernel):
+    """Consecutive split calls on one workspace give the same result, and the merge
+    counters at the end of the workspace are back at zero after every call."""
+    use_kernel(kernel)
+    w = _small(28, 4, 128, 16, (700, 300, 33), seed=31)
+    dev = Dev(w)
+    P = 5
+    nbytes = pa.pa_splitkv_workspace_bytes(w.B, w.Hq, w.D, P)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(3):
+        out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
+        pa.pa_decode_splitkv(out, None, dev.q, dev.k_cache, dev.v_cache, dev.block_tables,
+                             dev.seq_lens, w.scale, num_splits=P, workspace=ws)
+        torch.cuda.synchronize()
+        counters = ws[-(((w.B * w.Hq * 8 + 255) // 256) * 256):]
+        assert int(counters.count_nonzero()) == 0
+        outs.append(out)
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    ref, _ = oracle.decode(w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.scale)
+    assert_close(bf16_dev_to_f64(outs[0]), ref, f"fused merge {kernel}")
+
+
 def test_splitkv_small_workspace_is_rejected():
     w = _small(12, 2, 128, 16, (300,), seed=29)
     dev = Dev(w)
     out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
-    ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(16, dtype=torch.uint8, device="cuda")
     with pytest.raises(pa.PAError) as e:
         pa.pa_decode_splitkv(out, None, dev.q, dev.k_cache, dev.v_cache, dev.block_tables,
                              dev.seq_lens, w.scale, num_splits=4, workspace=ws)
@@ -238,8 +303,8 @@ def test_splitkv_small_workspace_is_rejected():
 def test_decode_step_replays_in_a_cuda_graph():
     w = W.qwen25_1p5b(8)
     dev = Dev(w)
-    P = pa.pa_auto_num_splits(w.B, w.Hkv, w.max_blocks, w.block_size)
-    ws = torch.empty(pa.pa_splitkv_workspace_bytes(w.B, w.Hq, w.D, P), dtype=torch.uint8,
+    P = pa.pa_auto_num_splits(w.B, w.Hq, w.Hkv, w.D, w.max_blocks, w.block_size)
+    ws = torch.zeros(pa.pa_splitkv_workspace_bytes(w.B, w.Hq, w.D, P), dtype=torch.uint8,
                      device="cuda")
     out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
     s = torch.cuda.Stream()

@@ -37,7 +37,7 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
     w = W.qwen25_7b(16)
     dev = Dev(w)
     dev.write()
-    P = pa.pa_auto_num_splits(w.B, w.Hkv, w.max_blocks, w.block_size)
+    P = pa.pa_auto_num_splits(w.B, w.Hq, w.Hkv, w.D, w.max_blocks, w.block_size)
     assert P > 1
     assert pa.pa_splitkv_workspace_bytes(w.B, w.Hq, w.D, P) <= pa.PA_NOALLOC_SCRATCH_BYTES
     ref1, ref1_lse, _ = dev.splitkv(P)
