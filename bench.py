@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU work for the oracle baseline sample")
     ap.add_argument("--e2e-steps", type=int, default=0, help="0 = min(steps, 500)")
+    ap.add_argument("--unfused", action="store_true",
+                    help="time pa_cache_write + pa_decode_splitkv instead of pa_decode_step")
     return ap.parse_args()
 
 
@@ -302,22 +304,24 @@ def run_ours(args, world, rank, local):
 
     ws = torch.zeros(max(1, pa.pa_splitkv_workspace_bytes(w.B, w.Hq, w.D, P)), dtype=torch.uint8,
                      device=dev)
-    fused = P > 1   # the split decode kernel merges its own partials (one cooperative launch)
+    merged = P > 1   # the split kernel merges its own partials (one cooperative launch)
 
     def step(r, ev0=None, ev1=None):
         kc, vc = pools[r]
-        pa.pa_cache_write(kn, vn, slots, kc, vc, stream=stream)
+        if args.unfused:
+            pa.pa_cache_write(kn, vn, slots, kc, vc, stream=stream)
         if ev0 is not None:
             ev0.record(stream)
-        if P > 1:
+        if args.unfused:
             pa.pa_decode_splitkv(out, lse, q, kc, vc, bt, sl, w.scale, num_splits=P, workspace=ws,
                                  stream=stream)
-        else:
-            pa.pa_decode(out, lse, q, kc, vc, bt, sl, w.scale, stream=stream)
+        else:   # one launch: write this step's K/V, attend, merge the splits
+            pa.pa_decode_step(out, lse, q, kn, vn, slots, kc, vc, bt, sl, w.scale, num_splits=P,
+                              workspace=ws, stream=stream)
         if ev1 is not None:
             ev1.record(stream)
 
-    launches_per_step = 3 if (P > 1 and not fused) else 2
+    launches_per_step = 2 if args.unfused else 1
     # CUDA graphs of S consecutive steps (cycling over the pool replicas), NG
     # copies, each step with its own pair of graph-recorded events around the
     # decode kernel.  Step i of the timed loop is step i % S of graph copy
@@ -395,9 +399,8 @@ def run_ours(args, world, rank, local):
             for d, h in ((d_q16, h_q), (bt, h_bt), (sl, h_sl), (d_kn16, h_kn), (d_vn16, h_vn),
                          (slots, h_slots)):
                 d.copy_(h, non_blocking=True)
-            pa.pa_cache_write(kn, vn, slots, kc, vc, stream=stream)
-            pa.pa_decode_splitkv(out, lse, q, kc, vc, bt, sl, w.scale, num_splits=P,
-                                 workspace=ws, stream=stream)
+            pa.pa_decode_step(out, lse, q, kn, vn, slots, kc, vc, bt, sl, w.scale, num_splits=P,
+                              workspace=ws, stream=stream)
             h_out.copy_(out.view(torch.int16), non_blocking=True)
             h_lse.copy_(lse, non_blocking=True)
 
@@ -416,17 +419,17 @@ def run_ours(args, world, rank, local):
     e2e_value = step_bytes * world / (e2e_ms * 1e-3) / 1e12
 
     peak, peak_kind = measured_peak_gbs()
-    # the timed call reads K, V, q and writes the bf16 output (its split partials and
-    # merge are overhead on top); above 64 splits it also covers the combine launch
-    kern_bytes = w.kv_bytes() + 2 * w.B * w.Hq * w.D * 2
+    # the timed launch reads K, V and q, writes the bf16 output and (fused step) moves
+    # this step's new K/V into the pool; its split partials and merge are overhead
+    kern_bytes = w.kv_bytes() + 2 * w.B * w.Hq * w.D * 2 + (0 if args.unfused else write_bytes)
     roofline = None
     if kern_ms_avg:
         ach = kern_bytes / (kern_ms_avg * 1e-3) / 1e9
         roofline = {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
                     "frac": round(ach / peak, 4), "traffic": recorded_traffic(args.workload, kernel_name),
                     "peak_kind": peak_kind,
-                    "kernel": kernel_name + (" + fused merge" if fused else
-                                             " + combine" if P > 1 else ""),
+                    "kernel": kernel_name + ("" if args.unfused else " (fused write)")
+                              + (" + split merge" if merged else ""),
                     "kernel_us": round(kern_ms_avg * 1e3, 3), "kernel_bytes": kern_bytes}
 
     cpu = None
@@ -443,7 +446,8 @@ def run_ours(args, world, rank, local):
             "data": "synthetic",
             "config": {"workload": args.workload, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
                        "block_size": w.block_size, "seq_lens_total": int(w.seq_lens.sum()),
-                       "splits": P, "step": "cache_write + split decode + combine",
+                       "splits": P, "step": ("cache_write, then split decode with merge" if args.unfused else
+                                "pa_decode_step: cache write + split decode + merge, one launch"),
                        "parallelism": f"replicas x{world}",
                        "l2": f"{R} pool replicas rotated per step ({touched/1e6:.0f} MB read per step)"},
             "us_per_step": ms_per_step * 1e3,

@@ -239,6 +239,30 @@ int pa_decode_splitkv_noalloc(void *out, float *lse, const void *q, const void *
                               const int32_t *seq_lens, int32_t B, int32_t Hq, float scale,
                               int32_t num_splits, int32_t *status, pa_stream_t stream);
 
+/*
+ * One whole decode step in one launch: the slot-mapping write of this step's
+ * new K/V and split-KV decode attention (prajwal7-2002 docs, row "Batched
+ * Paged Decode": the [B, 1] step writes the new token through the slot
+ * mapping and attends over the gathered blocks).  The same result as
+ *   pa_cache_write(k_new, v_new, slot_mapping, B, ...) then pa_decode_splitkv(...)
+ * when slot_mapping[b] is the slot of position seq_lens[b] - 1 of sequence b
+ * (write-then-attend), but without the separate write launch: the CTA that
+ * reads that position writes the token's rows just before loading them.
+ * k_new, v_new: device bf16 [B, Hkv, D] (row b is sequence b's new token);
+ * slot_mapping: device int64 [B], a negative slot means no write for that
+ * sequence.  A non-negative slot that is not position seq_lens[b] - 1 of
+ * sequence b is not written and sets PA_STATUS_BAD_SLOT (a slot this step
+ * does not read could be read by another sequence in the same launch).
+ * Every other argument, the workspace contract included, as
+ * pa_decode_splitkv; num_splits == 1 needs no workspace.
+ */
+int pa_decode_step(void *out, float *lse, const void *q, const void *k_new, const void *v_new,
+                   const int64_t *slot_mapping, void *k_cache, void *v_cache, pa_cache_desc cache,
+                   const int32_t *block_tables, int32_t max_blocks_per_seq,
+                   const int32_t *seq_lens, int32_t B, int32_t Hq, float scale,
+                   int32_t num_splits, void *workspace, size_t workspace_bytes, int32_t *status,
+                   pa_stream_t stream);
+
 /* P that pa_decode_splitkv uses for num_splits == 0 on the current device (PA_ECUDA on error). */
 int pa_auto_num_splits(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t max_blocks_per_seq,
                        int32_t block_size);

@@ -239,11 +239,18 @@ int sm_count_current() {
     return n;
 }
 
+// This step's new K/V for the fused write of pa_decode_step (all null: none).
+struct NewTokens {
+    const void *k_new = nullptr;
+    const void *v_new = nullptr;
+    const int64_t *slot_mapping = nullptr;
+};
+
 int run_decode(bool split, void *out, float *lse, float *part_o, float *part_lse, const void *q,
                const void *k_cache, const void *v_cache, const pa_cache_desc &c,
                const int32_t *block_tables, int32_t max_blocks, const int32_t *seq_lens,
                int32_t B, int32_t Hq, float scale, int32_t P, int32_t *status,
-               cudaStream_t stream, int32_t *counters = nullptr) {
+               cudaStream_t stream, int32_t *counters = nullptr, const NewTokens &nt = NewTokens()) {
     const int G = Hq / c.num_kv_heads;
     Kernel k;
     int rc = pick_kernel(G, c.head_dim, &k);
@@ -257,6 +264,11 @@ int run_decode(bool split, void *out, float *lse, float *part_o, float *part_lse
     p.num_splits = P;
     p.chunk = pa_partition_tokens(max_blocks, c.block_size, P);
     p.counters = counters;
+    p.k_new = static_cast<const uint16_t *>(nt.k_new);
+    p.v_new = static_cast<const uint16_t *>(nt.v_new);
+    p.slot_mapping = nt.slot_mapping;
+    p.k_pool = static_cast<uint16_t *>(const_cast<void *>(k_cache));
+    p.v_pool = static_cast<uint16_t *>(const_cast<void *>(v_cache));
     CUtensorMap kmap, vmap;
     cudaError_t e;
     if (k == Kernel::kTensorCore) {
@@ -400,11 +412,13 @@ int pa_combine(void *out, float *lse, const float *part_o, const float *part_lse
     return e == cudaSuccess ? PA_OK : PA_ECUDA;
 }
 
-int pa_decode_splitkv(void *out, float *lse, const void *q, const void *k_cache,
-                      const void *v_cache, pa_cache_desc cache, const int32_t *block_tables,
-                      int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t B, int32_t Hq,
-                      float scale, int32_t num_splits, void *workspace, size_t workspace_bytes,
-                      int32_t *status, pa_stream_t stream) {
+namespace {
+// Split-KV decode shared by pa_decode_splitkv and pa_decode_step.
+int splitkv_common(void *out, float *lse, const void *q, const void *k_cache, const void *v_cache,
+                   const pa_cache_desc &cache, const int32_t *block_tables,
+                   int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t B, int32_t Hq,
+                   float scale, int32_t num_splits, void *workspace, size_t workspace_bytes,
+                   int32_t *status, cudaStream_t stream, const NewTokens &nt) {
     int rc = check_decode_args(q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq,
                                seq_lens, B, Hq, scale);
     if (rc) return rc;
@@ -421,7 +435,7 @@ int pa_decode_splitkv(void *out, float *lse, const void *q, const void *k_cache,
     if (P == 1)
         return run_decode(false, out, lse, nullptr, nullptr, q, k_cache, v_cache, cache,
                           block_tables, max_blocks_per_seq, seq_lens, B, Hq, scale, 1, status,
-                          stream);
+                          stream, nullptr, nt);
     const size_t need = pa_splitkv_workspace_bytes(B, Hq, cache.head_dim, P);
     if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return PA_EWORKSPACE;
     const int64_t rows = static_cast<int64_t>(B) * Hq * P;
@@ -433,14 +447,44 @@ int pa_decode_splitkv(void *out, float *lse, const void *q, const void *k_cache,
     // One cooperative launch that merges its own partials when the whole grid
     // fits on the GPU at once; otherwise partials, then pa_combine.
     rc = run_decode(true, out, lse, part_o, part_lse, q, k_cache, v_cache, cache, block_tables,
-                    max_blocks_per_seq, seq_lens, B, Hq, scale, P, status, stream, counters);
+                    max_blocks_per_seq, seq_lens, B, Hq, scale, P, status, stream, counters, nt);
     if (rc != PA_ETOOLARGE) return rc;
     rc = run_decode(true, nullptr, nullptr, part_o, part_lse, q, k_cache, v_cache, cache,
-                    block_tables, max_blocks_per_seq, seq_lens, B, Hq, scale, P, status, stream);
+                    block_tables, max_blocks_per_seq, seq_lens, B, Hq, scale, P, status, stream,
+                    nullptr, nt);
     if (rc) return rc;
     cudaError_t e = pa::launch_combine(out, lse, part_o, part_lse, static_cast<int>(B * Hq), P,
                                        cache.head_dim, stream);
     return e == cudaSuccess ? PA_OK : PA_ECUDA;
+}
+}  // namespace
+
+int pa_decode_splitkv(void *out, float *lse, const void *q, const void *k_cache,
+                      const void *v_cache, pa_cache_desc cache, const int32_t *block_tables,
+                      int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t B, int32_t Hq,
+                      float scale, int32_t num_splits, void *workspace, size_t workspace_bytes,
+                      int32_t *status, pa_stream_t stream) {
+    return splitkv_common(out, lse, q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq,
+                          seq_lens, B, Hq, scale, num_splits, workspace, workspace_bytes, status,
+                          stream, NewTokens());
+}
+
+int pa_decode_step(void *out, float *lse, const void *q, const void *k_new, const void *v_new,
+                   const int64_t *slot_mapping, void *k_cache, void *v_cache, pa_cache_desc cache,
+                   const int32_t *block_tables, int32_t max_blocks_per_seq,
+                   const int32_t *seq_lens, int32_t B, int32_t Hq, float scale,
+                   int32_t num_splits, void *workspace, size_t workspace_bytes, int32_t *status,
+                   pa_stream_t stream) {
+    if (B == 0) return PA_OK;
+    if (!k_new || !v_new || !slot_mapping) return PA_EINVAL;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(slot_mapping, 8)) return PA_EINVAL;
+    NewTokens nt;
+    nt.k_new = k_new;
+    nt.v_new = v_new;
+    nt.slot_mapping = slot_mapping;
+    return splitkv_common(out, lse, q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq,
+                          seq_lens, B, Hq, scale, num_splits, workspace, workspace_bytes, status,
+                          stream, nt);
 }
 
 }  // extern "C"

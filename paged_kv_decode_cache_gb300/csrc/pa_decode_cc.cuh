@@ -126,10 +126,38 @@ decode_cc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         }
     };
 
+    // Fused cache write: the warp whose tile holds position L - 1 writes that
+    // token's K (lanes 0-15) and V (lanes 16-31) row of head g into the pool
+    // just before loading the tile.  The row is fetched up front.
+    const int last_pos = L - 1;
+    const bool writes = p.k_new && last_pos >= t_begin && last_pos < t_end;
+    const int64_t slot_b = writes ? p.slot_mapping[b] : -1;
+    constexpr int kRowChunks = D / 8;  // 16-byte chunks of one head row
+    const int wl = lane & 15;
+    uint4 newrow = make_uint4(0u, 0u, 0u, 0u);
+    if (writes && wl < kRowChunks)
+        newrow = reinterpret_cast<const uint4 *>((lane < 16 ? p.k_new : p.v_new) +
+                                                 (static_cast<int64_t>(b) * p.num_kv_heads + g) * D)[wl];
+    auto write_if_holder = [&](int j) {  // whole warp, before tile j is issued
+        const int tok0 = t_begin + (warp + j * NW) * kTile;
+        if (!writes || last_pos < tok0 || last_pos >= tok0 + kTile) return;
+        const int ph = bt[tok0 / bs];
+        if (slot_is_position(slot_b, ph, last_pos, bs) && ph < p.num_blocks) {
+            if (wl < kRowChunks)
+                reinterpret_cast<uint4 *>((lane < 16 ? p.k_pool : p.v_pool) +
+                                          (slot_b * p.num_kv_heads + g) * D)[wl] = newrow;
+            fence_proxy_async_global();
+        } else if (lane == 0 && slot_b >= 0) {
+            set_status(p.status, PA_STATUS_BAD_SLOT);
+        }
+        __syncwarp();
+    };
+
     int issued = 0;
-    if (lane == 0)
-        for (; issued < NST && issued < my_tiles; ++issued) issue(issued);
-    issued = __shfl_sync(0xffffffffu, issued, 0);
+    for (; issued < NST && issued < my_tiles; ++issued) {
+        write_if_holder(issued);
+        if (lane == 0) issue(issued);
+    }
 
     float m_run[G], l_run[G], o[G][C::kDPV];
 #pragma unroll
@@ -263,11 +291,14 @@ decode_cc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         }
         __syncwarp();
         // Stage s is free again: refill it with this warp's tile j + NST.
-        if (lane == 0 && issued < my_tiles) {
-            fence_proxy_async_smem();
-            issue(issued);
+        if (issued < my_tiles) {
+            write_if_holder(issued);
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                issue(issued);
+            }
+            ++issued;
         }
-        issued = __shfl_sync(0xffffffffu, issued + (issued < my_tiles ? 1 : 0), 0);
     }
     if (aborted) {
         // Let this warp's copies in flight land before the CTA leaves (bounded).

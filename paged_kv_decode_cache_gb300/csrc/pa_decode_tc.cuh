@@ -138,16 +138,35 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int bs = p.block_size;
 
-    int L = p.seq_lens[b];
+    // Global reads that do not depend on the sequence length go out first, so
+    // their latencies overlap: the length, this CTA's queries, and the block
+    // ids of its first chunk (for this thread's role).
     const int lmax = p.max_blocks * bs;
+    const int t_begin = part * p.chunk;
+    const int t_lim = min(t_begin + p.chunk, lmax);  // range end before the length is known
+    const int64_t row0 = static_cast<int64_t>(b) * p.num_q_heads + static_cast<int64_t>(g0) * G;
+    const int32_t *bt = p.block_tables + static_cast<int64_t>(b) * p.max_blocks;
+    int L = p.seq_lens[b];
+    constexpr int kQLoads = (N * (D / 8) + kTcThreads - 1) / kTcThreads;
+    uint4 qv[kQLoads];
+#pragma unroll
+    for (int j = 0; j < kQLoads; ++j) {
+        const int i = tid + j * kTcThreads, n = i / (D / 8), c = i % (D / 8);
+        qv[j] = make_uint4(0u, 0u, 0u, 0u);
+        if (i < N * (D / 8) && n % GP < G)
+            qv[j] = *reinterpret_cast<const uint4 *>(p.q + (row0 + (n / GP) * G + n % GP) * D + c * 8);
+    }
+    // token offset, within a chunk, whose block id this thread looks up
+    const int my_tok = (warp == kTcTmaKWarp || warp == kTcTmaVWarp)
+                           ? (lane < 2 * C::kTiles ? (lane >> 1) * kTile : -1)
+                           : (warp < 4 ? (tid / (kTile * HC)) * kTile + (tid & 15) : -1);
+    const int phys_first = (my_tok >= 0 && t_begin + my_tok < t_lim) ? bt[(t_begin + my_tok) / bs] : -1;
     if (L < 0 || L > lmax) {
         if (tid == 0 && part == 0 && g0 == 0) set_status(p.status, PA_STATUS_BAD_SEQLEN);
         L = L < 0 ? 0 : lmax;
     }
-    const int t_begin = part * p.chunk;
     const int t_end = min(t_begin + p.chunk, L);
     const int nch = t_end > t_begin ? (t_end - t_begin + C::kT - 1) / C::kT : 0;
-    const int64_t row0 = static_cast<int64_t>(b) * p.num_q_heads + static_cast<int64_t>(g0) * G;
 
     if (nch == 0) {  // empty range: zero output, lse = -inf
         for (int i = tid; i < HC * G * D; i += kTcThreads) {
@@ -165,7 +184,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                                  kTcThreads, [] { __syncthreads(); });
         return;
     }
-    const int32_t *bt = p.block_tables + static_cast<int64_t>(b) * p.max_blocks;
 
     // ---- set-up: TMEM, barriers, the Q operand, zeroed P^T buffers ---------------------
     if (warp == 0) tc5::tmem_alloc(tmem_slot, C::kTmemCols);
@@ -179,18 +197,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         prefetch_tensormap(&vmap);
     }
     if (tid < N) m_ref[tid] = -INFINITY;
-    {
-        const uint16_t *qg = p.q + row0 * D;
-        for (int i = tid; i < N * (D / 8); i += kTcThreads) {  // row n = (head', q), 16-byte chunk c
-            const int n = i / (D / 8), c = i % (D / 8);
-            const int hh = n / GP, q = n % GP;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (q < G) v = *reinterpret_cast<const uint4 *>(qg + (hh * G + q) * D + c * 8);
-            *reinterpret_cast<uint4 *>(qs + (c >> 3) * (N * kSubBytes) + swz128(n, c & 7)) = v;
-        }
-        for (int i = tid; i < kTcNBP * C::kPBytes / 16; i += kTcThreads)
-            reinterpret_cast<uint4 *>(ps)[i] = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int j = 0; j < kQLoads; ++j) {  // Q operand row n = (head', q), 16-byte chunk c
+        const int i = tid + j * kTcThreads, n = i / (D / 8), c = i % (D / 8);
+        if (i < N * (D / 8))
+            *reinterpret_cast<uint4 *>(qs + (c >> 3) * (N * kSubBytes) + swz128(n, c & 7)) = qv[j];
     }
+    for (int i = tid; i < kTcNBP * C::kPBytes / 16; i += kTcThreads)
+        reinterpret_cast<uint4 *>(ps)[i] = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async_smem();
     fence_barrier_init();
     tc5::fence_before_sync();
@@ -223,7 +237,24 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             const int tok0 = t_begin + c * C::kT + tile * kTile;
             return (carrier && tok0 < t_end) ? bt[tok0 / bs] : -1;
         };
-        int phys_next = lookup(0);
+        int phys_next = phys_first;
+        // Fused cache write: the CTA whose range holds position L - 1 writes that
+        // token's K (warp 5) or V (warp 6) rows of its HC heads into the pool just
+        // before loading the tile that holds it.  The rows are fetched up front.
+        const int last_pos = L - 1;
+        const bool writes = p.k_new && last_pos >= t_begin && last_pos < t_end;
+        constexpr int kNewChunks = HC * D / 8;                 // 16-byte chunks of HC rows
+        constexpr int kNewPerLane = (kNewChunks + 31) / 32;
+        uint4 newrow[kNewPerLane];
+        int64_t slot_b = -1;
+        if (writes) {
+            slot_b = p.slot_mapping[b];
+            const uint4 *src = reinterpret_cast<const uint4 *>(
+                (is_v ? p.v_new : p.k_new) + (static_cast<int64_t>(b) * p.num_kv_heads + g0) * D);
+#pragma unroll
+            for (int j = 0; j < kNewPerLane; ++j)
+                if (lane + 32 * j < kNewChunks) newrow[j] = src[lane + 32 * j];
+        }
         int issued = 0;
         for (int c = 0; c < nch; ++c) {
             const int s = c % nst;
@@ -240,6 +271,21 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                 else if (!is_v && sub == 0) set_status(p.status, PA_STATUS_BAD_BLOCK);
             }
             const uint32_t vm = __ballot_sync(0xffffffffu, valid);
+            const int chunk0 = t_begin + c * C::kT;
+            if (writes && last_pos >= chunk0 && last_pos < chunk0 + C::kT) {  // holds position L - 1
+                const int ph = __shfl_sync(0xffffffffu, phys, 2 * ((last_pos - chunk0) / kTile));
+                if (slot_is_position(slot_b, ph, last_pos, bs) && ph < p.num_blocks) {
+                    uint4 *dst = reinterpret_cast<uint4 *>((is_v ? p.v_pool : p.k_pool) +
+                                                           (slot_b * p.num_kv_heads + g0) * D);
+#pragma unroll
+                    for (int j = 0; j < kNewPerLane; ++j)
+                        if (lane + 32 * j < kNewChunks) dst[lane + 32 * j] = newrow[j];
+                    fence_proxy_async_global();
+                } else if (lane == 0 && !is_v && slot_b >= 0) {
+                    set_status(p.status, PA_STATUS_BAD_SLOT);
+                }
+                __syncwarp();
+            }
             if (lane == 0) mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(__popc(vm)) * C::kBoxBytes);
             __syncwarp();
             if (valid)
@@ -304,22 +350,21 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     } else {
         // ================= softmax warps: thread = row m of a chunk, and output dim d =================
         const int my_head = (tid >> 4) % HC;                // head of row m = tid
-        const int my_tok = (tid / (kTile * HC)) * kTile + (tid & 15);  // token offset within a chunk
         float l_thr[GP];
 #pragma unroll
         for (int q = 0; q < GP; ++q) l_thr[q] = 0.f;
         const float sl2 = p.scale_log2;
         bool dead = false;
-        auto lookup = [&](int c) -> int {
+        auto lookup = [&](int c) -> int {  // block of this row's token in chunk c (-1: none)
             const int tok = t_begin + c * C::kT + my_tok;
             return tok < t_end ? bt[tok / bs] : -1;
         };
-        int phys_next = lookup(0);
+        int phys_next = phys_first;
         for (int c = 0; c < nch; ++c) {
             const int sbuf = c % kTcNBS, pbuf = c % kTcNBP;
             const int phys = phys_next;
             if (c + 1 < nch) phys_next = lookup(c + 1);  // one chunk ahead
-            const bool in_pool = phys >= 0 && phys < p.num_blocks;
+            const bool in_pool = t_begin + c * C::kT + my_tok < t_end && phys >= 0 && phys < p.num_blocks;
             bool ok = wait_or_abort(&sdone[sbuf], (c / kTcNBS) & 1);
             ok = __all_sync(0xffffffffu, ok);
             float sv[N];

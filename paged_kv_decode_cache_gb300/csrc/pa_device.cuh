@@ -140,6 +140,19 @@ __device__ __forceinline__ bool named_sync_or(int id, int nthreads, bool v) {
 
 __device__ __forceinline__ float ldcg(const float *p) { return __ldcg(p); }
 
+// Order this thread's generic global writes before later async-proxy (TMA)
+// reads of the same memory (by any thread that synchronises with it after).
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Fused cache write: does `slot` hold position L - 1 of the sequence whose
+// block at that position is `phys`?  (The fused step only writes a token it
+// will read itself.)
+__device__ __forceinline__ bool slot_is_position(int64_t slot, int phys, int pos, int bs) {
+    return slot >= 0 && phys >= 0 && slot == static_cast<int64_t>(phys) * bs + pos % bs;
+}
+
 __device__ __forceinline__ void set_status(int32_t *status, int bits) {
     if (status) atomicOr(status, bits);
 }

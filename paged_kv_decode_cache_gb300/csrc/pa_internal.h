@@ -32,6 +32,14 @@ struct DecodeParams {
     // to finish merges the group's partials into out/lse.  counters has one
     // int per (sequence, head group), zero on entry and left zero on exit.
     int32_t *counters;      // null: partials only
+    // Fused cache write (pa_decode_step): sequence b's new token, the one at
+    // position L_b - 1, is written into the pools by the CTA that reads that
+    // position, right before its TMA load of that tile.  null: no write.
+    const uint16_t *k_new;  // bf16 [B, Hkv, D]
+    const uint16_t *v_new;
+    const int64_t *slot_mapping;  // [B]
+    uint16_t *k_pool;       // the pools, writable
+    uint16_t *v_pool;
 };
 
 // CUDA-core decode kernel launch (pa_decode_cc_d*.cu).  Returns a cudaError_t.

@@ -30,31 +30,48 @@ __device__ __forceinline__ int ld_acquire_gpu(const int *p) {
     return v;
 }
 
-// One merge task: output row `row`, dims [32 * slice, 32 * slice + 32), by one warp.
+// One merge task: output row `row`, dims [32 * slice, 32 * slice + 32), by one
+// warp.  Lane i holds the LSEs of partitions i, i + 32, ... (read once); the
+// row's log-sum-exp comes from two warp reductions, each lane turns its LSEs
+// into weights, and the partial outputs are streamed with eight loads in
+// flight per lane, each weight passed along by shuffle.
 template <int D>
 __device__ __forceinline__ void merge_slice(const DecodeParams &p, int64_t row, int slice, int lane) {
+    constexpr int kMaxHeld = 8;  // LSEs per lane held in registers: P <= 256
     const int P = p.num_splits;
     const float *pl = p.part_lse + row * P;
+    float lv[kMaxHeld];
     float M = -INFINITY;
-    for (int i = lane; i < P; i += 32) M = fmaxf(M, __ldcg(pl + i));
+#pragma unroll
+    for (int k = 0; k < kMaxHeld; ++k) {
+        const int i = lane + 32 * k;
+        lv[k] = i < P ? __ldcg(pl + i) : -INFINITY;
+        M = fmaxf(M, lv[k]);
+    }
 #pragma unroll
     for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     float total = -INFINITY, acc = 0.f;
     if (M != -INFINITY) {
         float z = 0.f;
-        for (int i = lane; i < P; i += 32) z += expf(__ldcg(pl + i) - M);
+#pragma unroll
+        for (int k = 0; k < kMaxHeld; ++k) z += (lv[k] == -INFINITY) ? 0.f : expf(lv[k] - M);
 #pragma unroll
         for (int off = 16; off; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
         total = M + logf(z);
         const float *po = p.part_o + row * P * D + slice * 32 + lane;
-        for (int base = 0; base < P; base += 32) {
-            const int i = base + lane;
-            const float wl = i < P ? expf(__ldcg(pl + i) - total) : 0.f;
-            const int n = min(32, P - base);
-#pragma unroll 8
-            for (int j = 0; j < n; ++j)
-                acc = fmaf(__shfl_sync(0xffffffffu, wl, j),
-                           __ldcg(po + static_cast<int64_t>(base + j) * D), acc);
+#pragma unroll 1
+        for (int k = 0; k < kMaxHeld && 32 * k < P; ++k) {
+            const float wl = (lv[k] == -INFINITY) ? 0.f : expf(lv[k] - total);
+            const int n = min(32, P - 32 * k);
+            float part[8];
+            for (int j0 = 0; j0 < n; j0 += 8) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    part[j] = (j0 + j < n) ? __ldcg(po + static_cast<int64_t>(32 * k + j0 + j) * D) : 0.f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    acc = fmaf(__shfl_sync(0xffffffffu, wl, (j0 + j) & 31), part[j], acc);
+            }
         }
     }
     static_cast<__nv_bfloat16 *>(p.out)[row * D + slice * 32 + lane] = __float2bfloat16_rn(acc);

@@ -53,6 +53,8 @@ _SIGNATURES = {
     "pa_combine": ([_P, _P, _P, _P, _I32, _I32, _I32, _I32, _P], ctypes.c_int),
     "pa_decode_splitkv": ([_P, _P, _P, _P, _P, CacheDesc, _P, _I32, _P, _I32, _I32, _F32, _I32,
                            _P, _SZ, _P, _P], ctypes.c_int),
+    "pa_decode_step": ([_P, _P, _P, _P, _P, _P, _P, _P, CacheDesc, _P, _I32, _P, _I32, _I32, _F32,
+                        _I32, _P, _SZ, _P, _P], ctypes.c_int),
     "pa_decode_splitkv_noalloc": ([_P, _P, _P, _P, _P, CacheDesc, _P, _I32, _P, _I32, _I32, _F32,
                                    _I32, _P, _P], ctypes.c_int),
     "pa_auto_num_splits": ([_I32, _I32, _I32, _I32, _I32, _I32], ctypes.c_int),
@@ -244,6 +246,33 @@ def pa_decode_splitkv(out, lse, q, k_cache, v_cache, block_tables, seq_lens, sca
                                  _ptr(seq_lens), B, Hq, float(scale), num_splits,
                                  _ptr(workspace), ws_bytes, _ptr(status), _stream(stream))
     _check("pa_decode_splitkv", rc)
+
+
+def pa_decode_step(out, lse, q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables,
+                   seq_lens, scale, num_splits=0, workspace=None, status=None, stream=None):
+    """Fused step: write this step's new K/V through slot_mapping and run split-KV decode."""
+    B, Hq, D = _decode_inputs(q, k_cache, v_cache, block_tables, seq_lens)
+    _need(out, "out", torch.bfloat16, 3)
+    _need(k_new, "k_new", torch.bfloat16, 3)
+    _need(v_new, "v_new", torch.bfloat16, 3)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1)
+    if tuple(k_new.shape) != (B, k_cache.shape[2], D) or v_new.shape != k_new.shape:
+        raise ValueError("k_new/v_new must be [B, Hkv, D]")
+    if slot_mapping.shape[0] != B:
+        raise ValueError("slot_mapping must be [B]")
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 2)
+    ws_bytes = 0
+    if workspace is not None:
+        if not (workspace.is_cuda and workspace.is_contiguous()):
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    rc = lib().pa_decode_step(_ptr(out), _ptr(lse), _ptr(q), _ptr(k_new), _ptr(v_new),
+                              _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache), cache_desc(k_cache),
+                              _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), B, Hq,
+                              float(scale), num_splits, _ptr(workspace), ws_bytes, _ptr(status),
+                              _stream(stream))
+    _check("pa_decode_step", rc)
 
 
 PA_NOALLOC_SCRATCH_BYTES = 4 << 20

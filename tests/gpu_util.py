@@ -63,6 +63,23 @@ class Dev:
                              status=self.status)
         return out, lse, P
 
+    def step(self, num_splits=0):
+        """Fused write + decode (pa_decode_step)."""
+        w = self.w
+        P = num_splits or pa.pa_auto_num_splits(w.B, w.Hq, w.Hkv, w.D, w.max_blocks, w.block_size)
+        ws = torch.zeros(max(1, pa.pa_splitkv_workspace_bytes(w.B, w.Hq, w.D, P)),
+                         dtype=torch.uint8, device="cuda")
+        out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device="cuda")
+        pa.pa_decode_step(out, lse, self.q, self.k_new, self.v_new, self.slot_mapping, self.k_cache,
+                          self.v_cache, self.block_tables, self.seq_lens, w.scale, num_splits=P,
+                          workspace=ws, status=self.status)
+        return out, lse, P
+
+    def pools(self):
+        f = lambda t: t.view(torch.int16).cpu().numpy().view(np.uint16)
+        return f(self.k_cache), f(self.v_cache)
+
     def partial(self, P):
         w = self.w
         po = torch.empty((w.B, w.Hq, P, w.D), dtype=torch.float32, device="cuda")

@@ -182,3 +182,20 @@ def test_combine_and_write_reject_bad_arguments(lib):
     assert lib.pa_cache_write(FAKE, FAKE, FAKE, -1, FAKE, FAKE, _desc(), None, None) == pa.PA_EINVAL
     assert lib.pa_decode_partial(FAKE, FAKE, FAKE, FAKE, FAKE, _desc(), FAKE, 7, FAKE, 4, 4, 0.1,
                                  0, None, None) == pa.PA_EINVAL
+
+
+def test_decode_step_rejects_bad_arguments(lib):
+    d = _desc()
+    args = lambda **kw: [kw.get(k, FAKE) for k in ("out",)] + [None] + [
+        kw.get(k, FAKE) for k in ("q", "kn", "vn", "slots", "k", "v")]
+    base = dict(out=FAKE, q=FAKE, kn=FAKE, vn=FAKE, slots=FAKE, k=FAKE, v=FAKE)
+    for bad in ("kn", "vn", "slots"):
+        a = dict(base, **{bad: None})
+        rc = lib.pa_decode_step(a["out"], None, a["q"], a["kn"], a["vn"], a["slots"], a["k"], a["v"],
+                                d, FAKE, 7, FAKE, 4, 4, 0.125, 1, None, 0, None, None)
+        assert rc == pa.PA_EINVAL, bad
+    rc = lib.pa_decode_step(FAKE, None, FAKE, ctypes.c_void_p((1 << 20) + 8), FAKE, FAKE, FAKE, FAKE,
+                            d, FAKE, 7, FAKE, 4, 4, 0.125, 1, None, 0, None, None)
+    assert rc == pa.PA_EINVAL   # misaligned k_new
+    assert lib.pa_decode_step(None, None, None, None, None, None, None, None, d, None, 7, None, 0,
+                              4, 0.125, 1, None, 0, None, None) == pa.PA_OK   # empty batch

@@ -288,6 +288,60 @@ def test_fused_merge_reuses_its_workspace(kernel, use_kernel):
     assert_close(bf16_dev_to_f64(outs[0]), ref, f"fused merge {kernel}")
 
 
+# ----------------------------------------------------- fused write + decode
+STEP_CASES = [
+    (28, 4, 128, 16, (4096, 700, 33, 1)),
+    (12, 2, 128, 16, (1, 17, 512, 2000)),
+    (16, 8, 128, 16, (129, 2048, 1000)),
+    (16, 4, 128, 256, (300, 513, 256, 1)),
+    (4, 2, 64, 16, (1, 17, 33, 100)),
+]
+
+
+@pytest.mark.parametrize("case", STEP_CASES, ids=lambda c: f"Hq{c[0]}-Hkv{c[1]}-D{c[2]}-bs{c[3]}")
+@pytest.mark.parametrize("P", [1, 3, 0])
+def test_decode_step_equals_write_then_decode(case, P, use_kernel):
+    """pa_decode_step gives bit-for-bit the result of pa_cache_write followed by
+    pa_decode_splitkv, leaves the pools exactly as the oracle's cache write does,
+    and matches the oracle within tolerance."""
+    w = _small(*case, seed=sum(case[4]) % 997, poison_unused=True)
+    kc, vc = oracle_after_write(w)
+    ref, ref_lse = oracle.decode(w.q, kc, vc, w.block_tables, w.seq_lens, w.scale)
+    for kernel in kernels_for(w.Hq, w.Hkv, w.D):
+        use_kernel(kernel)
+        fused = Dev(w)
+        out_f, lse_f, Pf = fused.step(P)
+        two = Dev(w)
+        two.write()
+        out_t, lse_t, _ = two.splitkv(Pf)
+        torch.cuda.synchronize()
+        assert fused.status_value() == 0 and two.status_value() == 0
+        assert torch.equal(out_f, out_t) and torch.equal(lse_f, lse_t), f"{kernel} P={Pf}"
+        gk, gv = fused.pools()
+        assert np.array_equal(gk, kc) and np.array_equal(gv, vc), f"{kernel}: pools differ"
+        assert_close(bf16_dev_to_f64(out_f), ref, f"pa_decode_step {kernel} P={Pf}")
+        assert_lse_close(lse_f.cpu().double().numpy(), ref_lse, f"pa_decode_step {kernel}")
+
+
+@pytest.mark.parametrize("kernel", ["cuda_core", "tensor_core"])
+def test_decode_step_refuses_a_slot_it_does_not_read(kernel, use_kernel):
+    """A slot that is not position L - 1 of its sequence is not written and is reported;
+    a negative slot is skipped silently."""
+    use_kernel(kernel)
+    w = _small(8, 2, 128, 16, (40, 20, 70), seed=37)
+    w.slot_mapping[0] = (w.slot_mapping[0] + 3) % (w.num_blocks * w.block_size)  # wrong position
+    w.slot_mapping[1] = -1                                                    # padding
+    dev = Dev(w)
+    k0, v0 = dev.pools()
+    dev.step(2)
+    torch.cuda.synchronize()
+    assert dev.status_value() & pa.PA_STATUS_BAD_SLOT
+    gk, gv = dev.pools()
+    kc, vc = k0.copy(), v0.copy()
+    oracle.cache_write(w.k_new[2:], w.v_new[2:], w.slot_mapping[2:], kc, vc)
+    assert np.array_equal(gk, kc) and np.array_equal(gv, vc)
+
+
 def test_splitkv_small_workspace_is_rejected():
     w = _small(12, 2, 128, 16, (300,), seed=29)
     dev = Dev(w)
