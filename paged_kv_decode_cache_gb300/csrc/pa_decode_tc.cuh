@@ -180,37 +180,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             else if (p.lse) p.lse[row0 + tid] = -INFINITY;
         }
         if (p.split)
-            merge_split_group<D>(p, b * gridDim.y + blockIdx.y, part, row0, HC * G, ticket, tid,
-                                 kTcThreads, [] { __syncthreads(); });
+            merge_split_group<D, kTcThreads / 32>(p, b * gridDim.y + blockIdx.y, part, row0, HC * G,
+                                                  ticket, tid, [] { __syncthreads(); });
         return;
     }
-
-    // ---- set-up: TMEM, barriers, the Q operand, zeroed P^T buffers ---------------------
-    if (warp == 0) tc5::tmem_alloc(tmem_slot, C::kTmemCols);
-    if (tid == 0) {
-        // every barrier completes on one arrival except "S free" and "P ready",
-        // which all 128 softmax threads arrive on
-        for (int i = 0; i < C::kNumBars; ++i)
-            mbar_init(&bars[i], (&bars[i] >= sfree && &bars[i] < pready + kTcNBP) ? 128u : 1u);
-        *abort_flag = 0;
-        prefetch_tensormap(&kmap);
-        prefetch_tensormap(&vmap);
-    }
-    if (tid < N) m_ref[tid] = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < kQLoads; ++j) {  // Q operand row n = (head', q), 16-byte chunk c
-        const int i = tid + j * kTcThreads, n = i / (D / 8), c = i % (D / 8);
-        if (i < N * (D / 8))
-            *reinterpret_cast<uint4 *>(qs + (c >> 3) * (N * kSubBytes) + swz128(n, c & 7)) = qv[j];
-    }
-    for (int i = tid; i < kTcNBP * C::kPBytes / 16; i += kTcThreads)
-        reinterpret_cast<uint4 *>(ps)[i] = make_uint4(0u, 0u, 0u, 0u);
-    fence_proxy_async_smem();
-    fence_barrier_init();
-    tc5::fence_before_sync();
-    __syncthreads();
-    tc5::fence_after_sync();
-    const uint32_t tmem = *tmem_slot;
 
     auto wait_or_abort = [&](uint64_t *bar, uint32_t parity) -> bool {
         for (uint32_t i = 0; i < kWaitLimit; ++i) {
@@ -222,47 +195,51 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         return false;
     };
 
-    if (warp == kTcTmaKWarp || warp == kTcTmaVWarp) {
-        // ================= TMA producers: K ring (warp 5), V ring (warp 6) =================
-        const bool is_v = warp == kTcTmaVWarp;
-        const int nst = is_v ? NV : NK;
-        uint8_t *ring = is_v ? vring : kring;
-        uint64_t *full = is_v ? vfull : kfull;
-        uint64_t *empty = is_v ? vempty : kempty;
-        const CUtensorMap *map = is_v ? &vmap : &kmap;
-        const uint64_t policy = l2_evict_first_policy();
-        const int tile = lane >> 1, sub = lane & 1;   // lanes < 2 x tiles carry boxes
-        const bool carrier = lane < 2 * C::kTiles;
-        auto lookup = [&](int c) -> int {  // block of this lane's tile in chunk c (-1: none)
-            const int tok0 = t_begin + c * C::kT + tile * kTile;
-            return (carrier && tok0 < t_end) ? bt[tok0 / bs] : -1;
-        };
-        int phys_next = phys_first;
-        // Fused cache write: the CTA whose range holds position L - 1 writes that
-        // token's K (warp 5) or V (warp 6) rows of its HC heads into the pool just
-        // before loading the tile that holds it.  The rows are fetched up front.
-        const int last_pos = L - 1;
-        const bool writes = p.k_new && last_pos >= t_begin && last_pos < t_end;
-        constexpr int kNewChunks = HC * D / 8;                 // 16-byte chunks of HC rows
-        constexpr int kNewPerLane = (kNewChunks + 31) / 32;
-        uint4 newrow[kNewPerLane];
-        int64_t slot_b = -1;
-        if (writes) {
-            slot_b = p.slot_mapping[b];
-            const uint4 *src = reinterpret_cast<const uint4 *>(
-                (is_v ? p.v_new : p.k_new) + (static_cast<int64_t>(b) * p.num_kv_heads + g0) * D);
+    // ---- TMA producers: K ring (warp 5), V ring (warp 6) ----------------------------------
+    // Each producer initialises its own ring's barriers and issues its first
+    // stages before the CTA-wide set-up barrier (those need no "empty" wait),
+    // so the first tiles are in flight while TMEM, Q and the other barriers
+    // are set up.
+    const bool producer = warp == kTcTmaKWarp || warp == kTcTmaVWarp;
+    const bool is_v = warp == kTcTmaVWarp;
+    const int nst = is_v ? NV : NK;
+    uint8_t *ring = is_v ? vring : kring;
+    uint64_t *full = is_v ? vfull : kfull;
+    uint64_t *empty = is_v ? vempty : kempty;
+    const CUtensorMap *map = is_v ? &vmap : &kmap;
+    const int tile = lane >> 1, sub = lane & 1;   // lanes < 2 x tiles carry boxes
+    const bool carrier = lane < 2 * C::kTiles;
+    int phys_next = phys_first;
+    // Fused cache write: the CTA whose range holds position L - 1 writes that
+    // token's K (warp 5) or V (warp 6) rows of its HC heads into the pool just
+    // before loading the tile that holds it.  The rows are fetched up front.
+    const int last_pos = L - 1;
+    const bool writes = producer && p.k_new && last_pos >= t_begin && last_pos < t_end;
+    constexpr int kNewChunks = HC * D / 8;                 // 16-byte chunks of HC rows
+    constexpr int kNewPerLane = (kNewChunks + 31) / 32;
+    uint4 newrow[kNewPerLane];
+    int64_t slot_b = -1;
+    if (writes) {
+        slot_b = p.slot_mapping[b];
+        const uint4 *src = reinterpret_cast<const uint4 *>(
+            (is_v ? p.v_new : p.k_new) + (static_cast<int64_t>(b) * p.num_kv_heads + g0) * D);
 #pragma unroll
-            for (int j = 0; j < kNewPerLane; ++j)
-                if (lane + 32 * j < kNewChunks) newrow[j] = src[lane + 32 * j];
-        }
-        int issued = 0;
-        for (int c = 0; c < nch; ++c) {
+        for (int j = 0; j < kNewPerLane; ++j)
+            if (lane + 32 * j < kNewChunks) newrow[j] = src[lane + 32 * j];
+    }
+    int issued = 0;
+    // Issues chunks [c_from, c_to) of this producer's ring; false once it aborts.
+    auto produce = [&](int c_from, int c_to, uint64_t policy) -> bool {
+        for (int c = c_from; c < c_to; ++c) {
             const int s = c % nst;
             const int phys = phys_next;
-            if (c + 1 < nch) phys_next = lookup(c + 1);  // in flight while the stage drains
+            if (c + 1 < nch) {  // next chunk's block id, in flight while this stage drains
+                const int tok1 = t_begin + (c + 1) * C::kT + tile * kTile;
+                phys_next = (carrier && tok1 < t_end) ? bt[tok1 / bs] : -1;
+            }
             if (c >= nst) {
                 const bool ok = wait_or_abort(&empty[s], ((c / nst) - 1) & 1);
-                if (!__all_sync(0xffffffffu, ok)) break;
+                if (!__all_sync(0xffffffffu, ok)) return false;
             }
             const int tok0 = t_begin + c * C::kT + tile * kTile;
             bool valid = false;
@@ -293,9 +270,54 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                             phys * bs + tok0 % bs, g0, sub, &full[s], policy);
             issued = c + 1;
         }
-        if (*abort_flag && lane == 0)  // let this CTA's copies land before it leaves
-            for (int c = max(0, issued - nst); c < issued; ++c)
-                mbar_wait_bounded(&full[c % nst], (c / nst) & 1);
+        return true;
+    };
+    const int c_pre = min(nch, nst);
+    if (producer) {
+        if (lane == 0) {
+            for (int i = 0; i < nst; ++i) {
+                mbar_init(&full[i], 1u);
+                mbar_init(&empty[i], 1u);
+            }
+            fence_barrier_init();
+            prefetch_tensormap(map);
+        }
+        __syncwarp();
+        produce(0, c_pre, l2_evict_first_policy());
+    }
+
+    // ---- set-up: TMEM, barriers, the Q operand, zeroed P^T buffers ---------------------
+    if (warp == 0) tc5::tmem_alloc(tmem_slot, C::kTmemCols);
+    if (tid == 0) {
+        // the MMA / softmax barriers (the rings' are the producers'): every one
+        // completes on one arrival except "S free" and "P ready", which all 128
+        // softmax threads arrive on
+        for (uint64_t *bar = sdone; bar < pfree + kTcNBP; ++bar)
+            mbar_init(bar, (bar >= sfree && bar < pready + kTcNBP) ? 128u : 1u);
+        *abort_flag = 0;
+    }
+    if (tid < N) m_ref[tid] = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kQLoads; ++j) {  // Q operand row n = (head', q), 16-byte chunk c
+        const int i = tid + j * kTcThreads, n = i / (D / 8), c = i % (D / 8);
+        if (i < N * (D / 8))
+            *reinterpret_cast<uint4 *>(qs + (c >> 3) * (N * kSubBytes) + swz128(n, c & 7)) = qv[j];
+    }
+    for (int i = tid; i < kTcNBP * C::kPBytes / 16; i += kTcThreads)
+        reinterpret_cast<uint4 *>(ps)[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+    fence_barrier_init();
+    tc5::fence_before_sync();
+    __syncthreads();
+    tc5::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (producer) {
+        if (produce(c_pre, nch, l2_evict_first_policy()) == false || *abort_flag) {
+            if (lane == 0)  // let this CTA's copies land before it leaves
+                for (int c = max(0, issued - nst); c < issued; ++c)
+                    mbar_wait_bounded(&full[c % nst], (c / nst) & 1);
+        }
     } else if (warp == kTcQkWarp) {
         // ================= QK issuer =================
         if (lane == 0) {
@@ -499,13 +521,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                 else if (p.lse) p.lse[r] = lse;
             }
         }
-        if (p.split)
-            merge_split_group<D>(p, b * gridDim.y + blockIdx.y, part, row0, HC * G, ticket, tid,
-                                 128, [] { named_sync(1, 128); });
     }
     tc5::fence_before_sync();
     __syncthreads();
     if (warp == 0) tc5::tmem_free(tmem, C::kTmemCols);
+    if (p.split)  // all eight warps share the merge
+        merge_split_group<D, kTcThreads / 32>(p, b * gridDim.y + blockIdx.y, part, row0, HC * G, ticket,
+                                              tid, [] { __syncthreads(); });
 }
 
 template <int HC, int GP>

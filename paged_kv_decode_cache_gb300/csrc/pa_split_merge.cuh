@@ -11,7 +11,7 @@
 //      row, 32-dim slice) goes to warp k of the group's P x nwarps warps; a
 //      task computes the row's log-sum-exp over the P partial LSEs and sums
 //      the weighted partial outputs of its slice (partials are read with
-//      L1-bypassing loads);
+//      L1-bypassing loads, all of a block of 32 partitions in flight at once);
 //   4. each CTA increments the group's departure counter; the last one puts
 //      both counters back to zero for the next call.
 // A wait that runs out sets PA_STATUS_TIMEOUT and the CTA skips the merge.
@@ -31,23 +31,24 @@ __device__ __forceinline__ int ld_acquire_gpu(const int *p) {
 }
 
 // One merge task: output row `row`, dims [32 * slice, 32 * slice + 32), by one
-// warp.  Lane i holds the LSEs of partitions i, i + 32, ... (read once); the
-// row's log-sum-exp comes from two warp reductions, each lane turns its LSEs
-// into weights, and the partial outputs are streamed with eight loads in
-// flight per lane, each weight passed along by shuffle.
+// warp.  Lane i holds the LSEs of partitions i, i + 32, ... ; the LSEs and the
+// first 32 partitions' outputs are loaded together (one round trip for
+// P <= 32), the row's log-sum-exp comes from two warp reductions, and each
+// further block of 32 partitions is loaded while the previous one is summed.
 template <int D>
 __device__ __forceinline__ void merge_slice(const DecodeParams &p, int64_t row, int slice, int lane) {
     constexpr int kMaxHeld = 8;  // LSEs per lane held in registers: P <= 256
     const int P = p.num_splits;
     const float *pl = p.part_lse + row * P;
-    float lv[kMaxHeld];
+    const float *po = p.part_o + row * P * D + slice * 32 + lane;
+    float lv[kMaxHeld], cur[32];
+#pragma unroll
+    for (int k = 0; k < kMaxHeld; ++k) lv[k] = lane + 32 * k < P ? __ldcg(pl + lane + 32 * k) : -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) cur[j] = j < P ? __ldcg(po + static_cast<int64_t>(j) * D) : 0.f;
     float M = -INFINITY;
 #pragma unroll
-    for (int k = 0; k < kMaxHeld; ++k) {
-        const int i = lane + 32 * k;
-        lv[k] = i < P ? __ldcg(pl + i) : -INFINITY;
-        M = fmaxf(M, lv[k]);
-    }
+    for (int k = 0; k < kMaxHeld; ++k) M = fmaxf(M, lv[k]);
 #pragma unroll
     for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     float total = -INFINITY, acc = 0.f;
@@ -58,19 +59,25 @@ __device__ __forceinline__ void merge_slice(const DecodeParams &p, int64_t row, 
 #pragma unroll
         for (int off = 16; off; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
         total = M + logf(z);
-        const float *po = p.part_o + row * P * D + slice * 32 + lane;
 #pragma unroll 1
         for (int k = 0; k < kMaxHeld && 32 * k < P; ++k) {
-            const float wl = (lv[k] == -INFINITY) ? 0.f : expf(lv[k] - total);
-            const int n = min(32, P - 32 * k);
-            float part[8];
-            for (int j0 = 0; j0 < n; j0 += 8) {
+            const int next = 32 * (k + 1);
+            float nxt[32];
+            if (next < P) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    part[j] = (j0 + j < n) ? __ldcg(po + static_cast<int64_t>(32 * k + j0 + j) * D) : 0.f;
+                for (int j = 0; j < 32; ++j)
+                    nxt[j] = next + j < P ? __ldcg(po + static_cast<int64_t>(next + j) * D) : 0.f;
+            }
+            float lk = lv[0];
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    acc = fmaf(__shfl_sync(0xffffffffu, wl, (j0 + j) & 31), part[j], acc);
+            for (int i = 1; i < kMaxHeld; ++i)
+                if (i == k) lk = lv[i];
+            const float wl = (lk == -INFINITY) ? 0.f : expf(lk - total);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc = fmaf(__shfl_sync(0xffffffffu, wl, j), cur[j], acc);
+            if (next < P) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) cur[j] = nxt[j];
             }
         }
     }
@@ -78,16 +85,13 @@ __device__ __forceinline__ void merge_slice(const DecodeParams &p, int64_t row, 
     if (slice == 0 && lane == 0 && p.lse) p.lse[row] = total;
 }
 
-// Merge tasks are spread over kMergeWarps warps per CTA, whatever the caller's
-// thread count, so every CTA of a group agrees on who does which task.
-constexpr int kMergeWarps = 4;
-
-// Called by all `nt` threads (whole warps, index t, nt >= 32 * kMergeWarps)
-// of a CTA after its partials for rows [row_first, row_first + nrows) are
-// written; `sync` synchronises those threads; `flag` is a shared int.
-template <int D, typename Sync>
+// Called by all 32 x kWarps threads (index t) of a CTA after its partials for
+// rows [row_first, row_first + nrows) are written; `sync` synchronises those
+// threads; `flag` is a shared int.  Every CTA of a group launches the same
+// kernel, so all agree on kWarps and hence on who does which task.
+template <int D, int kWarps, typename Sync>
 __device__ void merge_split_group(const DecodeParams &p, int group, int part, int64_t row_first,
-                                  int nrows, int *flag, int t, int nt, Sync sync) {
+                                  int nrows, int *flag, int t, Sync sync) {
     if (!p.counters) return;
     int *arrive = p.counters + 2 * group, *depart = arrive + 1;
     const int P = p.num_splits;
@@ -101,7 +105,6 @@ __device__ void merge_split_group(const DecodeParams &p, int group, int part, in
                 ok = true;
                 break;
             }
-            __nanosleep(64);
         }
         if (!ok) set_status(p.status, PA_STATUS_TIMEOUT);
         *flag = ok;
@@ -111,9 +114,8 @@ __device__ void merge_split_group(const DecodeParams &p, int group, int part, in
         __threadfence();
         const int warp = t >> 5, lane = t & 31;
         const int tasks = nrows * (D / 32);
-        if (warp < kMergeWarps)
-            for (int k = part * kMergeWarps + warp; k < tasks; k += P * kMergeWarps)
-                merge_slice<D>(p, row_first + k / (D / 32), k % (D / 32), lane);
+        for (int k = part * kWarps + warp; k < tasks; k += P * kWarps)
+            merge_slice<D>(p, row_first + k / (D / 32), k % (D / 32), lane);
     }
     sync();
     if (t == 0 && atomicAdd(depart, 1) == P - 1) {
