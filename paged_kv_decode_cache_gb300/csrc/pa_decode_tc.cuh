@@ -63,6 +63,8 @@ constexpr int kTcPvWarp = 7;
 constexpr int kTcNBS = 4;              // S buffers in TMEM
 constexpr int kTcNBP = 2;              // P^T buffers in shared memory
 constexpr float kTcLazyTau = 8.0f;     // log2 headroom before a reference max moves
+constexpr int kTcLook = 4;             // chunks a producer's block-id lookups run ahead
+constexpr int kTcMaskRing = 8;         // chunk validity masks the K producer publishes
 
 template <int HC, int GP>
 struct TcCfg {
@@ -86,7 +88,13 @@ struct TcCfg {
     static constexpr int kRedBytes = (kTcRows * GP + 3 * kN) * 4 + 16;
     static constexpr int kBarOff = (kRedOff + kRedBytes + 7) / 8 * 8;
     static constexpr int kNumBars = 2 * kNK + 2 * kNV + 2 * kTcNBS + 2 * kTcNBP;
-    static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 1024;
+    // validity masks [kTcMaskRing] (u64: chunk << 32 | lane mask), then the two
+    // producers' block-id rings [2][kTcLook + 1][32 lanes]
+    static constexpr int kMaskOff = kBarOff + kNumBars * 8;
+    static constexpr int kLookOff = kMaskOff + kTcMaskRing * 8;
+    static constexpr int kSmemBytes = kLookOff + 2 * (kTcLook + 1) * 32 * 4 + 1024;
+    // the K producer rewrites mask slot c % ring only once softmax c has read it
+    static_assert(kNK + kTcNBS <= kTcMaskRing, "mask ring");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory");
     static constexpr uint32_t kTmemCols = (kTcNBS + 1) * kN <= 128 ? 128u
                                           : (kTcNBS + 1) * kN <= 256 ? 256u : 512u;
@@ -133,14 +141,16 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     uint64_t *kfull = bars, *kempty = bars + NK, *vfull = bars + 2 * NK, *vempty = vfull + NV;
     uint64_t *sdone = vempty + NV, *sfree = sdone + kTcNBS, *pready = sfree + kTcNBS;
     uint64_t *pfree = pready + kTcNBP;
+    volatile uint64_t *mask_ring = reinterpret_cast<volatile uint64_t *>(smem + C::kMaskOff);
+    int *look_ring = reinterpret_cast<int *>(smem + C::kLookOff);  // [2][kTcLook + 1][32]
 
     const int part = blockIdx.x, g0 = blockIdx.y * HC, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int bs = p.block_size;
 
     // Global reads that do not depend on the sequence length go out first, so
-    // their latencies overlap: the length, this CTA's queries, and the block
-    // ids of its first chunk (for this thread's role).
+    // their latencies overlap: the length, this CTA's queries, and (producer
+    // lanes) the block ids of the first kTcLook chunks.
     const int lmax = p.max_blocks * bs;
     const int t_begin = part * p.chunk;
     const int t_lim = min(t_begin + p.chunk, lmax);  // range end before the length is known
@@ -156,11 +166,42 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         if (i < N * (D / 8) && n % GP < G)
             qv[j] = *reinterpret_cast<const uint4 *>(p.q + (row0 + (n / GP) * G + n % GP) * D + c * 8);
     }
-    // token offset, within a chunk, whose block id this thread looks up
-    const int my_tok = (warp == kTcTmaKWarp || warp == kTcTmaVWarp)
-                           ? (lane < 2 * C::kTiles ? (lane >> 1) * kTile : -1)
-                           : (warp < 4 ? (tid / (kTile * HC)) * kTile + (tid & 15) : -1);
-    const int phys_first = (my_tok >= 0 && t_begin + my_tok < t_lim) ? bt[(t_begin + my_tok) / bs] : -1;
+    // Block ids reach the TMA producers through cp.async copies into a small
+    // ring, kTcLook chunks ahead of use, so no issue waits on a lookup that is
+    // queued behind the KV stream.  Lanes 2 * tile + sub of a producer carry
+    // tile `tile` of a chunk; both lanes of a tile look its block up.
+    const bool producer = warp == kTcTmaKWarp || warp == kTcTmaVWarp;
+    const bool is_v = warp == kTcTmaVWarp;
+    const int tile = lane >> 1, sub = lane & 1;
+    const bool carrier = producer && lane < 2 * C::kTiles;
+    int *my_look = look_ring + (is_v ? (kTcLook + 1) * 32 : 0) + lane;  // slot j at my_look[32 * j]
+    auto look_ahead = [&](int c, int t_stop) {  // copy chunk c's block id; one commit group per chunk
+        const int tok0 = t_begin + c * C::kT + tile * kTile;
+        if (carrier && tok0 < t_stop) cp_async_4(my_look + 32 * (c % (kTcLook + 1)), bt + tok0 / bs);
+        cp_async_commit();
+    };
+    if (producer) {
+#pragma unroll
+        for (int c = 0; c < kTcLook; ++c) look_ahead(c, t_lim);
+    }
+    if (warp == kTcPvWarp && lane < 4) {
+        // The epilogue and the merge first touch the outputs after the KV
+        // stream has filled the memory queues; touching them now takes their
+        // address translations off that path.
+        const void *touch = nullptr;
+        const int64_t last = row0 + static_cast<int64_t>(HC) * G - 1;
+        const __nv_bfloat16 *out_rows = static_cast<const __nv_bfloat16 *>(p.out) + row0 * D;
+        if (p.split) {
+            if (lane == 0) touch = p.part_o + (row0 * p.num_splits + part) * D;
+            if (lane == 1) touch = p.part_o + (last * p.num_splits + part) * D;
+            if (lane == 2) touch = p.part_lse + row0 * p.num_splits + part;
+            if (lane == 3 && p.counters && p.out) touch = out_rows;  // the merge writes out
+        } else {
+            if (lane == 0) touch = out_rows;
+            if (lane == 1 && p.lse) touch = p.lse + row0;
+        }
+        if (touch) prefetch_l2(touch);
+    }
     if (L < 0 || L > lmax) {
         if (tid == 0 && part == 0 && g0 == 0) set_status(p.status, PA_STATUS_BAD_SEQLEN);
         L = L < 0 ? 0 : lmax;
@@ -169,6 +210,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     const int nch = t_end > t_begin ? (t_end - t_begin + C::kT - 1) / C::kT : 0;
 
     if (nch == 0) {  // empty range: zero output, lse = -inf
+        cp_async_wait<0>();
         for (int i = tid; i < HC * G * D; i += kTcThreads) {
             const int64_t r = row0 + i / D;
             const int d = i % D;
@@ -200,16 +242,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     // stages before the CTA-wide set-up barrier (those need no "empty" wait),
     // so the first tiles are in flight while TMEM, Q and the other barriers
     // are set up.
-    const bool producer = warp == kTcTmaKWarp || warp == kTcTmaVWarp;
-    const bool is_v = warp == kTcTmaVWarp;
     const int nst = is_v ? NV : NK;
     uint8_t *ring = is_v ? vring : kring;
     uint64_t *full = is_v ? vfull : kfull;
     uint64_t *empty = is_v ? vempty : kempty;
     const CUtensorMap *map = is_v ? &vmap : &kmap;
-    const int tile = lane >> 1, sub = lane & 1;   // lanes < 2 x tiles carry boxes
-    const bool carrier = lane < 2 * C::kTiles;
-    int phys_next = phys_first;
     // Fused cache write: the CTA whose range holds position L - 1 writes that
     // token's K (warp 5) or V (warp 6) rows of its HC heads into the pool just
     // before loading the tile that holds it.  The rows are fetched up front.
@@ -232,11 +269,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     auto produce = [&](int c_from, int c_to, uint64_t policy) -> bool {
         for (int c = c_from; c < c_to; ++c) {
             const int s = c % nst;
-            const int phys = phys_next;
-            if (c + 1 < nch) {  // next chunk's block id, in flight while this stage drains
-                const int tok1 = t_begin + (c + 1) * C::kT + tile * kTile;
-                phys_next = (carrier && tok1 < t_end) ? bt[tok1 / bs] : -1;
-            }
+            look_ahead(c + kTcLook, t_end);  // (an empty group past the range)
+            cp_async_wait<kTcLook>();        // chunk c's copy has landed
+            const int phys = carrier ? my_look[32 * (c % (kTcLook + 1))] : -1;
             if (c >= nst) {
                 const bool ok = wait_or_abort(&empty[s], ((c / nst) - 1) & 1);
                 if (!__all_sync(0xffffffffu, ok)) return false;
@@ -248,6 +283,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                 else if (!is_v && sub == 0) set_status(p.status, PA_STATUS_BAD_BLOCK);
             }
             const uint32_t vm = __ballot_sync(0xffffffffu, valid);
+            // publish which tiles of chunk c are loaded (bit 2 * tile) for the softmax
+            if (!is_v && lane == 0) mask_ring[c % kTcMaskRing] = (static_cast<uint64_t>(c) << 32) | vm;
             const int chunk0 = t_begin + c * C::kT;
             if (writes && last_pos >= chunk0 && last_pos < chunk0 + C::kT) {  // holds position L - 1
                 const int ph = __shfl_sync(0xffffffffu, phys, 2 * ((last_pos - chunk0) / kTile));
@@ -279,6 +316,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                 mbar_init(&full[i], 1u);
                 mbar_init(&empty[i], 1u);
             }
+            if (!is_v)  // no chunk's tag yet
+                for (int i = 0; i < kTcMaskRing; ++i) mask_ring[i] = ~uint64_t(0);
             fence_barrier_init();
             prefetch_tensormap(map);
         }
@@ -313,7 +352,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     const uint32_t tmem = *tmem_slot;
 
     if (producer) {
-        if (produce(c_pre, nch, l2_evict_first_policy()) == false || *abort_flag) {
+        const bool done = produce(c_pre, nch, l2_evict_first_policy());
+        cp_async_wait<0>();
+        if (!done || *abort_flag) {
             if (lane == 0)  // let this CTA's copies land before it leaves
                 for (int c = max(0, issued - nst); c < issued; ++c)
                     mbar_wait_bounded(&full[c % nst], (c / nst) & 1);
@@ -377,18 +418,30 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         for (int q = 0; q < GP; ++q) l_thr[q] = 0.f;
         const float sl2 = p.scale_log2;
         bool dead = false;
-        auto lookup = [&](int c) -> int {  // block of this row's token in chunk c (-1: none)
-            const int tok = t_begin + c * C::kT + my_tok;
-            return tok < t_end ? bt[tok / bs] : -1;
-        };
-        int phys_next = phys_first;
+        const int my_tile = tid / (kTile * HC);              // tile of row m = tid
+        const int my_tok = my_tile * kTile + (tid & 15);     // its token's offset in a chunk
         for (int c = 0; c < nch; ++c) {
             const int sbuf = c % kTcNBS, pbuf = c % kTcNBP;
-            const int phys = phys_next;
-            if (c + 1 < nch) phys_next = lookup(c + 1);  // one chunk ahead
-            const bool in_pool = t_begin + c * C::kT + my_tok < t_end && phys >= 0 && phys < p.num_blocks;
             bool ok = wait_or_abort(&sdone[sbuf], (c / kTcNBS) & 1);
+            // the K producer wrote chunk c's mask before its loads, hence before S c
+            uint64_t mk = 0;
+            if (ok) {
+                uint32_t i = 0;
+                for (; i < kWaitLimit; ++i) {
+                    mk = mask_ring[c % kTcMaskRing];
+                    if (static_cast<uint32_t>(mk >> 32) == static_cast<uint32_t>(c) || *abort_flag) break;
+                }
+                if (static_cast<uint32_t>(mk >> 32) != static_cast<uint32_t>(c)) {
+                    ok = false;
+                    if (i == kWaitLimit) {
+                        *abort_flag = 1;
+                        set_status(p.status, PA_STATUS_TIMEOUT);
+                    }
+                }
+            }
             ok = __all_sync(0xffffffffu, ok);
+            const bool in_pool =
+                t_begin + c * C::kT + my_tok < t_end && ((static_cast<uint32_t>(mk) >> (2 * my_tile)) & 1u);
             float sv[N];
             if (ok) {
                 tc5::fence_after_sync();
@@ -493,24 +546,31 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
 #pragma unroll
         for (int q = 0; q < GP; ++q) red[tid * GP + q] = l_thr[q];
         named_sync(1, 128);
-        if (tid < N) col[tid] = column_reduce<HC, GP, false>(red, tid);
-        named_sync(1, 128);  // col[] complete before it is read
+        if (tid < N) {  // row sum of column n, and its reciprocal (alpha_s is free now)
+            const float lsum = column_reduce<HC, GP, false>(red, tid);
+            col[tid] = lsum;
+            alpha_s[tid] = 1.f / lsum;
+        }
+        named_sync(1, 128);  // col[] / alpha_s complete before they are read
         if (okf) {
             tc5::fence_after_sync();
-            // O^T row d = tid, 16 columns at a time, normalised and stored
+            // O^T row d = tid, 16 columns at a time, normalised and stored; column
+            // n = (head hh, query q) goes to the CTA's output row hh * G + q
+            const int64_t stride = p.split ? static_cast<int64_t>(p.num_splits) * D : D;
+            float *of = p.split ? p.part_o + (row0 * p.num_splits + part) * D + tid : nullptr;
+            __nv_bfloat16 *oh = p.split ? nullptr : static_cast<__nv_bfloat16 *>(p.out) + row0 * D + tid;
 #pragma unroll 1
             for (int k = 0; k < N / 16; ++k) {
                 float ov[16];
                 tc5::ld_32x32b_x16(tc5::taddr(tmem, 32 * warp, C::kColO + 16 * k), ov);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const int n = 16 * k + i, hh = n / GP, q = n % GP;
+                    const int n = 16 * k + i, q = n % GP;
                     if (q >= G) continue;
-                    const float lsum = col[n];
-                    const float o = ov[i] / lsum;
-                    const int64_t r = row0 + hh * G + q;
-                    if (p.split) p.part_o[(r * p.num_splits + part) * D + tid] = o;
-                    else static_cast<__nv_bfloat16 *>(p.out)[r * D + tid] = __float2bfloat16_rn(o);
+                    const float o = ov[i] * alpha_s[n];
+                    const int64_t off = ((n / GP) * G + q) * stride;
+                    if (p.split) of[off] = o;
+                    else oh[off] = __float2bfloat16_rn(o);
                 }
             }
             if (tid < N && tid % GP < G) {

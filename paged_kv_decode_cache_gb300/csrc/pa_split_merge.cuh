@@ -8,10 +8,11 @@
 //      increments the group's arrival counter;
 //   2. it waits (bounded) until the counter reads P: every partial exists;
 //   3. the group's CTAs split the merge between them: merge task k = (output
-//      row, 32-dim slice) goes to warp k of the group's P x nwarps warps; a
-//      task computes the row's log-sum-exp over the P partial LSEs and sums
-//      the weighted partial outputs of its slice (partials are read with
-//      L1-bypassing loads, all of a block of 32 partitions in flight at once);
+//      row, dim slice) goes to warp k of the group's P x nwarps warps; a task
+//      computes the row's log-sum-exp over the P partial LSEs and sums the
+//      weighted partial outputs of its slice (partials are read with
+//      L1-bypassing loads).  Up to 32 partitions a lane owns a dim of a 32-dim
+//      slice; beyond, a lane owns partitions of an 8-dim slice;
 //   4. each CTA increments the group's departure counter; the last one puts
 //      both counters back to zero for the next call.
 // A wait that runs out sets PA_STATUS_TIMEOUT and the CTA skips the merge.
@@ -85,6 +86,70 @@ __device__ __forceinline__ void merge_slice(const DecodeParams &p, int64_t row, 
     if (slice == 0 && lane == 0 && p.lse) p.lse[row] = total;
 }
 
+// Merge task for many partitions (P > 32): output row `row`, dims
+// [8 * slice, 8 * slice + 8), by one warp whose lane i takes partitions i,
+// i + 32, ... : every LSE and partial output the lane needs is loaded at once
+// (one round trip), the lane sums its own weighted partials, and one warp
+// reduction per dim adds the lanes' sums.
+template <int D>
+__device__ __forceinline__ void merge_slice_wide(const DecodeParams &p, int64_t row, int slice, int lane) {
+    constexpr int kMaxHeld = 8;  // partitions per lane: P <= 256
+    const int P = p.num_splits;
+    const float *pl = p.part_lse + row * P;
+    const float *po = p.part_o + row * P * D + slice * 8;
+    float lv[kMaxHeld];
+    float4 lo[kMaxHeld], hi[kMaxHeld];
+#pragma unroll
+    for (int k = 0; k < kMaxHeld; ++k) {
+        const int i = lane + 32 * k;
+        lv[k] = -INFINITY;
+        lo[k] = hi[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i < P) {
+            lv[k] = __ldcg(pl + i);
+            lo[k] = __ldcg(reinterpret_cast<const float4 *>(po + static_cast<int64_t>(i) * D));
+            hi[k] = __ldcg(reinterpret_cast<const float4 *>(po + static_cast<int64_t>(i) * D + 4));
+        }
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < kMaxHeld; ++k) M = fmaxf(M, lv[k]);
+#pragma unroll
+    for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float total = -INFINITY, acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (M != -INFINITY) {
+        float z = 0.f;
+#pragma unroll
+        for (int k = 0; k < kMaxHeld; ++k) z += (lv[k] == -INFINITY) ? 0.f : expf(lv[k] - M);
+#pragma unroll
+        for (int off = 16; off; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+        total = M + logf(z);
+#pragma unroll
+        for (int k = 0; k < kMaxHeld; ++k) {
+            const float w = (lv[k] == -INFINITY) ? 0.f : expf(lv[k] - total);
+            acc[0] = fmaf(w, lo[k].x, acc[0]);
+            acc[1] = fmaf(w, lo[k].y, acc[1]);
+            acc[2] = fmaf(w, lo[k].z, acc[2]);
+            acc[3] = fmaf(w, lo[k].w, acc[3]);
+            acc[4] = fmaf(w, hi[k].x, acc[4]);
+            acc[5] = fmaf(w, hi[k].y, acc[5]);
+            acc[6] = fmaf(w, hi[k].z, acc[6]);
+            acc[7] = fmaf(w, hi[k].w, acc[7]);
+        }
+#pragma unroll
+        for (int off = 16; off; off >>= 1)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], off);
+    }
+    if (lane == 0) {
+        __nv_bfloat162 o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) o[j] = __floats2bfloat162_rn(acc[2 * j], acc[2 * j + 1]);
+        *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) + row * D + slice * 8) =
+            *reinterpret_cast<const uint4 *>(o);
+        if (slice == 0 && p.lse) p.lse[row] = total;
+    }
+}
+
 // Called by all 32 x kWarps threads (index t) of a CTA after its partials for
 // rows [row_first, row_first + nrows) are written; `sync` synchronises those
 // threads; `flag` is a shared int.  Every CTA of a group launches the same
@@ -113,9 +178,15 @@ __device__ void merge_split_group(const DecodeParams &p, int group, int part, in
     if (*flag) {
         __threadfence();
         const int warp = t >> 5, lane = t & 31;
-        const int tasks = nrows * (D / 32);
-        for (int k = part * kWarps + warp; k < tasks; k += P * kWarps)
-            merge_slice<D>(p, row_first + k / (D / 32), k % (D / 32), lane);
+        if (P <= 32) {  // lanes over dims: one round trip per 32-dim slice
+            const int tasks = nrows * (D / 32);
+            for (int k = part * kWarps + warp; k < tasks; k += P * kWarps)
+                merge_slice<D>(p, row_first + k / (D / 32), k % (D / 32), lane);
+        } else {        // lanes over partitions: one round trip per 8-dim slice
+            const int tasks = nrows * (D / 8);
+            for (int k = part * kWarps + warp; k < tasks; k += P * kWarps)
+                merge_slice_wide<D>(p, row_first + k / (D / 8), k % (D / 8), lane);
+        }
     }
     sync();
     if (t == 0 && atomicAdd(depart, 1) == P - 1) {

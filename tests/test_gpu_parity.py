@@ -135,6 +135,24 @@ def test_partials_match_oracle_partials(P, kernel, use_kernel):
     assert_lse_close(pl.cpu().double().numpy(), rl, "partial lse")
 
 
+@pytest.mark.parametrize("lens,P", [((1500,), 33), ((1500,), 100), ((1500,), 150), ((700, 1500), 60)])
+def test_fused_merge_many_partitions(lens, P, use_kernel):
+    """More than 32 partitions per row (the merge's partition-parallel tasks),
+    some of them empty past the sequence end; few sequences, so the cooperative
+    grid fits and the merge runs inside the decode launch."""
+    w = _small(12, 2, 128, 16, lens, seed=P)
+    kc, vc = oracle_after_write(w)
+    ref, ref_lse = oracle.decode(w.q, kc, vc, w.block_tables, w.seq_lens, w.scale)
+    for kernel in kernels_for(w.Hq, w.Hkv, w.D):
+        use_kernel(kernel)
+        dev = Dev(w)
+        dev.write()
+        so, sl, _ = dev.splitkv(P)
+        assert_close(bf16_dev_to_f64(so), ref, f"splitkv P={P} {kernel}")
+        assert_lse_close(sl.cpu().double().numpy(), ref_lse, f"splitkv P={P} {kernel}")
+        assert dev.status_value() == 0
+
+
 def test_combine_matches_oracle():
     g = torch.Generator().manual_seed(3)
     B, Hq, P, D = 3, 5, 9, 128
