@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU work for the oracle baseline sample")
     ap.add_argument("--e2e-steps", type=int, default=0, help="0 = min(steps, 500)")
+    ap.add_argument("--ref-seconds", type=float, default=150.0,
+                    help="total oracle time of --impl reference, spread over its steps")
     ap.add_argument("--unfused", action="store_true",
                     help="time pa_cache_write + pa_decode_splitkv instead of pa_decode_step")
     return ap.parse_args()
@@ -239,7 +241,7 @@ def run_reference(args, world, rank):
         return
     from paged_kv_decode_cache_gb300 import workloads as W
     w = W.WORKLOADS[args.workload]()
-    budget_per_step = max(0.005, 150.0 / max(1, args.steps + args.warmup))
+    budget_per_step = max(0.005, args.ref_seconds / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
         time_oracle(w, budget_per_step)
     secs = byts = 0.0
