@@ -60,6 +60,8 @@ def _bind(lib):
     lib.oracle_decode_partial.argtypes = [P, P, P, P, P, i32, i32, i32, i32,
                                           P, i32, P, i32, i32, f32, i32, i32, P, i32]
     lib.oracle_combine.argtypes = [P, P, P, P, i64, i32, i32]
+    lib.oracle_decode_mq.argtypes = [P, P, P, i32, P, P, i32, i32, i32, i32, P, i32, P, i32, i32,
+                                     f32, P, i32]
     lib.oracle_max_threads.argtypes = []
     for fn in (lib.oracle_cache_write, lib.oracle_decode_rows,
                lib.oracle_decode_partial, lib.oracle_combine, lib.oracle_max_threads):
@@ -188,6 +190,25 @@ def decode(q, k_cache, v_cache, block_tables, seq_lens, scale, nthreads: int = 0
     out, lse = decode_rows(q, k_cache, v_cache, block_tables, seq_lens, scale,
                            bb.ravel(), hh.ravel(), nthreads)
     return out.reshape(B, Hq, D), lse.reshape(B, Hq)
+
+
+def decode_mq(q, k_cache, v_cache, block_tables, seq_lens, scale, nthreads: int = 0):
+    """Causal multi-query attention: q is [B, q_len, Hq, D] (the last q_len
+    positions of each sequence); returns (out[B, q_len, Hq, D], lse[B, q_len, Hq])."""
+    q = _req(q, np.uint16)
+    B, q_len, Hq, D = q.shape
+    _, k_cache, v_cache, block_tables, seq_lens, _, _, _, nb, bs, hkv = _common(
+        q[:, 0], k_cache, v_cache, block_tables, seq_lens)
+    out = np.empty((B, q_len, Hq, D), np.float64)
+    lse = np.empty((B, q_len, Hq), np.float64)
+    nthr = nthreads if nthreads > 0 else max_threads()
+    scores = np.empty((max(nthr, max_threads()), block_tables.shape[1] * bs), np.float64)
+    rc = _load().oracle_decode_mq(_ptr(out), _ptr(lse), _ptr(q), q_len, _ptr(k_cache),
+                                  _ptr(v_cache), nb, bs, hkv, D, _ptr(block_tables),
+                                  block_tables.shape[1], _ptr(seq_lens), B, Hq, float(scale),
+                                  _ptr(scores), nthreads)
+    _check(rc, "oracle_decode_mq")
+    return out, lse
 
 
 def decode_partial(q, k_cache, v_cache, block_tables, seq_lens, scale, num_parts, chunk,

@@ -206,6 +206,59 @@ int oracle_decode_rows(double *out, double *lse,
 }
 
 /*
+ * Multi-query decode: the last q_len tokens of each sequence are this step's
+ * queries (speculative verification of drafted tokens, or a chunk of new
+ * tokens), already written into the pool.  The pages name both uses
+ * ("mini-infer" psmarter write-up, feature list items 3 and 5: chunked
+ * prefill, speculative decoding; "mini-infer" prajwal7-2002 docs, table
+ * "Core Capabilities at a Glance", row "Prompt Ingestion": 512-token chunks,
+ * and its overview of a draft model's tokens verified in parallel by the
+ * target) without giving the masking rule; the plainest reading is causal
+ * attention: query i of sequence b sits at position
+ * L - q_len + i (L = seq_lens[b]) and attends to tokens [0, L - q_len + i].
+ * A query at a negative position (L < q_len) sees no token: out = 0,
+ * lse = -inf.  q and out are [B, q_len, Hq, D]; lse is [B, q_len, Hq]
+ * (nullable).
+ */
+int oracle_decode_mq(double *out, double *lse,
+                     const uint16_t *q, int q_len, const uint16_t *k_cache, const uint16_t *v_cache,
+                     int num_blocks, int block_size, int num_kv_heads, int head_dim,
+                     const int32_t *block_tables, int max_blocks, const int32_t *seq_lens,
+                     int B, int Hq, float scale, double *scores, int nthreads) {
+    if (B <= 0 || q_len <= 0 || Hq <= 0 || num_kv_heads <= 0 || Hq % num_kv_heads != 0 ||
+        head_dim <= 0 || block_size <= 0 || max_blocks <= 0)
+        return ORACLE_EBADARG;
+    int rc = check_tables(block_tables, max_blocks, seq_lens, B, num_blocks, block_size);
+    if (rc) return rc;
+    const int group = Hq / num_kv_heads;
+    const int64_t lmax = (int64_t)max_blocks * block_size;
+    const int64_t n_rows = (int64_t)B * q_len * Hq;
+    const int nt = team_size(nthreads);
+#pragma omp parallel num_threads(nt)
+    {
+        int tid = 0;
+#ifdef _OPENMP
+        tid = omp_get_thread_num();
+#endif
+        double *my_scores = scores + (int64_t)tid * lmax;
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < n_rows; ++r) {  /* r = (b * q_len + i) * Hq + h */
+            const int h = (int)(r % Hq);
+            const int i = (int)((r / Hq) % q_len);
+            const int b = (int)(r / ((int64_t)Hq * q_len));
+            int visible = seq_lens[b] - q_len + i + 1;  /* tokens [0, position] */
+            if (visible < 0) visible = 0;
+            const double l = attend_range(out + r * head_dim, q + r * head_dim, k_cache, v_cache,
+                                          block_tables + (int64_t)b * max_blocks, 0, visible,
+                                          block_size, num_kv_heads, head_dim, h / group,
+                                          (double)scale, my_scores);
+            if (lse) lse[r] = l;
+        }
+    }
+    return ORACLE_OK;
+}
+
+/*
  * Split-K / split-KV partials (psmarter write-up, feature 7; tom-jerr
  * "Attention Backend" table).  Partition p of sequence b covers tokens
  * [p*chunk, min((p+1)*chunk, L)); part_o is [B, Hq, P, D] and part_lse is

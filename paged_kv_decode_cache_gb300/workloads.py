@@ -13,6 +13,9 @@ physically scattered.  Unused table entries are -1.
 
 The step is "write then attend": sequence b's new token sits at position
 L_b - 1 and is written through ``slot_mapping`` before attention reads it.
+With ``q_len`` > 1 (speculative verification, or a chunk of new tokens) the
+last q_len positions of each sequence are new: q is [B, q_len, Hq, D] and the
+write covers all of them.
 """
 from __future__ import annotations
 
@@ -38,13 +41,14 @@ class DecodeWorkload:
     max_blocks: int
     seq_lens: np.ndarray       # [B] int32, includes the token written this step
     block_tables: np.ndarray   # [B, max_blocks] int32, -1 padded
-    q: np.ndarray              # [B, Hq, D] uint16 (bf16 bits)
+    q: np.ndarray              # [B, Hq, D] uint16 (bf16 bits); [B, q_len, Hq, D] if q_len > 1
     k_cache: np.ndarray        # [num_blocks, bs, Hkv, D] uint16, before this step's write
     v_cache: np.ndarray
     k_new: np.ndarray          # [N, Hkv, D] uint16
     v_new: np.ndarray
     slot_mapping: np.ndarray   # [N] int64
     scale: float
+    q_len: int = 1             # new tokens (queries) per sequence
 
     @property
     def G(self) -> int:
@@ -55,7 +59,7 @@ class DecodeWorkload:
         return int(self.seq_lens.astype(np.int64).sum()) * 2 * self.Hkv * self.D * 2
 
     def qo_bytes(self) -> int:
-        return 2 * self.B * self.Hq * self.D * 2
+        return 2 * self.B * self.q_len * self.Hq * self.D * 2
 
     def write_bytes(self) -> int:
         """Bytes moved by the cache write: read k_new/v_new, write the same into the pools."""
@@ -72,7 +76,7 @@ def make_workload(name: str, *, B: int, Hq: int, Hkv: int, D: int, block_size: i
                   seq_lens: Sequence[int], num_blocks: int, seed: int,
                   max_blocks: Optional[int] = None, shared_prefix_blocks: int = 0,
                   scale: Optional[float] = None, poison_unused: bool = False,
-                  write_new: bool = True) -> DecodeWorkload:
+                  write_new: bool = True, q_len: int = 1) -> DecodeWorkload:
     """Build one seeded workload.
 
     ``shared_prefix_blocks`` > 0 makes the first that many table entries of
@@ -102,18 +106,22 @@ def make_workload(name: str, *, B: int, Hq: int, Hkv: int, D: int, block_size: i
             raise ValueError(f"pool of {num_blocks} blocks too small")
         tables[b, ns:nb] = perm[cursor:cursor + rest]
         cursor += rest
-    q = _bf16_bits(gen, (B, Hq, D))
+    if q_len < 1:
+        raise ValueError("q_len must be >= 1")
+    q = _bf16_bits(gen, (B, Hq, D) if q_len == 1 else (B, q_len, Hq, D))
     k_cache = _bf16_bits(gen, (num_blocks, block_size, Hkv, D))
     v_cache = _bf16_bits(gen, (num_blocks, block_size, Hkv, D))
     if write_new:
-        k_new = _bf16_bits(gen, (B, Hkv, D))
-        v_new = _bf16_bits(gen, (B, Hkv, D))
-        slots = np.full((B,), -1, dtype=np.int64)
+        # token j of sequence b's new ones sits at position L_b - q_len + j
+        k_new = _bf16_bits(gen, (B * q_len, Hkv, D))
+        v_new = _bf16_bits(gen, (B * q_len, Hkv, D))
+        slots = np.full((B * q_len,), -1, dtype=np.int64)
         for b in range(B):
             L = int(seq_lens[b])
-            if L > 0:
-                t = L - 1
-                slots[b] = int(tables[b, t // block_size]) * block_size + t % block_size
+            for j in range(q_len):
+                t = L - q_len + j
+                if t >= 0:
+                    slots[b * q_len + j] = int(tables[b, t // block_size]) * block_size + t % block_size
         if len(set(slots[slots >= 0].tolist())) != int((slots >= 0).sum()):
             raise ValueError("new tokens collide on a slot (a shared block is being written)")
     else:
@@ -131,7 +139,8 @@ def make_workload(name: str, *, B: int, Hq: int, Hkv: int, D: int, block_size: i
                           num_blocks=num_blocks, max_blocks=max_blocks, seq_lens=seq_lens,
                           block_tables=tables, q=q, k_cache=k_cache, v_cache=v_cache,
                           k_new=k_new, v_new=v_new, slot_mapping=slots,
-                          scale=float(np.float32(1.0 / math.sqrt(D))) if scale is None else scale)
+                          scale=float(np.float32(1.0 / math.sqrt(D))) if scale is None else scale,
+                          q_len=q_len)
 
 
 def _uniform_lens(seed: int, B: int, lo: int, hi: int) -> list[int]:
@@ -180,6 +189,15 @@ def qwen3_0p6b(B: int = 256, **kw) -> DecodeWorkload:
                          max_blocks=128, shared_prefix_blocks=8, seed=1005, **kw)
 
 
+def spec_verify(base: str, q_len: int, **kw) -> DecodeWorkload:
+    """Speculative verification on a decode workload: the last q_len positions
+    of every sequence are the target model's queries (q_len - 1 drafted tokens
+    plus the bonus position), written this step and attended causally."""
+    w = WORKLOADS[base](q_len=q_len, **kw)
+    w.name = f"{base}-spec{q_len}"
+    return w
+
+
 WORKLOADS = {
     "tiny": tiny,
     "qwen2.5-1.5b-B1": lambda **kw: qwen25_1p5b(1, **kw),
@@ -192,3 +210,10 @@ WORKLOADS = {
     "long-B2-L32768": lambda **kw: long_context(2, 32768, **kw),
     "qwen3-0.6b-B256": lambda **kw: qwen3_0p6b(256, **kw),
 }
+# multi-query (speculative verification) families: the pages' 1.5B target model
+# verifying drafts, and the 7B / Qwen3 layers with four queries per sequence
+WORKLOADS.update({
+    "qwen2.5-1.5b-B8-spec4": lambda **kw: spec_verify("qwen2.5-1.5b-B8", 4, **kw),
+    "qwen2.5-7b-bs16-spec4": lambda **kw: spec_verify("qwen2.5-7b-bs16", 4, **kw),
+    "qwen3-0.6b-B256-spec4": lambda **kw: spec_verify("qwen3-0.6b-B256", 4, **kw),
+})

@@ -16,6 +16,10 @@ What the pins follow (the "mini-infer" pages):
   - psmarter write-up, feature list items 1 and 7: block-table
     PagedAttention, split-K flash decoding.
   - tom-jerr "Attention Backend" table: split-KV paged decode, page_size 256.
+  - psmarter write-up, feature list items 3 and 5, and the prajwal7-2002
+    docs' "Prompt Ingestion" row and speculative-decoding overview: several
+    new tokens per sequence at once (chunked prefill, draft verification),
+    read as causal attention over the pool.
 """
 from __future__ import annotations
 
@@ -308,6 +312,89 @@ def pin_partial_ranges():
         vt = torch.from_numpy(v[a:bnd]).permute(1, 0, 2)
         o = torch.nn.functional.scaled_dot_product_attention(q, kt, vt, scale=float(w.scale))
         assert np.abs(po[0, :, p] - o[:, 0].numpy()).max() < 1e-12
+
+
+# ------------------------------------------------------ multi-query (causal)
+def causal_scores_and_sdpa(w: W.DecodeWorkload):
+    """torch SDPA (fp64, CPU) with an explicit boolean causal mask on contiguous
+    copies, plus numpy scores for the log-sum-exp.  Query i of sequence b sits at
+    position L - q_len + i and sees tokens [0, L - q_len + i]; a query at a
+    negative position sees nothing (expected output 0, lse -inf)."""
+    from scipy.special import logsumexp
+    out = np.zeros((w.B, w.q_len, w.Hq, w.D))
+    lse = np.full((w.B, w.q_len, w.Hq), -np.inf)
+    for b in range(w.B):
+        L = int(w.seq_lens[b])
+        if L == 0:
+            continue
+        k, v = contiguous_kv(w, b)                                         # [L, Hkv, D]
+        qf = bf16_to_f64(w.q[b])                                           # [q_len, Hq, D]
+        q = torch.from_numpy(qf).permute(1, 0, 2)                           # [Hq, q_len, D]
+        kt = torch.from_numpy(k).permute(1, 0, 2).repeat_interleave(w.G, dim=0)
+        vt = torch.from_numpy(v).permute(1, 0, 2).repeat_interleave(w.G, dim=0)
+        pos = L - w.q_len + np.arange(w.q_len)
+        mask = np.arange(L)[None, :] <= pos[:, None]                       # [q_len, L]
+        seen = mask.any(axis=1)
+        o = torch.nn.functional.scaled_dot_product_attention(
+            q, kt, vt, attn_mask=torch.from_numpy(mask), scale=float(w.scale))
+        o = o.permute(1, 0, 2).numpy()                                     # [q_len, Hq, D]
+        out[b][seen] = o[seen]
+        kg = np.repeat(k, w.G, axis=1)                                     # [L, Hq, D]
+        s = np.einsum("ihd,thd->iht", qf, kg) * w.scale                    # [q_len, Hq, L]
+        for i in np.nonzero(seen)[0]:
+            lse[b, i] = logsumexp(s[i][:, mask[i]], axis=1)
+    return out, lse
+
+
+def run_oracle_mq(w: W.DecodeWorkload):
+    return oracle.decode_mq(w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.scale)
+
+
+def pin_mq_sdpa_causal():
+    """Multi-query oracle equals masked SDPA (output) and logsumexp (lse) to 1e-12."""
+    cases = [
+        small_case(q_len=3),
+        small_case(B=2, Hq=4, Hkv=4, D=16, lens=(33, 5), nb=6, seed=31, q_len=4),         # G=1
+        small_case(B=3, Hq=7, Hkv=1, D=32, lens=(20, 1, 2), nb=6, seed=32, q_len=3),      # L < q_len
+        small_case(B=2, Hq=4, Hkv=2, D=16, bs=256, lens=(300, 7), nb=4, seed=33, q_len=5),
+        small_case(B=1, Hq=6, Hkv=2, D=24, lens=(70,), nb=6, seed=34, q_len=16),
+    ]
+    for w in cases:
+        out, lse = run_oracle_mq(w)
+        ref, ref_lse = causal_scores_and_sdpa(w)
+        err = np.abs(out - ref).max()
+        assert err < 1e-12, f"q_len {w.q_len} G {w.G}: oracle vs masked SDPA {err}"
+        fin = np.isfinite(ref_lse)
+        assert np.array_equal(fin, np.isfinite(lse)), "lse -inf pattern differs"
+        assert np.abs(lse[fin] - ref_lse[fin]).max() < 1e-12, "lse differs from logsumexp"
+
+
+def pin_mq_negative_positions_see_nothing():
+    """Queries at positions < 0 (L < q_len) give a zero row and lse = -inf."""
+    w = small_case(B=2, Hq=2, Hkv=1, D=8, lens=(2, 0), nb=3, seed=35, q_len=4)
+    out, lse = run_oracle_mq(w)
+    assert np.all(out[0, :2] == 0) and np.all(np.isneginf(lse[0, :2]))
+    assert np.all(np.isfinite(lse[0, 2:]))
+    assert np.all(out[1] == 0) and np.all(np.isneginf(lse[1]))
+    # position 0 sees exactly token 0: its V row, bit for bit after widening
+    k, v = contiguous_kv(w, 0)
+    assert np.array_equal(out[0, 2], np.repeat(v[0], w.G, axis=0))   # head h reads KV head h // G
+
+
+def pin_mq_last_query_is_decode():
+    """The last query (position L - 1) sees the whole sequence: it equals the
+    single-query decode of the same rows, and q_len = 1 is decode itself."""
+    w = small_case(B=3, Hq=6, Hkv=2, D=16, lens=(9, 33, 16), nb=8, seed=36, q_len=3)
+    out, lse = run_oracle_mq(w)
+    out1, lse1 = oracle.decode(np.ascontiguousarray(w.q[:, -1]), w.k_cache, w.v_cache,
+                               w.block_tables, w.seq_lens, w.scale)
+    assert np.array_equal(out[:, -1], out1) and np.array_equal(lse[:, -1], lse1)
+    # query i equals the decode of the sequence truncated to L - q_len + i + 1 tokens
+    for i in range(w.q_len):
+        lens_i = (w.seq_lens - w.q_len + i + 1).astype(np.int32)
+        oi, li = oracle.decode(np.ascontiguousarray(w.q[:, i]), w.k_cache, w.v_cache,
+                               w.block_tables, lens_i, w.scale)
+        assert np.array_equal(out[:, i], oi) and np.array_equal(lse[:, i], li)
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

@@ -44,6 +44,12 @@ MUTANTS = {
     "last token dropped": ("for (int t = t0; t < t1; ++t) {\n        const double w",
                            "for (int t = t0; t < t1 - 1; ++t) {\n        const double w"),
     "bf16 widened wrongly": ("((uint32_t)bits) << 16", "((uint32_t)bits) << 15"),
+    "mq causal limit off by one": ("int visible = seq_lens[b] - q_len + i + 1;",
+                                   "int visible = seq_lens[b] - q_len + i;"),
+    "mq query position ignored": ("const int i = (int)((r / Hq) % q_len);",
+                                  "const int i = q_len - 1;"),
+    "mq sequence index wrong": ("const int b = (int)(r / ((int64_t)Hq * q_len));",
+                                "const int b = (int)((r / Hq) % B);"),
 }
 
 
