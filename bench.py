@@ -208,6 +208,16 @@ def time_oracle(w, budget_s: float, max_rows: int | None = None, nthreads: int =
     if w.slot_mapping.size:
         oracle.cache_write(w.k_new, w.v_new, w.slot_mapping, kc, vc)
     t_write = time.perf_counter() - t0
+    if w.q_len > 1:   # multi-query: whole workload per repetition
+        reps, secs = 0, 0.0
+        while reps == 0 or secs < budget_s:
+            t0 = time.perf_counter()
+            oracle.decode_mq(w.q, kc, vc, w.block_tables, w.seq_lens, w.scale, threads)
+            secs += time.perf_counter() - t0
+            reps += 1
+        desc = (f"whole workload {w.name} (causal, q_len {w.q_len}) x {reps} reps, fp64, "
+                f"write {w.write_bytes()} B in {t_write*1e3:.1f} ms excluded")
+        return secs, float(w.kv_bytes() + w.qo_bytes()) * reps, reps * w.B * w.q_len * w.Hq, threads, desc
     total = w.B * w.Hq
     rb = (np.arange(total) // w.Hq).astype(np.int32)
     rh = (np.arange(total) % w.Hq).astype(np.int32)
@@ -296,25 +306,35 @@ def run_ours(args, world, rank, local):
     touched = w.kv_bytes()
     R = max(1, min(8, math.ceil(2.5 * L2_BYTES / max(touched, 1)) + 1)) if touched < 3 * L2_BYTES else 1
     pools = [(k0, v0)] + [(k0.clone(), v0.clone()) for _ in range(R - 1)]
-    P = args.splits or pa.pa_auto_num_splits(w.B, w.Hq, w.Hkv, w.D, w.max_blocks, w.block_size)
-    out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device=dev)
-    lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
+    mq = w.q_len > 1   # multi-query step: write the q_len new tokens, then causal decode
+    if mq:
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        P = args.splits or pa.pa_choose_num_splits_mq(w.B, w.q_len, w.Hq, w.Hkv, w.D, w.max_blocks,
+                                                      w.block_size, sms)
+    else:
+        P = args.splits or pa.pa_auto_num_splits(w.B, w.Hq, w.Hkv, w.D, w.max_blocks, w.block_size)
+    oshape = (w.B, w.q_len, w.Hq, w.D) if mq else (w.B, w.Hq, w.D)
+    out = torch.empty(oshape, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(oshape[:-1], dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(device=dev)
     forced = os.environ.get("PA_DECODE_KERNEL", "auto")
     use_tc = forced == "tensor_core" or (forced != "cuda_core" and w.D == 128)
     kernel_name = "decode_tc_kernel" if use_tc else "decode_cc_kernel"
 
-    ws = torch.zeros(max(1, pa.pa_splitkv_workspace_bytes(w.B, w.Hq, w.D, P)), dtype=torch.uint8,
+    ws = torch.zeros(max(1, pa.pa_splitkv_workspace_bytes(w.B * w.q_len, w.Hq, w.D, P)), dtype=torch.uint8,
                      device=dev)
     merged = P > 1   # the split kernel merges its own partials (one cooperative launch)
 
     def step(r, ev0=None, ev1=None):
         kc, vc = pools[r]
-        if args.unfused:
+        if args.unfused or mq:
             pa.pa_cache_write(kn, vn, slots, kc, vc, stream=stream)
         if ev0 is not None:
             ev0.record(stream)
-        if args.unfused:
+        if mq:
+            pa.pa_decode_mq(out, lse, q, kc, vc, bt, sl, w.scale, num_splits=P, workspace=ws,
+                            stream=stream)
+        elif args.unfused:
             pa.pa_decode_splitkv(out, lse, q, kc, vc, bt, sl, w.scale, num_splits=P, workspace=ws,
                                  stream=stream)
         else:   # one launch: write this step's K/V, attend, merge the splits
@@ -323,7 +343,8 @@ def run_ours(args, world, rank, local):
         if ev1 is not None:
             ev1.record(stream)
 
-    launches_per_step = 2 if args.unfused else 1
+    fused = not (args.unfused or mq)
+    launches_per_step = 1 if fused else 2
     # CUDA graphs of S consecutive steps (cycling over the pool replicas), NG
     # copies, each step with its own pair of graph-recorded events around the
     # decode kernel.  Step i of the timed loop is step i % S of graph copy
@@ -390,8 +411,8 @@ def run_ours(args, world, rank, local):
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
     h_q, h_bt, h_sl = pin(w.q.view(np.int16)), pin(w.block_tables), pin(w.seq_lens)
     h_kn, h_vn, h_slots = pin(w.k_new.view(np.int16)), pin(w.v_new.view(np.int16)), pin(w.slot_mapping)
-    h_out = torch.empty((w.B, w.Hq, w.D), dtype=torch.int16).pin_memory()
-    h_lse = torch.empty((w.B, w.Hq), dtype=torch.float32).pin_memory()
+    h_out = torch.empty(oshape, dtype=torch.int16).pin_memory()
+    h_lse = torch.empty(oshape[:-1], dtype=torch.float32).pin_memory()
     d_q16, d_kn16, d_vn16 = q.view(torch.int16), kn.view(torch.int16), vn.view(torch.int16)
     h2d = sum(t.numel() * t.element_size() for t in (h_q, h_bt, h_sl, h_kn, h_vn, h_slots))
     d2h = h_out.numel() * 2 + h_lse.numel() * 4
@@ -401,8 +422,13 @@ def run_ours(args, world, rank, local):
             for d, h in ((d_q16, h_q), (bt, h_bt), (sl, h_sl), (d_kn16, h_kn), (d_vn16, h_vn),
                          (slots, h_slots)):
                 d.copy_(h, non_blocking=True)
-            pa.pa_decode_step(out, lse, q, kn, vn, slots, kc, vc, bt, sl, w.scale, num_splits=P,
-                              workspace=ws, stream=stream)
+            if mq:
+                pa.pa_cache_write(kn, vn, slots, kc, vc, stream=stream)
+                pa.pa_decode_mq(out, lse, q, kc, vc, bt, sl, w.scale, num_splits=P, workspace=ws,
+                                stream=stream)
+            else:
+                pa.pa_decode_step(out, lse, q, kn, vn, slots, kc, vc, bt, sl, w.scale,
+                                  num_splits=P, workspace=ws, stream=stream)
             h_out.copy_(out.view(torch.int16), non_blocking=True)
             h_lse.copy_(lse, non_blocking=True)
 
@@ -423,14 +449,15 @@ def run_ours(args, world, rank, local):
     peak, peak_kind = measured_peak_gbs()
     # the timed launch reads K, V and q, writes the bf16 output and (fused step) moves
     # this step's new K/V into the pool; its split partials and merge are overhead
-    kern_bytes = w.kv_bytes() + 2 * w.B * w.Hq * w.D * 2 + (0 if args.unfused else write_bytes)
+    kern_bytes = w.kv_bytes() + w.qo_bytes() + (write_bytes if fused else 0)
     roofline = None
     if kern_ms_avg:
         ach = kern_bytes / (kern_ms_avg * 1e-3) / 1e9
         roofline = {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
                     "frac": round(ach / peak, 4), "traffic": recorded_traffic(args.workload, kernel_name),
                     "peak_kind": peak_kind,
-                    "kernel": kernel_name + ("" if args.unfused else " (fused write)")
+                    "kernel": kernel_name + (" (multi-query)" if mq else
+                                             "" if args.unfused else " (fused write)")
                               + (" + split merge" if merged else ""),
                     "kernel_us": round(kern_ms_avg * 1e3, 3), "kernel_bytes": kern_bytes}
 
@@ -448,7 +475,10 @@ def run_ours(args, world, rank, local):
             "data": "synthetic",
             "config": {"workload": args.workload, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
                        "block_size": w.block_size, "seq_lens_total": int(w.seq_lens.sum()),
-                       "splits": P, "step": ("cache_write, then split decode with merge" if args.unfused else
+                       "splits": P, "q_len": w.q_len,
+                       "step": ("cache_write of the q_len new tokens, then pa_decode_mq (causal)"
+                                if mq else "cache_write, then split decode with merge"
+                                if args.unfused else
                                 "pa_decode_step: cache write + split decode + merge, one launch"),
                        "parallelism": f"replicas x{world}",
                        "l2": f"{R} pool replicas rotated per step ({touched/1e6:.0f} MB read per step)"},

@@ -122,8 +122,8 @@ int pa_cache_write(const void *k_new, const void *v_new, const int64_t *slot_map
  * with G = Hq / Hkv <= 16 or D = 64 with G <= 8.  One CTA per (sequence, KV
  * head) holds the G query heads, so each KV tile is read once; use
  * pa_decode_splitkv when B * Hkv is small next to the SM count.
- * Two kernels implement the step: a tensor-core one (tcgen05, D = 128,
- * chosen for G >= 4) and a CUDA-core one (all other supported shapes).  The
+ * Two kernels implement the step: a tensor-core one (tcgen05, chosen
+ * whenever D = 128) and a CUDA-core one (D = 64).  The
  * environment variable PA_DECODE_KERNEL=cuda_core or =tensor_core forces one
  * of them (read on every call; a shape the forced kernel cannot run is
  * PA_EUNSUPPORTED).  Both are checked against the same oracle.
@@ -262,6 +262,45 @@ int pa_decode_step(void *out, float *lse, const void *q, const void *k_new, cons
                    const int32_t *seq_lens, int32_t B, int32_t Hq, float scale,
                    int32_t num_splits, void *workspace, size_t workspace_bytes, int32_t *status,
                    pa_stream_t stream);
+
+/*
+ * Multi-query decode: several new tokens per sequence attend at once, causally
+ * -- speculative verification of drafted tokens, or a small chunk of new
+ * tokens ("mini-infer" psmarter write-up, feature list items 3 and 5;
+ * prajwal7-2002 docs, table "Core Capabilities at a Glance", row "Prompt
+ * Ingestion", and the speculative-decoding overview: the target model
+ * verifies a draft's tokens in one pass).  The last q_len positions of every
+ * sequence are queries, their K/V already in the pool (pa_cache_write first):
+ * query i of sequence b sits at position seq_lens[b] - q_len + i and attends
+ * to positions [0, seq_lens[b] - q_len + i] (a negative position sees
+ * nothing: out = 0, lse = -inf).
+ * q: device bf16 [B, q_len, Hq, D]; out: device bf16 [B, q_len, Hq, D];
+ * lse: device fp32 [B, q_len, Hq] or NULL.  1 <= q_len <= 65535.
+ * Supported: D = 128, G = Hq / Hkv <= 16 (the tensor-core kernel; q_len > 1
+ * with PA_DECODE_KERNEL=cuda_core or D = 64 is PA_EUNSUPPORTED).  A CTA holds
+ * up to 16 / G query positions of its heads; more positions are spread over
+ * more CTAs, each reading the keys its queries can see (for q_len * G > 16
+ * the KV is read about q_len * G / 16 times: suited to verification, not to
+ * long prefill chunks).
+ * num_splits: 0 = pa_choose_num_splits_mq on the current device, 1 = no
+ * split (no workspace), P > 1 = split with the workspace contract of
+ * pa_decode_splitkv for pa_splitkv_workspace_bytes(B * q_len, Hq, D, P)
+ * bytes.  q_len = 1 is exactly pa_decode_splitkv.  Other arguments as
+ * pa_decode_splitkv.
+ */
+int pa_decode_mq(void *out, float *lse, const void *q, int32_t q_len, const void *k_cache,
+                 const void *v_cache, pa_cache_desc cache, const int32_t *block_tables,
+                 int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t B, int32_t Hq,
+                 float scale, int32_t num_splits, void *workspace, size_t workspace_bytes,
+                 int32_t *status, pa_stream_t stream);
+
+/*
+ * Split count for pa_decode_mq, by the rule of pa_choose_num_splits with the
+ * CTAs of every query-position group counted.  q_len = 1 gives
+ * pa_choose_num_splits.  Returns P >= 1, or PA_EINVAL / PA_EUNSUPPORTED.
+ */
+int pa_choose_num_splits_mq(int32_t B, int32_t q_len, int32_t Hq, int32_t Hkv, int32_t D,
+                            int32_t max_blocks_per_seq, int32_t block_size, int32_t sm_count);
 
 /* P that pa_decode_splitkv uses for num_splits == 0 on the current device (PA_ECUDA on error). */
 int pa_auto_num_splits(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t max_blocks_per_seq,

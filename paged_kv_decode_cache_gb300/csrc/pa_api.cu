@@ -3,6 +3,7 @@
 // Nothing here allocates device memory or synchronises the stream.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -37,6 +38,7 @@ constexpr int kMaxGroupCc = 8;    // query heads per KV head, CUDA-core kernel
 constexpr int kMaxGroupTc = 16;   // query heads per KV head, tensor-core kernel
 constexpr int kMaxGridZ = 65535;  // sequences per launch (gridDim.z)
 constexpr int kMinTilesPerSplit = 8;
+constexpr int64_t kMaxRowsQ = 1 << 24;  // B x q_len of one multi-query call
 constexpr int kMaxSplits = 256;
 constexpr int PA_ETOOLARGE = -100;  // internal: the cooperative grid does not fit at once
 
@@ -76,11 +78,11 @@ bool tc_shape(int G, int Hkv, int *HC, int *GP) {
 // CTAs per split of the decode grid: one per (sequence, KV head) for the
 // CUDA-core kernel, one per (sequence, group of HC KV heads) for the
 // tensor-core kernel.
-int64_t units_per_split(Kernel k, int B, int G, int Hkv) {
+int64_t units_per_split(Kernel k, int B, int G, int Hkv, int qpc = 1, int qgroups = 1) {
     if (k == Kernel::kTensorCore) {
         int hc = 1, gp = 1;
-        tc_shape(G, Hkv, &hc, &gp);
-        return static_cast<int64_t>(B) * (Hkv / hc);
+        tc_shape(G * qpc, Hkv, &hc, &gp);
+        return static_cast<int64_t>(B) * (Hkv / hc) * qgroups;
     }
     return static_cast<int64_t>(B) * Hkv;
 }
@@ -222,7 +224,17 @@ pa::DecodeParams base_params(const void *q, const pa_cache_desc &c, const int32_
     p.num_q_heads = Hq;
     p.max_blocks = max_blocks;
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.q_len = 1;
+    p.q_per_cta = 1;
+    p.head_groups = c.num_kv_heads;
     return p;
+}
+
+// Query positions per tensor-core CTA for q_len queries of G heads each: as
+// many as fit the kernel's column limit (G * positions <= 16).
+int queries_per_cta(int G, int q_len) {
+    if (q_len <= 1) return 1;
+    return std::min(q_len, std::max(1, kMaxGroupTc / G));
 }
 
 int sm_count_current() {
@@ -250,12 +262,17 @@ int run_decode(bool split, void *out, float *lse, float *part_o, float *part_lse
                const void *k_cache, const void *v_cache, const pa_cache_desc &c,
                const int32_t *block_tables, int32_t max_blocks, const int32_t *seq_lens,
                int32_t B, int32_t Hq, float scale, int32_t P, int32_t *status,
-               cudaStream_t stream, int32_t *counters = nullptr, const NewTokens &nt = NewTokens()) {
+               cudaStream_t stream, int32_t *counters = nullptr, const NewTokens &nt = NewTokens(),
+               int32_t q_len = 1) {
     const int G = Hq / c.num_kv_heads;
+    const int qpc = queries_per_cta(G, q_len);
     Kernel k;
-    int rc = pick_kernel(G, c.head_dim, &k);
+    int rc = pick_kernel(G * qpc, c.head_dim, &k);
     if (rc) return rc;
+    if (q_len > 1 && k != Kernel::kTensorCore) return PA_EUNSUPPORTED;  // multi-query: tensor cores only
     pa::DecodeParams p = base_params(q, c, block_tables, max_blocks, seq_lens, Hq, scale, status);
+    p.q_len = q_len;
+    p.q_per_cta = qpc;
     p.out = out;
     p.lse = lse;
     p.part_o = part_o;
@@ -273,7 +290,9 @@ int run_decode(bool split, void *out, float *lse, float *part_o, float *part_lse
     cudaError_t e;
     if (k == Kernel::kTensorCore) {
         int HC = 1, GP = 1;
-        if (!tc_shape(G, c.num_kv_heads, &HC, &GP)) return PA_EUNSUPPORTED;
+        if (!tc_shape(G * qpc, c.num_kv_heads, &HC, &GP)) return PA_EUNSUPPORTED;
+        p.head_groups = c.num_kv_heads / HC;
+        if (static_cast<int64_t>(p.head_groups) * ((q_len + qpc - 1) / qpc) > 65535) return PA_EUNSUPPORTED;
         rc = make_kv_map_heads(&kmap, k_cache, c, HC);
         if (!rc) rc = make_kv_map_heads(&vmap, v_cache, c, HC);
         if (rc) return rc;
@@ -345,14 +364,22 @@ int pa_partition_tokens(int32_t max_blocks_per_seq, int32_t block_size, int32_t 
 
 int pa_choose_num_splits(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
                          int32_t max_blocks_per_seq, int32_t block_size, int32_t sm_count) {
-    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || max_blocks_per_seq <= 0 ||
+    return pa_choose_num_splits_mq(B, 1, Hq, Hkv, D, max_blocks_per_seq, block_size, sm_count);
+}
+
+int pa_choose_num_splits_mq(int32_t B, int32_t q_len, int32_t Hq, int32_t Hkv, int32_t D,
+                            int32_t max_blocks_per_seq, int32_t block_size, int32_t sm_count) {
+    if (B < 0 || q_len <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || max_blocks_per_seq <= 0 ||
         block_size <= 0 || sm_count <= 0)
         return PA_EINVAL;
     if (B == 0) return 1;
+    const int G = Hq / Hkv;
+    const int qpc = queries_per_cta(G, q_len);
     Kernel k;
-    int rc = pick_kernel(Hq / Hkv, D, &k);
+    int rc = pick_kernel(G * qpc, D, &k);
     if (rc) return rc;
-    const int64_t units = units_per_split(k, B, Hq / Hkv, Hkv);
+    if (q_len > 1 && k != Kernel::kTensorCore) return PA_EUNSUPPORTED;
+    const int64_t units = units_per_split(k, B, G, Hkv, qpc, (q_len + qpc - 1) / qpc);
     const int64_t slots = static_cast<int64_t>(sm_count) * ctas_per_sm(k);
     int64_t P = slots / units;  // largest P whose grid still fits one wave
     const int64_t lmax = static_cast<int64_t>(max_blocks_per_seq) * block_size;
@@ -418,27 +445,32 @@ int splitkv_common(void *out, float *lse, const void *q, const void *k_cache, co
                    const pa_cache_desc &cache, const int32_t *block_tables,
                    int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t B, int32_t Hq,
                    float scale, int32_t num_splits, void *workspace, size_t workspace_bytes,
-                   int32_t *status, cudaStream_t stream, const NewTokens &nt) {
+                   int32_t *status, cudaStream_t stream, const NewTokens &nt, int32_t q_len = 1) {
     int rc = check_decode_args(q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq,
                                seq_lens, B, Hq, scale);
     if (rc) return rc;
     if (!out || !aligned(out, 16) || (lse && !aligned(lse, 4))) return PA_EINVAL;
-    if (num_splits < 0) return PA_EINVAL;
+    if (num_splits < 0 || q_len < 1) return PA_EINVAL;
+    if (static_cast<int64_t>(B) * q_len > kMaxRowsQ) return PA_EUNSUPPORTED;
     if (B == 0) return PA_OK;
     int P = num_splits;
     if (P == 0) {
-        P = pa_auto_num_splits(B, Hq, cache.num_kv_heads, cache.head_dim, max_blocks_per_seq,
-                               cache.block_size);
+        const int sms = sm_count_current();
+        if (sms <= 0) return PA_ECUDA;
+        P = pa_choose_num_splits_mq(B, q_len, Hq, cache.num_kv_heads, cache.head_dim,
+                                    max_blocks_per_seq, cache.block_size, sms);
         if (P < 0) return P;
     }
     if (P > 65535) return PA_EUNSUPPORTED;
     if (P == 1)
         return run_decode(false, out, lse, nullptr, nullptr, q, k_cache, v_cache, cache,
                           block_tables, max_blocks_per_seq, seq_lens, B, Hq, scale, 1, status,
-                          stream, nullptr, nt);
-    const size_t need = pa_splitkv_workspace_bytes(B, Hq, cache.head_dim, P);
+                          stream, nullptr, nt, q_len);
+    // rows of the partials: (sequence, query position, head)
+    const int32_t Bq = B * q_len;
+    const size_t need = pa_splitkv_workspace_bytes(Bq, Hq, cache.head_dim, P);
     if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return PA_EWORKSPACE;
-    const int64_t rows = static_cast<int64_t>(B) * Hq * P;
+    const int64_t rows = static_cast<int64_t>(Bq) * Hq * P;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     float *part_o = reinterpret_cast<float *>(ws);
     float *part_lse = reinterpret_cast<float *>(ws + round_up(rows * cache.head_dim * 4, 256));
@@ -447,17 +479,29 @@ int splitkv_common(void *out, float *lse, const void *q, const void *k_cache, co
     // One cooperative launch that merges its own partials when the whole grid
     // fits on the GPU at once; otherwise partials, then pa_combine.
     rc = run_decode(true, out, lse, part_o, part_lse, q, k_cache, v_cache, cache, block_tables,
-                    max_blocks_per_seq, seq_lens, B, Hq, scale, P, status, stream, counters, nt);
+                    max_blocks_per_seq, seq_lens, B, Hq, scale, P, status, stream, counters, nt,
+                    q_len);
     if (rc != PA_ETOOLARGE) return rc;
     rc = run_decode(true, nullptr, nullptr, part_o, part_lse, q, k_cache, v_cache, cache,
                     block_tables, max_blocks_per_seq, seq_lens, B, Hq, scale, P, status, stream,
-                    nullptr, nt);
+                    nullptr, nt, q_len);
     if (rc) return rc;
-    cudaError_t e = pa::launch_combine(out, lse, part_o, part_lse, static_cast<int>(B * Hq), P,
+    cudaError_t e = pa::launch_combine(out, lse, part_o, part_lse, static_cast<int>(Bq * Hq), P,
                                        cache.head_dim, stream);
     return e == cudaSuccess ? PA_OK : PA_ECUDA;
 }
 }  // namespace
+
+int pa_decode_mq(void *out, float *lse, const void *q, int32_t q_len, const void *k_cache,
+                 const void *v_cache, pa_cache_desc cache, const int32_t *block_tables,
+                 int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t B, int32_t Hq,
+                 float scale, int32_t num_splits, void *workspace, size_t workspace_bytes,
+                 int32_t *status, pa_stream_t stream) {
+    if (q_len < 1 || q_len > 65535) return PA_EINVAL;
+    return splitkv_common(out, lse, q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq,
+                          seq_lens, B, Hq, scale, num_splits, workspace, workspace_bytes, status,
+                          stream, NewTokens(), q_len);
+}
 
 int pa_decode_splitkv(void *out, float *lse, const void *q, const void *k_cache,
                       const void *v_cache, pa_cache_desc cache, const int32_t *block_tables,

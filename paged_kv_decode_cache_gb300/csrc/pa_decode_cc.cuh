@@ -359,8 +359,8 @@ decode_cc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     }
     if (p.split)
         merge_split_group<D, NW>(p, b * gridDim.y + g, part, static_cast<int64_t>(b) * p.num_q_heads + hq0,
-                                 G, reinterpret_cast<int *>(smem + C::kTicketOff), tid,
-                                 [] { __syncthreads(); });
+                                 G, G, p.num_q_heads, reinterpret_cast<int *>(smem + C::kTicketOff),
+                                 tid, [] { __syncthreads(); });
 }
 
 // Opt a kernel into more than 48 KB of dynamic shared memory, once per

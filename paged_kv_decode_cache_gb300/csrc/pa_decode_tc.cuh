@@ -61,10 +61,11 @@ constexpr int kTcTmaKWarp = 5;
 constexpr int kTcTmaVWarp = 6;
 constexpr int kTcPvWarp = 7;
 constexpr int kTcNBS = 4;              // S buffers in TMEM
-constexpr int kTcNBP = 2;              // P^T buffers in shared memory
 constexpr float kTcLazyTau = 8.0f;     // log2 headroom before a reference max moves
 constexpr int kTcLook = 4;             // chunks a producer's block-id lookups run ahead
 constexpr int kTcMaskRing = 8;         // chunk validity masks the K producer publishes
+
+constexpr int kTcSmemLimit = 227 * 1024;
 
 template <int HC, int GP>
 struct TcCfg {
@@ -73,31 +74,52 @@ struct TcCfg {
     static constexpr int kT = kTcRows / HC;                     // tokens per chunk
     static constexpr int kTiles = kT / kTile;                   // 16-token tiles per chunk
     static_assert(kTiles >= 1 && kTiles * HC * kTile == kTcRows, "tiles");
-    static constexpr int kNK = kN <= 32 ? 3 : 2;                // K stages
-    static constexpr int kNV = 3;                               // V stages
     static constexpr int kSubTile = kTcRows * kSubBytes;        // [128 m][64 d] bf16 = 16 KB
     static constexpr int kTileBytes = 2 * kSubTile;             // K (or V) of one chunk: 32 KB
     static constexpr int kBoxBytes = HC * kTile * kSubBytes;    // one TMA box: HC heads x 16 rows
+    static constexpr int kQBytes = 2 * kN * kSubBytes;          // [N][64] x 2 halves
+    static constexpr int kPBytes = 2 * kN * kSubBytes;          // 2 atoms of [N][64 m]
+    // P^T buffer: 2 atoms of [2N][64 m], rows 0..N-1 the hi and rows N..2N-1
+    // the lo bf16 part of p; one MMA with N' = 2N accumulates both into
+    // adjacent TMEM column ranges
+    static constexpr int kPBufBytes = 2 * kPBytes;
+    // red[128 rows][GP], col[N], m_ref[N], alpha[N], rel[N] (output row of
+    // column n relative to the CTA's first row, -1: padding), abort flag,
+    // TMEM slot, merge ticket
+    static constexpr int kRedBytes = (kTcRows * GP + 4 * kN) * 4 + 16;
+    // shared memory for nk K stages, nv V stages and nbp P^T buffers, laid out
+    // as below (rings, Q, P^T, scratch, barriers, masks, block-id rings, align)
+    static constexpr int smem_for(int nk, int nv, int nbp) {
+        return ((nk + nv) * kTileBytes + kQBytes + nbp * kPBufBytes + kRedBytes + 7) / 8 * 8 +
+               (2 * nk + 2 * nv + 2 * kTcNBS + 2 * nbp) * 8 + kTcMaskRing * 8 +
+               2 * (kTcLook + 1) * 32 * 4 + 1024;
+    }
+    // the deepest pipeline that fits: K and V stages first, then P^T buffers
+    static constexpr int kChoice = smem_for(3, 3, 2) <= kTcSmemLimit ? 0
+                                   : smem_for(3, 3, 1) <= kTcSmemLimit ? 1
+                                   : smem_for(2, 3, 2) <= kTcSmemLimit ? 2
+                                   : smem_for(2, 2, 2) <= kTcSmemLimit ? 3 : 4;
+    static constexpr int kNK = kChoice <= 1 ? 3 : 2;            // K stages
+    static constexpr int kNV = kChoice <= 2 ? 3 : 2;            // V stages
+    static constexpr int kNBP = (kChoice == 1 || kChoice == 4) ? 1 : 2;  // P^T buffers
     static constexpr int kVOff = kNK * kTileBytes;
     static constexpr int kQOff = (kNK + kNV) * kTileBytes;
-    static constexpr int kQBytes = 2 * kN * kSubBytes;          // [N][64] x 2 halves
     static constexpr int kPOff = kQOff + kQBytes;
-    static constexpr int kPBytes = 2 * kN * kSubBytes;          // P^T: 2 atoms of [N][64 m]
-    static constexpr int kRedOff = kPOff + kTcNBP * kPBytes;
-    // red[128 rows][GP], col[N] (per-column result), m_ref[N], alpha[N], abort flag, TMEM slot
-    static constexpr int kRedBytes = (kTcRows * GP + 3 * kN) * 4 + 16;
+    static constexpr int kRedOff = kPOff + kNBP * kPBufBytes;
     static constexpr int kBarOff = (kRedOff + kRedBytes + 7) / 8 * 8;
-    static constexpr int kNumBars = 2 * kNK + 2 * kNV + 2 * kTcNBS + 2 * kTcNBP;
+    static constexpr int kNumBars = 2 * kNK + 2 * kNV + 2 * kTcNBS + 2 * kNBP;
     // validity masks [kTcMaskRing] (u64: chunk << 32 | lane mask), then the two
     // producers' block-id rings [2][kTcLook + 1][32 lanes]
     static constexpr int kMaskOff = kBarOff + kNumBars * 8;
     static constexpr int kLookOff = kMaskOff + kTcMaskRing * 8;
     static constexpr int kSmemBytes = kLookOff + 2 * (kTcLook + 1) * 32 * 4 + 1024;
+    static_assert(kSmemBytes == smem_for(kNK, kNV, kNBP), "layout");
     // the K producer rewrites mask slot c % ring only once softmax c has read it
     static_assert(kNK + kTcNBS <= kTcMaskRing, "mask ring");
-    static_assert(kSmemBytes <= 227 * 1024, "shared memory");
-    static constexpr uint32_t kTmemCols = (kTcNBS + 1) * kN <= 128 ? 128u
-                                          : (kTcNBS + 1) * kN <= 256 ? 256u : 512u;
+    static_assert(kSmemBytes <= kTcSmemLimit, "shared memory");
+    // S buffers (NBS x N columns), then O^T: hi part (N) and lo part (N)
+    static constexpr uint32_t kTmemCols = (kTcNBS + 2) * kN <= 128 ? 128u
+                                          : (kTcNBS + 2) * kN <= 256 ? 256u : 512u;
     static constexpr int kColO = kTcNBS * kN;
 };
 
@@ -122,7 +144,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                  const DecodeParams p, int G) {
     constexpr int D = 128;
     using C = TcCfg<HC, GP>;
-    constexpr int N = C::kN, NK = C::kNK, NV = C::kNV;
+    constexpr int N = C::kN, NK = C::kNK, NV = C::kNV, NBP = C::kNBP;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
@@ -134,19 +156,28 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     float *col = red + kTcRows * GP;                                // [N] per-column result
     float *m_ref = col + N;                                         // [N] reference max
     float *alpha_s = m_ref + N;                                     // [N] rescale factors
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(alpha_s + N);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(alpha_s + N + 1);
-    int *ticket = reinterpret_cast<int *>(alpha_s + N + 2);
+    int *rel_s = reinterpret_cast<int *>(alpha_s + N);               // [N] output row offsets
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(alpha_s + 2 * N);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(alpha_s + 2 * N + 1);
+    int *ticket = reinterpret_cast<int *>(alpha_s + 2 * N + 2);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
     uint64_t *kfull = bars, *kempty = bars + NK, *vfull = bars + 2 * NK, *vempty = vfull + NV;
     uint64_t *sdone = vempty + NV, *sfree = sdone + kTcNBS, *pready = sfree + kTcNBS;
-    uint64_t *pfree = pready + kTcNBP;
+    uint64_t *pfree = pready + NBP;
     volatile uint64_t *mask_ring = reinterpret_cast<volatile uint64_t *>(smem + C::kMaskOff);
     int *look_ring = reinterpret_cast<int *>(smem + C::kLookOff);  // [2][kTcLook + 1][32]
 
-    const int part = blockIdx.x, g0 = blockIdx.y * HC, b = blockIdx.z;
+    const int part = blockIdx.x, b = blockIdx.z;
+    const int g0 = (blockIdx.y % p.head_groups) * HC;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int bs = p.block_size;
+    // This CTA's queries: positions qi0 .. qi0 + nq - 1 of the q_len new ones
+    // (q_len = 1: plain decode).  Per head, MMA column c < Gq is query
+    // qi0 + c / G of group member c % G; its output row is col_row(head, c).
+    const int qi0 = static_cast<int>(blockIdx.y / p.head_groups) * p.q_per_cta;
+    const int nq = min(p.q_per_cta, p.q_len - qi0);
+    const int Gq = nq * G;
+    const int Hq = p.num_q_heads;
 
     // Global reads that do not depend on the sequence length go out first, so
     // their latencies overlap: the length, this CTA's queries, and (producer
@@ -154,7 +185,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     const int lmax = p.max_blocks * bs;
     const int t_begin = part * p.chunk;
     const int t_lim = min(t_begin + p.chunk, lmax);  // range end before the length is known
-    const int64_t row0 = static_cast<int64_t>(b) * p.num_q_heads + static_cast<int64_t>(g0) * G;
+    const int64_t row0 = (static_cast<int64_t>(b) * p.q_len + qi0) * Hq + static_cast<int64_t>(g0) * G;
+    auto col_row = [&](int hh, int c) -> int64_t {
+        return row0 + static_cast<int64_t>(c / G) * Hq + hh * G + c % G;
+    };
     const int32_t *bt = p.block_tables + static_cast<int64_t>(b) * p.max_blocks;
     int L = p.seq_lens[b];
     constexpr int kQLoads = (N * (D / 8) + kTcThreads - 1) / kTcThreads;
@@ -163,8 +197,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     for (int j = 0; j < kQLoads; ++j) {
         const int i = tid + j * kTcThreads, n = i / (D / 8), c = i % (D / 8);
         qv[j] = make_uint4(0u, 0u, 0u, 0u);
-        if (i < N * (D / 8) && n % GP < G)
-            qv[j] = *reinterpret_cast<const uint4 *>(p.q + (row0 + (n / GP) * G + n % GP) * D + c * 8);
+        if (i < N * (D / 8) && n % GP < Gq)
+            qv[j] = *reinterpret_cast<const uint4 *>(p.q + col_row(n / GP, n % GP) * D + c * 8);
     }
     // Block ids reach the TMA producers through cp.async copies into a small
     // ring, kTcLook chunks ahead of use, so no issue waits on a lookup that is
@@ -189,7 +223,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         // stream has filled the memory queues; touching them now takes their
         // address translations off that path.
         const void *touch = nullptr;
-        const int64_t last = row0 + static_cast<int64_t>(HC) * G - 1;
+        const int64_t last = col_row(HC - 1, Gq - 1);
         const __nv_bfloat16 *out_rows = static_cast<const __nv_bfloat16 *>(p.out) + row0 * D;
         if (p.split) {
             if (lane == 0) touch = p.part_o + (row0 * p.num_splits + part) * D;
@@ -206,24 +240,28 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         if (tid == 0 && part == 0 && g0 == 0) set_status(p.status, PA_STATUS_BAD_SEQLEN);
         L = L < 0 ? 0 : lmax;
     }
-    const int t_end = min(t_begin + p.chunk, L);
+    // Query qi0 + k sits at position qbase + k and sees tokens up to it
+    // (causal); no key past this CTA's last query is read.
+    const int qbase = L - p.q_len + qi0;
+    const int t_end = min(t_begin + p.chunk, max(0, min(L, qbase + nq)));
     const int nch = t_end > t_begin ? (t_end - t_begin + C::kT - 1) / C::kT : 0;
 
     if (nch == 0) {  // empty range: zero output, lse = -inf
         cp_async_wait<0>();
-        for (int i = tid; i < HC * G * D; i += kTcThreads) {
-            const int64_t r = row0 + i / D;
-            const int d = i % D;
+        for (int i = tid; i < HC * Gq * D; i += kTcThreads) {
+            const int j = i / D, d = i % D;
+            const int64_t r = col_row(j / Gq, j % Gq);
             if (p.split) p.part_o[(r * p.num_splits + part) * D + d] = 0.f;
             else static_cast<__nv_bfloat16 *>(p.out)[r * D + d] = __float2bfloat16_rn(0.f);
         }
-        if (tid < HC * G) {
-            if (p.split) p.part_lse[(row0 + tid) * p.num_splits + part] = -INFINITY;
-            else if (p.lse) p.lse[row0 + tid] = -INFINITY;
+        if (tid < HC * Gq) {
+            const int64_t r = col_row(tid / Gq, tid % Gq);
+            if (p.split) p.part_lse[r * p.num_splits + part] = -INFINITY;
+            else if (p.lse) p.lse[r] = -INFINITY;
         }
         if (p.split)
-            merge_split_group<D, kTcThreads / 32>(p, b * gridDim.y + blockIdx.y, part, row0, HC * G,
-                                                  ticket, tid, [] { __syncthreads(); });
+            merge_split_group<D, kTcThreads / 32>(p, b * gridDim.y + blockIdx.y, part, row0, HC * Gq,
+                                                  HC * G, Hq, ticket, tid, [] { __syncthreads(); });
         return;
     }
 
@@ -331,8 +369,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         // the MMA / softmax barriers (the rings' are the producers'): every one
         // completes on one arrival except "S free" and "P ready", which all 128
         // softmax threads arrive on
-        for (uint64_t *bar = sdone; bar < pfree + kTcNBP; ++bar)
-            mbar_init(bar, (bar >= sfree && bar < pready + kTcNBP) ? 128u : 1u);
+        for (uint64_t *bar = sdone; bar < pfree + NBP; ++bar)
+            mbar_init(bar, (bar >= sfree && bar < pready + NBP) ? 128u : 1u);
         *abort_flag = 0;
     }
     if (tid < N) m_ref[tid] = -INFINITY;
@@ -342,7 +380,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         if (i < N * (D / 8))
             *reinterpret_cast<uint4 *>(qs + (c >> 3) * (N * kSubBytes) + swz128(n, c & 7)) = qv[j];
     }
-    for (int i = tid; i < kTcNBP * C::kPBytes / 16; i += kTcThreads)
+    for (int i = tid; i < NBP * C::kPBufBytes / 16; i += kTcThreads)
         reinterpret_cast<uint4 *>(ps)[i] = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async_smem();
     fence_barrier_init();
@@ -388,27 +426,28 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     } else if (warp == kTcPvWarp) {
         // ================= PV issuer =================
         if (lane == 0) {
-            constexpr uint32_t kIdPV = tc5::idesc_bf16_f32(kTcRows, N, true, false);
+            constexpr uint32_t kIdPV = tc5::idesc_bf16_f32(kTcRows, 2 * N, true, false);
             int done = 0;
             for (int c = 0; c < nch; ++c) {
-                if (!wait_or_abort(&pready[c % kTcNBP], (c / kTcNBP) & 1)) break;
+                if (!wait_or_abort(&pready[c % NBP], (c / NBP) & 1)) break;
                 if (!wait_or_abort(&vfull[c % NV], (c / NV) & 1)) break;
                 tc5::fence_after_sync();
                 const uint8_t *vt = vring + (c % NV) * C::kTileBytes;
-                const uint8_t *pt = ps + (c % kTcNBP) * C::kPBytes;
+                const uint8_t *pt = ps + (c % NBP) * C::kPBufBytes;
 #pragma unroll
                 for (int j = 0; j < kTcRows / 16; ++j) {
                     tc5::mma_bf16(tmem + C::kColO,
                                   tc5::sw128_desc(vt + j * 16 * kSubBytes, C::kSubTile, 1024),
-                                  tc5::sw128_desc(pt + (j >> 2) * (N * kSubBytes) + (j & 3) * 32, 16, 1024),
+                                  tc5::sw128_desc(pt + (j >> 2) * (2 * N * kSubBytes) + (j & 3) * 32, 16,
+                                                  1024),
                                   kIdPV, c > 0 || j > 0);
                 }
-                tc5::commit(&pfree[c % kTcNBP]);
+                tc5::commit(&pfree[c % NBP]);
                 tc5::commit(&vempty[c % NV]);
                 done = c + 1;
             }
             if (*abort_flag && done > 0)
-                mbar_wait_bounded(&pfree[(done - 1) % kTcNBP], ((done - 1) / kTcNBP) & 1);
+                mbar_wait_bounded(&pfree[(done - 1) % NBP], ((done - 1) / NBP) & 1);
         }
     } else {
         // ================= softmax warps: thread = row m of a chunk, and output dim d =================
@@ -421,7 +460,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         const int my_tile = tid / (kTile * HC);              // tile of row m = tid
         const int my_tok = my_tile * kTile + (tid & 15);     // its token's offset in a chunk
         for (int c = 0; c < nch; ++c) {
-            const int sbuf = c % kTcNBS, pbuf = c % kTcNBP;
+            const int sbuf = c % kTcNBS, pbuf = c % NBP;
             bool ok = wait_or_abort(&sdone[sbuf], (c / kTcNBS) & 1);
             // the K producer wrote chunk c's mask before its loads, hence before S c
             uint64_t mk = 0;
@@ -453,6 +492,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             tc5::fence_before_sync();
             mbar_arrive(&sfree[sbuf]);  // S buffer read: QK c + NBS may overwrite it
             const bool valid = ok && in_pool;
+            // causal: column q (query qi0 + q / G) sees this row's token only if
+            // the token is not past the query's position
+            const int cmin = max(0, t_begin + c * C::kT + my_tok - qbase) * G;
             float sc[GP], mr[GP];
             bool over = false;
 #pragma unroll
@@ -461,7 +503,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
 #pragma unroll
                 for (int hh = 1; hh < HC; ++hh)
                     if (my_head == hh) v = sv[hh * GP + q];
-                sc[q] = (valid && q < G) ? v * sl2 : -INFINITY;
+                sc[q] = (valid && q < Gq && q >= cmin) ? v * sl2 : -INFINITY;
                 mr[q] = m_ref[my_head * GP + q];
                 over |= sc[q] > mr[q] + kTcLazyTau;
             }
@@ -490,38 +532,44 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                     l_thr[q] *= alpha_s[my_head * GP + q];
                 }
                 if (c >= 1) {  // O^T (all chunks so far) is rescaled once PV c-1 is done
-                    bool ok3 = wait_or_abort(&pfree[(c - 1) % kTcNBP], ((c - 1) / kTcNBP) & 1);
+                    bool ok3 = wait_or_abort(&pfree[(c - 1) % NBP], ((c - 1) / NBP) & 1);
                     if (__all_sync(0xffffffffu, ok3)) {
                         tc5::fence_after_sync();
 #pragma unroll 1
-                        for (int k = 0; k < N / 16; ++k) {
+                        for (int k = 0; k < 2 * N / 16; ++k) {  // hi and lo parts
                             float ov[16];
                             const uint32_t ta = tc5::taddr(tmem, 32 * warp, C::kColO + 16 * k);
                             tc5::ld_32x32b_x16(ta, ov);
+                            const float *al = alpha_s + 16 * (k % (N / 16));
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) ov[i] *= alpha_s[16 * k + i];
+                            for (int i = 0; i < 16; ++i) ov[i] *= al[i];
                             tc5::st_32x32b_x16(ta, ov);
                         }
                     }
                 }
                 named_sync(1, 128);  // alpha_s / red read by all before any later reuse
             }
-            __nv_bfloat16 pb[GP];
+            // p = hi + lo, both bf16 (the PV MMA takes bf16 operands): the pair
+            // carries p to about 2^-17 relative, where hi alone would be 2^-9
+            __nv_bfloat16 pb[GP], pl[GP];
 #pragma unroll
             for (int q = 0; q < GP; ++q) {
-                pb[q] = __float2bfloat16_rn(valid && q < G ? fast_exp2(sc[q] - mr[q]) : 0.f);
-                l_thr[q] += __bfloat162float(pb[q]);
+                const float pf = sc[q] != -INFINITY ? fast_exp2(sc[q] - mr[q]) : 0.f;
+                pb[q] = __float2bfloat16_rn(pf);
+                pl[q] = __float2bfloat16_rn(pf - __bfloat162float(pb[q]));
+                l_thr[q] += __bfloat162float(pb[q]) + __bfloat162float(pl[q]);
             }
-            if (c >= kTcNBP) wait_or_abort(&pfree[pbuf], ((c / kTcNBP) - 1) & 1);  // PV c - NBP done
+            if (c >= NBP) wait_or_abort(&pfree[pbuf], ((c / NBP) - 1) & 1);  // PV c - NBP done
             {
                 // P^T[n][m] for this row's own head block; the other heads' columns stay zero
-                uint8_t *pt = ps + pbuf * C::kPBytes + (tid >> 6) * (N * kSubBytes);
+                uint8_t *pt = ps + pbuf * C::kPBufBytes + (tid >> 6) * (2 * N * kSubBytes);
                 const int tt = tid & 63;
 #pragma unroll
                 for (int q = 0; q < GP; ++q) {
-                    const int n = my_head * GP + q;
-                    *reinterpret_cast<__nv_bfloat16 *>(pt + n * kSubBytes + (((tt >> 3) ^ (n & 7)) << 4) +
-                                                       (tt & 7) * 2) = pb[q];
+                    const int n = my_head * GP + q;   // lo row N + n swizzles as n (N % 8 == 0)
+                    const uint32_t at = n * kSubBytes + (((tt >> 3) ^ (n & 7)) << 4) + (tt & 7) * 2;
+                    *reinterpret_cast<__nv_bfloat16 *>(pt + at) = pb[q];
+                    *reinterpret_cast<__nv_bfloat16 *>(pt + N * kSubBytes + at) = pl[q];
                 }
             }
             // an invalid row zeroes its V row, so 0 * (stale or NaN) never reaches O^T
@@ -540,16 +588,18 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         }
 
         // ---- epilogue: row sums, O^T, normalise, store ----------------------------------
-        bool okf = !dead && wait_or_abort(&pfree[(nch - 1) % kTcNBP], ((nch - 1) / kTcNBP) & 1);
+        bool okf = !dead && wait_or_abort(&pfree[(nch - 1) % NBP], ((nch - 1) / NBP) & 1);
         okf = named_sync_or(1, 128, !okf) ? false : true;
         // row sums of every column (head, q) over that head's rows, via shared memory
 #pragma unroll
         for (int q = 0; q < GP; ++q) red[tid * GP + q] = l_thr[q];
         named_sync(1, 128);
-        if (tid < N) {  // row sum of column n, and its reciprocal (alpha_s is free now)
+        if (tid < N) {  // row sum of column n, its reciprocal (alpha_s is free now), its row
             const float lsum = column_reduce<HC, GP, false>(red, tid);
             col[tid] = lsum;
-            alpha_s[tid] = 1.f / lsum;
+            alpha_s[tid] = lsum > 0.f ? 1.f / lsum : 0.f;  // 0: no key seen (causal)
+            const int c = tid % GP;
+            rel_s[tid] = c < Gq ? static_cast<int>(col_row(tid / GP, c) - row0) : -1;
         }
         named_sync(1, 128);  // col[] / alpha_s complete before they are read
         if (okf) {
@@ -561,22 +611,22 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             __nv_bfloat16 *oh = p.split ? nullptr : static_cast<__nv_bfloat16 *>(p.out) + row0 * D + tid;
 #pragma unroll 1
             for (int k = 0; k < N / 16; ++k) {
-                float ov[16];
+                float ov[16], lo[16];
                 tc5::ld_32x32b_x16(tc5::taddr(tmem, 32 * warp, C::kColO + 16 * k), ov);
+                tc5::ld_32x32b_x16(tc5::taddr(tmem, 32 * warp, C::kColO + N + 16 * k), lo);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const int n = 16 * k + i, q = n % GP;
-                    if (q >= G) continue;
-                    const float o = ov[i] * alpha_s[n];
-                    const int64_t off = ((n / GP) * G + q) * stride;
-                    if (p.split) of[off] = o;
-                    else oh[off] = __float2bfloat16_rn(o);
+                    const int n = 16 * k + i, rel = rel_s[n];
+                    if (rel < 0) continue;
+                    const float o = (ov[i] + lo[i]) * alpha_s[n];
+                    if (p.split) of[rel * stride] = o;
+                    else oh[rel * stride] = __float2bfloat16_rn(o);
                 }
             }
-            if (tid < N && tid % GP < G) {
-                const int n = tid, hh = n / GP, q = n % GP;
+            if (tid < N && rel_s[tid] >= 0) {
+                const int n = tid;
                 const float lse = (m_ref[n] + log2f(col[n])) * 0.69314718055994531f;
-                const int64_t r = row0 + hh * G + q;
+                const int64_t r = row0 + rel_s[n];
                 if (p.split) p.part_lse[r * p.num_splits + part] = lse;
                 else if (p.lse) p.lse[r] = lse;
             }
@@ -586,8 +636,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     __syncthreads();
     if (warp == 0) tc5::tmem_free(tmem, C::kTmemCols);
     if (p.split)  // all eight warps share the merge
-        merge_split_group<D, kTcThreads / 32>(p, b * gridDim.y + blockIdx.y, part, row0, HC * G, ticket,
-                                              tid, [] { __syncthreads(); });
+        merge_split_group<D, kTcThreads / 32>(p, b * gridDim.y + blockIdx.y, part, row0, HC * Gq,
+                                              HC * G, Hq, ticket, tid, [] { __syncthreads(); });
 }
 
 template <int HC, int GP>
@@ -605,7 +655,8 @@ cudaError_t launch_tc_instance(const CUtensorMap &kmap, const CUtensorMap &vmap,
         if (e != cudaSuccess) return e;
         smem_attr_done.fetch_or(bit, std::memory_order_release);
     }
-    return launch_maybe_cooperative(kern, dim3(p.num_splits, p.num_kv_heads / HC, B), kTcThreads,
+    const int qgroups = (p.q_len + p.q_per_cta - 1) / p.q_per_cta;
+    return launch_maybe_cooperative(kern, dim3(p.num_splits, p.head_groups * qgroups, B), kTcThreads,
                                     C::kSmemBytes, stream, p.counters != nullptr, kmap, vmap, p, G);
 }
 

@@ -40,6 +40,13 @@ struct DecodeParams {
     const int64_t *slot_mapping;  // [B]
     uint16_t *k_pool;       // the pools, writable
     uint16_t *v_pool;
+    // Multi-query decode: the last q_len positions of each sequence are
+    // queries (q, out: [B, q_len, Hq, D]; rows (b * q_len + i) * Hq + h), query
+    // i at position L - q_len + i attending causally.  A CTA takes q_per_cta
+    // consecutive query positions; gridDim.y = head_groups x query groups.
+    int32_t q_len;          // 1: plain decode
+    int32_t q_per_cta;
+    int32_t head_groups;    // CTAs across the KV heads (Hkv / heads per CTA)
 };
 
 // CUDA-core decode kernel launch (pa_decode_cc_d*.cu).  Returns a cudaError_t.

@@ -151,12 +151,16 @@ __device__ __forceinline__ void merge_slice_wide(const DecodeParams &p, int64_t 
 }
 
 // Called by all 32 x kWarps threads (index t) of a CTA after its partials for
-// rows [row_first, row_first + nrows) are written; `sync` synchronises those
-// threads; `flag` is a shared int.  Every CTA of a group launches the same
-// kernel, so all agree on kWarps and hence on who does which task.
+// its nrows rows are written: row j is row_first + (j / per_block) * stride +
+// j % per_block (blocks of consecutive rows, e.g. one per query position).
+// `sync` synchronises those threads; `flag` is a shared int.  Every CTA of a
+// group launches the same kernel, so all agree on kWarps and hence on who does
+// which task.
 template <int D, int kWarps, typename Sync>
 __device__ void merge_split_group(const DecodeParams &p, int group, int part, int64_t row_first,
-                                  int nrows, int *flag, int t, Sync sync) {
+                                  int nrows, int per_block, int64_t stride, int *flag, int t,
+                                  Sync sync) {
+    auto row_of = [&](int j) -> int64_t { return row_first + (j / per_block) * stride + j % per_block; };
     if (!p.counters) return;
     int *arrive = p.counters + 2 * group, *depart = arrive + 1;
     const int P = p.num_splits;
@@ -181,11 +185,11 @@ __device__ void merge_split_group(const DecodeParams &p, int group, int part, in
         if (P <= 32) {  // lanes over dims: one round trip per 32-dim slice
             const int tasks = nrows * (D / 32);
             for (int k = part * kWarps + warp; k < tasks; k += P * kWarps)
-                merge_slice<D>(p, row_first + k / (D / 32), k % (D / 32), lane);
+                merge_slice<D>(p, row_of(k / (D / 32)), k % (D / 32), lane);
         } else {        // lanes over partitions: one round trip per 8-dim slice
             const int tasks = nrows * (D / 8);
             for (int k = part * kWarps + warp; k < tasks; k += P * kWarps)
-                merge_slice_wide<D>(p, row_first + k / (D / 8), k % (D / 8), lane);
+                merge_slice_wide<D>(p, row_of(k / (D / 8)), k % (D / 8), lane);
         }
     }
     sync();

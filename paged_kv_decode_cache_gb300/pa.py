@@ -58,6 +58,9 @@ _SIGNATURES = {
     "pa_decode_splitkv_noalloc": ([_P, _P, _P, _P, _P, CacheDesc, _P, _I32, _P, _I32, _I32, _F32,
                                    _I32, _P, _P], ctypes.c_int),
     "pa_auto_num_splits": ([_I32, _I32, _I32, _I32, _I32, _I32], ctypes.c_int),
+    "pa_decode_mq": ([_P, _P, _P, _I32, _P, _P, CacheDesc, _P, _I32, _P, _I32, _I32, _F32, _I32,
+                      _P, _SZ, _P, _P], ctypes.c_int),
+    "pa_choose_num_splits_mq": ([_I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32], ctypes.c_int),
     "pa_strerror": ([ctypes.c_int], ctypes.c_char_p),
     "pa_version": ([], ctypes.c_int),
 }
@@ -138,6 +141,14 @@ def pa_choose_num_splits(B: int, Hq: int, Hkv: int, D: int, max_blocks_per_seq: 
                          block_size: int, sm_count: int) -> int:
     r = lib().pa_choose_num_splits(B, Hq, Hkv, D, max_blocks_per_seq, block_size, sm_count)
     _check("pa_choose_num_splits", min(r, 0))
+    return r
+
+
+def pa_choose_num_splits_mq(B: int, q_len: int, Hq: int, Hkv: int, D: int,
+                            max_blocks_per_seq: int, block_size: int, sm_count: int) -> int:
+    r = lib().pa_choose_num_splits_mq(B, q_len, Hq, Hkv, D, max_blocks_per_seq, block_size,
+                                      sm_count)
+    _check("pa_choose_num_splits_mq", min(r, 0))
     return r
 
 
@@ -276,6 +287,29 @@ def pa_decode_step(out, lse, q, k_new, v_new, slot_mapping, k_cache, v_cache, bl
 
 
 PA_NOALLOC_SCRATCH_BYTES = 4 << 20
+
+
+def pa_decode_mq(out, lse, q, k_cache, v_cache, block_tables, seq_lens, scale, num_splits=0,
+                 workspace=None, status=None, stream=None):
+    """Causal multi-query decode: q and out are [B, q_len, Hq, D], lse [B, q_len, Hq]."""
+    _need(q, "q", torch.bfloat16, 4)
+    B, q_len, Hq, D = q.shape
+    _decode_inputs(q.view(B, q_len * Hq, D), k_cache, v_cache, block_tables, seq_lens)
+    _need(out, "out", torch.bfloat16, 4)
+    if tuple(out.shape) != tuple(q.shape):
+        raise ValueError("out must be [B, q_len, Hq, D]")
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 3)
+    ws_bytes = 0
+    if workspace is not None:
+        if not (workspace.is_cuda and workspace.is_contiguous()):
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    rc = lib().pa_decode_mq(_ptr(out), _ptr(lse), _ptr(q), q_len, _ptr(k_cache), _ptr(v_cache),
+                            cache_desc(k_cache), _ptr(block_tables), block_tables.shape[1],
+                            _ptr(seq_lens), B, Hq, float(scale), num_splits, _ptr(workspace),
+                            ws_bytes, _ptr(status), _stream(stream))
+    _check("pa_decode_mq", rc)
 
 
 def pa_decode_splitkv_noalloc(out, lse, q, k_cache, v_cache, block_tables, seq_lens, scale,

@@ -76,6 +76,24 @@ class Dev:
                           workspace=ws, status=self.status)
         return out, lse, P
 
+    def mq(self, num_splits=0):
+        """Causal multi-query decode (pa_decode_mq) of the workload's q_len queries."""
+        w = self.w
+        q_len = w.q_len
+        q = self.q.view(w.B, q_len, w.Hq, w.D)
+        P = num_splits
+        if P == 0:
+            sms = torch.cuda.get_device_properties(0).multi_processor_count
+            P = pa.pa_choose_num_splits_mq(w.B, q_len, w.Hq, w.Hkv, w.D, w.max_blocks,
+                                           w.block_size, sms)
+        ws = torch.zeros(max(1, pa.pa_splitkv_workspace_bytes(w.B * q_len, w.Hq, w.D, P)),
+                         dtype=torch.uint8, device="cuda")
+        out = torch.empty((w.B, q_len, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((w.B, q_len, w.Hq), dtype=torch.float32, device="cuda")
+        pa.pa_decode_mq(out, lse, q, self.k_cache, self.v_cache, self.block_tables, self.seq_lens,
+                        w.scale, num_splits=P, workspace=ws, status=self.status)
+        return out, lse, P
+
     def pools(self):
         f = lambda t: t.view(torch.int16).cpu().numpy().view(np.uint16)
         return f(self.k_cache), f(self.v_cache)

@@ -199,3 +199,44 @@ def test_decode_step_rejects_bad_arguments(lib):
     assert rc == pa.PA_EINVAL   # misaligned k_new
     assert lib.pa_decode_step(None, None, None, None, None, None, None, None, d, None, 7, None, 0,
                               4, 0.125, 1, None, 0, None, None) == pa.PA_OK   # empty batch
+
+
+def test_mq_split_policy(lib, monkeypatch):
+    monkeypatch.delenv("PA_DECODE_KERNEL", raising=False)
+    for args in ((8, 28, 4, 128, 256, 16, 152), (1, 28, 4, 128, 2048, 16, 152),
+                 (256, 16, 8, 128, 128, 16, 152), (3, 12, 2, 128, 100, 16, 132)):
+        B, Hq, Hkv, D, mb, bs, sms = args
+        assert pa.pa_choose_num_splits_mq(B, 1, Hq, Hkv, D, mb, bs, sms) == \
+            pa.pa_choose_num_splits(B, Hq, Hkv, D, mb, bs, sms)
+    # 7B layer, 4 queries: 16 // 7 = 2 positions per CTA -> 2 query groups of 4 heads
+    # per sequence -> 16 CTAs per split -> one wave of 152 SMs holds P = 9
+    assert pa.pa_choose_num_splits_mq(8, 4, 28, 4, 128, 256, 16, 152) == 9
+    # Qwen3 shape, 4 queries: all fit one CTA per 8 KV heads -> as q_len = 1
+    assert pa.pa_choose_num_splits_mq(256, 4, 16, 8, 128, 128, 16, 152) == 1
+    # more query groups never give more splits
+    prev = 10 ** 9
+    for q_len in (1, 2, 3, 5, 8, 16, 64):
+        P = pa.pa_choose_num_splits_mq(1, q_len, 12, 2, 128, 512, 16, 152)
+        assert 1 <= P <= prev
+        prev = P
+
+
+def test_mq_rejects_what_it_cannot_run(lib, monkeypatch):
+    monkeypatch.delenv("PA_DECODE_KERNEL", raising=False)
+    assert lib.pa_choose_num_splits_mq(2, 2, 8, 2, 64, 16, 16, 152) == pa.PA_EUNSUPPORTED   # D = 64
+    assert lib.pa_choose_num_splits_mq(2, 0, 8, 2, 128, 16, 16, 152) == pa.PA_EINVAL
+    assert lib.pa_choose_num_splits_mq(2, 1, 8, 2, 64, 16, 16, 152) >= 1                    # decode
+    monkeypatch.setenv("PA_DECODE_KERNEL", "cuda_core")
+    assert lib.pa_choose_num_splits_mq(2, 2, 8, 2, 128, 16, 16, 152) == pa.PA_EUNSUPPORTED
+    monkeypatch.delenv("PA_DECODE_KERNEL")
+    d = _desc(d=128)
+    for q_len in (0, -3, 70000):
+        rc = lib.pa_decode_mq(FAKE, None, FAKE, q_len, FAKE, FAKE, d, FAKE, 7, FAKE, 4, 4, 0.1, 1,
+                              None, 0, None, None)
+        assert rc == pa.PA_EINVAL, q_len
+    rc = lib.pa_decode_mq(FAKE, None, FAKE, 2, FAKE, FAKE, d, FAKE, 7, FAKE, 4, 4, 0.1, 3,
+                          None, 0, None, None)
+    assert rc == pa.PA_EWORKSPACE       # P > 1 without a workspace
+    rc = lib.pa_decode_mq(FAKE, None, FAKE, 2, FAKE, FAKE, _desc(d=64), FAKE, 7, FAKE, 4, 4, 0.1, 1,
+                          None, 0, None, None)
+    assert rc == pa.PA_EUNSUPPORTED     # D = 64

@@ -396,3 +396,80 @@ def test_decode_step_replays_in_a_cuda_graph():
     graph.replay()
     torch.cuda.synchronize()
     assert torch.equal(out, eager)
+
+
+# ------------------------------------------- multi-query (causal) decode
+MQ_SMALL = [
+    # (Hq, Hkv, D, bs, lens, q_len)
+    (8, 8, 128, 16, (1, 15, 16, 17, 40), 4),        # G = 1, all 4 queries in one CTA
+    (12, 2, 128, 16, (48, 130, 7), 2),              # G = 6
+    (28, 4, 128, 16, (257, 16, 3), 4),              # G = 7: 2 query groups
+    (16, 8, 128, 16, (200, 129, 5), 8),             # G = 2, 16 columns per head
+    (32, 2, 128, 16, (129, 300), 3),                # G = 16: one query per CTA
+    (16, 4, 128, 256, (300, 513, 2), 5),            # pages; L < q_len
+    (6, 2, 128, 16, (70, 33), 16),                  # G = 3: 5 queries per CTA, 4 groups
+]
+
+
+@pytest.mark.parametrize("case", MQ_SMALL, ids=lambda c: f"Hq{c[0]}-Hkv{c[1]}-bs{c[3]}-q{c[5]}")
+def test_mq_small_elementwise(case):
+    Hq, Hkv, D, bs, lens, q_len = case
+    nb = sum((L + bs - 1) // bs for L in lens) + 5
+    w = W.make_workload("mq", B=len(lens), Hq=Hq, Hkv=Hkv, D=D, block_size=bs, seq_lens=list(lens),
+                        num_blocks=nb, seed=sum(lens) + q_len, poison_unused=True, q_len=q_len)
+    kc, vc = oracle_after_write(w)
+    ref, ref_lse = oracle.decode_mq(w.q, kc, vc, w.block_tables, w.seq_lens, w.scale)
+    dev = Dev(w)
+    dev.write()
+    for P in (1, 2, 3, 7, 0):
+        out, lse, Pu = dev.mq(P)
+        assert_close(bf16_dev_to_f64(out), ref, f"pa_decode_mq P={Pu}")
+        assert_lse_close(lse.cpu().double().numpy(), ref_lse, f"pa_decode_mq P={Pu}")
+    assert dev.status_value() == 0
+
+
+def test_mq_single_query_is_splitkv_bit_exact():
+    w = W.make_workload("mq1", B=3, Hq=28, Hkv=4, D=128, block_size=16, seq_lens=[300, 17, 1024],
+                        num_blocks=100, seed=5, q_len=1)
+    dev = Dev(w)
+    dev.write()
+    for P in (1, 4):
+        o1, l1, _ = dev.splitkv(P)
+        q = dev.q.view(w.B, 1, w.Hq, w.D)
+        ws = torch.zeros(max(1, pa.pa_splitkv_workspace_bytes(w.B, w.Hq, w.D, P)),
+                         dtype=torch.uint8, device="cuda")
+        o2 = torch.empty((w.B, 1, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
+        l2 = torch.empty((w.B, 1, w.Hq), dtype=torch.float32, device="cuda")
+        pa.pa_decode_mq(o2, l2, q, dev.k_cache, dev.v_cache, dev.block_tables, dev.seq_lens,
+                        w.scale, num_splits=P, workspace=ws)
+        assert torch.equal(o1, o2[:, 0]) and torch.equal(l1, l2[:, 0]), f"P={P}"
+
+
+def test_mq_chunk_of_64_queries():
+    """A small prefill-like chunk: 64 new tokens per sequence, G = 7 (32 query groups)."""
+    w = W.make_workload("chunk", B=2, Hq=28, Hkv=4, D=128, block_size=16, seq_lens=[600, 64],
+                        num_blocks=48, seed=77, q_len=64)
+    kc, vc = oracle_after_write(w)
+    ref, ref_lse = oracle.decode_mq(w.q, kc, vc, w.block_tables, w.seq_lens, w.scale)
+    dev = Dev(w)
+    dev.write()
+    for P in (1, 3):
+        out, lse, _ = dev.mq(P)
+        assert_close(bf16_dev_to_f64(out), ref, f"chunk P={P}")
+        assert_lse_close(lse.cpu().double().numpy(), ref_lse, f"chunk P={P}")
+
+
+@pytest.mark.parametrize("name", ["qwen2.5-1.5b-B8-spec4", "qwen2.5-7b-bs16-spec4",
+                                  "qwen3-0.6b-B256-spec4"])
+def test_mq_workload_full_size(name):
+    """The bench's launch configuration (auto P) and unsplit, against the oracle."""
+    w = W.WORKLOADS[name]()
+    kc, vc = oracle_after_write(w)
+    ref, ref_lse = oracle.decode_mq(w.q, kc, vc, w.block_tables, w.seq_lens, w.scale)
+    dev = Dev(w)
+    dev.write()
+    for P in (0, 1):
+        out, lse, Pu = dev.mq(P)
+        assert_close(bf16_dev_to_f64(out), ref, f"{name} P={Pu}")
+        assert_lse_close(lse.cpu().double().numpy(), ref_lse, f"{name} P={Pu}")
+    assert dev.status_value() == 0
