@@ -588,9 +588,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         }
 
         // ---- epilogue: row sums, O^T, normalise, store ----------------------------------
-        bool okf = !dead && wait_or_abort(&pfree[(nch - 1) % NBP], ((nch - 1) / NBP) & 1);
-        okf = named_sync_or(1, 128, !okf) ? false : true;
-        // row sums of every column (head, q) over that head's rows, via shared memory
+        // The row sums are final once the last chunk's p is written, so they are
+        // reduced (through shared memory) while its PV still runs.
 #pragma unroll
         for (int q = 0; q < GP; ++q) red[tid * GP + q] = l_thr[q];
         named_sync(1, 128);
@@ -601,7 +600,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             const int c = tid % GP;
             rel_s[tid] = c < Gq ? static_cast<int>(col_row(tid / GP, c) - row0) : -1;
         }
-        named_sync(1, 128);  // col[] / alpha_s complete before they are read
+        bool okf = !dead && wait_or_abort(&pfree[(nch - 1) % NBP], ((nch - 1) / NBP) & 1);
+        // (this barrier also publishes col[], alpha_s and rel_s)
+        okf = named_sync_or(1, 128, !okf) ? false : true;
         if (okf) {
             tc5::fence_after_sync();
             // O^T row d = tid, 16 columns at a time, normalised and stored; column
