@@ -60,6 +60,9 @@ def _bind(lib):
     lib.oracle_decode_partial.argtypes = [P, P, P, P, P, i32, i32, i32, i32,
                                           P, i32, P, i32, i32, f32, i32, i32, P, i32]
     lib.oracle_combine.argtypes = [P, P, P, P, i64, i32, i32]
+    lib.oracle_e4m3_to_bf16.argtypes = [P, P, i64]
+    lib.oracle_bf16_to_e4m3.argtypes = [P, P, i64, f32]
+    lib.oracle_cache_write_fp8.argtypes = [P, P, P, i64, P, P, i32, i32, i32, i32, f32, f32]
     lib.oracle_decode_mq.argtypes = [P, P, P, i32, P, P, i32, i32, i32, i32, P, i32, P, i32, i32,
                                      f32, P, i32]
     lib.oracle_max_threads.argtypes = []
@@ -190,6 +193,53 @@ def decode(q, k_cache, v_cache, block_tables, seq_lens, scale, nthreads: int = 0
     out, lse = decode_rows(q, k_cache, v_cache, block_tables, seq_lens, scale,
                            bb.ravel(), hh.ravel(), nthreads)
     return out.reshape(B, Hq, D), lse.reshape(B, Hq)
+
+
+# ------------------------------------------------------------------ FP8 KV
+def e4m3_to_bf16(codes):
+    """Exact widening of e4m3 codes (uint8) to bf16 bit patterns (uint16)."""
+    codes = _req(codes, np.uint8)
+    out = np.empty(codes.shape, np.uint16)
+    _check(_load().oracle_e4m3_to_bf16(_ptr(out), _ptr(codes), codes.size), "oracle_e4m3_to_bf16")
+    return out
+
+
+def bf16_to_e4m3(x, scale):
+    """Quantise bf16 bit patterns to e4m3 codes: RNE of fp32(x) / scale, saturating at +-448."""
+    x = _req(x, np.uint16)
+    out = np.empty(x.shape, np.uint8)
+    _check(_load().oracle_bf16_to_e4m3(_ptr(out), _ptr(x), x.size, float(scale)),
+           "oracle_bf16_to_e4m3")
+    return out
+
+
+def cache_write_fp8(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale):
+    """In-place slot-mapping scatter of quantised rows into uint8 e4m3 pools."""
+    k_new = _req(k_new, np.uint16)
+    v_new = _req(v_new, np.uint16)
+    slot_mapping = _req(slot_mapping, np.int64)
+    if k_cache.dtype != np.uint8 or v_cache.dtype != np.uint8:
+        raise TypeError("fp8 pools must be uint8")
+    if not (k_cache.flags.c_contiguous and v_cache.flags.c_contiguous):
+        raise ValueError("pools must be C-contiguous")
+    nb, bs, hkv, d = k_cache.shape
+    rc = _load().oracle_cache_write_fp8(_ptr(k_new), _ptr(v_new), _ptr(slot_mapping),
+                                        slot_mapping.shape[0], _ptr(k_cache), _ptr(v_cache),
+                                        nb, bs, hkv, d, float(k_scale), float(v_scale))
+    _check(rc, "oracle_cache_write_fp8")
+
+
+def decode_fp8(q, k_cache, v_cache, block_tables, seq_lens, scale, k_scale, v_scale,
+               nthreads: int = 0):
+    """Exact attention over e4m3 pools holding k_scale * K and v_scale * V.
+    A per-pool scale factors out of the attention exactly: scores use
+    scale * k_scale on the widened codes, and the output is multiplied by
+    v_scale.  Returns (out[B, Hq, D], lse[B, Hq]) in fp64."""
+    kw = e4m3_to_bf16(k_cache)
+    vw = e4m3_to_bf16(v_cache)
+    out, lse = decode(q, kw, vw, block_tables, seq_lens, np.float32(scale) * np.float32(k_scale),
+                      nthreads)
+    return out * float(v_scale), lse
 
 
 def decode_mq(q, k_cache, v_cache, block_tables, seq_lens, scale, nthreads: int = 0):

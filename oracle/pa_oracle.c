@@ -107,6 +107,95 @@ int oracle_cache_write(const uint16_t *k_new, const uint16_t *v_new,
     return ORACLE_OK;
 }
 
+/*
+ * FP8 KV cache.  The pages say only that the KV-cache manager supports
+ * several quantisation schemes ("Mini-Infer: A High-Performance LLM Inference
+ * Acceleration Engine for Production Environments", section "Memory
+ * Optimization and KV Cache Management"); the plainest
+ * reading for a KV cache is OCP FP8 E4M3 ("e4m3fn": 1 sign bit, 4 exponent
+ * bits with bias 7, 3 mantissa bits, no infinities, S.1111.111 = NaN, largest
+ * finite value 448) with one fp32 scale per pool: a stored code c means the
+ * value e4m3(c) * scale.  Writing a bf16 value x stores
+ *     c = round_to_nearest_even_e4m3(fp32(x) / scale)   (fp32 IEEE division),
+ * saturating at +-448 (the largest finite code) and keeping NaN as NaN.
+ */
+static double e4m3_value(uint8_t c) {
+    const int e = (c >> 3) & 15, m = c & 7;
+    double mag;
+    if (e == 15 && m == 7) mag = NAN;
+    else if (e == 0) mag = ldexp((double)m, -9);          /* subnormal: m/8 * 2^-6 */
+    else mag = ldexp((double)(8 + m), e - 10);            /* (1 + m/8) * 2^(e-7) */
+    return (c & 0x80) ? -mag : mag;
+}
+
+static uint8_t f32_to_e4m3_sat(float f) {
+    if (isnan(f)) return 0x7F;
+    const uint8_t sign = signbit(f) ? 0x80 : 0x00;
+    const double a = fabs((double)f);
+    if (a >= 448.0) return sign | 0x7E;
+    /* codes 0x00..0x7E are increasing in value: bracket a, take the nearer,
+     * ties to the even code (the code's last bit is the mantissa's) */
+    int lo = 0, hi = 0x7E;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) / 2;
+        if (e4m3_value((uint8_t)mid) <= a) lo = mid;
+        else hi = mid;
+    }
+    const double dl = a - e4m3_value((uint8_t)lo), dh = e4m3_value((uint8_t)hi) - a;
+    const int code = dl < dh ? lo : dh < dl ? hi : ((lo & 1) ? hi : lo);
+    return sign | (uint8_t)code;
+}
+
+/* Widen e4m3 codes to bf16 bit patterns (exact: every e4m3 value is a bf16 value). */
+int oracle_e4m3_to_bf16(uint16_t *out, const uint8_t *in, int64_t n) {
+    if (n < 0) return ORACLE_EBADARG;
+    for (int64_t i = 0; i < n; ++i) {
+        const float f = (float)e4m3_value(in[i]);
+        uint32_t bits;
+        memcpy(&bits, &f, sizeof bits);
+        out[i] = isnan(f) ? (uint16_t)(0x7FC0 | ((in[i] & 0x80) << 8)) : (uint16_t)(bits >> 16);
+    }
+    return ORACLE_OK;
+}
+
+/* Quantise bf16 values to e4m3 codes with one scale, as defined above. */
+int oracle_bf16_to_e4m3(uint8_t *out, const uint16_t *in, int64_t n, float scale) {
+    if (n < 0 || !(scale > 0.0f)) return ORACLE_EBADARG;
+    for (int64_t i = 0; i < n; ++i) {
+        const float x = (float)bf16_to_f64(in[i]);
+        out[i] = f32_to_e4m3_sat(x / scale);
+    }
+    return ORACLE_OK;
+}
+
+/* Slot-mapping write into e4m3 pools: the cache write above, with each new
+ * K (V) row quantised with k_scale (v_scale). */
+int oracle_cache_write_fp8(const uint16_t *k_new, const uint16_t *v_new,
+                           const int64_t *slot_mapping, int64_t n_tokens,
+                           uint8_t *k_cache, uint8_t *v_cache,
+                           int num_blocks, int block_size, int num_kv_heads, int head_dim,
+                           float k_scale, float v_scale) {
+    if (n_tokens < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+        !(k_scale > 0.0f) || !(v_scale > 0.0f))
+        return ORACLE_EBADARG;
+    const int64_t n_slots = (int64_t)num_blocks * block_size;
+    const int64_t row = (int64_t)num_kv_heads * head_dim;
+    for (int64_t i = 0; i < n_tokens; ++i) {
+        const int64_t s = slot_mapping[i];
+        if (s < 0) continue;
+        if (s >= n_slots) return ORACLE_ESLOT;
+        for (int64_t j = 0; j < i; ++j)
+            if (slot_mapping[j] == s) return ORACLE_ESLOT;
+    }
+    for (int64_t i = 0; i < n_tokens; ++i) {
+        const int64_t s = slot_mapping[i];
+        if (s < 0) continue;
+        oracle_bf16_to_e4m3(k_cache + s * row, k_new + i * row, row, k_scale);
+        oracle_bf16_to_e4m3(v_cache + s * row, v_new + i * row, row, v_scale);
+    }
+    return ORACLE_OK;
+}
+
 /* Pointer to K or V row (token t of sequence b, KV head g) through the block table. */
 static const uint16_t *gather_row(const uint16_t *cache, const int32_t *bt_row, int t,
                                   int block_size, int num_kv_heads, int head_dim, int g) {

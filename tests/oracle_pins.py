@@ -397,4 +397,95 @@ def pin_mq_last_query_is_decode():
         assert np.array_equal(out[:, i], oi) and np.array_equal(lse[:, i], li)
 
 
+# ------------------------------------------------------------------ FP8 KV
+# ("Mini-Infer: A High-Performance LLM Inference Acceleration Engine for
+# Production Environments", section "Memory Optimization and KV Cache
+# Management": several quantisation schemes; read as OCP e4m3 with one fp32
+# scale per pool.)  torch's float8_e4m3fn is the independent reference.
+def _torch_e4m3(codes: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(codes)).view(torch.float8_e4m3fn)
+
+
+def pin_fp8_widen_every_code():
+    """All 256 codes widen to bf16 exactly as torch's e4m3 type does (NaN codes to NaN)."""
+    codes = np.arange(256, dtype=np.uint8)
+    got = oracle.e4m3_to_bf16(codes)
+    ref = _torch_e4m3(codes).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    nan = np.isnan(_torch_e4m3(codes).float().numpy())
+    assert list(codes[nan]) == [0x7F, 0xFF]
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.all(np.isnan(bf16_to_f64(got[nan])))
+
+
+def pin_fp8_quantise_matches_torch_in_range():
+    """bf16 / scale (fp32) rounded to e4m3 equals torch's cast, bit for bit, inside +-448,
+    including values exactly halfway between codes (ties to even) and subnormals."""
+    rng = np.random.default_rng(41)
+    vals = [rng.standard_normal(4000) * 3, rng.standard_normal(1000) * 1e-2,
+            rng.uniform(-440, 440, 1000)]
+    w = _torch_e4m3(np.arange(0x7F, dtype=np.uint8)).float().numpy().astype(np.float64)
+    mids = (w[1:] + w[:-1]) / 2                                     # halfway points (exact in bf16)
+    x = np.concatenate(vals + [mids, -mids])
+    bits = f64_to_bf16_bits(x)
+    for scale in (1.0, 0.0625, 0.37):
+        got = oracle.bf16_to_e4m3(bits, scale)
+        xf = torch.from_numpy(bf16_to_f64(bits)).float() / torch.tensor(scale, dtype=torch.float32)
+        inside = xf.abs() <= 448
+        ref = xf.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        assert np.array_equal(got[inside.numpy()], ref[inside.numpy()]), f"scale {scale}"
+
+
+def pin_fp8_quantise_saturates_and_round_trips():
+    """Beyond +-448 the code saturates to +-448; NaN stays NaN; every finite code
+    survives widen-then-quantise with scale 1."""
+    big = f64_to_bf16_bits(np.array([449.0, 1e4, -3e5, -449.0]))
+    assert list(oracle.bf16_to_e4m3(big, 1.0)) == [0x7E, 0x7E, 0xFE, 0xFE]
+    nan = np.array([0x7FC0], np.uint16)
+    assert oracle.bf16_to_e4m3(nan, 1.0)[0] & 0x7F == 0x7F
+    codes = np.array([c for c in range(256) if c & 0x7F != 0x7F], np.uint8)
+    assert np.array_equal(oracle.bf16_to_e4m3(oracle.e4m3_to_bf16(codes), 1.0), codes)
+
+
+def pin_fp8_decode_equals_sdpa_on_dequantised_cache():
+    """Attention over e4m3 pools equals SDPA over torch-dequantised contiguous K/V
+    (code * scale in fp64, the softmax scale applied as given): the factored
+    scales agree to fp32 rounding of scale * k_scale (1e-6)."""
+    w = small_case(B=3, Hq=6, Hkv=2, D=32, lens=(5, 16, 41), nb=24, seed=51)
+    ks, vs = 0.043, 0.029
+    k8 = oracle.bf16_to_e4m3(w.k_cache, ks)
+    v8 = oracle.bf16_to_e4m3(w.v_cache, vs)
+    out, lse = oracle.decode_fp8(w.q, k8, v8, w.block_tables, w.seq_lens, w.scale, ks, vs)
+    kd = _torch_e4m3(k8).double().numpy() * ks
+    vd = _torch_e4m3(v8).double().numpy() * vs
+    for b in range(w.B):
+        L = int(w.seq_lens[b])
+        t = np.arange(L)
+        phys, off = w.block_tables[b][t // w.block_size], t % w.block_size
+        kt = torch.from_numpy(kd[phys, off]).permute(1, 0, 2).repeat_interleave(w.G, dim=0)
+        vt = torch.from_numpy(vd[phys, off]).permute(1, 0, 2).repeat_interleave(w.G, dim=0)
+        q = torch.from_numpy(bf16_to_f64(w.q[b]))[:, None, :]
+        o = torch.nn.functional.scaled_dot_product_attention(q, kt, vt, scale=float(w.scale))
+        err = np.abs(out[b] - o[:, 0].numpy()).max()
+        assert err < 1e-6, f"fp8 decode vs dequantised SDPA: {err}"
+
+
+def pin_fp8_cache_write_quantises_the_new_rows():
+    """The fp8 write stores exactly bf16_to_e4m3 of each new row at its slot."""
+    w = W.make_workload("pin", B=3, Hq=4, Hkv=2, D=16, block_size=16, seq_lens=[1, 16, 35],
+                        num_blocks=12, seed=52)
+    kc = np.full(w.k_cache.shape, 0x11, np.uint8)
+    vc = np.full(w.v_cache.shape, 0x22, np.uint8)
+    oracle.cache_write_fp8(w.k_new, w.v_new, w.slot_mapping, kc, vc, 0.5, 0.25)
+    ek = np.full_like(kc, 0x11).reshape(-1, w.Hkv, w.D)
+    ev = np.full_like(vc, 0x22).reshape(-1, w.Hkv, w.D)
+    ek[w.slot_mapping] = _torch_e4m3_from(w.k_new, 0.5)
+    ev[w.slot_mapping] = _torch_e4m3_from(w.v_new, 0.25)
+    assert np.array_equal(kc.reshape(ek.shape), ek) and np.array_equal(vc.reshape(ev.shape), ev)
+
+
+def _torch_e4m3_from(bits: np.ndarray, scale: float) -> np.ndarray:
+    x = torch.from_numpy(bf16_to_f64(bits)).float() / torch.tensor(scale, dtype=torch.float32)
+    return x.clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

@@ -50,6 +50,9 @@ MUTANTS = {
                                   "const int i = q_len - 1;"),
     "mq sequence index wrong": ("const int b = (int)(r / ((int64_t)Hq * q_len));",
                                 "const int b = (int)((r / Hq) % B);"),
+    "e4m3 exponent bias off by one": ("ldexp((double)(8 + m), e - 10)", "ldexp((double)(8 + m), e - 9)"),
+    "e4m3 ties rounded up": ("dh < dl ? hi : ((lo & 1) ? hi : lo)", "dh < dl ? hi : hi"),
+    "e4m3 overflow to NaN": ("if (a >= 448.0) return sign | 0x7E;", "if (a >= 448.0) return sign | 0x7F;"),
 }
 
 
