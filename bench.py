@@ -208,6 +208,18 @@ def time_oracle(w, budget_s: float, max_rows: int | None = None, nthreads: int =
     if w.slot_mapping.size:
         oracle.cache_write(w.k_new, w.v_new, w.slot_mapping, kc, vc)
     t_write = time.perf_counter() - t0
+    if w.fp8:   # e4m3 pools: whole workload per repetition
+        kc8, vc8 = w.k_cache8.copy(), w.v_cache8.copy()
+        oracle.cache_write_fp8(w.k_new, w.v_new, w.slot_mapping, kc8, vc8, w.k_scale, w.v_scale)
+        reps, secs = 0, 0.0
+        while reps == 0 or secs < budget_s:
+            t0 = time.perf_counter()
+            oracle.decode_fp8(w.q, kc8, vc8, w.block_tables, w.seq_lens, w.scale, w.k_scale,
+                              w.v_scale, threads)
+            secs += time.perf_counter() - t0
+            reps += 1
+        desc = f"whole workload {w.name} (e4m3 pools, widened) x {reps} reps, fp64, write excluded"
+        return secs, float(w.kv_bytes() + w.qo_bytes()) * reps, reps * w.B * w.Hq, threads, desc
     if w.q_len > 1:   # multi-query: whole workload per repetition
         reps, secs = 0, 0.0
         while reps == 0 or secs < budget_s:
@@ -302,7 +314,8 @@ def run_ours(args, world, rank, local):
     bt = to_dev(w.block_tables)
     sl = to_dev(w.seq_lens)
     kn, vn, slots = to_dev(w.k_new), to_dev(w.v_new), to_dev(w.slot_mapping)
-    k0, v0 = to_dev(w.k_cache), to_dev(w.v_cache)
+    fp8 = w.fp8   # e4m3 pools: write with pa_cache_write_fp8, decode with pa_decode_splitkv_fp8
+    k0, v0 = (to_dev(w.k_cache8), to_dev(w.v_cache8)) if fp8 else (to_dev(w.k_cache), to_dev(w.v_cache))
     touched = w.kv_bytes()
     R = max(1, min(8, math.ceil(2.5 * L2_BYTES / max(touched, 1)) + 1)) if touched < 3 * L2_BYTES else 1
     pools = [(k0, v0)] + [(k0.clone(), v0.clone()) for _ in range(R - 1)]
@@ -327,11 +340,16 @@ def run_ours(args, world, rank, local):
 
     def step(r, ev0=None, ev1=None):
         kc, vc = pools[r]
-        if args.unfused or mq:
+        if fp8:
+            pa.pa_cache_write_fp8(kn, vn, slots, kc, vc, w.k_scale, w.v_scale, stream=stream)
+        elif args.unfused or mq:
             pa.pa_cache_write(kn, vn, slots, kc, vc, stream=stream)
         if ev0 is not None:
             ev0.record(stream)
-        if mq:
+        if fp8:
+            pa.pa_decode_splitkv_fp8(out, lse, q, kc, vc, w.k_scale, w.v_scale, bt, sl, w.scale,
+                                     num_splits=P, workspace=ws, stream=stream)
+        elif mq:
             pa.pa_decode_mq(out, lse, q, kc, vc, bt, sl, w.scale, num_splits=P, workspace=ws,
                             stream=stream)
         elif args.unfused:
@@ -343,7 +361,7 @@ def run_ours(args, world, rank, local):
         if ev1 is not None:
             ev1.record(stream)
 
-    fused = not (args.unfused or mq)
+    fused = not (args.unfused or mq or fp8)
     launches_per_step = 1 if fused else 2
     # CUDA graphs of S consecutive steps (cycling over the pool replicas), NG
     # copies, each step with its own pair of graph-recorded events around the
@@ -422,7 +440,11 @@ def run_ours(args, world, rank, local):
             for d, h in ((d_q16, h_q), (bt, h_bt), (sl, h_sl), (d_kn16, h_kn), (d_vn16, h_vn),
                          (slots, h_slots)):
                 d.copy_(h, non_blocking=True)
-            if mq:
+            if fp8:
+                pa.pa_cache_write_fp8(kn, vn, slots, kc, vc, w.k_scale, w.v_scale, stream=stream)
+                pa.pa_decode_splitkv_fp8(out, lse, q, kc, vc, w.k_scale, w.v_scale, bt, sl, w.scale,
+                                         num_splits=P, workspace=ws, stream=stream)
+            elif mq:
                 pa.pa_cache_write(kn, vn, slots, kc, vc, stream=stream)
                 pa.pa_decode_mq(out, lse, q, kc, vc, bt, sl, w.scale, num_splits=P, workspace=ws,
                                 stream=stream)
@@ -456,7 +478,7 @@ def run_ours(args, world, rank, local):
         roofline = {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
                     "frac": round(ach / peak, 4), "traffic": recorded_traffic(args.workload, kernel_name),
                     "peak_kind": peak_kind,
-                    "kernel": kernel_name + (" (multi-query)" if mq else
+                    "kernel": kernel_name + (" (fp8 pools)" if fp8 else " (multi-query)" if mq else
                                              "" if args.unfused else " (fused write)")
                               + (" + split merge" if merged else ""),
                     "kernel_us": round(kern_ms_avg * 1e3, 3), "kernel_bytes": kern_bytes}
@@ -476,7 +498,9 @@ def run_ours(args, world, rank, local):
             "config": {"workload": args.workload, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
                        "block_size": w.block_size, "seq_lens_total": int(w.seq_lens.sum()),
                        "splits": P, "q_len": w.q_len,
-                       "step": ("cache_write of the q_len new tokens, then pa_decode_mq (causal)"
+                       "step": ("pa_cache_write_fp8, then pa_decode_splitkv_fp8 (e4m3 pools)"
+                                if fp8 else
+                                "cache_write of the q_len new tokens, then pa_decode_mq (causal)"
                                 if mq else "cache_write, then split decode with merge"
                                 if args.unfused else
                                 "pa_decode_step: cache write + split decode + merge, one launch"),

@@ -295,6 +295,44 @@ int pa_decode_mq(void *out, float *lse, const void *q, int32_t q_len, const void
                  int32_t *status, pa_stream_t stream);
 
 /*
+ * FP8 KV cache.  The pages say only that the KV-cache manager supports several
+ * quantisation schemes ("Mini-Infer: A High-Performance LLM Inference
+ * Acceleration Engine for Production Environments", section "Memory
+ * Optimization and KV Cache Management").  Here: pools of one-byte OCP e4m3
+ * codes (4 exponent bits, bias 7; 3 mantissa bits; no infinities; 0x7F/0xFF
+ * NaN; largest finite 448), [num_blocks, block_size, Hkv, D] uint8, with one
+ * fp32 scale per pool: a code c stands for e4m3(c) * scale.  Half the bytes
+ * of a bf16 pool per token.
+ */
+
+/*
+ * Slot-mapping write into FP8 pools: as pa_cache_write, each new bf16 row
+ * stored as round_to_nearest_even_e4m3(fp32(x) / scale), saturating at +-448
+ * (NaN stays NaN).  k_scale, v_scale: finite and > 0, else PA_EINVAL.
+ * k_cache, v_cache: device uint8 pools described by `cache`.
+ */
+int pa_cache_write_fp8(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                       int64_t n_tokens, void *k_cache, void *v_cache, pa_cache_desc cache,
+                       float k_scale, float v_scale, int32_t *status, pa_stream_t stream);
+
+/*
+ * Split-KV decode attention over FP8 pools: pa_decode_splitkv's arguments and
+ * results (num_splits 0 = pa_auto_num_splits, 1 = no split and no workspace,
+ * the same workspace contract otherwise), with k_cache / v_cache e4m3 pools
+ * and their scales.  The result is attention over the dequantised values
+ * (code * scale); the tensor-core kernel widens each landed tile to fp16
+ * exactly and runs its MMAs in fp16 (q is rounded to fp16: |q| must stay below
+ * 65504).  Supported: head_dim 128, Hq / Hkv <= 16 (PA_EUNSUPPORTED
+ * otherwise, and with PA_DECODE_KERNEL=cuda_core).
+ */
+int pa_decode_splitkv_fp8(void *out, float *lse, const void *q, const void *k_cache,
+                          const void *v_cache, pa_cache_desc cache, float k_scale, float v_scale,
+                          const int32_t *block_tables, int32_t max_blocks_per_seq,
+                          const int32_t *seq_lens, int32_t B, int32_t Hq, float scale,
+                          int32_t num_splits, void *workspace, size_t workspace_bytes,
+                          int32_t *status, pa_stream_t stream);
+
+/*
  * Split count for pa_decode_mq, by the rule of pa_choose_num_splits with the
  * CTAs of every query-position group counted.  q_len = 1 gives
  * pa_choose_num_splits.  Returns P >= 1, or PA_EINVAL / PA_EUNSUPPORTED.

@@ -22,6 +22,9 @@ cudaError_t launch_decode_cc_d128(int G, const CUtensorMap &kmap, const CUtensor
 cudaError_t launch_decode_tc(int HC, int GP, int G, const CUtensorMap &kmap,
                              const CUtensorMap &vmap, const DecodeParams &p, int B,
                              cudaStream_t stream);
+cudaError_t launch_decode_tc_f8(int HC, int GP, int G, const CUtensorMap &kmap,
+                                const CUtensorMap &vmap, const DecodeParams &p, int B,
+                                cudaStream_t stream);
 
 cudaError_t launch_decode_cc(int D, int G, const CUtensorMap &kmap, const CUtensorMap &vmap,
                              const DecodeParams &p, int B, cudaStream_t stream) {
@@ -177,6 +180,25 @@ int make_kv_map_heads(CUtensorMap *map, const void *base, const pa_cache_desc &c
     return r == CUDA_SUCCESS ? PA_OK : PA_ECUDA;
 }
 
+// An FP8 pool (one-byte e4m3 codes) for the tensor-core kernel: a 3-D view
+// (128 codes = one token row of one head, token rows, heads); one box is 16
+// token rows of HC heads, head-major, 128-byte swizzled.
+int make_kv_map_fp8(CUtensorMap *map, const void *base, const pa_cache_desc &c, int HC) {
+    auto enc = encode_fn();
+    if (!enc) return PA_ECUDA;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(c.head_dim),
+                                static_cast<cuuint64_t>(c.num_blocks) * c.block_size,
+                                static_cast<cuuint64_t>(c.num_kv_heads)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(c.num_kv_heads) * c.head_dim,
+                                   static_cast<cuuint64_t>(c.head_dim)};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(c.head_dim), 16u, static_cast<cuuint32_t>(HC)};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ECUDA;
+}
+
 int check_cache_desc(const pa_cache_desc &c) {
     if (c.num_blocks <= 0 || c.block_size <= 0 || c.num_kv_heads <= 0 || c.head_dim <= 0)
         return PA_EINVAL;
@@ -227,6 +249,7 @@ pa::DecodeParams base_params(const void *q, const pa_cache_desc &c, const int32_
     p.q_len = 1;
     p.q_per_cta = 1;
     p.head_groups = c.num_kv_heads;
+    p.v_scale = 1.f;
     return p;
 }
 
@@ -251,6 +274,11 @@ int sm_count_current() {
     return n;
 }
 
+// Scales of FP8 (e4m3) pools: a stored code c means c * scale.
+struct Fp8Scales {
+    float k_scale, v_scale;
+};
+
 // This step's new K/V for the fused write of pa_decode_step (all null: none).
 struct NewTokens {
     const void *k_new = nullptr;
@@ -263,13 +291,13 @@ int run_decode(bool split, void *out, float *lse, float *part_o, float *part_lse
                const int32_t *block_tables, int32_t max_blocks, const int32_t *seq_lens,
                int32_t B, int32_t Hq, float scale, int32_t P, int32_t *status,
                cudaStream_t stream, int32_t *counters = nullptr, const NewTokens &nt = NewTokens(),
-               int32_t q_len = 1) {
+               int32_t q_len = 1, const Fp8Scales *f8 = nullptr) {
     const int G = Hq / c.num_kv_heads;
     const int qpc = queries_per_cta(G, q_len);
     Kernel k;
     int rc = pick_kernel(G * qpc, c.head_dim, &k);
     if (rc) return rc;
-    if (q_len > 1 && k != Kernel::kTensorCore) return PA_EUNSUPPORTED;  // multi-query: tensor cores only
+    if ((q_len > 1 || f8) && k != Kernel::kTensorCore) return PA_EUNSUPPORTED;  // tensor cores only
     pa::DecodeParams p = base_params(q, c, block_tables, max_blocks, seq_lens, Hq, scale, status);
     p.q_len = q_len;
     p.q_per_cta = qpc;
@@ -293,10 +321,19 @@ int run_decode(bool split, void *out, float *lse, float *part_o, float *part_lse
         if (!tc_shape(G * qpc, c.num_kv_heads, &HC, &GP)) return PA_EUNSUPPORTED;
         p.head_groups = c.num_kv_heads / HC;
         if (static_cast<int64_t>(p.head_groups) * ((q_len + qpc - 1) / qpc) > 65535) return PA_EUNSUPPORTED;
-        rc = make_kv_map_heads(&kmap, k_cache, c, HC);
-        if (!rc) rc = make_kv_map_heads(&vmap, v_cache, c, HC);
-        if (rc) return rc;
-        e = pa::launch_decode_tc(HC, GP, G, kmap, vmap, p, B, stream);
+        if (f8) {
+            p.scale_log2 = scale * f8->k_scale * 1.4426950408889634f;
+            p.v_scale = f8->v_scale;
+            rc = make_kv_map_fp8(&kmap, k_cache, c, HC);
+            if (!rc) rc = make_kv_map_fp8(&vmap, v_cache, c, HC);
+            if (rc) return rc;
+            e = pa::launch_decode_tc_f8(HC, GP, G, kmap, vmap, p, B, stream);
+        } else {
+            rc = make_kv_map_heads(&kmap, k_cache, c, HC);
+            if (!rc) rc = make_kv_map_heads(&vmap, v_cache, c, HC);
+            if (rc) return rc;
+            e = pa::launch_decode_tc(HC, GP, G, kmap, vmap, p, B, stream);
+        }
     } else {
         rc = make_kv_map(&kmap, k_cache, c);
         if (!rc) rc = make_kv_map(&vmap, v_cache, c);
@@ -445,7 +482,8 @@ int splitkv_common(void *out, float *lse, const void *q, const void *k_cache, co
                    const pa_cache_desc &cache, const int32_t *block_tables,
                    int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t B, int32_t Hq,
                    float scale, int32_t num_splits, void *workspace, size_t workspace_bytes,
-                   int32_t *status, cudaStream_t stream, const NewTokens &nt, int32_t q_len = 1) {
+                   int32_t *status, cudaStream_t stream, const NewTokens &nt, int32_t q_len = 1,
+                   const Fp8Scales *f8 = nullptr) {
     int rc = check_decode_args(q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq,
                                seq_lens, B, Hq, scale);
     if (rc) return rc;
@@ -465,7 +503,7 @@ int splitkv_common(void *out, float *lse, const void *q, const void *k_cache, co
     if (P == 1)
         return run_decode(false, out, lse, nullptr, nullptr, q, k_cache, v_cache, cache,
                           block_tables, max_blocks_per_seq, seq_lens, B, Hq, scale, 1, status,
-                          stream, nullptr, nt, q_len);
+                          stream, nullptr, nt, q_len, f8);
     // rows of the partials: (sequence, query position, head)
     const int32_t Bq = B * q_len;
     const size_t need = pa_splitkv_workspace_bytes(Bq, Hq, cache.head_dim, P);
@@ -480,11 +518,11 @@ int splitkv_common(void *out, float *lse, const void *q, const void *k_cache, co
     // fits on the GPU at once; otherwise partials, then pa_combine.
     rc = run_decode(true, out, lse, part_o, part_lse, q, k_cache, v_cache, cache, block_tables,
                     max_blocks_per_seq, seq_lens, B, Hq, scale, P, status, stream, counters, nt,
-                    q_len);
+                    q_len, f8);
     if (rc != PA_ETOOLARGE) return rc;
     rc = run_decode(true, nullptr, nullptr, part_o, part_lse, q, k_cache, v_cache, cache,
                     block_tables, max_blocks_per_seq, seq_lens, B, Hq, scale, P, status, stream,
-                    nullptr, nt, q_len);
+                    nullptr, nt, q_len, f8);
     if (rc) return rc;
     cudaError_t e = pa::launch_combine(out, lse, part_o, part_lse, static_cast<int>(Bq * Hq), P,
                                        cache.head_dim, stream);
@@ -501,6 +539,42 @@ int pa_decode_mq(void *out, float *lse, const void *q, int32_t q_len, const void
     return splitkv_common(out, lse, q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq,
                           seq_lens, B, Hq, scale, num_splits, workspace, workspace_bytes, status,
                           stream, NewTokens(), q_len);
+}
+
+int pa_cache_write_fp8(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                       int64_t n_tokens, void *k_cache, void *v_cache, pa_cache_desc cache,
+                       float k_scale, float v_scale, int32_t *status, pa_stream_t stream) {
+    if (n_tokens < 0) return PA_EINVAL;
+    int rc = check_cache_desc(cache);
+    if (rc) return rc;
+    if (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
+        return PA_EINVAL;
+    if (n_tokens == 0) return PA_OK;
+    if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache) return PA_EINVAL;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) ||
+        !aligned(v_cache, 16) || !aligned(slot_mapping, 8))
+        return PA_EINVAL;
+    const int row_elems = cache.num_kv_heads * cache.head_dim;
+    cudaError_t e = pa::launch_cache_write_fp8(
+        k_new, v_new, slot_mapping, n_tokens, k_cache, v_cache,
+        static_cast<int64_t>(cache.num_blocks) * cache.block_size, row_elems, k_scale, v_scale,
+        status, stream);
+    return e == cudaSuccess ? PA_OK : PA_ECUDA;
+}
+
+int pa_decode_splitkv_fp8(void *out, float *lse, const void *q, const void *k_cache,
+                          const void *v_cache, pa_cache_desc cache, float k_scale, float v_scale,
+                          const int32_t *block_tables, int32_t max_blocks_per_seq,
+                          const int32_t *seq_lens, int32_t B, int32_t Hq, float scale,
+                          int32_t num_splits, void *workspace, size_t workspace_bytes,
+                          int32_t *status, pa_stream_t stream) {
+    if (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
+        return PA_EINVAL;
+    if (cache.head_dim != 128) return PA_EUNSUPPORTED;
+    const Fp8Scales f8{k_scale, v_scale};
+    return splitkv_common(out, lse, q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq,
+                          seq_lens, B, Hq, scale, num_splits, workspace, workspace_bytes, status,
+                          stream, NewTokens(), 1, &f8);
 }
 
 int pa_decode_splitkv(void *out, float *lse, const void *q, const void *k_cache,

@@ -1,7 +1,9 @@
-// The two small kernels around decode attention:
-//   - cache write: slot-mapping scatter of this step's K/V into the block pool;
+// The small kernels around decode attention:
+//   - cache write: slot-mapping scatter of this step's K/V into the block pool
+//     (bf16 pools: a copy; FP8 pools: quantised to e4m3 with the pool's scale);
 //   - combine: log-sum-exp merge of split-KV partials into bf16 output.
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 
 #include "pa_device.cuh"
 #include "pa_internal.h"
@@ -47,6 +49,57 @@ cudaError_t launch_cache_write(const void *k_new, const void *v_new, const int64
     cache_write_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
         static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), slots, n,
         static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), n_slots, row_chunks, status);
+    return cudaGetLastError();
+}
+
+// FP8 pools: each thread quantises 8 bf16 values of a new K or V row (one
+// 16-byte chunk) to e4m3 codes (8 bytes): fp32(x) / scale, rounded to
+// nearest even, saturating at the largest finite code (+-448), NaN kept.
+__global__ void __launch_bounds__(256)
+cache_write_fp8_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
+                       const int64_t *__restrict__ slots, int64_t n, uint2 *__restrict__ k_cache,
+                       uint2 *__restrict__ v_cache, int64_t n_slots, int row_chunks, float k_scale,
+                       float v_scale, int32_t *status) {
+    const int64_t total = n * 2 * row_chunks;
+    for (int64_t x = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; x < total;
+         x += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t c = x % row_chunks;
+        const int64_t r = x / row_chunks;  // (token, which)
+        const int64_t i = r >> 1;
+        const bool is_v = r & 1;
+        const int64_t s = slots[i];
+        if (s < 0) continue;
+        if (s >= n_slots) {
+            if (c == 0 && !is_v) set_status(status, PA_STATUS_BAD_SLOT);
+            continue;
+        }
+        const uint4 in = (is_v ? v_new : k_new)[i * row_chunks + c];
+        const float scale = is_v ? v_scale : k_scale;
+        const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+        uint32_t out[2] = {0u, 0u};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const __nv_fp8_storage_t lo = __nv_cvt_float_to_fp8(bf16lo(w[k]) / scale, __NV_SATFINITE, __NV_E4M3);
+            const __nv_fp8_storage_t hi = __nv_cvt_float_to_fp8(bf16hi(w[k]) / scale, __NV_SATFINITE, __NV_E4M3);
+            out[k >> 1] |= (static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 8)) << (16 * (k & 1));
+        }
+        (is_v ? v_cache : k_cache)[s * row_chunks + c] = make_uint2(out[0], out[1]);
+    }
+}
+
+cudaError_t launch_cache_write_fp8(const void *k_new, const void *v_new, const int64_t *slots,
+                                   int64_t n, void *k_cache, void *v_cache, int64_t n_slots,
+                                   int row_elems, float k_scale, float v_scale, int32_t *status,
+                                   cudaStream_t stream) {
+    const int row_chunks = row_elems / 8;
+    const int64_t total = n * 2 * row_chunks;
+    const int threads = 256;
+    int64_t blocks = (total + threads - 1) / threads;
+    if (blocks > 65535LL * 16) blocks = 65535LL * 16;
+    cache_write_fp8_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+        static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), slots, n,
+        static_cast<uint2 *>(k_cache), static_cast<uint2 *>(v_cache), n_slots, row_chunks, k_scale,
+        v_scale, status);
     return cudaGetLastError();
 }
 

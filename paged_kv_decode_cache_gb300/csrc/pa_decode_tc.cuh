@@ -45,6 +45,9 @@
 // on an abort at their per-chunk vote.
 #pragma once
 
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 #include <atomic>
 
 #include "pa_device.cuh"
@@ -56,6 +59,9 @@ namespace pa {
 
 constexpr int kTcRows = 128;           // rows m per chunk (M of QK)
 constexpr int kTcThreads = 256;        // 4 softmax warps + 2 MMA warps + 2 TMA warps
+constexpr int kTcThreadsF8 = 384;      // FP8 pools: + 4 warps that widen the e4m3 tiles
+constexpr int kTcCvtKWarp = 8;         // warps 8, 9: K converters; 10, 11: V converters
+constexpr int kTcCvtVWarp = 10;
 constexpr int kTcQkWarp = 4;
 constexpr int kTcTmaKWarp = 5;
 constexpr int kTcTmaVWarp = 6;
@@ -67,7 +73,7 @@ constexpr int kTcMaskRing = 8;         // chunk validity masks the K producer pu
 
 constexpr int kTcSmemLimit = 227 * 1024;
 
-template <int HC, int GP>
+template <int HC, int GP, bool F8 = false>
 struct TcCfg {
     static constexpr int kN = HC * GP;                          // MMA N
     static_assert(kN % 16 == 0 && kN >= 16 && kN <= 64, "MMA N");
@@ -89,10 +95,11 @@ struct TcCfg {
     static constexpr int kRedBytes = (kTcRows * GP + 4 * kN) * 4 + 16;
     // shared memory for nk K stages, nv V stages and nbp P^T buffers, laid out
     // as below (rings, Q, P^T, scratch, barriers, masks, block-id rings, align)
+    // (FP8: a "converted" barrier per K and V stage and the V producer's mask ring)
     static constexpr int smem_for(int nk, int nv, int nbp) {
         return ((nk + nv) * kTileBytes + kQBytes + nbp * kPBufBytes + kRedBytes + 7) / 8 * 8 +
-               (2 * nk + 2 * nv + 2 * kTcNBS + 2 * nbp) * 8 + kTcMaskRing * 8 +
-               2 * (kTcLook + 1) * 32 * 4 + 1024;
+               (2 * nk + 2 * nv + 2 * kTcNBS + 2 * nbp + (F8 ? nk + nv : 0)) * 8 +
+               kTcMaskRing * 8 * (F8 ? 2 : 1) + 2 * (kTcLook + 1) * 32 * 4 + 1024;
     }
     // the deepest pipeline that fits: K and V stages first, then P^T buffers
     static constexpr int kChoice = smem_for(3, 3, 2) <= kTcSmemLimit ? 0
@@ -107,11 +114,12 @@ struct TcCfg {
     static constexpr int kPOff = kQOff + kQBytes;
     static constexpr int kRedOff = kPOff + kNBP * kPBufBytes;
     static constexpr int kBarOff = (kRedOff + kRedBytes + 7) / 8 * 8;
-    static constexpr int kNumBars = 2 * kNK + 2 * kNV + 2 * kTcNBS + 2 * kNBP;
+    static constexpr int kNumBars = 2 * kNK + 2 * kNV + 2 * kTcNBS + 2 * kNBP + (F8 ? kNK + kNV : 0);
     // validity masks [kTcMaskRing] (u64: chunk << 32 | lane mask), then the two
     // producers' block-id rings [2][kTcLook + 1][32 lanes]
     static constexpr int kMaskOff = kBarOff + kNumBars * 8;
-    static constexpr int kLookOff = kMaskOff + kTcMaskRing * 8;
+    static constexpr int kVMaskOff = kMaskOff + kTcMaskRing * 8;   // FP8 only
+    static constexpr int kLookOff = kVMaskOff + (F8 ? kTcMaskRing * 8 : 0);
     static constexpr int kSmemBytes = kLookOff + 2 * (kTcLook + 1) * 32 * 4 + 1024;
     static_assert(kSmemBytes == smem_for(kNK, kNV, kNBP), "layout");
     // the K producer rewrites mask slot c % ring only once softmax c has read it
@@ -138,12 +146,46 @@ __device__ __forceinline__ float column_reduce(const float *red, int n) {
     return acc;
 }
 
-template <int HC, int GP>
-__global__ void __launch_bounds__(kTcThreads, 1)
+// 16-bit operand value of p for the PV MMA: bf16, or fp16 with FP8 pools
+// (whose K/V tiles are widened to fp16).
+template <bool F8>
+__device__ __forceinline__ uint16_t p16_bits(float x) {
+    if constexpr (F8) return __half_as_ushort(__float2half_rn(x));
+    else return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+template <bool F8>
+__device__ __forceinline__ float p16_value(uint16_t b) {
+    if constexpr (F8) return __half2float(__ushort_as_half(b));
+    else return __bfloat162float(__ushort_as_bfloat16(b));
+}
+
+// Widens 16 e4m3 codes to 16 fp16 values (exact: e4m3 is a subset of fp16),
+// one cvt per pair of codes: the low byte of each 16-bit pair becomes the low
+// half of the result.
+__device__ __forceinline__ uint2 e4m3x4_to_f16x4(uint32_t w) {
+    uint2 r;
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "mov.b32 {lo, hi}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+        : "=r"(r.x), "=r"(r.y)
+        : "r"(w));
+    return r;
+}
+__device__ __forceinline__ void e4m3x16_to_f16(const uint4 &in, uint4 &lo, uint4 &hi) {
+    const uint2 a = e4m3x4_to_f16x4(in.x), b = e4m3x4_to_f16x4(in.y);
+    const uint2 c = e4m3x4_to_f16x4(in.z), d = e4m3x4_to_f16x4(in.w);
+    lo = make_uint4(a.x, a.y, b.x, b.y);
+    hi = make_uint4(c.x, c.y, d.x, d.y);
+}
+
+template <int HC, int GP, bool F8>
+__global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                  const DecodeParams p, int G) {
     constexpr int D = 128;
-    using C = TcCfg<HC, GP>;
+    constexpr int kThreads = F8 ? kTcThreadsF8 : kTcThreads;
+    using C = TcCfg<HC, GP, F8>;
     constexpr int N = C::kN, NK = C::kNK, NV = C::kNV, NBP = C::kNBP;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -164,7 +206,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     uint64_t *kfull = bars, *kempty = bars + NK, *vfull = bars + 2 * NK, *vempty = vfull + NV;
     uint64_t *sdone = vempty + NV, *sfree = sdone + kTcNBS, *pready = sfree + kTcNBS;
     uint64_t *pfree = pready + NBP;
+    uint64_t *kconv = pfree + NBP, *vconv = kconv + NK;   // FP8: stage widened to fp16
     volatile uint64_t *mask_ring = reinterpret_cast<volatile uint64_t *>(smem + C::kMaskOff);
+    volatile uint64_t *vmask_ring = reinterpret_cast<volatile uint64_t *>(smem + C::kVMaskOff);
     int *look_ring = reinterpret_cast<int *>(smem + C::kLookOff);  // [2][kTcLook + 1][32]
 
     const int part = blockIdx.x, b = blockIdx.z;
@@ -191,11 +235,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     };
     const int32_t *bt = p.block_tables + static_cast<int64_t>(b) * p.max_blocks;
     int L = p.seq_lens[b];
-    constexpr int kQLoads = (N * (D / 8) + kTcThreads - 1) / kTcThreads;
+    constexpr int kQLoads = (N * (D / 8) + kThreads - 1) / kThreads;
     uint4 qv[kQLoads];
 #pragma unroll
     for (int j = 0; j < kQLoads; ++j) {
-        const int i = tid + j * kTcThreads, n = i / (D / 8), c = i % (D / 8);
+        const int i = tid + j * kThreads, n = i / (D / 8), c = i % (D / 8);
         qv[j] = make_uint4(0u, 0u, 0u, 0u);
         if (i < N * (D / 8) && n % GP < Gq)
             qv[j] = *reinterpret_cast<const uint4 *>(p.q + col_row(n / GP, n % GP) * D + c * 8);
@@ -248,7 +292,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
 
     if (nch == 0) {  // empty range: zero output, lse = -inf
         cp_async_wait<0>();
-        for (int i = tid; i < HC * Gq * D; i += kTcThreads) {
+        for (int i = tid; i < HC * Gq * D; i += kThreads) {
             const int j = i / D, d = i % D;
             const int64_t r = col_row(j / Gq, j % Gq);
             if (p.split) p.part_o[(r * p.num_splits + part) * D + d] = 0.f;
@@ -260,7 +304,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             else if (p.lse) p.lse[r] = -INFINITY;
         }
         if (p.split)
-            merge_split_group<D, kTcThreads / 32>(p, b * gridDim.y + blockIdx.y, part, row0, HC * Gq,
+            merge_split_group<D, kThreads / 32>(p, b * gridDim.y + blockIdx.y, part, row0, HC * Gq,
                                                   HC * G, Hq, ticket, tid, [] { __syncthreads(); });
         return;
     }
@@ -322,7 +366,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             }
             const uint32_t vm = __ballot_sync(0xffffffffu, valid);
             // publish which tiles of chunk c are loaded (bit 2 * tile) for the softmax
-            if (!is_v && lane == 0) mask_ring[c % kTcMaskRing] = (static_cast<uint64_t>(c) << 32) | vm;
+            // (and, FP8, for the V converter, which zeroes the V rows not loaded)
+            if (lane == 0 && !is_v) mask_ring[c % kTcMaskRing] = (static_cast<uint64_t>(c) << 32) | vm;
+            if (F8 && lane == 0 && is_v) vmask_ring[c % kTcMaskRing] = (static_cast<uint64_t>(c) << 32) | vm;
             const int chunk0 = t_begin + c * C::kT;
             if (writes && last_pos >= chunk0 && last_pos < chunk0 + C::kT) {  // holds position L - 1
                 const int ph = __shfl_sync(0xffffffffu, phys, 2 * ((last_pos - chunk0) / kTile));
@@ -338,11 +384,22 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                 }
                 __syncwarp();
             }
-            if (lane == 0) mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(__popc(vm)) * C::kBoxBytes);
-            __syncwarp();
-            if (valid)
-                tma_load_4d(ring + s * C::kTileBytes + sub * C::kSubTile + tile * C::kBoxBytes, map, 0,
-                            phys * bs + tok0 % bs, g0, sub, &full[s], policy);
+            if constexpr (F8) {
+                // one box per tile (16 rows x HC heads x 128 one-byte codes) into the
+                // stage's upper half, where the converter widens it in place
+                if (lane == 0)
+                    mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(__popc(vm & 0x55555555u)) * C::kBoxBytes);
+                __syncwarp();
+                if (valid && sub == 0)
+                    tma_load_3d(ring + s * C::kTileBytes + C::kSubTile + tile * C::kBoxBytes, map, 0,
+                                phys * bs + tok0 % bs, g0, &full[s], policy);
+            } else {
+                if (lane == 0) mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(__popc(vm)) * C::kBoxBytes);
+                __syncwarp();
+                if (valid)
+                    tma_load_4d(ring + s * C::kTileBytes + sub * C::kSubTile + tile * C::kBoxBytes, map, 0,
+                                phys * bs + tok0 % bs, g0, sub, &full[s], policy);
+            }
             issued = c + 1;
         }
         return true;
@@ -354,8 +411,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                 mbar_init(&full[i], 1u);
                 mbar_init(&empty[i], 1u);
             }
-            if (!is_v)  // no chunk's tag yet
-                for (int i = 0; i < kTcMaskRing; ++i) mask_ring[i] = ~uint64_t(0);
+            for (int i = 0; i < kTcMaskRing; ++i) {  // no chunk's tag yet
+                if (!is_v) mask_ring[i] = ~uint64_t(0);
+                else if (F8) vmask_ring[i] = ~uint64_t(0);
+            }
             fence_barrier_init();
             prefetch_tensormap(map);
         }
@@ -371,16 +430,28 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         // softmax threads arrive on
         for (uint64_t *bar = sdone; bar < pfree + NBP; ++bar)
             mbar_init(bar, (bar >= sfree && bar < pready + NBP) ? 128u : 1u);
+        if (F8)  // "converted": the 64 threads of a converter pair arrive
+            for (uint64_t *bar = kconv; bar < vconv + NV; ++bar) mbar_init(bar, 64u);
         *abort_flag = 0;
     }
     if (tid < N) m_ref[tid] = -INFINITY;
 #pragma unroll
     for (int j = 0; j < kQLoads; ++j) {  // Q operand row n = (head', q), 16-byte chunk c
-        const int i = tid + j * kTcThreads, n = i / (D / 8), c = i % (D / 8);
-        if (i < N * (D / 8))
-            *reinterpret_cast<uint4 *>(qs + (c >> 3) * (N * kSubBytes) + swz128(n, c & 7)) = qv[j];
+        const int i = tid + j * kThreads, n = i / (D / 8), c = i % (D / 8);
+        if (i < N * (D / 8)) {
+            uint4 v = qv[j];
+            if constexpr (F8) {  // the MMA takes fp16 operands with FP8 pools
+                uint32_t *w = reinterpret_cast<uint32_t *>(&v);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const __half2 h = __floats2half2_rn(bf16lo(w[k]), bf16hi(w[k]));
+                    w[k] = *reinterpret_cast<const uint32_t *>(&h);
+                }
+            }
+            *reinterpret_cast<uint4 *>(qs + (c >> 3) * (N * kSubBytes) + swz128(n, c & 7)) = v;
+        }
     }
-    for (int i = tid; i < NBP * C::kPBufBytes / 16; i += kTcThreads)
+    for (int i = tid; i < NBP * C::kPBufBytes / 16; i += kThreads)
         reinterpret_cast<uint4 *>(ps)[i] = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async_smem();
     fence_barrier_init();
@@ -400,12 +471,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     } else if (warp == kTcQkWarp) {
         // ================= QK issuer =================
         if (lane == 0) {
-            constexpr uint32_t kIdQK = tc5::idesc_bf16_f32(kTcRows, N, false, false);
+            constexpr uint32_t kIdQK = tc5::idesc_bf16_f32(kTcRows, N, false, false, F8);
             int done = 0;
             for (int c = 0; c < nch; ++c) {
                 // S buffer c % NBS is free once softmax c - NBS has read it; K c has landed
                 if (c >= kTcNBS && !wait_or_abort(&sfree[c % kTcNBS], ((c / kTcNBS) - 1) & 1)) break;
-                if (!wait_or_abort(&kfull[c % NK], (c / NK) & 1)) break;
+                if (!wait_or_abort(F8 ? &kconv[c % NK] : &kfull[c % NK], (c / NK) & 1)) break;
                 tc5::fence_after_sync();
                 const uint8_t *kt = kring + (c % NK) * C::kTileBytes;
                 const uint32_t dcol = tmem + (c % kTcNBS) * N;
@@ -426,11 +497,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     } else if (warp == kTcPvWarp) {
         // ================= PV issuer =================
         if (lane == 0) {
-            constexpr uint32_t kIdPV = tc5::idesc_bf16_f32(kTcRows, 2 * N, true, false);
+            constexpr uint32_t kIdPV = tc5::idesc_bf16_f32(kTcRows, 2 * N, true, false, F8);
             int done = 0;
             for (int c = 0; c < nch; ++c) {
                 if (!wait_or_abort(&pready[c % NBP], (c / NBP) & 1)) break;
-                if (!wait_or_abort(&vfull[c % NV], (c / NV) & 1)) break;
+                if (!wait_or_abort(F8 ? &vconv[c % NV] : &vfull[c % NV], (c / NV) & 1)) break;
                 tc5::fence_after_sync();
                 const uint8_t *vt = vring + (c % NV) * C::kTileBytes;
                 const uint8_t *pt = ps + (c % NBP) * C::kPBufBytes;
@@ -448,6 +519,70 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             }
             if (*abort_flag && done > 0)
                 mbar_wait_bounded(&pfree[(done - 1) % NBP], ((done - 1) / NBP) & 1);
+        }
+    } else if (F8 && warp >= kTcCvtKWarp) {
+        // ================= FP8 converters: widen each landed e4m3 stage to fp16 =================
+        // Warps 8-9 take the K ring, 10-11 the V ring; thread ct owns rows ct and
+        // ct + 64 of a chunk.  A row's 128 codes (in the stage's upper half, as TMA
+        // wrote them, 128-byte swizzled) are read whole before its two fp16
+        // half-rows are written (the second one over the codes), so no row
+        // touches another's bytes.  V rows the producer did not load, or past the
+        // range, are written as zeros, so 0 * (stale bytes) never reaches O^T.
+        const bool cv = warp >= kTcCvtVWarp;
+        const int ct = tid - 32 * (cv ? kTcCvtVWarp : kTcCvtKWarp);
+        const int nst_c = cv ? NV : NK;
+        uint8_t *ring_c = cv ? vring : kring;
+        uint64_t *full_c = cv ? vfull : kfull;
+        uint64_t *conv_c = cv ? vconv : kconv;
+        for (int c = 0; c < nch; ++c) {
+            const int s = c % nst_c;
+            if (!wait_or_abort(&full_c[s], (c / nst_c) & 1)) break;
+            uint32_t vm = 0xffffffffu;
+            if (cv) {  // the V producer wrote chunk c's mask before its loads
+                uint64_t mk = 0;
+                uint32_t i = 0;
+                for (; i < kWaitLimit; ++i) {
+                    mk = vmask_ring[c % kTcMaskRing];
+                    if (static_cast<uint32_t>(mk >> 32) == static_cast<uint32_t>(c) || *abort_flag) break;
+                }
+                if (static_cast<uint32_t>(mk >> 32) != static_cast<uint32_t>(c)) {
+                    if (i == kWaitLimit) {
+                        *abort_flag = 1;
+                        set_status(p.status, PA_STATUS_TIMEOUT);
+                    }
+                    break;
+                }
+                vm = static_cast<uint32_t>(mk);
+            }
+            uint8_t *st = ring_c + s * C::kTileBytes;
+            // both rows' codes are loaded first (the rows are disjoint), then widened
+            uint4 raw[2][8];
+            bool keep[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int m = ct + 64 * h;
+                const int tl = m / (kTile * HC);
+                keep[h] = !cv || (((vm >> (2 * tl)) & 1u) && t_begin + c * C::kT + tl * kTile + (m & 15) < t_end);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    raw[h][j] = *reinterpret_cast<const uint4 *>(st + C::kSubTile + m * kSubBytes +
+                                                                 ((j ^ (m & 7)) << 4));
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int m = ct + 64 * h;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {  // codes 16j..16j+15 = half (j / 4), chunks 2(j%4), +1
+                    uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+                    if (keep[h]) e4m3x16_to_f16(raw[h][j], lo, hi);
+                    const int cj = (j & 3) * 2;
+                    uint8_t *row = st + (j >> 2) * C::kSubTile + m * kSubBytes;
+                    *reinterpret_cast<uint4 *>(row + ((cj ^ (m & 7)) << 4)) = lo;
+                    *reinterpret_cast<uint4 *>(row + (((cj + 1) ^ (m & 7)) << 4)) = hi;
+                }
+            }
+            fence_proxy_async_smem();  // the MMA (async proxy) reads what these threads wrote
+            mbar_arrive(&conv_c[s]);
         }
     } else {
         // ================= softmax warps: thread = row m of a chunk, and output dim d =================
@@ -551,13 +686,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             }
             // p = hi + lo, both bf16 (the PV MMA takes bf16 operands): the pair
             // carries p to about 2^-17 relative, where hi alone would be 2^-9
-            __nv_bfloat16 pb[GP], pl[GP];
+            uint16_t pb[GP], pl[GP];  // bf16 (fp16 with FP8 pools) bit patterns
 #pragma unroll
             for (int q = 0; q < GP; ++q) {
                 const float pf = sc[q] != -INFINITY ? fast_exp2(sc[q] - mr[q]) : 0.f;
-                pb[q] = __float2bfloat16_rn(pf);
-                pl[q] = __float2bfloat16_rn(pf - __bfloat162float(pb[q]));
-                l_thr[q] += __bfloat162float(pb[q]) + __bfloat162float(pl[q]);
+                pb[q] = p16_bits<F8>(pf);
+                pl[q] = p16_bits<F8>(pf - p16_value<F8>(pb[q]));
+                l_thr[q] += p16_value<F8>(pb[q]) + p16_value<F8>(pl[q]);
             }
             if (c >= NBP) wait_or_abort(&pfree[pbuf], ((c / NBP) - 1) & 1);  // PV c - NBP done
             {
@@ -568,12 +703,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                 for (int q = 0; q < GP; ++q) {
                     const int n = my_head * GP + q;   // lo row N + n swizzles as n (N % 8 == 0)
                     const uint32_t at = n * kSubBytes + (((tt >> 3) ^ (n & 7)) << 4) + (tt & 7) * 2;
-                    *reinterpret_cast<__nv_bfloat16 *>(pt + at) = pb[q];
-                    *reinterpret_cast<__nv_bfloat16 *>(pt + N * kSubBytes + at) = pl[q];
+                    *reinterpret_cast<uint16_t *>(pt + at) = pb[q];
+                    *reinterpret_cast<uint16_t *>(pt + N * kSubBytes + at) = pl[q];
                 }
             }
             // an invalid row zeroes its V row, so 0 * (stale or NaN) never reaches O^T
-            if (!valid && wait_or_abort(&vfull[c % NV], (c / NV) & 1)) {
+            // (with FP8 pools the V converter writes those rows as zeros)
+            if (!F8 && !valid && wait_or_abort(&vfull[c % NV], (c / NV) & 1)) {
                 uint8_t *vrow = vring + (c % NV) * C::kTileBytes + tid * kSubBytes;
 #pragma unroll
                 for (int sub = 0; sub < 2; ++sub)
@@ -596,7 +732,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         if (tid < N) {  // row sum of column n, its reciprocal (alpha_s is free now), its row
             const float lsum = column_reduce<HC, GP, false>(red, tid);
             col[tid] = lsum;
-            alpha_s[tid] = lsum > 0.f ? 1.f / lsum : 0.f;  // 0: no key seen (causal)
+            alpha_s[tid] = lsum > 0.f ? p.v_scale / lsum : 0.f;  // 0: no key seen (causal)
             const int c = tid % GP;
             rel_s[tid] = c < Gq ? static_cast<int>(col_row(tid / GP, c) - row0) : -1;
         }
@@ -637,15 +773,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     __syncthreads();
     if (warp == 0) tc5::tmem_free(tmem, C::kTmemCols);
     if (p.split)  // all eight warps share the merge
-        merge_split_group<D, kTcThreads / 32>(p, b * gridDim.y + blockIdx.y, part, row0, HC * Gq,
+        merge_split_group<D, kThreads / 32>(p, b * gridDim.y + blockIdx.y, part, row0, HC * Gq,
                                               HC * G, Hq, ticket, tid, [] { __syncthreads(); });
 }
 
-template <int HC, int GP>
+template <int HC, int GP, bool F8>
 cudaError_t launch_tc_instance(const CUtensorMap &kmap, const CUtensorMap &vmap,
                                const DecodeParams &p, int B, int G, cudaStream_t stream) {
-    using C = TcCfg<HC, GP>;
-    auto kern = decode_tc_kernel<HC, GP>;
+    using C = TcCfg<HC, GP, F8>;
+    auto kern = decode_tc_kernel<HC, GP, F8>;
     static std::atomic<uint64_t> smem_attr_done{0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -657,7 +793,8 @@ cudaError_t launch_tc_instance(const CUtensorMap &kmap, const CUtensorMap &vmap,
         smem_attr_done.fetch_or(bit, std::memory_order_release);
     }
     const int qgroups = (p.q_len + p.q_per_cta - 1) / p.q_per_cta;
-    return launch_maybe_cooperative(kern, dim3(p.num_splits, p.head_groups * qgroups, B), kTcThreads,
+    return launch_maybe_cooperative(kern, dim3(p.num_splits, p.head_groups * qgroups, B),
+                                    F8 ? kTcThreadsF8 : kTcThreads,
                                     C::kSmemBytes, stream, p.counters != nullptr, kmap, vmap, p, G);
 }
 

@@ -8,7 +8,7 @@ cudaError_t launch_decode_tc(int HC, int GP, int G, const CUtensorMap &kmap,
                              const CUtensorMap &vmap, const DecodeParams &p, int B,
                              cudaStream_t stream) {
 #define PA_TC_CASE(hc, gp) \
-    if (HC == hc && GP == gp) return launch_tc_instance<hc, gp>(kmap, vmap, p, B, G, stream);
+    if (HC == hc && GP == gp) return launch_tc_instance<hc, gp, false>(kmap, vmap, p, B, G, stream);
     PA_TC_CASE(1, 16)
     PA_TC_CASE(2, 8)
     PA_TC_CASE(2, 16)

@@ -47,6 +47,9 @@ struct DecodeParams {
     int32_t q_len;          // 1: plain decode
     int32_t q_per_cta;
     int32_t head_groups;    // CTAs across the KV heads (Hkv / heads per CTA)
+    // FP8 pools (e4m3 codes): scale_log2 already includes k_scale; the output
+    // is multiplied by v_scale.  1 for bf16 pools.
+    float v_scale;
 };
 
 // CUDA-core decode kernel launch (pa_decode_cc_d*.cu).  Returns a cudaError_t.
@@ -59,5 +62,10 @@ cudaError_t launch_combine(void *out, float *lse, const float *part_o, const flo
 cudaError_t launch_cache_write(const void *k_new, const void *v_new, const int64_t *slots,
                                int64_t n, void *k_cache, void *v_cache, int64_t n_slots,
                                int row_bytes, int32_t *status, cudaStream_t stream);
+
+cudaError_t launch_cache_write_fp8(const void *k_new, const void *v_new, const int64_t *slots,
+                                   int64_t n, void *k_cache, void *v_cache, int64_t n_slots,
+                                   int row_elems, float k_scale, float v_scale, int32_t *status,
+                                   cudaStream_t stream);
 
 }  // namespace pa

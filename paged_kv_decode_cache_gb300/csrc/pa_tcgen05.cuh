@@ -50,12 +50,14 @@ __device__ __forceinline__ uint64_t sw128_desc(const void *smem_ptr, uint32_t lb
     return d;
 }
 
-// Instruction descriptor, kind::f16 with bf16 A and B and an fp32
-// accumulator.  a_mn / b_mn select MN-major (transposed) operands.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, bool b_mn) {
+// Instruction descriptor, kind::f16 with bf16 (or, with f16 = true, fp16) A
+// and B and an fp32 accumulator.  a_mn / b_mn select MN-major (transposed)
+// operands.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, bool b_mn,
+                                                      bool f16 = false) {
     return (1u << 4)                                  // accumulator format: f32
-           | (1u << 7)                                // A format: bf16
-           | (1u << 10)                               // B format: bf16
+           | (static_cast<uint32_t>(!f16) << 7)       // A format: bf16 (1) or fp16 (0)
+           | (static_cast<uint32_t>(!f16) << 10)      // B format: bf16 (1) or fp16 (0)
            | (static_cast<uint32_t>(a_mn) << 15)      // A major-ness
            | (static_cast<uint32_t>(b_mn) << 16)      // B major-ness
            | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8

@@ -49,6 +49,15 @@ class DecodeWorkload:
     slot_mapping: np.ndarray   # [N] int64
     scale: float
     q_len: int = 1             # new tokens (queries) per sequence
+    # FP8 variant: e4m3 codes of the pools (uint8) and the per-pool scales
+    k_cache8: Optional[np.ndarray] = None
+    v_cache8: Optional[np.ndarray] = None
+    k_scale: float = 1.0
+    v_scale: float = 1.0
+
+    @property
+    def fp8(self) -> bool:
+        return self.k_cache8 is not None
 
     @property
     def G(self) -> int:
@@ -56,15 +65,16 @@ class DecodeWorkload:
 
     def kv_bytes(self) -> int:
         """Bytes of K and V that attention must read (each token once per KV head)."""
-        return int(self.seq_lens.astype(np.int64).sum()) * 2 * self.Hkv * self.D * 2
+        elem = 1 if self.fp8 else 2
+        return int(self.seq_lens.astype(np.int64).sum()) * 2 * self.Hkv * self.D * elem
 
     def qo_bytes(self) -> int:
         return 2 * self.B * self.q_len * self.Hq * self.D * 2
 
     def write_bytes(self) -> int:
-        """Bytes moved by the cache write: read k_new/v_new, write the same into the pools."""
+        """Bytes moved by the cache write: read k_new/v_new (bf16), write them into the pools."""
         n = int((self.slot_mapping >= 0).sum())
-        return 2 * (2 * n * self.Hkv * self.D * 2)
+        return 2 * n * self.Hkv * self.D * (2 + (1 if self.fp8 else 2))
 
 
 def _bf16_bits(gen: torch.Generator, shape: Sequence[int]) -> np.ndarray:
@@ -189,6 +199,22 @@ def qwen3_0p6b(B: int = 256, **kw) -> DecodeWorkload:
                          max_blocks=128, shared_prefix_blocks=8, seed=1005, **kw)
 
 
+def with_fp8_pools(w: DecodeWorkload) -> DecodeWorkload:
+    """FP8 variant of a workload: the same bf16 pools rounded to e4m3 codes by
+    torch's float8_e4m3fn cast, with one scale per pool chosen as amax / 448
+    (so the codes span the format).  The new-token rows stay bf16."""
+    def codes(bits: np.ndarray):
+        x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).float()
+        amax = float(torch.nan_to_num(x, nan=0.0).abs().max())
+        scale = float(np.float32(max(amax, 1e-30) / 448.0))
+        c = (x / torch.tensor(scale, dtype=torch.float32)).clamp(-448, 448)
+        return c.to(torch.float8_e4m3fn).view(torch.uint8).numpy().copy(), scale
+    w.k_cache8, w.k_scale = codes(w.k_cache)
+    w.v_cache8, w.v_scale = codes(w.v_cache)
+    w.name = w.name + "-fp8"
+    return w
+
+
 def spec_verify(base: str, q_len: int, **kw) -> DecodeWorkload:
     """Speculative verification on a decode workload: the last q_len positions
     of every sequence are the target model's queries (q_len - 1 drafted tokens
@@ -213,6 +239,10 @@ WORKLOADS = {
 # multi-query (speculative verification) families: the pages' 1.5B target model
 # verifying drafts, and the 7B / Qwen3 layers with four queries per sequence
 WORKLOADS.update({
+    # FP8 (e4m3) pools: the 7B layer, the long-context stress, the Qwen3 batch
+    "qwen2.5-7b-bs16-fp8": lambda **kw: with_fp8_pools(qwen25_7b(16, **kw)),
+    "long-B2-L32768-fp8": lambda **kw: with_fp8_pools(long_context(2, 32768, **kw)),
+    "qwen3-0.6b-B256-fp8": lambda **kw: with_fp8_pools(qwen3_0p6b(256, **kw)),
     "qwen2.5-1.5b-B8-spec4": lambda **kw: spec_verify("qwen2.5-1.5b-B8", 4, **kw),
     "qwen2.5-7b-bs16-spec4": lambda **kw: spec_verify("qwen2.5-7b-bs16", 4, **kw),
     "qwen3-0.6b-B256-spec4": lambda **kw: spec_verify("qwen3-0.6b-B256", 4, **kw),

@@ -240,3 +240,20 @@ def test_mq_rejects_what_it_cannot_run(lib, monkeypatch):
     rc = lib.pa_decode_mq(FAKE, None, FAKE, 2, FAKE, FAKE, _desc(d=64), FAKE, 7, FAKE, 4, 4, 0.1, 1,
                           None, 0, None, None)
     assert rc == pa.PA_EUNSUPPORTED     # D = 64
+
+
+def test_fp8_rejects_bad_arguments(lib, monkeypatch):
+    monkeypatch.delenv("PA_DECODE_KERNEL", raising=False)
+    d = _desc(d=128)
+    for ks, vs in ((0.0, 1.0), (1.0, -1.0), (float("nan"), 1.0), (1.0, float("inf"))):
+        assert lib.pa_cache_write_fp8(FAKE, FAKE, FAKE, 3, FAKE, FAKE, d, ks, vs, None, None) == pa.PA_EINVAL
+        assert lib.pa_decode_splitkv_fp8(FAKE, None, FAKE, FAKE, FAKE, d, ks, vs, FAKE, 7, FAKE, 4, 4,
+                                         0.1, 1, None, 0, None, None) == pa.PA_EINVAL
+    assert lib.pa_decode_splitkv_fp8(FAKE, None, FAKE, FAKE, FAKE, _desc(d=64), 1.0, 1.0, FAKE, 7,
+                                     FAKE, 4, 4, 0.1, 1, None, 0, None, None) == pa.PA_EUNSUPPORTED
+    assert lib.pa_decode_splitkv_fp8(FAKE, None, FAKE, FAKE, FAKE, d, 1.0, 1.0, FAKE, 7, FAKE, 4, 4,
+                                     0.1, 3, None, 0, None, None) == pa.PA_EWORKSPACE
+    monkeypatch.setenv("PA_DECODE_KERNEL", "cuda_core")
+    assert lib.pa_decode_splitkv_fp8(FAKE, None, FAKE, FAKE, FAKE, d, 1.0, 1.0, FAKE, 7, FAKE, 4, 4,
+                                     0.1, 1, None, 0, None, None) == pa.PA_EUNSUPPORTED
+    assert lib.pa_cache_write_fp8(FAKE, FAKE, FAKE, 0, FAKE, FAKE, d, 1.0, 1.0, None, None) == pa.PA_OK

@@ -473,3 +473,99 @@ def test_mq_workload_full_size(name):
         assert_close(bf16_dev_to_f64(out), ref, f"{name} P={Pu}")
         assert_lse_close(lse.cpu().double().numpy(), ref_lse, f"{name} P={Pu}")
     assert dev.status_value() == 0
+
+
+# ------------------------------------------------------------- FP8 (e4m3) pools
+def _fp8_dev(w):
+    """Device copies of an FP8 workload's pools (uint8 codes)."""
+    return (torch.from_numpy(w.k_cache8).cuda(), torch.from_numpy(w.v_cache8).cuda())
+
+
+def test_fp8_cache_write_bit_exact():
+    """The quantising write equals the oracle's, byte for byte, on sentinel pools:
+    ordinary values, ties, tiny values, values past +-448 * scale and infinities."""
+    rng = np.random.default_rng(8)
+    nb, bs, hkv, d = 30, 16, 4, 128
+    n = 200
+    slots = rng.choice(nb * bs, n, replace=False).astype(np.int64)
+    slots[::9] = -1
+    x = rng.standard_normal((2, n, hkv, d)) * 3
+    x[:, ::5] *= 1e-3                                   # subnormal codes
+    x[:, 1::7] *= 400                                   # saturation
+    bits = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    bits[0, 3, 0, :4] = [0x7F80, 0xFF80, 0x0000, 0x8000]  # +inf, -inf, +0, -0
+    kn, vn = bits[0].copy(), bits[1].copy()
+    ks, vs = 0.0625, 0.011
+    kc = np.full((nb, bs, hkv, d), 0x5A, np.uint8)
+    vc = np.full((nb, bs, hkv, d), 0xA5, np.uint8)
+    dk, dv = torch.from_numpy(kc).cuda(), torch.from_numpy(vc).cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.pa_cache_write_fp8(u16_to_dev_bf16(kn), u16_to_dev_bf16(vn), torch.from_numpy(slots).cuda(),
+                          dk, dv, ks, vs, status=status)
+    oracle.cache_write_fp8(kn, vn, slots, kc, vc, ks, vs)
+    assert np.array_equal(dk.cpu().numpy(), kc) and np.array_equal(dv.cpu().numpy(), vc)
+    assert status.item() == 0
+
+
+FP8_SMALL = [
+    # (Hq, Hkv, bs, lens)
+    (8, 8, 16, (1, 15, 16, 17, 33)),                # G = 1
+    (28, 4, 16, (257, 16, 1)),                      # G = 7
+    (16, 8, 16, (200, 129, 5)),                     # G = 2
+    (32, 2, 16, (129, 300)),                        # G = 16
+    (16, 4, 256, (300, 513, 2)),                    # pages
+    (2, 2, 16, (0, 5)),                             # empty sequence
+]
+
+
+@pytest.mark.parametrize("case", FP8_SMALL, ids=lambda c: f"Hq{c[0]}-Hkv{c[1]}-bs{c[2]}")
+def test_fp8_decode_small_elementwise(case):
+    Hq, Hkv, bs, lens = case
+    nb = sum((L + bs - 1) // bs for L in lens) + 5
+    w = W.with_fp8_pools(W.make_workload("f8", B=len(lens), Hq=Hq, Hkv=Hkv, D=128, block_size=bs,
+                                         seq_lens=list(lens), num_blocks=nb, seed=sum(lens) + 3,
+                                         poison_unused=True, write_new=False))
+    ref, ref_lse = oracle.decode_fp8(w.q, w.k_cache8, w.v_cache8, w.block_tables, w.seq_lens,
+                                     w.scale, w.k_scale, w.v_scale)
+    dev = Dev(w)
+    kc, vc = _fp8_dev(w)
+    for P in (1, 2, 3, 7, 0):
+        Pu = P or pa.pa_auto_num_splits(w.B, w.Hq, w.Hkv, w.D, w.max_blocks, w.block_size)
+        ws = torch.zeros(max(1, pa.pa_splitkv_workspace_bytes(w.B, w.Hq, w.D, Pu)),
+                         dtype=torch.uint8, device="cuda")
+        out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device="cuda")
+        pa.pa_decode_splitkv_fp8(out, lse, dev.q, kc, vc, w.k_scale, w.v_scale, dev.block_tables,
+                                 dev.seq_lens, w.scale, num_splits=Pu, workspace=ws,
+                                 status=dev.status)
+        assert_close(bf16_dev_to_f64(out), ref, f"fp8 P={Pu}")
+        assert_lse_close(lse.cpu().double().numpy(), ref_lse, f"fp8 P={Pu}")
+    assert dev.status_value() == 0
+
+
+@pytest.mark.parametrize("name", ["qwen2.5-7b-bs16-fp8", "qwen3-0.6b-B256-fp8", "long-B2-L32768-fp8"])
+def test_fp8_workload_full_size(name):
+    """Write this step's tokens with pa_cache_write_fp8, then decode (auto P and
+    unsplit), against the oracle's write and decode."""
+    w = W.WORKLOADS[name]()
+    kc8, vc8 = w.k_cache8.copy(), w.v_cache8.copy()
+    oracle.cache_write_fp8(w.k_new, w.v_new, w.slot_mapping, kc8, vc8, w.k_scale, w.v_scale)
+    ref, ref_lse = oracle.decode_fp8(w.q, kc8, vc8, w.block_tables, w.seq_lens, w.scale,
+                                     w.k_scale, w.v_scale)
+    dev = Dev(w)
+    kc, vc = _fp8_dev(w)
+    pa.pa_cache_write_fp8(dev.k_new, dev.v_new, dev.slot_mapping, kc, vc, w.k_scale, w.v_scale,
+                          status=dev.status)
+    assert np.array_equal(kc.cpu().numpy(), kc8) and np.array_equal(vc.cpu().numpy(), vc8)
+    for P in (0, 1):
+        Pu = P or pa.pa_auto_num_splits(w.B, w.Hq, w.Hkv, w.D, w.max_blocks, w.block_size)
+        ws = torch.zeros(max(1, pa.pa_splitkv_workspace_bytes(w.B, w.Hq, w.D, Pu)),
+                         dtype=torch.uint8, device="cuda")
+        out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device="cuda")
+        pa.pa_decode_splitkv_fp8(out, lse, dev.q, kc, vc, w.k_scale, w.v_scale, dev.block_tables,
+                                 dev.seq_lens, w.scale, num_splits=Pu, workspace=ws,
+                                 status=dev.status)
+        assert_close(bf16_dev_to_f64(out), ref, f"{name} P={Pu}")
+        assert_lse_close(lse.cpu().double().numpy(), ref_lse, f"{name} P={Pu}")
+    assert dev.status_value() == 0
