@@ -139,7 +139,7 @@ int pa_decode(void *out, float *lse, const void *q, const void *k_cache, const v
  * largest P for which the B * Hkv * P CTAs fit one wave of the decode kernel
  * that the group size Hq / Hkv and head_dim D select (2 CTAs per SM for the
  * CUDA-core kernel, 1 for the tensor-core kernel), capped so that every
- * partition keeps at least eight 16-token tiles.  Host-only; depends only on
+ * partition keeps at least four 16-token tiles.  Host-only; depends only on
  * its arguments and the PA_DECODE_KERNEL override described at pa_decode.
  * Returns P >= 1, or PA_EINVAL / PA_EUNSUPPORTED.
  */

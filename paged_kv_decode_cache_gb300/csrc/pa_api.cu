@@ -40,7 +40,7 @@ namespace {
 constexpr int kMaxGroupCc = 8;    // query heads per KV head, CUDA-core kernel
 constexpr int kMaxGroupTc = 16;   // query heads per KV head, tensor-core kernel
 constexpr int kMaxGridZ = 65535;  // sequences per launch (gridDim.z)
-constexpr int kMinTilesPerSplit = 8;
+constexpr int kMinTilesPerSplit = 4;  // 64 tokens: fewer idle SMs at 4k tokens
 constexpr int64_t kMaxRowsQ = 1 << 24;  // B x q_len of one multi-query call
 constexpr int kMaxSplits = 256;
 constexpr int PA_ETOOLARGE = -100;  // internal: the cooperative grid does not fit at once

@@ -90,7 +90,7 @@ def test_split_policy(lib, monkeypatch, B, Hq, Hkv, D, mb, bs, sms):
     units = _units(B, Hq, Hkv, D)
     if P > 1:
         assert units * P <= slots              # one wave of resident CTAs
-        assert chunk >= 16 * 8 or chunk * P >= lmax
+        assert chunk >= 16 * 4 or chunk * P >= lmax
     if units >= slots:
         assert P == 1
 
