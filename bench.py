@@ -334,7 +334,11 @@ def run_ours(args, world, rank, local):
     use_tc = forced == "tensor_core" or (forced != "cuda_core" and w.D == 128)
     kernel_name = "decode_tc_kernel" if use_tc else "decode_cc_kernel"
 
-    ws = torch.zeros(max(1, pa.pa_splitkv_workspace_bytes(w.B * w.q_len, w.Hq, w.D, P)), dtype=torch.uint8,
+    cascade = w.cascade_blocks > 0   # shared prefix attended once, then the suffixes, then a merge
+    ws_bytes = (pa.pa_cascade_workspace_bytes(w.B, w.Hq, w.Hkv, w.D, w.cascade_blocks, w.max_blocks,
+                                              w.block_size) if cascade
+                else pa.pa_splitkv_workspace_bytes(w.B * w.q_len, w.Hq, w.D, P))
+    ws = torch.zeros(max(1, ws_bytes), dtype=torch.uint8,
                      device=dev)
     merged = P > 1   # the split kernel merges its own partials (one cooperative launch)
 
@@ -342,11 +346,14 @@ def run_ours(args, world, rank, local):
         kc, vc = pools[r]
         if fp8:
             pa.pa_cache_write_fp8(kn, vn, slots, kc, vc, w.k_scale, w.v_scale, stream=stream)
-        elif args.unfused or mq:
+        elif args.unfused or mq or cascade:
             pa.pa_cache_write(kn, vn, slots, kc, vc, stream=stream)
         if ev0 is not None:
             ev0.record(stream)
-        if fp8:
+        if cascade:
+            pa.pa_decode_cascade(out, lse, q, kc, vc, w.cascade_blocks, bt, sl, w.scale, workspace=ws,
+                                 stream=stream)
+        elif fp8:
             pa.pa_decode_splitkv_fp8(out, lse, q, kc, vc, w.k_scale, w.v_scale, bt, sl, w.scale,
                                      num_splits=P, workspace=ws, stream=stream)
         elif mq:
@@ -361,8 +368,8 @@ def run_ours(args, world, rank, local):
         if ev1 is not None:
             ev1.record(stream)
 
-    fused = not (args.unfused or mq or fp8)
-    launches_per_step = 1 if fused else 2
+    fused = not (args.unfused or mq or fp8 or cascade)
+    launches_per_step = 4 if cascade else 1 if fused else 2   # cascade: write, prefix, suffix, combine
     # CUDA graphs of S consecutive steps (cycling over the pool replicas), NG
     # copies, each step with its own pair of graph-recorded events around the
     # decode kernel.  Step i of the timed loop is step i % S of graph copy
@@ -440,7 +447,11 @@ def run_ours(args, world, rank, local):
             for d, h in ((d_q16, h_q), (bt, h_bt), (sl, h_sl), (d_kn16, h_kn), (d_vn16, h_vn),
                          (slots, h_slots)):
                 d.copy_(h, non_blocking=True)
-            if fp8:
+            if cascade:
+                pa.pa_cache_write(kn, vn, slots, kc, vc, stream=stream)
+                pa.pa_decode_cascade(out, lse, q, kc, vc, w.cascade_blocks, bt, sl, w.scale,
+                                     workspace=ws, stream=stream)
+            elif fp8:
                 pa.pa_cache_write_fp8(kn, vn, slots, kc, vc, w.k_scale, w.v_scale, stream=stream)
                 pa.pa_decode_splitkv_fp8(out, lse, q, kc, vc, w.k_scale, w.v_scale, bt, sl, w.scale,
                                          num_splits=P, workspace=ws, stream=stream)
@@ -478,7 +489,8 @@ def run_ours(args, world, rank, local):
         roofline = {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
                     "frac": round(ach / peak, 4), "traffic": recorded_traffic(args.workload, kernel_name),
                     "peak_kind": peak_kind,
-                    "kernel": kernel_name + (" (fp8 pools)" if fp8 else " (multi-query)" if mq else
+                    "kernel": kernel_name + (" (cascade: prefix + suffix + combine)" if cascade else
+                                             " (fp8 pools)" if fp8 else " (multi-query)" if mq else
                                              "" if args.unfused else " (fused write)")
                               + (" + split merge" if merged else ""),
                     "kernel_us": round(kern_ms_avg * 1e3, 3), "kernel_bytes": kern_bytes}
@@ -498,7 +510,8 @@ def run_ours(args, world, rank, local):
             "config": {"workload": args.workload, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
                        "block_size": w.block_size, "seq_lens_total": int(w.seq_lens.sum()),
                        "splits": P, "q_len": w.q_len,
-                       "step": ("pa_cache_write_fp8, then pa_decode_splitkv_fp8 (e4m3 pools)"
+                       "step": ("pa_cache_write, then pa_decode_cascade (3 launches)" if cascade else
+                                "pa_cache_write_fp8, then pa_decode_splitkv_fp8 (e4m3 pools)"
                                 if fp8 else
                                 "cache_write of the q_len new tokens, then pa_decode_mq (causal)"
                                 if mq else "cache_write, then split decode with merge"

@@ -295,6 +295,35 @@ int pa_decode_mq(void *out, float *lse, const void *q, int32_t q_len, const void
                  int32_t *status, pa_stream_t stream);
 
 /*
+ * Cascade decode over a shared prefix: the first n_prefix_blocks entries of
+ * every sequence's block table name the same physical blocks (a prefix-cache
+ * hit shared by the batch: "mini-infer" prajwal7-2002 docs, table "Core
+ * Capabilities at a Glance", row "Prompt Caching", radix-tree prefix cache;
+ * psmarter write-up, feature list item 4, prefix caching).  The result is
+ * pa_decode_splitkv's, computed in three launches: (1) the prefix once, all B
+ * sequences' queries attending it together (one CTA reads a prefix block for
+ * up to 16 / G sequences); (2) every sequence's remaining positions,
+ * [n_prefix_blocks * block_size, seq_lens[b]); (3) a log-sum-exp merge of both
+ * passes' fp32 partials.  Requires seq_lens[b] >= n_prefix_blocks *
+ * block_size (a shorter sequence sets PA_STATUS_BAD_SEQLEN and its result is
+ * undefined); 0 <= n_prefix_blocks < max_blocks_per_seq (0: plain
+ * pa_decode_splitkv).  The library reads the prefix's block ids from table
+ * row 0.  workspace: pa_cascade_workspace_bytes(...) bytes (fp32 partials),
+ * 256-byte aligned.  Tensor-core kernel only: head_dim 128, Hq / Hkv <= 16.
+ */
+int pa_decode_cascade(void *out, float *lse, const void *q, const void *k_cache,
+                      const void *v_cache, pa_cache_desc cache, int32_t n_prefix_blocks,
+                      const int32_t *block_tables, int32_t max_blocks_per_seq,
+                      const int32_t *seq_lens, int32_t B, int32_t Hq, float scale,
+                      void *workspace, size_t workspace_bytes, int32_t *status,
+                      pa_stream_t stream);
+
+/* Workspace bytes pa_decode_cascade needs on the current device (0 on bad arguments). */
+size_t pa_cascade_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+                                  int32_t n_prefix_blocks, int32_t max_blocks_per_seq,
+                                  int32_t block_size);
+
+/*
  * FP8 KV cache.  The pages say only that the KV-cache manager supports several
  * quantisation schemes ("Mini-Infer: A High-Performance LLM Inference
  * Acceleration Engine for Production Environments", section "Memory

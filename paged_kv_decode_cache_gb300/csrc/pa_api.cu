@@ -250,6 +250,12 @@ pa::DecodeParams base_params(const void *q, const pa_cache_desc &c, const int32_
     p.q_per_cta = 1;
     p.head_groups = c.num_kv_heads;
     p.v_scale = 1.f;
+    p.causal = 1;
+    p.seq_len_const = -1;
+    p.seq_len_offset = 0;
+    p.part_stride = 0;   // run_decode: the partition count
+    p.part_offset = 0;
+    p.table_stride = max_blocks;
     return p;
 }
 
@@ -274,6 +280,16 @@ int sm_count_current() {
     return n;
 }
 
+// Settings of one pass of a cascade decode (defaults: an ordinary call).
+struct PassOpts {
+    int32_t causal = 1;
+    int32_t seq_len_const = -1;   // >= 0: every sequence has this length
+    int32_t seq_len_offset = 0;   // subtracted from seq_lens[b]
+    int32_t part_stride = 0;      // 0: the pass's own partition count
+    int32_t part_offset = 0;
+    int32_t table_stride = 0;     // 0: max_blocks
+};
+
 // Scales of FP8 (e4m3) pools: a stored code c means c * scale.
 struct Fp8Scales {
     float k_scale, v_scale;
@@ -291,7 +307,7 @@ int run_decode(bool split, void *out, float *lse, float *part_o, float *part_lse
                const int32_t *block_tables, int32_t max_blocks, const int32_t *seq_lens,
                int32_t B, int32_t Hq, float scale, int32_t P, int32_t *status,
                cudaStream_t stream, int32_t *counters = nullptr, const NewTokens &nt = NewTokens(),
-               int32_t q_len = 1, const Fp8Scales *f8 = nullptr) {
+               int32_t q_len = 1, const Fp8Scales *f8 = nullptr, const PassOpts &po = PassOpts()) {
     const int G = Hq / c.num_kv_heads;
     const int qpc = queries_per_cta(G, q_len);
     Kernel k;
@@ -307,6 +323,15 @@ int run_decode(bool split, void *out, float *lse, float *part_o, float *part_lse
     p.part_lse = part_lse;
     p.split = split ? 1 : 0;
     p.num_splits = P;
+    p.part_stride = po.part_stride ? po.part_stride : P;
+    p.part_offset = po.part_offset;
+    p.causal = po.causal;
+    p.seq_len_const = po.seq_len_const;
+    p.seq_len_offset = po.seq_len_offset;
+    if (po.table_stride) p.table_stride = po.table_stride;
+    if ((po.table_stride || po.seq_len_const >= 0 || po.seq_len_offset || !po.causal ||
+         po.part_offset) && k != Kernel::kTensorCore)
+        return PA_EUNSUPPORTED;  // cascade passes: tensor cores only
     p.chunk = pa_partition_tokens(max_blocks, c.block_size, P);
     p.counters = counters;
     p.k_new = static_cast<const uint16_t *>(nt.k_new);
@@ -575,6 +600,87 @@ int pa_decode_splitkv_fp8(void *out, float *lse, const void *q, const void *k_ca
     return splitkv_common(out, lse, q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq,
                           seq_lens, B, Hq, scale, num_splits, workspace, workspace_bytes, status,
                           stream, NewTokens(), 1, &f8);
+}
+
+// Cascade decode: partition counts of the prefix pass (all B sequences' queries
+// as one multi-query call over the shared blocks) and of the suffix pass.
+static int cascade_splits(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t n_prefix_blocks,
+                          int32_t max_blocks_per_seq, int32_t block_size, int *P1, int *P2) {
+    const int sms = sm_count_current();
+    if (sms <= 0) return PA_ECUDA;
+    *P1 = pa_choose_num_splits_mq(1, B, Hq, Hkv, D, n_prefix_blocks, block_size, sms);
+    if (*P1 < 0) return *P1;
+    *P2 = pa_choose_num_splits(B, Hq, Hkv, D, max_blocks_per_seq - n_prefix_blocks, block_size, sms);
+    if (*P2 < 0) return *P2;
+    return PA_OK;
+}
+
+size_t pa_cascade_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+                                  int32_t n_prefix_blocks, int32_t max_blocks_per_seq,
+                                  int32_t block_size) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || n_prefix_blocks <= 0 ||
+        n_prefix_blocks >= max_blocks_per_seq)
+        return 0;
+    int P1 = 0, P2 = 0;
+    if (cascade_splits(B, Hq, Hkv, D, n_prefix_blocks, max_blocks_per_seq, block_size, &P1, &P2))
+        return 0;
+    return pa_splitkv_workspace_bytes(B, Hq, D, P1 + P2 < 2 ? 2 : P1 + P2);
+}
+
+int pa_decode_cascade(void *out, float *lse, const void *q, const void *k_cache,
+                      const void *v_cache, pa_cache_desc cache, int32_t n_prefix_blocks,
+                      const int32_t *block_tables, int32_t max_blocks_per_seq,
+                      const int32_t *seq_lens, int32_t B, int32_t Hq, float scale,
+                      void *workspace, size_t workspace_bytes, int32_t *status,
+                      pa_stream_t stream) {
+    int rc = check_decode_args(q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq,
+                               seq_lens, B, Hq, scale);
+    if (rc) return rc;
+    if (!out || !aligned(out, 16) || (lse && !aligned(lse, 4))) return PA_EINVAL;
+    if (n_prefix_blocks < 0 || n_prefix_blocks >= max_blocks_per_seq) return PA_EINVAL;
+    if (B == 0) return PA_OK;
+    if (n_prefix_blocks == 0)  // nothing shared: plain split decode
+        return splitkv_common(out, lse, q, k_cache, v_cache, cache, block_tables,
+                              max_blocks_per_seq, seq_lens, B, Hq, scale, 0, workspace,
+                              workspace_bytes, status, stream, NewTokens());
+    int P1 = 0, P2 = 0;
+    rc = cascade_splits(B, Hq, cache.num_kv_heads, cache.head_dim, n_prefix_blocks,
+                        max_blocks_per_seq, cache.block_size, &P1, &P2);
+    if (rc) return rc;
+    const int PT = P1 + P2;
+    const size_t need = pa_splitkv_workspace_bytes(B, Hq, cache.head_dim, PT);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return PA_EWORKSPACE;
+    const int64_t rows = static_cast<int64_t>(B) * Hq;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    float *part_o = reinterpret_cast<float *>(ws);
+    float *part_lse = reinterpret_cast<float *>(ws + round_up(rows * PT * cache.head_dim * 4, 256));
+    const int32_t prefix_len = n_prefix_blocks * cache.block_size;
+    // 1. the shared prefix, once: every sequence's queries as the q_len = B
+    //    queries of one non-causal call over table row 0's first blocks
+    PassOpts pre;
+    pre.causal = 0;
+    pre.seq_len_const = prefix_len;
+    pre.part_stride = PT;
+    pre.part_offset = 0;
+    rc = run_decode(true, nullptr, nullptr, part_o, part_lse, q, k_cache, v_cache, cache,
+                    block_tables, n_prefix_blocks, seq_lens, 1, Hq, scale, P1, status, stream,
+                    nullptr, NewTokens(), B, nullptr, pre);
+    if (rc) return rc;
+    // 2. each sequence's own blocks: the table from entry n_prefix_blocks on,
+    //    lengths less the prefix
+    PassOpts suf;
+    suf.seq_len_offset = prefix_len;
+    suf.part_stride = PT;
+    suf.part_offset = P1;
+    suf.table_stride = max_blocks_per_seq;
+    rc = run_decode(true, nullptr, nullptr, part_o, part_lse, q, k_cache, v_cache, cache,
+                    block_tables + n_prefix_blocks, max_blocks_per_seq - n_prefix_blocks, seq_lens,
+                    B, Hq, scale, P2, status, stream, nullptr, NewTokens(), 1, nullptr, suf);
+    if (rc) return rc;
+    // 3. one log-sum-exp merge of the P1 + P2 partials of every row
+    cudaError_t e = pa::launch_combine(out, lse, part_o, part_lse, static_cast<int>(rows), PT,
+                                       cache.head_dim, stream);
+    return e == cudaSuccess ? PA_OK : PA_ECUDA;
 }
 
 int pa_decode_splitkv(void *out, float *lse, const void *q, const void *k_cache,

@@ -233,8 +233,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     auto col_row = [&](int hh, int c) -> int64_t {
         return row0 + static_cast<int64_t>(c / G) * Hq + hh * G + c % G;
     };
-    const int32_t *bt = p.block_tables + static_cast<int64_t>(b) * p.max_blocks;
-    int L = p.seq_lens[b];
+    const int32_t *bt = p.block_tables + static_cast<int64_t>(b) * p.table_stride;
+    int L = p.seq_len_const >= 0 ? p.seq_len_const : p.seq_lens[b] - p.seq_len_offset;
     constexpr int kQLoads = (N * (D / 8) + kThreads - 1) / kThreads;
     uint4 qv[kQLoads];
 #pragma unroll
@@ -270,9 +270,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         const int64_t last = col_row(HC - 1, Gq - 1);
         const __nv_bfloat16 *out_rows = static_cast<const __nv_bfloat16 *>(p.out) + row0 * D;
         if (p.split) {
-            if (lane == 0) touch = p.part_o + (row0 * p.num_splits + part) * D;
-            if (lane == 1) touch = p.part_o + (last * p.num_splits + part) * D;
-            if (lane == 2) touch = p.part_lse + row0 * p.num_splits + part;
+            if (lane == 0) touch = p.part_o + (row0 * p.part_stride + p.part_offset + part) * D;
+            if (lane == 1) touch = p.part_o + (last * p.part_stride + p.part_offset + part) * D;
+            if (lane == 2) touch = p.part_lse + row0 * p.part_stride + p.part_offset + part;
             if (lane == 3 && p.counters && p.out) touch = out_rows;  // the merge writes out
         } else {
             if (lane == 0) touch = out_rows;
@@ -285,9 +285,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         L = L < 0 ? 0 : lmax;
     }
     // Query qi0 + k sits at position qbase + k and sees tokens up to it
-    // (causal); no key past this CTA's last query is read.
-    const int qbase = L - p.q_len + qi0;
-    const int t_end = min(t_begin + p.chunk, max(0, min(L, qbase + nq)));
+    // (causal); no key past this CTA's last query is read.  Non-causal
+    // (cascade prefix pass): every query sees all L keys.
+    const int qbase = p.causal ? L - p.q_len + qi0 : L;
+    const int t_end = min(t_begin + p.chunk, max(0, min(L, p.causal ? qbase + nq : L)));
     const int nch = t_end > t_begin ? (t_end - t_begin + C::kT - 1) / C::kT : 0;
 
     if (nch == 0) {  // empty range: zero output, lse = -inf
@@ -295,12 +296,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         for (int i = tid; i < HC * Gq * D; i += kThreads) {
             const int j = i / D, d = i % D;
             const int64_t r = col_row(j / Gq, j % Gq);
-            if (p.split) p.part_o[(r * p.num_splits + part) * D + d] = 0.f;
+            if (p.split) p.part_o[(r * p.part_stride + p.part_offset + part) * D + d] = 0.f;
             else static_cast<__nv_bfloat16 *>(p.out)[r * D + d] = __float2bfloat16_rn(0.f);
         }
         if (tid < HC * Gq) {
             const int64_t r = col_row(tid / Gq, tid % Gq);
-            if (p.split) p.part_lse[r * p.num_splits + part] = -INFINITY;
+            if (p.split) p.part_lse[r * p.part_stride + p.part_offset + part] = -INFINITY;
             else if (p.lse) p.lse[r] = -INFINITY;
         }
         if (p.split)
@@ -743,8 +744,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             tc5::fence_after_sync();
             // O^T row d = tid, 16 columns at a time, normalised and stored; column
             // n = (head hh, query q) goes to the CTA's output row hh * G + q
-            const int64_t stride = p.split ? static_cast<int64_t>(p.num_splits) * D : D;
-            float *of = p.split ? p.part_o + (row0 * p.num_splits + part) * D + tid : nullptr;
+            const int64_t stride = p.split ? static_cast<int64_t>(p.part_stride) * D : D;
+            float *of = p.split ? p.part_o + (row0 * p.part_stride + p.part_offset + part) * D + tid : nullptr;
             __nv_bfloat16 *oh = p.split ? nullptr : static_cast<__nv_bfloat16 *>(p.out) + row0 * D + tid;
 #pragma unroll 1
             for (int k = 0; k < N / 16; ++k) {
@@ -764,7 +765,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                 const int n = tid;
                 const float lse = (m_ref[n] + log2f(col[n])) * 0.69314718055994531f;
                 const int64_t r = row0 + rel_s[n];
-                if (p.split) p.part_lse[r * p.num_splits + part] = lse;
+                if (p.split) p.part_lse[r * p.part_stride + p.part_offset + part] = lse;
                 else if (p.lse) p.lse[r] = lse;
             }
         }

@@ -50,6 +50,15 @@ struct DecodeParams {
     // FP8 pools (e4m3 codes): scale_log2 already includes k_scale; the output
     // is multiplied by v_scale.  1 for bf16 pools.
     float v_scale;
+    // Cascade passes (tensor-core kernel): causal = 0 lets every query see all
+    // L keys; L is seq_len_const when >= 0, else seq_lens[b] - seq_len_offset;
+    // partials of row r, partition p go to [r * part_stride + part_offset + p].
+    int32_t causal;
+    int32_t seq_len_const;
+    int32_t seq_len_offset;
+    int32_t part_stride;
+    int32_t part_offset;
+    int32_t table_stride;   // entries between block-table rows (>= max_blocks)
 };
 
 // CUDA-core decode kernel launch (pa_decode_cc_d*.cu).  Returns a cudaError_t.

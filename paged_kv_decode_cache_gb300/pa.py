@@ -61,6 +61,9 @@ _SIGNATURES = {
     "pa_decode_mq": ([_P, _P, _P, _I32, _P, _P, CacheDesc, _P, _I32, _P, _I32, _I32, _F32, _I32,
                       _P, _SZ, _P, _P], ctypes.c_int),
     "pa_choose_num_splits_mq": ([_I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32], ctypes.c_int),
+    "pa_decode_cascade": ([_P, _P, _P, _P, _P, CacheDesc, _I32, _P, _I32, _P, _I32, _I32, _F32, _P,
+                           _SZ, _P, _P], ctypes.c_int),
+    "pa_cascade_workspace_bytes": ([_I32, _I32, _I32, _I32, _I32, _I32, _I32], _SZ),
     "pa_cache_write_fp8": ([_P, _P, _P, _I64, _P, _P, CacheDesc, _F32, _F32, _P, _P], ctypes.c_int),
     "pa_decode_splitkv_fp8": ([_P, _P, _P, _P, _P, CacheDesc, _F32, _F32, _P, _I32, _P, _I32, _I32,
                                _F32, _I32, _P, _SZ, _P, _P], ctypes.c_int),
@@ -313,6 +316,32 @@ def pa_decode_mq(out, lse, q, k_cache, v_cache, block_tables, seq_lens, scale, n
                             _ptr(seq_lens), B, Hq, float(scale), num_splits, _ptr(workspace),
                             ws_bytes, _ptr(status), _stream(stream))
     _check("pa_decode_mq", rc)
+
+
+def pa_cascade_workspace_bytes(B: int, Hq: int, Hkv: int, D: int, n_prefix_blocks: int,
+                               max_blocks_per_seq: int, block_size: int) -> int:
+    return int(lib().pa_cascade_workspace_bytes(B, Hq, Hkv, D, n_prefix_blocks, max_blocks_per_seq,
+                                                block_size))
+
+
+def pa_decode_cascade(out, lse, q, k_cache, v_cache, n_prefix_blocks, block_tables, seq_lens, scale,
+                      workspace=None, status=None, stream=None):
+    """Decode with the first n_prefix_blocks table entries shared by every sequence:
+    the prefix is attended once for the whole batch, then each suffix, then merged."""
+    B, Hq, D = _decode_inputs(q, k_cache, v_cache, block_tables, seq_lens)
+    _need(out, "out", torch.bfloat16, 3)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 2)
+    ws_bytes = 0
+    if workspace is not None:
+        if not (workspace.is_cuda and workspace.is_contiguous()):
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    rc = lib().pa_decode_cascade(_ptr(out), _ptr(lse), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                 cache_desc(k_cache), n_prefix_blocks, _ptr(block_tables),
+                                 block_tables.shape[1], _ptr(seq_lens), B, Hq, float(scale),
+                                 _ptr(workspace), ws_bytes, _ptr(status), _stream(stream))
+    _check("pa_decode_cascade", rc)
 
 
 def _need_pool8(t, name):

@@ -54,6 +54,7 @@ class DecodeWorkload:
     v_cache8: Optional[np.ndarray] = None
     k_scale: float = 1.0
     v_scale: float = 1.0
+    cascade_blocks: int = 0    # > 0: decode with the first this-many table entries as a shared prefix
 
     @property
     def fp8(self) -> bool:
@@ -215,6 +216,12 @@ def with_fp8_pools(w: DecodeWorkload) -> DecodeWorkload:
     return w
 
 
+def _cascade(w: DecodeWorkload, n: int) -> DecodeWorkload:
+    w.cascade_blocks = n
+    w.name = w.name + "-cascade"
+    return w
+
+
 def spec_verify(base: str, q_len: int, **kw) -> DecodeWorkload:
     """Speculative verification on a decode workload: the last q_len positions
     of every sequence are the target model's queries (q_len - 1 drafted tokens
@@ -239,6 +246,8 @@ WORKLOADS = {
 # multi-query (speculative verification) families: the pages' 1.5B target model
 # verifying drafts, and the 7B / Qwen3 layers with four queries per sequence
 WORKLOADS.update({
+    # the Qwen3 batch decoded as a cascade over its 8 shared prefix blocks
+    "qwen3-0.6b-B256-cascade": lambda **kw: _cascade(qwen3_0p6b(256, **kw), 8),
     # FP8 (e4m3) pools: the 7B layer, the long-context stress, the Qwen3 batch
     "qwen2.5-7b-bs16-fp8": lambda **kw: with_fp8_pools(qwen25_7b(16, **kw)),
     "long-B2-L32768-fp8": lambda **kw: with_fp8_pools(long_context(2, 32768, **kw)),

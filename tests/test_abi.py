@@ -257,3 +257,13 @@ def test_fp8_rejects_bad_arguments(lib, monkeypatch):
     assert lib.pa_decode_splitkv_fp8(FAKE, None, FAKE, FAKE, FAKE, d, 1.0, 1.0, FAKE, 7, FAKE, 4, 4,
                                      0.1, 1, None, 0, None, None) == pa.PA_EUNSUPPORTED
     assert lib.pa_cache_write_fp8(FAKE, FAKE, FAKE, 0, FAKE, FAKE, d, 1.0, 1.0, None, None) == pa.PA_OK
+
+
+def test_cascade_rejects_bad_arguments(lib):
+    d = _desc(d=128)
+    for npre in (-1, 7, 9):   # max_blocks = 7
+        rc = lib.pa_decode_cascade(FAKE, None, FAKE, FAKE, FAKE, d, npre, FAKE, 7, FAKE, 4, 4, 0.1,
+                                   None, 0, None, None)
+        assert rc == pa.PA_EINVAL, npre
+    assert lib.pa_cascade_workspace_bytes(4, 4, 4, 128, 0, 7, 16) == 0
+    assert lib.pa_cascade_workspace_bytes(4, 4, 4, 128, 7, 7, 16) == 0

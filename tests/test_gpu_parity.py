@@ -569,3 +569,54 @@ def test_fp8_workload_full_size(name):
         assert_close(bf16_dev_to_f64(out), ref, f"{name} P={Pu}")
         assert_lse_close(lse.cpu().double().numpy(), ref_lse, f"{name} P={Pu}")
     assert dev.status_value() == 0
+
+
+# ------------------------------------------------ cascade decode (shared prefix)
+CASCADE = [
+    # (Hq, Hkv, bs, lens, shared prefix blocks)
+    (16, 8, 16, (200, 129, 300, 150), 8),           # Qwen3-like, G = 2
+    (28, 4, 16, (300, 257, 1000), 4),               # G = 7: one sequence per CTA column group
+    (12, 2, 16, (70, 100, 33), 2),                  # G = 6
+    (32, 2, 16, (129, 300), 3),                     # G = 16
+    (16, 4, 256, (300, 513), 1),                    # 256-token pages
+    (4, 2, 16, tuple(range(40, 80)), 2),            # 40 sequences: several query groups
+]
+
+
+@pytest.mark.parametrize("case", CASCADE, ids=lambda c: f"Hq{c[0]}-Hkv{c[1]}-bs{c[2]}-B{len(c[3])}")
+def test_cascade_matches_oracle(case):
+    Hq, Hkv, bs, lens, npre = case
+    nb = sum((L + bs - 1) // bs for L in lens) + 5
+    w = W.make_workload("casc", B=len(lens), Hq=Hq, Hkv=Hkv, D=128, block_size=bs, seq_lens=list(lens),
+                        num_blocks=nb, seed=npre + len(lens), shared_prefix_blocks=npre,
+                        poison_unused=True, write_new=False)
+    ref, ref_lse = oracle.decode(w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.scale)
+    dev = Dev(w)
+    ws = torch.zeros(max(1, pa.pa_cascade_workspace_bytes(w.B, w.Hq, w.Hkv, w.D, npre, w.max_blocks,
+                                                          w.block_size)), dtype=torch.uint8, device="cuda")
+    out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device="cuda")
+    pa.pa_decode_cascade(out, lse, dev.q, dev.k_cache, dev.v_cache, npre, dev.block_tables,
+                         dev.seq_lens, w.scale, workspace=ws, status=dev.status)
+    assert_close(bf16_dev_to_f64(out), ref, "cascade")
+    assert_lse_close(lse.cpu().double().numpy(), ref_lse, "cascade")
+    assert dev.status_value() == 0
+
+
+def test_cascade_full_size_qwen3():
+    """The Qwen3 batch (256 sequences, 8 shared prefix blocks) after this step's write."""
+    w = W.WORKLOADS["qwen3-0.6b-B256-cascade"]()
+    kc, vc = oracle_after_write(w)
+    ref, ref_lse = oracle.decode(w.q, kc, vc, w.block_tables, w.seq_lens, w.scale)
+    dev = Dev(w)
+    dev.write()
+    ws = torch.zeros(pa.pa_cascade_workspace_bytes(w.B, w.Hq, w.Hkv, w.D, w.cascade_blocks,
+                                                   w.max_blocks, w.block_size),
+                     dtype=torch.uint8, device="cuda")
+    out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device="cuda")
+    pa.pa_decode_cascade(out, lse, dev.q, dev.k_cache, dev.v_cache, w.cascade_blocks,
+                         dev.block_tables, dev.seq_lens, w.scale, workspace=ws, status=dev.status)
+    assert_close(bf16_dev_to_f64(out), ref, "cascade qwen3")
+    assert_lse_close(lse.cpu().double().numpy(), ref_lse, "cascade qwen3")
+    assert dev.status_value() == 0
