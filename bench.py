@@ -12,8 +12,10 @@ device synchronise on each side, timed with CUDA events on the launching
 stream; every step is replayed from a CUDA graph (one graph per pool
 replica), and consecutive steps rotate over enough copies of the KV pool that
 the data a step reads was evicted from the 129 MB L2 before it is read again.
-The decode kernel's own duration is measured with events recorded inside the
-graphs.  Prints one JSON line (rank 0).
+A step that is one launch (the default fused step) has its kernel duration
+taken as the timed region over the launches; other steps sample the decode
+kernel with events recorded inside the graphs (one step per graph copy, since
+event nodes slow the steps around them).  Prints one JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
@@ -371,10 +373,13 @@ def run_ours(args, world, rank, local):
     fused = not (args.unfused or mq or fp8 or cascade)
     launches_per_step = 4 if cascade else 1 if fused else 2   # cascade: write, prefix, suffix, combine
     # CUDA graphs of S consecutive steps (cycling over the pool replicas), NG
-    # copies, each step with its own pair of graph-recorded events around the
-    # decode kernel.  Step i of the timed loop is step i % S of graph copy
-    # (i // S) % NG, so after the loop every event pair holds a duration
-    # measured inside the timed region.
+    # copies.  Event nodes in a graph cost the steps around them several us of
+    # launch gaps, so only the first step of each graph copy carries a pair of
+    # events around the decode kernel: a sample of its duration measured inside
+    # the timed region.  Step i of the timed loop is step i % S of graph copy
+    # (i // S) % NG.  A step that is a single launch (the fused step) is timed
+    # more exactly by the whole region: its average launch duration is the
+    # region's time over the launches, gaps included.
     S = R * max(1, math.ceil(16 / R))
     NG = 8
     try:
@@ -388,7 +393,7 @@ def run_ours(args, world, rank, local):
     stream.synchronize()
 
     def capture(steps):
-        evs = [(mk(), mk()) if mk else (None, None) for _ in steps]
+        evs = [(mk(), mk()) if (mk and i == 0) else (None, None) for i in range(len(steps))]
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for r, (e0, e1) in zip(steps, evs):
@@ -425,10 +430,14 @@ def run_ours(args, world, rank, local):
     kern_ms = []
     if mk and n_full:
         for g, evs in full[:min(NG, n_full)]:
-            kern_ms += [e0.elapsed_time(e1) for e0, e1 in evs]
-    kern_ms_avg = statistics.mean(kern_ms) if kern_ms else None
+            kern_ms += [e0.elapsed_time(e1) for e0, e1 in evs if e0 is not None]
+    kern_ms_sampled = statistics.mean(kern_ms) if kern_ms else None
 
     ms_per_step = elapsed_ms / args.steps
+    if fused:   # one launch per step: the timed region over the launches
+        kern_ms_avg, kern_method = ms_per_step, "timed region / launches (one launch per step)"
+    else:
+        kern_ms_avg, kern_method = kern_ms_sampled, "CUDA events around the launch, sampled steps"
     value = step_bytes * world / (ms_per_step * 1e-3) / 1e12
 
     # ---- end to end through the public API, host buffers, copies inside the region
@@ -493,7 +502,10 @@ def run_ours(args, world, rank, local):
                                              " (fp8 pools)" if fp8 else " (multi-query)" if mq else
                                              "" if args.unfused else " (fused write)")
                               + (" + split merge" if merged else ""),
-                    "kernel_us": round(kern_ms_avg * 1e3, 3), "kernel_bytes": kern_bytes}
+                    "kernel_us": round(kern_ms_avg * 1e3, 3), "kernel_bytes": kern_bytes,
+                    "kernel_timing": kern_method,
+                    "kernel_us_event_sample": (round(kern_ms_sampled * 1e3, 3)
+                                               if kern_ms_sampled else None)}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
