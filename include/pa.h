@@ -119,7 +119,7 @@ int pa_cache_write(const void *k_new, const void *v_new, const int64_t *slot_map
  * q: device bf16 [B, Hq, D].  block_tables: device int32 [B, max_blocks_per_seq].
  * seq_lens: device int32 [B].  B == 0 is a no-op.
  * Supported: Hq % Hkv == 0, block_size a multiple of 16, and either D = 128
- * with G = Hq / Hkv <= 16 or D = 64 with G <= 8.  One CTA per (sequence, KV
+ * with G = Hq / Hkv <= 32 or D = 64 with G <= 8.  One CTA per (sequence, KV
  * head) holds the G query heads, so each KV tile is read once; use
  * pa_decode_splitkv when B * Hkv is small next to the SM count.
  * Two kernels implement the step: a tensor-core one (tcgen05, chosen
@@ -276,11 +276,11 @@ int pa_decode_step(void *out, float *lse, const void *q, const void *k_new, cons
  * nothing: out = 0, lse = -inf).
  * q: device bf16 [B, q_len, Hq, D]; out: device bf16 [B, q_len, Hq, D];
  * lse: device fp32 [B, q_len, Hq] or NULL.  1 <= q_len <= 65535.
- * Supported: D = 128, G = Hq / Hkv <= 16 (the tensor-core kernel; q_len > 1
+ * Supported: D = 128, G = Hq / Hkv <= 32 (the tensor-core kernel; q_len > 1
  * with PA_DECODE_KERNEL=cuda_core or D = 64 is PA_EUNSUPPORTED).  A CTA holds
- * up to 16 / G query positions of its heads; more positions are spread over
- * more CTAs, each reading the keys its queries can see (for q_len * G > 16
- * the KV is read about q_len * G / 16 times: suited to verification, not to
+ * up to 32 / G query positions of its heads; more positions are spread over
+ * more CTAs, each reading the keys its queries can see (for q_len * G > 32
+ * the KV is read about q_len * G / 32 times: suited to verification, not to
  * long prefill chunks).
  * num_splits: 0 = pa_choose_num_splits_mq on the current device, 1 = no
  * split (no workspace), P > 1 = split with the workspace contract of
@@ -302,14 +302,14 @@ int pa_decode_mq(void *out, float *lse, const void *q, int32_t q_len, const void
  * psmarter write-up, feature list item 4, prefix caching).  The result is
  * pa_decode_splitkv's, computed in three launches: (1) the prefix once, all B
  * sequences' queries attending it together (one CTA reads a prefix block for
- * up to 16 / G sequences); (2) every sequence's remaining positions,
+ * up to 32 / G sequences); (2) every sequence's remaining positions,
  * [n_prefix_blocks * block_size, seq_lens[b]); (3) a log-sum-exp merge of both
  * passes' fp32 partials.  Requires seq_lens[b] >= n_prefix_blocks *
  * block_size (a shorter sequence sets PA_STATUS_BAD_SEQLEN and its result is
  * undefined); 0 <= n_prefix_blocks < max_blocks_per_seq (0: plain
  * pa_decode_splitkv).  The library reads the prefix's block ids from table
  * row 0.  workspace: pa_cascade_workspace_bytes(...) bytes (fp32 partials),
- * 256-byte aligned.  Tensor-core kernel only: head_dim 128, Hq / Hkv <= 16.
+ * 256-byte aligned.  Tensor-core kernel only: head_dim 128, Hq / Hkv <= 32.
  */
 int pa_decode_cascade(void *out, float *lse, const void *q, const void *k_cache,
                       const void *v_cache, pa_cache_desc cache, int32_t n_prefix_blocks,
@@ -351,7 +351,7 @@ int pa_cache_write_fp8(const void *k_new, const void *v_new, const int64_t *slot
  * and their scales.  The result is attention over the dequantised values
  * (code * scale); the tensor-core kernel widens each landed tile to fp16
  * exactly and runs its MMAs in fp16 (q is rounded to fp16: |q| must stay below
- * 65504).  Supported: head_dim 128, Hq / Hkv <= 16 (PA_EUNSUPPORTED
+ * 65504).  Supported: head_dim 128, Hq / Hkv <= 32 (PA_EUNSUPPORTED
  * otherwise, and with PA_DECODE_KERNEL=cuda_core).
  */
 int pa_decode_splitkv_fp8(void *out, float *lse, const void *q, const void *k_cache,

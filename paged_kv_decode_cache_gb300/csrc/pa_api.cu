@@ -38,7 +38,7 @@ cudaError_t launch_decode_cc(int D, int G, const CUtensorMap &kmap, const CUtens
 namespace {
 
 constexpr int kMaxGroupCc = 8;    // query heads per KV head, CUDA-core kernel
-constexpr int kMaxGroupTc = 16;   // query heads per KV head, tensor-core kernel
+constexpr int kMaxGroupTc = 32;   // MMA columns per KV head (query heads x positions), tensor cores
 constexpr int kMaxGridZ = 65535;  // sequences per launch (gridDim.z)
 constexpr int kMinTilesPerSplit = 4;  // 64 tokens: fewer idle SMs at 4k tokens
 constexpr int64_t kMaxRowsQ = 1 << 24;  // B x q_len of one multi-query call
@@ -58,14 +58,16 @@ int next_pow2(int x) {
     return p;
 }
 
-// Shape of the tensor-core kernel for Hkv KV heads of G query heads each: HC
-// KV heads share a CTA (a power of two dividing Hkv, at most 8: a chunk is
-// 128 rows = 128 / HC tokens x HC heads) and every head's query group is
-// padded to GP columns, with HC * GP (the MMA N) between 16 and 64.
+// Shape of the tensor-core kernel for Hkv KV heads of G columns each (query
+// heads, times query positions for multi-query calls): HC KV heads share a
+// CTA (a power of two dividing Hkv, at most 8: a chunk is 128 rows = 128 / HC
+// tokens x HC heads) and every head's columns are padded to GP, with HC * GP
+// (the MMA N) between 16 and 64; more than 16 columns take a CTA per head.
 bool tc_shape(int G, int Hkv, int *HC, int *GP) {
     if (G < 1 || G > kMaxGroupTc || Hkv < 1) return false;
     int hc = 1;
     while (hc < 8 && Hkv % (hc * 2) == 0) hc *= 2;
+    if (G > 16) hc = 1;
     int gp = 1;
     for (;;) {
         gp = next_pow2(G);

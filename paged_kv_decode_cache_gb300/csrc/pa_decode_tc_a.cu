@@ -1,5 +1,5 @@
 // Tensor-core (tcgen05) paged decode kernels, head_dim 128: one instance per
-// (HC heads per CTA, GP padded group size) with HC * GP in {16, 32, 64}.
+// (HC heads per CTA, GP padded group size) with HC * GP in {16, 32, 64}; GP = 32 only with HC = 1.
 #include "pa_decode_tc.cuh"
 
 namespace pa {
@@ -10,6 +10,7 @@ cudaError_t launch_decode_tc(int HC, int GP, int G, const CUtensorMap &kmap,
 #define PA_TC_CASE(hc, gp) \
     if (HC == hc && GP == gp) return launch_tc_instance<hc, gp, false>(kmap, vmap, p, B, G, stream);
     PA_TC_CASE(1, 16)
+    PA_TC_CASE(1, 32)
     PA_TC_CASE(2, 8)
     PA_TC_CASE(2, 16)
     PA_TC_CASE(4, 4)

@@ -10,6 +10,7 @@ cudaError_t launch_decode_tc_f8(int HC, int GP, int G, const CUtensorMap &kmap,
 #define PA_TC_CASE(hc, gp) \
     if (HC == hc && GP == gp) return launch_tc_instance<hc, gp, true>(kmap, vmap, p, B, G, stream);
     PA_TC_CASE(1, 16)
+    PA_TC_CASE(1, 32)
     PA_TC_CASE(2, 8)
     PA_TC_CASE(2, 16)
     PA_TC_CASE(4, 4)

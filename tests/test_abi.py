@@ -60,6 +60,8 @@ def _tc_heads_per_cta(G, Hkv):
     hc = 1
     while hc < 8 and Hkv % (hc * 2) == 0:
         hc *= 2
+    if G > 16:      # more than 16 columns: one KV head per CTA
+        hc = 1
     while True:
         gp = 1
         while gp < G:
@@ -112,7 +114,8 @@ def test_kernel_override_rejects_what_it_cannot_run(lib, monkeypatch):
     assert lib.pa_choose_num_splits(1, 32, 2, 128, 16, 16, 152) == pa.PA_EUNSUPPORTED  # G = 16
     monkeypatch.delenv("PA_DECODE_KERNEL")
     assert lib.pa_choose_num_splits(1, 32, 2, 128, 16, 16, 152) >= 1                   # tensor cores
-    assert lib.pa_choose_num_splits(1, 34, 2, 128, 16, 16, 152) == pa.PA_EUNSUPPORTED  # G = 17
+    assert lib.pa_choose_num_splits(1, 64, 2, 128, 16, 16, 152) >= 1                   # G = 32
+    assert lib.pa_choose_num_splits(1, 66, 2, 128, 16, 16, 152) == pa.PA_EUNSUPPORTED  # G = 33
 
 
 def test_partition_tokens(lib):
@@ -141,7 +144,7 @@ FAKE = ctypes.c_void_p(1 << 20)  # aligned, never dereferenced: these calls fail
     (dict(q=None), pa.PA_EINVAL),
     (dict(Hq=5), pa.PA_EINVAL),                 # Hq % Hkv != 0
     (dict(Hq=18), pa.PA_EUNSUPPORTED),          # G = 9 > 8 at D = 64
-    (dict(Hq=34, desc=_desc(d=128)), pa.PA_EUNSUPPORTED),   # G = 17 > 16
+    (dict(Hq=66, desc=_desc(d=128)), pa.PA_EUNSUPPORTED),   # G = 33 > 32
     (dict(desc=_desc(d=96)), pa.PA_EUNSUPPORTED),
     (dict(desc=_desc(bs=8)), pa.PA_EUNSUPPORTED),
     (dict(desc=_desc(nb=0)), pa.PA_EINVAL),
@@ -208,9 +211,9 @@ def test_mq_split_policy(lib, monkeypatch):
         B, Hq, Hkv, D, mb, bs, sms = args
         assert pa.pa_choose_num_splits_mq(B, 1, Hq, Hkv, D, mb, bs, sms) == \
             pa.pa_choose_num_splits(B, Hq, Hkv, D, mb, bs, sms)
-    # 7B layer, 4 queries: 16 // 7 = 2 positions per CTA -> 2 query groups of 4 heads
-    # per sequence -> 16 CTAs per split -> one wave of 152 SMs holds P = 9
-    assert pa.pa_choose_num_splits_mq(8, 4, 28, 4, 128, 256, 16, 152) == 9
+    # 7B layer, 4 queries: 32 // 7 = 4 positions per CTA -> 28 columns, one KV head
+    # per CTA -> 4 CTAs per sequence per split -> one wave of 152 SMs holds P = 4
+    assert pa.pa_choose_num_splits_mq(8, 4, 28, 4, 128, 256, 16, 152) == 4
     # Qwen3 shape, 4 queries: all fit one CTA per 8 KV heads -> as q_len = 1
     assert pa.pa_choose_num_splits_mq(256, 4, 16, 8, 128, 128, 16, 152) == 1
     # more query groups never give more splits

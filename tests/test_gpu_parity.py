@@ -26,7 +26,7 @@ def kernels_for(Hq, Hkv, D):
     ks = []
     if G <= 8:
         ks.append("cuda_core")
-    if D == 128 and G <= 16:
+    if D == 128 and G <= 32:
         ks.append("tensor_core")
     return ks
 
@@ -90,6 +90,7 @@ SMALL = [
     (4, 1, 64, 256, (1000,)),                       # G = 4, pages, long-ish
     (2, 2, 128, 16, (0, 5)),                        # empty sequence
     (32, 2, 128, 16, (129, 300)),                   # G = 16 (tensor cores only)
+    (48, 2, 128, 16, (200, 65)),                    # G = 24: one KV head per CTA, 32 columns
     (24, 2, 128, 256, (700, 1)),                    # G = 12, pages (tensor cores only)
     (8, 2, 128, 16, (127, 128, 129, 255, 256, 257)),  # chunk boundaries of 128 tokens
 ]
