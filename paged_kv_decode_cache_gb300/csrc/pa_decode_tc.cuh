@@ -311,9 +311,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     }
 
     auto wait_or_abort = [&](uint64_t *bar, uint32_t parity) -> bool {
+        const uint64_t t0 = globaltimer_ns();
         for (uint32_t i = 0; i < kWaitLimit; ++i) {
             if (mbar_try_wait(bar, parity)) return true;
             if (*abort_flag) return false;
+            if (wait_expired(i, t0)) break;
         }
         *abort_flag = 1;
         set_status(p.status, PA_STATUS_TIMEOUT);
@@ -542,9 +544,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             if (cv) {  // the V producer wrote chunk c's mask before its loads
                 uint64_t mk = 0;
                 uint32_t i = 0;
+                const uint64_t t0 = globaltimer_ns();
                 for (; i < kWaitLimit; ++i) {
                     mk = vmask_ring[c % kTcMaskRing];
                     if (static_cast<uint32_t>(mk >> 32) == static_cast<uint32_t>(c) || *abort_flag) break;
+                    if (wait_expired(i, t0)) {
+                        i = kWaitLimit;
+                        break;
+                    }
                 }
                 if (static_cast<uint32_t>(mk >> 32) != static_cast<uint32_t>(c)) {
                     if (i == kWaitLimit) {
@@ -602,9 +609,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             uint64_t mk = 0;
             if (ok) {
                 uint32_t i = 0;
+                const uint64_t t0 = globaltimer_ns();
                 for (; i < kWaitLimit; ++i) {
                     mk = mask_ring[c % kTcMaskRing];
                     if (static_cast<uint32_t>(mk >> 32) == static_cast<uint32_t>(c) || *abort_flag) break;
+                    if (wait_expired(i, t0)) {
+                        i = kWaitLimit;
+                        break;
+                    }
                 }
                 if (static_cast<uint32_t>(mk >> 32) != static_cast<uint32_t>(c)) {
                     ok = false;

@@ -21,10 +21,23 @@ constexpr int kTile = 16;
 constexpr int kSubElems = 64;
 constexpr int kSubBytes = 128;
 
-// Bounded waits: iterations of mbarrier.try_wait before a warp gives up,
-// flags PA_STATUS_TIMEOUT and stops consuming.  A healthy copy completes in
-// a few microseconds; this is seconds.
+// Bounded waits: a warp polls for at most about a second (the GPU's global
+// nanosecond timer, read every 256 polls) and at most kWaitLimit polls, then
+// gives up, flags PA_STATUS_TIMEOUT and stops consuming.  A healthy copy or
+// merge completes in microseconds.
 constexpr uint32_t kWaitLimit = 1u << 24;
+constexpr uint64_t kWaitNs = 1000000000ull;
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// True once poll i of a wait that started at t0 is past the time limit.
+__device__ __forceinline__ bool wait_expired(uint32_t i, uint64_t t0) {
+    return (i & 255u) == 255u && globaltimer_ns() - t0 > kWaitNs;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -67,8 +80,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 
 // Wait for phase `parity` of `bar` to complete; false after kWaitLimit tries.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kWaitLimit; ++i)
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 0; i < kWaitLimit; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
+        if (wait_expired(i, t0)) break;
+    }
     return false;
 }
 

@@ -169,11 +169,13 @@ __device__ void merge_split_group(const DecodeParams &p, int group, int part, in
     if (t == 0) {
         atomicAdd(arrive, 1);
         bool ok = false;
+        const uint64_t t0 = globaltimer_ns();
         for (uint32_t i = 0; i < kWaitLimit; ++i) {
             if (ld_acquire_gpu(arrive) >= P) {
                 ok = true;
                 break;
             }
+            if (wait_expired(i, t0)) break;
         }
         if (!ok) set_status(p.status, PA_STATUS_TIMEOUT);
         *flag = ok;

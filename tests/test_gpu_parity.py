@@ -621,3 +621,39 @@ def test_cascade_full_size_qwen3():
     assert_close(bf16_dev_to_f64(out), ref, "cascade qwen3")
     assert_lse_close(lse.cpu().double().numpy(), ref_lse, "cascade qwen3")
     assert dev.status_value() == 0
+
+
+# ------------------------------------------------ a wait that nothing completes
+@pytest.mark.parametrize("kernel", ["cuda_core", "tensor_core"])
+def test_merge_wait_times_out_and_the_context_survives(kernel, use_kernel):
+    """The split merge waits for all P partitions to arrive; with the
+    workspace's arrival counters preset far below zero that count is never
+    reached.  Every CTA gives up after about a second, sets PA_STATUS_TIMEOUT
+    and returns (the wait comes after all of the CTA's copies and MMAs have
+    completed); the host reads the status and the next call is correct."""
+    import time
+    use_kernel(kernel)
+    w = _small(28 if kernel == "tensor_core" else 8, 4, 128, 16, (1000,), seed=3)
+    dev = Dev(w)
+    dev.write()
+    P = 4
+    ws = torch.zeros(pa.pa_splitkv_workspace_bytes(w.B, w.Hq, w.D, P), dtype=torch.uint8,
+                     device="cuda")
+    rows = w.B * w.Hq * P
+    rnd = lambda x: (x + 255) // 256 * 256                         # noqa: E731
+    counters = rnd(rows * w.D * 4) + rnd(rows * 4)                 # the workspace's last region
+    ws[counters:].view(torch.int32).fill_(-(1 << 30))
+    out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
+    t0 = time.time()
+    pa.pa_decode_splitkv(out, None, dev.q, dev.k_cache, dev.v_cache, dev.block_tables,
+                         dev.seq_lens, w.scale, num_splits=P, workspace=ws, status=dev.status)
+    torch.cuda.synchronize()
+    elapsed = time.time() - t0
+    assert dev.status_value() & pa.PA_STATUS_TIMEOUT
+    assert elapsed < 30, f"timed-out wait took {elapsed:.1f} s"
+    dev.status.zero_()
+    kc, vc = oracle_after_write(w)
+    ref, ref_lse = oracle.decode(w.q, kc, vc, w.block_tables, w.seq_lens, w.scale)
+    so, sl, _ = dev.splitkv(P)
+    assert_close(bf16_dev_to_f64(so), ref, f"after timeout {kernel}")
+    assert dev.status_value() == 0
