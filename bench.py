@@ -103,11 +103,40 @@ def measured_peak_gbs():
         return 6800.0, "fallback"
 
 
+def _code_only(text: str) -> str:
+    """C/CUDA source with comments removed and whitespace collapsed.
+
+    String and character literals are kept as written, so a change to code
+    (or to an inline-asm string) changes the result and a comment edit does not.
+    """
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            out.append(" ")
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def csrc_hash() -> str:
+    """Fingerprint of the kernels' code (comments and layout ignored)."""
     h = hashlib.sha256()
     for p in sorted(glob.glob(os.path.join(ROOT, "paged_kv_decode_cache_gb300", "csrc", "*"))):
-        with open(p, "rb") as f:
-            h.update(os.path.basename(p).encode() + f.read())
+        with open(p, encoding="utf-8", errors="replace") as f:
+            h.update(os.path.basename(p).encode() + b"\0" + _code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
