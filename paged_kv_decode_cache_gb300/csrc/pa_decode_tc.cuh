@@ -1,48 +1,67 @@
 // Paged decode attention on the 5th-generation tensor cores (tcgen05), for
 // head_dim 128.
 //
-// One CTA per (partition p, group of HC KV heads, sequence b) streams its
-// token range in chunks of T = 128 / HC tokens, loading whole paged blocks:
-// one TMA box per 16-token tile and 64-element half-row brings that tile for
-// all HC heads (16 rows x HC heads x 128 bytes, head-major in shared memory),
-// so the HBM reads of a block are contiguous bursts.  A chunk is therefore
-// 128 rows m = (tile, head, row) of K (and of V), and both contractions are
-// dense 128-row tiles:
+// One CTA per (partition p, group of HC KV heads and of queries, sequence b)
+// streams its token range in chunks of T = 128 / HC tokens, loading whole
+// paged blocks: one TMA box per 16-token tile and 64-element half-row brings
+// that tile for all HC heads (16 rows x HC heads x 128 bytes, head-major in
+// shared memory), so the HBM reads of a block are contiguous bursts.  A chunk
+// is therefore 128 rows m = (tile, head, row) of K (and of V), and both
+// contractions are dense 128-row tiles:
 //
 //   QK:  S[128 m, N] = K_chunk[128 m, 128 d] . Q^T[128 d, N]
-//        N = HC x GP columns n = (head', q): query head q of KV head head',
-//        zero-padded to GP per head.  A = the K chunk as TMA lands it
-//        (K-major, 128-byte swizzle), B = the packed queries.  Only the
-//        columns with head' = head(m) are used.
-//   PV:  O^T[128 d, N] += V_chunk^T[128 d, 128 m] . P^T[128 m, N]
-//        A = the V chunk read transposed (MN-major descriptor, no copy),
-//        B = P^T, block-diagonal by head: row m only has its own head's GP
-//        columns, the rest stay zero, so O^T[d, (h, q)] sums over head h's
+//        N = HC x GP columns n = (head', c): column c < Gq of KV head head'
+//        is query position qi0 + c / G of group member c % G (one position
+//        when q_len = 1), zero-padded to GP per head.  A = the K chunk as TMA
+//        lands it (K-major, 128-byte swizzle), B = the packed queries.  Only
+//        the columns with head' = head(m) are used.
+//   PV:  O^T[128 d, 2N] += V_chunk^T[128 d, 128 m] . [P_hi | P_lo]^T[128 m, 2N]
+//        A = the V chunk read transposed (MN-major descriptor, no copy).
+//        p is split into a 16-bit part and the 16-bit rounding of its
+//        remainder, so the pair carries p to about 2^-17 relative; one MMA
+//        with N' = 2N accumulates both halves into adjacent TMEM columns,
+//        which the epilogue adds.  B is block-diagonal by head: row m only
+//        has its own head's GP columns, so O^T[d, (h, c)] sums over head h's
 //        tokens only.
 //
-// S (NBS buffers) and O^T live in TMEM (N columns each): lane = row m for S
-// and lane = head dim d for O.  The CTA is warp-specialised:
+// S (NBS buffers of N columns) and O^T (2N columns) live in TMEM: lane = row m
+// for S and lane = head dim d for O.  The CTA is warp-specialised:
 //   warps 0-3 (softmax): thread t owns row m = t of each chunk and output dim
-//        d = t.  It loads its S row (tcgen05.ld), keeps its head's GP scores,
-//        forms p = exp2(s - m_ref) against a per-(head, q) reference max,
-//        writes p into P^T and arrives on the chunk's "P ready" barrier.
+//        d = t.  It loads its S row (tcgen05.ld), keeps its head's GP scores
+//        (masked where the token is past the range, its tile was not loaded,
+//        or, with causal queries, past the column's position), forms
+//        p = exp2(s - m_ref) against a per-column reference max, writes the
+//        hi/lo pair into P^T and arrives on the chunk's "P ready" barrier.
 //        m_ref only moves when some score exceeds it by more than 2^8 (a
 //        CTA-wide vote, one barrier per chunk); then the chunk max is
 //        reduced, O^T is rescaled in TMEM and the row sums with it.  Row sums
-//        stay per thread and are reduced once at the end.
+//        stay per thread and are reduced under the last PV; the epilogue reads
+//        O^T, normalises it and stores a bf16 row (or an fp32 partial and its
+//        log-sum-exp when the range is split).
 //   warp 4 (QK issuer) and warp 7 (PV issuer): one thread each issues its
 //        MMAs as soon as their inputs are ready (QK: K landed and the S buffer
 //        released by the softmax threads; PV: P^T written and V landed) and
 //        commits to the barriers that publish S, release the K stage, release
 //        the P buffer and the V stage.
 //   warps 5, 6 (TMA): stream K and V through separate rings (NK and NV
-//        stages of 32 KB), looking every tile up in the block table; tiles
-//        past the range or with a bad block id are not loaded and their rows
-//        are masked (and their V rows zeroed).
-// Softmax threads decide row validity from the block table themselves, so
-// they never depend on a stage after its MMA has released it.  Every mbarrier
-// wait is bounded and honours a CTA-wide abort flag; the softmax warps agree
-// on an abort at their per-chunk vote.
+//        stages of 32 KB).  Block ids arrive by cp.async into a small ring
+//        kTcLook chunks ahead of use, so an issue never waits on a lookup
+//        queued behind the KV stream.  Tiles past the range or with a bad
+//        block id are not loaded; the K producer publishes, per chunk, a
+//        tagged mask of the tiles it loaded, which the softmax threads read
+//        (so they never touch a stage after its MMA has released it), and an
+//        invalid row's V is zeroed.  With new K/V rows given, the producer
+//        whose range holds position L - 1 writes them into the pool through
+//        the slot mapping just before loading that tile.
+//   warps 8-11 (FP8 pools only): the producers land e4m3 codes in the upper
+//        half of a stage; these warps widen them to fp16 in place (K by 8, 9,
+//        V by 10, 11) and release the stage to the MMAs.  k_scale is folded
+//        into the softmax scale and v_scale into the epilogue.
+// With the range split, the CTAs of one (sequence, head group) merge their
+// partials in the same launch: once all P have arrived, they share the
+// merge tasks (pa_split_merge.cuh).  Every mbarrier wait and spin is bounded in polls and
+// in time and honours a CTA-wide abort flag; the softmax warps agree on an
+// abort at their per-chunk vote.
 #pragma once
 
 #include <cuda_fp16.h>
