@@ -190,10 +190,19 @@ int pa_combine(void *out, float *lse, const float *part_o, const float *part_lse
 /*
  * Split-KV ("flash decoding") decode attention: per-partition partials into
  * the caller's workspace, merged by log-sum-exp into out/lse, all on
- * `stream`.  When the split grid fits on the GPU at once the decode kernel
- * is launched cooperatively and merges its own partials (the CTAs of each
- * sequence and head group meet at a counter, then share the merge), so
- * there is one launch; otherwise pa_combine runs after it.
+ * `stream`.  The decode kernel merges its own partials in the same launch
+ * where it can:
+ *   - tensor-core kernel, P <= 16, and all B x (Hkv / heads per CTA) x
+ *     (query groups) clusters of P CTAs resident at once: the P partitions
+ *     of each sequence and head group form a thread-block cluster and merge
+ *     through distributed shared memory (the workspace's partial and counter
+ *     regions are not touched);
+ *   - otherwise, when the split grid fits on the GPU at once: a cooperative
+ *     launch whose CTAs of each sequence and head group meet at a counter in
+ *     the workspace, then share the merge;
+ *   - otherwise pa_combine runs after the decode kernel.
+ * PA_SPLIT_MERGE=grid in the environment (read on every call) skips the
+ * cluster merge.
  * num_splits == 0 picks P with pa_auto_num_splits; P == 1 runs pa_decode
  * directly and needs no workspace.  workspace: device, at least
  * pa_splitkv_workspace_bytes(B, Hq, D, P) bytes, 256-byte aligned, else

@@ -122,6 +122,17 @@ int pick_kernel(int G, int D, Kernel *k) {
     return PA_EUNSUPPORTED;
 }
 
+// How the partitions of an in-launch split merge meet: by default the
+// tensor-core kernel makes the P CTAs of a (sequence, head group) one
+// thread-block cluster when P <= 16 and all the launch's clusters can be
+// resident at once, and merges through distributed shared memory; otherwise
+// (and with PA_SPLIT_MERGE=grid in the environment, read on every call) the
+// grid is launched cooperatively and the partials meet in global memory.
+bool merge_forced_grid() {
+    const char *env = std::getenv("PA_SPLIT_MERGE");
+    return env && std::strcmp(env, "grid") == 0;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 
@@ -336,6 +347,8 @@ int run_decode(bool split, void *out, float *lse, float *part_o, float *part_lse
         return PA_EUNSUPPORTED;  // cascade passes: tensor cores only
     p.chunk = pa_partition_tokens(max_blocks, c.block_size, P);
     p.counters = counters;
+    p.cluster_merge = split && counters && k == Kernel::kTensorCore && P >= 2 &&
+                      P <= pa::kMaxClusterMerge && !merge_forced_grid();
     p.k_new = static_cast<const uint16_t *>(nt.k_new);
     p.v_new = static_cast<const uint16_t *>(nt.v_new);
     p.slot_mapping = nt.slot_mapping;

@@ -108,6 +108,8 @@ struct TcCfg {
     // the lo bf16 part of p; one MMA with N' = 2N accumulates both into
     // adjacent TMEM column ranges
     static constexpr int kPBufBytes = 2 * kPBytes;
+    // (a cluster merge stages the partial O^T, kN x 128 fp32, in the P^T buffers)
+    static_assert(kPBufBytes >= kN * 128 * 4, "cluster merge stage");
     // red[128 rows][GP], col[N], m_ref[N], alpha[N], rel[N] (output row of
     // column n relative to the CTA's first row, -1: padding), abort flag,
     // TMEM slot, merge ticket
@@ -312,6 +314,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
 
     if (nch == 0) {  // empty range: zero output, lse = -inf
         cp_async_wait<0>();
+        if (p.cluster_merge) {  // a stage with no key seen (its O^T is never read)
+            if (tid < N) {
+                rel_s[tid] = tid % GP < Gq ? static_cast<int>(col_row(tid / GP, tid % GP) - row0) : -1;
+                col[tid] = -INFINITY;
+            }
+            merge_cluster<D, kThreads>(p, reinterpret_cast<const float *>(ps), col, rel_s, N, row0, tid);
+            return;
+        }
         for (int i = tid; i < HC * Gq * D; i += kThreads) {
             const int j = i / D, d = i % D;
             const int64_t r = col_row(j / Gq, j % Gq);
@@ -775,8 +785,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             tc5::fence_after_sync();
             // O^T row d = tid, 16 columns at a time, normalised and stored; column
             // n = (head hh, query q) goes to the CTA's output row hh * G + q
+            // (cluster merge: column n's row goes to the stage, ostage[n][d])
+            const bool staged = p.cluster_merge != 0;
             const int64_t stride = p.split ? static_cast<int64_t>(p.part_stride) * D : D;
             float *of = p.split ? p.part_o + (row0 * p.part_stride + p.part_offset + part) * D + tid : nullptr;
+            float *ostage = reinterpret_cast<float *>(ps) + tid;
             __nv_bfloat16 *oh = p.split ? nullptr : static_cast<__nv_bfloat16 *>(p.out) + row0 * D + tid;
 #pragma unroll 1
             for (int k = 0; k < N / 16; ++k) {
@@ -788,7 +801,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                     const int n = 16 * k + i, rel = rel_s[n];
                     if (rel < 0) continue;
                     const float o = (ov[i] + lo[i]) * alpha_s[n];
-                    if (p.split) of[rel * stride] = o;
+                    if (staged) ostage[n * D] = o;
+                    else if (p.split) of[rel * stride] = o;
                     else oh[rel * stride] = __float2bfloat16_rn(o);
                 }
             }
@@ -796,15 +810,20 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                 const int n = tid;
                 const float lse = (m_ref[n] + log2f(col[n])) * 0.69314718055994531f;
                 const int64_t r = row0 + rel_s[n];
-                if (p.split) p.part_lse[r * p.part_stride + p.part_offset + part] = lse;
+                if (staged) col[n] = lse;
+                else if (p.split) p.part_lse[r * p.part_stride + p.part_offset + part] = lse;
                 else if (p.lse) p.lse[r] = lse;
             }
+        } else if (p.cluster_merge && tid < N) {
+            col[tid] = -INFINITY;  // aborted: this partition drops out of the merge
         }
     }
     tc5::fence_before_sync();
     __syncthreads();
     if (warp == 0) tc5::tmem_free(tmem, C::kTmemCols);
-    if (p.split)  // all eight warps share the merge
+    if (p.cluster_merge)  // all warps of all the cluster's CTAs share the merge
+        merge_cluster<D, kThreads>(p, reinterpret_cast<const float *>(ps), col, rel_s, N, row0, tid);
+    else if (p.split)  // all eight warps share the merge
         merge_split_group<D, kThreads / 32>(p, b * gridDim.y + blockIdx.y, part, row0, HC * Gq,
                                               HC * G, Hq, ticket, tid, [] { __syncthreads(); });
 }
@@ -825,9 +844,23 @@ cudaError_t launch_tc_instance(const CUtensorMap &kmap, const CUtensorMap &vmap,
         smem_attr_done.fetch_or(bit, std::memory_order_release);
     }
     const int qgroups = (p.q_len + p.q_per_cta - 1) / p.q_per_cta;
-    return launch_maybe_cooperative(kern, dim3(p.num_splits, p.head_groups * qgroups, B),
-                                    F8 ? kTcThreadsF8 : kTcThreads,
-                                    C::kSmemBytes, stream, p.counters != nullptr, kmap, vmap, p, G);
+    const dim3 grid(p.num_splits, p.head_groups * qgroups, B);
+    const int threads = F8 ? kTcThreadsF8 : kTcThreads;
+    if (p.cluster_merge) {
+        // One cluster per (sequence, head group, query group), all resident at
+        // once (a second wave of clusters would cost more than the merge saves).
+        static std::atomic<int> cap[64 * 32];
+        const int64_t clusters = static_cast<int64_t>(grid.y) * grid.z;
+        if (p.num_splits >= 2 && p.num_splits <= kMaxClusterMerge &&
+            clusters <= max_active_clusters(kern, p.num_splits, threads, C::kSmemBytes, dev, cap))
+            return launch_clustered(kern, grid, p.num_splits, threads, C::kSmemBytes, stream, kmap, vmap, p, G);
+        DecodeParams q = p;  // merge through global memory instead
+        q.cluster_merge = 0;
+        return launch_maybe_cooperative(kern, grid, threads, C::kSmemBytes, stream, q.counters != nullptr,
+                                        kmap, vmap, q, G);
+    }
+    return launch_maybe_cooperative(kern, grid, threads, C::kSmemBytes, stream, p.counters != nullptr,
+                                    kmap, vmap, p, G);
 }
 
 }  // namespace pa

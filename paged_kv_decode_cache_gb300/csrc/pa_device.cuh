@@ -3,6 +3,8 @@
 // shared-memory addressing of the 128-byte-swizzled K/V tiles.
 #pragma once
 
+#include <atomic>
+
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -184,6 +186,30 @@ __device__ __forceinline__ bool named_sync_or(int id, int nthreads, bool v) {
 
 __device__ __forceinline__ float ldcg(const float *p) { return __ldcg(p); }
 
+// Thread-block clusters.  cluster_sync(): every thread of every CTA of the
+// cluster arrives (release: its shared-memory writes become visible to the
+// cluster) and waits for all the others (acquire).  Not the .aligned form, so
+// the threads of a warp need not be converged.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// The shared::cluster address of the same location in CTA `rank`'s shared memory.
+__device__ __forceinline__ uint32_t map_shared_rank(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ float ld_shared_cluster(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 // Order this thread's generic global writes before later async-proxy (TMA)
 // reads of the same memory (by any thread that synchronises with it after).
 __device__ __forceinline__ void fence_proxy_async_global() {
@@ -228,6 +254,68 @@ inline cudaError_t launch_maybe_cooperative(Kernel kern, dim3 grid, int threads,
     }
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
     return e == cudaSuccess ? cudaGetLastError() : e;
+}
+
+// Launch `kern` with thread-block clusters of `cluster_x` CTAs along x (x a
+// multiple of it).  Sizes above 8 are allowed where the device schedules them;
+// returns cudaErrorInvalidConfiguration when no such cluster fits an SM group
+// at all (the caller then launches without clusters).
+template <typename Kernel, typename... Args>
+inline cudaError_t launch_clustered(Kernel kern, dim3 grid, int cluster_x, int threads, int smem,
+                                    cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(cluster_x);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
+    return e == cudaSuccess ? cudaGetLastError() : e;
+}
+
+// How many clusters of `cluster_x` CTAs of `kern` (threads, smem per CTA) can
+// be resident on device `dev` at once (0: none can be scheduled).  Asked once
+// per (kernel, device, size) for sizes 1..31 and devices 0..63; the answers
+// are kept in `cache` (count + 1 at [dev * 32 + size], 0 = not asked yet),
+// which the caller owns (one per kernel).  Sizes above 8 are opted into first.
+template <typename Kernel>
+inline int max_active_clusters(Kernel kern, int cluster_x, int threads, int smem, int dev,
+                               std::atomic<int> *cache) {
+    if (cluster_x < 1 || cluster_x > 31 || dev < 0 || dev > 63) return 0;
+    std::atomic<int> &slot = cache[dev * 32 + cluster_x];
+    const int known = slot.load(std::memory_order_acquire);
+    if (known > 0) return known - 1;
+    int n = 0;
+    bool ok = true;
+    if (cluster_x > 8 &&
+        cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+        ok = false;
+    if (ok) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(cluster_x), 1, 1);
+        cfg.blockDim = dim3(threads, 1, 1);
+        cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(cluster_x);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) ok = false;
+    }
+    if (!ok) {
+        cudaGetLastError();  // clear a refusal, so it does not surface later
+        n = 0;
+    }
+    slot.store(n + 1, std::memory_order_release);
+    return n;
 }
 
 }  // namespace pa

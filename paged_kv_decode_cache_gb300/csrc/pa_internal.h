@@ -9,6 +9,9 @@
 
 namespace pa {
 
+// Most partitions a split merge takes through one thread-block cluster.
+constexpr int kMaxClusterMerge = 16;
+
 // Everything a decode CTA needs besides the two tensor maps.
 struct DecodeParams {
     void *out;              // bf16 [B, Hq, D]            (unsplit)
@@ -32,6 +35,11 @@ struct DecodeParams {
     // to finish merges the group's partials into out/lse.  counters has one
     // int per (sequence, head group), zero on entry and left zero on exit.
     int32_t *counters;      // null: partials only
+    // Cluster merge (split only, tensor-core kernel): the P CTAs of a
+    // (sequence, head group) are one thread-block cluster and merge their
+    // partials through distributed shared memory; counters, part_o and
+    // part_lse are then unused.
+    int32_t cluster_merge;
     // Fused cache write (pa_decode_step): sequence b's new token, the one at
     // position L_b - 1, is written into the pools by the CTA that reads that
     // position, right before its TMA load of that tile.  null: no write.

@@ -201,4 +201,56 @@ __device__ void merge_split_group(const DecodeParams &p, int group, int part, in
     }
 }
 
+// Cluster merge: the P CTAs of one (sequence, head group) are a thread-block
+// cluster.  Each has left, in its own shared memory, its normalised partial
+// output ostage[n][D] (fp32) and its log-sum-exp lse_s[n] (-inf: no key seen,
+// then ostage is not read) for the n < ncols MMA columns; rel[n] is column
+// n's output row relative to row0 (-1: padding), the same in every CTA of the
+// cluster.  After a cluster barrier, CTA `rank` merges output elements
+// e = (n, d) = rank * kThreads + t, then every P * kThreads-th one, reading
+// each peer's stage through distributed shared memory (all 2P loads of an
+// element are issued together), and writes the bf16 output (and the row's
+// log-sum-exp).  A second barrier keeps every stage alive until all peers
+// have read it.  Called by all kThreads threads of every CTA of the cluster.
+template <int D, int kThreads>
+__device__ void merge_cluster(const DecodeParams &p, const float *ostage, const float *lse_s,
+                              const int *rel, int ncols, int64_t row0, int t) {
+    cluster_sync();
+    const int P = p.num_splits;
+    const uint32_t rank = cluster_ctarank();
+    const uint32_t o_loc = smem_u32(ostage), l_loc = smem_u32(lse_s);
+    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
+    for (int e = static_cast<int>(rank) * kThreads + t; e < ncols * D; e += P * kThreads) {
+        const int n = e / D, d = e % D;
+        const int r = rel[n];
+        if (r < 0) continue;
+        float lv[kMaxClusterMerge], ov[kMaxClusterMerge];
+#pragma unroll
+        for (int k = 0; k < kMaxClusterMerge; ++k) {
+            lv[k] = -INFINITY;
+            ov[k] = 0.f;
+            if (k < P) {
+                lv[k] = ld_shared_cluster(map_shared_rank(l_loc + 4u * n, k));
+                ov[k] = ld_shared_cluster(map_shared_rank(o_loc + 4u * e, k));
+            }
+        }
+        float M = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < kMaxClusterMerge; ++k) M = fmaxf(M, lv[k]);
+        float total = -INFINITY, acc = 0.f;
+        if (M != -INFINITY) {
+            float z = 0.f;
+#pragma unroll
+            for (int k = 0; k < kMaxClusterMerge; ++k) z += lv[k] == -INFINITY ? 0.f : expf(lv[k] - M);
+            total = M + logf(z);
+#pragma unroll
+            for (int k = 0; k < kMaxClusterMerge; ++k)
+                if (lv[k] != -INFINITY) acc = fmaf(expf(lv[k] - total), ov[k], acc);
+        }
+        out[(row0 + r) * D + d] = __float2bfloat16_rn(acc);
+        if (d == 0 && p.lse) p.lse[row0 + r] = total;
+    }
+    cluster_sync();
+}
+
 }  // namespace pa

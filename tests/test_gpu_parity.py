@@ -39,6 +39,18 @@ def use_kernel(monkeypatch):
     monkeypatch.delenv("PA_DECODE_KERNEL", raising=False)
 
 
+@pytest.fixture
+def merge_path(monkeypatch):
+    """'cluster' (the default where P <= 16) or 'grid' (PA_SPLIT_MERGE=grid)."""
+    def _set(path):
+        if path == "grid":
+            monkeypatch.setenv("PA_SPLIT_MERGE", "grid")
+        else:
+            monkeypatch.delenv("PA_SPLIT_MERGE", raising=False)
+    yield _set
+    monkeypatch.delenv("PA_SPLIT_MERGE", raising=False)
+
+
 # ---------------------------------------------------------------- cache write
 def test_cache_write_bit_exact_with_sentinels():
     rng = np.random.default_rng(0)
@@ -624,25 +636,32 @@ def test_cascade_full_size_qwen3():
 
 
 # ------------------------------------------------ a wait that nothing completes
+def _preset_counters(w, P, value):
+    """Split-KV workspace whose merge counters (its last region) all hold `value`."""
+    ws = torch.zeros(pa.pa_splitkv_workspace_bytes(w.B, w.Hq, w.D, P), dtype=torch.uint8,
+                     device="cuda")
+    rows = w.B * w.Hq * P
+    rnd = lambda x: (x + 255) // 256 * 256                         # noqa: E731
+    counters = rnd(rows * w.D * 4) + rnd(rows * 4)
+    ws[counters:].view(torch.int32).fill_(value)
+    return ws
+
+
 @pytest.mark.parametrize("kernel", ["cuda_core", "tensor_core"])
-def test_merge_wait_times_out_and_the_context_survives(kernel, use_kernel):
-    """The split merge waits for all P partitions to arrive; with the
+def test_merge_wait_times_out_and_the_context_survives(kernel, use_kernel, merge_path):
+    """The grid-wide split merge waits for all P partitions to arrive; with the
     workspace's arrival counters preset far below zero that count is never
     reached.  Every CTA gives up after about a second, sets PA_STATUS_TIMEOUT
     and returns (the wait comes after all of the CTA's copies and MMAs have
     completed); the host reads the status and the next call is correct."""
     import time
     use_kernel(kernel)
+    merge_path("grid")
     w = _small(28 if kernel == "tensor_core" else 8, 4, 128, 16, (1000,), seed=3)
     dev = Dev(w)
     dev.write()
     P = 4
-    ws = torch.zeros(pa.pa_splitkv_workspace_bytes(w.B, w.Hq, w.D, P), dtype=torch.uint8,
-                     device="cuda")
-    rows = w.B * w.Hq * P
-    rnd = lambda x: (x + 255) // 256 * 256                         # noqa: E731
-    counters = rnd(rows * w.D * 4) + rnd(rows * 4)                 # the workspace's last region
-    ws[counters:].view(torch.int32).fill_(-(1 << 30))
+    ws = _preset_counters(w, P, -(1 << 30))
     out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
     t0 = time.time()
     pa.pa_decode_splitkv(out, None, dev.q, dev.k_cache, dev.v_cache, dev.block_tables,
@@ -656,4 +675,102 @@ def test_merge_wait_times_out_and_the_context_survives(kernel, use_kernel):
     ref, ref_lse = oracle.decode(w.q, kc, vc, w.block_tables, w.seq_lens, w.scale)
     so, sl, _ = dev.splitkv(P)
     assert_close(bf16_dev_to_f64(so), ref, f"after timeout {kernel}")
+    assert dev.status_value() == 0
+
+
+# ------------------------------------------- split merge: cluster and grid paths
+MERGE_CASES = [
+    # (Hq, Hkv, bs, lens)
+    (28, 4, 16, (1000, 300, 1, 17)),        # G = 7, HC = 4; short sequences: empty partitions
+    (16, 8, 16, (700, 129)),                # G = 2, HC = 8
+    (48, 2, 16, (900, 65)),                 # G = 24: one head per CTA, 32 columns
+    (16, 4, 256, (2000, 513, 2)),           # pages
+]
+
+
+@pytest.mark.parametrize("path", ["cluster", "grid"])
+@pytest.mark.parametrize("case", MERGE_CASES, ids=lambda c: f"Hq{c[0]}-Hkv{c[1]}-bs{c[2]}")
+def test_split_merge_paths(case, path, merge_path):
+    """pa_decode_splitkv and pa_decode_step at P = 2 .. 17 through either merge
+    (P <= 16: one cluster per (sequence, head group) by default; 17: always the
+    grid-wide merge), element by element against the oracle."""
+    merge_path(path)
+    Hq, Hkv, bs, lens = case
+    w = _small(Hq, Hkv, 128, bs, lens, seed=sum(lens), poison_unused=True)
+    kc, vc = oracle_after_write(w)
+    ref, ref_lse = oracle.decode(w.q, kc, vc, w.block_tables, w.seq_lens, w.scale)
+    dev = Dev(w)
+    dev.write()
+    for P in (2, 3, 8, 9, 16, 17):
+        so, sl, _ = dev.splitkv(P)
+        assert_close(bf16_dev_to_f64(so), ref, f"splitkv P={P} {path}")
+        assert_lse_close(sl.cpu().double().numpy(), ref_lse, f"splitkv P={P} {path}")
+    dev2 = Dev(w)
+    for P in (4, 16):
+        so, sl, _ = dev2.step(P)
+        assert_close(bf16_dev_to_f64(so), ref, f"step P={P} {path}")
+    assert dev.status_value() == 0 and dev2.status_value() == 0
+
+
+@pytest.mark.parametrize("P", [2, 4, 9, 16])
+def test_cluster_merge_leaves_the_counters_alone(P, merge_path):
+    """With P <= 16 the partitions merge inside their cluster: the workspace's
+    grid-merge counters are neither read nor written.  Preset far below zero
+    (which makes the grid-wide merge time out), they do not delay or disturb
+    the call, which shows the cluster path ran."""
+    import time
+    merge_path("cluster")
+    w = _small(28, 4, 128, 16, (1000, 37), seed=P)
+    dev = Dev(w)
+    dev.write()
+    dev.splitkv(P)                      # loads the kernel and sizes the cluster once
+    ws = _preset_counters(w, P, -(1 << 30))
+    before = ws.clone()
+    out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
+    torch.cuda.synchronize()
+    t0 = time.time()
+    pa.pa_decode_splitkv(out, None, dev.q, dev.k_cache, dev.v_cache, dev.block_tables,
+                         dev.seq_lens, w.scale, num_splits=P, workspace=ws, status=dev.status)
+    torch.cuda.synchronize()
+    assert time.time() - t0 < 0.5
+    assert dev.status_value() == 0
+    rows = w.B * w.Hq * P
+    tail = (rows * w.D * 4 + 255) // 256 * 256 + (rows * 4 + 255) // 256 * 256
+    assert torch.equal(ws[tail:], before[tail:])
+    kc, vc = oracle_after_write(w)
+    ref, _ = oracle.decode(w.q, kc, vc, w.block_tables, w.seq_lens, w.scale)
+    assert_close(bf16_dev_to_f64(out), ref, f"cluster P={P}")
+
+
+@pytest.mark.parametrize("path", ["cluster", "grid"])
+def test_split_merge_paths_mq_and_fp8(path, merge_path):
+    """Multi-query (2 query groups per head group) and FP8 pools through either merge."""
+    merge_path(path)
+    w = W.make_workload("mq", B=3, Hq=28, Hkv=4, D=128, block_size=16, seq_lens=[900, 40, 3],
+                        num_blocks=70, seed=12, poison_unused=True, q_len=4)
+    kc, vc = oracle_after_write(w)
+    ref, ref_lse = oracle.decode_mq(w.q, kc, vc, w.block_tables, w.seq_lens, w.scale)
+    dev = Dev(w)
+    dev.write()
+    for P in (3, 16):
+        out, lse, _ = dev.mq(P)
+        assert_close(bf16_dev_to_f64(out), ref, f"mq P={P} {path}")
+        assert_lse_close(lse.cpu().double().numpy(), ref_lse, f"mq P={P} {path}")
+    w = W.with_fp8_pools(W.make_workload("f8", B=2, Hq=28, Hkv=4, D=128, block_size=16,
+                                         seq_lens=[1100, 9], num_blocks=80, seed=13,
+                                         poison_unused=True, write_new=False))
+    ref, ref_lse = oracle.decode_fp8(w.q, w.k_cache8, w.v_cache8, w.block_tables, w.seq_lens,
+                                     w.scale, w.k_scale, w.v_scale)
+    dev = Dev(w)
+    k8, v8 = _fp8_dev(w)
+    for P in (5, 16):
+        ws = torch.zeros(pa.pa_splitkv_workspace_bytes(w.B, w.Hq, w.D, P), dtype=torch.uint8,
+                         device="cuda")
+        out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device="cuda")
+        pa.pa_decode_splitkv_fp8(out, lse, dev.q, k8, v8, w.k_scale, w.v_scale, dev.block_tables,
+                                 dev.seq_lens, w.scale, num_splits=P, workspace=ws,
+                                 status=dev.status)
+        assert_close(bf16_dev_to_f64(out), ref, f"fp8 P={P} {path}")
+        assert_lse_close(lse.cpu().double().numpy(), ref_lse, f"fp8 P={P} {path}")
     assert dev.status_value() == 0
