@@ -783,36 +783,57 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         okf = named_sync_or(1, 128, !okf) ? false : true;
         if (okf) {
             tc5::fence_after_sync();
-            // O^T row d = tid, 16 columns at a time, normalised and stored; column
-            // n = (head hh, query q) goes to the CTA's output row hh * G + q
-            // (cluster merge: column n's row goes to the stage, ostage[n][d])
-            const bool staged = p.cluster_merge != 0;
-            const int64_t stride = p.split ? static_cast<int64_t>(p.part_stride) * D : D;
-            float *of = p.split ? p.part_o + (row0 * p.part_stride + p.part_offset + part) * D + tid : nullptr;
+            // O^T row d = tid, 16 columns at a time, normalised and staged in the
+            // idle P^T buffers as rows ostage[n][d] (fp32 partials when split,
+            // else bf16), column n = (head hh, query q) being output row
+            // row0 + rel_s[n].  The cluster merge reads the stage in place;
+            // otherwise each column's row is copied out by one bulk copy.
+            const bool split = p.split != 0;
             float *ostage = reinterpret_cast<float *>(ps) + tid;
-            __nv_bfloat16 *oh = p.split ? nullptr : static_cast<__nv_bfloat16 *>(p.out) + row0 * D + tid;
+            __nv_bfloat16 *ostage16 = reinterpret_cast<__nv_bfloat16 *>(ps) + tid;
 #pragma unroll 1
             for (int k = 0; k < N / 16; ++k) {
-                float ov[16], lo[16];
+                float ov[16], lo[16], al[16];
+                int rel[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {  // the columns' rows and scales, ahead of the stores
+                    rel[i] = rel_s[16 * k + i];
+                    al[i] = alpha_s[16 * k + i];
+                }
                 tc5::ld_32x32b_x16(tc5::taddr(tmem, 32 * warp, C::kColO + 16 * k), ov);
                 tc5::ld_32x32b_x16(tc5::taddr(tmem, 32 * warp, C::kColO + N + 16 * k), lo);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const int n = 16 * k + i, rel = rel_s[n];
-                    if (rel < 0) continue;
-                    const float o = (ov[i] + lo[i]) * alpha_s[n];
-                    if (staged) ostage[n * D] = o;
-                    else if (p.split) of[rel * stride] = o;
-                    else oh[rel * stride] = __float2bfloat16_rn(o);
+                    if (rel[i] < 0) continue;
+                    const float o = (ov[i] + lo[i]) * al[i];
+                    if (split) ostage[(16 * k + i) * D] = o;
+                    else ostage16[(16 * k + i) * D] = __float2bfloat16_rn(o);
                 }
+            }
+            const bool copy_out = !p.cluster_merge;
+            if (copy_out) {  // the stage is complete before any row of it is copied
+                fence_proxy_async_smem();
+                named_sync(1, 128);
             }
             if (tid < N && rel_s[tid] >= 0) {
                 const int n = tid;
                 const float lse = (m_ref[n] + log2f(col[n])) * 0.69314718055994531f;
                 const int64_t r = row0 + rel_s[n];
-                if (staged) col[n] = lse;
-                else if (p.split) p.part_lse[r * p.part_stride + p.part_offset + part] = lse;
-                else if (p.lse) p.lse[r] = lse;
+                if (p.cluster_merge) {
+                    col[n] = lse;
+                } else if (split) {
+                    const int64_t slot = r * p.part_stride + p.part_offset + part;
+                    bulk_store_s2g(p.part_o + slot * D, ostage - tid + n * D, D * 4);
+                    bulk_commit();
+                    p.part_lse[slot] = lse;
+                    bulk_wait_all();              // the row is written ...
+                    fence_proxy_async_global();   // ... and ordered before the merge's release
+                } else {
+                    bulk_store_s2g(static_cast<__nv_bfloat16 *>(p.out) + r * D, ostage16 - tid + n * D, D * 2);
+                    bulk_commit();
+                    if (p.lse) p.lse[r] = lse;
+                    bulk_wait_all_read();  // the stage is read before the CTA moves on
+                }
             }
         } else if (p.cluster_merge && tid < N) {
             col[tid] = -INFINITY;  // aborted: this partition drops out of the merge

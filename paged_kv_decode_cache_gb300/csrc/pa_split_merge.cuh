@@ -4,8 +4,8 @@
 // The split kernel is then launched cooperatively, so every CTA of the grid
 // is resident at once and CTAs may wait for each other.  Protocol, per group
 // of P CTAs (the P partitions of one sequence and head group):
-//   1. each CTA writes its partials, fences them to device scope and
-//      increments the group's arrival counter;
+//   1. each CTA writes its partials; after a CTA barrier one thread
+//      increments the group's arrival counter with release semantics;
 //   2. it waits (bounded) until the counter reads P: every partial exists;
 //   3. the group's CTAs split the merge between them: merge task k = (output
 //      row, dim slice) goes to warp k of the group's P x nwarps warps; a task
@@ -24,6 +24,12 @@
 #include "pa_internal.h"
 
 namespace pa {
+
+// Release pattern: a gpu-scope fence, then a relaxed atomic add.
+__device__ __forceinline__ void red_add_release_gpu(int *p, int v) {
+    asm volatile("fence.acq_rel.gpu;\n\tred.relaxed.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v)
+                 : "memory");
+}
 
 __device__ __forceinline__ int ld_acquire_gpu(const int *p) {
     int v;
@@ -164,10 +170,11 @@ __device__ void merge_split_group(const DecodeParams &p, int group, int part, in
     if (!p.counters) return;
     int *arrive = p.counters + 2 * group, *depart = arrive + 1;
     const int P = p.num_splits;
-    __threadfence();
+    // Release: the barrier orders every thread's partial stores before thread
+    // 0's gpu-scope release fence, which makes them visible before its arrival.
     sync();
     if (t == 0) {
-        atomicAdd(arrive, 1);
+        red_add_release_gpu(arrive, 1);
         bool ok = false;
         const uint64_t t0 = globaltimer_ns();
         for (uint32_t i = 0; i < kWaitLimit; ++i) {
@@ -180,9 +187,10 @@ __device__ void merge_split_group(const DecodeParams &p, int group, int part, in
         if (!ok) set_status(p.status, PA_STATUS_TIMEOUT);
         *flag = ok;
     }
+    // Acquire: thread 0 saw all P arrivals with an acquire load; the barrier
+    // orders every thread's partial loads after it.
     sync();
     if (*flag) {
-        __threadfence();
         const int warp = t >> 5, lane = t & 31;
         if (P <= 32) {  // lanes over dims: one round trip per 32-dim slice
             const int tasks = nrows * (D / 32);
