@@ -6,15 +6,15 @@
 // of P CTAs (the P partitions of one sequence and head group):
 //   1. each CTA writes its partials; after a CTA barrier one thread
 //      increments the group's arrival counter with release semantics;
-//   2. it waits (bounded) until the counter reads P: every partial exists;
+//   2. the CTA whose arrival makes P resets the counter to zero at once; the
+//      others wait (bounded) until it reads P or drops to at most their own
+//      arrival value (the reset): every partial exists;
 //   3. the group's CTAs split the merge between them: merge task k = (output
 //      row, dim slice) goes to warp k of the group's P x nwarps warps; a task
 //      computes the row's log-sum-exp over the P partial LSEs and sums the
 //      weighted partial outputs of its slice (partials are read with
 //      L1-bypassing loads).  Up to 32 partitions a lane owns a dim of a 32-dim
 //      slice; beyond, a lane owns partitions of an 8-dim slice;
-//   4. each CTA increments the group's departure counter; the last one puts
-//      both counters back to zero for the next call.
 // A wait that runs out sets PA_STATUS_TIMEOUT and the CTA skips the merge.
 #pragma once
 
@@ -25,10 +25,19 @@
 
 namespace pa {
 
-// Release pattern: a gpu-scope fence, then a relaxed atomic add.
+// Release pattern: a gpu-scope fence, then a relaxed atomic add (the fence
+// also acquires what this thread's earlier atomics read).
 __device__ __forceinline__ void red_add_release_gpu(int *p, int v) {
     asm volatile("fence.acq_rel.gpu;\n\tred.relaxed.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v)
                  : "memory");
+}
+__device__ __forceinline__ int atom_add_release_gpu(int *p, int v) {
+    int old;
+    asm volatile("fence.acq_rel.gpu;\n\tatom.relaxed.gpu.global.add.s32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "l"(p), "r"(v)
+                 : "memory");
+    return old;
 }
 
 __device__ __forceinline__ int ld_acquire_gpu(const int *p) {
@@ -168,27 +177,38 @@ __device__ void merge_split_group(const DecodeParams &p, int group, int part, in
                                   Sync sync) {
     auto row_of = [&](int j) -> int64_t { return row_first + (j / per_block) * stride + j % per_block; };
     if (!p.counters) return;
-    int *arrive = p.counters + 2 * group, *depart = arrive + 1;
+    int *arrive = p.counters + 2 * group;  // (the pair's second int is not used)
     const int P = p.num_splits;
     // Release: the barrier orders every thread's partial stores before thread
     // 0's gpu-scope release fence, which makes them visible before its arrival.
     sync();
     if (t == 0) {
-        red_add_release_gpu(arrive, 1);
+        const int old = atom_add_release_gpu(arrive, 1);
         bool ok = false;
-        const uint64_t t0 = globaltimer_ns();
-        for (uint32_t i = 0; i < kWaitLimit; ++i) {
-            if (ld_acquire_gpu(arrive) >= P) {
-                ok = true;
-                break;
+        if (old == P - 1) {
+            // Last to arrive: acquire everyone's partials, then put the counter
+            // back to zero (a release, so a waiter that reads zero acquires too).
+            red_add_release_gpu(arrive, -P);
+            ok = true;
+        } else {
+            // Done once the counter reads P, or reads at most this CTA's own
+            // arrival value (it was reset, which happens only after the P-th).
+            const uint64_t t0 = globaltimer_ns();
+            for (uint32_t i = 0; i < kWaitLimit; ++i) {
+                const int v = ld_acquire_gpu(arrive);
+                if (v >= P || v <= old) {
+                    ok = true;
+                    break;
+                }
+                if (wait_expired(i, t0)) break;
             }
-            if (wait_expired(i, t0)) break;
         }
         if (!ok) set_status(p.status, PA_STATUS_TIMEOUT);
         *flag = ok;
     }
-    // Acquire: thread 0 saw all P arrivals with an acquire load; the barrier
-    // orders every thread's partial loads after it.
+    // Acquire: thread 0 saw all P arrivals with an acquire load (or as the last
+    // arriver, after its fence); the barrier orders every thread's partial
+    // loads after it.
     sync();
     if (*flag) {
         const int warp = t >> 5, lane = t & 31;
@@ -201,11 +221,6 @@ __device__ void merge_split_group(const DecodeParams &p, int group, int part, in
             for (int k = part * kWarps + warp; k < tasks; k += P * kWarps)
                 merge_slice_wide<D>(p, row_of(k / (D / 8)), k % (D / 8), lane);
         }
-    }
-    sync();
-    if (t == 0 && atomicAdd(depart, 1) == P - 1) {
-        *arrive = 0;
-        *depart = 0;
     }
 }
 
