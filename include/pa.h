@@ -54,6 +54,13 @@
  *     than the table allows).  The offending element is skipped, never
  *     dereferenced.  The caller zeroes it and reads it back when convenient.
  *   - A call writes every element of its outputs.
+ *   - Stream order holds for every call.  The head_dim-128 (tensor-core)
+ *     decode kernel is launched with programmatic stream serialization: it
+ *     may become resident while the previous kernel in the stream finishes,
+ *     but waits for that kernel's completion (griddepcontrol.wait) before it
+ *     reads or writes any global memory, and lets the next such launch queue
+ *     once all of its CTAs run.  PA_PDL=0 in the environment (read on every
+ *     call) launches it plainly.
  */
 #ifndef PA_H_
 #define PA_H_

@@ -133,6 +133,15 @@ bool merge_forced_grid() {
     return env && std::strcmp(env, "grid") == 0;
 }
 
+// The tensor-core kernel is launched with programmatic stream serialization
+// (programmatic dependent launch) unless PA_PDL=0 is in the environment (read
+// on every call): it may then become resident while the previous kernel in
+// the stream finishes, and waits for it before touching global memory.
+bool pdl_enabled() {
+    const char *env = std::getenv("PA_PDL");
+    return !(env && std::strcmp(env, "0") == 0);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 
@@ -349,6 +358,7 @@ int run_decode(bool split, void *out, float *lse, float *part_o, float *part_lse
     p.counters = counters;
     p.cluster_merge = split && counters && k == Kernel::kTensorCore && P >= 2 &&
                       P <= pa::kMaxClusterMerge && !merge_forced_grid();
+    p.pdl = k == Kernel::kTensorCore && pdl_enabled();
     p.k_new = static_cast<const uint16_t *>(nt.k_new);
     p.v_new = static_cast<const uint16_t *>(nt.v_new);
     p.slot_mapping = nt.slot_mapping;

@@ -389,7 +389,7 @@ cudaError_t launch_cc_instance(const CUtensorMap &kmap, const CUtensorMap &vmap,
     cudaError_t e = ensure_smem_attr(smem_attr_done, kern, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     return launch_maybe_cooperative(kern, dim3(p.num_splits, p.num_kv_heads, B), NW * 32,
-                                    C::kSmemBytes, stream, p.counters != nullptr, kmap, vmap, p);
+                                    C::kSmemBytes, stream, p.counters != nullptr, false, kmap, vmap, p);
 }
 
 }  // namespace pa

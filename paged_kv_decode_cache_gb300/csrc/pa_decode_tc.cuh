@@ -232,6 +232,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     volatile uint64_t *vmask_ring = reinterpret_cast<volatile uint64_t *>(smem + C::kVMaskOff);
     int *look_ring = reinterpret_cast<int *>(smem + C::kLookOff);  // [2][kTcLook + 1][32]
 
+    // Launched after another kernel with programmatic stream serialization,
+    // this CTA may be running before that kernel has finished: no global
+    // memory is read or written above this wait.  The next such launch may be
+    // scheduled once every CTA of this grid is past it (it then waits in turn).
+    griddep_wait();
+    griddep_launch_dependents();
+
     const int part = blockIdx.x, b = blockIdx.z;
     const int g0 = (blockIdx.y % p.head_groups) * HC;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -874,14 +881,15 @@ cudaError_t launch_tc_instance(const CUtensorMap &kmap, const CUtensorMap &vmap,
         const int64_t clusters = static_cast<int64_t>(grid.y) * grid.z;
         if (p.num_splits >= 2 && p.num_splits <= kMaxClusterMerge &&
             clusters <= max_active_clusters(kern, p.num_splits, threads, C::kSmemBytes, dev, cap))
-            return launch_clustered(kern, grid, p.num_splits, threads, C::kSmemBytes, stream, kmap, vmap, p, G);
+            return launch_clustered(kern, grid, p.num_splits, threads, C::kSmemBytes, stream, p.pdl != 0,
+                                    kmap, vmap, p, G);
         DecodeParams q = p;  // merge through global memory instead
         q.cluster_merge = 0;
         return launch_maybe_cooperative(kern, grid, threads, C::kSmemBytes, stream, q.counters != nullptr,
-                                        kmap, vmap, q, G);
+                                        q.pdl != 0, kmap, vmap, q, G);
     }
     return launch_maybe_cooperative(kern, grid, threads, C::kSmemBytes, stream, p.counters != nullptr,
-                                    kmap, vmap, p, G);
+                                    p.pdl != 0, kmap, vmap, p, G);
 }
 
 }  // namespace pa

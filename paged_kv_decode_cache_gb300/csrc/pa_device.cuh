@@ -246,22 +246,42 @@ __device__ __forceinline__ void set_status(int32_t *status, int bits) {
     if (status) atomicOr(status, bits);
 }
 
+// Programmatic dependent launch.  griddep_wait(): returns once the grids this
+// one depends on (the previous kernel in the stream, when this one was
+// launched with programmatic stream serialization) have completed and their
+// memory is visible; at once otherwise.  griddep_launch_dependents(): the next
+// such launch may be scheduled once every CTA of this grid has executed it.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Launch `kern` normally, or cooperatively (all CTAs resident at once, as CTAs
 // that wait for each other need) when `cooperative`; a cooperative grid larger
-// than what fits at once fails with cudaErrorCooperativeLaunchTooLarge.
+// than what fits at once fails with cudaErrorCooperativeLaunchTooLarge.  `pdl`:
+// with programmatic stream serialization, for kernels that call griddep_wait()
+// before any global memory access.
 template <typename Kernel, typename... Args>
 inline cudaError_t launch_maybe_cooperative(Kernel kern, dim3 grid, int threads, int smem,
-                                            cudaStream_t stream, bool cooperative, Args... args) {
+                                            cudaStream_t stream, bool cooperative, bool pdl,
+                                            Args... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(threads, 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (cooperative) {
+        attr[na].id = cudaLaunchAttributeCooperative;
+        attr[na++].val.cooperative = 1;
+    }
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na++].val.programmaticStreamSerializationAllowed = 1;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = cooperative ? 1 : 0;
+    cfg.numAttrs = na;
     if (cooperative) {
         int per_sm = 0, dev = 0, sms = 0;
         cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
@@ -281,19 +301,21 @@ inline cudaError_t launch_maybe_cooperative(Kernel kern, dim3 grid, int threads,
 // at all (the caller then launches without clusters).
 template <typename Kernel, typename... Args>
 inline cudaError_t launch_clustered(Kernel kern, dim3 grid, int cluster_x, int threads, int smem,
-                                    cudaStream_t stream, Args... args) {
+                                    cudaStream_t stream, bool pdl, Args... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(threads, 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(cluster_x);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 2 : 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
     return e == cudaSuccess ? cudaGetLastError() : e;
 }

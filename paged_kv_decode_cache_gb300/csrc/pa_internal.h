@@ -40,6 +40,10 @@ struct DecodeParams {
     // partials through distributed shared memory; counters, part_o and
     // part_lse are then unused.
     int32_t cluster_merge;
+    // Host side only: launch with programmatic stream serialization (the
+    // kernel waits for the previous kernel in the stream before it touches
+    // global memory, but may become resident while that kernel finishes).
+    int32_t pdl;
     // Fused cache write (pa_decode_step): sequence b's new token, the one at
     // position L_b - 1, is written into the pools by the CTA that reads that
     // position, right before its TMA load of that tile.  null: no write.

@@ -774,3 +774,61 @@ def test_split_merge_paths_mq_and_fp8(path, merge_path):
         assert_close(bf16_dev_to_f64(out), ref, f"fp8 P={P} {path}")
         assert_lse_close(lse.cpu().double().numpy(), ref_lse, f"fp8 P={P} {path}")
     assert dev.status_value() == 0
+
+
+# ------------------------------------- programmatic dependent launch: chained calls
+@pytest.mark.parametrize("path", ["cluster", "grid"])
+@pytest.mark.parametrize("graph", [False, True])
+def test_chained_steps_see_the_previous_output(path, graph, merge_path):
+    """The tensor-core kernel is launched with programmatic stream serialization,
+    so a launch may become resident while the previous one finishes.  Chain
+    eight calls whose queries are the previous call's output (a step's own
+    fused write first), eagerly and replayed from a CUDA graph: each link must
+    equal the oracle applied to the previous link's result, so no call may read
+    its inputs before the previous kernel has written them."""
+    merge_path(path)
+    w = W.make_workload("chain", B=3, Hq=28, Hkv=4, D=128, block_size=16,
+                        seq_lens=[300, 17, 129], num_blocks=40, seed=21)
+    dev = Dev(w)
+    P, n = 4, 8
+    ws = [torch.zeros(pa.pa_splitkv_workspace_bytes(w.B, w.Hq, w.D, P), dtype=torch.uint8,
+                      device="cuda") for _ in range(n)]
+    outs = [torch.full((w.B, w.Hq, w.D), 1e4, dtype=torch.bfloat16, device="cuda")
+            for _ in range(n)]
+
+    def chain():
+        pa.pa_decode_step(outs[0], None, dev.q, dev.k_new, dev.v_new, dev.slot_mapping,
+                          dev.k_cache, dev.v_cache, dev.block_tables, dev.seq_lens, w.scale,
+                          num_splits=P, workspace=ws[0], status=dev.status)
+        for i in range(1, n):
+            pa.pa_decode_splitkv(outs[i], None, outs[i - 1], dev.k_cache, dev.v_cache,
+                                 dev.block_tables, dev.seq_lens, w.scale, num_splits=P,
+                                 workspace=ws[i], status=dev.status)
+
+    if graph:
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            chain()                                   # warm-up: loads the kernels
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        for o in outs:
+            o.fill_(1e4)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            chain()
+        for o in outs:
+            o.fill_(1e4)
+        torch.cuda.synchronize()
+        g.replay()
+    else:
+        chain()
+    torch.cuda.synchronize()
+    assert dev.status_value() == 0
+    kc, vc = oracle_after_write(w)
+    q = w.q
+    for i in range(n):
+        ref, _ = oracle.decode(q, kc, vc, w.block_tables, w.seq_lens, w.scale)
+        got = bf16_dev_to_f64(outs[i])
+        assert_close(got, ref, f"link {i} ({path}, graph={graph})")
+        q = outs[i].view(torch.int16).cpu().numpy().view(np.uint16)   # the next link's queries
