@@ -110,23 +110,31 @@ struct TcCfg {
     static constexpr int kPBufBytes = 2 * kPBytes;
     // (a cluster merge stages the partial O^T, kN x 128 fp32, in the P^T buffers)
     static_assert(kPBufBytes >= kN * 128 * 4, "cluster merge stage");
-    // red[128 rows][GP], col[N], m_ref[N], alpha[N], rel[N] (output row of
+    // red[128 rows][GPr], col[N], m_ref[N], alpha[N], rel[N] (output row of
     // column n relative to the CTA's first row, -1: padding), abort flag,
-    // TMEM slot, merge ticket
-    static constexpr int kRedBytes = (kTcRows * GP + 4 * kN) * 4 + 16;
+    // TMEM slot, merge ticket.  Thread t writes its row t of red, so rows are
+    // GP + 1 floats apart where that fits (a warp's stores then fall in 32
+    // different banks; GP apart they share 32 / GP banks).
+    static constexpr int red_bytes(int gpr) { return (kTcRows * gpr + 4 * kN) * 4 + 16; }
     // shared memory for nk K stages, nv V stages and nbp P^T buffers, laid out
     // as below (rings, Q, P^T, scratch, barriers, masks, block-id rings, align)
     // (FP8: a "converted" barrier per K and V stage and the V producer's mask ring)
-    static constexpr int smem_for(int nk, int nv, int nbp) {
-        return ((nk + nv) * kTileBytes + kQBytes + nbp * kPBufBytes + kRedBytes + 7) / 8 * 8 +
+    static constexpr int smem_for(int nk, int nv, int nbp, int gpr = GP) {
+        return ((nk + nv) * kTileBytes + kQBytes + nbp * kPBufBytes + red_bytes(gpr) + 7) / 8 * 8 +
                (2 * nk + 2 * nv + 2 * kTcNBS + 2 * nbp + (F8 ? nk + nv : 0)) * 8 +
                kTcMaskRing * 8 * (F8 ? 2 : 1) + 2 * (kTcLook + 1) * 32 * 4 + 1024;
     }
     // the deepest pipeline that fits: K and V stages first, then P^T buffers
-    static constexpr int kChoice = smem_for(3, 3, 2) <= kTcSmemLimit ? 0
-                                   : smem_for(3, 3, 1) <= kTcSmemLimit ? 1
-                                   : smem_for(2, 3, 2) <= kTcSmemLimit ? 2
-                                   : smem_for(2, 2, 2) <= kTcSmemLimit ? 3 : 4;
+    static constexpr int choice_for(int gpr) {
+        return smem_for(3, 3, 2, gpr) <= kTcSmemLimit ? 0
+               : smem_for(3, 3, 1, gpr) <= kTcSmemLimit ? 1
+               : smem_for(2, 3, 2, gpr) <= kTcSmemLimit ? 2
+               : smem_for(2, 2, 2, gpr) <= kTcSmemLimit ? 3 : 4;
+    }
+    // the padded scratch only where it costs no pipeline depth
+    static constexpr int kGPr = choice_for(GP + 1) == choice_for(GP) ? GP + 1 : GP;
+    static constexpr int kRedBytes = red_bytes(kGPr);
+    static constexpr int kChoice = choice_for(kGPr);
     static constexpr int kNK = kChoice <= 1 ? 3 : 2;            // K stages
     static constexpr int kNV = kChoice <= 2 ? 3 : 2;            // V stages
     static constexpr int kNBP = (kChoice == 1 || kChoice == 4) ? 1 : 2;  // P^T buffers
@@ -142,7 +150,7 @@ struct TcCfg {
     static constexpr int kVMaskOff = kMaskOff + kTcMaskRing * 8;   // FP8 only
     static constexpr int kLookOff = kVMaskOff + (F8 ? kTcMaskRing * 8 : 0);
     static constexpr int kSmemBytes = kLookOff + 2 * (kTcLook + 1) * 32 * 4 + 1024;
-    static_assert(kSmemBytes == smem_for(kNK, kNV, kNBP), "layout");
+    static_assert(kSmemBytes == smem_for(kNK, kNV, kNBP, kGPr), "layout");
     // the K producer rewrites mask slot c % ring only once softmax c has read it
     static_assert(kNK + kTcNBS <= kTcMaskRing, "mask ring");
     static_assert(kSmemBytes <= kTcSmemLimit, "shared memory");
@@ -152,32 +160,38 @@ struct TcCfg {
     static constexpr int kColO = kTcNBS * kN;
 };
 
-// Max (or sum) over the rows of column n's head of a [128 rows][GP] array:
+// Max (or sum) over the rows of column n's head of a [128 rows][GPr] array:
 // row m = (tile * HC + head) * 16 + r holds the GP values of its own head.
-template <int HC, int GP, bool kMax>
+template <int HC, int GP, int GPr, bool kMax>
 __device__ __forceinline__ float column_reduce(const float *red, int n) {
     const int hh = n / GP, q = n % GP;
     float acc = kMax ? -INFINITY : 0.f;
 #pragma unroll 1
     for (int t = 0; t < kTcRows / (kTile * HC); ++t) {
-        const float *base = red + ((t * HC + hh) * kTile) * GP + q;
+        const float *base = red + ((t * HC + hh) * kTile) * GPr + q;
 #pragma unroll
-        for (int r = 0; r < kTile; ++r) acc = kMax ? fmaxf(acc, base[r * GP]) : acc + base[r * GP];
+        for (int r = 0; r < kTile; ++r) acc = kMax ? fmaxf(acc, base[r * GPr]) : acc + base[r * GPr];
     }
     return acc;
 }
 
-// 16-bit operand value of p for the PV MMA: bf16, or fp16 with FP8 pools
+// 16-bit operand values of p for the PV MMA: bf16, or fp16 with FP8 pools
 // (whose K/V tiles are widened to fp16).
-template <bool F8>
-__device__ __forceinline__ uint16_t p16_bits(float x) {
-    if constexpr (F8) return __half_as_ushort(__float2half_rn(x));
-    else return __bfloat16_as_ushort(__float2bfloat16_rn(x));
-}
 template <bool F8>
 __device__ __forceinline__ float p16_value(uint16_t b) {
     if constexpr (F8) return __half2float(__ushort_as_half(b));
     else return __bfloat162float(__ushort_as_bfloat16(b));
+}
+// Two values at once (one packed conversion): a in the low 16 bits, b in the high.
+template <bool F8>
+__device__ __forceinline__ uint32_t p16x2_bits(float a, float b) {
+    if constexpr (F8) {
+        const __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<const uint32_t *>(&h);
+    } else {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<const uint32_t *>(&h);
+    }
 }
 
 // Widens 16 e4m3 codes to 16 fp16 values (exact: e4m3 is a subset of fp16),
@@ -215,8 +229,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     uint8_t *vring = smem + C::kVOff;
     uint8_t *qs = smem + C::kQOff;
     uint8_t *ps = smem + C::kPOff;
-    float *red = reinterpret_cast<float *>(smem + C::kRedOff);      // [128 rows][GP] scratch
-    float *col = red + kTcRows * GP;                                // [N] per-column result
+    float *red = reinterpret_cast<float *>(smem + C::kRedOff);      // [128 rows][GPr] scratch
+    float *col = red + kTcRows * C::kGPr;                           // [N] per-column result
     float *m_ref = col + N;                                         // [N] reference max
     float *alpha_s = m_ref + N;                                     // [N] rescale factors
     int *rel_s = reinterpret_cast<int *>(alpha_s + N);               // [N] output row offsets
@@ -700,10 +714,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                 }
                 // chunk max of every column (head, q) over that head's rows, via shared memory
 #pragma unroll
-                for (int q = 0; q < GP; ++q) red[tid * GP + q] = sc[q];
+                for (int q = 0; q < GP; ++q) red[tid * C::kGPr + q] = sc[q];
                 named_sync(1, 128);
                 if (tid < N) {
-                    const float cm = column_reduce<HC, GP, true>(red, tid);
+                    const float cm = column_reduce<HC, GP, C::kGPr, true>(red, tid);
                     const float old = m_ref[tid];
                     const float mn = fmaxf(old, cm);
                     alpha_s[tid] = (mn == -INFINITY) ? 1.f : fast_exp2(old - mn);
@@ -737,11 +751,18 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             // carries p to about 2^-17 relative, where hi alone would be 2^-9
             uint16_t pb[GP], pl[GP];  // bf16 (fp16 with FP8 pools) bit patterns
 #pragma unroll
-            for (int q = 0; q < GP; ++q) {
-                const float pf = sc[q] != -INFINITY ? fast_exp2(sc[q] - mr[q]) : 0.f;
-                pb[q] = p16_bits<F8>(pf);
-                pl[q] = p16_bits<F8>(pf - p16_value<F8>(pb[q]));
-                l_thr[q] += p16_value<F8>(pb[q]) + p16_value<F8>(pl[q]);
+            for (int q = 0; q < GP; q += 2) {  // two columns per packed conversion
+                const float p0 = sc[q] != -INFINITY ? fast_exp2(sc[q] - mr[q]) : 0.f;
+                const float p1 = sc[q + 1] != -INFINITY ? fast_exp2(sc[q + 1] - mr[q + 1]) : 0.f;
+                const uint32_t hi = p16x2_bits<F8>(p0, p1);
+                pb[q] = static_cast<uint16_t>(hi);
+                pb[q + 1] = static_cast<uint16_t>(hi >> 16);
+                const float h0 = p16_value<F8>(pb[q]), h1 = p16_value<F8>(pb[q + 1]);
+                const uint32_t lo = p16x2_bits<F8>(p0 - h0, p1 - h1);
+                pl[q] = static_cast<uint16_t>(lo);
+                pl[q + 1] = static_cast<uint16_t>(lo >> 16);
+                l_thr[q] += h0 + p16_value<F8>(pl[q]);
+                l_thr[q + 1] += h1 + p16_value<F8>(pl[q + 1]);
             }
             if (c >= NBP) wait_or_abort(&pfree[pbuf], ((c / NBP) - 1) & 1);  // PV c - NBP done
             {
@@ -776,10 +797,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         // The row sums are final once the last chunk's p is written, so they are
         // reduced (through shared memory) while its PV still runs.
 #pragma unroll
-        for (int q = 0; q < GP; ++q) red[tid * GP + q] = l_thr[q];
+        for (int q = 0; q < GP; ++q) red[tid * C::kGPr + q] = l_thr[q];
         named_sync(1, 128);
         if (tid < N) {  // row sum of column n, its reciprocal (alpha_s is free now), its row
-            const float lsum = column_reduce<HC, GP, false>(red, tid);
+            const float lsum = column_reduce<HC, GP, C::kGPr, false>(red, tid);
             col[tid] = lsum;
             alpha_s[tid] = lsum > 0.f ? p.v_scale / lsum : 0.f;  // 0: no key seen (causal)
             const int c = tid % GP;
