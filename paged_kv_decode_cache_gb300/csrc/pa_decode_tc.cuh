@@ -36,8 +36,9 @@
 //        CTA-wide vote, one barrier per chunk); then the chunk max is
 //        reduced, O^T is rescaled in TMEM and the row sums with it.  Row sums
 //        stay per thread and are reduced under the last PV; the epilogue reads
-//        O^T, normalises it and stores a bf16 row (or an fp32 partial and its
-//        log-sum-exp when the range is split).
+//        O^T, normalises it and stages it as rows in the idle P^T buffers
+//        (bf16, or fp32 partials when the range is split), which one bulk
+//        copy per row writes out (the cluster merge reads them in place).
 //   warp 4 (QK issuer) and warp 7 (PV issuer): one thread each issues its
 //        MMAs as soon as their inputs are ready (QK: K landed and the S buffer
 //        released by the softmax threads; PV: P^T written and V landed) and
@@ -59,7 +60,10 @@
 //        into the softmax scale and v_scale into the epilogue.
 // With the range split, the CTAs of one (sequence, head group) merge their
 // partials in the same launch: once all P have arrived, they share the
-// merge tasks (pa_split_merge.cuh).  Every mbarrier wait and spin is bounded in polls and
+// merge tasks, through global memory or, as one thread-block cluster,
+// through distributed shared memory (pa_split_merge.cuh).  The kernel waits
+// for the previous kernel in the stream (programmatic dependent launch)
+// before it touches global memory.  Every mbarrier wait and spin is bounded in polls and
 // in time and honours a CTA-wide abort flag; the softmax warps agree on an
 // abort at their per-chunk vote.
 #pragma once
