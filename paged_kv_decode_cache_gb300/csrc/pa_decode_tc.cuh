@@ -108,10 +108,15 @@ struct TcCfg {
     static constexpr int kBoxBytes = HC * kTile * kSubBytes;    // one TMA box: HC heads x 16 rows
     static constexpr int kQBytes = 2 * kN * kSubBytes;          // [N][64] x 2 halves
     static constexpr int kPBytes = 2 * kN * kSubBytes;          // 2 atoms of [N][64 m]
-    // P^T buffer: 2 atoms of [2N][64 m], rows 0..N-1 the hi and rows N..2N-1
-    // the lo bf16 part of p; one MMA with N' = 2N accumulates both into
-    // adjacent TMEM column ranges
+    // P^T buffer: the hi (columns n' = 0..N-1) and lo (n' = N..2N-1) bf16
+    // parts of p; one MMA with N' = 2N accumulates both into adjacent TMEM
+    // column ranges.  Layout, 128-byte swizzle: for N = 32 and 64 MN-major,
+    // [2N / 64 atoms][128 m][64 n'] (a row's 2GP values are whole 16-byte
+    // chunks, written with vector stores); for N = 16 (64-byte rows) K-major,
+    // 2 atoms of [2N][64 m].
+    static constexpr bool kPMn = kN == 32 || kN == 64;
     static constexpr int kPBufBytes = 2 * kPBytes;
+    static_assert(!kPMn || kPBufBytes == (2 * kN / 64) * kSubTile, "MN-major P^T: whole atoms");
     // (a cluster merge stages the partial O^T, kN x 128 fp32, in the P^T buffers)
     static_assert(kPBufBytes >= kN * 128 * 4, "cluster merge stage");
     // red[128 rows][GPr], col[N], m_ref[N], alpha[N], rel[N] (output row of
@@ -554,7 +559,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     } else if (warp == kTcPvWarp) {
         // ================= PV issuer =================
         if (lane == 0) {
-            constexpr uint32_t kIdPV = tc5::idesc_bf16_f32(kTcRows, 2 * N, true, false, F8);
+            constexpr uint32_t kIdPV = tc5::idesc_bf16_f32(kTcRows, 2 * N, true, C::kPMn, F8);
             int done = 0;
             for (int c = 0; c < nch; ++c) {
                 if (!wait_or_abort(&pready[c % NBP], (c / NBP) & 1)) break;
@@ -563,11 +568,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                 const uint8_t *vt = vring + (c % NV) * C::kTileBytes;
                 const uint8_t *pt = ps + (c % NBP) * C::kPBufBytes;
 #pragma unroll
-                for (int j = 0; j < kTcRows / 16; ++j) {
+                for (int j = 0; j < kTcRows / 16; ++j) {  // K = 16 rows m per MMA
+                    const uint64_t bdesc =
+                        C::kPMn ? tc5::sw128_desc(pt + j * 16 * kSubBytes, C::kSubTile, 1024)
+                                : tc5::sw128_desc(pt + (j >> 2) * (2 * N * kSubBytes) + (j & 3) * 32, 16, 1024);
                     tc5::mma_bf16(tmem + C::kColO,
-                                  tc5::sw128_desc(vt + j * 16 * kSubBytes, C::kSubTile, 1024),
-                                  tc5::sw128_desc(pt + (j >> 2) * (2 * N * kSubBytes) + (j & 3) * 32, 16,
-                                                  1024),
+                                  tc5::sw128_desc(vt + j * 16 * kSubBytes, C::kSubTile, 1024), bdesc,
                                   kIdPV, c > 0 || j > 0);
                 }
                 tc5::commit(&pfree[c % NBP]);
@@ -753,23 +759,43 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             }
             // p = hi + lo, both bf16 (the PV MMA takes bf16 operands): the pair
             // carries p to about 2^-17 relative, where hi alone would be 2^-9
-            uint16_t pb[GP], pl[GP];  // bf16 (fp16 with FP8 pools) bit patterns
+            // bf16 (fp16 with FP8 pools) bit patterns, two columns per word
+            uint32_t hw[GP / 2], lw[GP / 2];
 #pragma unroll
             for (int q = 0; q < GP; q += 2) {  // two columns per packed conversion
                 const float p0 = sc[q] != -INFINITY ? fast_exp2(sc[q] - mr[q]) : 0.f;
                 const float p1 = sc[q + 1] != -INFINITY ? fast_exp2(sc[q + 1] - mr[q + 1]) : 0.f;
                 const uint32_t hi = p16x2_bits<F8>(p0, p1);
-                pb[q] = static_cast<uint16_t>(hi);
-                pb[q + 1] = static_cast<uint16_t>(hi >> 16);
-                const float h0 = p16_value<F8>(pb[q]), h1 = p16_value<F8>(pb[q + 1]);
+                const float h0 = p16_value<F8>(static_cast<uint16_t>(hi));
+                const float h1 = p16_value<F8>(static_cast<uint16_t>(hi >> 16));
                 const uint32_t lo = p16x2_bits<F8>(p0 - h0, p1 - h1);
-                pl[q] = static_cast<uint16_t>(lo);
-                pl[q + 1] = static_cast<uint16_t>(lo >> 16);
-                l_thr[q] += h0 + p16_value<F8>(pl[q]);
-                l_thr[q + 1] += h1 + p16_value<F8>(pl[q + 1]);
+                hw[q / 2] = hi;
+                lw[q / 2] = lo;
+                l_thr[q] += h0 + p16_value<F8>(static_cast<uint16_t>(lo));
+                l_thr[q + 1] += h1 + p16_value<F8>(static_cast<uint16_t>(lo >> 16));
             }
             if (c >= NBP) wait_or_abort(&pfree[pbuf], ((c / NBP) - 1) & 1);  // PV c - NBP done
-            {
+            if constexpr (C::kPMn) {
+                // row m = tid of P^T, this row's own head's columns (hi, then lo at
+                // N + n); the other heads' columns stay zero
+                uint8_t *row = ps + pbuf * C::kPBufBytes + tid * kSubBytes;
+                auto at = [&](int n) -> uint32_t {  // byte offset of column n of the row
+                    return (n >> 6) * C::kSubTile + ((((n & 63) >> 3) ^ (tid & 7)) << 4) + (n & 7) * 2;
+                };
+                const int n0 = my_head * GP;
+                if constexpr (GP >= 8) {
+#pragma unroll
+                    for (int g = 0; g < GP / 8; ++g) {
+                        *reinterpret_cast<uint4 *>(row + at(n0 + 8 * g)) =
+                            make_uint4(hw[4 * g], hw[4 * g + 1], hw[4 * g + 2], hw[4 * g + 3]);
+                        *reinterpret_cast<uint4 *>(row + at(N + n0 + 8 * g)) =
+                            make_uint4(lw[4 * g], lw[4 * g + 1], lw[4 * g + 2], lw[4 * g + 3]);
+                    }
+                } else {  // GP = 4: half a chunk
+                    *reinterpret_cast<uint2 *>(row + at(n0)) = make_uint2(hw[0], hw[1]);
+                    *reinterpret_cast<uint2 *>(row + at(N + n0)) = make_uint2(lw[0], lw[1]);
+                }
+            } else {
                 // P^T[n][m] for this row's own head block; the other heads' columns stay zero
                 uint8_t *pt = ps + pbuf * C::kPBufBytes + (tid >> 6) * (2 * N * kSubBytes);
                 const int tt = tid & 63;
@@ -777,8 +803,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                 for (int q = 0; q < GP; ++q) {
                     const int n = my_head * GP + q;   // lo row N + n swizzles as n (N % 8 == 0)
                     const uint32_t at = n * kSubBytes + (((tt >> 3) ^ (n & 7)) << 4) + (tt & 7) * 2;
-                    *reinterpret_cast<uint16_t *>(pt + at) = pb[q];
-                    *reinterpret_cast<uint16_t *>(pt + N * kSubBytes + at) = pl[q];
+                    const uint32_t sh = (q & 1) * 16;
+                    *reinterpret_cast<uint16_t *>(pt + at) = static_cast<uint16_t>(hw[q / 2] >> sh);
+                    *reinterpret_cast<uint16_t *>(pt + N * kSubBytes + at) = static_cast<uint16_t>(lw[q / 2] >> sh);
                 }
             }
             // an invalid row zeroes its V row, so 0 * (stale or NaN) never reaches O^T
