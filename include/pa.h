@@ -97,7 +97,9 @@ enum {
     PA_STATUS_BAD_BLOCK = 1,  /* block table entry outside [0, num_blocks) */
     PA_STATUS_BAD_SLOT = 2,   /* slot_mapping entry >= num_blocks * block_size */
     PA_STATUS_BAD_SEQLEN = 4, /* seq_len < 0 or > max_blocks_per_seq * block_size */
-    PA_STATUS_TIMEOUT = 8     /* a bounded wait on an async copy gave up */
+    PA_STATUS_TIMEOUT = 8     /* a bounded wait (an async copy, an MMA, the
+                                 split merge's arrival) gave up after about a
+                                 second; that call's outputs are not valid */
 };
 
 /*
@@ -216,8 +218,9 @@ int pa_combine(void *out, float *lse, const float *part_o, const float *part_lse
  * PA_EWORKSPACE.  It must be zero-filled before its first use (cudaMemset):
  * the merge counters in it start at zero and every completed call leaves
  * them at zero again, so a workspace can be reused call after call (not by
- * calls that overlap on the GPU).  Results equal pa_decode's up to fp32
- * rounding order.
+ * calls that overlap on the GPU).  A call that reported PA_STATUS_TIMEOUT
+ * may leave them non-zero: zero the workspace again before reusing it.
+ * Results equal pa_decode's up to fp32 rounding order.
  */
 int pa_decode_splitkv(void *out, float *lse, const void *q, const void *k_cache,
                       const void *v_cache, pa_cache_desc cache, const int32_t *block_tables,
