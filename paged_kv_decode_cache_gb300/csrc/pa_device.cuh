@@ -295,10 +295,10 @@ inline cudaError_t launch_maybe_cooperative(Kernel kern, dim3 grid, int threads,
     return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
-// Launch `kern` with thread-block clusters of `cluster_x` CTAs along x (x a
-// multiple of it).  Sizes above 8 are allowed where the device schedules them;
-// returns cudaErrorInvalidConfiguration when no such cluster fits an SM group
-// at all (the caller then launches without clusters).
+// Launch `kern` with thread-block clusters of `cluster_x` CTAs along x (grid.x
+// a multiple of it); `pdl` as for launch_maybe_cooperative.  Sizes above 8
+// need the kernel's non-portable-size attribute, which max_active_clusters
+// sets; callers ask it first whether (and how many) such clusters fit.
 template <typename Kernel, typename... Args>
 inline cudaError_t launch_clustered(Kernel kern, dim3 grid, int cluster_x, int threads, int smem,
                                     cudaStream_t stream, bool pdl, Args... args) {
