@@ -311,7 +311,10 @@ def run_reference(args, world, rank):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": args.workload},
+        "data": "synthetic",
+        "config": {"workload": args.workload, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+                   "block_size": w.block_size, "seq_lens_total": int(w.seq_lens.sum()),
+                   "q_len": w.q_len, "step": "the oracle's cache write and decode, fp64, host cores"},
         "cpu_baseline": {"value": value, "unit": "TB/s", "cores": threads, "kind": "oracle",
                          "sample": f"per step: {desc}"},
         "e2e": {"value": value, "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

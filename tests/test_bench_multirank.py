@@ -59,3 +59,5 @@ def test_reference_arm_prints_once_under_torchrun():
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    cfg = line["config"]                                # the same workload keys as our arm's line
+    assert cfg["workload"] == "tiny" and cfg["B"] == 4 and cfg["D"] == 64 and cfg["q_len"] == 1
