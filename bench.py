@@ -31,6 +31,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -162,7 +163,9 @@ class ClockSampler:
     def __init__(self, gpu: str):
         self.gpu = gpu
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        # raw samples (the JSON line carries their summary): PA_BENCH_CLOCKS_DIR, else a temp dir
+        out = os.environ.get("PA_BENCH_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(out, f"clocks_bench_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
