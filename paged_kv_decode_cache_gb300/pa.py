@@ -10,6 +10,8 @@ Outputs are caller-allocated, as in the C ABI.  Work is enqueued on
 from __future__ import annotations
 
 import ctypes
+import functools
+import itertools
 import os
 import re
 import threading
@@ -130,6 +132,33 @@ def _need(t: torch.Tensor, name: str, dtype: torch.dtype, ndim: int):
         raise ValueError(f"{name} must be a CUDA tensor")
 
 
+def _one_cuda_device(devices, fn: str) -> Optional[torch.device]:
+    """The one CUDA device among `devices` (None when there is none: the
+    per-tensor checks then reject the call); several raise ValueError."""
+    cuda = {d for d in devices if d.type == "cuda"}
+    if len(cuda) > 1:
+        raise ValueError(f"{fn}: tensors on several devices ({', '.join(sorted(map(str, cuda)))})")
+    return next(iter(cuda)) if cuda else None
+
+
+def _on_tensors_device(fn):
+    """Run a wrapper on the device its tensors live on (and that device's
+    current stream when none is given): the C library launches on the current
+    device.  A call whose device is already current runs unchanged."""
+    @functools.wraps(fn)
+    def call(*args, **kwargs):
+        dev = _one_cuda_device([a.device for a in itertools.chain(args, kwargs.values())
+                                if isinstance(a, torch.Tensor)], fn.__name__)
+        stream = kwargs.get("stream")
+        if dev is not None and stream is not None and stream.device != dev:
+            raise ValueError(f"{fn.__name__}: stream on {stream.device}, tensors on {dev}")
+        if dev is None or dev.index == torch.cuda.current_device():
+            return fn(*args, **kwargs)
+        with torch.cuda.device(dev):
+            return fn(*args, **kwargs)
+    return call
+
+
 def cache_desc(k_cache: torch.Tensor) -> CacheDesc:
     nb, bs, hkv, d = k_cache.shape
     return CacheDesc(nb, bs, hkv, d)
@@ -175,6 +204,7 @@ def pa_auto_num_splits(B: int, Hq: int, Hkv: int, D: int, max_blocks_per_seq: in
     return r
 
 
+@_on_tensors_device
 def pa_cache_write(k_new, v_new, slot_mapping, k_cache, v_cache, status=None, stream=None):
     _need(k_new, "k_new", torch.bfloat16, 3)
     _need(v_new, "v_new", torch.bfloat16, 3)
@@ -205,6 +235,7 @@ def _decode_inputs(q, k_cache, v_cache, block_tables, seq_lens):
     return B, Hq, D
 
 
+@_on_tensors_device
 def pa_decode(out, lse, q, k_cache, v_cache, block_tables, seq_lens, scale, status=None,
               stream=None):
     B, Hq, D = _decode_inputs(q, k_cache, v_cache, block_tables, seq_lens)
@@ -219,6 +250,7 @@ def pa_decode(out, lse, q, k_cache, v_cache, block_tables, seq_lens, scale, stat
     _check("pa_decode", rc)
 
 
+@_on_tensors_device
 def pa_decode_partial(part_o, part_lse, q, k_cache, v_cache, block_tables, seq_lens, scale,
                       num_splits, status=None, stream=None):
     B, Hq, D = _decode_inputs(q, k_cache, v_cache, block_tables, seq_lens)
@@ -233,6 +265,7 @@ def pa_decode_partial(part_o, part_lse, q, k_cache, v_cache, block_tables, seq_l
     _check("pa_decode_partial", rc)
 
 
+@_on_tensors_device
 def pa_combine(out, lse, part_o, part_lse, stream=None):
     _need(part_o, "part_o", torch.float32, 4)
     _need(part_lse, "part_lse", torch.float32, 3)
@@ -247,6 +280,7 @@ def pa_combine(out, lse, part_o, part_lse, stream=None):
     _check("pa_combine", rc)
 
 
+@_on_tensors_device
 def pa_decode_splitkv(out, lse, q, k_cache, v_cache, block_tables, seq_lens, scale,
                       num_splits=0, workspace=None, status=None, stream=None):
     B, Hq, D = _decode_inputs(q, k_cache, v_cache, block_tables, seq_lens)
@@ -265,6 +299,7 @@ def pa_decode_splitkv(out, lse, q, k_cache, v_cache, block_tables, seq_lens, sca
     _check("pa_decode_splitkv", rc)
 
 
+@_on_tensors_device
 def pa_decode_step(out, lse, q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables,
                    seq_lens, scale, num_splits=0, workspace=None, status=None, stream=None):
     """Fused step: write this step's new K/V through slot_mapping and run split-KV decode."""
@@ -295,6 +330,7 @@ def pa_decode_step(out, lse, q, k_new, v_new, slot_mapping, k_cache, v_cache, bl
 PA_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
+@_on_tensors_device
 def pa_decode_mq(out, lse, q, k_cache, v_cache, block_tables, seq_lens, scale, num_splits=0,
                  workspace=None, status=None, stream=None):
     """Causal multi-query decode: q and out are [B, q_len, Hq, D], lse [B, q_len, Hq]."""
@@ -324,6 +360,7 @@ def pa_cascade_workspace_bytes(B: int, Hq: int, Hkv: int, D: int, n_prefix_block
                                                 block_size))
 
 
+@_on_tensors_device
 def pa_decode_cascade(out, lse, q, k_cache, v_cache, n_prefix_blocks, block_tables, seq_lens, scale,
                       workspace=None, status=None, stream=None):
     """Decode with the first n_prefix_blocks table entries shared by every sequence:
@@ -348,6 +385,7 @@ def _need_pool8(t, name):
     _need(t, name, torch.uint8, 4)
 
 
+@_on_tensors_device
 def pa_cache_write_fp8(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale,
                        status=None, stream=None):
     """Quantising slot-mapping write into uint8 e4m3 pools [num_blocks, bs, Hkv, D]."""
@@ -366,6 +404,7 @@ def pa_cache_write_fp8(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_
     _check("pa_cache_write_fp8", rc)
 
 
+@_on_tensors_device
 def pa_decode_splitkv_fp8(out, lse, q, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens,
                           scale, num_splits=0, workspace=None, status=None, stream=None):
     """Split-KV decode over uint8 e4m3 pools with per-pool scales."""
@@ -393,6 +432,7 @@ def pa_decode_splitkv_fp8(out, lse, q, k_cache, v_cache, k_scale, v_scale, block
     _check("pa_decode_splitkv_fp8", rc)
 
 
+@_on_tensors_device
 def pa_decode_splitkv_noalloc(out, lse, q, k_cache, v_cache, block_tables, seq_lens, scale,
                               num_splits=0, status=None, stream=None):
     """Split-KV decode with the partials in the library's built-in device array

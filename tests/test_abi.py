@@ -5,6 +5,7 @@ import ctypes
 import subprocess
 
 import pytest
+import torch
 
 from paged_kv_decode_cache_gb300 import build as B
 from paged_kv_decode_cache_gb300 import pa
@@ -270,3 +271,18 @@ def test_cascade_rejects_bad_arguments(lib):
         assert rc == pa.PA_EINVAL, npre
     assert lib.pa_cascade_workspace_bytes(4, 4, 4, 128, 0, 7, 16) == 0
     assert lib.pa_cascade_workspace_bytes(4, 4, 4, 128, 7, 7, 16) == 0
+
+
+def test_wrappers_run_on_their_tensors_device():
+    """Every tensor wrapper checks that its tensors share one CUDA device (and
+    runs there); the check itself needs no GPU."""
+    one = pa._one_cuda_device
+    assert one([torch.device("cpu")], "f") is None
+    assert one([torch.device("cuda", 1), torch.device("cuda", 1), torch.device("cpu")], "f") == \
+        torch.device("cuda", 1)
+    with pytest.raises(ValueError, match="several devices"):
+        one([torch.device("cuda", 0), torch.device("cuda", 1)], "f")
+    for name in ("pa_cache_write", "pa_decode", "pa_decode_partial", "pa_combine",
+                 "pa_decode_splitkv", "pa_decode_step", "pa_decode_mq", "pa_decode_cascade",
+                 "pa_cache_write_fp8", "pa_decode_splitkv_fp8", "pa_decode_splitkv_noalloc"):
+        assert getattr(pa, name).__wrapped__.__name__ == name
