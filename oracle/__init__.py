@@ -55,16 +55,17 @@ def _bind(lib):
     P = ctypes.c_void_p
     i32, i64, f32 = ctypes.c_int, ctypes.c_int64, ctypes.c_float
     lib.oracle_cache_write.argtypes = [P, P, P, i64, P, P, i32, i32, i32, i32]
+    f64 = ctypes.c_double
     lib.oracle_decode_rows.argtypes = [P, P, P, P, i32, P, P, P, i32, i32, i32, i32,
-                                       P, i32, P, i32, i32, f32, P, i32]
+                                       P, i32, P, i32, i32, f64, P, i32]
     lib.oracle_decode_partial.argtypes = [P, P, P, P, P, i32, i32, i32, i32,
-                                          P, i32, P, i32, i32, f32, i32, i32, P, i32]
+                                          P, i32, P, i32, i32, f64, i32, i32, P, i32]
     lib.oracle_combine.argtypes = [P, P, P, P, i64, i32, i32]
     lib.oracle_e4m3_to_bf16.argtypes = [P, P, i64]
     lib.oracle_bf16_to_e4m3.argtypes = [P, P, i64, f32]
     lib.oracle_cache_write_fp8.argtypes = [P, P, P, i64, P, P, i32, i32, i32, i32, f32, f32]
     lib.oracle_decode_mq.argtypes = [P, P, P, i32, P, P, i32, i32, i32, i32, P, i32, P, i32, i32,
-                                     f32, P, i32]
+                                     f64, P, i32]
     lib.oracle_max_threads.argtypes = []
     for fn in (lib.oracle_cache_write, lib.oracle_decode_rows,
                lib.oracle_decode_partial, lib.oracle_combine, lib.oracle_max_threads):
@@ -125,6 +126,11 @@ def _req(a, dtype):
     return np.ascontiguousarray(a)
 
 
+def _f32(x) -> float:
+    """The fp32 value of a scale, as the library receives it, widened to a Python float."""
+    return float(np.float32(x))
+
+
 def _check(rc, what):
     if rc != ORACLE_OK:
         raise OracleError(f"{what} failed with code {rc}")
@@ -167,7 +173,15 @@ def _common(q, k_cache, v_cache, block_tables, seq_lens):
 
 def decode_rows(q, k_cache, v_cache, block_tables, seq_lens, scale, rows_b, rows_h,
                 nthreads: int = 0):
-    """Exact attention for the listed (b, h) rows: returns (out[n, D], lse[n]) in fp64."""
+    """Exact attention for the listed (b, h) rows: returns (out[n, D], lse[n]) in fp64.
+    ``scale`` is taken as the fp32 value the library's callers pass."""
+    return _decode_rows_exact(q, k_cache, v_cache, block_tables, seq_lens, _f32(scale), rows_b,
+                              rows_h, nthreads)
+
+
+def _decode_rows_exact(q, k_cache, v_cache, block_tables, seq_lens, scale, rows_b, rows_h,
+                       nthreads: int = 0):
+    """decode_rows with ``scale`` used as given, in double precision."""
     q, k_cache, v_cache, block_tables, seq_lens, B, Hq, D, nb, bs, hkv = _common(
         q, k_cache, v_cache, block_tables, seq_lens)
     rows_b = _req(rows_b, np.int32)
@@ -187,11 +201,15 @@ def decode_rows(q, k_cache, v_cache, block_tables, seq_lens, scale, rows_b, rows
 
 def decode(q, k_cache, v_cache, block_tables, seq_lens, scale, nthreads: int = 0):
     """Exact attention for every (b, h): returns (out[B, Hq, D], lse[B, Hq]) in fp64."""
+    return _decode_exact(q, k_cache, v_cache, block_tables, seq_lens, _f32(scale), nthreads)
+
+
+def _decode_exact(q, k_cache, v_cache, block_tables, seq_lens, scale, nthreads: int = 0):
     B, Hq, D = np.asarray(q).shape
     bb, hh = np.meshgrid(np.arange(B, dtype=np.int32), np.arange(Hq, dtype=np.int32),
                          indexing="ij")
-    out, lse = decode_rows(q, k_cache, v_cache, block_tables, seq_lens, scale,
-                           bb.ravel(), hh.ravel(), nthreads)
+    out, lse = _decode_rows_exact(q, k_cache, v_cache, block_tables, seq_lens, scale,
+                                  bb.ravel(), hh.ravel(), nthreads)
     return out.reshape(B, Hq, D), lse.reshape(B, Hq)
 
 
@@ -231,15 +249,17 @@ def cache_write_fp8(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_sca
 
 def decode_fp8(q, k_cache, v_cache, block_tables, seq_lens, scale, k_scale, v_scale,
                nthreads: int = 0):
-    """Exact attention over e4m3 pools holding k_scale * K and v_scale * V.
-    A per-pool scale factors out of the attention exactly: scores use
-    scale * k_scale on the widened codes, and the output is multiplied by
+    """Exact attention over e4m3 pools whose code c stands for e4m3(c) * k_scale
+    (K) and e4m3(c) * v_scale (V), the scales being the fp32 values the library
+    receives.  A per-pool scale factors out of the attention exactly: the
+    scores are (scale * k_scale) times the dot products with the widened codes,
+    that product formed in double precision, and the output is multiplied by
     v_scale.  Returns (out[B, Hq, D], lse[B, Hq]) in fp64."""
     kw = e4m3_to_bf16(k_cache)
     vw = e4m3_to_bf16(v_cache)
-    out, lse = decode(q, kw, vw, block_tables, seq_lens, np.float32(scale) * np.float32(k_scale),
-                      nthreads)
-    return out * float(v_scale), lse
+    out, lse = _decode_exact(q, kw, vw, block_tables, seq_lens, _f32(scale) * _f32(k_scale),
+                             nthreads)
+    return out * _f32(v_scale), lse
 
 
 def decode_mq(q, k_cache, v_cache, block_tables, seq_lens, scale, nthreads: int = 0):
@@ -255,7 +275,7 @@ def decode_mq(q, k_cache, v_cache, block_tables, seq_lens, scale, nthreads: int 
     scores = np.empty((max(nthr, max_threads()), block_tables.shape[1] * bs), np.float64)
     rc = _load().oracle_decode_mq(_ptr(out), _ptr(lse), _ptr(q), q_len, _ptr(k_cache),
                                   _ptr(v_cache), nb, bs, hkv, D, _ptr(block_tables),
-                                  block_tables.shape[1], _ptr(seq_lens), B, Hq, float(scale),
+                                  block_tables.shape[1], _ptr(seq_lens), B, Hq, _f32(scale),
                                   _ptr(scores), nthreads)
     _check(rc, "oracle_decode_mq")
     return out, lse
@@ -273,7 +293,7 @@ def decode_partial(q, k_cache, v_cache, block_tables, seq_lens, scale, num_parts
     rc = _load().oracle_decode_partial(_ptr(part_o), _ptr(part_lse), _ptr(q), _ptr(k_cache),
                                        _ptr(v_cache), nb, bs, hkv, D, _ptr(block_tables),
                                        block_tables.shape[1], _ptr(seq_lens), B, Hq,
-                                       float(scale), num_parts, chunk, _ptr(scores), nthreads)
+                                       _f32(scale), num_parts, chunk, _ptr(scores), nthreads)
     _check(rc, "oracle_decode_partial")
     return part_o, part_lse
 

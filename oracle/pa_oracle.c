@@ -252,7 +252,10 @@ static double attend_range(double *out_row, const uint16_t *q_row,
 
 /*
  * Decode attention for an explicit list of (b, h) rows.  out is
- * [n_rows, D], lse is [n_rows] (nullable).  `scores` is caller-provided work
+ * [n_rows, D], lse is [n_rows] (nullable).  `scale` multiplies every dot
+ * product in double precision: the library's fp32 softmax scale, widened
+ * exactly (or, over FP8 pools, that scale times the pool's k_scale, the
+ * product formed in double).  `scores` is caller-provided work
  * memory of [team size, max_blocks * block_size] doubles: each OpenMP thread
  * keeps the scores of its current row in its own slice.
  */
@@ -261,7 +264,7 @@ int oracle_decode_rows(double *out, double *lse,
                        const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
                        int num_blocks, int block_size, int num_kv_heads, int head_dim,
                        const int32_t *block_tables, int max_blocks, const int32_t *seq_lens,
-                       int B, int Hq, float scale, double *scores, int nthreads) {
+                       int B, int Hq, double scale, double *scores, int nthreads) {
     if (B <= 0 || Hq <= 0 || num_kv_heads <= 0 || Hq % num_kv_heads != 0 || head_dim <= 0 ||
         block_size <= 0 || max_blocks <= 0 || n_rows < 0)
         return ORACLE_EBADARG;
@@ -286,7 +289,7 @@ int oracle_decode_rows(double *out, double *lse,
             const double l = attend_range(out + (int64_t)i * head_dim,
                                           q + ((int64_t)b * Hq + h) * head_dim, k_cache, v_cache,
                                           block_tables + (int64_t)b * max_blocks, 0, seq_lens[b],
-                                          block_size, num_kv_heads, head_dim, g, (double)scale,
+                                          block_size, num_kv_heads, head_dim, g, scale,
                                           my_scores);
             if (lse) lse[i] = l;
         }
@@ -313,7 +316,7 @@ int oracle_decode_mq(double *out, double *lse,
                      const uint16_t *q, int q_len, const uint16_t *k_cache, const uint16_t *v_cache,
                      int num_blocks, int block_size, int num_kv_heads, int head_dim,
                      const int32_t *block_tables, int max_blocks, const int32_t *seq_lens,
-                     int B, int Hq, float scale, double *scores, int nthreads) {
+                     int B, int Hq, double scale, double *scores, int nthreads) {
     if (B <= 0 || q_len <= 0 || Hq <= 0 || num_kv_heads <= 0 || Hq % num_kv_heads != 0 ||
         head_dim <= 0 || block_size <= 0 || max_blocks <= 0)
         return ORACLE_EBADARG;
@@ -340,7 +343,7 @@ int oracle_decode_mq(double *out, double *lse,
             const double l = attend_range(out + r * head_dim, q + r * head_dim, k_cache, v_cache,
                                           block_tables + (int64_t)b * max_blocks, 0, visible,
                                           block_size, num_kv_heads, head_dim, h / group,
-                                          (double)scale, my_scores);
+                                          scale, my_scores);
             if (lse) lse[r] = l;
         }
     }
@@ -357,7 +360,7 @@ int oracle_decode_partial(double *part_o, double *part_lse,
                           const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
                           int num_blocks, int block_size, int num_kv_heads, int head_dim,
                           const int32_t *block_tables, int max_blocks, const int32_t *seq_lens,
-                          int B, int Hq, float scale, int num_parts, int chunk,
+                          int B, int Hq, double scale, int num_parts, int chunk,
                           double *scores, int nthreads) {
     if (B <= 0 || Hq <= 0 || num_kv_heads <= 0 || Hq % num_kv_heads != 0 || head_dim <= 0 ||
         block_size <= 0 || max_blocks <= 0 || num_parts <= 0 || chunk <= 0)
@@ -387,7 +390,7 @@ int oracle_decode_partial(double *part_o, double *part_lse,
                                                  q + ((int64_t)b * Hq + h) * head_dim, k_cache, v_cache,
                                                  block_tables + (int64_t)b * max_blocks, (int)t0, (int)t1,
                                                  block_size, num_kv_heads, head_dim, h / group,
-                                                 (double)scale, my_scores);
+                                                 scale, my_scores);
                 }
             }
         }

@@ -448,15 +448,15 @@ def pin_fp8_quantise_saturates_and_round_trips():
 
 def pin_fp8_decode_equals_sdpa_on_dequantised_cache():
     """Attention over e4m3 pools equals SDPA over torch-dequantised contiguous K/V
-    (code * scale in fp64, the softmax scale applied as given): the factored
-    scales agree to fp32 rounding of scale * k_scale (1e-6)."""
+    (code * scale in fp64, with the fp32 pool scales the library receives, the
+    softmax scale applied as given): the factored scales agree to fp64 rounding."""
     w = small_case(B=3, Hq=6, Hkv=2, D=32, lens=(5, 16, 41), nb=24, seed=51)
     ks, vs = 0.043, 0.029
     k8 = oracle.bf16_to_e4m3(w.k_cache, ks)
     v8 = oracle.bf16_to_e4m3(w.v_cache, vs)
     out, lse = oracle.decode_fp8(w.q, k8, v8, w.block_tables, w.seq_lens, w.scale, ks, vs)
-    kd = _torch_e4m3(k8).double().numpy() * ks
-    vd = _torch_e4m3(v8).double().numpy() * vs
+    kd = _torch_e4m3(k8).double().numpy() * float(np.float32(ks))
+    vd = _torch_e4m3(v8).double().numpy() * float(np.float32(vs))
     for b in range(w.B):
         L = int(w.seq_lens[b])
         t = np.arange(L)
@@ -466,7 +466,7 @@ def pin_fp8_decode_equals_sdpa_on_dequantised_cache():
         q = torch.from_numpy(bf16_to_f64(w.q[b]))[:, None, :]
         o = torch.nn.functional.scaled_dot_product_attention(q, kt, vt, scale=float(w.scale))
         err = np.abs(out[b] - o[:, 0].numpy()).max()
-        assert err < 1e-6, f"fp8 decode vs dequantised SDPA: {err}"
+        assert err < 1e-12, f"fp8 decode vs dequantised SDPA: {err}"
 
 
 def pin_fp8_cache_write_quantises_the_new_rows():
