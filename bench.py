@@ -41,6 +41,7 @@ sys.path.insert(0, ROOT)
 
 DEFAULT_WORKLOAD = "qwen2.5-7b-bs16"
 L2_BYTES = 129 * 1000 * 1000
+GPU_HEADSTART_CYCLES = 400_000   # ~0.2 ms of GPU spin before a timed region
 METRIC = "paged decode attention: achieved HBM TB/s (% of ~8 TB/s) and us/call"
 
 
@@ -60,6 +61,11 @@ def parse():
                     help="total oracle time of --impl reference, spread over its steps")
     ap.add_argument("--unfused", action="store_true",
                     help="time pa_cache_write + pa_decode_splitkv instead of pa_decode_step")
+    ap.add_argument("--configs", choices=["main", "none"], default="main",
+                    help="also measure every config of the metric (per-call latency, steady "
+                         "state, cache write, oracle at 1 and all cores) into the line's 'configs'")
+    ap.add_argument("--config-oracle-seconds", type=float, default=0.6,
+                    help="CPU time per oracle sample in the configs sweep")
     return ap.parse_args()
 
 
@@ -367,8 +373,8 @@ def run_ours(args, world, rank, local):
     out = torch.empty(oshape, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(oshape[:-1], dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(device=dev)
-    forced = os.environ.get("PA_DECODE_KERNEL", "auto")
-    use_tc = forced == "tensor_core" or (forced != "cuda_core" and w.D == 128)
+    forced = pa.pa_get_option(pa.PA_OPT_DECODE_KERNEL)
+    use_tc = forced == pa.PA_KERNEL_TENSOR_CORE or (forced != pa.PA_KERNEL_CUDA_CORE and w.D == 128)
     kernel_name = "decode_tc_kernel" if use_tc else "decode_cc_kernel"
 
     cascade = w.cascade_blocks > 0   # shared prefix attended once, then the suffixes, then a merge
@@ -446,6 +452,12 @@ def run_ours(args, world, rank, local):
             for r in range(n_single):
                 single[r % R][0].replay()
 
+    # Every graph the timed loop replays runs once first (its first replay
+    # uploads it), then the W warm-up steps; the timed region holds only
+    # steady-state steps whatever W is.
+    with torch.cuda.stream(stream):
+        for g, _ in full + single:
+            g.replay()
     wf, wr = divmod(args.warmup, S)
     run_steps(wf, wr)
     stream.synchronize()
@@ -454,6 +466,10 @@ def run_ours(args, world, rank, local):
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     with ClockSampler(gpu_for_smi(dev)) as clk:
+        with torch.cuda.stream(stream):
+            # the GPU idles here while the host queues the timed replays, so the
+            # region measures the GPU's steps, not the host's submission latency
+            torch.cuda._sleep(GPU_HEADSTART_CYCLES)
         t_start.record(stream)
         run_steps(n_full, n_rem)
         t_end.record(stream)
@@ -553,6 +569,7 @@ def run_ours(args, world, rank, local):
     a0 = torch.cuda.Event(enable_timing=True)
     a1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
+        torch.cuda._sleep(GPU_HEADSTART_CYCLES)
         a0.record(stream)
         for j in range(n_e2e):
             e2e_graphs[j % 2].replay()
@@ -589,6 +606,10 @@ def run_ours(args, world, rank, local):
         cpu = {"value": byts / secs / 1e12, "unit": "TB/s", "cores": threads, "kind": "oracle",
                "sample": desc}
 
+    configs = None
+    if rank == 0 and world == 1 and args.configs != "none":
+        configs = measure_configs(args, dev, peak)
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "TB/s", "n_gpus": world,
@@ -617,8 +638,151 @@ def run_ours(args, world, rank, local):
             "gpu_launches": args.steps * launches_per_step,
             "kernel_samples": len(kern_ms),
             "clocks": clocks,
+            "configs": configs,
         }
         print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------ every config of the metric
+# (config number of the metric's list, workload) for the sweep: the tiny parity
+# case, the Qwen2.5-1.5B layer at B = 1 and 8, the Qwen2.5-7B layer at 16-token
+# blocks and 256-token pages, the four long-context shapes, the Qwen3 batch.
+CONFIG_SWEEP = [
+    (1, "tiny"), (2, "qwen2.5-1.5b-B1"), (2, "qwen2.5-1.5b-B8"), (3, "qwen2.5-7b-bs16"),
+    (3, "qwen2.5-7b-bs256"), (4, "long-B1-L4096"), (4, "long-B2-L4096"), (4, "long-B1-L32768"),
+    (4, "long-B2-L32768"), (5, "qwen3-0.6b-B256"),
+]
+PER_CALL_WARMUP, PER_CALL_CALLS = 10, 50
+
+
+def _pct(xs, q):
+    return float(np.percentile(np.asarray(xs), q))
+
+
+def measure_configs(args, dev, peak):
+    """Each config of the metric on this GPU, the same fused step the headline
+    times (pa_decode_step: cache write + split decode + merge, automatic split):
+
+    - per call: 10 warm-up calls, then 50 calls each between a pair of CUDA
+      events, the L2 flushed before every call by writing a buffer twice its
+      size (outside the events); median, p10 and p90 in us;
+    - steady state: back-to-back replays of a CUDA graph over enough pool
+      replicas that each step reads its KV from HBM, timed as a region;
+    - the cache write alone (pa_cache_write of the step's new tokens), per call
+      as above, with its read + write bytes;
+    - long-context shapes: the same per-call latency unsplit (P = 1), which
+      shows what the split buys;
+    - bytes: logical (every token of every sequence, K + V, plus q and out) and
+      unique (a pool row shared by several sequences counted once), each with
+      its fraction of the measured copy peak at the median per-call time and
+      at the steady-state time;
+    - the fp64 oracle on the host, 1 core and all cores, on a bounded sample.
+    """
+    import torch
+
+    from paged_kv_decode_cache_gb300 import pa
+    from paged_kv_decode_cache_gb300 import workloads as W
+    import oracle
+
+    def bf(a):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        return (t.view(torch.int16).view(torch.bfloat16) if a.dtype == np.uint16 else t).to(dev)
+
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    all_cores = oracle.max_threads()
+    out_all = {}
+    with ClockSampler(gpu_for_smi(dev)) as clk:
+        for cfg, name in CONFIG_SWEEP:
+            w = W.WORKLOADS[name]()
+            q, bt, sl = bf(w.q), bf(w.block_tables), bf(w.seq_lens)
+            kn, vn, slots = bf(w.k_new), bf(w.v_new), bf(w.slot_mapping)
+            k0, v0 = bf(w.k_cache), bf(w.v_cache)
+            P = pa.pa_auto_num_splits(w.B, w.Hq, w.Hkv, w.D, w.max_blocks, w.block_size)
+            ws = torch.zeros(max(1, pa.pa_splitkv_workspace_bytes(w.B, w.Hq, w.D, P)),
+                             dtype=torch.uint8, device=dev)
+            out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device=dev)
+            lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
+
+            def step(kc, vc, splits=P):
+                pa.pa_decode_step(out, lse, q, kn, vn, slots, kc, vc, bt, sl, w.scale,
+                                  num_splits=splits, workspace=ws, stream=stream)
+
+            def per_call(fn):
+                with torch.cuda.stream(stream):
+                    for _ in range(PER_CALL_WARMUP):
+                        flush.fill_(1)
+                        fn()
+                    evs = [(torch.cuda.Event(enable_timing=True),
+                            torch.cuda.Event(enable_timing=True)) for _ in range(PER_CALL_CALLS)]
+                    for e0, e1 in evs:
+                        flush.fill_(1)
+                        e0.record(stream)
+                        fn()
+                        e1.record(stream)
+                stream.synchronize()
+                us = [e0.elapsed_time(e1) * 1e3 for e0, e1 in evs]
+                return {"us_p50": round(_pct(us, 50), 3), "us_p10": round(_pct(us, 10), 3),
+                        "us_p90": round(_pct(us, 90), 3)}
+
+            lat = per_call(lambda: step(k0, v0))
+            unsplit = per_call(lambda: step(k0, v0, 1)) if cfg == 4 else None
+            wr = per_call(lambda: pa.pa_cache_write(kn, vn, slots, k0, v0, stream=stream))
+
+            # steady state: one graph of S steps over R pool replicas, replayed back to back
+            touched = w.kv_bytes()
+            R = (max(1, min(8, math.ceil(2.5 * L2_BYTES / max(touched, 1)) + 1))
+                 if touched < 3 * L2_BYTES else 1)
+            pools = [(k0, v0)] + [(k0.clone(), v0.clone()) for _ in range(R - 1)]
+            S = R * max(1, math.ceil(16 / R))
+            with torch.cuda.stream(stream):
+                for kc, vc in pools:
+                    step(kc, vc)
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for k in range(S):
+                    step(*pools[k % R])
+            reps = max(4, int(math.ceil(2000.0 / max(1.0, lat["us_p50"] * S))))
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    g.replay()
+                torch.cuda._sleep(GPU_HEADSTART_CYCLES)
+                a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a0.record(stream)
+                for _ in range(reps):
+                    g.replay()
+                a1.record(stream)
+            a1.synchronize()
+            graph_us = a0.elapsed_time(a1) * 1e3 / (reps * S)
+
+            logical = w.kv_bytes() + w.qo_bytes() + w.write_bytes()
+            unique = w.unique_kv_bytes() + w.qo_bytes() + w.write_bytes()
+            frac = lambda b, us: round(b / (us * 1e-6) / 1e9 / peak, 4)   # noqa: E731
+            row = {"config": cfg, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+                   "block_size": w.block_size, "seq_lens_total": int(w.seq_lens.sum()),
+                   "splits": P, **lat, "calls": PER_CALL_CALLS,
+                   "graph_us": round(graph_us, 3), "graph_pool_replicas": R,
+                   "bytes_logical": logical, "bytes_unique": unique,
+                   "frac_logical_p50": frac(logical, lat["us_p50"]),
+                   "frac_unique_p50": frac(unique, lat["us_p50"]),
+                   "frac_logical_graph": frac(logical, graph_us),
+                   "frac_unique_graph": frac(unique, graph_us),
+                   "cache_write": {**wr, "tokens": int((w.slot_mapping >= 0).sum()),
+                                   "bytes_read_plus_written": w.write_bytes()}}
+            if unsplit:
+                row["unsplit"] = unsplit
+            for cores in (1, all_cores):
+                secs, byts, rows, threads, desc = time_oracle(w, args.config_oracle_seconds,
+                                                              nthreads=cores)
+                row[f"oracle_{'1core' if cores == 1 else 'allcores'}"] = {
+                    "TBps": byts / secs / 1e12, "cores": threads, "sample": desc}
+            out_all[name] = row
+            del pools, k0, v0, g
+            torch.cuda.empty_cache()
+    return {"peak_gbs": peak, "l2_between_calls": "flushed (2x L2 written)",
+            "step": "pa_decode_step (fused cache write + split decode + merge), auto P",
+            "clocks": clk.summary(), "workloads": out_all}
 
 
 def main():

@@ -59,8 +59,8 @@
  *     may become resident while the previous kernel in the stream finishes,
  *     but waits for that kernel's completion (griddepcontrol.wait) before it
  *     reads or writes any global memory, and lets the next such launch queue
- *     once all of its CTAs run.  PA_PDL=0 in the environment (read on every
- *     call) launches it plainly.
+ *     once all of its CTAs run.  pa_set_option(PA_OPT_PDL, 0) launches it
+ *     plainly.
  */
 #ifndef PA_H_
 #define PA_H_
@@ -91,6 +91,34 @@ enum {
     PA_EWORKSPACE = -3,   /* workspace missing or smaller than required */
     PA_ECUDA = -4         /* a CUDA call or kernel launch failed */
 };
+
+/*
+ * Process-wide switches, for tests and measurements (the defaults are what the
+ * library is tuned for).  Each starts from the environment variable named
+ * beside it, read once, the first time the library needs any of them; after
+ * that only pa_set_option changes them.  A call uses the values current when it
+ * is made; the switches are shared by all host threads and devices.
+ */
+enum {
+    PA_OPT_DECODE_KERNEL = 0, /* which decode kernel runs: PA_KERNEL_* below
+                                 (PA_DECODE_KERNEL=cuda_core|tensor_core) */
+    PA_OPT_SPLIT_MERGE = 1,   /* PA_MERGE_AUTO, or PA_MERGE_GRID: never merge split
+                                 partials through a thread-block cluster
+                                 (PA_SPLIT_MERGE=grid) */
+    PA_OPT_PDL = 2            /* 1: programmatic stream serialization for the
+                                 tensor-core kernel; 0: plain launches (PA_PDL=0) */
+};
+enum {
+    PA_KERNEL_AUTO = 0,        /* tensor cores wherever they can run the shape */
+    PA_KERNEL_CUDA_CORE = 1,   /* force the CUDA-core kernel */
+    PA_KERNEL_TENSOR_CORE = 2  /* force the tensor-core kernel */
+};
+enum { PA_MERGE_AUTO = 0, PA_MERGE_GRID = 1 };
+
+/* Set a switch; PA_EINVAL for an unknown switch or value. */
+int pa_set_option(int32_t option, int32_t value);
+/* Current value of a switch, or PA_EINVAL. */
+int pa_get_option(int32_t option);
 
 /* Device status bits (OR-ed into *status). */
 enum {
@@ -132,10 +160,9 @@ int pa_cache_write(const void *k_new, const void *v_new, const int64_t *slot_map
  * head) holds the G query heads, so each KV tile is read once; use
  * pa_decode_splitkv when B * Hkv is small next to the SM count.
  * Two kernels implement the step: a tensor-core one (tcgen05, chosen
- * whenever D = 128) and a CUDA-core one (D = 64).  The
- * environment variable PA_DECODE_KERNEL=cuda_core or =tensor_core forces one
- * of them (read on every call; a shape the forced kernel cannot run is
- * PA_EUNSUPPORTED).  Both are checked against the same oracle.
+ * whenever D = 128) and a CUDA-core one (D = 64).  The switch
+ * PA_OPT_DECODE_KERNEL forces one of them (a shape the forced kernel cannot
+ * run is PA_EUNSUPPORTED).  Both are checked against the same oracle.
  */
 int pa_decode(void *out, float *lse, const void *q, const void *k_cache, const void *v_cache,
               pa_cache_desc cache, const int32_t *block_tables, int32_t max_blocks_per_seq,
@@ -149,13 +176,16 @@ int pa_decode(void *out, float *lse, const void *q, const void *k_cache, const v
  * that the group size Hq / Hkv and head_dim D select (2 CTAs per SM for the
  * CUDA-core kernel, 1 for the tensor-core kernel), capped so that every
  * partition keeps at least four 16-token tiles.  Host-only; depends only on
- * its arguments and the PA_DECODE_KERNEL override described at pa_decode.
+ * its arguments and the PA_OPT_DECODE_KERNEL switch.
  * Returns P >= 1, or PA_EINVAL / PA_EUNSUPPORTED.
  */
 int pa_choose_num_splits(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
                          int32_t max_blocks_per_seq, int32_t block_size, int32_t sm_count);
 
 /*
+ * Split-K partitioning of each sequence's tokens (psmarter "mini-infer" forum
+ * write-up, feature list item 7: flash decoding splits the KV of a long
+ * sequence into partitions that are attended in parallel and then merged).
  * Tokens per partition for P splits: ceil(ceil(max_blocks_per_seq*bs / P) / 16) * 16.
  * Partition p of sequence b covers tokens [p * chunk, min((p + 1) * chunk, L_b)).
  * Returns the chunk, or PA_EINVAL.
@@ -172,7 +202,9 @@ int pa_partition_tokens(int32_t max_blocks_per_seq, int32_t block_size, int32_t 
 size_t pa_splitkv_workspace_bytes(int32_t B, int32_t Hq, int32_t D, int32_t num_splits);
 
 /*
- * Per-partition decode attention (the first half of split-KV decoding).
+ * Per-partition decode attention, the first half of split-K flash decoding
+ * (psmarter write-up, feature list item 7: each partition of a sequence's KV
+ * is attended on its own).
  * part_o: device fp32 [B, Hq, P, D], each partial normalised over its own
  * token range; part_lse: device fp32 [B, Hq, P], natural-log LSE of the
  * range, -inf for an empty range (and then part_o = 0).  Partition ranges as
@@ -185,8 +217,9 @@ int pa_decode_partial(float *part_o, float *part_lse, const void *q, const void 
                       pa_stream_t stream);
 
 /*
- * Log-sum-exp merge of P partials per (b, h) (the combine step that split-K
- * flash decoding implies):
+ * Log-sum-exp merge of P partials per (b, h), the second half of split-K
+ * flash decoding (psmarter write-up, feature list item 7: the partitions'
+ * partial results are merged into the exact output):
  *   lse = M + ln sum_p exp(lse_p - M),  M = max_p lse_p
  *   out = sum_p exp(lse_p - lse) * o_p           (bf16, round to nearest even)
  * A partial with lse_p = -inf has weight 0; if all are -inf, out = 0 and
@@ -210,8 +243,8 @@ int pa_combine(void *out, float *lse, const float *part_o, const float *part_lse
  *     launch whose CTAs of each sequence and head group meet at a counter in
  *     the workspace, then share the merge;
  *   - otherwise pa_combine runs after the decode kernel.
- * PA_SPLIT_MERGE=grid in the environment (read on every call) skips the
- * cluster merge.
+ * Partitions beyond 256 are always merged by pa_combine.
+ * pa_set_option(PA_OPT_SPLIT_MERGE, PA_MERGE_GRID) skips the cluster merge.
  * num_splits == 0 picks P with pa_auto_num_splits; P == 1 runs pa_decode
  * directly and needs no workspace.  workspace: device, at least
  * pa_splitkv_workspace_bytes(B, Hq, D, P) bytes, 256-byte aligned, else
@@ -243,14 +276,19 @@ int pa_decode_splitkv(void *out, float *lse, const void *q, const void *k_cache,
  * loads the library holds until the process exits.
  *   - The first call on a device looks up that array's device address
  *     (cudaGetSymbolAddress, with the device current) and caches it; make
- *     that first call before any stream capture.
+ *     that first call before any stream capture.  The address is looked up
+ *     again when the device's current context has changed (after
+ *     cudaDeviceReset the library's module is loaded anew); make the first
+ *     call after such a reset before any capture too.
+ *   - Arguments are checked exactly as pa_decode_splitkv checks them before
+ *     the array is touched; a rejected call enqueues nothing.
  *   - Returns PA_EWORKSPACE when the split's partials,
  *     pa_splitkv_workspace_bytes(B, Hq, D, P), exceed the array.
  *   - Every call shares the one array: calls whose kernels overlap on the
  *     GPU (other streams, other host threads) race on it and must be
  *     serialised by the caller.  Each call clears the merge counters it
  *     uses (cudaMemsetAsync on `stream`, no allocation) and writes every
- *     partial before reading it.
+ *     partial before reading it.  num_splits == 1 does not use the array.
  */
 int pa_decode_splitkv_noalloc(void *out, float *lse, const void *q, const void *k_cache,
                               const void *v_cache, pa_cache_desc cache,
@@ -296,7 +334,7 @@ int pa_decode_step(void *out, float *lse, const void *q, const void *k_new, cons
  * q: device bf16 [B, q_len, Hq, D]; out: device bf16 [B, q_len, Hq, D];
  * lse: device fp32 [B, q_len, Hq] or NULL.  1 <= q_len <= 65535.
  * Supported: D = 128, G = Hq / Hkv <= 32 (the tensor-core kernel; q_len > 1
- * with PA_DECODE_KERNEL=cuda_core or D = 64 is PA_EUNSUPPORTED).  A CTA holds
+ * with the CUDA-core kernel forced, or D = 64, is PA_EUNSUPPORTED).  A CTA holds
  * up to 32 / G query positions of its heads; more positions are spread over
  * more CTAs, each reading the keys its queries can see (for q_len * G > 32
  * the KV is read about q_len * G / 32 times: suited to verification, not to
@@ -371,7 +409,7 @@ int pa_cache_write_fp8(const void *k_new, const void *v_new, const int64_t *slot
  * (code * scale); the tensor-core kernel widens each landed tile to fp16
  * exactly and runs its MMAs in fp16 (q is rounded to fp16: |q| must stay below
  * 65504).  Supported: head_dim 128, Hq / Hkv <= 32 (PA_EUNSUPPORTED
- * otherwise, and with PA_DECODE_KERNEL=cuda_core).
+ * otherwise, and with the CUDA-core kernel forced).
  */
 int pa_decode_splitkv_fp8(void *out, float *lse, const void *q, const void *k_cache,
                           const void *v_cache, pa_cache_desc cache, float k_scale, float v_scale,

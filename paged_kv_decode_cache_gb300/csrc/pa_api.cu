@@ -92,21 +92,42 @@ int64_t units_per_split(Kernel k, int B, int G, int Hkv, int qpc = 1, int qgroup
     return static_cast<int64_t>(B) * Hkv;
 }
 
+// Process-wide switches (pa_set_option), each initialised once from its
+// environment variable the first time any of them is read.
+std::atomic<int> g_options[3];
+std::once_flag g_options_once;
+
+int option(int which) {
+    std::call_once(g_options_once, [] {
+        const char *k = std::getenv("PA_DECODE_KERNEL");
+        g_options[PA_OPT_DECODE_KERNEL].store(
+            k && std::strcmp(k, "cuda_core") == 0     ? PA_KERNEL_CUDA_CORE
+            : k && std::strcmp(k, "tensor_core") == 0 ? PA_KERNEL_TENSOR_CORE
+                                                      : PA_KERNEL_AUTO);
+        const char *m = std::getenv("PA_SPLIT_MERGE");
+        g_options[PA_OPT_SPLIT_MERGE].store(m && std::strcmp(m, "grid") == 0 ? PA_MERGE_GRID
+                                                                            : PA_MERGE_AUTO);
+        const char *d = std::getenv("PA_PDL");
+        g_options[PA_OPT_PDL].store(d && std::strcmp(d, "0") == 0 ? 0 : 1);
+    });
+    return g_options[which].load(std::memory_order_relaxed);
+}
+
 // Which decode kernel runs for a GQA group of G heads of dimension D.  The
-// tensor-core kernel needs D = 128 and G <= 16; the CUDA-core kernel takes
+// tensor-core kernel needs D = 128 and G <= 32; the CUDA-core kernel takes
 // D in {64, 128} and G <= 8.  By default the tensor cores take every shape
-// they can.  PA_DECODE_KERNEL=cuda_core or =tensor_core in the environment
-// forces one of them (read on every call; unsupported shapes are rejected).
+// they can; the PA_OPT_DECODE_KERNEL option can force one of them (a shape the
+// forced kernel cannot run is rejected).
 int pick_kernel(int G, int D, Kernel *k) {
     const bool tc_ok = D == 128 && G >= 1 && G <= kMaxGroupTc;
     const bool cc_ok = (D == 64 || D == 128) && G >= 1 && G <= kMaxGroupCc;
-    const char *env = std::getenv("PA_DECODE_KERNEL");
-    if (env && std::strcmp(env, "cuda_core") == 0) {
+    const int forced = option(PA_OPT_DECODE_KERNEL);
+    if (forced == PA_KERNEL_CUDA_CORE) {
         if (!cc_ok) return PA_EUNSUPPORTED;
         *k = Kernel::kCudaCore;
         return PA_OK;
     }
-    if (env && std::strcmp(env, "tensor_core") == 0) {
+    if (forced == PA_KERNEL_TENSOR_CORE) {
         if (!tc_ok) return PA_EUNSUPPORTED;
         *k = Kernel::kTensorCore;
         return PA_OK;
@@ -126,21 +147,15 @@ int pick_kernel(int G, int D, Kernel *k) {
 // tensor-core kernel makes the P CTAs of a (sequence, head group) one
 // thread-block cluster when P <= 16 and all the launch's clusters can be
 // resident at once, and merges through distributed shared memory; otherwise
-// (and with PA_SPLIT_MERGE=grid in the environment, read on every call) the
-// grid is launched cooperatively and the partials meet in global memory.
-bool merge_forced_grid() {
-    const char *env = std::getenv("PA_SPLIT_MERGE");
-    return env && std::strcmp(env, "grid") == 0;
-}
+// (and with PA_OPT_SPLIT_MERGE = PA_MERGE_GRID) the grid is launched
+// cooperatively and the partials meet in global memory.
+bool merge_forced_grid() { return option(PA_OPT_SPLIT_MERGE) == PA_MERGE_GRID; }
 
 // The tensor-core kernel is launched with programmatic stream serialization
-// (programmatic dependent launch) unless PA_PDL=0 is in the environment (read
-// on every call): it may then become resident while the previous kernel in
-// the stream finishes, and waits for it before touching global memory.
-bool pdl_enabled() {
-    const char *env = std::getenv("PA_PDL");
-    return !(env && std::strcmp(env, "0") == 0);
-}
+// (programmatic dependent launch) unless PA_OPT_PDL is 0: it may then become
+// resident while the previous kernel in the stream finishes, and waits for it
+// before touching global memory.
+bool pdl_enabled() { return option(PA_OPT_PDL) != 0; }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -398,7 +413,31 @@ int run_decode(bool split, void *out, float *lse, float *part_o, float *part_lse
 
 extern "C" {
 
-int pa_version(void) { return 100; }
+int pa_version(void) { return 200; }
+
+int pa_set_option(int32_t which, int32_t value) {
+    switch (which) {
+        case PA_OPT_DECODE_KERNEL:
+            if (value < PA_KERNEL_AUTO || value > PA_KERNEL_TENSOR_CORE) return PA_EINVAL;
+            break;
+        case PA_OPT_SPLIT_MERGE:
+            if (value != PA_MERGE_AUTO && value != PA_MERGE_GRID) return PA_EINVAL;
+            break;
+        case PA_OPT_PDL:
+            if (value != 0 && value != 1) return PA_EINVAL;
+            break;
+        default:
+            return PA_EINVAL;
+    }
+    option(which);  // the environment's defaults first, so they cannot overwrite this
+    g_options[which].store(value, std::memory_order_relaxed);
+    return PA_OK;
+}
+
+int pa_get_option(int32_t which) {
+    if (which < PA_OPT_DECODE_KERNEL || which > PA_OPT_PDL) return PA_EINVAL;
+    return option(which);
+}
 
 const char *pa_strerror(int code) {
     switch (code) {
@@ -527,13 +566,18 @@ int pa_combine(void *out, float *lse, const float *part_o, const float *part_lse
 }
 
 namespace {
-// Split-KV decode shared by pa_decode_splitkv and pa_decode_step.
+// Split-KV decode shared by pa_decode_splitkv, pa_decode_step, pa_decode_mq,
+// pa_decode_splitkv_fp8 and pa_decode_splitkv_noalloc.  With library_scratch
+// the workspace is the library's own array (pa::noalloc_scratch), looked up
+// only after every argument check has passed, and the merge counters in it
+// are cleared on `stream` before the kernel runs (a caller's workspace keeps
+// its counters at zero between calls instead).
 int splitkv_common(void *out, float *lse, const void *q, const void *k_cache, const void *v_cache,
                    const pa_cache_desc &cache, const int32_t *block_tables,
                    int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t B, int32_t Hq,
                    float scale, int32_t num_splits, void *workspace, size_t workspace_bytes,
                    int32_t *status, cudaStream_t stream, const NewTokens &nt, int32_t q_len = 1,
-                   const Fp8Scales *f8 = nullptr) {
+                   const Fp8Scales *f8 = nullptr, bool library_scratch = false) {
     int rc = check_decode_args(q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq,
                                seq_lens, B, Hq, scale);
     if (rc) return rc;
@@ -557,6 +601,10 @@ int splitkv_common(void *out, float *lse, const void *q, const void *k_cache, co
     // rows of the partials: (sequence, query position, head)
     const int32_t Bq = B * q_len;
     const size_t need = pa_splitkv_workspace_bytes(Bq, Hq, cache.head_dim, P);
+    if (library_scratch) {
+        rc = pa::noalloc_scratch(&workspace, &workspace_bytes);
+        if (rc) return rc;
+    }
     if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return PA_EWORKSPACE;
     const int64_t rows = static_cast<int64_t>(Bq) * Hq * P;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -565,11 +613,17 @@ int splitkv_common(void *out, float *lse, const void *q, const void *k_cache, co
     int32_t *counters = reinterpret_cast<int32_t *>(ws + round_up(rows * cache.head_dim * 4, 256) +
                                                     round_up(rows * 4, 256));
     // One cooperative launch that merges its own partials when the whole grid
-    // fits on the GPU at once; otherwise partials, then pa_combine.
-    rc = run_decode(true, out, lse, part_o, part_lse, q, k_cache, v_cache, cache, block_tables,
-                    max_blocks_per_seq, seq_lens, B, Hq, scale, P, status, stream, counters, nt,
-                    q_len, f8);
-    if (rc != PA_ETOOLARGE) return rc;
+    // fits on the GPU at once and its merge tasks can hold every partition;
+    // otherwise partials, then pa_combine.
+    if (P <= pa::kMaxGridMerge) {
+        if (library_scratch &&
+            cudaMemsetAsync(counters, 0, static_cast<size_t>(Bq) * Hq * 8, stream) != cudaSuccess)
+            return PA_ECUDA;
+        rc = run_decode(true, out, lse, part_o, part_lse, q, k_cache, v_cache, cache, block_tables,
+                        max_blocks_per_seq, seq_lens, B, Hq, scale, P, status, stream, counters, nt,
+                        q_len, f8);
+        if (rc != PA_ETOOLARGE) return rc;
+    }
     rc = run_decode(true, nullptr, nullptr, part_o, part_lse, q, k_cache, v_cache, cache,
                     block_tables, max_blocks_per_seq, seq_lens, B, Hq, scale, P, status, stream,
                     nullptr, nt, q_len, f8);
@@ -579,6 +633,22 @@ int splitkv_common(void *out, float *lse, const void *q, const void *k_cache, co
     return e == cudaSuccess ? PA_OK : PA_ECUDA;
 }
 }  // namespace
+
+}  // extern "C"
+
+namespace pa {
+int decode_splitkv_library_scratch(void *out, float *lse, const void *q, const void *k_cache,
+                                   const void *v_cache, const pa_cache_desc &cache,
+                                   const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                   const int32_t *seq_lens, int32_t B, int32_t Hq, float scale,
+                                   int32_t num_splits, int32_t *status, cudaStream_t stream) {
+    return splitkv_common(out, lse, q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq,
+                          seq_lens, B, Hq, scale, num_splits, nullptr, 0, status, stream,
+                          NewTokens(), 1, nullptr, true);
+}
+}  // namespace pa
+
+extern "C" {
 
 int pa_decode_mq(void *out, float *lse, const void *q, int32_t q_len, const void *k_cache,
                  const void *v_cache, pa_cache_desc cache, const int32_t *block_tables,

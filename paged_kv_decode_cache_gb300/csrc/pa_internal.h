@@ -11,6 +11,10 @@ namespace pa {
 
 // Most partitions a split merge takes through one thread-block cluster.
 constexpr int kMaxClusterMerge = 16;
+// Most partitions the in-launch grid merge takes (its tasks hold up to 8 LSEs
+// per lane of a warp); a split with more partitions writes partials and is
+// merged by the separate combine kernel, which takes any count.
+constexpr int kMaxGridMerge = 256;
 
 // Everything a decode CTA needs besides the two tensor maps.
 struct DecodeParams {
@@ -83,6 +87,20 @@ cudaError_t launch_combine(void *out, float *lse, const float *part_o, const flo
 cudaError_t launch_cache_write(const void *k_new, const void *v_new, const int64_t *slots,
                                int64_t n, void *k_cache, void *v_cache, int64_t n_slots,
                                int row_bytes, int32_t *status, cudaStream_t stream);
+
+// Split-KV decode on the library's own scratch array (pa_decode_splitkv_noalloc):
+// the device address and size of that array on the current device and
+// context, looked up on first use (pa_noalloc.cu).  Returns PA_OK or a PA_E* code.
+int noalloc_scratch(void **addr, size_t *bytes);
+
+// pa_decode_splitkv with the library's scratch array as its workspace
+// (pa_api.cu): every argument is checked first, then the array is looked up and
+// the merge counters the call uses are cleared on `stream`.
+int decode_splitkv_library_scratch(void *out, float *lse, const void *q, const void *k_cache,
+                                   const void *v_cache, const pa_cache_desc &cache,
+                                   const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                   const int32_t *seq_lens, int32_t B, int32_t Hq, float scale,
+                                   int32_t num_splits, int32_t *status, cudaStream_t stream);
 
 cudaError_t launch_cache_write_fp8(const void *k_new, const void *v_new, const int64_t *slots,
                                    int64_t n, void *k_cache, void *v_cache, int64_t n_slots,

@@ -53,7 +53,7 @@ __device__ __forceinline__ int ld_acquire_gpu(const int *p) {
 // further block of 32 partitions is loaded while the previous one is summed.
 template <int D>
 __device__ __forceinline__ void merge_slice(const DecodeParams &p, int64_t row, int slice, int lane) {
-    constexpr int kMaxHeld = 8;  // LSEs per lane held in registers: P <= 256
+    constexpr int kMaxHeld = kMaxGridMerge / 32;  // LSEs per lane held in registers
     const int P = p.num_splits;
     const float *pl = p.part_lse + row * P;
     const float *po = p.part_o + row * P * D + slice * 32 + lane;
@@ -108,7 +108,7 @@ __device__ __forceinline__ void merge_slice(const DecodeParams &p, int64_t row, 
 // reduction per dim adds the lanes' sums.
 template <int D>
 __device__ __forceinline__ void merge_slice_wide(const DecodeParams &p, int64_t row, int slice, int lane) {
-    constexpr int kMaxHeld = 8;  // partitions per lane: P <= 256
+    constexpr int kMaxHeld = kMaxGridMerge / 32;  // partitions per lane
     const int P = p.num_splits;
     const float *pl = p.part_lse + row * P;
     const float *po = p.part_o + row * P * D + slice * 8;
@@ -171,6 +171,7 @@ __device__ __forceinline__ void merge_slice_wide(const DecodeParams &p, int64_t 
 // `sync` synchronises those threads; `flag` is a shared int.  Every CTA of a
 // group launches the same kernel, so all agree on kWarps and hence on who does
 // which task.
+// (The host launches this merge only for P <= kMaxGridMerge.)
 template <int D, int kWarps, typename Sync>
 __device__ void merge_split_group(const DecodeParams &p, int group, int part, int64_t row_first,
                                   int nrows, int per_block, int64_t stride, int *flag, int t,

@@ -23,6 +23,9 @@ from . import build as _build
 
 PA_OK, PA_EINVAL, PA_EUNSUPPORTED, PA_EWORKSPACE, PA_ECUDA = 0, -1, -2, -3, -4
 PA_STATUS_BAD_BLOCK, PA_STATUS_BAD_SLOT, PA_STATUS_BAD_SEQLEN, PA_STATUS_TIMEOUT = 1, 2, 4, 8
+PA_OPT_DECODE_KERNEL, PA_OPT_SPLIT_MERGE, PA_OPT_PDL = 0, 1, 2
+PA_KERNEL_AUTO, PA_KERNEL_CUDA_CORE, PA_KERNEL_TENSOR_CORE = 0, 1, 2
+PA_MERGE_AUTO, PA_MERGE_GRID = 0, 1
 
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "pa.h")
 
@@ -69,6 +72,8 @@ _SIGNATURES = {
     "pa_cache_write_fp8": ([_P, _P, _P, _I64, _P, _P, CacheDesc, _F32, _F32, _P, _P], ctypes.c_int),
     "pa_decode_splitkv_fp8": ([_P, _P, _P, _P, _P, CacheDesc, _F32, _F32, _P, _I32, _P, _I32, _I32,
                                _F32, _I32, _P, _SZ, _P, _P], ctypes.c_int),
+    "pa_set_option": ([_I32, _I32], ctypes.c_int),
+    "pa_get_option": ([_I32], ctypes.c_int),
     "pa_strerror": ([ctypes.c_int], ctypes.c_char_p),
     "pa_version": ([], ctypes.c_int),
 }
@@ -170,6 +175,18 @@ def pa_strerror(code: int) -> str:
 
 def pa_version() -> int:
     return lib().pa_version()
+
+
+def pa_set_option(option: int, value: int) -> None:
+    """Set a process-wide switch (PA_OPT_*): raises PAError on an unknown switch or value."""
+    _check("pa_set_option", lib().pa_set_option(option, value))
+
+
+def pa_get_option(option: int) -> int:
+    v = lib().pa_get_option(option)
+    if v < 0:
+        _check("pa_get_option", v)
+    return v
 
 
 def pa_choose_num_splits(B: int, Hq: int, Hkv: int, D: int, max_blocks_per_seq: int,

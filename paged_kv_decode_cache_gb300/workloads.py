@@ -69,6 +69,18 @@ class DecodeWorkload:
         elem = 1 if self.fp8 else 2
         return int(self.seq_lens.astype(np.int64).sum()) * 2 * self.Hkv * self.D * elem
 
+    def unique_kv_bytes(self) -> int:
+        """Bytes of K and V in distinct pool rows that attention reads: a block
+        shared by several sequences (a prefix-cache hit) counts once."""
+        elem = 1 if self.fp8 else 2
+        depth = {}   # rows of each physical block read by some sequence (its deepest reader)
+        for b in range(self.B):
+            L = int(self.seq_lens[b])
+            for j in range((L + self.block_size - 1) // self.block_size):
+                blk = int(self.block_tables[b, j])
+                depth[blk] = max(depth.get(blk, 0), min(self.block_size, L - j * self.block_size))
+        return sum(depth.values()) * 2 * self.Hkv * self.D * elem
+
     def qo_bytes(self) -> int:
         return 2 * self.B * self.q_len * self.Hq * self.D * 2
 

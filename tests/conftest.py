@@ -29,3 +29,36 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+_KERNELS = {"auto": 0, "cuda_core": 1, "tensor_core": 2}
+
+
+@pytest.fixture
+def use_kernel():
+    """Force a decode kernel ("auto", "cuda_core" or "tensor_core") through the
+    library's PA_OPT_DECODE_KERNEL switch; the previous value comes back after
+    the test."""
+    from paged_kv_decode_cache_gb300 import build, pa
+    build.build()
+    prev = pa.pa_get_option(pa.PA_OPT_DECODE_KERNEL)
+
+    def _set(kernel):
+        pa.pa_set_option(pa.PA_OPT_DECODE_KERNEL, _KERNELS[kernel])
+    yield _set
+    pa.pa_set_option(pa.PA_OPT_DECODE_KERNEL, prev)
+
+
+@pytest.fixture
+def merge_path():
+    """'cluster' (the default where P <= 16) or 'grid' (PA_OPT_SPLIT_MERGE =
+    PA_MERGE_GRID); the previous value comes back after the test."""
+    from paged_kv_decode_cache_gb300 import build, pa
+    build.build()
+    prev = pa.pa_get_option(pa.PA_OPT_SPLIT_MERGE)
+
+    def _set(path):
+        pa.pa_set_option(pa.PA_OPT_SPLIT_MERGE,
+                         pa.PA_MERGE_GRID if path == "grid" else pa.PA_MERGE_AUTO)
+    yield _set
+    pa.pa_set_option(pa.PA_OPT_SPLIT_MERGE, prev)

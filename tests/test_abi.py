@@ -82,8 +82,8 @@ def _units(B, Hq, Hkv, D):
 
 
 @pytest.mark.parametrize("B,Hq,Hkv,D,mb,bs,sms", SPLIT_CASES)
-def test_split_policy(lib, monkeypatch, B, Hq, Hkv, D, mb, bs, sms):
-    monkeypatch.delenv("PA_DECODE_KERNEL", raising=False)
+def test_split_policy(lib, use_kernel, B, Hq, Hkv, D, mb, bs, sms):
+    use_kernel("auto")
     P = pa.pa_choose_num_splits(B, Hq, Hkv, D, mb, bs, sms)
     lmax = mb * bs
     slots = _ctas_per_sm(Hq, Hkv, D) * sms
@@ -98,22 +98,22 @@ def test_split_policy(lib, monkeypatch, B, Hq, Hkv, D, mb, bs, sms):
         assert P == 1
 
 
-def test_split_policy_fills_small_batches(lib, monkeypatch):
-    monkeypatch.delenv("PA_DECODE_KERNEL", raising=False)
+def test_split_policy_fills_small_batches(lib, use_kernel):
+    use_kernel("auto")
     # one work unit (B=1, all 4 KV heads in one CTA) at 32k tokens: the split fills every SM
     P = pa.pa_choose_num_splits(1, 28, 4, 128, 2048, 16, 152)
     assert P >= 0.9 * 152
     # the CUDA-core kernel has one CTA per KV head and two CTAs per SM
-    monkeypatch.setenv("PA_DECODE_KERNEL", "cuda_core")
+    use_kernel("cuda_core")
     assert 4 * pa.pa_choose_num_splits(1, 28, 4, 128, 2048, 16, 152) >= 0.9 * 2 * 152
 
 
-def test_kernel_override_rejects_what_it_cannot_run(lib, monkeypatch):
-    monkeypatch.setenv("PA_DECODE_KERNEL", "tensor_core")
+def test_kernel_override_rejects_what_it_cannot_run(lib, use_kernel):
+    use_kernel("tensor_core")
     assert lib.pa_choose_num_splits(1, 8, 2, 64, 16, 16, 152) == pa.PA_EUNSUPPORTED   # D = 64
-    monkeypatch.setenv("PA_DECODE_KERNEL", "cuda_core")
+    use_kernel("cuda_core")
     assert lib.pa_choose_num_splits(1, 32, 2, 128, 16, 16, 152) == pa.PA_EUNSUPPORTED  # G = 16
-    monkeypatch.delenv("PA_DECODE_KERNEL")
+    use_kernel("auto")
     assert lib.pa_choose_num_splits(1, 32, 2, 128, 16, 16, 152) >= 1                   # tensor cores
     assert lib.pa_choose_num_splits(1, 64, 2, 128, 16, 16, 152) >= 1                   # G = 32
     assert lib.pa_choose_num_splits(1, 66, 2, 128, 16, 16, 152) == pa.PA_EUNSUPPORTED  # G = 33
@@ -205,8 +205,8 @@ def test_decode_step_rejects_bad_arguments(lib):
                               4, 0.125, 1, None, 0, None, None) == pa.PA_OK   # empty batch
 
 
-def test_mq_split_policy(lib, monkeypatch):
-    monkeypatch.delenv("PA_DECODE_KERNEL", raising=False)
+def test_mq_split_policy(lib, use_kernel):
+    use_kernel("auto")
     for args in ((8, 28, 4, 128, 256, 16, 152), (1, 28, 4, 128, 2048, 16, 152),
                  (256, 16, 8, 128, 128, 16, 152), (3, 12, 2, 128, 100, 16, 132)):
         B, Hq, Hkv, D, mb, bs, sms = args
@@ -225,14 +225,14 @@ def test_mq_split_policy(lib, monkeypatch):
         prev = P
 
 
-def test_mq_rejects_what_it_cannot_run(lib, monkeypatch):
-    monkeypatch.delenv("PA_DECODE_KERNEL", raising=False)
+def test_mq_rejects_what_it_cannot_run(lib, use_kernel):
+    use_kernel("auto")
     assert lib.pa_choose_num_splits_mq(2, 2, 8, 2, 64, 16, 16, 152) == pa.PA_EUNSUPPORTED   # D = 64
     assert lib.pa_choose_num_splits_mq(2, 0, 8, 2, 128, 16, 16, 152) == pa.PA_EINVAL
     assert lib.pa_choose_num_splits_mq(2, 1, 8, 2, 64, 16, 16, 152) >= 1                    # decode
-    monkeypatch.setenv("PA_DECODE_KERNEL", "cuda_core")
+    use_kernel("cuda_core")
     assert lib.pa_choose_num_splits_mq(2, 2, 8, 2, 128, 16, 16, 152) == pa.PA_EUNSUPPORTED
-    monkeypatch.delenv("PA_DECODE_KERNEL")
+    use_kernel("auto")
     d = _desc(d=128)
     for q_len in (0, -3, 70000):
         rc = lib.pa_decode_mq(FAKE, None, FAKE, q_len, FAKE, FAKE, d, FAKE, 7, FAKE, 4, 4, 0.1, 1,
@@ -246,8 +246,8 @@ def test_mq_rejects_what_it_cannot_run(lib, monkeypatch):
     assert rc == pa.PA_EUNSUPPORTED     # D = 64
 
 
-def test_fp8_rejects_bad_arguments(lib, monkeypatch):
-    monkeypatch.delenv("PA_DECODE_KERNEL", raising=False)
+def test_fp8_rejects_bad_arguments(lib, use_kernel):
+    use_kernel("auto")
     d = _desc(d=128)
     for ks, vs in ((0.0, 1.0), (1.0, -1.0), (float("nan"), 1.0), (1.0, float("inf"))):
         assert lib.pa_cache_write_fp8(FAKE, FAKE, FAKE, 3, FAKE, FAKE, d, ks, vs, None, None) == pa.PA_EINVAL
@@ -257,7 +257,7 @@ def test_fp8_rejects_bad_arguments(lib, monkeypatch):
                                      FAKE, 4, 4, 0.1, 1, None, 0, None, None) == pa.PA_EUNSUPPORTED
     assert lib.pa_decode_splitkv_fp8(FAKE, None, FAKE, FAKE, FAKE, d, 1.0, 1.0, FAKE, 7, FAKE, 4, 4,
                                      0.1, 3, None, 0, None, None) == pa.PA_EWORKSPACE
-    monkeypatch.setenv("PA_DECODE_KERNEL", "cuda_core")
+    use_kernel("cuda_core")
     assert lib.pa_decode_splitkv_fp8(FAKE, None, FAKE, FAKE, FAKE, d, 1.0, 1.0, FAKE, 7, FAKE, 4, 4,
                                      0.1, 1, None, 0, None, None) == pa.PA_EUNSUPPORTED
     assert lib.pa_cache_write_fp8(FAKE, FAKE, FAKE, 0, FAKE, FAKE, d, 1.0, 1.0, None, None) == pa.PA_OK
@@ -286,3 +286,66 @@ def test_wrappers_run_on_their_tensors_device():
                  "pa_decode_splitkv", "pa_decode_step", "pa_decode_mq", "pa_decode_cascade",
                  "pa_cache_write_fp8", "pa_decode_splitkv_fp8", "pa_decode_splitkv_noalloc"):
         assert getattr(pa, name).__wrapped__.__name__ == name
+
+
+def test_options_set_get_and_reject(lib):
+    prev = [pa.pa_get_option(o) for o in (pa.PA_OPT_DECODE_KERNEL, pa.PA_OPT_SPLIT_MERGE,
+                                          pa.PA_OPT_PDL)]
+    try:
+        for opt, values in ((pa.PA_OPT_DECODE_KERNEL, (0, 1, 2)), (pa.PA_OPT_SPLIT_MERGE, (0, 1)),
+                            (pa.PA_OPT_PDL, (0, 1))):
+            for v in values:
+                pa.pa_set_option(opt, v)
+                assert pa.pa_get_option(opt) == v
+            assert lib.pa_set_option(opt, max(values) + 1) == pa.PA_EINVAL
+            assert lib.pa_set_option(opt, -1) == pa.PA_EINVAL
+        assert lib.pa_set_option(3, 0) == pa.PA_EINVAL
+        assert lib.pa_get_option(3) == pa.PA_EINVAL
+        # the split policy follows the switch, not the environment
+        pa.pa_set_option(pa.PA_OPT_DECODE_KERNEL, pa.PA_KERNEL_CUDA_CORE)
+        assert lib.pa_choose_num_splits(1, 32, 2, 128, 16, 16, 152) == pa.PA_EUNSUPPORTED
+        pa.pa_set_option(pa.PA_OPT_DECODE_KERNEL, pa.PA_KERNEL_AUTO)
+        assert lib.pa_choose_num_splits(1, 32, 2, 128, 16, 16, 152) >= 1
+    finally:
+        for o, v in zip((pa.PA_OPT_DECODE_KERNEL, pa.PA_OPT_SPLIT_MERGE, pa.PA_OPT_PDL), prev):
+            pa.pa_set_option(o, v)
+
+
+def test_options_start_from_the_environment_read_once(lib, tmp_path):
+    """In a fresh process the switches start from PA_DECODE_KERNEL, PA_SPLIT_MERGE
+    and PA_PDL; changing the environment afterwards changes nothing."""
+    import os
+    import sys
+    code = (
+        "import os, sys; sys.path.insert(0, %r)\n"
+        "from paged_kv_decode_cache_gb300 import pa\n"
+        "a = [pa.pa_get_option(o) for o in (0, 1, 2)]\n"
+        "os.environ['PA_DECODE_KERNEL'] = 'tensor_core'; os.environ['PA_PDL'] = '1'\n"
+        "b = [pa.pa_get_option(o) for o in (0, 1, 2)]\n"
+        "print(a, b)\n" % os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    env = dict(os.environ, PA_DECODE_KERNEL="cuda_core", PA_SPLIT_MERGE="grid", PA_PDL="0")
+    out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                         check=True).stdout.strip()
+    assert out == "[1, 1, 0] [1, 1, 0]"
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(desc=_desc(d=0)), pa.PA_EINVAL),
+    (dict(desc=_desc(d=-1)), pa.PA_EINVAL),
+    (dict(desc=_desc(d=256)), pa.PA_EUNSUPPORTED),
+    (dict(Hq=5), pa.PA_EINVAL),                 # Hq % Hkv != 0
+    (dict(q=None), pa.PA_EINVAL),
+    (dict(out=None), pa.PA_EINVAL),
+    (dict(splits=-1), pa.PA_EINVAL),
+    (dict(splits=70000), pa.PA_EUNSUPPORTED),
+    (dict(B=-1), pa.PA_EINVAL),
+])
+def test_noalloc_rejects_bad_arguments_before_touching_its_array(lib, kw, code):
+    """The allocation-free entry point checks its arguments exactly as
+    pa_decode_splitkv does, before it looks up or clears its built-in array
+    (no CUDA call is made here: this machine may have no GPU)."""
+    a = dict(out=FAKE, q=FAKE, desc=_desc(), B=4, Hq=4, splits=4)
+    a.update(kw)
+    rc = lib.pa_decode_splitkv_noalloc(a["out"], None, a["q"], FAKE, FAKE, a["desc"], FAKE, 7, FAKE,
+                                       a["B"], a["Hq"], 0.125, a["splits"], None, None)
+    assert rc == code

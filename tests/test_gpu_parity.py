@@ -7,7 +7,7 @@ import torch
 
 import oracle
 from gpu_util import (Dev, assert_close, assert_lse_close, bf16_dev_to_f64, oracle_after_write,
-                      oracle_rows, sample_rows, u16_to_dev_bf16)
+                      u16_to_dev_bf16)
 from paged_kv_decode_cache_gb300 import pa
 from paged_kv_decode_cache_gb300 import workloads as W
 
@@ -29,26 +29,6 @@ def kernels_for(Hq, Hkv, D):
     if D == 128 and G <= 32:
         ks.append("tensor_core")
     return ks
-
-
-@pytest.fixture
-def use_kernel(monkeypatch):
-    def _set(kernel):
-        monkeypatch.setenv("PA_DECODE_KERNEL", kernel)
-    yield _set
-    monkeypatch.delenv("PA_DECODE_KERNEL", raising=False)
-
-
-@pytest.fixture
-def merge_path(monkeypatch):
-    """'cluster' (the default where P <= 16) or 'grid' (PA_SPLIT_MERGE=grid)."""
-    def _set(path):
-        if path == "grid":
-            monkeypatch.setenv("PA_SPLIT_MERGE", "grid")
-        else:
-            monkeypatch.delenv("PA_SPLIT_MERGE", raising=False)
-    yield _set
-    monkeypatch.delenv("PA_SPLIT_MERGE", raising=False)
 
 
 # ---------------------------------------------------------------- cache write
@@ -166,6 +146,27 @@ def test_fused_merge_many_partitions(lens, P, use_kernel):
         assert dev.status_value() == 0
 
 
+@pytest.mark.parametrize("Hkv", [1, 2])
+@pytest.mark.parametrize("P", [257, 300])
+def test_more_partitions_than_the_in_launch_merge_holds(P, Hkv, use_kernel):
+    """More than 256 partitions of one sequence (CUDA-core kernel, D = 64, whose
+    small CTAs let such a grid be resident at once): the in-launch merge holds
+    at most 256 partitions per row, so these partials are merged by the
+    combine kernel instead; no partition may be dropped."""
+    use_kernel("cuda_core")
+    L = 16 * P - 5                       # 16-token partitions, the last one ragged
+    w = _small(2 * Hkv, Hkv, 64, 16, (L,), seed=P + Hkv)
+    kc, vc = oracle_after_write(w)
+    ref, ref_lse = oracle.decode(w.q, kc, vc, w.block_tables, w.seq_lens, w.scale)
+    dev = Dev(w)
+    dev.write()
+    assert pa.pa_partition_tokens(w.max_blocks, w.block_size, P) == 16
+    so, sl, _ = dev.splitkv(P)
+    assert_close(bf16_dev_to_f64(so), ref, f"splitkv P={P}")
+    assert_lse_close(sl.cpu().double().numpy(), ref_lse, f"splitkv P={P}")
+    assert dev.status_value() == 0
+
+
 def test_combine_matches_oracle():
     g = torch.Generator().manual_seed(3)
     B, Hq, P, D = 3, 5, 9, 128
@@ -189,13 +190,20 @@ FULL = ["tiny", "qwen2.5-1.5b-B1", "qwen2.5-1.5b-B8", "qwen2.5-7b-bs16", "qwen2.
 
 @pytest.mark.parametrize("name", FULL)
 def test_workload_full_size(name, use_kernel):
-    """The bench's launch configuration (auto kernel, auto split) plus the unsplit
-    call, then each kernel forced, on the full-size workload; all rows for small
-    batches, a seeded sample otherwise."""
+    """The bench's launch configuration (the fused step: auto kernel, auto split),
+    then split and unsplit decode with each kernel forced, on the full-size
+    workload, every (b, h) row against the oracle."""
     w = W.WORKLOADS[name]()
     kc, vc = oracle_after_write(w)
-    rb, rh = sample_rows(w, 160, seed=len(name))
-    ref, ref_lse = oracle_rows(w, kc, vc, rb, rh)
+    ref, ref_lse = oracle.decode(w.q, kc, vc, w.block_tables, w.seq_lens, w.scale)
+    fused = Dev(w)
+    out_f, lse_f, Pf = fused.step(0)
+    assert fused.status_value() == 0
+    gk, gv = fused.pools()
+    assert np.array_equal(gk, kc) and np.array_equal(gv, vc), f"{name}: pools after the step"
+    assert_close(bf16_dev_to_f64(out_f), ref, f"{name} step P={Pf}")
+    assert_lse_close(lse_f.cpu().double().numpy(), ref_lse, f"{name} step P={Pf}")
+    del fused
     dev = Dev(w)
     dev.write()
     for kernel in ["auto"] + kernels_for(w.Hq, w.Hkv, w.D):
@@ -204,8 +212,8 @@ def test_workload_full_size(name, use_kernel):
         out_u, lse_u = dev.decode()
         assert dev.status_value() == 0
         for tag, o, l in (("splitkv", out_s, lse_s), ("decode", out_u, lse_u)):
-            assert_close(bf16_dev_to_f64(o)[rb, rh], ref, f"{name} {tag} {kernel} P={P}")
-            assert_lse_close(l.cpu().double().numpy()[rb, rh], ref_lse, f"{name} {tag} {kernel}")
+            assert_close(bf16_dev_to_f64(o), ref, f"{name} {tag} {kernel} P={P}")
+            assert_lse_close(l.cpu().double().numpy(), ref_lse, f"{name} {tag} {kernel}")
 
 
 # ------------------------------------------------------ bit-exact invariants
@@ -470,6 +478,26 @@ def test_mq_chunk_of_64_queries():
         out, lse, _ = dev.mq(P)
         assert_close(bf16_dev_to_f64(out), ref, f"chunk P={P}")
         assert_lse_close(lse.cpu().double().numpy(), ref_lse, f"chunk P={P}")
+
+
+@pytest.mark.parametrize("B", [1, 8])
+def test_mq_chunk_of_512_queries_qwen25_1p5b(B):
+    """A 512-token chunked-prefill chunk per sequence on the Qwen2.5-1.5B-shaped
+    layer (Hq = 12, Hkv = 2, the context including the chunk ~ U[512, 2048]):
+    auto split and unsplit, every row against the oracle."""
+    lens = W._uniform_lens(2002 + B, B, 512, 2048)
+    nb = sum((L + 15) // 16 for L in lens) + 8
+    w = W.make_workload("chunk512", B=B, Hq=12, Hkv=2, D=128, block_size=16, seq_lens=lens,
+                        num_blocks=nb, max_blocks=128, seed=512 + B, q_len=512)
+    kc, vc = oracle_after_write(w)
+    ref, ref_lse = oracle.decode_mq(w.q, kc, vc, w.block_tables, w.seq_lens, w.scale)
+    dev = Dev(w)
+    dev.write()
+    for P in (0, 1):
+        out, lse, Pu = dev.mq(P)
+        assert_close(bf16_dev_to_f64(out), ref, f"chunk512 B={B} P={Pu}")
+        assert_lse_close(lse.cpu().double().numpy(), ref_lse, f"chunk512 B={B} P={Pu}")
+    assert dev.status_value() == 0
 
 
 @pytest.mark.parametrize("name", ["qwen2.5-1.5b-B8-spec4", "qwen2.5-7b-bs16-spec4",

@@ -102,3 +102,16 @@ def test_fp8_variant_codes_and_scales():
         # codes are subnormal with an absolute step of 2^-9 (times the scale)
         assert bool((err <= x.abs() * 2.0 ** -4 + scale * 2.0 ** -10 + 1e-12).all())
     assert w.name.endswith("-fp8") and w.fp8
+
+
+def test_unique_bytes_count_a_shared_prefix_once():
+    """Unique KV bytes: the prefix blocks every sequence shares count once; with
+    no sharing they equal the logical bytes."""
+    w = W.make_workload("u", B=3, Hq=4, Hkv=2, D=16, block_size=16, seq_lens=[40, 33, 17],
+                        num_blocks=12, seed=1, shared_prefix_blocks=1, write_new=False)
+    row = 2 * w.Hkv * w.D * 2
+    assert w.kv_bytes() == (40 + 33 + 17) * row
+    assert w.unique_kv_bytes() == (16 + (40 - 16) + (33 - 16) + (17 - 16)) * row
+    w = W.make_workload("u", B=2, Hq=4, Hkv=2, D=16, block_size=16, seq_lens=[40, 5],
+                        num_blocks=6, seed=1, write_new=False)
+    assert w.unique_kv_bytes() == w.kv_bytes()

@@ -67,3 +67,17 @@ def test_noalloc_rejects_splits_beyond_the_builtin_array():
         pa.pa_decode_splitkv_noalloc(out, None, dev.q, dev.k_cache, dev.v_cache,
                                      dev.block_tables, dev.seq_lens, w.scale, num_splits=P)
     assert e.value.code == pa.PA_EWORKSPACE
+
+
+def test_noalloc_unsplit_call_equals_pa_decode():
+    """num_splits = 1 does not use the built-in array: the result is pa_decode's, bit for bit."""
+    w = W.make_workload("one", B=3, Hq=28, Hkv=4, D=128, block_size=16, seq_lens=[300, 17, 1],
+                        num_blocks=30, seed=4)
+    dev = Dev(w)
+    dev.write()
+    ref, ref_lse = dev.decode()
+    got, got_lse = _noalloc(dev, 1)
+    torch.cuda.synchronize()
+    assert torch.equal(got, ref) and torch.equal(got_lse, ref_lse)
+    assert dev.status_value() == 0
+
