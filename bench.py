@@ -7,15 +7,17 @@ log-sum-exp combine.  Inputs are seeded synthetic tensors shaped like the
 workload named by --workload (default: the Qwen2.5-7B-shaped layer, B=8,
 Hq=28, Hkv=4, D=128, every L=4096, 16-token blocks).
 
-Timing: W warm-up steps, then exactly K steps between a barrier and a
-device synchronise on each side, timed with CUDA events on the launching
-stream; every step is replayed from a CUDA graph (one graph per pool
-replica), and consecutive steps rotate over enough copies of the KV pool that
-the data a step reads was evicted from the 129 MB L2 before it is read again.
-A step that is one launch (the default fused step) has its kernel duration
-taken as the timed region over the launches; other steps sample the decode
-kernel with events recorded inside the graphs (one step per graph copy, since
-event nodes slow the steps around them).  Prints one JSON line (rank 0).
+Timing: every graph of the timed region replayed once and W warm-up steps,
+then exactly K steps between a barrier and a device synchronise on each side,
+timed with CUDA events on the launching stream.  The K steps are replayed
+from CUDA graphs that hold exactly those steps, queued while the GPU spins
+for a head start, and consecutive steps rotate over enough copies of the KV
+pool that the data a step reads was evicted from the 129 MB L2 before it is
+read again.  A step that is one launch (the default fused step) has its
+kernel duration taken as the timed region over the launches; other steps
+sample the decode kernel with events recorded around it in separate graphs
+after the timed region.  The line's "configs" object measures every config
+of the metric (see measure_configs).  Prints one JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
@@ -411,16 +413,16 @@ def run_ours(args, world, rank, local):
         if ev1 is not None:
             ev1.record(stream)
 
-    fused = not (args.unfused or mq or fp8 or cascade)
-    launches_per_step = 4 if cascade else 1 if fused else 2   # cascade: write, prefix, suffix, combine
-    # CUDA graphs of S consecutive steps (cycling over the pool replicas), NG
-    # copies.  Event nodes in a graph cost the steps around them several us of
-    # launch gaps, so only the first step of each graph copy carries a pair of
-    # events around the decode kernel: a sample of its duration measured inside
-    # the timed region.  Step i of the timed loop is step i % S of graph copy
-    # (i // S) % NG.  A step that is a single launch (the fused step) is timed
-    # more exactly by the whole region: its average launch duration is the
-    # region's time over the launches, gaps included.
+    launches_per_step = (4 if cascade else 2 if (args.unfused or mq or fp8) else 1)
+    # The timed region replays CUDA graphs that hold exactly the K timed steps
+    # (consecutive steps cycle over the pool replicas): one graph when K <= 1024,
+    # else K // 1024 replays of a 1024-step graph and one graph of the rest.  A
+    # step that is a single launch (the fused step) is timed by the whole
+    # region: its average launch duration is the region's time over the
+    # launches, gaps included.  Other steps sample the decode kernel's duration
+    # after the timed region, from NG graphs of S steps whose first step carries
+    # a pair of events around the decode launch (event nodes cost the steps
+    # around them several us of launch gaps, so they stay out of the region).
     S = R * max(1, math.ceil(16 / R))
     NG = 8
     try:
@@ -433,33 +435,28 @@ def run_ours(args, world, rank, local):
             step(r)
     stream.synchronize()
 
-    def capture(steps):
-        evs = [(mk(), mk()) if (mk and i == 0) else (None, None) for i in range(len(steps))]
+    def capture(n, events=False):
+        evs = [(mk(), mk()) if (events and mk and i == 0) else (None, None) for i in range(n)]
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            for r, (e0, e1) in zip(steps, evs):
-                step(r, e0, e1)
+            for k, (e0, e1) in enumerate(evs):
+                step(k % R, e0, e1)
         return g, evs
 
-    full = [capture([k % R for k in range(S)]) for _ in range(NG)]
-    single = [capture([r]) for r in range(R)]
-    n_full, n_rem = divmod(args.steps, S)
+    C = min(args.steps, 1024)
+    timed = [capture(C)[0]] * (args.steps // C)
+    if args.steps % C:
+        timed.append(capture(args.steps % C)[0])
+    warm = capture(max(1, min(args.warmup, 1024)))[0]
 
-    def run_steps(n_full_graphs, n_single, offset=0):
-        with torch.cuda.stream(stream):
-            for j in range(n_full_graphs):
-                full[(offset + j) % NG][0].replay()
-            for r in range(n_single):
-                single[r % R][0].replay()
-
-    # Every graph the timed loop replays runs once first (its first replay
-    # uploads it), then the W warm-up steps; the timed region holds only
-    # steady-state steps whatever W is.
+    # Every graph of the timed region runs once first (its first replay uploads
+    # it), then the W warm-up steps: the timed region holds only steady-state
+    # steps whatever K and W are.
     with torch.cuda.stream(stream):
-        for g, _ in full + single:
+        for g in {id(g): g for g in timed}.values():
             g.replay()
-    wf, wr = divmod(args.warmup, S)
-    run_steps(wf, wr)
+        for _ in range(max(1, math.ceil(args.warmup / 1024))):
+            warm.replay()
     stream.synchronize()
     barrier(world)
     torch.cuda.synchronize()
@@ -470,17 +467,26 @@ def run_ours(args, world, rank, local):
             # the GPU idles here while the host queues the timed replays, so the
             # region measures the GPU's steps, not the host's submission latency
             torch.cuda._sleep(GPU_HEADSTART_CYCLES)
-        t_start.record(stream)
-        run_steps(n_full, n_rem)
-        t_end.record(stream)
+            t_start.record(stream)
+            for g in timed:
+                g.replay()
+            t_end.record(stream)
         t_end.synchronize()
     torch.cuda.synchronize()
     barrier(world)
     elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
     clocks = clk.summary()
     kern_ms = []
-    if mk and n_full:
-        for g, evs in full[:min(NG, n_full)]:
+    fused = not (args.unfused or mq or fp8 or cascade)
+    if mk and not fused:
+        samples = [capture(S, events=True) for _ in range(NG)]
+        with torch.cuda.stream(stream):
+            for g, _ in samples:
+                g.replay()
+            for g, _ in samples:
+                g.replay()
+        stream.synchronize()
+        for g, evs in samples:
             kern_ms += [e0.elapsed_time(e1) for e0, e1 in evs if e0 is not None]
     kern_ms_sampled = statistics.mean(kern_ms) if kern_ms else None
 
