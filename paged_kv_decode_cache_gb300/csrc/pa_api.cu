@@ -296,8 +296,20 @@ pa::DecodeParams base_params(const void *q, const pa_cache_desc &c, const int32_
     return p;
 }
 
+// Multi-query calls with more query columns per KV head than the decode
+// kernel holds in one CTA (q_len * G > 32) run the prefill-shaped kernel,
+// whose CTAs take 128 query rows each and read each KV block once per tile.
+bool prefill_shape(int G, int q_len) {
+    return q_len > 1 && static_cast<int64_t>(q_len) * G > kMaxGroupTc;
+}
+int prefill_positions_per_tile(int G) { return pa::kPrefillRows / G; }
+int64_t prefill_tiles(int G, int q_len) {
+    const int qpt = prefill_positions_per_tile(G);
+    return (q_len + qpt - 1) / qpt;
+}
+
 // Query positions per tensor-core CTA for q_len queries of G heads each: as
-// many as fit the kernel's column limit (G * positions <= 16).
+// many as fit the kernel's column limit (G * positions <= 32).
 int queries_per_cta(int G, int q_len) {
     if (q_len <= 1) return 1;
     return std::min(q_len, std::max(1, kMaxGroupTc / G));
@@ -381,7 +393,18 @@ int run_decode(bool split, void *out, float *lse, float *part_o, float *part_lse
     p.v_pool = static_cast<uint16_t *>(const_cast<void *>(v_cache));
     CUtensorMap kmap, vmap;
     cudaError_t e;
-    if (k == Kernel::kTensorCore) {
+    if (k == Kernel::kTensorCore && !f8 && !nt.k_new && prefill_shape(G, q_len) &&
+        p.chunk <= pa::kPrefillMaxTiles * 16) {
+        // queries on the MMA's M side; split partials are merged by the combine kernel
+        if (counters) return PA_ETOOLARGE;
+        p.q_per_cta = prefill_positions_per_tile(G);
+        p.cluster_merge = 0;
+        if (prefill_tiles(G, q_len) * c.num_kv_heads > 65535) return PA_EUNSUPPORTED;
+        rc = make_kv_map_heads(&kmap, k_cache, c, 1);
+        if (!rc) rc = make_kv_map_heads(&vmap, v_cache, c, 1);
+        if (rc) return rc;
+        e = pa::launch_prefill_tc(kmap, vmap, p, B, G, stream);
+    } else if (k == Kernel::kTensorCore) {
         int HC = 1, GP = 1;
         if (!tc_shape(G * qpc, c.num_kv_heads, &HC, &GP)) return PA_EUNSUPPORTED;
         p.head_groups = c.num_kv_heads / HC;
@@ -505,7 +528,9 @@ int pa_choose_num_splits_mq(int32_t B, int32_t q_len, int32_t Hq, int32_t Hkv, i
     int rc = pick_kernel(G * qpc, D, &k);
     if (rc) return rc;
     if (q_len > 1 && k != Kernel::kTensorCore) return PA_EUNSUPPORTED;
-    const int64_t units = units_per_split(k, B, G, Hkv, qpc, (q_len + qpc - 1) / qpc);
+    const bool prefill = k == Kernel::kTensorCore && prefill_shape(G, q_len);
+    const int64_t units = prefill ? static_cast<int64_t>(B) * Hkv * prefill_tiles(G, q_len)
+                                  : units_per_split(k, B, G, Hkv, qpc, (q_len + qpc - 1) / qpc);
     const int64_t slots = static_cast<int64_t>(sm_count) * ctas_per_sm(k);
     int64_t P = slots / units;  // largest P whose grid still fits one wave
     const int64_t lmax = static_cast<int64_t>(max_blocks_per_seq) * block_size;
@@ -514,6 +539,8 @@ int pa_choose_num_splits_mq(int32_t B, int32_t q_len, int32_t Hq, int32_t Hkv, i
     if (P > p_by_tiles) P = p_by_tiles;
     if (P > kMaxSplits) P = kMaxSplits;
     if (P < 1) P = 1;
+    // the prefill-shaped kernel keeps a partition's tiles in shared memory
+    if (prefill) P = std::max<int64_t>(P, (tiles + pa::kPrefillMaxTiles - 1) / pa::kPrefillMaxTiles);
     // Drop partitions that the rounding of the chunk to whole tiles leaves empty.
     const int chunk = pa_partition_tokens(max_blocks_per_seq, block_size, static_cast<int>(P));
     P = (lmax + chunk - 1) / chunk;

@@ -116,6 +116,13 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
     return pol;
 }
 
+// L2 policy for data that other CTAs read again soon (no eviction preference).
+__device__ __forceinline__ uint64_t l2_evict_normal_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 // 4-D tiled TMA load of one box into shared memory, completing on `bar`.
 __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, int c0, int c1,
                                             int c2, int c3, uint64_t *bar, uint64_t policy) {

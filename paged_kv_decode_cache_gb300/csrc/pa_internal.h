@@ -11,6 +11,13 @@ namespace pa {
 
 // Most partitions a split merge takes through one thread-block cluster.
 constexpr int kMaxClusterMerge = 16;
+// Multi-query calls whose query positions times group size exceed the decode
+// kernel's 32 MMA columns per KV head take the prefill-shaped kernel
+// (pa_prefill_tc.cu): 128 query rows (position, group member) per CTA, each
+// CTA's token range at most kPrefillMaxTiles 16-token tiles.
+constexpr int kPrefillRows = 128;
+constexpr int kPrefillMaxTiles = 2048;
+
 // Most partitions the in-launch grid merge takes (its tasks hold up to 8 LSEs
 // per lane of a warp); a split with more partitions writes partials and is
 // merged by the separate combine kernel, which takes any count.
@@ -80,6 +87,12 @@ struct DecodeParams {
 // CUDA-core decode kernel launch (pa_decode_cc_d*.cu).  Returns a cudaError_t.
 cudaError_t launch_decode_cc(int D, int G, const CUtensorMap &kmap, const CUtensorMap &vmap,
                              const DecodeParams &p, int B, cudaStream_t stream);
+
+// Prefill-shaped multi-query kernel (pa_prefill_tc.cu): grid (num_splits,
+// query tiles x Hkv, B); p.q_per_cta query positions per tile; writes out/lse,
+// or fp32 partials when p.split (no in-launch merge).
+cudaError_t launch_prefill_tc(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParams &p,
+                              int B, int G, cudaStream_t stream);
 
 cudaError_t launch_combine(void *out, float *lse, const float *part_o, const float *part_lse,
                            int rows, int P, int D, cudaStream_t stream);

@@ -1,0 +1,467 @@
+// Multi-query paged attention with the queries on the MMA's M side, for
+// chunks of many new tokens per sequence (chunked prefill of a prompt, a
+// long run of new tokens) and for many sequences' queries over one shared
+// prefix (the cascade's prefix pass).  Head dim 128, tensor cores (tcgen05).
+//
+// One CTA per (partition p, query tile, KV head g, sequence b).  A query tile
+// is 128 MMA rows r = (query position qi0 + r / G, group member r % G): up to
+// 128 / G consecutive query positions with all G query heads of KV head g, so
+// the CTA reads each KV block of its range once for 128 query rows (the decode
+// kernel, with queries as MMA columns, holds at most 32 columns per head).
+// The CTA streams its token range in chunks of T = 64 tokens (four 16-token
+// tiles through the block table):
+//
+//   QK:  S[128 r, 64 t] = Q[128 r, 128 d] . K_chunk^T[128 d, 64 t]
+//        A = the query tile (K-major, 128-byte swizzle), B = the K chunk as
+//        TMA lands it ([64 t][128 d], K-major).
+//   PV:  O[128 r, 128 d] += P[128 r, 64 t] . V_chunk[64 t, 128 d]
+//        A = p written by the softmax threads (K-major), B = the V chunk as
+//        TMA lands it, read MN-major (no transpose).  p is a bf16 pair
+//        hi + lo carrying it to about 2^-17 relative (two MMAs per chunk).
+//
+// S (two buffers of 64 columns) and O (128 columns) live in TMEM, lane = row
+// r.  Warps 0-3 (softmax, thread = row r) load their S row, mask keys past the
+// range, past the row's causal position or in tiles not loaded, keep a
+// per-row reference max that moves only when a score exceeds it by more than
+// 2^8 (the warp then rescales its rows of O in TMEM once the previous PV has
+// finished), and write the hi/lo rows of P; the epilogue normalises O and
+// writes bf16 rows (or fp32 partials with the range split) by bulk copies.
+// Warp 4 issues QK, warp 7 issues PV; warps 5 and 6 stream K and V through
+// 3-stage rings of 16 KB, one TMA box per 16-token tile and 64-element half.
+// A tile past the range or with a bad block id is loaded from a coordinate
+// past the pool, which fills the box with zeros.  Every wait is bounded.
+#include <cuda_bf16.h>
+
+#include <atomic>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+#include "pa_tcgen05.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int kPfRows = 128;                     // query rows per CTA (M of both MMAs)
+constexpr int kPfT = 64;                         // tokens per chunk (N of QK, K of PV)
+constexpr int kPfThreads = 256;
+constexpr int kPfQkWarp = 4, kPfTmaKWarp = 5, kPfTmaVWarp = 6, kPfPvWarp = 7;
+constexpr int kPfNK = 3, kPfNV = 3;              // K and V stages
+constexpr int kPfNS = 2;                         // S buffers in TMEM
+constexpr int kPfNP = 2;                         // P buffers (hi + lo) in shared memory
+constexpr int kPfTilesPerChunk = kPfT / kTile;   // 4
+constexpr int kPfHalf = kPfT * kSubBytes;        // one 64-element half of a chunk: 8 KB
+constexpr int kPfStage = 2 * kPfHalf;            // 16 KB
+constexpr int kPfBox = kTile * kSubBytes;        // one TMA box: 16 rows x 128 B
+constexpr int kPfQHalf = kPfRows * kSubBytes;    // 16 KB
+constexpr int kPfPPart = kPfRows * kPfT * 2;     // [128 rows][64 tokens] bf16 = 16 KB
+constexpr int kPfPBuf = 2 * kPfPPart;            // hi, then lo
+constexpr float kPfLazyTau = 8.0f;               // log2 headroom before a row's reference max moves
+
+constexpr int kPfKOff = 0;
+constexpr int kPfVOff = kPfKOff + kPfNK * kPfStage;
+constexpr int kPfQOff = kPfVOff + kPfNV * kPfStage;
+constexpr int kPfPOff = kPfQOff + 2 * kPfQHalf;
+constexpr int kPfRowsOff = kPfPOff + kPfNP * kPfPBuf;
+constexpr int kPfBarOff = kPfRowsOff + kPrefillMaxTiles * 4;
+constexpr int kPfNumBars = 2 * kPfNK + 2 * kPfNV + 2 * kPfNS + 2 * kPfNP;
+constexpr int kPfMiscOff = kPfBarOff + kPfNumBars * 8;
+constexpr int kPfSmemBytes = kPfMiscOff + 16 + 1024;   // + room to align the base to 1024
+constexpr uint32_t kPfTmemCols = 256;                  // S: 2 x 64 columns, then O: 128
+constexpr int kPfColO = kPfNS * kPfT;
+static_assert(kPfColO + 128 <= static_cast<int>(kPfTmemCols), "TMEM columns");
+static_assert(kPfSmemBytes <= 227 * 1024, "shared memory");
+static_assert(kPfNP * kPfPBuf >= kPfRows * 128 * 4, "the epilogue stages fp32 rows in the P buffers");
+static_assert(kPfStage % 1024 == 0 && kPfQHalf % 1024 == 0 && kPfPPart % 1024 == 0, "swizzle atoms");
+
+__global__ void __launch_bounds__(kPfThreads, 1)
+prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                  const DecodeParams p, int G) {
+    constexpr int D = 128;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~uintptr_t(1023));
+    uint8_t *kring = smem + kPfKOff;
+    uint8_t *vring = smem + kPfVOff;
+    uint8_t *qs = smem + kPfQOff;
+    uint8_t *ps = smem + kPfPOff;
+    int *tile_row = reinterpret_cast<int *>(smem + kPfRowsOff);  // pool row of each 16-token tile, -1: none
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kPfBarOff);
+    uint64_t *kfull = bars, *kempty = kfull + kPfNK, *vfull = kempty + kPfNK, *vempty = vfull + kPfNV;
+    uint64_t *sdone = vempty + kPfNV, *sfree = sdone + kPfNS, *pready = sfree + kPfNS;
+    uint64_t *pfree = pready + kPfNP;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kPfMiscOff);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kPfMiscOff + 4);
+
+    // Launched with programmatic stream serialization: no global memory is
+    // touched before the previous kernel in the stream has completed.
+    griddep_wait();
+    griddep_launch_dependents();
+
+    const int part = blockIdx.x, b = blockIdx.z;
+    const int Hkv = p.num_kv_heads, Hq = p.num_q_heads;
+    const int g = blockIdx.y % Hkv;
+    const int qi0 = static_cast<int>(blockIdx.y / Hkv) * p.q_per_cta;  // the tile's first query position
+    const int nq = min(p.q_per_cta, p.q_len - qi0);
+    const int nrows = nq * G;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int bs = p.block_size;
+    const int lmax = p.max_blocks * bs;
+    int L = p.seq_len_const >= 0 ? p.seq_len_const : p.seq_lens[b] - p.seq_len_offset;
+    if (L < 0 || L > lmax) {
+        if (tid == 0 && part == 0 && blockIdx.y == 0) set_status(p.status, PA_STATUS_BAD_SEQLEN);
+        L = L < 0 ? 0 : lmax;
+    }
+    // Query qi0 + k sits at position qbase + k and sees keys up to it (causal);
+    // without the causal rule every query sees all L keys.
+    const int qbase = L - p.q_len + qi0;
+    const int t_stop = p.causal ? min(L, qbase + nq) : L;
+    const int t_begin = part * p.chunk;
+    const int t_end = min(t_begin + p.chunk, max(0, t_stop));
+    const int nch = t_end > t_begin ? (t_end - t_begin + kPfT - 1) / kPfT : 0;
+    // output row of tile row r: ((b * q_len + position) * Hq + g * G + member)
+    const int64_t orow0 = (static_cast<int64_t>(b) * p.q_len + qi0) * Hq + static_cast<int64_t>(g) * G;
+    auto out_row = [&](int r) -> int64_t { return orow0 + static_cast<int64_t>(r / G) * Hq + r % G; };
+
+    if (nch == 0) {  // no key in range: zero output, lse = -inf
+        for (int i = tid; i < nrows * D; i += kPfThreads) {
+            const int64_t o = out_row(i / D);
+            if (p.split) p.part_o[(o * p.part_stride + p.part_offset + part) * D + i % D] = 0.f;
+            else static_cast<__nv_bfloat16 *>(p.out)[o * D + i % D] = __float2bfloat16_rn(0.f);
+        }
+        for (int r = tid; r < nrows; r += kPfThreads) {
+            if (p.split) p.part_lse[out_row(r) * p.part_stride + p.part_offset + part] = -INFINITY;
+            else if (p.lse) p.lse[out_row(r)] = -INFINITY;
+        }
+        return;
+    }
+
+    // ---- set-up: the range's tile rows, the query tile, barriers, TMEM ----------------
+    const int ntiles = (t_end - t_begin + kTile - 1) / kTile;  // <= kPrefillMaxTiles (host)
+    const int32_t *bt = p.block_tables + static_cast<int64_t>(b) * p.table_stride;
+    for (int i = tid; i < ntiles; i += kPfThreads) {
+        const int tok = t_begin + i * kTile;
+        const int phys = bt[tok / bs];
+        int row = -1;
+        if (phys >= 0 && phys < p.num_blocks) row = phys * bs + tok % bs;
+        else set_status(p.status, PA_STATUS_BAD_BLOCK);
+        tile_row[i] = row;
+    }
+    constexpr int kQLoads = kPfRows * (D / 8) / kPfThreads;  // 16-byte chunks per thread
+    uint4 qv[kQLoads];
+#pragma unroll
+    for (int j = 0; j < kQLoads; ++j) {
+        const int i = tid + j * kPfThreads, r = i / (D / 8), c = i % (D / 8);
+        qv[j] = make_uint4(0u, 0u, 0u, 0u);
+        if (r < nrows) qv[j] = *reinterpret_cast<const uint4 *>(p.q + out_row(r) * D + c * 8);
+    }
+#pragma unroll
+    for (int j = 0; j < kQLoads; ++j) {  // Q[r][d]: half d / 64, swizzled 16-byte chunk
+        const int i = tid + j * kPfThreads, r = i / (D / 8), c = i % (D / 8);
+        *reinterpret_cast<uint4 *>(qs + (c >> 3) * kPfQHalf + swz128(r, c & 7)) = qv[j];
+    }
+    if (warp == 0) tc5::tmem_alloc(tmem_slot, kPfTmemCols);
+    if (tid == 0) {
+        for (int i = 0; i < kPfNK; ++i) {
+            mbar_init(&kfull[i], 1u);
+            mbar_init(&kempty[i], 1u);
+        }
+        for (int i = 0; i < kPfNV; ++i) {
+            mbar_init(&vfull[i], 1u);
+            mbar_init(&vempty[i], 1u);
+        }
+        for (int i = 0; i < kPfNS; ++i) {
+            mbar_init(&sdone[i], 1u);
+            mbar_init(&sfree[i], 128u);  // the 128 softmax threads release an S buffer
+        }
+        for (int i = 0; i < kPfNP; ++i) {
+            mbar_init(&pready[i], 128u);  // ... and publish a P buffer
+            mbar_init(&pfree[i], 1u);
+        }
+        *abort_flag = 0;
+    }
+    if (lane == 0 && warp == kPfTmaKWarp) prefetch_tensormap(&kmap);
+    if (lane == 0 && warp == kPfTmaVWarp) prefetch_tensormap(&vmap);
+    fence_proxy_async_smem();  // the query tile, written here, is read by the MMA
+    fence_barrier_init();
+    tc5::fence_before_sync();
+    __syncthreads();
+    tc5::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    auto wait_or_abort = [&](uint64_t *bar, uint32_t parity) -> bool {
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t i = 0; i < kWaitLimit; ++i) {
+            if (mbar_try_wait(bar, parity)) return true;
+            if (*abort_flag) return false;
+            if (wait_expired(i, t0)) break;
+        }
+        *abort_flag = 1;
+        set_status(p.status, PA_STATUS_TIMEOUT);
+        return false;
+    };
+
+    if (warp == kPfTmaKWarp || warp == kPfTmaVWarp) {
+        // ================= TMA producers: K (warp 5), V (warp 6) =================
+        // lanes 0-7: lane = 2 * tile + half issues that box of each chunk
+        const bool is_v = warp == kPfTmaVWarp;
+        uint8_t *ring = is_v ? vring : kring;
+        uint64_t *full = is_v ? vfull : kfull;
+        uint64_t *empty = is_v ? vempty : kempty;
+        const CUtensorMap *map = is_v ? &vmap : &kmap;
+        const int nst = is_v ? kPfNV : kPfNK;
+        const int tile = lane >> 1, half = lane & 1;
+        const int oob_row = p.num_blocks * bs;  // a box starting here lies past the pool: zeros
+        const uint64_t policy = l2_evict_normal_policy();  // other query tiles read these blocks too
+        int issued = 0;
+        for (int c = 0; c < nch; ++c) {
+            const int s = c % nst;
+            if (c >= nst) {
+                const bool ok = wait_or_abort(&empty[s], ((c / nst) - 1) & 1);
+                if (!__all_sync(0xffffffffu, ok)) break;
+            }
+            if (lane == 0) mbar_arrive_expect_tx(&full[s], 2u * kPfTilesPerChunk * kPfBox);
+            __syncwarp();
+            if (lane < 2 * kPfTilesPerChunk) {
+                const int ti = c * kPfTilesPerChunk + tile;
+                const int row = ti < ntiles ? tile_row[ti] : -1;
+                tma_load_4d(ring + s * kPfStage + half * kPfHalf + tile * kPfBox, map, 0,
+                            row >= 0 ? row : oob_row, g, half, &full[s], policy);
+            }
+            issued = c + 1;
+        }
+        if (*abort_flag && lane == 0)  // let this CTA's copies land before it leaves
+            for (int c = max(0, issued - nst); c < issued; ++c) mbar_wait_bounded(&full[c % nst], (c / nst) & 1);
+    } else if (warp == kPfQkWarp) {
+        // ================= QK issuer =================
+        if (lane == 0) {
+            constexpr uint32_t kIdQK = tc5::idesc_bf16_f32(kPfRows, kPfT, false, false);
+            int done = 0;
+            for (int c = 0; c < nch; ++c) {
+                // S buffer c % NS is free once softmax c - NS has read it; K c has landed
+                if (c >= kPfNS && !wait_or_abort(&sfree[c % kPfNS], ((c / kPfNS) - 1) & 1)) break;
+                if (!wait_or_abort(&kfull[c % kPfNK], (c / kPfNK) & 1)) break;
+                tc5::fence_after_sync();
+                const uint8_t *kt = kring + (c % kPfNK) * kPfStage;
+                const uint32_t dcol = tmem + (c % kPfNS) * kPfT;
+#pragma unroll
+                for (int j = 0; j < D / 16; ++j) {  // K = 16 dims per MMA
+                    const int hf = j >> 2, off = (j & 3) * 32;
+                    tc5::mma_bf16(dcol, tc5::sw128_desc(qs + hf * kPfQHalf + off, 16, 1024),
+                                  tc5::sw128_desc(kt + hf * kPfHalf + off, 16, 1024), kIdQK, j > 0);
+                }
+                tc5::commit(&sdone[c % kPfNS]);
+                tc5::commit(&kempty[c % kPfNK]);
+                done = c + 1;
+            }
+            if (*abort_flag && done > 0)  // let issued MMAs finish before TMEM is freed
+                mbar_wait_bounded(&sdone[(done - 1) % kPfNS], ((done - 1) / kPfNS) & 1);
+        }
+    } else if (warp == kPfPvWarp) {
+        // ================= PV issuer =================
+        if (lane == 0) {
+            constexpr uint32_t kIdPV = tc5::idesc_bf16_f32(kPfRows, D, false, true);
+            int done = 0;
+            for (int c = 0; c < nch; ++c) {
+                if (!wait_or_abort(&pready[c % kPfNP], (c / kPfNP) & 1)) break;
+                if (!wait_or_abort(&vfull[c % kPfNV], (c / kPfNV) & 1)) break;
+                tc5::fence_after_sync();
+                const uint8_t *vt = vring + (c % kPfNV) * kPfStage;
+                const uint8_t *pb = ps + (c % kPfNP) * kPfPBuf;
+#pragma unroll
+                for (int hl = 0; hl < 2; ++hl) {  // hi part, then lo part of p
+#pragma unroll
+                    for (int j = 0; j < kPfT / 16; ++j)  // K = 16 tokens per MMA
+                        tc5::mma_bf16(tmem + kPfColO, tc5::sw128_desc(pb + hl * kPfPPart + j * 32, 16, 1024),
+                                      tc5::sw128_desc(vt + j * 16 * kSubBytes, kPfHalf, 1024), kIdPV,
+                                      c > 0 || hl > 0 || j > 0);
+                }
+                tc5::commit(&pfree[c % kPfNP]);
+                tc5::commit(&vempty[c % kPfNV]);
+                done = c + 1;
+            }
+            if (*abort_flag && done > 0)
+                mbar_wait_bounded(&pfree[(done - 1) % kPfNP], ((done - 1) / kPfNP) & 1);
+        }
+    } else {
+        // ================= softmax warps: thread = query row r =================
+        const int r = tid;
+        const bool row_ok = r < nrows;
+        const int pos = p.causal ? qbase + r / G : L - 1;  // the last key row r sees
+        const float sl2 = p.scale_log2;
+        float m_ref = -INFINITY, l = 0.f;
+        bool dead = false;
+        for (int c = 0; c < nch; ++c) {
+            const int sb = c % kPfNS, pb = c % kPfNP;
+            const bool ok = __all_sync(0xffffffffu, wait_or_abort(&sdone[sb], (c / kPfNS) & 1));
+            float sv[kPfT];
+            if (ok) {
+                tc5::fence_after_sync();
+#pragma unroll
+                for (int k = 0; k < kPfT / 16; ++k)
+                    tc5::ld_32x32b_x16(tc5::taddr(tmem, 32 * warp, sb * kPfT + 16 * k),
+                                       *reinterpret_cast<float(*)[16]>(&sv[16 * k]));
+            }
+            tc5::fence_before_sync();
+            mbar_arrive(&sfree[sb]);  // S buffer read: QK c + NS may overwrite it
+            if (!ok || *abort_flag) {
+                dead = true;
+                break;
+            }
+            const int tok0 = t_begin + c * kPfT;
+            bool tile_ok[kPfTilesPerChunk];
+#pragma unroll
+            for (int k = 0; k < kPfTilesPerChunk; ++k) {
+                const int ti = c * kPfTilesPerChunk + k;
+                tile_ok[k] = ti < ntiles && tile_row[ti] >= 0;
+            }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < kPfT; ++k) {
+                const int t = tok0 + k;
+                const bool valid = row_ok && tile_ok[k / kTile] && t < t_end && t <= pos;
+                sv[k] = valid ? sv[k] * sl2 : -INFINITY;
+                mx = fmaxf(mx, sv[k]);
+            }
+            // Lazy rescaling: a row's reference max moves only when a score exceeds
+            // it by more than 2^8; the warp then rescales its 32 rows of O together
+            // (TMEM loads and stores are warp-wide) once PV c - 1 has finished.
+            if (__any_sync(0xffffffffu, mx > m_ref + kPfLazyTau)) {
+                const float mn = fmaxf(m_ref, mx);
+                const float alpha = mn == -INFINITY ? 1.f : fast_exp2(m_ref - mn);
+                l *= alpha;
+                if (c > 0) {
+                    const bool ok2 = __all_sync(
+                        0xffffffffu, wait_or_abort(&pfree[(c - 1) % kPfNP], ((c - 1) / kPfNP) & 1));
+                    if (ok2) {
+                        tc5::fence_after_sync();
+#pragma unroll 1
+                        for (int k = 0; k < D / 16; ++k) {
+                            float ov[16];
+                            const uint32_t ta = tc5::taddr(tmem, 32 * warp, kPfColO + 16 * k);
+                            tc5::ld_32x32b_x16(ta, ov);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) ov[i] *= alpha;
+                            tc5::st_32x32b_x16(ta, ov);
+                        }
+                    }
+                }
+                m_ref = mn;
+            }
+            // p = hi + lo, two bf16 values per word
+            uint32_t hw[kPfT / 2], lw[kPfT / 2];
+#pragma unroll
+            for (int k = 0; k < kPfT; k += 2) {
+                const float p0 = sv[k] != -INFINITY ? fast_exp2(sv[k] - m_ref) : 0.f;
+                const float p1 = sv[k + 1] != -INFINITY ? fast_exp2(sv[k + 1] - m_ref) : 0.f;
+                const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+                const float h0 = __low2float(h), h1 = __high2float(h);
+                const __nv_bfloat162 lo = __floats2bfloat162_rn(p0 - h0, p1 - h1);
+                hw[k / 2] = *reinterpret_cast<const uint32_t *>(&h);
+                lw[k / 2] = *reinterpret_cast<const uint32_t *>(&lo);
+                l += (h0 + __low2float(lo)) + (h1 + __high2float(lo));
+            }
+            if (c >= kPfNP) wait_or_abort(&pfree[pb], ((c / kPfNP) - 1) & 1);  // PV c - NP is done
+            uint8_t *prow = ps + pb * kPfPBuf + r * kSubBytes;
+#pragma unroll
+            for (int j = 0; j < kPfT / 8; ++j) {  // 16-byte chunk j holds tokens 8j .. 8j + 7
+                const uint32_t off = static_cast<uint32_t>((j ^ (r & 7)) << 4);
+                *reinterpret_cast<uint4 *>(prow + off) =
+                    make_uint4(hw[4 * j], hw[4 * j + 1], hw[4 * j + 2], hw[4 * j + 3]);
+                *reinterpret_cast<uint4 *>(prow + kPfPPart + off) =
+                    make_uint4(lw[4 * j], lw[4 * j + 1], lw[4 * j + 2], lw[4 * j + 3]);
+            }
+            // V rows that were loaded from the pool but lie past the range (the
+            // tail of the tile holding key t_end - 1) may hold anything, even
+            // NaN: they are zeroed, so that 0 * V never reaches O.
+            if (c == nch - 1) {
+                const int z0 = t_end - tok0;
+                const int z1 = min(kPfT, (t_end + kTile - 1) / kTile * kTile - tok0);
+                if (z1 > z0 && wait_or_abort(&vfull[c % kPfNV], (c / kPfNV) & 1)) {
+                    uint8_t *vt = vring + (c % kPfNV) * kPfStage;
+                    for (int i = tid; i < (z1 - z0) * 16; i += 128) {
+                        const int row = z0 + i / 16, hc = i % 16;
+                        *reinterpret_cast<uint4 *>(vt + (hc >> 3) * kPfHalf + swz128(row, hc & 7)) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+            }
+            fence_proxy_async_smem();  // P (and zeroed V rows) are read by the MMA
+            tc5::fence_before_sync();
+            mbar_arrive(&pready[pb]);
+        }
+
+        // ---- epilogue: O row r, normalised, staged in the idle P buffers, bulk-copied out ----
+        const bool okf = !dead && __all_sync(0xffffffffu, wait_or_abort(&pfree[(nch - 1) % kPfNP],
+                                                                        ((nch - 1) / kPfNP) & 1));
+        if (okf) {
+            tc5::fence_after_sync();
+            const bool split = p.split != 0;
+            const float inv = l > 0.f ? p.v_scale / l : 0.f;  // 0: no key seen
+            uint8_t *stage = ps + r * (split ? D * 4 : D * 2);
+#pragma unroll 1
+            for (int k = 0; k < D / 16; ++k) {
+                float ov[16];
+                tc5::ld_32x32b_x16(tc5::taddr(tmem, 32 * warp, kPfColO + 16 * k), ov);
+                if (split) {
+                    float4 *dst = reinterpret_cast<float4 *>(stage) + 4 * k;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        dst[i] = make_float4(ov[4 * i] * inv, ov[4 * i + 1] * inv, ov[4 * i + 2] * inv,
+                                             ov[4 * i + 3] * inv);
+                } else {
+                    uint32_t w[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const __nv_bfloat162 h = __floats2bfloat162_rn(ov[2 * i] * inv, ov[2 * i + 1] * inv);
+                        w[i] = *reinterpret_cast<const uint32_t *>(&h);
+                    }
+                    uint4 *dst = reinterpret_cast<uint4 *>(stage) + 2 * k;
+                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                }
+            }
+            fence_proxy_async_smem();  // the bulk copy (async proxy) reads the staged row
+            if (row_ok) {
+                const float lse = l > 0.f ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
+                const int64_t o = out_row(r);
+                if (split) {
+                    const int64_t slot = o * p.part_stride + p.part_offset + part;
+                    bulk_store_s2g(p.part_o + slot * D, stage, D * 4);
+                    bulk_commit();
+                    p.part_lse[slot] = lse;
+                } else {
+                    bulk_store_s2g(static_cast<__nv_bfloat16 *>(p.out) + o * D, stage, D * 2);
+                    bulk_commit();
+                    if (p.lse) p.lse[o] = lse;
+                }
+                bulk_wait_all_read();
+            }
+        }
+    }
+    tc5::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc5::tmem_free(tmem, kPfTmemCols);
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_tc(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParams &p,
+                              int B, int G, cudaStream_t stream) {
+    static std::atomic<uint64_t> smem_attr_done{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(smem_attr_done.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kPfSmemBytes);
+        if (e != cudaSuccess) return e;
+        smem_attr_done.fetch_or(bit, std::memory_order_release);
+    }
+    const int qtiles = (p.q_len + p.q_per_cta - 1) / p.q_per_cta;
+    const dim3 grid(p.num_splits, qtiles * p.num_kv_heads, B);
+    return launch_maybe_cooperative(prefill_tc_kernel, grid, kPfThreads, kPfSmemBytes, stream, false,
+                                    p.pdl != 0, kmap, vmap, p, G);
+}
+
+}  // namespace pa

@@ -243,6 +243,16 @@ def spec_verify(base: str, q_len: int, **kw) -> DecodeWorkload:
     return w
 
 
+def prefill_chunk(base: str, q_len: int, **kw) -> DecodeWorkload:
+    """Chunked prefill on a decode workload: the last q_len positions of every
+    sequence are one chunk of new prompt tokens, written this step and
+    attended causally (every base length is at least q_len)."""
+    w = WORKLOADS[base](q_len=q_len, **kw)
+    assert int(w.seq_lens.min()) >= q_len
+    w.name = f"{base}-chunk{q_len}"
+    return w
+
+
 WORKLOADS = {
     "tiny": tiny,
     "qwen2.5-1.5b-B1": lambda **kw: qwen25_1p5b(1, **kw),
@@ -267,4 +277,7 @@ WORKLOADS.update({
     "qwen2.5-1.5b-B8-spec4": lambda **kw: spec_verify("qwen2.5-1.5b-B8", 4, **kw),
     "qwen2.5-7b-bs16-spec4": lambda **kw: spec_verify("qwen2.5-7b-bs16", 4, **kw),
     "qwen3-0.6b-B256-spec4": lambda **kw: spec_verify("qwen3-0.6b-B256", 4, **kw),
+    # one 512-token chunked-prefill chunk per sequence on the Qwen2.5-1.5B layer
+    "qwen2.5-1.5b-B1-chunk512": lambda **kw: prefill_chunk("qwen2.5-1.5b-B1", 512, **kw),
+    "qwen2.5-1.5b-B8-chunk512": lambda **kw: prefill_chunk("qwen2.5-1.5b-B8", 512, **kw),
 })

@@ -349,3 +349,18 @@ def test_noalloc_rejects_bad_arguments_before_touching_its_array(lib, kw, code):
     rc = lib.pa_decode_splitkv_noalloc(a["out"], None, a["q"], FAKE, FAKE, a["desc"], FAKE, 7, FAKE,
                                        a["B"], a["Hq"], 0.125, a["splits"], None, None)
     assert rc == code
+
+
+def test_mq_split_policy_prefill_shape(lib, use_kernel):
+    """Calls with more query columns per KV head than the decode kernel holds
+    (q_len * G > 32) count one CTA per (sequence, KV head, tile of 128 / G
+    positions); a partition never exceeds 2048 tiles of 16 tokens."""
+    use_kernel("auto")
+    # Qwen2.5-1.5B layer, 512-token chunk: 21 positions per tile -> 25 tiles per KV head
+    assert pa.pa_choose_num_splits_mq(8, 512, 12, 2, 128, 128, 16, 152) == 1       # 400 CTAs
+    assert pa.pa_choose_num_splits_mq(1, 512, 12, 2, 128, 128, 16, 152) == 3       # 50 CTAs
+    # G = 7, 64 queries: 18 positions per tile -> 4 tiles
+    assert pa.pa_choose_num_splits_mq(2, 64, 28, 4, 128, 256, 16, 152) == 4        # 32 CTAs x 4
+    # a 64k-token table needs at least 2 partitions of at most 32768 tokens
+    assert pa.pa_choose_num_splits_mq(64, 128, 8, 1, 128, 4096, 16, 152) >= 2
+

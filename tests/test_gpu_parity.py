@@ -449,6 +449,50 @@ def test_mq_small_elementwise(case):
     assert dev.status_value() == 0
 
 
+# More query columns per KV head than the decode kernel holds (q_len * G > 32):
+# the prefill-shaped kernel, 128 query rows per CTA.
+MQ_PREFILL = [
+    # (Hq, Hkv, bs, lens, q_len)
+    (8, 8, 16, (1, 40, 200), 64),        # G = 1: 128 positions per tile; L < q_len
+    (28, 4, 16, (300, 64, 129), 40),     # G = 7: 18 positions (126 rows) per tile, 3 tiles
+    (64, 2, 16, (500, 37), 9),           # G = 32: 4 positions per tile
+    (12, 2, 256, (700, 513), 100),       # G = 6, 256-token pages
+    (6, 2, 16, (1000,), 200),            # G = 3: 42 positions per tile, 5 tiles
+    (16, 8, 16, (17, 15), 33),           # G = 2, every sequence shorter than q_len
+    (16, 2, 16, (129, 191, 64), 65),     # G = 8: chunk and tile boundaries
+]
+
+
+@pytest.mark.parametrize("case", MQ_PREFILL, ids=lambda c: f"Hq{c[0]}-Hkv{c[1]}-bs{c[2]}-q{c[4]}")
+def test_mq_prefill_shape_elementwise(case):
+    Hq, Hkv, bs, lens, q_len = case
+    nb = sum((L + bs - 1) // bs for L in lens) + 5
+    w = W.make_workload("pf", B=len(lens), Hq=Hq, Hkv=Hkv, D=128, block_size=bs, seq_lens=list(lens),
+                        num_blocks=nb, seed=sum(lens) + q_len, poison_unused=True, q_len=q_len)
+    kc, vc = oracle_after_write(w)
+    ref, ref_lse = oracle.decode_mq(w.q, kc, vc, w.block_tables, w.seq_lens, w.scale)
+    dev = Dev(w)
+    dev.write()
+    for P in (1, 2, 3, 7, 0):
+        out, lse, Pu = dev.mq(P)
+        assert_close(bf16_dev_to_f64(out), ref, f"prefill-shaped mq P={Pu}")
+        assert_lse_close(lse.cpu().double().numpy(), ref_lse, f"prefill-shaped mq P={Pu}")
+    assert dev.status_value() == 0
+
+
+def test_mq_prefill_shape_reports_a_bad_block():
+    """A bad block id inside a prefill-shaped call is reported and never read."""
+    w = W.make_workload("pfbad", B=2, Hq=28, Hkv=4, D=128, block_size=16, seq_lens=[300, 200],
+                        num_blocks=40, seed=9, q_len=40)
+    w.block_tables[0, 3] = w.num_blocks + 7
+    w.block_tables[1, 1] = -3
+    dev = Dev(w)
+    out, lse, _ = dev.mq(1)
+    torch.cuda.synchronize()
+    assert dev.status_value() & pa.PA_STATUS_BAD_BLOCK
+    assert torch.isfinite(out.float()).all()
+
+
 def test_mq_single_query_is_splitkv_bit_exact():
     w = W.make_workload("mq1", B=3, Hq=28, Hkv=4, D=128, block_size=16, seq_lens=[300, 17, 1024],
                         num_blocks=100, seed=5, q_len=1)
