@@ -296,10 +296,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             float sv[kPfT];
             if (ok) {
                 tc5::fence_after_sync();
+                uint32_t raw[kPfT / 16][16];
 #pragma unroll
                 for (int k = 0; k < kPfT / 16; ++k)
-                    tc5::ld_32x32b_x16(tc5::taddr(tmem, 32 * warp, sb * kPfT + 16 * k),
-                                       *reinterpret_cast<float(*)[16]>(&sv[16 * k]));
+                    tc5::ld_32x32b_x16_nowait(tc5::taddr(tmem, 32 * warp, sb * kPfT + 16 * k), raw[k]);
+                tc5::wait_ld();
+#pragma unroll
+                for (int k = 0; k < kPfT; ++k) sv[k] = __uint_as_float(raw[k / 16][k % 16]);
             }
             tc5::fence_before_sync();
             mbar_arrive(&sfree[sb]);  // S buffer read: QK c + NS may overwrite it
@@ -309,18 +312,31 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             }
             const int tok0 = t_begin + c * kPfT;
             bool tile_ok[kPfTilesPerChunk];
+            bool all_tiles = true;
 #pragma unroll
             for (int k = 0; k < kPfTilesPerChunk; ++k) {
                 const int ti = c * kPfTilesPerChunk + k;
                 tile_ok[k] = ti < ntiles && tile_row[ti] >= 0;
+                all_tiles &= tile_ok[k];
             }
+            // Most chunks are seen whole by every row of the warp: no mask then.
+            const int tok_last = tok0 + kPfT - 1;
+            const bool whole = __all_sync(0xffffffffu, row_ok && all_tiles && tok_last < t_end && tok_last <= pos);
             float mx = -INFINITY;
+            if (whole) {
 #pragma unroll
-            for (int k = 0; k < kPfT; ++k) {
-                const int t = tok0 + k;
-                const bool valid = row_ok && tile_ok[k / kTile] && t < t_end && t <= pos;
-                sv[k] = valid ? sv[k] * sl2 : -INFINITY;
-                mx = fmaxf(mx, sv[k]);
+                for (int k = 0; k < kPfT; ++k) {
+                    sv[k] *= sl2;
+                    mx = fmaxf(mx, sv[k]);
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < kPfT; ++k) {
+                    const int t = tok0 + k;
+                    const bool valid = row_ok && tile_ok[k / kTile] && t < t_end && t <= pos;
+                    sv[k] = valid ? sv[k] * sl2 : -INFINITY;
+                    mx = fmaxf(mx, sv[k]);
+                }
             }
             // Lazy rescaling: a row's reference max moves only when a score exceeds
             // it by more than 2^8; the warp then rescales its 32 rows of O together
@@ -347,18 +363,21 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 }
                 m_ref = mn;
             }
-            // p = hi + lo, two bf16 values per word
+            // p = hi + lo, two bf16 values per word.  A masked score is -inf and
+            // gives p = 0 (a row that has seen no key yet subtracts 0, not -inf).
+            // The row sum adds p itself: hi + lo equals it to about 2^-17.
+            const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
             uint32_t hw[kPfT / 2], lw[kPfT / 2];
 #pragma unroll
             for (int k = 0; k < kPfT; k += 2) {
-                const float p0 = sv[k] != -INFINITY ? fast_exp2(sv[k] - m_ref) : 0.f;
-                const float p1 = sv[k + 1] != -INFINITY ? fast_exp2(sv[k + 1] - m_ref) : 0.f;
+                const float p0 = fast_exp2(sv[k] - m_use);
+                const float p1 = fast_exp2(sv[k + 1] - m_use);
                 const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
-                const float h0 = __low2float(h), h1 = __high2float(h);
-                const __nv_bfloat162 lo = __floats2bfloat162_rn(p0 - h0, p1 - h1);
+                const float2 hf = __bfloat1622float2(h);
+                const __nv_bfloat162 lo = __floats2bfloat162_rn(p0 - hf.x, p1 - hf.y);
                 hw[k / 2] = *reinterpret_cast<const uint32_t *>(&h);
                 lw[k / 2] = *reinterpret_cast<const uint32_t *>(&lo);
-                l += (h0 + __low2float(lo)) + (h1 + __high2float(lo));
+                l += p0 + p1;
             }
             if (c >= kPfNP) wait_or_abort(&pfree[pb], ((c / kPfNP) - 1) & 1);  // PV c - NP is done
             uint8_t *prow = ps + pb * kPfPBuf + r * kSubBytes;
