@@ -361,7 +361,7 @@ def run_ours(args, world, rank, local):
     kn, vn, slots = to_dev(w.k_new), to_dev(w.v_new), to_dev(w.slot_mapping)
     fp8 = w.fp8   # e4m3 pools: write with pa_cache_write_fp8, decode with pa_decode_splitkv_fp8
     k0, v0 = (to_dev(w.k_cache8), to_dev(w.v_cache8)) if fp8 else (to_dev(w.k_cache), to_dev(w.v_cache))
-    touched = w.kv_bytes()
+    touched = w.unique_kv_bytes()   # the pool rows a step reads (shared blocks once)
     R = max(1, min(8, math.ceil(2.5 * L2_BYTES / max(touched, 1)) + 1)) if touched < 3 * L2_BYTES else 1
     pools = [(k0, v0)] + [(k0.clone(), v0.clone()) for _ in range(R - 1)]
     mq = w.q_len > 1   # multi-query step: write the q_len new tokens, then causal decode
@@ -377,9 +377,14 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.Stream(device=dev)
     forced = pa.pa_get_option(pa.PA_OPT_DECODE_KERNEL)
     use_tc = forced == pa.PA_KERNEL_TENSOR_CORE or (forced != pa.PA_KERNEL_CUDA_CORE and w.D == 128)
-    kernel_name = "decode_tc_kernel" if use_tc else "decode_cc_kernel"
+    # multi-query calls with more than 32 query columns per KV head run the prefill-shaped kernel
+    kernel_name = ("prefill_tc_kernel" if use_tc and w.q_len * w.G > 32 else
+                   "decode_tc_kernel" if use_tc else "decode_cc_kernel")
 
-    cascade = w.cascade_blocks > 0   # shared prefix attended once, then the suffixes, then a merge
+    cascade = w.cascade_blocks > 0   # decoded through pa_decode_cascade
+    # the cascade proper (prefix once, suffixes, merge) where the library finds it pays,
+    # else pa_decode_cascade runs plain split decode
+    cascade_runs = cascade and pa.pa_cascade_pays(w.B, w.Hkv, w.D, w.cascade_blocks, w.block_size)
     ws_bytes = (pa.pa_cascade_workspace_bytes(w.B, w.Hq, w.Hkv, w.D, w.cascade_blocks, w.max_blocks,
                                               w.block_size) if cascade
                 else pa.pa_splitkv_workspace_bytes(w.B * w.q_len, w.Hq, w.D, P))
@@ -413,7 +418,7 @@ def run_ours(args, world, rank, local):
         if ev1 is not None:
             ev1.record(stream)
 
-    launches_per_step = (4 if cascade else 2 if (args.unfused or mq or fp8) else 1)
+    launches_per_step = (4 if cascade_runs else 2 if (args.unfused or mq or fp8 or cascade) else 1)
     # The timed region replays CUDA graphs that hold exactly the K timed steps
     # (consecutive steps cycle over the pool replicas): one graph when K <= 1024,
     # else K // 1024 replays of a 1024-step graph and one graph of the rest.  A
@@ -597,7 +602,8 @@ def run_ours(args, world, rank, local):
         roofline = {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
                     "frac": round(ach / peak, 4), "traffic": recorded_traffic(args.workload, kernel_name),
                     "peak_kind": peak_kind,
-                    "kernel": kernel_name + (" (cascade: prefix + suffix + combine)" if cascade else
+                    "kernel": kernel_name + (" (cascade: prefix + suffix + combine)" if cascade_runs else
+                                             " (shared prefix: plain split decode)" if cascade else
                                              " (fp8 pools)" if fp8 else " (multi-query)" if mq else
                                              "" if args.unfused else " (fused write)")
                               + (" + split merge" if merged else ""),
@@ -625,7 +631,10 @@ def run_ours(args, world, rank, local):
             "config": {"workload": args.workload, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
                        "block_size": w.block_size, "seq_lens_total": int(w.seq_lens.sum()),
                        "splits": P, "q_len": w.q_len,
-                       "step": ("pa_cache_write, then pa_decode_cascade (3 launches)" if cascade else
+                       "step": ("pa_cache_write, then pa_decode_cascade (cascade: 3 launches)"
+                                if cascade_runs else
+                                "pa_cache_write, then pa_decode_cascade (plain split decode: the "
+                                "cascade does not pay)" if cascade else
                                 "pa_cache_write_fp8, then pa_decode_splitkv_fp8 (e4m3 pools)"
                                 if fp8 else
                                 "cache_write of the q_len new tokens, then pa_decode_mq (causal)"
@@ -736,7 +745,7 @@ def measure_configs(args, dev, peak):
             wr = per_call(lambda: pa.pa_cache_write(kn, vn, slots, k0, v0, stream=stream))
 
             # steady state: one graph of S steps over R pool replicas, replayed back to back
-            touched = w.kv_bytes()
+            touched = w.unique_kv_bytes()
             R = (max(1, min(8, math.ceil(2.5 * L2_BYTES / max(touched, 1)) + 1))
                  if touched < 3 * L2_BYTES else 1)
             pools = [(k0, v0)] + [(k0.clone(), v0.clone()) for _ in range(R - 1)]

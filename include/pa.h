@@ -105,9 +105,13 @@ enum {
     PA_OPT_SPLIT_MERGE = 1,   /* PA_MERGE_AUTO, or PA_MERGE_GRID: never merge split
                                  partials through a thread-block cluster
                                  (PA_SPLIT_MERGE=grid) */
-    PA_OPT_PDL = 2            /* 1: programmatic stream serialization for the
+    PA_OPT_PDL = 2,           /* 1: programmatic stream serialization for the
                                  tensor-core kernel; 0: plain launches (PA_PDL=0) */
+    PA_OPT_CASCADE = 3        /* pa_decode_cascade: PA_CASCADE_AUTO (the cascade
+                                 where it pays), _ALWAYS or _NEVER
+                                 (PA_CASCADE=always|never) */
 };
+enum { PA_CASCADE_AUTO = 0, PA_CASCADE_ALWAYS = 1, PA_CASCADE_NEVER = 2 };
 enum {
     PA_KERNEL_AUTO = 0,        /* tensor cores wherever they can run the shape */
     PA_KERNEL_CUDA_CORE = 1,   /* force the CUDA-core kernel */
@@ -352,21 +356,26 @@ int pa_decode_mq(void *out, float *lse, const void *q, int32_t q_len, const void
                  int32_t *status, pa_stream_t stream);
 
 /*
- * Cascade decode over a shared prefix: the first n_prefix_blocks entries of
+ * Decode over a shared prefix, as a cascade where that pays: the first n_prefix_blocks entries of
  * every sequence's block table name the same physical blocks (a prefix-cache
  * hit shared by the batch: "mini-infer" prajwal7-2002 docs, table "Core
  * Capabilities at a Glance", row "Prompt Caching", radix-tree prefix cache;
  * psmarter write-up, feature list item 4, prefix caching).  The result is
- * pa_decode_splitkv's, computed in three launches: (1) the prefix once, all B
- * sequences' queries attending it together (one CTA reads a prefix block for
- * up to 32 / G sequences); (2) every sequence's remaining positions,
+ * pa_decode_splitkv's.  The cascade computes it in three launches: (1) the
+ * prefix once, all B sequences' queries attending it together (128 query
+ * rows, i.e. 128 / G sequences, per CTA of the prefill-shaped kernel when
+ * B * G > 32); (2) every sequence's remaining positions,
  * [n_prefix_blocks * block_size, seq_lens[b]); (3) a log-sum-exp merge of both
- * passes' fp32 partials.  Requires seq_lens[b] >= n_prefix_blocks *
+ * passes' fp32 partials.  It pays when re-reading the prefix for every
+ * sequence would cost more than those launches: with PA_OPT_CASCADE at
+ * PA_CASCADE_AUTO the call runs the cascade when (B - 1) x the prefix's K/V
+ * bytes reach 256 MB, and pa_decode_splitkv otherwise (the same result).  Requires seq_lens[b] >= n_prefix_blocks *
  * block_size (a shorter sequence sets PA_STATUS_BAD_SEQLEN and its result is
  * undefined); 0 <= n_prefix_blocks < max_blocks_per_seq (0: plain
  * pa_decode_splitkv).  The library reads the prefix's block ids from table
- * row 0.  workspace: pa_cascade_workspace_bytes(...) bytes (fp32 partials),
- * 256-byte aligned.  Tensor-core kernel only: head_dim 128, Hq / Hkv <= 32.
+ * row 0.  workspace: pa_cascade_workspace_bytes(...) bytes (fp32 partials,
+ * enough for either path), 256-byte aligned, zero-filled before its first use
+ * (the pa_decode_splitkv contract).  Tensor-core kernel only: head_dim 128, Hq / Hkv <= 32.
  */
 int pa_decode_cascade(void *out, float *lse, const void *q, const void *k_cache,
                       const void *v_cache, pa_cache_desc cache, int32_t n_prefix_blocks,
@@ -374,6 +383,11 @@ int pa_decode_cascade(void *out, float *lse, const void *q, const void *k_cache,
                       const int32_t *seq_lens, int32_t B, int32_t Hq, float scale,
                       void *workspace, size_t workspace_bytes, int32_t *status,
                       pa_stream_t stream);
+
+/* 1 when pa_decode_cascade runs the cascade for this shape under the current
+ * PA_OPT_CASCADE switch, 0 when it runs pa_decode_splitkv; PA_EINVAL on bad
+ * arguments.  Host-only. */
+int pa_cascade_pays(int32_t B, int32_t Hkv, int32_t D, int32_t n_prefix_blocks, int32_t block_size);
 
 /* Workspace bytes pa_decode_cascade needs on the current device (0 on bad arguments). */
 size_t pa_cascade_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,

@@ -94,7 +94,7 @@ int64_t units_per_split(Kernel k, int B, int G, int Hkv, int qpc = 1, int qgroup
 
 // Process-wide switches (pa_set_option), each initialised once from its
 // environment variable the first time any of them is read.
-std::atomic<int> g_options[3];
+std::atomic<int> g_options[4];
 std::once_flag g_options_once;
 
 int option(int which) {
@@ -109,6 +109,10 @@ int option(int which) {
                                                                             : PA_MERGE_AUTO);
         const char *d = std::getenv("PA_PDL");
         g_options[PA_OPT_PDL].store(d && std::strcmp(d, "0") == 0 ? 0 : 1);
+        const char *cs = std::getenv("PA_CASCADE");
+        g_options[PA_OPT_CASCADE].store(cs && std::strcmp(cs, "always") == 0  ? PA_CASCADE_ALWAYS
+                                        : cs && std::strcmp(cs, "never") == 0 ? PA_CASCADE_NEVER
+                                                                              : PA_CASCADE_AUTO);
     });
     return g_options[which].load(std::memory_order_relaxed);
 }
@@ -449,6 +453,9 @@ int pa_set_option(int32_t which, int32_t value) {
         case PA_OPT_PDL:
             if (value != 0 && value != 1) return PA_EINVAL;
             break;
+        case PA_OPT_CASCADE:
+            if (value < PA_CASCADE_AUTO || value > PA_CASCADE_NEVER) return PA_EINVAL;
+            break;
         default:
             return PA_EINVAL;
     }
@@ -458,7 +465,7 @@ int pa_set_option(int32_t which, int32_t value) {
 }
 
 int pa_get_option(int32_t which) {
-    if (which < PA_OPT_DECODE_KERNEL || which > PA_OPT_PDL) return PA_EINVAL;
+    if (which < PA_OPT_DECODE_KERNEL || which > PA_OPT_CASCADE) return PA_EINVAL;
     return option(which);
 }
 
@@ -737,6 +744,27 @@ static int cascade_splits(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t
     return PA_OK;
 }
 
+// Does attending the shared prefix once for the whole batch pay?  Without the
+// cascade every sequence reads the prefix again: B - 1 extra reads of its K/V,
+// from L2 while the prefix fits there.  The cascade costs two extra launches
+// and a merge (about 10 us on the GB300).  It pays when the extra reads are
+// large enough to take longer than that even from L2: (B - 1) x prefix bytes
+// of at least 256 MB (a 2048-token prefix of 8 KV heads for 256 sequences is
+// 2.1 GB; 8 blocks of the same heads, 134 MB, is served from L2 faster than
+// the cascade's launches).
+static bool cascade_pays(int32_t B, int32_t Hkv, int32_t D, int32_t n_prefix_blocks,
+                         int32_t block_size) {
+    const int mode = option(PA_OPT_CASCADE);
+    if (mode != PA_CASCADE_AUTO) return mode == PA_CASCADE_ALWAYS;
+    const double prefix_bytes = static_cast<double>(n_prefix_blocks) * block_size * Hkv * D * 2 * 2;
+    return (B - 1) * prefix_bytes >= 256.0 * (1 << 20);
+}
+
+int pa_cascade_pays(int32_t B, int32_t Hkv, int32_t D, int32_t n_prefix_blocks, int32_t block_size) {
+    if (B <= 0 || Hkv <= 0 || D <= 0 || n_prefix_blocks < 0 || block_size <= 0) return PA_EINVAL;
+    return n_prefix_blocks > 0 && cascade_pays(B, Hkv, D, n_prefix_blocks, block_size) ? 1 : 0;
+}
+
 size_t pa_cascade_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
                                   int32_t n_prefix_blocks, int32_t max_blocks_per_seq,
                                   int32_t block_size) {
@@ -746,7 +774,10 @@ size_t pa_cascade_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
     int P1 = 0, P2 = 0;
     if (cascade_splits(B, Hq, Hkv, D, n_prefix_blocks, max_blocks_per_seq, block_size, &P1, &P2))
         return 0;
-    return pa_splitkv_workspace_bytes(B, Hq, D, P1 + P2 < 2 ? 2 : P1 + P2);
+    // enough for either path (the plain split decode when the cascade does not pay)
+    const int P = pa_auto_num_splits(B, Hq, Hkv, D, max_blocks_per_seq, block_size);
+    return std::max(pa_splitkv_workspace_bytes(B, Hq, D, P1 + P2 < 2 ? 2 : P1 + P2),
+                    P > 0 ? pa_splitkv_workspace_bytes(B, Hq, D, P) : 0);
 }
 
 int pa_decode_cascade(void *out, float *lse, const void *q, const void *k_cache,
@@ -761,7 +792,9 @@ int pa_decode_cascade(void *out, float *lse, const void *q, const void *k_cache,
     if (!out || !aligned(out, 16) || (lse && !aligned(lse, 4))) return PA_EINVAL;
     if (n_prefix_blocks < 0 || n_prefix_blocks >= max_blocks_per_seq) return PA_EINVAL;
     if (B == 0) return PA_OK;
-    if (n_prefix_blocks == 0)  // nothing shared: plain split decode
+    // nothing shared, or too little to pay for the cascade's launches: plain split decode
+    if (n_prefix_blocks == 0 ||
+        !cascade_pays(B, cache.num_kv_heads, cache.head_dim, n_prefix_blocks, cache.block_size))
         return splitkv_common(out, lse, q, k_cache, v_cache, cache, block_tables,
                               max_blocks_per_seq, seq_lens, B, Hq, scale, 0, workspace,
                               workspace_bytes, status, stream, NewTokens());

@@ -23,7 +23,8 @@ from . import build as _build
 
 PA_OK, PA_EINVAL, PA_EUNSUPPORTED, PA_EWORKSPACE, PA_ECUDA = 0, -1, -2, -3, -4
 PA_STATUS_BAD_BLOCK, PA_STATUS_BAD_SLOT, PA_STATUS_BAD_SEQLEN, PA_STATUS_TIMEOUT = 1, 2, 4, 8
-PA_OPT_DECODE_KERNEL, PA_OPT_SPLIT_MERGE, PA_OPT_PDL = 0, 1, 2
+PA_OPT_DECODE_KERNEL, PA_OPT_SPLIT_MERGE, PA_OPT_PDL, PA_OPT_CASCADE = 0, 1, 2, 3
+PA_CASCADE_AUTO, PA_CASCADE_ALWAYS, PA_CASCADE_NEVER = 0, 1, 2
 PA_KERNEL_AUTO, PA_KERNEL_CUDA_CORE, PA_KERNEL_TENSOR_CORE = 0, 1, 2
 PA_MERGE_AUTO, PA_MERGE_GRID = 0, 1
 
@@ -69,6 +70,7 @@ _SIGNATURES = {
     "pa_decode_cascade": ([_P, _P, _P, _P, _P, CacheDesc, _I32, _P, _I32, _P, _I32, _I32, _F32, _P,
                            _SZ, _P, _P], ctypes.c_int),
     "pa_cascade_workspace_bytes": ([_I32, _I32, _I32, _I32, _I32, _I32, _I32], _SZ),
+    "pa_cascade_pays": ([_I32, _I32, _I32, _I32, _I32], ctypes.c_int),
     "pa_cache_write_fp8": ([_P, _P, _P, _I64, _P, _P, CacheDesc, _F32, _F32, _P, _P], ctypes.c_int),
     "pa_decode_splitkv_fp8": ([_P, _P, _P, _P, _P, CacheDesc, _F32, _F32, _P, _I32, _P, _I32, _I32,
                                _F32, _I32, _P, _SZ, _P, _P], ctypes.c_int),
@@ -375,6 +377,13 @@ def pa_cascade_workspace_bytes(B: int, Hq: int, Hkv: int, D: int, n_prefix_block
                                max_blocks_per_seq: int, block_size: int) -> int:
     return int(lib().pa_cascade_workspace_bytes(B, Hq, Hkv, D, n_prefix_blocks, max_blocks_per_seq,
                                                 block_size))
+
+
+def pa_cascade_pays(B: int, Hkv: int, D: int, n_prefix_blocks: int, block_size: int) -> bool:
+    """Whether pa_decode_cascade runs the cascade (True) or plain split decode."""
+    r = lib().pa_cascade_pays(B, Hkv, D, n_prefix_blocks, block_size)
+    _check("pa_cascade_pays", min(r, 0))
+    return r == 1
 
 
 @_on_tensors_device

@@ -212,6 +212,19 @@ def qwen3_0p6b(B: int = 256, **kw) -> DecodeWorkload:
                          max_blocks=128, shared_prefix_blocks=8, seed=1005, **kw)
 
 
+def qwen3_long_prefix(B: int = 256, prefix_blocks: int = 128, **kw) -> DecodeWorkload:
+    """Qwen3-0.6B-shaped batch behind a long shared prefix (a system prompt held
+    once in the prefix cache): B=256, Hq=16, Hkv=8, D=128, bs=16; the first
+    prefix_blocks table entries (2048 tokens) are the same blocks for every
+    sequence, then each sequence's own U[1, 256] tokens."""
+    own = _uniform_lens(2006, B, 1, 256)
+    lens = [prefix_blocks * 16 + n for n in own]
+    return make_workload(f"qwen3-0.6b-B{B}-prefix{prefix_blocks * 16}", B=B, Hq=16, Hkv=8, D=128,
+                         block_size=16, seq_lens=lens, num_blocks=prefix_blocks + B * 16,
+                         max_blocks=prefix_blocks + 16, shared_prefix_blocks=prefix_blocks,
+                         seed=1006, **kw)
+
+
 def with_fp8_pools(w: DecodeWorkload) -> DecodeWorkload:
     """FP8 variant of a workload: the same bf16 pools rounded to e4m3 codes by
     torch's float8_e4m3fn cast, with one scale per pool chosen as amax / 448
@@ -277,6 +290,10 @@ WORKLOADS.update({
     "qwen2.5-1.5b-B8-spec4": lambda **kw: spec_verify("qwen2.5-1.5b-B8", 4, **kw),
     "qwen2.5-7b-bs16-spec4": lambda **kw: spec_verify("qwen2.5-7b-bs16", 4, **kw),
     "qwen3-0.6b-B256-spec4": lambda **kw: spec_verify("qwen3-0.6b-B256", 4, **kw),
+    # a long shared prefix (2048 tokens) in front of every sequence, decoded
+    # plainly and as a cascade
+    "qwen3-0.6b-B256-prefix2048": lambda **kw: qwen3_long_prefix(256, 128, **kw),
+    "qwen3-0.6b-B256-prefix2048-cascade": lambda **kw: _cascade(qwen3_long_prefix(256, 128, **kw), 128),
     # one 512-token chunked-prefill chunk per sequence on the Qwen2.5-1.5B layer
     "qwen2.5-1.5b-B1-chunk512": lambda **kw: prefill_chunk("qwen2.5-1.5b-B1", 512, **kw),
     "qwen2.5-1.5b-B8-chunk512": lambda **kw: prefill_chunk("qwen2.5-1.5b-B8", 512, **kw),

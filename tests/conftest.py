@@ -62,3 +62,18 @@ def merge_path():
                          pa.PA_MERGE_GRID if path == "grid" else pa.PA_MERGE_AUTO)
     yield _set
     pa.pa_set_option(pa.PA_OPT_SPLIT_MERGE, prev)
+
+
+@pytest.fixture
+def cascade_mode():
+    """Set PA_OPT_CASCADE ("auto", "always" or "never"); the previous value comes back after the test."""
+    from paged_kv_decode_cache_gb300 import build, pa
+    build.build()
+    prev = pa.pa_get_option(pa.PA_OPT_CASCADE)
+
+    def _set(mode):
+        pa.pa_set_option(pa.PA_OPT_CASCADE, {"auto": pa.PA_CASCADE_AUTO, "always": pa.PA_CASCADE_ALWAYS,
+                                             "never": pa.PA_CASCADE_NEVER}[mode])
+    yield _set
+    pa.pa_set_option(pa.PA_OPT_CASCADE, prev)
+

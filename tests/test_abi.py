@@ -289,25 +289,25 @@ def test_wrappers_run_on_their_tensors_device():
 
 
 def test_options_set_get_and_reject(lib):
-    prev = [pa.pa_get_option(o) for o in (pa.PA_OPT_DECODE_KERNEL, pa.PA_OPT_SPLIT_MERGE,
-                                          pa.PA_OPT_PDL)]
+    opts = (pa.PA_OPT_DECODE_KERNEL, pa.PA_OPT_SPLIT_MERGE, pa.PA_OPT_PDL, pa.PA_OPT_CASCADE)
+    prev = [pa.pa_get_option(o) for o in opts]
     try:
         for opt, values in ((pa.PA_OPT_DECODE_KERNEL, (0, 1, 2)), (pa.PA_OPT_SPLIT_MERGE, (0, 1)),
-                            (pa.PA_OPT_PDL, (0, 1))):
+                            (pa.PA_OPT_PDL, (0, 1)), (pa.PA_OPT_CASCADE, (0, 1, 2))):
             for v in values:
                 pa.pa_set_option(opt, v)
                 assert pa.pa_get_option(opt) == v
             assert lib.pa_set_option(opt, max(values) + 1) == pa.PA_EINVAL
             assert lib.pa_set_option(opt, -1) == pa.PA_EINVAL
-        assert lib.pa_set_option(3, 0) == pa.PA_EINVAL
-        assert lib.pa_get_option(3) == pa.PA_EINVAL
+        assert lib.pa_set_option(4, 0) == pa.PA_EINVAL
+        assert lib.pa_get_option(4) == pa.PA_EINVAL
         # the split policy follows the switch, not the environment
         pa.pa_set_option(pa.PA_OPT_DECODE_KERNEL, pa.PA_KERNEL_CUDA_CORE)
         assert lib.pa_choose_num_splits(1, 32, 2, 128, 16, 16, 152) == pa.PA_EUNSUPPORTED
         pa.pa_set_option(pa.PA_OPT_DECODE_KERNEL, pa.PA_KERNEL_AUTO)
         assert lib.pa_choose_num_splits(1, 32, 2, 128, 16, 16, 152) >= 1
     finally:
-        for o, v in zip((pa.PA_OPT_DECODE_KERNEL, pa.PA_OPT_SPLIT_MERGE, pa.PA_OPT_PDL), prev):
+        for o, v in zip(opts, prev):
             pa.pa_set_option(o, v)
 
 
@@ -363,4 +363,20 @@ def test_mq_split_policy_prefill_shape(lib, use_kernel):
     assert pa.pa_choose_num_splits_mq(2, 64, 28, 4, 128, 256, 16, 152) == 4        # 32 CTAs x 4
     # a 64k-token table needs at least 2 partitions of at most 32768 tokens
     assert pa.pa_choose_num_splits_mq(64, 128, 8, 1, 128, 4096, 16, 152) >= 2
+
+
+def test_cascade_runs_where_it_pays(lib, cascade_mode):
+    """The automatic choice: the cascade when (B - 1) x the prefix's K/V bytes
+    reach 256 MB; the switch forces either path."""
+    cascade_mode("auto")
+    assert not pa.pa_cascade_pays(256, 8, 128, 8, 16)      # 8 blocks: 255 x 512 KiB = 128 MiB
+    assert pa.pa_cascade_pays(256, 8, 128, 128, 16)        # 2048 tokens: 255 x 8 MiB
+    assert not pa.pa_cascade_pays(1, 8, 128, 4096, 16)     # one sequence: nothing to share
+    assert pa.pa_cascade_pays(5, 8, 128, 2048, 16)         # a 128 MiB prefix read 5 times
+    assert not pa.pa_cascade_pays(256, 8, 128, 0, 16)
+    assert lib.pa_cascade_pays(0, 8, 128, 8, 16) == pa.PA_EINVAL
+    cascade_mode("always")
+    assert pa.pa_cascade_pays(256, 8, 128, 8, 16)
+    cascade_mode("never")
+    assert not pa.pa_cascade_pays(256, 8, 128, 128, 16)
 

@@ -668,8 +668,12 @@ CASCADE = [
 ]
 
 
+@pytest.mark.parametrize("mode", ["always", "auto"])
 @pytest.mark.parametrize("case", CASCADE, ids=lambda c: f"Hq{c[0]}-Hkv{c[1]}-bs{c[2]}-B{len(c[3])}")
-def test_cascade_matches_oracle(case):
+def test_cascade_matches_oracle(case, mode, cascade_mode):
+    """The cascade (forced) and the automatic choice, which for these short
+    prefixes is plain split decode."""
+    cascade_mode(mode)
     Hq, Hkv, bs, lens, npre = case
     nb = sum((L + bs - 1) // bs for L in lens) + 5
     w = W.make_workload("casc", B=len(lens), Hq=Hq, Hkv=Hkv, D=128, block_size=bs, seq_lens=list(lens),
@@ -688,9 +692,14 @@ def test_cascade_matches_oracle(case):
     assert dev.status_value() == 0
 
 
-def test_cascade_full_size_qwen3():
-    """The Qwen3 batch (256 sequences, 8 shared prefix blocks) after this step's write."""
+@pytest.mark.parametrize("mode", ["always", "auto"])
+def test_cascade_full_size_qwen3(mode, cascade_mode):
+    """The Qwen3 batch (256 sequences, 8 shared prefix blocks) after this step's
+    write, through the cascade and through the automatic choice (plain split
+    decode: these 8 blocks are read from L2 faster than the cascade's launches)."""
+    cascade_mode(mode)
     w = W.WORKLOADS["qwen3-0.6b-B256-cascade"]()
+    assert pa.pa_cascade_pays(w.B, w.Hkv, w.D, w.cascade_blocks, w.block_size) == (mode == "always")
     kc, vc = oracle_after_write(w)
     ref, ref_lse = oracle.decode(w.q, kc, vc, w.block_tables, w.seq_lens, w.scale)
     dev = Dev(w)
@@ -704,6 +713,34 @@ def test_cascade_full_size_qwen3():
                          dev.block_tables, dev.seq_lens, w.scale, workspace=ws, status=dev.status)
     assert_close(bf16_dev_to_f64(out), ref, "cascade qwen3")
     assert_lse_close(lse.cpu().double().numpy(), ref_lse, "cascade qwen3")
+    assert dev.status_value() == 0
+
+
+@pytest.mark.parametrize("cascade", [True, False])
+def test_long_shared_prefix_full_size(cascade, cascade_mode):
+    """256 Qwen3-shaped sequences behind one 2048-token shared prefix, after
+    this step's write: the cascade (prefix once for the whole batch on the
+    prefill-shaped kernel, then each sequence's own blocks, then the merge)
+    and the plain fused step, every row against the oracle's plain decode."""
+    w = W.WORKLOADS["qwen3-0.6b-B256-prefix2048"]()
+    kc, vc = oracle_after_write(w)
+    ref, ref_lse = oracle.decode(w.q, kc, vc, w.block_tables, w.seq_lens, w.scale)
+    dev = Dev(w)
+    if cascade:
+        cascade_mode("auto")
+        assert pa.pa_cascade_pays(w.B, w.Hkv, w.D, 128, w.block_size)   # the automatic choice
+        dev.write()
+        npre = 128
+        ws = torch.zeros(pa.pa_cascade_workspace_bytes(w.B, w.Hq, w.Hkv, w.D, npre, w.max_blocks,
+                                                       w.block_size), dtype=torch.uint8, device="cuda")
+        out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device="cuda")
+        pa.pa_decode_cascade(out, lse, dev.q, dev.k_cache, dev.v_cache, npre, dev.block_tables,
+                             dev.seq_lens, w.scale, workspace=ws, status=dev.status)
+    else:
+        out, lse, _ = dev.step(0)
+    assert_close(bf16_dev_to_f64(out), ref, f"long prefix cascade={cascade}")
+    assert_lse_close(lse.cpu().double().numpy(), ref_lse, f"long prefix cascade={cascade}")
     assert dev.status_value() == 0
 
 
