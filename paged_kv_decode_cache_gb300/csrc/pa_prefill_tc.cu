@@ -19,14 +19,17 @@
 //        TMA lands it, read MN-major (no transpose).  p is a bf16 pair
 //        hi + lo carrying it to about 2^-17 relative (two MMAs per chunk).
 //
-// S (two buffers of 64 columns) and O (128 columns) live in TMEM, lane = row
-// r.  Warps 0-3 (softmax, thread = row r) load their S row, mask keys past the
-// range, past the row's causal position or in tiles not loaded, keep a
+// Two softmax warpgroups take alternate chunks: group g (warps 4g .. 4g + 3,
+// thread = row r) handles chunks g, g + 2, ... with its own S buffer, P buffer
+// and O accumulator in TMEM (lane = row r), so the two groups' exponentials
+// overlap each other and the MMAs.  A thread loads its S row, masks keys past
+// the range, past the row's causal position or in tiles not loaded, keeps a
 // per-row reference max that moves only when a score exceeds it by more than
-// 2^8 (the warp then rescales its rows of O in TMEM once the previous PV has
-// finished), and write the hi/lo rows of P; the epilogue normalises O and
+// 2^8 (the warp then rescales its rows of its group's O once the group's
+// previous PV has finished), and writes the hi/lo rows of P.  The epilogue
+// merges the two groups' (O, max, sum) like two partitions, normalises and
 // writes bf16 rows (or fp32 partials with the range split) by bulk copies.
-// Warp 4 issues QK, warp 7 issues PV; warps 5 and 6 stream K and V through
+// Warp 8 issues QK, warp 11 issues PV; warps 9 and 10 stream K and V through
 // 3-stage rings of 16 KB, one TMA box per 16-token tile and 64-element half.
 // A tile past the range or with a bad block id is loaded from a coordinate
 // past the pool, which fills the box with zeros.  Every wait is bounded.
@@ -43,11 +46,11 @@ namespace {
 
 constexpr int kPfRows = 128;                     // query rows per CTA (M of both MMAs)
 constexpr int kPfT = 64;                         // tokens per chunk (N of QK, K of PV)
-constexpr int kPfThreads = 256;
-constexpr int kPfQkWarp = 4, kPfTmaKWarp = 5, kPfTmaVWarp = 6, kPfPvWarp = 7;
+constexpr int kPfThreads = 384;                  // 2 softmax warpgroups, QK, K TMA, V TMA, PV
+constexpr int kPfQkWarp = 8, kPfTmaKWarp = 9, kPfTmaVWarp = 10, kPfPvWarp = 11;
 constexpr int kPfNK = 3, kPfNV = 3;              // K and V stages
-constexpr int kPfNS = 2;                         // S buffers in TMEM
-constexpr int kPfNP = 2;                         // P buffers (hi + lo) in shared memory
+constexpr int kPfNS = 2;                         // S buffers in TMEM (one per softmax group)
+constexpr int kPfNP = 2;                         // P buffers (hi + lo) in shared memory (one per group)
 constexpr int kPfTilesPerChunk = kPfT / kTile;   // 4
 constexpr int kPfHalf = kPfT * kSubBytes;        // one 64-element half of a chunk: 8 KB
 constexpr int kPfStage = 2 * kPfHalf;            // 16 KB
@@ -64,11 +67,12 @@ constexpr int kPfPOff = kPfQOff + 2 * kPfQHalf;
 constexpr int kPfRowsOff = kPfPOff + kPfNP * kPfPBuf;
 constexpr int kPfBarOff = kPfRowsOff + kPrefillMaxTiles * 4;
 constexpr int kPfNumBars = 2 * kPfNK + 2 * kPfNV + 2 * kPfNS + 2 * kPfNP;
-constexpr int kPfMiscOff = kPfBarOff + kPfNumBars * 8;
+constexpr int kPfXOff = kPfBarOff + kPfNumBars * 8;   // group 1's row maxima and sums [2][128]
+constexpr int kPfMiscOff = kPfXOff + 2 * kPfRows * 4;
 constexpr int kPfSmemBytes = kPfMiscOff + 16 + 1024;   // + room to align the base to 1024
-constexpr uint32_t kPfTmemCols = 256;                  // S: 2 x 64 columns, then O: 128
-constexpr int kPfColO = kPfNS * kPfT;
-static_assert(kPfColO + 128 <= static_cast<int>(kPfTmemCols), "TMEM columns");
+constexpr uint32_t kPfTmemCols = 512;                  // S: 2 x 64 columns, then O0, O1: 128 each
+constexpr int kPfColO = kPfNS * kPfT;                  // O of group g at kPfColO + 128 g
+static_assert(kPfColO + 2 * 128 <= static_cast<int>(kPfTmemCols), "TMEM columns");
 static_assert(kPfSmemBytes <= 227 * 1024, "shared memory");
 static_assert(kPfNP * kPfPBuf >= kPfRows * 128 * 4, "the epilogue stages fp32 rows in the P buffers");
 static_assert(kPfStage % 1024 == 0 && kPfQHalf % 1024 == 0 && kPfPPart % 1024 == 0, "swizzle atoms");
@@ -146,18 +150,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         else set_status(p.status, PA_STATUS_BAD_BLOCK);
         tile_row[i] = row;
     }
-    constexpr int kQLoads = kPfRows * (D / 8) / kPfThreads;  // 16-byte chunks per thread
+    constexpr int kQChunks = kPfRows * (D / 8);                       // 16-byte chunks of the tile
+    constexpr int kQLoads = (kQChunks + kPfThreads - 1) / kPfThreads;  // per thread
     uint4 qv[kQLoads];
 #pragma unroll
     for (int j = 0; j < kQLoads; ++j) {
         const int i = tid + j * kPfThreads, r = i / (D / 8), c = i % (D / 8);
         qv[j] = make_uint4(0u, 0u, 0u, 0u);
-        if (r < nrows) qv[j] = *reinterpret_cast<const uint4 *>(p.q + out_row(r) * D + c * 8);
+        if (i < kQChunks && r < nrows) qv[j] = *reinterpret_cast<const uint4 *>(p.q + out_row(r) * D + c * 8);
     }
 #pragma unroll
     for (int j = 0; j < kQLoads; ++j) {  // Q[r][d]: half d / 64, swizzled 16-byte chunk
         const int i = tid + j * kPfThreads, r = i / (D / 8), c = i % (D / 8);
-        *reinterpret_cast<uint4 *>(qs + (c >> 3) * kPfQHalf + swz128(r, c & 7)) = qv[j];
+        if (i < kQChunks) *reinterpret_cast<uint4 *>(qs + (c >> 3) * kPfQHalf + swz128(r, c & 7)) = qv[j];
     }
     if (warp == 0) tc5::tmem_alloc(tmem_slot, kPfTmemCols);
     if (tid == 0) {
@@ -171,10 +176,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         }
         for (int i = 0; i < kPfNS; ++i) {
             mbar_init(&sdone[i], 1u);
-            mbar_init(&sfree[i], 128u);  // the 128 softmax threads release an S buffer
+            mbar_init(&sfree[i], 128u);  // the 128 threads of softmax group i release S buffer i
         }
         for (int i = 0; i < kPfNP; ++i) {
-            mbar_init(&pready[i], 128u);  // ... and publish a P buffer
+            mbar_init(&pready[i], 128u);  // ... and publish P buffer i
             mbar_init(&pfree[i], 1u);
         }
         *abort_flag = 0;
@@ -201,7 +206,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     };
 
     if (warp == kPfTmaKWarp || warp == kPfTmaVWarp) {
-        // ================= TMA producers: K (warp 5), V (warp 6) =================
+        // ================= TMA producers: K (warp 9), V (warp 10) =================
         // lanes 0-7: lane = 2 * tile + half issues that box of each chunk
         const bool is_v = warp == kPfTmaVWarp;
         uint8_t *ring = is_v ? vring : kring;
@@ -267,13 +272,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 tc5::fence_after_sync();
                 const uint8_t *vt = vring + (c % kPfNV) * kPfStage;
                 const uint8_t *pb = ps + (c % kPfNP) * kPfPBuf;
+                const uint32_t ocol = tmem + kPfColO + (c % 2) * 128;  // the O of chunk c's group
 #pragma unroll
                 for (int hl = 0; hl < 2; ++hl) {  // hi part, then lo part of p
 #pragma unroll
                     for (int j = 0; j < kPfT / 16; ++j)  // K = 16 tokens per MMA
-                        tc5::mma_bf16(tmem + kPfColO, tc5::sw128_desc(pb + hl * kPfPPart + j * 32, 16, 1024),
+                        tc5::mma_bf16(ocol, tc5::sw128_desc(pb + hl * kPfPPart + j * 32, 16, 1024),
                                       tc5::sw128_desc(vt + j * 16 * kSubBytes, kPfHalf, 1024), kIdPV,
-                                      c > 0 || hl > 0 || j > 0);
+                                      c >= 2 || hl > 0 || j > 0);
                 }
                 tc5::commit(&pfree[c % kPfNP]);
                 tc5::commit(&vempty[c % kPfNV]);
@@ -283,33 +289,32 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 mbar_wait_bounded(&pfree[(done - 1) % kPfNP], ((done - 1) / kPfNP) & 1);
         }
     } else {
-        // ================= softmax warps: thread = query row r =================
-        const int r = tid;
+        // ================= softmax groups: group grp = warp / 4, thread = query row r =================
+        const int grp = warp >> 2, wq = warp & 3;  // wq: this warp's quarter of the TMEM lanes
+        const int r = tid & (kPfRows - 1);
         const bool row_ok = r < nrows;
         const int pos = p.causal ? qbase + r / G : L - 1;  // the last key row r sees
         const float sl2 = p.scale_log2;
+        const uint32_t ocol = tmem + kPfColO + grp * 128;   // this group's O
+        uint8_t *prow = ps + grp * kPfPBuf + r * kSubBytes;   // this group's P row r
         float m_ref = -INFINITY, l = 0.f;
-        bool dead = false;
-        for (int c = 0; c < nch; ++c) {
-            const int sb = c % kPfNS, pb = c % kPfNP;
-            const bool ok = __all_sync(0xffffffffu, wait_or_abort(&sdone[sb], (c / kPfNS) & 1));
+        for (int c = grp; c < nch; c += 2) {
+            const bool ok = __all_sync(0xffffffffu, wait_or_abort(&sdone[grp], (c / 2) & 1));
             float sv[kPfT];
             if (ok) {
                 tc5::fence_after_sync();
-                uint32_t raw[kPfT / 16][16];
+                uint32_t raw[kPfT];
 #pragma unroll
                 for (int k = 0; k < kPfT / 16; ++k)
-                    tc5::ld_32x32b_x16_nowait(tc5::taddr(tmem, 32 * warp, sb * kPfT + 16 * k), raw[k]);
+                    tc5::ld_32x32b_x16_nowait(tc5::taddr(tmem, 32 * wq, grp * kPfT + 16 * k),
+                                              *reinterpret_cast<uint32_t(*)[16]>(&raw[16 * k]));
                 tc5::wait_ld();
 #pragma unroll
-                for (int k = 0; k < kPfT; ++k) sv[k] = __uint_as_float(raw[k / 16][k % 16]);
+                for (int k = 0; k < kPfT; ++k) sv[k] = __uint_as_float(raw[k]);
             }
             tc5::fence_before_sync();
-            mbar_arrive(&sfree[sb]);  // S buffer read: QK c + NS may overwrite it
-            if (!ok || *abort_flag) {
-                dead = true;
-                break;
-            }
+            mbar_arrive(&sfree[grp]);  // S buffer read: QK c + 2 may overwrite it
+            if (!ok || *abort_flag) break;
             const int tok0 = t_begin + c * kPfT;
             bool tile_ok[kPfTilesPerChunk];
             bool all_tiles = true;
@@ -338,56 +343,59 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                     mx = fmaxf(mx, sv[k]);
                 }
             }
+            // The group's previous PV (chunk c - 2) must be done before its O is
+            // rescaled or its P buffer rewritten.
+            const bool prev_done =
+                c < 2 || __all_sync(0xffffffffu, wait_or_abort(&pfree[grp], ((c / 2) - 1) & 1));
             // Lazy rescaling: a row's reference max moves only when a score exceeds
             // it by more than 2^8; the warp then rescales its 32 rows of O together
-            // (TMEM loads and stores are warp-wide) once PV c - 1 has finished.
+            // (TMEM loads and stores are warp-wide).
             if (__any_sync(0xffffffffu, mx > m_ref + kPfLazyTau)) {
                 const float mn = fmaxf(m_ref, mx);
                 const float alpha = mn == -INFINITY ? 1.f : fast_exp2(m_ref - mn);
                 l *= alpha;
-                if (c > 0) {
-                    const bool ok2 = __all_sync(
-                        0xffffffffu, wait_or_abort(&pfree[(c - 1) % kPfNP], ((c - 1) / kPfNP) & 1));
-                    if (ok2) {
-                        tc5::fence_after_sync();
+                if (c >= 2 && prev_done) {
+                    tc5::fence_after_sync();
 #pragma unroll 1
-                        for (int k = 0; k < D / 16; ++k) {
-                            float ov[16];
-                            const uint32_t ta = tc5::taddr(tmem, 32 * warp, kPfColO + 16 * k);
-                            tc5::ld_32x32b_x16(ta, ov);
+                    for (int k = 0; k < D / 16; ++k) {
+                        float ov[16];
+                        const uint32_t ta = tc5::taddr(ocol, 32 * wq, 16 * k);
+                        tc5::ld_32x32b_x16(ta, ov);
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) ov[i] *= alpha;
-                            tc5::st_32x32b_x16(ta, ov);
-                        }
+                        for (int i = 0; i < 16; ++i) ov[i] *= alpha;
+                        tc5::st_32x32b_x16(ta, ov);
                     }
                 }
                 m_ref = mn;
             }
-            // p = hi + lo, two bf16 values per word.  A masked score is -inf and
-            // gives p = 0 (a row that has seen no key yet subtracts 0, not -inf).
-            // The row sum adds p itself: hi + lo equals it to about 2^-17.
+            // p = hi + lo, two bf16 values per word, written in two halves of 32
+            // tokens.  A masked score is -inf and gives p = 0 (a row that has seen
+            // no key yet subtracts 0, not -inf).  The row sum adds p itself: hi +
+            // lo equals it to about 2^-17.
             const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-            uint32_t hw[kPfT / 2], lw[kPfT / 2];
 #pragma unroll
-            for (int k = 0; k < kPfT; k += 2) {
-                const float p0 = fast_exp2(sv[k] - m_use);
-                const float p1 = fast_exp2(sv[k + 1] - m_use);
-                const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
-                const float2 hf = __bfloat1622float2(h);
-                const __nv_bfloat162 lo = __floats2bfloat162_rn(p0 - hf.x, p1 - hf.y);
-                hw[k / 2] = *reinterpret_cast<const uint32_t *>(&h);
-                lw[k / 2] = *reinterpret_cast<const uint32_t *>(&lo);
-                l += p0 + p1;
-            }
-            if (c >= kPfNP) wait_or_abort(&pfree[pb], ((c / kPfNP) - 1) & 1);  // PV c - NP is done
-            uint8_t *prow = ps + pb * kPfPBuf + r * kSubBytes;
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t hw[kPfT / 4], lw[kPfT / 4];
 #pragma unroll
-            for (int j = 0; j < kPfT / 8; ++j) {  // 16-byte chunk j holds tokens 8j .. 8j + 7
-                const uint32_t off = static_cast<uint32_t>((j ^ (r & 7)) << 4);
-                *reinterpret_cast<uint4 *>(prow + off) =
-                    make_uint4(hw[4 * j], hw[4 * j + 1], hw[4 * j + 2], hw[4 * j + 3]);
-                *reinterpret_cast<uint4 *>(prow + kPfPPart + off) =
-                    make_uint4(lw[4 * j], lw[4 * j + 1], lw[4 * j + 2], lw[4 * j + 3]);
+                for (int k = 0; k < kPfT / 2; k += 2) {
+                    const float p0 = fast_exp2(sv[hf * kPfT / 2 + k] - m_use);
+                    const float p1 = fast_exp2(sv[hf * kPfT / 2 + k + 1] - m_use);
+                    const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+                    const float2 hv = __bfloat1622float2(h);
+                    const __nv_bfloat162 lo = __floats2bfloat162_rn(p0 - hv.x, p1 - hv.y);
+                    hw[k / 2] = *reinterpret_cast<const uint32_t *>(&h);
+                    lw[k / 2] = *reinterpret_cast<const uint32_t *>(&lo);
+                    l += p0 + p1;
+                }
+#pragma unroll
+                for (int j = 0; j < kPfT / 16; ++j) {  // 16-byte chunk 4 hf + j: tokens 8 (4 hf + j) ..
+                    const int ch = 4 * hf + j;
+                    const uint32_t off = static_cast<uint32_t>((ch ^ (r & 7)) << 4);
+                    *reinterpret_cast<uint4 *>(prow + off) =
+                        make_uint4(hw[4 * j], hw[4 * j + 1], hw[4 * j + 2], hw[4 * j + 3]);
+                    *reinterpret_cast<uint4 *>(prow + kPfPPart + off) =
+                        make_uint4(lw[4 * j], lw[4 * j + 1], lw[4 * j + 2], lw[4 * j + 3]);
+                }
             }
             // V rows that were loaded from the pool but lie past the range (the
             // tail of the tile holding key t_end - 1) may hold anything, even
@@ -397,7 +405,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 const int z1 = min(kPfT, (t_end + kTile - 1) / kTile * kTile - tok0);
                 if (z1 > z0 && wait_or_abort(&vfull[c % kPfNV], (c / kPfNV) & 1)) {
                     uint8_t *vt = vring + (c % kPfNV) * kPfStage;
-                    for (int i = tid; i < (z1 - z0) * 16; i += 128) {
+                    for (int i = r; i < (z1 - z0) * 16; i += kPfRows) {
                         const int row = z0 + i / 16, hc = i % 16;
                         *reinterpret_cast<uint4 *>(vt + (hc >> 3) * kPfHalf + swz128(row, hc & 7)) =
                             make_uint4(0u, 0u, 0u, 0u);
@@ -406,32 +414,55 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             }
             fence_proxy_async_smem();  // P (and zeroed V rows) are read by the MMA
             tc5::fence_before_sync();
-            mbar_arrive(&pready[pb]);
+            mbar_arrive(&pready[grp]);
         }
 
-        // ---- epilogue: O row r, normalised, staged in the idle P buffers, bulk-copied out ----
-        const bool okf = !dead && __all_sync(0xffffffffu, wait_or_abort(&pfree[(nch - 1) % kPfNP],
-                                                                        ((nch - 1) / kPfNP) & 1));
+        // ---- epilogue: the two groups' rows merged, normalised, staged in the idle P
+        //      buffers and bulk-copied out by group 0 ----
+        float *xm = reinterpret_cast<float *>(smem + kPfXOff), *xl = xm + kPfRows;
+        if (grp == 1) {
+            xm[r] = m_ref;
+            xl[r] = l;
+        }
+        named_sync(1, 2 * kPfRows);
+        // every PV has completed once the last one has (one issuer, committed in order)
+        const bool okf = grp == 0 && __all_sync(0xffffffffu, wait_or_abort(&pfree[(nch - 1) % 2],
+                                                                           ((nch - 1) / 2) & 1)) &&
+                         *abort_flag == 0;
         if (okf) {
             tc5::fence_after_sync();
+            const bool has1 = nch >= 2;  // group 1 took a chunk: its O holds data
+            const float m1 = has1 ? xm[r] : -INFINITY, l1 = has1 ? xl[r] : 0.f;
+            const float M = fmaxf(m_ref, m1);
+            const float a0 = m_ref == -INFINITY ? 0.f : fast_exp2(m_ref - M);
+            const float a1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - M);
+            const float lt = a0 * l + a1 * l1;
+            const float inv = lt > 0.f ? p.v_scale / lt : 0.f;  // 0: no key seen
+            const float w0 = a0 * inv, w1 = a1 * inv;
             const bool split = p.split != 0;
-            const float inv = l > 0.f ? p.v_scale / l : 0.f;  // 0: no key seen
             uint8_t *stage = ps + r * (split ? D * 4 : D * 2);
 #pragma unroll 1
             for (int k = 0; k < D / 16; ++k) {
-                float ov[16];
-                tc5::ld_32x32b_x16(tc5::taddr(tmem, 32 * warp, kPfColO + 16 * k), ov);
+                float ov[16], o1[16];
+                tc5::ld_32x32b_x16(tc5::taddr(tmem + kPfColO, 32 * wq, 16 * k), ov);
+                if (has1) {
+                    tc5::ld_32x32b_x16(tc5::taddr(tmem + kPfColO + 128, 32 * wq, 16 * k), o1);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) ov[i] = ov[i] * w0 + o1[i] * w1;
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) ov[i] *= w0;
+                }
                 if (split) {
                     float4 *dst = reinterpret_cast<float4 *>(stage) + 4 * k;
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
-                        dst[i] = make_float4(ov[4 * i] * inv, ov[4 * i + 1] * inv, ov[4 * i + 2] * inv,
-                                             ov[4 * i + 3] * inv);
+                        dst[i] = make_float4(ov[4 * i], ov[4 * i + 1], ov[4 * i + 2], ov[4 * i + 3]);
                 } else {
                     uint32_t w[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        const __nv_bfloat162 h = __floats2bfloat162_rn(ov[2 * i] * inv, ov[2 * i + 1] * inv);
+                        const __nv_bfloat162 h = __floats2bfloat162_rn(ov[2 * i], ov[2 * i + 1]);
                         w[i] = *reinterpret_cast<const uint32_t *>(&h);
                     }
                     uint4 *dst = reinterpret_cast<uint4 *>(stage) + 2 * k;
@@ -441,7 +472,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             }
             fence_proxy_async_smem();  // the bulk copy (async proxy) reads the staged row
             if (row_ok) {
-                const float lse = l > 0.f ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
+                const float lse = lt > 0.f ? (M + log2f(lt)) * 0.69314718055994531f : -INFINITY;
                 const int64_t o = out_row(r);
                 if (split) {
                     const int64_t slot = o * p.part_stride + p.part_offset + part;
