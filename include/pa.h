@@ -337,12 +337,14 @@ int pa_decode_step(void *out, float *lse, const void *q, const void *k_new, cons
  * nothing: out = 0, lse = -inf).
  * q: device bf16 [B, q_len, Hq, D]; out: device bf16 [B, q_len, Hq, D];
  * lse: device fp32 [B, q_len, Hq] or NULL.  1 <= q_len <= 65535.
- * Supported: D = 128, G = Hq / Hkv <= 32 (the tensor-core kernel; q_len > 1
- * with the CUDA-core kernel forced, or D = 64, is PA_EUNSUPPORTED).  A CTA holds
- * up to 32 / G query positions of its heads; more positions are spread over
- * more CTAs, each reading the keys its queries can see (for q_len * G > 32
- * the KV is read about q_len * G / 32 times: suited to verification, not to
- * long prefill chunks).
+ * Supported: D = 128, G = Hq / Hkv <= 32 (the tensor-core kernels; q_len > 1
+ * with the CUDA-core kernel forced, or D = 64, is PA_EUNSUPPORTED).  Two
+ * kernels serve it: with q_len * G <= 32 (verification of a few drafted
+ * tokens) the decode kernel holds the q_len positions of a KV head's G query
+ * heads as MMA columns in one CTA; with more (a chunked-prefill chunk, e.g.
+ * 512 tokens) a prefill-shaped kernel holds 128 query rows (128 / G
+ * positions x G heads) per CTA on the MMA's M side and reads each KV block
+ * once per such tile (split partials are then merged by the combine step).
  * num_splits: 0 = pa_choose_num_splits_mq on the current device, 1 = no
  * split (no workspace), P > 1 = split with the workspace contract of
  * pa_decode_splitkv for pa_splitkv_workspace_bytes(B * q_len, Hq, D, P)
