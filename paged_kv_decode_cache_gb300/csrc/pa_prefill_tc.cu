@@ -399,7 +399,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             }
             // V rows that were loaded from the pool but lie past the range (the
             // tail of the tile holding key t_end - 1) may hold anything, even
-            // NaN: they are zeroed, so that 0 * V never reaches O.
+            // NaN: they are zeroed, so that 0 * V never reaches O.  (The wait on
+            // the V stage is in chunk c's phase: PV c - 2 has finished, and the
+            // one PV issuer works in chunk order, so PV c - 3, the stage's
+            // previous user, was issued before it.)
             if (c == nch - 1) {
                 const int z0 = t_end - tok0;
                 const int z1 = min(kPfT, (t_end + kTile - 1) / kTile * kTile - tok0);
