@@ -422,9 +422,9 @@ int pa_cache_write_fp8(const void *k_new, const void *v_new, const int64_t *slot
  * results (num_splits 0 = pa_auto_num_splits, 1 = no split and no workspace,
  * the same workspace contract otherwise), with k_cache / v_cache e4m3 pools
  * and their scales.  The result is attention over the dequantised values
- * (code * scale); the tensor-core kernel widens each landed tile to fp16
- * exactly and runs its MMAs in fp16 (q is rounded to fp16: |q| must stay below
- * 65504).  Supported: head_dim 128, Hq / Hkv <= 32 (PA_EUNSUPPORTED
+ * (code * scale); the tensor-core kernel keeps the codes one byte wide in
+ * shared memory, widens each chunk to fp16 exactly into tensor memory and runs
+ * its MMAs in fp16 (q is rounded to fp16: |q| must stay below 65504).  Supported: head_dim 128, Hq / Hkv <= 32 (PA_EUNSUPPORTED
  * otherwise, and with the CUDA-core kernel forced).
  */
 int pa_decode_splitkv_fp8(void *out, float *lse, const void *q, const void *k_cache,

@@ -45,7 +45,7 @@
 //        commits to the barriers that publish S, release the K stage, release
 //        the P buffer and the V stage.
 //   warps 5, 6 (TMA): stream K and V through separate rings (NK and NV
-//        stages of 32 KB).  Block ids arrive by cp.async into a small ring
+//        stages of 32 KB, 16 KB with FP8 pools).  Block ids arrive by cp.async into a small ring
 //        kTcLook chunks ahead of use, so an issue never waits on a lookup
 //        queued behind the KV stream.  Tiles past the range or with a bad
 //        block id are not loaded; the K producer publishes, per chunk, a
@@ -54,10 +54,12 @@
 //        invalid row's V is zeroed.  With new K/V rows given, the producer
 //        whose range holds position L - 1 writes them into the pool through
 //        the slot mapping just before loading that tile.
-//   warps 8-11 (FP8 pools only): the producers land e4m3 codes in the upper
-//        half of a stage; these warps widen them to fp16 in place (K by 8, 9,
-//        V by 10, 11) and release the stage to the MMAs.  k_scale is folded
-//        into the softmax scale and v_scale into the epilogue.
+//   warps 8-11 (FP8 pools only): the producers land the e4m3 codes in 16 KB
+//        stages (so twice the token rows are in flight for the same shared
+//        memory); warp 8 + q widens TMEM lanes 32 q .. 32 q + 31 of each
+//        chunk's K and V^T into fp16 operand buffers in TMEM (two per tensor),
+//        from which the QK and PV MMAs read their A operand.  k_scale is
+//        folded into the softmax scale and v_scale into the epilogue.
 // With the range split, the CTAs of one (sequence, head group) merge their
 // partials in the same launch: once all P have arrived, they share the
 // merge tasks, through global memory or, as one thread-block cluster,
@@ -82,9 +84,7 @@ namespace pa {
 
 constexpr int kTcRows = 128;           // rows m per chunk (M of QK)
 constexpr int kTcThreads = 256;        // 4 softmax warps + 2 MMA warps + 2 TMA warps
-constexpr int kTcThreadsF8 = 384;      // FP8 pools: + 4 warps that widen the e4m3 tiles
-constexpr int kTcCvtKWarp = 8;         // warps 8, 9: K converters; 10, 11: V converters
-constexpr int kTcCvtVWarp = 10;
+constexpr int kTcCvtWarp = 8;          // FP8 pools: first of the warps that widen the e4m3 codes
 constexpr int kTcQkWarp = 4;
 constexpr int kTcTmaKWarp = 5;
 constexpr int kTcTmaVWarp = 6;
@@ -99,6 +99,11 @@ constexpr int kTcSmemLimit = 227 * 1024;
 template <int HC, int GP, bool F8 = false>
 struct TcCfg {
     static constexpr int kN = HC * GP;                          // MMA N
+    // FP8 converter warps: 8 (warps 8-11 widen K, 12-15 V) where the softmax
+    // fits the 128 registers a thread of 512 gets (MMA N <= 32, GP <= 8), else
+    // 4 (each widens K, then V, of its TMEM lane quarter)
+    static constexpr int kCvtWarps = !F8 ? 0 : (kN <= 32 && GP <= 8) ? 8 : 4;
+    static constexpr int kThreads = kTcThreads + 32 * kCvtWarps;
     static_assert(kN % 16 == 0 && kN >= 16 && kN <= 64, "MMA N");
     static constexpr int kT = kTcRows / HC;                     // tokens per chunk
     static constexpr int kTiles = kT / kTile;                   // 16-token tiles per chunk
@@ -125,48 +130,72 @@ struct TcCfg {
     // GP + 1 floats apart where that fits (a warp's stores then fall in 32
     // different banks; GP apart they share 32 / GP banks).
     static constexpr int red_bytes(int gpr) { return (kTcRows * gpr + 4 * kN) * 4 + 16; }
+    // S buffers in TMEM (FP8 pools with N = 64 keep 2, to leave room for the
+    // widened operands)
+    static constexpr int kNBS = (F8 && kN == 64) ? 2 : kTcNBS;
+    // chunk validity masks the producers publish (ring slots)
+    static constexpr int kMaskRing = F8 ? 16 : kTcMaskRing;
+    // A K (V) stage in shared memory: a bf16 chunk (32 KB), or with FP8 pools
+    // the chunk's one-byte codes (16 KB), which the converter warps widen into
+    // TMEM (the MMAs read their A operands there).
+    static constexpr int kStageBytes = F8 ? kTcRows * 128 : kTileBytes;
     // shared memory for nk K stages, nv V stages and nbp P^T buffers, laid out
     // as below (rings, Q, P^T, scratch, barriers, masks, block-id rings, align)
-    // (FP8: a "converted" barrier per K and V stage and the V producer's mask ring)
+    // (FP8: the operand buffers' "widened" and "released" barriers, 2 each for
+    // K and V, and the V producer's mask ring)
     static constexpr int smem_for(int nk, int nv, int nbp, int gpr = GP) {
-        return ((nk + nv) * kTileBytes + kQBytes + nbp * kPBufBytes + red_bytes(gpr) + 7) / 8 * 8 +
-               (2 * nk + 2 * nv + 2 * kTcNBS + 2 * nbp + (F8 ? nk + nv : 0)) * 8 +
-               kTcMaskRing * 8 * (F8 ? 2 : 1) + 2 * (kTcLook + 1) * 32 * 4 + 1024;
+        return ((nk + nv) * kStageBytes + kQBytes + nbp * kPBufBytes + red_bytes(gpr) + 7) / 8 * 8 +
+               (2 * nk + 2 * nv + 2 * kNBS + 2 * nbp + (F8 ? 8 : 0)) * 8 +
+               kMaskRing * 8 * (F8 ? 2 : 1) + 2 * (kTcLook + 1) * 32 * 4 + 1024;
     }
-    // the deepest pipeline that fits: K and V stages first, then P^T buffers
+    // bf16: the deepest pipeline that fits: K and V stages first, then P^T buffers
     static constexpr int choice_for(int gpr) {
         return smem_for(3, 3, 2, gpr) <= kTcSmemLimit ? 0
                : smem_for(3, 3, 1, gpr) <= kTcSmemLimit ? 1
                : smem_for(2, 3, 2, gpr) <= kTcSmemLimit ? 2
                : smem_for(2, 2, 2, gpr) <= kTcSmemLimit ? 3 : 4;
     }
+    // FP8: the most code stages (as many K as V) that fit beside two P^T buffers
+    static constexpr int f8_stages(int gpr) {
+        return smem_for(6, 6, 2, gpr) <= kTcSmemLimit ? 6
+               : smem_for(5, 5, 2, gpr) <= kTcSmemLimit ? 5
+               : smem_for(4, 4, 2, gpr) <= kTcSmemLimit ? 4 : 3;
+    }
+    static constexpr int depth_for(int gpr) { return F8 ? f8_stages(gpr) : choice_for(gpr); }
     // the padded scratch only where it costs no pipeline depth
-    static constexpr int kGPr = choice_for(GP + 1) == choice_for(GP) ? GP + 1 : GP;
+    static constexpr int kGPr = depth_for(GP + 1) == depth_for(GP) ? GP + 1 : GP;
     static constexpr int kRedBytes = red_bytes(kGPr);
     static constexpr int kChoice = choice_for(kGPr);
-    static constexpr int kNK = kChoice <= 1 ? 3 : 2;            // K stages
-    static constexpr int kNV = kChoice <= 2 ? 3 : 2;            // V stages
-    static constexpr int kNBP = (kChoice == 1 || kChoice == 4) ? 1 : 2;  // P^T buffers
-    static constexpr int kVOff = kNK * kTileBytes;
-    static constexpr int kQOff = (kNK + kNV) * kTileBytes;
+    static constexpr int kNK = F8 ? f8_stages(kGPr) : kChoice <= 1 ? 3 : 2;  // K stages
+    static constexpr int kNV = F8 ? f8_stages(kGPr) : kChoice <= 2 ? 3 : 2;  // V stages
+    static constexpr int kNBP = F8 ? 2 : (kChoice == 1 || kChoice == 4) ? 1 : 2;  // P^T buffers
+    static constexpr int kVOff = kNK * kStageBytes;
+    static constexpr int kQOff = (kNK + kNV) * kStageBytes;
     static constexpr int kPOff = kQOff + kQBytes;
     static constexpr int kRedOff = kPOff + kNBP * kPBufBytes;
     static constexpr int kBarOff = (kRedOff + kRedBytes + 7) / 8 * 8;
-    static constexpr int kNumBars = 2 * kNK + 2 * kNV + 2 * kTcNBS + 2 * kNBP + (F8 ? kNK + kNV : 0);
-    // validity masks [kTcMaskRing] (u64: chunk << 32 | lane mask), then the two
+    static constexpr int kNumBars = 2 * kNK + 2 * kNV + 2 * kNBS + 2 * kNBP + (F8 ? 8 : 0);
+    // validity masks [kMaskRing] (u64: chunk << 32 | lane mask), then the two
     // producers' block-id rings [2][kTcLook + 1][32 lanes]
     static constexpr int kMaskOff = kBarOff + kNumBars * 8;
-    static constexpr int kVMaskOff = kMaskOff + kTcMaskRing * 8;   // FP8 only
-    static constexpr int kLookOff = kVMaskOff + (F8 ? kTcMaskRing * 8 : 0);
+    static constexpr int kVMaskOff = kMaskOff + kMaskRing * 8;   // FP8 only
+    static constexpr int kLookOff = kVMaskOff + (F8 ? kMaskRing * 8 : 0);
     static constexpr int kSmemBytes = kLookOff + 2 * (kTcLook + 1) * 32 * 4 + 1024;
     static_assert(kSmemBytes == smem_for(kNK, kNV, kNBP, kGPr), "layout");
     // the K producer rewrites mask slot c % ring only once softmax c has read it
-    static_assert(kNK + kTcNBS <= kTcMaskRing, "mask ring");
+    // (FP8: the producer runs at most NK stages, 3 chunks of converter and
+    // operand buffers and NBS S buffers ahead of the softmax)
+    static_assert(kNK + kNBS + (F8 ? 3 : 0) <= kMaskRing, "mask ring");
     static_assert(kSmemBytes <= kTcSmemLimit, "shared memory");
-    // S buffers (NBS x N columns), then O^T: hi part (N) and lo part (N)
-    static constexpr uint32_t kTmemCols = (kTcNBS + 2) * kN <= 128 ? 128u
-                                          : (kTcNBS + 2) * kN <= 256 ? 256u : 512u;
-    static constexpr int kColO = kTcNBS * kN;
+    // TMEM: S buffers (NBS x N columns), O^T (hi part N, lo part N), then with
+    // FP8 pools the widened K and V^T operands, two buffers of 64 columns each
+    // (128 rows x 128 16-bit values), starting on a 64-column boundary
+    static constexpr int kColO = kNBS * kN;
+    static constexpr int kColK = (kColO + 2 * kN + 63) / 64 * 64;
+    static constexpr int kColV = kColK + 128;
+    static constexpr int kColsUsed = F8 ? kColV + 128 : kColO + 2 * kN;
+    static constexpr uint32_t kTmemCols = kColsUsed <= 128 ? 128u : kColsUsed <= 256 ? 256u : 512u;
+    static_assert(kColsUsed <= 512, "TMEM columns");
 };
 
 // Max (or sum) over the rows of column n's head of a [128 rows][GPr] array:
@@ -223,14 +252,25 @@ __device__ __forceinline__ void e4m3x16_to_f16(const uint4 &in, uint4 &lo, uint4
     hi = make_uint4(c.x, c.y, d.x, d.y);
 }
 
+// FP8 pools: the widened V^T operand in TMEM.  Its lanes are 16-lane groups
+// of 16 head dims, 8 x 8 transposed loads giving each thread dims 2 i and
+// 2 i + 1 of a group, which 16-lane stores put in lanes i and i + 8: lane L
+// holds dim vt_dim(L).  Its columns pair rows of 16-row groups the same way
+// (rows 2 j, 2 j + 1 and 8 + 2 j, 9 + 2 j of a group share the thread, and
+// land in adjacent columns): row m is index vt_row_k(m) of the contraction.
+__host__ __device__ constexpr int vt_dim(int L) { return (L & ~15) | ((L & 7) << 1) | ((L >> 3) & 1); }
+__host__ __device__ constexpr int vt_row_k(int m) {
+    return (m & ~15) | (((m >> 1) & 3) << 2) | (((m >> 3) & 1) << 1) | (m & 1);
+}
+
 template <int HC, int GP, bool F8>
-__global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 1)
+__global__ void __launch_bounds__((TcCfg<HC, GP, F8>::kThreads), 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                  const DecodeParams p, int G) {
     constexpr int D = 128;
-    constexpr int kThreads = F8 ? kTcThreadsF8 : kTcThreads;
     using C = TcCfg<HC, GP, F8>;
-    constexpr int N = C::kN, NK = C::kNK, NV = C::kNV, NBP = C::kNBP;
+    constexpr int kThreads = C::kThreads;
+    constexpr int N = C::kN, NK = C::kNK, NV = C::kNV, NBP = C::kNBP, NBS = C::kNBS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
@@ -248,9 +288,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     int *ticket = reinterpret_cast<int *>(alpha_s + 2 * N + 2);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
     uint64_t *kfull = bars, *kempty = bars + NK, *vfull = bars + 2 * NK, *vempty = vfull + NV;
-    uint64_t *sdone = vempty + NV, *sfree = sdone + kTcNBS, *pready = sfree + kTcNBS;
+    uint64_t *sdone = vempty + NV, *sfree = sdone + NBS, *pready = sfree + NBS;
     uint64_t *pfree = pready + NBP;
-    uint64_t *kconv = pfree + NBP, *vconv = kconv + NK;   // FP8: stage widened to fp16
+    // FP8: operand buffer (chunk c & 1) widened into TMEM, and released by its MMAs
+    uint64_t *kconv = pfree + NBP, *kopfree = kconv + 2, *vconv = kopfree + 2, *vopfree = vconv + 2;
     volatile uint64_t *mask_ring = reinterpret_cast<volatile uint64_t *>(smem + C::kMaskOff);
     volatile uint64_t *vmask_ring = reinterpret_cast<volatile uint64_t *>(smem + C::kVMaskOff);
     int *look_ring = reinterpret_cast<int *>(smem + C::kLookOff);  // [2][kTcLook + 1][32]
@@ -370,15 +411,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     }
 
     auto wait_or_abort = [&](uint64_t *bar, uint32_t parity) -> bool {
-        const uint64_t t0 = globaltimer_ns();
-        for (uint32_t i = 0; i < kWaitLimit; ++i) {
-            if (mbar_try_wait(bar, parity)) return true;
-            if (*abort_flag) return false;
-            if (wait_expired(i, t0)) break;
-        }
-        *abort_flag = 1;
-        set_status(p.status, PA_STATUS_TIMEOUT);
-        return false;
+        return mbar_try_wait(bar, parity) || mbar_wait_or_abort_slow(bar, parity, abort_flag, p.status);
     };
 
     // ---- TMA producers: K ring (warp 5), V ring (warp 6) ----------------------------------
@@ -429,8 +462,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             const uint32_t vm = __ballot_sync(0xffffffffu, valid);
             // publish which tiles of chunk c are loaded (bit 2 * tile) for the softmax
             // (and, FP8, for the V converter, which zeroes the V rows not loaded)
-            if (lane == 0 && !is_v) mask_ring[c % kTcMaskRing] = (static_cast<uint64_t>(c) << 32) | vm;
-            if (F8 && lane == 0 && is_v) vmask_ring[c % kTcMaskRing] = (static_cast<uint64_t>(c) << 32) | vm;
+            if (lane == 0 && !is_v) mask_ring[c % C::kMaskRing] = (static_cast<uint64_t>(c) << 32) | vm;
+            if (F8 && lane == 0 && is_v) vmask_ring[c % C::kMaskRing] = (static_cast<uint64_t>(c) << 32) | vm;
             const int chunk0 = t_begin + c * C::kT;
             if (writes && last_pos >= chunk0 && last_pos < chunk0 + C::kT) {  // holds position L - 1
                 const int ph = __shfl_sync(0xffffffffu, phys, 2 * ((last_pos - chunk0) / kTile));
@@ -448,18 +481,18 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             }
             if constexpr (F8) {
                 // one box per tile (16 rows x HC heads x 128 one-byte codes) into the
-                // stage's upper half, where the converter widens it in place
+                // code stage, from which the converter warps widen it into TMEM
                 if (lane == 0)
                     mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(__popc(vm & 0x55555555u)) * C::kBoxBytes);
                 __syncwarp();
                 if (valid && sub == 0)
-                    tma_load_3d(ring + s * C::kTileBytes + C::kSubTile + tile * C::kBoxBytes, map, 0,
+                    tma_load_3d(ring + s * C::kStageBytes + tile * C::kBoxBytes, map, 0,
                                 phys * bs + tok0 % bs, g0, &full[s], policy);
             } else {
                 if (lane == 0) mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(__popc(vm)) * C::kBoxBytes);
                 __syncwarp();
                 if (valid)
-                    tma_load_4d(ring + s * C::kTileBytes + sub * C::kSubTile + tile * C::kBoxBytes, map, 0,
+                    tma_load_4d(ring + s * C::kStageBytes + sub * C::kSubTile + tile * C::kBoxBytes, map, 0,
                                 phys * bs + tok0 % bs, g0, sub, &full[s], policy);
             }
             issued = c + 1;
@@ -471,9 +504,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         if (lane == 0) {
             for (int i = 0; i < nst; ++i) {
                 mbar_init(&full[i], 1u);
-                mbar_init(&empty[i], 1u);
+                // released by the MMA's commit, or (FP8) by the four converter warps
+                mbar_init(&empty[i], F8 ? 4u : 1u);
             }
-            for (int i = 0; i < kTcMaskRing; ++i) {  // no chunk's tag yet
+            for (int i = 0; i < C::kMaskRing; ++i) {  // no chunk's tag yet
                 if (!is_v) mask_ring[i] = ~uint64_t(0);
                 else if (F8) vmask_ring[i] = ~uint64_t(0);
             }
@@ -488,12 +522,17 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     if (warp == 0) tc5::tmem_alloc(tmem_slot, C::kTmemCols);
     if (tid == 0) {
         // the MMA / softmax barriers (the rings' are the producers'): every one
-        // completes on one arrival except "S free" and "P ready", which all 128
-        // softmax threads arrive on
+        // completes on one arrival except "S free" and "P ready", which each of
+        // the 4 softmax warps arrives on once
         for (uint64_t *bar = sdone; bar < pfree + NBP; ++bar)
-            mbar_init(bar, (bar >= sfree && bar < pready + NBP) ? 128u : 1u);
-        if (F8)  // "converted": the 64 threads of a converter pair arrive
-            for (uint64_t *bar = kconv; bar < vconv + NV; ++bar) mbar_init(bar, 64u);
+            mbar_init(bar, (bar >= sfree && bar < pready + NBP) ? 4u : 1u);
+        if (F8)  // operand buffers: "widened" by the four converter warps, "released" by a commit
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(&kconv[i], 4u);
+                mbar_init(&vconv[i], 4u);
+                mbar_init(&kopfree[i], 1u);
+                mbar_init(&vopfree[i], 1u);
+            }
         *abort_flag = 0;
     }
     if (tid < N) m_ref[tid] = -INFINITY;
@@ -536,77 +575,118 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             constexpr uint32_t kIdQK = tc5::idesc_bf16_f32(kTcRows, N, false, false, F8);
             int done = 0;
             for (int c = 0; c < nch; ++c) {
-                // S buffer c % NBS is free once softmax c - NBS has read it; K c has landed
-                if (c >= kTcNBS && !wait_or_abort(&sfree[c % kTcNBS], ((c / kTcNBS) - 1) & 1)) break;
-                if (!wait_or_abort(F8 ? &kconv[c % NK] : &kfull[c % NK], (c / NK) & 1)) break;
+                // S buffer c % NBS is free once softmax c - NBS has read it; K c has
+                // landed (FP8: has been widened into TMEM operand buffer c & 1)
+                if (c >= NBS && !wait_or_abort(&sfree[c % NBS], ((c / NBS) - 1) & 1)) break;
+                if (!wait_or_abort(F8 ? &kconv[c & 1] : &kfull[c % NK], F8 ? (c >> 1) & 1 : (c / NK) & 1)) break;
                 tc5::fence_after_sync();
-                const uint8_t *kt = kring + (c % NK) * C::kTileBytes;
-                const uint32_t dcol = tmem + (c % kTcNBS) * N;
+                const uint8_t *kt = kring + (c % NK) * C::kStageBytes;
+                const uint32_t dcol = tmem + (c % NBS) * N;
 #pragma unroll
-                for (int j = 0; j < D / 16; ++j) {
+                for (int j = 0; j < D / 16; ++j) {  // K = 16 dims d per MMA
                     const int half = j >> 2, off = (j & 3) * 32;
-                    tc5::mma_bf16(dcol, tc5::sw128_desc(kt + half * C::kSubTile + off, 16, 1024),
-                                  tc5::sw128_desc(qs + half * (N * kSubBytes) + off, 16, 1024),
-                                  kIdQK, j > 0);
+                    const uint64_t qdesc = tc5::sw128_desc(qs + half * (N * kSubBytes) + off, 16, 1024);
+                    if constexpr (F8)  // A: lane m, column d / 2 of the widened chunk
+                        tc5::mma_f16_tmem_a(dcol, tmem + C::kColK + 64 * (c & 1) + 8 * j, qdesc, kIdQK, j > 0);
+                    else
+                        tc5::mma_bf16(dcol, tc5::sw128_desc(kt + half * C::kSubTile + off, 16, 1024), qdesc,
+                                      kIdQK, j > 0);
                 }
-                tc5::commit(&sdone[c % kTcNBS]);
-                tc5::commit(&kempty[c % NK]);
+                tc5::commit(&sdone[c % NBS]);
+                tc5::commit(F8 ? &kopfree[c & 1] : &kempty[c % NK]);
                 done = c + 1;
             }
             if (*abort_flag && done > 0)  // let issued MMAs finish before TMEM is freed
-                mbar_wait_bounded(&sdone[(done - 1) % kTcNBS], ((done - 1) / kTcNBS) & 1);
+                mbar_wait_bounded(&sdone[(done - 1) % NBS], ((done - 1) / NBS) & 1);
         }
     } else if (warp == kTcPvWarp) {
         // ================= PV issuer =================
         if (lane == 0) {
-            constexpr uint32_t kIdPV = tc5::idesc_bf16_f32(kTcRows, 2 * N, true, C::kPMn, F8);
+            // (V^T read transposed from shared memory, or FP8: from TMEM, K-major)
+            constexpr uint32_t kIdPV = tc5::idesc_bf16_f32(kTcRows, 2 * N, !F8, C::kPMn, F8);
             int done = 0;
             for (int c = 0; c < nch; ++c) {
                 if (!wait_or_abort(&pready[c % NBP], (c / NBP) & 1)) break;
-                if (!wait_or_abort(F8 ? &vconv[c % NV] : &vfull[c % NV], (c / NV) & 1)) break;
+                if (!wait_or_abort(F8 ? &vconv[c & 1] : &vfull[c % NV], F8 ? (c >> 1) & 1 : (c / NV) & 1)) break;
                 tc5::fence_after_sync();
-                const uint8_t *vt = vring + (c % NV) * C::kTileBytes;
+                const uint8_t *vt = vring + (c % NV) * C::kStageBytes;
                 const uint8_t *pt = ps + (c % NBP) * C::kPBufBytes;
 #pragma unroll
-                for (int j = 0; j < kTcRows / 16; ++j) {  // K = 16 rows m per MMA
+                for (int j = 0; j < kTcRows / 16; ++j) {  // K = 16 rows of P^T per MMA
                     const uint64_t bdesc =
                         C::kPMn ? tc5::sw128_desc(pt + j * 16 * kSubBytes, C::kSubTile, 1024)
                                 : tc5::sw128_desc(pt + (j >> 2) * (2 * N * kSubBytes) + (j & 3) * 32, 16, 1024);
-                    tc5::mma_bf16(tmem + C::kColO,
-                                  tc5::sw128_desc(vt + j * 16 * kSubBytes, C::kSubTile, 1024), bdesc,
-                                  kIdPV, c > 0 || j > 0);
+                    if constexpr (F8)  // A: V^T widened into TMEM, 16 rows of P^T = 8 columns
+                        tc5::mma_f16_tmem_a(tmem + C::kColO, tmem + C::kColV + 64 * (c & 1) + 8 * j, bdesc,
+                                            kIdPV, c > 0 || j > 0);
+                    else
+                        tc5::mma_bf16(tmem + C::kColO, tc5::sw128_desc(vt + j * 16 * kSubBytes, C::kSubTile, 1024),
+                                      bdesc, kIdPV, c > 0 || j > 0);
                 }
                 tc5::commit(&pfree[c % NBP]);
-                tc5::commit(&vempty[c % NV]);
+                tc5::commit(F8 ? &vopfree[c & 1] : &vempty[c % NV]);
                 done = c + 1;
             }
             if (*abort_flag && done > 0)
                 mbar_wait_bounded(&pfree[(done - 1) % NBP], ((done - 1) / NBP) & 1);
         }
-    } else if (F8 && warp >= kTcCvtKWarp) {
-        // ================= FP8 converters: widen each landed e4m3 stage to fp16 =================
-        // Warps 8-9 take the K ring, 10-11 the V ring; thread ct owns rows ct and
-        // ct + 64 of a chunk.  A row's 128 codes (in the stage's upper half, as TMA
-        // wrote them, 128-byte swizzled) are read whole before its two fp16
-        // half-rows are written (the second one over the codes), so no row
-        // touches another's bytes.  V rows the producer did not load, or past the
-        // range, are written as zeros, so 0 * (stale bytes) never reaches O^T.
-        const bool cv = warp >= kTcCvtVWarp;
-        const int ct = tid - 32 * (cv ? kTcCvtVWarp : kTcCvtKWarp);
-        const int nst_c = cv ? NV : NK;
-        uint8_t *ring_c = cv ? vring : kring;
-        uint64_t *full_c = cv ? vfull : kfull;
-        uint64_t *conv_c = cv ? vconv : kconv;
+    } else if (F8 && warp >= kTcCvtWarp) {
+        // ================= FP8 converters: widen each chunk's e4m3 codes into TMEM =================
+        // Warp 8 + q4 writes TMEM lanes 32 q4 .. 32 q4 + 31 of both operand
+        // buffers (c & 1) of chunk c:
+        //   K (QK's A): lane m = row m of the chunk, column d / 2 = fp16 pair
+        //     (d, d + 1): thread = row, its 128 codes read whole.
+        //   V^T (PV's A): lane L holds head dim vt_dim(L) of the V rows, column
+        //     = pair of rows, in the order that transposed 8 x 8 loads of byte
+        //     pairs and 16-lane stores give (vt_row_k maps row m to its index
+        //     along the contraction; the P^T rows follow the same order).
+        //   Rows the V producer did not load, or past the range, widen to zeros,
+        //   so 0 * (stale bytes) never reaches O^T.
+        // An operand buffer is rewritten once the MMAs of chunk c - 2 have read
+        // it; the code stage is released once its codes are widened.  The
+        // passes are loops, not unrolled: the warp roles of a CTA run different
+        // code at once, and compact loops stay in the instruction cache.
+        const int q4 = warp & 3;
+        const bool do_k = C::kCvtWarps == 4 || warp < kTcCvtWarp + 4;
+        const bool do_v = C::kCvtWarps == 4 || warp >= kTcCvtWarp + 4;
+        const int m = 32 * q4 + lane;  // this thread's K row
         for (int c = 0; c < nch; ++c) {
-            const int s = c % nst_c;
-            if (!wait_or_abort(&full_c[s], (c / nst_c) & 1)) break;
-            uint32_t vm = 0xffffffffu;
-            if (cv) {  // the V producer wrote chunk c's mask before its loads
-                uint64_t mk = 0;
+            const int ob = c & 1;
+            // ---- K: 32 columns (64 codes of row m) per pass ----
+            if (do_k) {
+                if (!wait_or_abort(&kfull[c % NK], (c / NK) & 1)) break;
+                if (c >= 2 && !wait_or_abort(&kopfree[ob], ((c >> 1) - 1) & 1)) break;
+                tc5::fence_after_sync();
+                const uint8_t *krow = kring + (c % NK) * C::kStageBytes + m * kSubBytes;
+                const uint32_t kcol = tc5::taddr(tmem, 32 * q4, C::kColK + 64 * ob);
+#pragma unroll 1
+                for (int hf = 0; hf < 2; ++hf) {
+                    uint32_t w[32];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {  // codes 16 (4 hf + j) .. + 15 -> columns 8 (4 hf + j) ..
+                        uint4 a, b;
+                        e4m3x16_to_f16(*reinterpret_cast<const uint4 *>(krow + (((4 * hf + j) ^ (m & 7)) << 4)), a, b);
+                        w[8 * j + 0] = a.x, w[8 * j + 1] = a.y, w[8 * j + 2] = a.z, w[8 * j + 3] = a.w;
+                        w[8 * j + 4] = b.x, w[8 * j + 5] = b.y, w[8 * j + 6] = b.z, w[8 * j + 7] = b.w;
+                    }
+                    tc5::st_32x32b_x32_nowait(kcol + 32 * hf, w);
+                }
+                __syncwarp();  // the stage's codes are read (the stores took them)
+                if (lane == 0) mbar_arrive(&kempty[c % NK]);
+                tc5::wait_st();
+                tc5::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&kconv[ob]);
+            }
+
+            // ---- V^T: 16 dims x 128 rows (four transposed 4-matrix loads) per pass ----
+            if (!do_v) continue;
+            uint64_t mk = 0;
+            {  // the V producer wrote chunk c's mask before its loads
                 uint32_t i = 0;
                 const uint64_t t0 = globaltimer_ns();
                 for (; i < kWaitLimit; ++i) {
-                    mk = vmask_ring[c % kTcMaskRing];
+                    mk = vmask_ring[c % C::kMaskRing];
                     if (static_cast<uint32_t>(mk >> 32) == static_cast<uint32_t>(c) || *abort_flag) break;
                     if (wait_expired(i, t0)) {
                         i = kWaitLimit;
@@ -620,37 +700,56 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                     }
                     break;
                 }
-                vm = static_cast<uint32_t>(mk);
             }
-            uint8_t *st = ring_c + s * C::kTileBytes;
-            // both rows' codes are loaded first (the rows are disjoint), then widened
-            uint4 raw[2][8];
-            bool keep[2];
+            if (!wait_or_abort(&vfull[c % NV], (c / NV) & 1)) break;
+            if (c >= 2 && !wait_or_abort(&vopfree[ob], ((c >> 1) - 1) & 1)) break;
+            tc5::fence_after_sync();
+            const uint32_t vm = static_cast<uint32_t>(mk);
+            const int tok_c = t_begin + c * C::kT;
+            constexpr uint32_t kAllTiles = 0x55555555u & ((1u << (2 * C::kTiles)) - 1u);
+            const bool whole = (vm & kAllTiles) == kAllTiles && tok_c + C::kT <= t_end;
+            // pass u: dims 16 dc .. 16 dc + 15 (dc = 2 q4 + u); load k takes row groups
+            // g = 2 k, 2 k + 1, lane t giving the address of row t % 8 of matrix
+            // t / 8 = 2 (g - 2 k) + h (rows 16 g + 8 h .. + 7)
+            const int mi = lane >> 3, r8 = lane & 7;
+            const uint32_t vsrc = smem_u32(vring + (c % NV) * C::kStageBytes) +
+                                  (16 * (mi >> 1) + 8 * (mi & 1) + r8) * kSubBytes;
+            const uint32_t vcol = tc5::taddr(tmem, 32 * q4, C::kColV + 64 * ob);
+#pragma unroll 1
+            for (int u = 0; u < 2; ++u) {
+                uint32_t w[32];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int m = ct + 64 * h;
-                const int tl = m / (kTile * HC);
-                keep[h] = !cv || (((vm >> (2 * tl)) & 1u) && t_begin + c * C::kT + tl * kTile + (m & 15) < t_end);
+                for (int k = 0; k < 4; ++k) {
+                    uint32_t r[4];
+                    ldsm_x4_trans(vsrc + 32 * k * kSubBytes + (((2 * q4 + u) ^ r8) << 4), r);
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    raw[h][j] = *reinterpret_cast<const uint4 *>(st + C::kSubTile + m * kSubBytes +
-                                                                 ((j ^ (m & 7)) << 4));
-            }
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int m = ct + 64 * h;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {  // codes 16j..16j+15 = half (j / 4), chunks 2(j%4), +1
-                    uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
-                    if (keep[h]) e4m3x16_to_f16(raw[h][j], lo, hi);
-                    const int cj = (j & 3) * 2;
-                    uint8_t *row = st + (j >> 2) * C::kSubTile + m * kSubBytes;
-                    *reinterpret_cast<uint4 *>(row + ((cj ^ (m & 7)) << 4)) = lo;
-                    *reinterpret_cast<uint4 *>(row + (((cj + 1) ^ (m & 7)) << 4)) = hi;
+                    for (int gg = 0; gg < 2; ++gg) {
+                        // lane t holds rows 16 g + 8 h + 2 (t % 4) and + 1 of dims 16 dc + 2 (t / 4) and + 1
+                        const uint2 a = e4m3x4_to_f16x4(__byte_perm(r[2 * gg], 0u, 0x3120));      // h = 0
+                        const uint2 b = e4m3x4_to_f16x4(__byte_perm(r[2 * gg + 1], 0u, 0x3120));  // h = 1
+                        uint32_t ka = 0xffffffffu, kb = 0xffffffffu;
+                        if (!whole) {
+                            const int tl = (2 * k + gg) / HC;
+                            const bool tile_ok = (vm >> (2 * tl)) & 1u;
+                            const int r0 = tok_c + tl * kTile + 2 * (lane & 3);
+                            ka = (tile_ok && r0 < t_end ? 0x0000ffffu : 0u) | (tile_ok && r0 + 1 < t_end ? 0xffff0000u : 0u);
+                            kb = (tile_ok && r0 + 8 < t_end ? 0x0000ffffu : 0u) | (tile_ok && r0 + 9 < t_end ? 0xffff0000u : 0u);
+                        }
+                        // repetition g = 2 k + gg of the store: columns 8 g + 2 (t % 4) (+ 1)
+                        w[8 * k + 4 * gg + 0] = a.x & ka;  // dim 2 (t / 4): lane t / 4, rows of h = 0
+                        w[8 * k + 4 * gg + 1] = b.x & kb;  //               rows of h = 1
+                        w[8 * k + 4 * gg + 2] = a.y & ka;  // dim 2 (t / 4) + 1: lane t / 4 + 8
+                        w[8 * k + 4 * gg + 3] = b.y & kb;
+                    }
                 }
+                tc5::st_16x256b_x8_nowait(vcol + ((16 * u) << 16), w);
             }
-            fence_proxy_async_smem();  // the MMA (async proxy) reads what these threads wrote
-            mbar_arrive(&conv_c[s]);
+            __syncwarp();  // the stage's codes are read
+            if (lane == 0) mbar_arrive(&vempty[c % NV]);
+            tc5::wait_st();
+            tc5::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&vconv[ob]);
         }
     } else {
         // ================= softmax warps: thread = row m of a chunk, and output dim d =================
@@ -663,15 +762,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         const int my_tile = tid / (kTile * HC);              // tile of row m = tid
         const int my_tok = my_tile * kTile + (tid & 15);     // its token's offset in a chunk
         for (int c = 0; c < nch; ++c) {
-            const int sbuf = c % kTcNBS, pbuf = c % NBP;
-            bool ok = wait_or_abort(&sdone[sbuf], (c / kTcNBS) & 1);
+            const int sbuf = c % NBS, pbuf = c % NBP;
+            bool ok = wait_or_abort(&sdone[sbuf], (c / NBS) & 1);
             // the K producer wrote chunk c's mask before its loads, hence before S c
             uint64_t mk = 0;
             if (ok) {
                 uint32_t i = 0;
                 const uint64_t t0 = globaltimer_ns();
                 for (; i < kWaitLimit; ++i) {
-                    mk = mask_ring[c % kTcMaskRing];
+                    mk = mask_ring[c % C::kMaskRing];
                     if (static_cast<uint32_t>(mk >> 32) == static_cast<uint32_t>(c) || *abort_flag) break;
                     if (wait_expired(i, t0)) {
                         i = kWaitLimit;
@@ -698,7 +797,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                                        *reinterpret_cast<float(*)[16]>(&sv[16 * k]));
             }
             tc5::fence_before_sync();
-            mbar_arrive(&sfree[sbuf]);  // S buffer read: QK c + NBS may overwrite it
+            __syncwarp();  // (one arrival per warp, once all its lanes have read)
+            if (lane == 0) mbar_arrive(&sfree[sbuf]);  // S buffer read: QK c + NBS may overwrite it
             const bool valid = ok && in_pool;
             // causal: column q (query qi0 + q / G) sees this row's token only if
             // the token is not past the query's position
@@ -775,12 +875,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                 l_thr[q + 1] += h1 + p16_value<F8>(static_cast<uint16_t>(lo >> 16));
             }
             if (c >= NBP) wait_or_abort(&pfree[pbuf], ((c / NBP) - 1) & 1);  // PV c - NBP done
+            // row k of P^T along the PV contraction: row m = tid (FP8: in the
+            // order of the widened V^T's columns)
+            const int prow = F8 ? vt_row_k(tid) : tid;
             if constexpr (C::kPMn) {
-                // row m = tid of P^T, this row's own head's columns (hi, then lo at
+                // row k of P^T, this row's own head's columns (hi, then lo at
                 // N + n); the other heads' columns stay zero
-                uint8_t *row = ps + pbuf * C::kPBufBytes + tid * kSubBytes;
+                uint8_t *row = ps + pbuf * C::kPBufBytes + prow * kSubBytes;
                 auto at = [&](int n) -> uint32_t {  // byte offset of column n of the row
-                    return (n >> 6) * C::kSubTile + ((((n & 63) >> 3) ^ (tid & 7)) << 4) + (n & 7) * 2;
+                    return (n >> 6) * C::kSubTile + ((((n & 63) >> 3) ^ (prow & 7)) << 4) + (n & 7) * 2;
                 };
                 const int n0 = my_head * GP;
                 if constexpr (GP >= 8) {
@@ -796,9 +899,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                     *reinterpret_cast<uint2 *>(row + at(N + n0)) = make_uint2(lw[0], lw[1]);
                 }
             } else {
-                // P^T[n][m] for this row's own head block; the other heads' columns stay zero
-                uint8_t *pt = ps + pbuf * C::kPBufBytes + (tid >> 6) * (2 * N * kSubBytes);
-                const int tt = tid & 63;
+                // P^T[n][k] for this row's own head block; the other heads' columns stay zero
+                uint8_t *pt = ps + pbuf * C::kPBufBytes + (prow >> 6) * (2 * N * kSubBytes);
+                const int tt = prow & 63;
 #pragma unroll
                 for (int q = 0; q < GP; ++q) {
                     const int n = my_head * GP + q;   // lo row N + n swizzles as n (N % 8 == 0)
@@ -811,7 +914,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             // an invalid row zeroes its V row, so 0 * (stale or NaN) never reaches O^T
             // (with FP8 pools the V converter writes those rows as zeros)
             if (!F8 && !valid && wait_or_abort(&vfull[c % NV], (c / NV) & 1)) {
-                uint8_t *vrow = vring + (c % NV) * C::kTileBytes + tid * kSubBytes;
+                uint8_t *vrow = vring + (c % NV) * C::kStageBytes + tid * kSubBytes;
 #pragma unroll
                 for (int sub = 0; sub < 2; ++sub)
 #pragma unroll
@@ -821,7 +924,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             }
             fence_proxy_async_smem();
             tc5::fence_before_sync();
-            mbar_arrive(&pready[pbuf]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&pready[pbuf]);
         }
 
         // ---- epilogue: row sums, O^T, normalise, store ----------------------------------
@@ -847,9 +951,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             // else bf16), column n = (head hh, query q) being output row
             // row0 + rel_s[n].  The cluster merge reads the stage in place;
             // otherwise each column's row is copied out by one bulk copy.
+            // (FP8: lane tid of O^T is head dim vt_dim(tid))
             const bool split = p.split != 0;
-            float *ostage = reinterpret_cast<float *>(ps) + tid;
-            __nv_bfloat16 *ostage16 = reinterpret_cast<__nv_bfloat16 *>(ps) + tid;
+            float *ostage0 = reinterpret_cast<float *>(ps);
+            __nv_bfloat16 *ostage16_0 = reinterpret_cast<__nv_bfloat16 *>(ps);
+            float *ostage = ostage0 + (F8 ? vt_dim(tid) : tid);
+            __nv_bfloat16 *ostage16 = ostage16_0 + (F8 ? vt_dim(tid) : tid);
 #pragma unroll 1
             for (int k = 0; k < N / 16; ++k) {
                 float ov[16], lo[16], al[16];
@@ -882,13 +989,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                     col[n] = lse;
                 } else if (split) {
                     const int64_t slot = r * p.part_stride + p.part_offset + part;
-                    bulk_store_s2g(p.part_o + slot * D, ostage - tid + n * D, D * 4);
+                    bulk_store_s2g(p.part_o + slot * D, ostage0 + n * D, D * 4);
                     bulk_commit();
                     p.part_lse[slot] = lse;
                     bulk_wait_all();              // the row is written ...
                     fence_proxy_async_global();   // ... and ordered before the merge's release
                 } else {
-                    bulk_store_s2g(static_cast<__nv_bfloat16 *>(p.out) + r * D, ostage16 - tid + n * D, D * 2);
+                    bulk_store_s2g(static_cast<__nv_bfloat16 *>(p.out) + r * D, ostage16_0 + n * D, D * 2);
                     bulk_commit();
                     if (p.lse) p.lse[r] = lse;
                     bulk_wait_all_read();  // the stage is read before the CTA moves on
@@ -925,7 +1032,7 @@ cudaError_t launch_tc_instance(const CUtensorMap &kmap, const CUtensorMap &vmap,
     }
     const int qgroups = (p.q_len + p.q_per_cta - 1) / p.q_per_cta;
     const dim3 grid(p.num_splits, p.head_groups * qgroups, B);
-    const int threads = F8 ? kTcThreadsF8 : kTcThreads;
+    const int threads = C::kThreads;
     if (p.cluster_merge) {
         // One cluster per (sequence, head group, query group), all resident at
         // once (a second wave of clusters would cost more than the merge saves).

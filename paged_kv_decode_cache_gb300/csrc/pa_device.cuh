@@ -109,6 +109,14 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     return false;
 }
 
+// The polling part of a bounded wait that honours a CTA-wide abort flag:
+// false once the flag is set (by another warp) or the wait has run out, in
+// which case it sets the flag and PA_STATUS_TIMEOUT.  Kept out of line, so
+// that the many wait sites of a warp-specialised kernel share one copy of
+// the loop (callers try the barrier once inline first).
+static __device__ __noinline__ bool mbar_wait_or_abort_slow(uint64_t *bar, uint32_t parity,
+                                                           volatile int *abort_flag, int32_t *status);
+
 // L2 policy for data read exactly once (the KV stream).
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
     uint64_t pol;
@@ -184,6 +192,17 @@ __device__ __forceinline__ uint32_t swz128(int row, int chunk) {
     return static_cast<uint32_t>(row * kSubBytes + ((chunk ^ (row & 7)) << 4));
 }
 
+// Four 8 x 8 matrices of 16-bit elements, transposed: lanes 8i .. 8i + 7 give
+// the shared-memory addresses of rows 0..7 of matrix i (16 bytes each), and
+// lane t receives in r[i] the elements (row 2 (t % 4), column t / 4) (low
+// half) and (row 2 (t % 4) + 1, column t / 4) (high half) of matrix i.
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t saddr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(saddr)
+                 : "memory");
+}
+
 // Plain arrive (count 1) on an mbarrier.
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(
@@ -251,6 +270,19 @@ __device__ __forceinline__ bool slot_is_position(int64_t slot, int phys, int pos
 
 __device__ __forceinline__ void set_status(int32_t *status, int bits) {
     if (status) atomicOr(status, bits);
+}
+
+static __device__ __noinline__ bool mbar_wait_or_abort_slow(uint64_t *bar, uint32_t parity,
+                                                           volatile int *abort_flag, int32_t *status) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 0; i < kWaitLimit; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (wait_expired(i, t0)) break;
+    }
+    *abort_flag = 1;
+    set_status(status, PA_STATUS_TIMEOUT);
+    return false;
 }
 
 // Programmatic dependent launch.  griddep_wait(): returns once the grids this

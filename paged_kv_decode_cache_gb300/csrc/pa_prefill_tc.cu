@@ -176,10 +176,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         }
         for (int i = 0; i < kPfNS; ++i) {
             mbar_init(&sdone[i], 1u);
-            mbar_init(&sfree[i], 128u);  // the 128 threads of softmax group i release S buffer i
+            mbar_init(&sfree[i], 4u);  // the 4 warps of softmax group i release S buffer i
         }
         for (int i = 0; i < kPfNP; ++i) {
-            mbar_init(&pready[i], 128u);  // ... and publish P buffer i
+            mbar_init(&pready[i], 4u);  // ... and publish P buffer i
             mbar_init(&pfree[i], 1u);
         }
         *abort_flag = 0;
@@ -194,15 +194,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     const uint32_t tmem = *tmem_slot;
 
     auto wait_or_abort = [&](uint64_t *bar, uint32_t parity) -> bool {
-        const uint64_t t0 = globaltimer_ns();
-        for (uint32_t i = 0; i < kWaitLimit; ++i) {
-            if (mbar_try_wait(bar, parity)) return true;
-            if (*abort_flag) return false;
-            if (wait_expired(i, t0)) break;
-        }
-        *abort_flag = 1;
-        set_status(p.status, PA_STATUS_TIMEOUT);
-        return false;
+        return mbar_try_wait(bar, parity) || mbar_wait_or_abort_slow(bar, parity, abort_flag, p.status);
     };
 
     if (warp == kPfTmaKWarp || warp == kPfTmaVWarp) {
@@ -313,7 +305,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 for (int k = 0; k < kPfT; ++k) sv[k] = __uint_as_float(raw[k]);
             }
             tc5::fence_before_sync();
-            mbar_arrive(&sfree[grp]);  // S buffer read: QK c + 2 may overwrite it
+            __syncwarp();  // (one arrival per warp, once all its lanes have read)
+            if (lane == 0) mbar_arrive(&sfree[grp]);  // S buffer read: QK c + 2 may overwrite it
             if (!ok || *abort_flag) break;
             const int tok0 = t_begin + c * kPfT;
             bool tile_ok[kPfTilesPerChunk];
@@ -417,7 +410,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             }
             fence_proxy_async_smem();  // P (and zeroed V rows) are read by the MMA
             tc5::fence_before_sync();
-            mbar_arrive(&pready[grp]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&pready[grp]);
         }
 
         // ---- epilogue: the two groups' rows merged, normalised, staged in the idle P

@@ -1,6 +1,7 @@
 // Thin wrappers over the sm_100-family tensor-core instructions used by the
-// tensor-core decode kernel: TMEM allocation, tcgen05.mma (kind::f16, one CTA),
-// commit to an mbarrier, TMEM loads/stores in the 32x32b shape, the tcgen05
+// tensor-core kernels: TMEM allocation, tcgen05.mma (kind::f16, one CTA; A
+// from shared memory or TMEM), commit to an mbarrier, TMEM loads/stores in the
+// 32x32b and 16x256b shapes, the tcgen05
 // fences, and the shared-memory matrix descriptor for 128-byte-swizzled
 // operands.
 #pragma once
@@ -75,6 +76,20 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]; issued by one thread.  A sits in TMEM with
+// its M rows on the lanes and its K elements along the columns, two 16-bit
+// values per 32-bit column (element 2c in the low half of column c); a_tmem
+// addresses the first column of this MMA's K slice (K = 16: 8 columns).
+__device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                               uint32_t idesc, bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(static_cast<uint32_t>(accumulate))
+        : "memory");
+}
+
 // Arrive once on `bar` when every MMA this thread issued so far has completed.
 __device__ __forceinline__ void commit(uint64_t *bar) {
     asm volatile(
@@ -125,6 +140,50 @@ __device__ __forceinline__ void st_32x32b_x16(uint32_t taddr, const float (&v)[1
         "r"(__float_as_uint(v[15]))
         : "memory");
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// 16 columns of 32 bits from registers into TMEM without the wait; call
+// wait_st() before the stores must be visible (then fence_before_sync()).
+__device__ __forceinline__ void st_32x32b_x16_nowait(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, "
+        "%10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+__device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// 32 lanes x 32 columns of 32 bits from registers into TMEM without the wait
+// (thread t: lane t, v[i] at column i).
+__device__ __forceinline__ void st_32x32b_x32_nowait(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+        "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+        "%30, %31, %32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
+        "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),
+        "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+}
+
+// 16 lanes x 256 bits (8 columns of 32 bits), eight times (columns 8 r ..
+// 8 r + 7 for v[4 r .. 4 r + 3]), without the wait.  Thread t writes, per
+// repetition r, v[4r] at (lane t / 4, column 8 r + 2 (t % 4)), v[4r + 1] at
+// (lane t / 4, column 8 r + 2 (t % 4) + 1), v[4r + 2] and v[4r + 3] at the
+// same columns of lane t / 4 + 8 (lanes and columns relative to taddr, whose
+// lane is the first of the 16).
+__device__ __forceinline__ void st_16x256b_x8_nowait(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.16x256b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+        "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+        "%30, %31, %32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
+        "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),
+        "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
 }
 
 // TMEM address of (lane, column).

@@ -600,6 +600,8 @@ FP8_SMALL = [
     (32, 2, 16, (129, 300)),                        # G = 16
     (16, 4, 256, (300, 513, 2)),                    # pages
     (2, 2, 16, (0, 5)),                             # empty sequence
+    (64, 4, 16, (100, 257, 31)),                    # G = 16, 4 heads per CTA (MMA N = 64)
+    (32, 1, 16, (140, 64)),                         # G = 32, one head per CTA (MMA N = 64)
 ]
 
 
