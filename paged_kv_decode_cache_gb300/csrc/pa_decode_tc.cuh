@@ -100,9 +100,9 @@ template <int HC, int GP, bool F8 = false>
 struct TcCfg {
     static constexpr int kN = HC * GP;                          // MMA N
     // FP8 converter warps: 8 (warps 8-11 widen K, 12-15 V) where the softmax
-    // fits the 128 registers a thread of 512 gets (MMA N <= 32, GP <= 8), else
-    // 4 (each widens K, then V, of its TMEM lane quarter)
-    static constexpr int kCvtWarps = !F8 ? 0 : (kN <= 32 && GP <= 8) ? 8 : 4;
+    // fits the 128 registers a thread of 512 gets (GP <= 8), else 4 (each
+    // widens K, then V, of its TMEM lane quarter)
+    static constexpr int kCvtWarps = !F8 ? 0 : GP <= 8 ? 8 : 4;
     static constexpr int kThreads = kTcThreads + 32 * kCvtWarps;
     static_assert(kN % 16 == 0 && kN >= 16 && kN <= 64, "MMA N");
     static constexpr int kT = kTcRows / HC;                     // tokens per chunk
@@ -761,6 +761,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         bool dead = false;
         const int my_tile = tid / (kTile * HC);              // tile of row m = tid
         const int my_tok = my_tile * kTile + (tid & 15);     // its token's offset in a chunk
+        // The 16-row groups of warp w's rows are heads (2 w) % HC (lanes 0-15)
+        // and that + 1 (lanes 16-31): the warp loads those two heads' GP
+        // columns of S, each lane keeps its own.
+        const int head_a = HC == 1 ? 0 : (2 * warp) % HC;
+        // this row's head's reference maxima (m_ref only moves after a vote)
+        float mr[GP];
+#pragma unroll
+        for (int q = 0; q < GP; ++q) mr[q] = -INFINITY;
         for (int c = 0; c < nch; ++c) {
             const int sbuf = c % NBS, pbuf = c % NBP;
             bool ok = wait_or_abort(&sdone[sbuf], (c / NBS) & 1);
@@ -788,13 +796,29 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             ok = __all_sync(0xffffffffu, ok);
             const bool in_pool =
                 t_begin + c * C::kT + my_tok < t_end && ((static_cast<uint32_t>(mk) >> (2 * my_tile)) & 1u);
-            float sv[N];
+            float sv[GP];  // this row's head's GP scores
             if (ok) {
                 tc5::fence_after_sync();
+                const uint32_t scol = tc5::taddr(tmem, 32 * warp, sbuf * N + head_a * GP);
+                if constexpr (GP >= 16) {
+                    static_assert(HC == 1 || GP == 16, "S columns");
+                    uint32_t ra[GP], rb[HC == 1 ? 1 : GP];
 #pragma unroll
-                for (int k = 0; k < N / 16; ++k)
-                    tc5::ld_32x32b_x16(tc5::taddr(tmem, 32 * warp, sbuf * N + 16 * k),
-                                       *reinterpret_cast<float(*)[16]>(&sv[16 * k]));
+                    for (int k = 0; k < GP / 16; ++k)
+                        tc5::ld_32x32b_x16_nowait(scol + 16 * k, *reinterpret_cast<uint32_t(*)[16]>(&ra[16 * k]));
+                    if constexpr (HC > 1) tc5::ld_32x32b_x16_nowait(scol + GP, *reinterpret_cast<uint32_t(*)[16]>(&rb[0]));
+                    tc5::wait_ld();
+#pragma unroll
+                    for (int q = 0; q < GP; ++q)
+                        sv[q] = __uint_as_float(HC == 1 || lane < 16 ? ra[q] : rb[HC == 1 ? 0 : q]);
+                } else {
+                    uint32_t ra[GP], rb[GP];
+                    tc5::ld_32x32b_nowait<GP>(scol, ra);
+                    tc5::ld_32x32b_nowait<GP>(scol + GP, rb);
+                    tc5::wait_ld();
+#pragma unroll
+                    for (int q = 0; q < GP; ++q) sv[q] = __uint_as_float(lane < 16 ? ra[q] : rb[q]);
+                }
             }
             tc5::fence_before_sync();
             __syncwarp();  // (one arrival per warp, once all its lanes have read)
@@ -803,16 +827,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             // causal: column q (query qi0 + q / G) sees this row's token only if
             // the token is not past the query's position
             const int cmin = max(0, t_begin + c * C::kT + my_tok - qbase) * G;
-            float sc[GP], mr[GP];
+            float sc[GP];
             bool over = false;
 #pragma unroll
             for (int q = 0; q < GP; ++q) {
-                float v = sv[q];
-#pragma unroll
-                for (int hh = 1; hh < HC; ++hh)
-                    if (my_head == hh) v = sv[hh * GP + q];
-                sc[q] = (valid && q < Gq && q >= cmin) ? v * sl2 : -INFINITY;
-                mr[q] = m_ref[my_head * GP + q];
+                sc[q] = (valid && q < Gq && q >= cmin) ? sv[q] * sl2 : -INFINITY;
                 over |= sc[q] > mr[q] + kTcLazyTau;
             }
             // one vote per chunk: does any reference max have to move (or is the CTA aborting)?

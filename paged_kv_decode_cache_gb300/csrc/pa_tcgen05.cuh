@@ -128,6 +128,29 @@ __device__ __forceinline__ void ld_32x32b_x16_nowait(uint32_t taddr, uint32_t (&
 }
 __device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// NC (2, 4 or 8) columns of 32 bits per lane without the wait.
+template <int NC>
+__device__ __forceinline__ void ld_32x32b_nowait(uint32_t taddr, uint32_t (&r)[NC]) {
+    static_assert(NC == 2 || NC == 4 || NC == 8, "columns");
+    if constexpr (NC == 2) {
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];"
+                     : "=r"(r[0]), "=r"(r[1])
+                     : "r"(taddr)
+                     : "memory");
+    } else if constexpr (NC == 4) {
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                     : "r"(taddr)
+                     : "memory");
+    } else {
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                       "=r"(r[6]), "=r"(r[7])
+                     : "r"(taddr)
+                     : "memory");
+    }
+}
+
 __device__ __forceinline__ void st_32x32b_x16(uint32_t taddr, const float (&v)[16]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, "
