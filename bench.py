@@ -388,6 +388,15 @@ def run_ours(args, world, rank, local):
     # the cascade proper (prefix once, suffixes, merge) where the library finds it pays,
     # else pa_decode_cascade runs plain split decode
     cascade_runs = cascade and pa.pa_cascade_pays(w.B, w.Hkv, w.D, w.cascade_blocks, w.block_size)
+    cascade_kernels = 0   # kernel launches of the cascade proper
+    if cascade_runs:
+        # the library's partition counts of the two passes: a split suffix pass merges all
+        # P1 + P2 partials itself when a merge task can hold them (else a combine follows)
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        p1 = pa.pa_choose_num_splits_mq(1, w.B, w.Hq, w.Hkv, w.D, w.cascade_blocks, w.block_size, sms)
+        p2 = pa.pa_choose_num_splits(w.B, w.Hq, w.Hkv, w.D, w.max_blocks - w.cascade_blocks,
+                                     w.block_size, sms)
+        cascade_kernels = 2 if p2 >= 2 and p1 + p2 <= 256 else 3
     ws_bytes = (pa.pa_cascade_workspace_bytes(w.B, w.Hq, w.Hkv, w.D, w.cascade_blocks, w.max_blocks,
                                               w.block_size) if cascade
                 else pa.pa_splitkv_workspace_bytes(w.B * w.q_len, w.Hq, w.D, P))
@@ -421,7 +430,8 @@ def run_ours(args, world, rank, local):
         if ev1 is not None:
             ev1.record(stream)
 
-    launches_per_step = (4 if cascade_runs else 2 if (args.unfused or mq or fp8 or cascade) else 1)
+    launches_per_step = (1 + cascade_kernels if cascade_runs else
+                         2 if (args.unfused or mq or fp8 or cascade) else 1)
     # The timed region replays CUDA graphs that hold exactly the K timed steps
     # (consecutive steps cycle over the pool replicas): one graph when K <= 1024,
     # else K // 1024 replays of a 1024-step graph and one graph of the rest.  A
@@ -605,7 +615,8 @@ def run_ours(args, world, rank, local):
         roofline = {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
                     "frac": round(ach / peak, 4), "traffic": recorded_traffic(args.workload, kernel_name),
                     "peak_kind": peak_kind,
-                    "kernel": kernel_name + (" (cascade: prefix + suffix + combine)" if cascade_runs else
+                    "kernel": kernel_name + ((" (cascade: prefix + suffix with merge)" if cascade_kernels == 2
+                                              else " (cascade: prefix + suffix + combine)") if cascade_runs else
                                              " (shared prefix: plain split decode)" if cascade else
                                              " (fp8 pools)" if fp8 else " (multi-query)" if mq else
                                              "" if args.unfused else " (fused write)")
@@ -634,7 +645,7 @@ def run_ours(args, world, rank, local):
             "config": {"workload": args.workload, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
                        "block_size": w.block_size, "seq_lens_total": int(w.seq_lens.sum()),
                        "splits": P, "q_len": w.q_len,
-                       "step": ("pa_cache_write, then pa_decode_cascade (cascade: 3 launches)"
+                       "step": (f"pa_cache_write, then pa_decode_cascade (cascade: {cascade_kernels} launches)"
                                 if cascade_runs else
                                 "pa_cache_write, then pa_decode_cascade (plain split decode: the "
                                 "cascade does not pay)" if cascade else

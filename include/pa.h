@@ -363,15 +363,17 @@ int pa_decode_mq(void *out, float *lse, const void *q, int32_t q_len, const void
  * hit shared by the batch: "mini-infer" prajwal7-2002 docs, table "Core
  * Capabilities at a Glance", row "Prompt Caching", radix-tree prefix cache;
  * psmarter write-up, feature list item 4, prefix caching).  The result is
- * pa_decode_splitkv's.  The cascade computes it in three launches: (1) the
- * prefix once, all B sequences' queries attending it together (128 query
- * rows, i.e. 128 / G sequences, per CTA of the prefill-shaped kernel when
- * B * G > 32); (2) every sequence's remaining positions,
- * [n_prefix_blocks * block_size, seq_lens[b]); (3) a log-sum-exp merge of both
- * passes' fp32 partials.  It pays when re-reading the prefix for every
- * sequence would cost more than those launches: with PA_OPT_CASCADE at
+ * pa_decode_splitkv's.  The cascade computes it in two or three launches:
+ * (1) the prefix once, all B sequences' queries attending it together (128
+ * query rows, i.e. 128 / G sequences, per CTA of the prefill-shaped kernel
+ * when B * G > 32); (2) every sequence's remaining positions,
+ * [n_prefix_blocks * block_size, seq_lens[b]), which, when that pass is split
+ * (at least two partitions per sequence) and both passes have at most 256
+ * partitions together, also merges both passes' fp32 partials; else (3) a
+ * log-sum-exp combine of them.  It pays when attending the prefix once per
+ * sequence would cost more than that: with PA_OPT_CASCADE at
  * PA_CASCADE_AUTO the call runs the cascade when (B - 1) x the prefix's K/V
- * bytes reach 256 MB, and pa_decode_splitkv otherwise (the same result).  Requires seq_lens[b] >= n_prefix_blocks *
+ * bytes reach 1 GiB, and pa_decode_splitkv otherwise (the same result).  Requires seq_lens[b] >= n_prefix_blocks *
  * block_size (a shorter sequence sets PA_STATUS_BAD_SEQLEN and its result is
  * undefined); 0 <= n_prefix_blocks < max_blocks_per_seq (0: plain
  * pa_decode_splitkv).  The library reads the prefix's block ids from table

@@ -387,8 +387,10 @@ int run_decode(bool split, void *out, float *lse, float *part_o, float *part_lse
         return PA_EUNSUPPORTED;  // cascade passes: tensor cores only
     p.chunk = pa_partition_tokens(max_blocks, c.block_size, P);
     p.counters = counters;
+    // (a cluster merges its own P partials only: not a pass that shares its
+    // rows' partial slots with another pass)
     p.cluster_merge = split && counters && k == Kernel::kTensorCore && P >= 2 &&
-                      P <= pa::kMaxClusterMerge && !merge_forced_grid();
+                      P <= pa::kMaxClusterMerge && p.part_stride == P && !merge_forced_grid();
     p.pdl = k == Kernel::kTensorCore && pdl_enabled();
     p.k_new = static_cast<const uint16_t *>(nt.k_new);
     p.v_new = static_cast<const uint16_t *>(nt.v_new);
@@ -745,19 +747,21 @@ static int cascade_splits(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t
 }
 
 // Does attending the shared prefix once for the whole batch pay?  Without the
-// cascade every sequence reads the prefix again: B - 1 extra reads of its K/V,
-// from L2 while the prefix fits there.  The cascade costs two extra launches
-// and a merge (about 10 us on the GB300).  It pays when the extra reads are
-// large enough to take longer than that even from L2: (B - 1) x prefix bytes
-// of at least 256 MB (a 2048-token prefix of 8 KV heads for 256 sequences is
-// 2.1 GB; 8 blocks of the same heads, 134 MB, is served from L2 faster than
-// the cascade's launches).
+// cascade every sequence attends the prefix again: B - 1 extra passes over its
+// K/V.  Those passes mostly hit L2 (the sequences' CTAs of one partition read
+// the same blocks at about the same time, even for a prefix larger than L2),
+// so what they cost is L2 traffic and the SMs' work on the extra rows, against
+// the cascade's extra launch and merge.  Calibrated on this GPU: the cascade
+// pays once the extra reads reach 1 GiB (256 sequences behind a 2048-token
+// prefix of 8 KV heads, 2.1 GB: 3.4x faster; plain decode is faster for 4
+// sequences behind 65536 tokens, 805 MB, for 8 behind 16384, 470 MB, and for
+// 256 behind 8 blocks, 134 MB).
 static bool cascade_pays(int32_t B, int32_t Hkv, int32_t D, int32_t n_prefix_blocks,
                          int32_t block_size) {
     const int mode = option(PA_OPT_CASCADE);
     if (mode != PA_CASCADE_AUTO) return mode == PA_CASCADE_ALWAYS;
     const double prefix_bytes = static_cast<double>(n_prefix_blocks) * block_size * Hkv * D * 2 * 2;
-    return (B - 1) * prefix_bytes >= 256.0 * (1 << 20);
+    return (B - 1) * prefix_bytes >= 1024.0 * (1 << 20);
 }
 
 int pa_cascade_pays(int32_t B, int32_t Hkv, int32_t D, int32_t n_prefix_blocks, int32_t block_size) {
@@ -822,12 +826,27 @@ int pa_decode_cascade(void *out, float *lse, const void *q, const void *k_cache,
                     nullptr, NewTokens(), B, nullptr, pre);
     if (rc) return rc;
     // 2. each sequence's own blocks: the table from entry n_prefix_blocks on,
-    //    lengths less the prefix
+    //    lengths less the prefix.  Where the suffix is split (P2 >= 2: its
+    //    grid fits on the GPU at once, and the merge tasks spread over P2
+    //    CTAs per group) and a merge task can hold every partition, this
+    //    launch also merges the P1 + P2 partials of every row (the prefix
+    //    pass's are complete: the launch waits for the previous one before it
+    //    reads anything).  An unsplit suffix leaves the merge to the combine
+    //    kernel, which spreads it over the whole GPU.
     PassOpts suf;
     suf.seq_len_offset = prefix_len;
     suf.part_stride = PT;
     suf.part_offset = P1;
     suf.table_stride = max_blocks_per_seq;
+    if (P2 >= 2 && PT <= pa::kMaxGridMerge) {
+        int32_t *counters = reinterpret_cast<int32_t *>(
+            ws + round_up(rows * PT * cache.head_dim * 4, 256) + round_up(rows * PT * 4, 256));
+        rc = run_decode(true, out, lse, part_o, part_lse, q, k_cache, v_cache, cache,
+                        block_tables + n_prefix_blocks, max_blocks_per_seq - n_prefix_blocks,
+                        seq_lens, B, Hq, scale, P2, status, stream, counters, NewTokens(), 1,
+                        nullptr, suf);
+        if (rc != PA_ETOOLARGE) return rc;
+    }
     rc = run_decode(true, nullptr, nullptr, part_o, part_lse, q, k_cache, v_cache, cache,
                     block_tables + n_prefix_blocks, max_blocks_per_seq - n_prefix_blocks, seq_lens,
                     B, Hq, scale, P2, status, stream, nullptr, NewTokens(), 1, nullptr, suf);

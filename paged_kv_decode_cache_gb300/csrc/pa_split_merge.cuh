@@ -16,6 +16,10 @@
 //      L1-bypassing loads).  Up to 32 partitions a lane owns a dim of a 32-dim
 //      slice; beyond, a lane owns partitions of an 8-dim slice;
 // A wait that runs out sets PA_STATUS_TIMEOUT and the CTA skips the merge.
+// A task merges all part_stride partials of its row: part_stride = P for an
+// ordinary call; a cascade's suffix pass (P CTAs per group) also merges the
+// prefix pass's partials, which the previous launch left in the row's other
+// slots.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -54,7 +58,7 @@ __device__ __forceinline__ int ld_acquire_gpu(const int *p) {
 template <int D>
 __device__ __forceinline__ void merge_slice(const DecodeParams &p, int64_t row, int slice, int lane) {
     constexpr int kMaxHeld = kMaxGridMerge / 32;  // LSEs per lane held in registers
-    const int P = p.num_splits;
+    const int P = p.part_stride;                  // partials of the row
     const float *pl = p.part_lse + row * P;
     const float *po = p.part_o + row * P * D + slice * 32 + lane;
     float lv[kMaxHeld], cur[32];
@@ -109,7 +113,7 @@ __device__ __forceinline__ void merge_slice(const DecodeParams &p, int64_t row, 
 template <int D>
 __device__ __forceinline__ void merge_slice_wide(const DecodeParams &p, int64_t row, int slice, int lane) {
     constexpr int kMaxHeld = kMaxGridMerge / 32;  // partitions per lane
-    const int P = p.num_splits;
+    const int P = p.part_stride;                  // partials of the row
     const float *pl = p.part_lse + row * P;
     const float *po = p.part_o + row * P * D + slice * 8;
     float lv[kMaxHeld];
@@ -213,7 +217,7 @@ __device__ void merge_split_group(const DecodeParams &p, int group, int part, in
     sync();
     if (*flag) {
         const int warp = t >> 5, lane = t & 31;
-        if (P <= 32) {  // lanes over dims: one round trip per 32-dim slice
+        if (p.part_stride <= 32) {  // lanes over dims: one round trip per 32-dim slice
             const int tasks = nrows * (D / 32);
             for (int k = part * kWarps + warp; k < tasks; k += P * kWarps)
                 merge_slice<D>(p, row_of(k / (D / 32)), k % (D / 32), lane);

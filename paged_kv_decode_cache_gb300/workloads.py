@@ -294,6 +294,12 @@ WORKLOADS.update({
     # plainly and as a cascade
     "qwen3-0.6b-B256-prefix2048": lambda **kw: qwen3_long_prefix(256, 128, **kw),
     "qwen3-0.6b-B256-prefix2048-cascade": lambda **kw: _cascade(qwen3_long_prefix(256, 128, **kw), 128),
+    # a few sequences behind a 16384-token shared prefix (a long shared document)
+    "qwen3-0.6b-B8-prefix16384": lambda **kw: qwen3_long_prefix(8, 1024, **kw),
+    "qwen3-0.6b-B8-prefix16384-cascade": lambda **kw: _cascade(qwen3_long_prefix(8, 1024, **kw), 1024),
+    # parallel samples of one 65536-token document: a prefix larger than L2
+    "qwen3-0.6b-B4-prefix65536": lambda **kw: qwen3_long_prefix(4, 4096, **kw),
+    "qwen3-0.6b-B4-prefix65536-cascade": lambda **kw: _cascade(qwen3_long_prefix(4, 4096, **kw), 4096),
     # one 512-token chunked-prefill chunk per sequence on the Qwen2.5-1.5B layer
     "qwen2.5-1.5b-B1-chunk512": lambda **kw: prefill_chunk("qwen2.5-1.5b-B1", 512, **kw),
     "qwen2.5-1.5b-B8-chunk512": lambda **kw: prefill_chunk("qwen2.5-1.5b-B8", 512, **kw),

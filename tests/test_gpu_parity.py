@@ -718,21 +718,28 @@ def test_cascade_full_size_qwen3(mode, cascade_mode):
     assert dev.status_value() == 0
 
 
+@pytest.mark.parametrize("name,npre,pays", [("qwen3-0.6b-B256-prefix2048", 128, True),
+                                            ("qwen3-0.6b-B8-prefix16384", 1024, False),
+                                            ("qwen3-0.6b-B4-prefix65536", 4096, False)])
 @pytest.mark.parametrize("cascade", [True, False])
-def test_long_shared_prefix_full_size(cascade, cascade_mode):
-    """256 Qwen3-shaped sequences behind one 2048-token shared prefix, after
-    this step's write: the cascade (prefix once for the whole batch on the
-    prefill-shaped kernel, then each sequence's own blocks, then the merge)
-    and the plain fused step, every row against the oracle's plain decode."""
-    w = W.WORKLOADS["qwen3-0.6b-B256-prefix2048"]()
+def test_long_shared_prefix_full_size(name, npre, pays, cascade, cascade_mode):
+    """Qwen3-shaped sequences behind one long shared prefix (256 behind 2048
+    tokens, 8 behind 16384, 4 behind 65536), after this step's write: the
+    cascade (prefix once for the whole batch, then each sequence's own
+    blocks, then the merge: a combine kernel after the 256 unsplit suffixes,
+    inside the split suffix pass for the others; forced where the automatic
+    choice is plain decode) and the plain fused step, every row against the
+    oracle's plain decode."""
+    w = W.WORKLOADS[name]()
     kc, vc = oracle_after_write(w)
     ref, ref_lse = oracle.decode(w.q, kc, vc, w.block_tables, w.seq_lens, w.scale)
     dev = Dev(w)
     if cascade:
         cascade_mode("auto")
-        assert pa.pa_cascade_pays(w.B, w.Hkv, w.D, 128, w.block_size)   # the automatic choice
+        assert bool(pa.pa_cascade_pays(w.B, w.Hkv, w.D, npre, w.block_size)) == pays  # the automatic choice
+        if not pays:
+            cascade_mode("always")
         dev.write()
-        npre = 128
         ws = torch.zeros(pa.pa_cascade_workspace_bytes(w.B, w.Hq, w.Hkv, w.D, npre, w.max_blocks,
                                                        w.block_size), dtype=torch.uint8, device="cuda")
         out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
