@@ -402,7 +402,12 @@ def run_ours(args, world, rank, local):
                 else pa.pa_splitkv_workspace_bytes(w.B * w.q_len, w.Hq, w.D, P))
     ws = torch.zeros(max(1, ws_bytes), dtype=torch.uint8,
                      device=dev)
-    merged = P > 1   # the split kernel merges its own partials (one cooperative launch)
+    # kernel launches of the decode call (not the cascade proper): 1 unsplit or split with
+    # the merge inside the launch, 2 when a combine follows (a grid that takes waves)
+    sms_count = torch.cuda.get_device_properties(dev).multi_processor_count
+    decode_launches = pa.pa_decode_launches(w.B, w.q_len, w.Hq, w.Hkv, w.D, w.max_blocks,
+                                            w.block_size, P, sms_count)
+    merged = P > 1 and decode_launches == 1   # the split kernel merges its own partials
 
     def step(r, ev0=None, ev1=None):
         kc, vc = pools[r]
@@ -431,7 +436,7 @@ def run_ours(args, world, rank, local):
             ev1.record(stream)
 
     launches_per_step = (1 + cascade_kernels if cascade_runs else
-                         2 if (args.unfused or mq or fp8 or cascade) else 1)
+                         (1 if (args.unfused or mq or fp8 or cascade) else 0) + decode_launches)
     # The timed region replays CUDA graphs that hold exactly the K timed steps
     # (consecutive steps cycle over the pool replicas): one graph when K <= 1024,
     # else K // 1024 replays of a 1024-step graph and one graph of the rest.  A
@@ -495,7 +500,8 @@ def run_ours(args, world, rank, local):
     elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
     clocks = clk.summary()
     kern_ms = []
-    fused = not (args.unfused or mq or fp8 or cascade)
+    fused_write = not (args.unfused or mq or fp8 or cascade)   # pa_decode_step writes the new K/V
+    fused = fused_write and decode_launches == 1                  # ... in the step's only launch
     if mk and not fused:
         samples = [capture(S, events=True) for _ in range(NG)]
         with torch.cuda.stream(stream):
@@ -608,7 +614,7 @@ def run_ours(args, world, rank, local):
     peak, peak_kind = measured_peak_gbs()
     # the timed launch reads K, V and q, writes the bf16 output and (fused step) moves
     # this step's new K/V into the pool; its split partials and merge are overhead
-    kern_bytes = attn_bytes + (write_bytes if fused else 0)
+    kern_bytes = attn_bytes + (write_bytes if fused_write else 0)
     roofline = None
     if kern_ms_avg:
         ach = kern_bytes / (kern_ms_avg * 1e-3) / 1e9
@@ -620,7 +626,8 @@ def run_ours(args, world, rank, local):
                                              " (shared prefix: plain split decode)" if cascade else
                                              " (fp8 pools)" if fp8 else " (multi-query)" if mq else
                                              "" if args.unfused else " (fused write)")
-                              + (" + split merge" if merged else ""),
+                              + (" + split merge" if merged else
+                                 " + combine" if decode_launches == 2 and not cascade_runs else ""),
                     "kernel_us": round(kern_ms_avg * 1e3, 3), "kernel_bytes": kern_bytes,
                     "kernel_timing": kern_method,
                     "kernel_us_event_sample": (round(kern_ms_sampled * 1e3, 3)
@@ -654,7 +661,9 @@ def run_ours(args, world, rank, local):
                                 "cache_write of the q_len new tokens, then pa_decode_mq (causal)"
                                 if mq else "cache_write, then split decode with merge"
                                 if args.unfused else
-                                "pa_decode_step: cache write + split decode + merge, one launch"),
+                                "pa_decode_step: cache write + split decode + merge, one launch"
+                                if decode_launches == 1 else
+                                "pa_decode_step: cache write + split decode (partials), then the combine"),
                        "parallelism": f"replicas x{world}",
                        "l2": f"{R} pool replicas rotated per step ({touched/1e6:.0f} MB read per step)"},
             "us_per_step": ms_per_step * 1e3,
@@ -811,7 +820,8 @@ def measure_configs(args, dev, peak):
             del pools, k0, v0, g
             torch.cuda.empty_cache()
     return {"peak_gbs": peak, "l2_between_calls": "flushed (2x L2 written)",
-            "step": "pa_decode_step (fused cache write + split decode + merge), auto P",
+            "step": "pa_decode_step (fused cache write + split decode + merge: in the launch, or by "
+                    "the combine kernel after a grid that runs in waves), auto P",
             "clocks": clk.summary(), "workloads": out_all}
 
 

@@ -179,8 +179,11 @@ int pa_decode(void *out, float *lse, const void *q, const void *k_cache, const v
  * largest P for which the B * Hkv * P CTAs fit one wave of the decode kernel
  * that the group size Hq / Hkv and head_dim D select (2 CTAs per SM for the
  * CUDA-core kernel, 1 for the tensor-core kernel), capped so that every
- * partition keeps at least four 16-token tiles.  Host-only; depends only on
- * its arguments and the PA_OPT_DECODE_KERNEL switch.
+ * partition keeps at least four 16-token tiles.  A batch with more CTAs than
+ * one wave holds runs in waves: its sequences are split into partitions of
+ * about 48 tiles (of max_blocks_per_seq * block_size tokens), which evens the
+ * waves out when the lengths differ.  Host-only; depends only on its
+ * arguments and the PA_OPT_DECODE_KERNEL switch.
  * Returns P >= 1, or PA_EINVAL / PA_EUNSUPPORTED.
  */
 int pa_choose_num_splits(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
@@ -447,6 +450,18 @@ int pa_choose_num_splits_mq(int32_t B, int32_t q_len, int32_t Hq, int32_t Hkv, i
 /* P that pa_decode_splitkv uses for num_splits == 0 on the current device (PA_ECUDA on error). */
 int pa_auto_num_splits(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t max_blocks_per_seq,
                        int32_t block_size);
+
+/*
+ * Kernel launches that pa_decode_splitkv, pa_decode_step, pa_decode_mq and
+ * pa_decode_splitkv_fp8 make for this shape with num_splits partitions (0:
+ * the automatic choice for sm_count SMs): 1 unsplit, or split with the
+ * partials merged inside the launch (its grid fits on the GPU at once and
+ * P <= 256); 2 otherwise (partials, then the combine kernel).  0 for B = 0;
+ * PA_EINVAL on bad arguments.  Host-only.
+ */
+int pa_decode_launches(int32_t B, int32_t q_len, int32_t Hq, int32_t Hkv, int32_t D,
+                       int32_t max_blocks_per_seq, int32_t block_size, int32_t num_splits,
+                       int32_t sm_count);
 
 /* Static description of a return code. */
 const char *pa_strerror(int code);

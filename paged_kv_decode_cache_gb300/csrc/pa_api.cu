@@ -41,6 +41,7 @@ constexpr int kMaxGroupCc = 8;    // query heads per KV head, CUDA-core kernel
 constexpr int kMaxGroupTc = 32;   // MMA columns per KV head (query heads x positions), tensor cores
 constexpr int kMaxGridZ = 65535;  // sequences per launch (gridDim.z)
 constexpr int kMinTilesPerSplit = 4;  // 64 tokens: fewer idle SMs at 4k tokens
+constexpr int kMultiWaveTiles = 48;   // tiles per partition of a batch that takes several waves
 constexpr int64_t kMaxRowsQ = 1 << 24;  // B x q_len of one multi-query call
 constexpr int kMaxSplits = 256;
 constexpr int PA_ETOOLARGE = -100;  // internal: the cooperative grid does not fit at once
@@ -541,9 +542,17 @@ int pa_choose_num_splits_mq(int32_t B, int32_t q_len, int32_t Hq, int32_t Hkv, i
     const int64_t units = prefill ? static_cast<int64_t>(B) * Hkv * prefill_tiles(G, q_len)
                                   : units_per_split(k, B, G, Hkv, qpc, (q_len + qpc - 1) / qpc);
     const int64_t slots = static_cast<int64_t>(sm_count) * ctas_per_sm(k);
-    int64_t P = slots / units;  // largest P whose grid still fits one wave
     const int64_t lmax = static_cast<int64_t>(max_blocks_per_seq) * block_size;
     const int64_t tiles = (lmax + 15) / 16;
+    int64_t P = slots / units;  // largest P whose grid still fits one wave
+    if (P < 1 && !prefill) {
+        // More units than CTA slots: the grid runs in waves, and sequences of
+        // different lengths end at different times.  Partitions of about 48
+        // tiles even the waves out (a Qwen3 batch of 256 sequences of
+        // U[129, 2048] tokens: 1.1x faster with 3 partitions than unsplit);
+        // their partials are merged by a combine launch.
+        P = (tiles + kMultiWaveTiles - 1) / kMultiWaveTiles;
+    }
     const int64_t p_by_tiles = (tiles + kMinTilesPerSplit - 1) / kMinTilesPerSplit;
     if (P > p_by_tiles) P = p_by_tiles;
     if (P > kMaxSplits) P = kMaxSplits;
@@ -602,6 +611,22 @@ int pa_combine(void *out, float *lse, const float *part_o, const float *part_lse
 }
 
 namespace {
+// Whether a split call (P partitions) merges its partials in the same launch:
+// its cooperative grid must fit on the GPU at once (sm_count x the kernel's
+// CTAs per SM) and a merge task must hold every partition; the prefill-shaped
+// kernel never does.  Otherwise partials, then pa_combine.
+bool merge_in_launch(int32_t B, int32_t q_len, int32_t Hq, int32_t Hkv, int32_t D, int32_t P,
+                     int sm_count) {
+    if (P < 2 || P > pa::kMaxGridMerge || sm_count <= 0) return false;
+    const int G = Hq / Hkv;
+    const int qpc = queries_per_cta(G, q_len);
+    Kernel k;
+    if (pick_kernel(G * qpc, D, &k)) return false;
+    if (k == Kernel::kTensorCore && prefill_shape(G, q_len)) return false;
+    const int64_t units = units_per_split(k, B, G, Hkv, qpc, (q_len + qpc - 1) / qpc);
+    return units * P <= static_cast<int64_t>(sm_count) * ctas_per_sm(k);
+}
+
 // Split-KV decode shared by pa_decode_splitkv, pa_decode_step, pa_decode_mq,
 // pa_decode_splitkv_fp8 and pa_decode_splitkv_noalloc.  With library_scratch
 // the workspace is the library's own array (pa::noalloc_scratch), looked up
@@ -651,7 +676,7 @@ int splitkv_common(void *out, float *lse, const void *q, const void *k_cache, co
     // One cooperative launch that merges its own partials when the whole grid
     // fits on the GPU at once and its merge tasks can hold every partition;
     // otherwise partials, then pa_combine.
-    if (P <= pa::kMaxGridMerge) {
+    if (merge_in_launch(B, q_len, Hq, cache.num_kv_heads, cache.head_dim, P, sm_count_current())) {
         if (library_scratch &&
             cudaMemsetAsync(counters, 0, static_cast<size_t>(Bq) * Hq * 8, stream) != cudaSuccess)
             return PA_ECUDA;
@@ -883,6 +908,23 @@ int pa_decode_step(void *out, float *lse, const void *q, const void *k_new, cons
     return splitkv_common(out, lse, q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq,
                           seq_lens, B, Hq, scale, num_splits, workspace, workspace_bytes, status,
                           stream, nt);
+}
+
+
+int pa_decode_launches(int32_t B, int32_t q_len, int32_t Hq, int32_t Hkv, int32_t D,
+                       int32_t max_blocks_per_seq, int32_t block_size, int32_t num_splits,
+                       int32_t sm_count) {
+    if (B < 0 || q_len <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 ||
+        max_blocks_per_seq <= 0 || block_size <= 0 || num_splits < 0 || sm_count <= 0)
+        return PA_EINVAL;
+    if (B == 0) return 0;
+    int P = num_splits;
+    if (P == 0) {
+        P = pa_choose_num_splits_mq(B, q_len, Hq, Hkv, D, max_blocks_per_seq, block_size, sm_count);
+        if (P < 0) return P;
+    }
+    if (P == 1) return 1;
+    return merge_in_launch(B, q_len, Hq, Hkv, D, P, sm_count) ? 1 : 2;
 }
 
 }  // extern "C"

@@ -67,6 +67,7 @@ _SIGNATURES = {
     "pa_decode_mq": ([_P, _P, _P, _I32, _P, _P, CacheDesc, _P, _I32, _P, _I32, _I32, _F32, _I32,
                       _P, _SZ, _P, _P], ctypes.c_int),
     "pa_choose_num_splits_mq": ([_I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32], ctypes.c_int),
+    "pa_decode_launches": ([_I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32], ctypes.c_int),
     "pa_decode_cascade": ([_P, _P, _P, _P, _P, CacheDesc, _I32, _P, _I32, _P, _I32, _I32, _F32, _P,
                            _SZ, _P, _P], ctypes.c_int),
     "pa_cascade_workspace_bytes": ([_I32, _I32, _I32, _I32, _I32, _I32, _I32], _SZ),
@@ -203,6 +204,14 @@ def pa_choose_num_splits_mq(B: int, q_len: int, Hq: int, Hkv: int, D: int,
     r = lib().pa_choose_num_splits_mq(B, q_len, Hq, Hkv, D, max_blocks_per_seq, block_size,
                                       sm_count)
     _check("pa_choose_num_splits_mq", min(r, 0))
+    return r
+
+
+def pa_decode_launches(B: int, q_len: int, Hq: int, Hkv: int, D: int, max_blocks_per_seq: int,
+                       block_size: int, num_splits: int, sm_count: int) -> int:
+    r = lib().pa_decode_launches(B, q_len, Hq, Hkv, D, max_blocks_per_seq, block_size, num_splits,
+                                 sm_count)
+    _check("pa_decode_launches", min(r, 0))
     return r
 
 

@@ -91,11 +91,35 @@ def test_split_policy(lib, use_kernel, B, Hq, Hkv, D, mb, bs, sms):
     chunk = pa.pa_partition_tokens(mb, bs, P)
     assert chunk % 16 == 0 and chunk * P >= lmax and chunk * (P - 1) < lmax  # no empty tail split
     units = _units(B, Hq, Hkv, D)
-    if P > 1:
+    if P > 1 and units <= slots:
         assert units * P <= slots              # one wave of resident CTAs
         assert chunk >= 16 * 4 or chunk * P >= lmax
-    if units >= slots:
-        assert P == 1
+    if units > slots:   # waves: partitions of about 48 tiles, without empty tails
+        tiles = (lmax + 15) // 16
+        p0 = min(-(-tiles // 48), -(-tiles // 4))
+        assert P == -(-lmax // pa.pa_partition_tokens(mb, bs, max(1, p0)))
+
+
+def test_multi_wave_batches_split_into_48_tile_partitions(lib, use_kernel):
+    use_kernel("auto")
+    # the Qwen3 batch: 256 sequences of up to 2048 tokens, 8 KV heads per CTA, 148 SMs
+    assert pa.pa_choose_num_splits(256, 16, 8, 128, 128, 16, 148) == 3
+    assert pa.pa_choose_num_splits(256, 16, 8, 128, 16, 16, 148) == 1      # 256 tokens: one partition
+    assert pa.pa_choose_num_splits(148, 16, 8, 128, 128, 16, 148) == 1     # exactly one wave
+
+
+def test_decode_launches(lib, use_kernel):
+    use_kernel("auto")
+    L = pa.pa_decode_launches
+    assert L(8, 1, 28, 4, 128, 256, 16, 1, 148) == 1          # unsplit
+    assert L(8, 1, 28, 4, 128, 256, 16, 0, 148) == 1          # split, one wave: merged in the launch
+    assert L(1, 1, 28, 4, 128, 2048, 16, 0, 148) == 1
+    assert L(256, 1, 16, 8, 128, 128, 16, 0, 148) == 2        # waves: partials, then the combine
+    assert L(8, 1, 28, 4, 128, 4096, 16, 257, 148) == 2       # more partitions than a merge task holds
+    assert L(8, 512, 12, 2, 128, 128, 16, 2, 148) == 2        # the prefill-shaped kernel
+    assert L(0, 1, 28, 4, 128, 256, 16, 0, 148) == 0
+    assert lib.pa_decode_launches(8, 1, 28, 5, 128, 256, 16, 0, 148) == pa.PA_EINVAL
+    assert lib.pa_decode_launches(8, 1, 28, 4, 128, 256, 16, 0, 0) == pa.PA_EINVAL
 
 
 def test_split_policy_fills_small_batches(lib, use_kernel):
@@ -215,8 +239,9 @@ def test_mq_split_policy(lib, use_kernel):
     # 7B layer, 4 queries: 32 // 7 = 4 positions per CTA -> 28 columns, one KV head
     # per CTA -> 4 CTAs per sequence per split -> one wave of 152 SMs holds P = 4
     assert pa.pa_choose_num_splits_mq(8, 4, 28, 4, 128, 256, 16, 152) == 4
-    # Qwen3 shape, 4 queries: all fit one CTA per 8 KV heads -> as q_len = 1
-    assert pa.pa_choose_num_splits_mq(256, 4, 16, 8, 128, 128, 16, 152) == 1
+    # Qwen3 shape, 4 queries: all fit one CTA per 8 KV heads -> as q_len = 1 (256 units:
+    # waves, partitions of 48 tiles)
+    assert pa.pa_choose_num_splits_mq(256, 4, 16, 8, 128, 128, 16, 152) == 3
     # more query groups never give more splits
     prev = 10 ** 9
     for q_len in (1, 2, 3, 5, 8, 16, 64):
