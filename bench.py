@@ -411,18 +411,21 @@ def run_ours(args, world, rank, local):
 
     def step(r, ev0=None, ev1=None):
         kc, vc = pools[r]
-        if fp8:
+        if fp8 and args.unfused:
             pa.pa_cache_write_fp8(kn, vn, slots, kc, vc, w.k_scale, w.v_scale, stream=stream)
-        elif args.unfused or mq or cascade:
+        elif (args.unfused or mq or cascade) and not fp8:
             pa.pa_cache_write(kn, vn, slots, kc, vc, stream=stream)
         if ev0 is not None:
             ev0.record(stream)
         if cascade:
             pa.pa_decode_cascade(out, lse, q, kc, vc, w.cascade_blocks, bt, sl, w.scale, workspace=ws,
                                  stream=stream)
-        elif fp8:
+        elif fp8 and args.unfused:
             pa.pa_decode_splitkv_fp8(out, lse, q, kc, vc, w.k_scale, w.v_scale, bt, sl, w.scale,
                                      num_splits=P, workspace=ws, stream=stream)
+        elif fp8:   # one launch: quantise and write this step's K/V, attend, merge the splits
+            pa.pa_decode_step_fp8(out, lse, q, kn, vn, slots, kc, vc, w.k_scale, w.v_scale, bt, sl,
+                                  w.scale, num_splits=P, workspace=ws, stream=stream)
         elif mq:
             pa.pa_decode_mq(out, lse, q, kc, vc, bt, sl, w.scale, num_splits=P, workspace=ws,
                             stream=stream)
@@ -436,7 +439,7 @@ def run_ours(args, world, rank, local):
             ev1.record(stream)
 
     launches_per_step = (1 + cascade_kernels if cascade_runs else
-                         (1 if (args.unfused or mq or fp8 or cascade) else 0) + decode_launches)
+                         (1 if (args.unfused or mq or cascade) else 0) + decode_launches)
     # The timed region replays CUDA graphs that hold exactly the K timed steps
     # (consecutive steps cycle over the pool replicas): one graph when K <= 1024,
     # else K // 1024 replays of a 1024-step graph and one graph of the rest.  A
@@ -500,7 +503,7 @@ def run_ours(args, world, rank, local):
     elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
     clocks = clk.summary()
     kern_ms = []
-    fused_write = not (args.unfused or mq or fp8 or cascade)   # pa_decode_step writes the new K/V
+    fused_write = not (args.unfused or mq or cascade)   # pa_decode_step[_fp8] writes the new K/V
     fused = fused_write and decode_launches == 1                  # ... in the step's only launch
     if mk and not fused:
         samples = [capture(S, events=True) for _ in range(NG)]
@@ -566,10 +569,14 @@ def run_ours(args, world, rank, local):
             pa.pa_cache_write(kn_e, vn_e, slots_e, kc, vc, stream=stream)
             pa.pa_decode_cascade(out_e, lse_e, q_e, kc, vc, w.cascade_blocks, bt_e, sl_e, w.scale,
                                  workspace=ws, stream=stream)
-        elif fp8:
+        elif fp8 and args.unfused:
             pa.pa_cache_write_fp8(kn_e, vn_e, slots_e, kc, vc, w.k_scale, w.v_scale, stream=stream)
             pa.pa_decode_splitkv_fp8(out_e, lse_e, q_e, kc, vc, w.k_scale, w.v_scale, bt_e, sl_e,
                                      w.scale, num_splits=P, workspace=ws, stream=stream)
+        elif fp8:
+            pa.pa_decode_step_fp8(out_e, lse_e, q_e, kn_e, vn_e, slots_e, kc, vc, w.k_scale,
+                                  w.v_scale, bt_e, sl_e, w.scale, num_splits=P, workspace=ws,
+                                  stream=stream)
         elif mq:
             pa.pa_cache_write(kn_e, vn_e, slots_e, kc, vc, stream=stream)
             pa.pa_decode_mq(out_e, lse_e, q_e, kc, vc, bt_e, sl_e, w.scale, num_splits=P,
@@ -657,6 +664,9 @@ def run_ours(args, world, rank, local):
                                 "pa_cache_write, then pa_decode_cascade (plain split decode: the "
                                 "cascade does not pay)" if cascade else
                                 "pa_cache_write_fp8, then pa_decode_splitkv_fp8 (e4m3 pools)"
+                                if fp8 and args.unfused else
+                                "pa_decode_step_fp8: quantising cache write + split decode + merge "
+                                f"(e4m3 pools), {decode_launches} launch{'es' if decode_launches > 1 else ''}"
                                 if fp8 else
                                 "cache_write of the q_len new tokens, then pa_decode_mq (causal)"
                                 if mq else "cache_write, then split decode with merge"

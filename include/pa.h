@@ -440,6 +440,25 @@ int pa_decode_splitkv_fp8(void *out, float *lse, const void *q, const void *k_ca
                           int32_t *status, pa_stream_t stream);
 
 /*
+ * One whole decode step over FP8 pools in one launch: pa_decode_step's
+ * fused write, quantised as pa_cache_write_fp8 quantises (the same codes,
+ * byte for byte), and pa_decode_splitkv_fp8's attention.  The same result as
+ *   pa_cache_write_fp8(k_new, v_new, slot_mapping, B, ...) then
+ *   pa_decode_splitkv_fp8(...)
+ * when slot_mapping[b] is the slot of position seq_lens[b] - 1 of sequence b;
+ * a non-negative slot that is not is not written and sets
+ * PA_STATUS_BAD_SLOT.  k_new, v_new: device bf16 [B, Hkv, D]; every other
+ * argument as pa_decode_step and pa_decode_splitkv_fp8.
+ */
+int pa_decode_step_fp8(void *out, float *lse, const void *q, const void *k_new, const void *v_new,
+                       const int64_t *slot_mapping, void *k_cache, void *v_cache,
+                       pa_cache_desc cache, float k_scale, float v_scale,
+                       const int32_t *block_tables, int32_t max_blocks_per_seq,
+                       const int32_t *seq_lens, int32_t B, int32_t Hq, float scale,
+                       int32_t num_splits, void *workspace, size_t workspace_bytes,
+                       int32_t *status, pa_stream_t stream);
+
+/*
  * Split count for pa_decode_mq, by the rule of pa_choose_num_splits with the
  * CTAs of every query-position group counted.  q_len = 1 gives
  * pa_choose_num_splits.  Returns P >= 1, or PA_EINVAL / PA_EUNSUPPORTED.
@@ -452,8 +471,8 @@ int pa_auto_num_splits(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t ma
                        int32_t block_size);
 
 /*
- * Kernel launches that pa_decode_splitkv, pa_decode_step, pa_decode_mq and
- * pa_decode_splitkv_fp8 make for this shape with num_splits partitions (0:
+ * Kernel launches that pa_decode_splitkv, pa_decode_step, pa_decode_mq,
+ * pa_decode_splitkv_fp8 and pa_decode_step_fp8 make for this shape with num_splits partitions (0:
  * the automatic choice for sm_count SMs): 1 unsplit, or split with the
  * partials merged inside the launch (its grid fits on the GPU at once and
  * P <= 256); 2 otherwise (partials, then the combine kernel).  0 for B = 0;

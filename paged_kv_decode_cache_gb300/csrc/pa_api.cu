@@ -292,6 +292,7 @@ pa::DecodeParams base_params(const void *q, const pa_cache_desc &c, const int32_
     p.q_per_cta = 1;
     p.head_groups = c.num_kv_heads;
     p.v_scale = 1.f;
+    p.k_scale = 1.f;
     p.causal = 1;
     p.seq_len_const = -1;
     p.seq_len_offset = 0;
@@ -419,6 +420,7 @@ int run_decode(bool split, void *out, float *lse, float *part_o, float *part_lse
         if (f8) {
             p.scale_log2 = scale * f8->k_scale * 1.4426950408889634f;
             p.v_scale = f8->v_scale;
+            p.k_scale = f8->k_scale;
             rc = make_kv_map_fp8(&kmap, k_cache, c, HC);
             if (!rc) rc = make_kv_map_fp8(&vmap, v_cache, c, HC);
             if (rc) return rc;
@@ -741,6 +743,29 @@ int pa_cache_write_fp8(const void *k_new, const void *v_new, const int64_t *slot
         static_cast<int64_t>(cache.num_blocks) * cache.block_size, row_elems, k_scale, v_scale,
         status, stream);
     return e == cudaSuccess ? PA_OK : PA_ECUDA;
+}
+
+int pa_decode_step_fp8(void *out, float *lse, const void *q, const void *k_new, const void *v_new,
+                       const int64_t *slot_mapping, void *k_cache, void *v_cache,
+                       pa_cache_desc cache, float k_scale, float v_scale,
+                       const int32_t *block_tables, int32_t max_blocks_per_seq,
+                       const int32_t *seq_lens, int32_t B, int32_t Hq, float scale,
+                       int32_t num_splits, void *workspace, size_t workspace_bytes,
+                       int32_t *status, pa_stream_t stream) {
+    if (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
+        return PA_EINVAL;
+    if (cache.head_dim != 128) return PA_EUNSUPPORTED;
+    if (B == 0) return PA_OK;
+    if (!k_new || !v_new || !slot_mapping) return PA_EINVAL;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(slot_mapping, 8)) return PA_EINVAL;
+    NewTokens nt;
+    nt.k_new = k_new;
+    nt.v_new = v_new;
+    nt.slot_mapping = slot_mapping;
+    const Fp8Scales f8{k_scale, v_scale};
+    return splitkv_common(out, lse, q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq,
+                          seq_lens, B, Hq, scale, num_splits, workspace, workspace_bytes, status,
+                          stream, nt, 1, &f8);
 }
 
 int pa_decode_splitkv_fp8(void *out, float *lse, const void *q, const void *k_cache,

@@ -74,16 +74,7 @@ cache_write_fp8_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict_
             continue;
         }
         const uint4 in = (is_v ? v_new : k_new)[i * row_chunks + c];
-        const float scale = is_v ? v_scale : k_scale;
-        const uint32_t w[4] = {in.x, in.y, in.z, in.w};
-        uint32_t out[2] = {0u, 0u};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const __nv_fp8_storage_t lo = __nv_cvt_float_to_fp8(bf16lo(w[k]) / scale, __NV_SATFINITE, __NV_E4M3);
-            const __nv_fp8_storage_t hi = __nv_cvt_float_to_fp8(bf16hi(w[k]) / scale, __NV_SATFINITE, __NV_E4M3);
-            out[k >> 1] |= (static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 8)) << (16 * (k & 1));
-        }
-        (is_v ? v_cache : k_cache)[s * row_chunks + c] = make_uint2(out[0], out[1]);
+        (is_v ? v_cache : k_cache)[s * row_chunks + c] = e4m3x8_from_bf16(in, is_v ? v_scale : k_scale);
     }
 }
 

@@ -471,7 +471,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     const bool writes = producer && p.k_new && last_pos >= t_begin && last_pos < t_end;
     constexpr int kNewChunks = HC * D / 8;                 // 16-byte chunks of HC rows
     constexpr int kNewPerLane = (kNewChunks + 31) / 32;
-    uint4 newrow[kNewPerLane];
+    uint4 newrow[kNewPerLane];   // (FP8 pools: newcode, its e4m3 codes)
+    uint2 newcode[F8 ? kNewPerLane : 1];
     int64_t slot_b = -1;
     if (writes) {
         slot_b = p.slot_mapping[b];
@@ -480,6 +481,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
 #pragma unroll
         for (int j = 0; j < kNewPerLane; ++j)
             if (lane + 32 * j < kNewChunks) newrow[j] = src[lane + 32 * j];
+        if constexpr (F8) {  // quantised here, out of the issue loop
+            const float wscale = is_v ? p.v_scale : p.k_scale;
+#pragma unroll
+            for (int j = 0; j < kNewPerLane; ++j)
+                if (lane + 32 * j < kNewChunks) newcode[j] = e4m3x8_from_bf16(newrow[j], wscale);
+        }
     }
     int issued = 0;
     // Issues chunks [c_from, c_to) of this producer's ring; false once it aborts.
@@ -508,11 +515,20 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             if (writes && last_pos >= chunk0 && last_pos < chunk0 + C::kT) {  // holds position L - 1
                 const int ph = __shfl_sync(0xffffffffu, phys, 2 * ((last_pos - chunk0) / kTile));
                 if (slot_is_position(slot_b, ph, last_pos, bs) && ph < p.num_blocks) {
-                    uint4 *dst = reinterpret_cast<uint4 *>((is_v ? p.v_pool : p.k_pool) +
-                                                           (slot_b * p.num_kv_heads + g0) * D);
+                    if constexpr (F8) {  // one byte per value, quantised with the pool's scale
+                        uint2 *dst = reinterpret_cast<uint2 *>(
+                            reinterpret_cast<uint8_t *>(is_v ? p.v_pool : p.k_pool) +
+                            (slot_b * p.num_kv_heads + g0) * D);
 #pragma unroll
-                    for (int j = 0; j < kNewPerLane; ++j)
-                        if (lane + 32 * j < kNewChunks) dst[lane + 32 * j] = newrow[j];
+                        for (int j = 0; j < kNewPerLane; ++j)
+                            if (lane + 32 * j < kNewChunks) dst[lane + 32 * j] = newcode[j];
+                    } else {
+                        uint4 *dst = reinterpret_cast<uint4 *>((is_v ? p.v_pool : p.k_pool) +
+                                                               (slot_b * p.num_kv_heads + g0) * D);
+#pragma unroll
+                        for (int j = 0; j < kNewPerLane; ++j)
+                            if (lane + 32 * j < kNewChunks) dst[lane + 32 * j] = newrow[j];
+                    }
                     fence_proxy_async_global();
                 } else if (lane == 0 && !is_v && slot_b >= 0) {
                     set_status(p.status, PA_STATUS_BAD_SLOT);

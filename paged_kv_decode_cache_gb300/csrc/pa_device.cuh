@@ -7,6 +7,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -198,6 +199,23 @@ __device__ __forceinline__ float fast_exp2(float x) {
 // Two bf16 packed in a 32-bit word -> two floats (exact: bf16 is the top half of fp32).
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// FP8 pools: 8 bf16 values (one 16-byte chunk of a K or V row) to their e4m3
+// codes (8 bytes, the same order): fp32(x) / scale, rounded to nearest even,
+// saturating at the largest finite code (+-448), NaN kept.  The one
+// definition of a stored code, for the cache write and the decode step's
+// fused write alike.
+__device__ __forceinline__ uint2 e4m3x8_from_bf16(const uint4 &in, float scale) {
+    const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+    uint32_t out[2] = {0u, 0u};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const __nv_fp8_storage_t lo = __nv_cvt_float_to_fp8(bf16lo(w[k]) / scale, __NV_SATFINITE, __NV_E4M3);
+        const __nv_fp8_storage_t hi = __nv_cvt_float_to_fp8(bf16hi(w[k]) / scale, __NV_SATFINITE, __NV_E4M3);
+        out[k >> 1] |= (static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 8)) << (16 * (k & 1));
+    }
+    return make_uint2(out[0], out[1]);
+}
 
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a tile of
 // 128-byte rows written by TMA with CU_TENSOR_MAP_SWIZZLE_128B (the chunk

@@ -71,8 +71,10 @@ struct DecodeParams {
     int32_t q_per_cta;
     int32_t head_groups;    // CTAs across the KV heads (Hkv / heads per CTA)
     // FP8 pools (e4m3 codes): scale_log2 already includes k_scale; the output
-    // is multiplied by v_scale.  1 for bf16 pools.
+    // is multiplied by v_scale.  1 for bf16 pools.  The fused write quantises
+    // the new rows with the pools' scales (k_scale, v_scale).
     float v_scale;
+    float k_scale;
     // Cascade passes (tensor-core kernel): causal = 0 lets every query see all
     // L keys; L is seq_len_const when >= 0, else seq_lens[b] - seq_len_offset;
     // partials of row r, partition p go to [r * part_stride + part_offset + p].

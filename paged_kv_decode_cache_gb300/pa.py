@@ -75,6 +75,8 @@ _SIGNATURES = {
     "pa_cache_write_fp8": ([_P, _P, _P, _I64, _P, _P, CacheDesc, _F32, _F32, _P, _P], ctypes.c_int),
     "pa_decode_splitkv_fp8": ([_P, _P, _P, _P, _P, CacheDesc, _F32, _F32, _P, _I32, _P, _I32, _I32,
                                _F32, _I32, _P, _SZ, _P, _P], ctypes.c_int),
+    "pa_decode_step_fp8": ([_P, _P, _P, _P, _P, _P, _P, _P, CacheDesc, _F32, _F32, _P, _I32, _P, _I32,
+                            _I32, _F32, _I32, _P, _SZ, _P, _P], ctypes.c_int),
     "pa_set_option": ([_I32, _I32], ctypes.c_int),
     "pa_get_option": ([_I32], ctypes.c_int),
     "pa_strerror": ([ctypes.c_int], ctypes.c_char_p),
@@ -465,6 +467,44 @@ def pa_decode_splitkv_fp8(out, lse, q, k_cache, v_cache, k_scale, v_scale, block
                                      Hq, float(scale), num_splits, _ptr(workspace), ws_bytes,
                                      _ptr(status), _stream(stream))
     _check("pa_decode_splitkv_fp8", rc)
+
+
+@_on_tensors_device
+def pa_decode_step_fp8(out, lse, q, k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale,
+                       block_tables, seq_lens, scale, num_splits=0, workspace=None, status=None,
+                       stream=None):
+    """Fused step over uint8 e4m3 pools: quantise and write this step's new K/V
+    through slot_mapping, then split-KV decode."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need_pool8(k_cache, "k_cache")
+    _need_pool8(v_cache, "v_cache")
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    B, Hq, D = q.shape
+    if v_cache.shape != k_cache.shape or k_cache.shape[3] != D or block_tables.shape[0] != B:
+        raise ValueError("inconsistent q / cache / table shapes")
+    _need(out, "out", torch.bfloat16, 3)
+    _need(k_new, "k_new", torch.bfloat16, 3)
+    _need(v_new, "v_new", torch.bfloat16, 3)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1)
+    if tuple(k_new.shape) != (B, k_cache.shape[2], D) or v_new.shape != k_new.shape:
+        raise ValueError("k_new/v_new must be [B, Hkv, D]")
+    if slot_mapping.shape[0] != B:
+        raise ValueError("slot_mapping must be [B]")
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 2)
+    ws_bytes = 0
+    if workspace is not None:
+        if not (workspace.is_cuda and workspace.is_contiguous()):
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    rc = lib().pa_decode_step_fp8(_ptr(out), _ptr(lse), _ptr(q), _ptr(k_new), _ptr(v_new),
+                                  _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache),
+                                  cache_desc(k_cache), float(k_scale), float(v_scale),
+                                  _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), B, Hq,
+                                  float(scale), num_splits, _ptr(workspace), ws_bytes, _ptr(status),
+                                  _stream(stream))
+    _check("pa_decode_step_fp8", rc)
 
 
 @_on_tensors_device

@@ -658,6 +658,82 @@ def test_fp8_workload_full_size(name):
     assert dev.status_value() == 0
 
 
+@pytest.mark.parametrize("name", ["qwen2.5-7b-bs16-fp8", "qwen3-0.6b-B256-fp8", "long-B2-L32768-fp8"])
+def test_fp8_step_full_size(name):
+    """pa_decode_step_fp8: the fused quantising write leaves both pools byte for
+    byte as the oracle's pa_cache_write_fp8 does, and the output equals the two
+    calls (write, then decode) bit for bit and the oracle within tolerance,
+    at auto P and unsplit."""
+    w = W.WORKLOADS[name]()
+    kc8, vc8 = w.k_cache8.copy(), w.v_cache8.copy()
+    oracle.cache_write_fp8(w.k_new, w.v_new, w.slot_mapping, kc8, vc8, w.k_scale, w.v_scale)
+    ref, ref_lse = oracle.decode_fp8(w.q, kc8, vc8, w.block_tables, w.seq_lens, w.scale,
+                                     w.k_scale, w.v_scale)
+    dev = Dev(w)
+    for P in (0, 1):
+        Pu = P or pa.pa_auto_num_splits(w.B, w.Hq, w.Hkv, w.D, w.max_blocks, w.block_size)
+        ws = torch.zeros(max(1, pa.pa_splitkv_workspace_bytes(w.B, w.Hq, w.D, Pu)),
+                         dtype=torch.uint8, device="cuda")
+        outs = []
+        for fused in (True, False):
+            kc, vc = _fp8_dev(w)
+            out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
+            lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device="cuda")
+            if fused:
+                pa.pa_decode_step_fp8(out, lse, dev.q, dev.k_new, dev.v_new, dev.slot_mapping, kc, vc,
+                                      w.k_scale, w.v_scale, dev.block_tables, dev.seq_lens, w.scale,
+                                      num_splits=Pu, workspace=ws, status=dev.status)
+            else:
+                pa.pa_cache_write_fp8(dev.k_new, dev.v_new, dev.slot_mapping, kc, vc, w.k_scale,
+                                      w.v_scale, status=dev.status)
+                pa.pa_decode_splitkv_fp8(out, lse, dev.q, kc, vc, w.k_scale, w.v_scale,
+                                         dev.block_tables, dev.seq_lens, w.scale, num_splits=Pu,
+                                         workspace=ws, status=dev.status)
+            assert np.array_equal(kc.cpu().numpy(), kc8) and np.array_equal(vc.cpu().numpy(), vc8)
+            outs.append((out, lse))
+        assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+        assert_close(bf16_dev_to_f64(outs[0][0]), ref, f"{name} fused P={Pu}")
+        assert_lse_close(outs[0][1].cpu().double().numpy(), ref_lse, f"{name} fused P={Pu}")
+    assert dev.status_value() == 0
+
+
+def test_fp8_step_slots():
+    """The fused FP8 write skips a negative slot and refuses (PA_STATUS_BAD_SLOT,
+    nothing written) a slot that is not position L - 1 of its sequence; the
+    other sequences' rows are written and attended as the oracle's."""
+    lens = (40, 17, 100)
+    w = W.with_fp8_pools(W.make_workload("f8s", B=3, Hq=16, Hkv=8, D=128, block_size=16,
+                                         seq_lens=list(lens), num_blocks=20, seed=77))
+    slots = w.slot_mapping.copy()
+    slots[1] = -1
+    dev = Dev(w)
+    kc, vc = _fp8_dev(w)
+    out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
+    pa.pa_decode_step_fp8(out, None, dev.q, dev.k_new, dev.v_new, torch.from_numpy(slots).cuda(),
+                          kc, vc, w.k_scale, w.v_scale, dev.block_tables, dev.seq_lens, w.scale,
+                          num_splits=1, status=dev.status)
+    kc8, vc8 = w.k_cache8.copy(), w.v_cache8.copy()
+    oracle.cache_write_fp8(w.k_new, w.v_new, slots, kc8, vc8, w.k_scale, w.v_scale)
+    assert np.array_equal(kc.cpu().numpy(), kc8) and np.array_equal(vc.cpu().numpy(), vc8)
+    ref, _ = oracle.decode_fp8(w.q, kc8, vc8, w.block_tables, w.seq_lens, w.scale, w.k_scale,
+                               w.v_scale)
+    assert_close(bf16_dev_to_f64(out), ref, "fp8 step, one slot skipped")
+    assert dev.status_value() == 0
+    # sequence 2's slot moved to position 0 of sequence 0: not written, flagged
+    bad = w.slot_mapping.copy()
+    bad[2] = w.block_tables[0, 0] * 16
+    kc, vc = _fp8_dev(w)
+    pa.pa_decode_step_fp8(out, None, dev.q, dev.k_new, dev.v_new, torch.from_numpy(bad).cuda(),
+                          kc, vc, w.k_scale, w.v_scale, dev.block_tables, dev.seq_lens, w.scale,
+                          num_splits=1, status=dev.status)
+    assert dev.status_value() & pa.PA_STATUS_BAD_SLOT
+    written = bad.copy()
+    written[2] = -1
+    kc8, vc8 = w.k_cache8.copy(), w.v_cache8.copy()
+    oracle.cache_write_fp8(w.k_new, w.v_new, written, kc8, vc8, w.k_scale, w.v_scale)
+    assert np.array_equal(kc.cpu().numpy(), kc8) and np.array_equal(vc.cpu().numpy(), vc8)
+
+
 # ------------------------------------------------ cascade decode (shared prefix)
 CASCADE = [
     # (Hq, Hkv, bs, lens, shared prefix blocks)
