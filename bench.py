@@ -396,7 +396,9 @@ def run_ours(args, world, rank, local):
         p1 = pa.pa_choose_num_splits_mq(1, w.B, w.Hq, w.Hkv, w.D, w.cascade_blocks, w.block_size, sms)
         p2 = pa.pa_choose_num_splits(w.B, w.Hq, w.Hkv, w.D, w.max_blocks - w.cascade_blocks,
                                      w.block_size, sms)
-        cascade_kernels = 2 if p2 >= 2 and p1 + p2 <= 256 else 3
+        suffix_merges = pa.pa_decode_launches(w.B, 1, w.Hq, w.Hkv, w.D, w.max_blocks - w.cascade_blocks,
+                                              w.block_size, p2, sms) == 1
+        cascade_kernels = 2 if p2 >= 2 and suffix_merges and p1 + p2 <= 256 else 3
     ws_bytes = (pa.pa_cascade_workspace_bytes(w.B, w.Hq, w.Hkv, w.D, w.cascade_blocks, w.max_blocks,
                                               w.block_size) if cascade
                 else pa.pa_splitkv_workspace_bytes(w.B * w.q_len, w.Hq, w.D, P))

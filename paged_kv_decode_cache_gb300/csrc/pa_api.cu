@@ -888,7 +888,8 @@ int pa_decode_cascade(void *out, float *lse, const void *q, const void *k_cache,
     suf.part_stride = PT;
     suf.part_offset = P1;
     suf.table_stride = max_blocks_per_seq;
-    if (P2 >= 2 && PT <= pa::kMaxGridMerge) {
+    if (PT <= pa::kMaxGridMerge &&
+        merge_in_launch(B, 1, Hq, cache.num_kv_heads, cache.head_dim, P2, sm_count_current())) {
         int32_t *counters = reinterpret_cast<int32_t *>(
             ws + round_up(rows * PT * cache.head_dim * 4, 256) + round_up(rows * PT * 4, 256));
         rc = run_decode(true, out, lse, part_o, part_lse, q, k_cache, v_cache, cache,
