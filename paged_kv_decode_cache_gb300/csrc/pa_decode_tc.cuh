@@ -95,6 +95,9 @@ constexpr int kTcLook = 4;             // chunks a producer's block-id lookups r
 constexpr int kTcMaskRing = 8;         // chunk validity masks the K producer publishes
 
 constexpr int kTcSmemLimit = 227 * 1024;
+// room to round the dynamic shared memory base (at least 16-byte aligned) up
+// to the 1024-byte swizzle-atom boundary
+constexpr int kAlignSlack = 1024 - 16;
 
 template <int HC, int GP, bool F8 = false>
 struct TcCfg {
@@ -145,8 +148,8 @@ struct TcCfg {
     // K and V, and the V producer's mask ring)
     static constexpr int smem_for(int nk, int nv, int nbp, int gpr = GP) {
         return ((nk + nv) * kStageBytes + kQBytes + nbp * kPBufBytes + red_bytes(gpr) + 7) / 8 * 8 +
-               (2 * nk + 2 * nv + 2 * kNBS + 2 * nbp + (F8 ? 8 : 0)) * 8 +
-               kMaskRing * 8 * (F8 ? 2 : 1) + 2 * (kTcLook + 1) * 32 * 4 + 1024;
+               (2 * nk + 2 * nv + 2 * kNBS + 2 * nbp + (F8 ? 8 : 0) + 2) * 8 +
+               kMaskRing * 8 * (F8 ? 2 : 1) + 2 * (kTcLook + 1) * 32 * 4 + kAlignSlack;
     }
     // bf16: the deepest pipeline that fits: K and V stages first, then P^T buffers
     static constexpr int choice_for(int gpr) {
@@ -174,13 +177,14 @@ struct TcCfg {
     static constexpr int kPOff = kQOff + kQBytes;
     static constexpr int kRedOff = kPOff + kNBP * kPBufBytes;
     static constexpr int kBarOff = (kRedOff + kRedBytes + 7) / 8 * 8;
-    static constexpr int kNumBars = 2 * kNK + 2 * kNV + 2 * kNBS + 2 * kNBP + (F8 ? 8 : 0);
+    // (+ 2: the MMA issuers' drain barriers, committed to only by an aborting CTA)
+    static constexpr int kNumBars = 2 * kNK + 2 * kNV + 2 * kNBS + 2 * kNBP + (F8 ? 8 : 0) + 2;
     // validity masks [kMaskRing] (u64: chunk << 32 | lane mask), then the two
     // producers' block-id rings [2][kTcLook + 1][32 lanes]
     static constexpr int kMaskOff = kBarOff + kNumBars * 8;
     static constexpr int kVMaskOff = kMaskOff + kMaskRing * 8;   // FP8 only
     static constexpr int kLookOff = kVMaskOff + (F8 ? kMaskRing * 8 : 0);
-    static constexpr int kSmemBytes = kLookOff + 2 * (kTcLook + 1) * 32 * 4 + 1024;
+    static constexpr int kSmemBytes = kLookOff + 2 * (kTcLook + 1) * 32 * 4 + kAlignSlack;
     static_assert(kSmemBytes == smem_for(kNK, kNV, kNBP, kGPr), "layout");
     // the K producer rewrites mask slot c % ring only once softmax c has read it
     // (FP8: the producer runs at most NK stages, 3 chunks of converter and
@@ -271,7 +275,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     using C = TcCfg<HC, GP, F8>;
     constexpr int kThreads = C::kThreads;
     constexpr int N = C::kN, NK = C::kNK, NV = C::kNV, NBP = C::kNBP, NBS = C::kNBS;
-    extern __shared__ uint8_t smem_raw[];
+    extern __shared__ __align__(16) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
     uint8_t *kring = smem;
@@ -292,6 +296,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     uint64_t *pfree = pready + NBP;
     // FP8: operand buffer (chunk c & 1) widened into TMEM, and released by its MMAs
     uint64_t *kconv = pfree + NBP, *kopfree = kconv + 2, *vconv = kopfree + 2, *vopfree = vconv + 2;
+    // QK and PV issuers: an aborting CTA commits here, so that it frees TMEM
+    // only once every MMA it issued has completed
+    uint64_t *drain = bars + C::kNumBars - 2;
     volatile uint64_t *mask_ring = reinterpret_cast<volatile uint64_t *>(smem + C::kMaskOff);
     volatile uint64_t *vmask_ring = reinterpret_cast<volatile uint64_t *>(smem + C::kVMaskOff);
     int *look_ring = reinterpret_cast<int *>(smem + C::kLookOff);  // [2][kTcLook + 1][32]
@@ -582,6 +589,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         // the 4 softmax warps arrives on once
         for (uint64_t *bar = sdone; bar < pfree + NBP; ++bar)
             mbar_init(bar, (bar >= sfree && bar < pready + NBP) ? 4u : 1u);
+        mbar_init(&drain[0], 1u);
+        mbar_init(&drain[1], 1u);
         if (F8)  // operand buffers: "widened" by the four converter warps, "released" by a commit
             for (int i = 0; i < 2; ++i) {
                 mbar_init(&kconv[i], 4u);
@@ -652,8 +661,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                 tc5::commit(F8 ? &kopfree[c & 1] : &kempty[c % NK]);
                 done = c + 1;
             }
-            if (*abort_flag && done > 0)  // let issued MMAs finish before TMEM is freed
-                mbar_wait_bounded(&sdone[(done - 1) % NBS], ((done - 1) / NBS) & 1);
+            if (*abort_flag && done > 0) {  // let issued MMAs finish before TMEM is freed
+                tc5::commit(&drain[0]);
+                mbar_wait_bounded(&drain[0], 0);
+            }
         }
     } else if (warp == kTcPvWarp) {
         // ================= PV issuer =================
@@ -683,8 +694,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                 tc5::commit(F8 ? &vopfree[c & 1] : &vempty[c % NV]);
                 done = c + 1;
             }
-            if (*abort_flag && done > 0)
-                mbar_wait_bounded(&pfree[(done - 1) % NBP], ((done - 1) / NBP) & 1);
+            if (*abort_flag && done > 0) {
+                tc5::commit(&drain[1]);
+                mbar_wait_bounded(&drain[1], 0);
+            }
         }
     } else if (F8 && warp >= kTcCvtWarp) {
         // ================= FP8 converters: widen each chunk's e4m3 codes into TMEM =================

@@ -66,7 +66,9 @@ constexpr int kPfQOff = kPfVOff + kPfNV * kPfStage;
 constexpr int kPfPOff = kPfQOff + 2 * kPfQHalf;
 constexpr int kPfRowsOff = kPfPOff + kPfNP * kPfPBuf;
 constexpr int kPfBarOff = kPfRowsOff + kPrefillMaxTiles * 4;
-constexpr int kPfNumBars = 2 * kPfNK + 2 * kPfNV + 2 * kPfNS + 2 * kPfNP;
+// (+ 2: one per MMA issuer that an aborting CTA commits to, so that it frees
+// TMEM only after every MMA it issued has completed)
+constexpr int kPfNumBars = 2 * kPfNK + 2 * kPfNV + 2 * kPfNS + 2 * kPfNP + 2;
 constexpr int kPfXOff = kPfBarOff + kPfNumBars * 8;   // group 1's row maxima and sums [2][128]
 constexpr int kPfMiscOff = kPfXOff + 2 * kPfRows * 4;
 constexpr int kPfSmemBytes = kPfMiscOff + 16 + 1024;   // + room to align the base to 1024
@@ -93,6 +95,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     uint64_t *kfull = bars, *kempty = kfull + kPfNK, *vfull = kempty + kPfNK, *vempty = vfull + kPfNV;
     uint64_t *sdone = vempty + kPfNV, *sfree = sdone + kPfNS, *pready = sfree + kPfNS;
     uint64_t *pfree = pready + kPfNP;
+    uint64_t *drain = pfree + kPfNP;  // [2]: QK issuer, PV issuer (abort only)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kPfMiscOff);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kPfMiscOff + 4);
 
@@ -182,6 +185,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             mbar_init(&pready[i], 4u);  // ... and publish P buffer i
             mbar_init(&pfree[i], 1u);
         }
+        mbar_init(&drain[0], 1u);
+        mbar_init(&drain[1], 1u);
         *abort_flag = 0;
     }
     if (lane == 0 && warp == kPfTmaKWarp) prefetch_tensormap(&kmap);
@@ -250,8 +255,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 tc5::commit(&kempty[c % kPfNK]);
                 done = c + 1;
             }
-            if (*abort_flag && done > 0)  // let issued MMAs finish before TMEM is freed
-                mbar_wait_bounded(&sdone[(done - 1) % kPfNS], ((done - 1) / kPfNS) & 1);
+            if (*abort_flag && done > 0) {  // let issued MMAs finish before TMEM is freed
+                tc5::commit(&drain[0]);
+                mbar_wait_bounded(&drain[0], 0);
+            }
         }
     } else if (warp == kPfPvWarp) {
         // ================= PV issuer =================
@@ -277,8 +284,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 tc5::commit(&vempty[c % kPfNV]);
                 done = c + 1;
             }
-            if (*abort_flag && done > 0)
-                mbar_wait_bounded(&pfree[(done - 1) % kPfNP], ((done - 1) / kPfNP) & 1);
+            if (*abort_flag && done > 0) {
+                tc5::commit(&drain[1]);
+                mbar_wait_bounded(&drain[1], 0);
+            }
         }
     } else {
         // ================= softmax groups: group grp = warp / 4, thread = query row r =================
