@@ -453,7 +453,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         }
         if (p.split)
             merge_split_group<D, kThreads / 32>(p, b * gridDim.y + blockIdx.y, part, row0, HC * Gq,
-                                                  HC * G, Hq, ticket, tid, [] { __syncthreads(); });
+                                                  HC * G, Hq, ticket, tid, [] { __syncthreads(); },
+                                                  reinterpret_cast<float *>(ps));
         return;
     }
 
@@ -1100,7 +1101,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         merge_cluster<D, kThreads>(p, reinterpret_cast<const float *>(ps), col, rel_s, N, row0, tid);
     else if (p.split)  // all eight warps share the merge
         merge_split_group<D, kThreads / 32>(p, b * gridDim.y + blockIdx.y, part, row0, HC * Gq,
-                                              HC * G, Hq, ticket, tid, [] { __syncthreads(); });
+                                              HC * G, Hq, ticket, tid, [] { __syncthreads(); },
+                                              reinterpret_cast<float *>(ps));
 }
 
 template <int HC, int GP, bool F8>

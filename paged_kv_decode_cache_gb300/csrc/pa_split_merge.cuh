@@ -9,12 +9,15 @@
 //   2. the CTA whose arrival makes P resets the counter to zero at once; the
 //      others wait (bounded) until it reads P or drops to at most their own
 //      arrival value (the reset): every partial exists;
-//   3. the group's CTAs split the merge between them: merge task k = (output
-//      row, dim slice) goes to warp k of the group's P x nwarps warps; a task
-//      computes the row's log-sum-exp over the P partial LSEs and sums the
-//      weighted partial outputs of its slice (partials are read with
-//      L1-bypassing loads).  Up to 32 partitions a lane owns a dim of a 32-dim
-//      slice; beyond, a lane owns partitions of an 8-dim slice;
+//   3. the group's CTAs split the merge between them: a merge task (output
+//      row, dim slice) computes the row's log-sum-exp over the P partial LSEs
+//      and sums the weighted partial outputs of its slice (partials are read
+//      with L1-bypassing loads).  Up to 32 partitions task k goes to warp k of
+//      the group's P x nwarps warps, a lane owning a dim of a 32-dim slice;
+//      beyond, a task goes to ceil(P / 32) warps of one CTA, each taking 32
+//      partitions with its lanes over a 32-dim slice, and their sums meet in
+//      shared memory (the CUDA-core kernel: one warp, a lane owning
+//      partitions of an 8-dim slice);
 // A wait that runs out sets PA_STATUS_TIMEOUT and the CTA skips the merge.
 // A task merges all part_stride partials of its row: part_stride = P for an
 // ordinary call; a cascade's suffix pass (P CTAs per group) also merges the
@@ -169,6 +172,74 @@ __device__ __forceinline__ void merge_slice_wide(const DecodeParams &p, int64_t 
     }
 }
 
+// Merge for many partitions with a shared-memory scratch: a task (output
+// row, 32-dim slice) goes to nb = ceil(part_stride / 32) warps of one CTA,
+// which merges kWarps / nb tasks at once; warp j of a task takes partitions
+// 32j .. 32j + 31 with its lanes over the slice's dims, so every partial read
+// is one whole 128-byte line.  Each warp loads all the row's LSEs and its 32
+// partial lines at once (one round trip), computes the row's log-sum-exp
+// itself and sums its weighted lines; the task's warps then add their sums
+// in `scratch` (kWarps x 32 floats), in partition-block order.  The CTA's
+// loop runs the same number of rounds in every thread (`sync` is a CTA
+// barrier).  Needs nb <= kWarps.
+template <int D, int kWarps, typename RowOf, typename Sync>
+__device__ void merge_tasks_cta(const DecodeParams &p, RowOf row_of, int nrows, int part,
+                                float *scratch, int t, Sync sync) {
+    constexpr int kBlocks = kMaxGridMerge / 32;  // partition blocks of 32 at most
+    const int PS = p.part_stride;
+    const int nb = (PS + 31) / 32;
+    const int per = kWarps / nb;                  // tasks one CTA merges at once
+    const int warp = t >> 5, lane = t & 31, slot = warp / nb, blk = warp % nb;
+    const int tasks = nrows * (D / 32);
+    for (int base = part * per; base < tasks; base += p.num_splits * per) {
+        const int k = base + slot;
+        const bool active = slot < per && k < tasks;
+        int64_t row = 0;
+        int slice = 0;
+        if (active) {
+            row = row_of(k / (D / 32));
+            slice = k % (D / 32);
+            const float *pl = p.part_lse + row * PS;
+            const float *po = p.part_o + (row * PS + 32 * blk) * D + slice * 32 + lane;
+            float lv[kBlocks], ov[32];
+#pragma unroll
+            for (int i = 0; i < kBlocks; ++i) lv[i] = lane + 32 * i < PS ? __ldcg(pl + lane + 32 * i) : -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) ov[j] = 32 * blk + j < PS ? __ldcg(po + static_cast<int64_t>(j) * D) : 0.f;
+            float M = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < kBlocks; ++i) M = fmaxf(M, lv[i]);
+#pragma unroll
+            for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+            float total = -INFINITY, acc = 0.f;
+            if (M != -INFINITY) {
+                float z = 0.f;
+#pragma unroll
+                for (int i = 0; i < kBlocks; ++i) z += (lv[i] == -INFINITY) ? 0.f : expf(lv[i] - M);
+#pragma unroll
+                for (int off = 16; off; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+                total = M + logf(z);
+                float mine = lv[0];  // the LSE of partition 32 * blk + lane
+#pragma unroll
+                for (int i = 1; i < kBlocks; ++i)
+                    if (i == blk) mine = lv[i];
+                const float wl = (mine == -INFINITY) ? 0.f : expf(mine - total);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) acc = fmaf(__shfl_sync(0xffffffffu, wl, j), ov[j], acc);
+            }
+            scratch[warp * 32 + lane] = acc;
+            if (blk == 0 && slice == 0 && lane == 0 && p.lse) p.lse[row] = total;
+        }
+        sync();
+        if (active && blk == 0) {
+            float o = 0.f;
+            for (int j = 0; j < nb; ++j) o += scratch[(warp + j) * 32 + lane];
+            static_cast<__nv_bfloat16 *>(p.out)[row * D + slice * 32 + lane] = __float2bfloat16_rn(o);
+        }
+        sync();
+    }
+}
+
 // Called by all 32 x kWarps threads (index t) of a CTA after its partials for
 // its nrows rows are written: row j is row_first + (j / per_block) * stride +
 // j % per_block (blocks of consecutive rows, e.g. one per query position).
@@ -179,7 +250,7 @@ __device__ __forceinline__ void merge_slice_wide(const DecodeParams &p, int64_t 
 template <int D, int kWarps, typename Sync>
 __device__ void merge_split_group(const DecodeParams &p, int group, int part, int64_t row_first,
                                   int nrows, int per_block, int64_t stride, int *flag, int t,
-                                  Sync sync) {
+                                  Sync sync, float *scratch = nullptr) {
     auto row_of = [&](int j) -> int64_t { return row_first + (j / per_block) * stride + j % per_block; };
     if (!p.counters) return;
     int *arrive = p.counters + 2 * group;  // (the pair's second int is not used)
@@ -221,6 +292,8 @@ __device__ void merge_split_group(const DecodeParams &p, int group, int part, in
             const int tasks = nrows * (D / 32);
             for (int k = part * kWarps + warp; k < tasks; k += P * kWarps)
                 merge_slice<D>(p, row_of(k / (D / 32)), k % (D / 32), lane);
+        } else if (scratch && (p.part_stride + 31) / 32 <= kWarps) {  // warps over partitions
+            merge_tasks_cta<D, kWarps>(p, row_of, nrows, part, scratch, t, sync);
         } else {        // lanes over partitions: one round trip per 8-dim slice
             const int tasks = nrows * (D / 8);
             for (int k = part * kWarps + warp; k < tasks; k += P * kWarps)
