@@ -128,7 +128,8 @@ def test_partials_match_oracle_partials(P, kernel, use_kernel):
     assert_lse_close(pl.cpu().double().numpy(), rl, "partial lse")
 
 
-@pytest.mark.parametrize("lens,P", [((1500,), 33), ((1500,), 100), ((1500,), 150), ((700, 1500), 60)])
+@pytest.mark.parametrize("lens,P", [((1500,), 33), ((1500,), 100), ((1500,), 150), ((700, 1500), 60),
+                                    ((2100,), 64), ((2100,), 65), ((2100,), 128)])
 def test_fused_merge_many_partitions(lens, P, use_kernel):
     """More than 32 partitions per row (the merge's partition-parallel tasks),
     some of them empty past the sequence end; few sequences, so the cooperative
@@ -627,6 +628,29 @@ def test_fp8_decode_small_elementwise(case):
                                  status=dev.status)
         assert_close(bf16_dev_to_f64(out), ref, f"fp8 P={Pu}")
         assert_lse_close(lse.cpu().double().numpy(), ref_lse, f"fp8 P={Pu}")
+    assert dev.status_value() == 0
+
+
+@pytest.mark.parametrize("P", [33, 64, 100, 140])
+def test_fp8_merge_many_partitions(P):
+    """FP8 pools with more than 32 partitions per row: the sixteen-warp CTAs
+    share each merge task between ceil(P / 32) warps and several tasks at once."""
+    lens = (2390,)  # one sequence: every partition's CTA is resident at once
+    w = W.with_fp8_pools(W.make_workload("f8m", B=1, Hq=28, Hkv=4, D=128, block_size=16,
+                                         seq_lens=list(lens), num_blocks=160, seed=P,
+                                         write_new=False))
+    ref, ref_lse = oracle.decode_fp8(w.q, w.k_cache8, w.v_cache8, w.block_tables, w.seq_lens,
+                                     w.scale, w.k_scale, w.v_scale)
+    dev = Dev(w)
+    kc, vc = _fp8_dev(w)
+    ws = torch.zeros(max(1, pa.pa_splitkv_workspace_bytes(w.B, w.Hq, w.D, P)), dtype=torch.uint8,
+                     device="cuda")
+    out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device="cuda")
+    pa.pa_decode_splitkv_fp8(out, lse, dev.q, kc, vc, w.k_scale, w.v_scale, dev.block_tables,
+                             dev.seq_lens, w.scale, num_splits=P, workspace=ws, status=dev.status)
+    assert_close(bf16_dev_to_f64(out), ref, f"fp8 P={P}")
+    assert_lse_close(lse.cpu().double().numpy(), ref_lse, f"fp8 P={P}")
     assert dev.status_value() == 0
 
 
