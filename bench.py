@@ -531,8 +531,12 @@ def run_ours(args, world, rank, local):
     # A step's inputs (q, block tables, lengths, new K/V, slots) are staged in one
     # pinned host buffer with a device twin of the same layout, whose slices are
     # the tensors handed to the API; the result (out, lse) comes back the same
-    # way: one host->device and one device->host copy per step.  Steps are
-    # replayed from CUDA graphs, as a serving loop runs its decode step.
+    # way: one host->device and one device->host copy per step.  As a serving
+    # loop double-buffers its staging, step k uses device and host twins k % 2
+    # and its copies run on their own streams: its inputs go up while step
+    # k - 1 decodes, its result comes down while step k + 1 decodes.  Every
+    # step's two copies are inside the timed region, which ends once the last
+    # result is on the host.  Steps are replayed from CUDA graphs.
     def packed(arrays):
         offs, n = [], 0
         for a in arrays:
@@ -546,58 +550,89 @@ def run_ours(args, world, rank, local):
     hv = h_in.numpy()
     for a, o in zip(ins, in_offs):
         hv[o:o + a.nbytes] = a.view(np.uint8).ravel()
-    d_in = torch.empty(in_bytes, dtype=torch.uint8, device=dev)
     def dview(buf, off, a, dtype):
         return buf[off:off + a.nbytes].view(dtype).view(a.shape)
-    q_e = dview(d_in, in_offs[0], ins[0], torch.bfloat16)
-    bt_e = dview(d_in, in_offs[1], ins[1], torch.int32)
-    sl_e = dview(d_in, in_offs[2], ins[2], torch.int32)
-    kn_e = dview(d_in, in_offs[3], ins[3], torch.bfloat16)
-    vn_e = dview(d_in, in_offs[4], ins[4], torch.bfloat16)
-    slots_e = dview(d_in, in_offs[5], ins[5], torch.int64)
     o_proto = np.zeros(oshape, np.uint16)
     l_proto = np.zeros(oshape[:-1], np.float32)
     out_offs, out_bytes = packed([o_proto, l_proto])
-    d_out = torch.zeros(out_bytes, dtype=torch.uint8, device=dev)
-    h_out = torch.zeros(out_bytes, dtype=torch.uint8).pin_memory()
-    out_e = dview(d_out, out_offs[0], o_proto, torch.bfloat16)
-    lse_e = dview(d_out, out_offs[1], l_proto, torch.float32)
+    d_ins = [torch.empty(in_bytes, dtype=torch.uint8, device=dev) for _ in range(2)]
+    d_outs = [torch.zeros(out_bytes, dtype=torch.uint8, device=dev) for _ in range(2)]
+    h_outs = [torch.zeros(out_bytes, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    views = []
+    for d_in, d_out in zip(d_ins, d_outs):
+        views.append(dict(q=dview(d_in, in_offs[0], ins[0], torch.bfloat16),
+                          bt=dview(d_in, in_offs[1], ins[1], torch.int32),
+                          sl=dview(d_in, in_offs[2], ins[2], torch.int32),
+                          kn=dview(d_in, in_offs[3], ins[3], torch.bfloat16),
+                          vn=dview(d_in, in_offs[4], ins[4], torch.bfloat16),
+                          slots=dview(d_in, in_offs[5], ins[5], torch.int64),
+                          out=dview(d_out, out_offs[0], o_proto, torch.bfloat16),
+                          lse=dview(d_out, out_offs[1], l_proto, torch.float32)))
     h2d, d2h = in_bytes, out_bytes
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev_ready = [torch.cuda.Event() for _ in range(2)]  # inputs k up, result k - 2 down
+    ev_dec = [torch.cuda.Event() for _ in range(2)]    # step k has run
+    ev_out = [torch.cuda.Event() for _ in range(2)]    # result k is on the host
 
-    def e2e_step(r):
+    def e2e_decode(v, r):
         kc, vc = pools[r]
-        d_in.copy_(h_in, non_blocking=True)
         if cascade:
-            pa.pa_cache_write(kn_e, vn_e, slots_e, kc, vc, stream=stream)
-            pa.pa_decode_cascade(out_e, lse_e, q_e, kc, vc, w.cascade_blocks, bt_e, sl_e, w.scale,
-                                 workspace=ws, stream=stream)
+            pa.pa_cache_write(v["kn"], v["vn"], v["slots"], kc, vc, stream=stream)
+            pa.pa_decode_cascade(v["out"], v["lse"], v["q"], kc, vc, w.cascade_blocks, v["bt"], v["sl"],
+                                 w.scale, workspace=ws, stream=stream)
         elif fp8 and args.unfused:
-            pa.pa_cache_write_fp8(kn_e, vn_e, slots_e, kc, vc, w.k_scale, w.v_scale, stream=stream)
-            pa.pa_decode_splitkv_fp8(out_e, lse_e, q_e, kc, vc, w.k_scale, w.v_scale, bt_e, sl_e,
-                                     w.scale, num_splits=P, workspace=ws, stream=stream)
+            pa.pa_cache_write_fp8(v["kn"], v["vn"], v["slots"], kc, vc, w.k_scale, w.v_scale, stream=stream)
+            pa.pa_decode_splitkv_fp8(v["out"], v["lse"], v["q"], kc, vc, w.k_scale, w.v_scale, v["bt"],
+                                     v["sl"], w.scale, num_splits=P, workspace=ws, stream=stream)
         elif fp8:
-            pa.pa_decode_step_fp8(out_e, lse_e, q_e, kn_e, vn_e, slots_e, kc, vc, w.k_scale,
-                                  w.v_scale, bt_e, sl_e, w.scale, num_splits=P, workspace=ws,
-                                  stream=stream)
+            pa.pa_decode_step_fp8(v["out"], v["lse"], v["q"], v["kn"], v["vn"], v["slots"], kc, vc,
+                                  w.k_scale, w.v_scale, v["bt"], v["sl"], w.scale, num_splits=P,
+                                  workspace=ws, stream=stream)
         elif mq:
-            pa.pa_cache_write(kn_e, vn_e, slots_e, kc, vc, stream=stream)
-            pa.pa_decode_mq(out_e, lse_e, q_e, kc, vc, bt_e, sl_e, w.scale, num_splits=P,
+            pa.pa_cache_write(v["kn"], v["vn"], v["slots"], kc, vc, stream=stream)
+            pa.pa_decode_mq(v["out"], v["lse"], v["q"], kc, vc, v["bt"], v["sl"], w.scale, num_splits=P,
                             workspace=ws, stream=stream)
         else:
-            pa.pa_decode_step(out_e, lse_e, q_e, kn_e, vn_e, slots_e, kc, vc, bt_e, sl_e, w.scale,
-                              num_splits=P, workspace=ws, stream=stream)
-        h_out.copy_(d_out, non_blocking=True)
+            pa.pa_decode_step(v["out"], v["lse"], v["q"], v["kn"], v["vn"], v["slots"], kc, vc, v["bt"],
+                              v["sl"], w.scale, num_splits=P, workspace=ws, stream=stream)
 
-    with torch.cuda.stream(stream):
-        for r in range(R):  # eager warm-up of every replica before capture
-            e2e_step(r)
+    def e2e_steps_on(n, rot0):
+        """n pipelined steps issued from `stream`, forked to the two copy streams
+        and joined back.  Step k's upload waits for step k - 2 (whose input
+        buffer it reuses), and its "ready" event also covers the download of
+        step k - 2's result (whose output buffer step k reuses), so a step
+        waits on one event; uploads and downloads use separate queues."""
+        fork = torch.cuda.Event()
+        fork.record(stream)
+        s_in.wait_event(fork)
+        s_out.wait_event(fork)
+        for k in range(n):
+            i = k % 2
+            with torch.cuda.stream(s_in):
+                if k >= 2:
+                    s_in.wait_event(ev_dec[i])
+                d_ins[i].copy_(h_in, non_blocking=True)          # inputs k
+                if k >= 2:
+                    s_in.wait_event(ev_out[i])
+                ev_ready[i].record(s_in)
+            stream.wait_event(ev_ready[i])
+            e2e_decode(views[i], (rot0 + k) % R)
+            ev_dec[i].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_dec[i])
+                h_outs[i].copy_(d_outs[i], non_blocking=True)    # result k
+                ev_out[i].record(s_out)
+        for i in range(min(2, n)):
+            stream.wait_event(ev_out[i])
+
+    with torch.cuda.stream(stream):  # eager warm-up of every replica before capture
+        e2e_steps_on(max(R, 2), 0)
     stream.synchronize()
     e2e_graphs = []
     for _ in range(2):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            for k in range(S):
-                e2e_step(k % R)
+            e2e_steps_on(S, 0)
         e2e_graphs.append(g)
     n_e2e = max(1, e2e_steps // S)
     with torch.cuda.stream(stream):
@@ -615,9 +650,10 @@ def run_ours(args, world, rank, local):
         a1.record(stream)
     a1.synchronize()
     e2e_ms = max_over_ranks(a0.elapsed_time(a1), world) / (n_e2e * S)
-    # the staged result is the library's output
-    assert np.array_equal(h_out.numpy()[out_offs[0]:out_offs[0] + o_proto.nbytes],
-                          d_out[out_offs[0]:out_offs[0] + o_proto.nbytes].cpu().numpy())
+    # the staged results are the library's output
+    last = (S - 1) % 2
+    assert np.array_equal(h_outs[last].numpy()[out_offs[0]:out_offs[0] + o_proto.nbytes],
+                          d_outs[last][out_offs[0]:out_offs[0] + o_proto.nbytes].cpu().numpy())
     e2e_value = step_bytes * world / (e2e_ms * 1e-3) / 1e12
 
     peak, peak_kind = measured_peak_gbs()
