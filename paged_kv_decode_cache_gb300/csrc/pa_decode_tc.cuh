@@ -310,14 +310,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     // it (it then waits in turn).
     //
     // Meanwhile the PV issuer's warp (idle until the first P) warms L2 with
-    // this CTA's first 3 chunks of K and V, so that those copies are served
-    // from L2 once the wait is over (the 7B layer's step: 18.0 -> 16.6 us,
-    // 18.5 -> 17.6 us with FP8 pools; deeper warm-ups were slower).  The
+    // this CTA's first 2 chunks of K and V (4 of codes with FP8 pools), so
+    // that those copies are served from L2 once the wait is over (the 7B
+    // layer's step: 18.0 -> 16.6 us, 18.5 -> 17.6 us with FP8 pools; one
+    // chunk more or less was slower for either).  The
     // length and block ids it reads may still be the previous kernel's to
     // write: they only pick which boxes to warm (an id outside the pool warms
     // nothing), and every load after the wait reads the current values.
     if (threadIdx.x >= 32 * kTcPvWarp && threadIdx.x < 32 * (kTcPvWarp + 1)) {
-        constexpr int kPre = 3;  // chunks
+        constexpr int kPre = F8 ? 4 : 2;  // chunks
         const int ln = threadIdx.x & 31;
         if (ln < kPre * C::kTiles) {
             const int c = ln / C::kTiles, tl = ln % C::kTiles;
