@@ -179,7 +179,9 @@ int pa_decode(void *out, float *lse, const void *q, const void *k_cache, const v
  * largest P for which the B * Hkv * P CTAs fit one wave of the decode kernel
  * that the group size Hq / Hkv and head_dim D select (2 CTAs per SM for the
  * CUDA-core kernel, 1 for the tensor-core kernel), capped so that every
- * partition keeps at least four 16-token tiles.  A batch with more CTAs than
+ * partition keeps at least two 16-token tiles, and at 32 partitions where
+ * partitions of four tiles would number 32 or fewer (more than 32 partitions
+ * take a costlier merge).  A batch with more CTAs than
  * one wave holds runs in waves: its sequences are split into partitions of
  * about 48 tiles (of max_blocks_per_seq * block_size tokens), which evens the
  * waves out when the lengths differ.  Host-only; depends only on its

@@ -40,7 +40,8 @@ namespace {
 constexpr int kMaxGroupCc = 8;    // query heads per KV head, CUDA-core kernel
 constexpr int kMaxGroupTc = 32;   // MMA columns per KV head (query heads x positions), tensor cores
 constexpr int kMaxGridZ = 65535;  // sequences per launch (gridDim.z)
-constexpr int kMinTilesPerSplit = 4;  // 64 tokens: fewer idle SMs at 4k tokens
+constexpr int kMinTilesPerSplit = 2;  // 32 tokens: one MMA chunk of four KV heads
+constexpr int kNarrowMergeSplits = 32;  // partitions the one-warp-per-task merge holds
 constexpr int kMultiWaveTiles = 48;   // tiles per partition of a batch that takes several waves
 constexpr int64_t kMaxRowsQ = 1 << 24;  // B x q_len of one multi-query call
 constexpr int kMaxSplits = 256;
@@ -557,6 +558,13 @@ int pa_choose_num_splits_mq(int32_t B, int32_t q_len, int32_t Hq, int32_t Hkv, i
     }
     const int64_t p_by_tiles = (tiles + kMinTilesPerSplit - 1) / kMinTilesPerSplit;
     if (P > p_by_tiles) P = p_by_tiles;
+    // Past 32 partitions the in-launch merge gives each task several warps of
+    // one CTA (about 1 us more per step); that pays only where partitions of
+    // 4 tiles would already be more than 32 (one sequence of 4k tokens:
+    // P = 128 beats 64), not where the smaller floor alone crosses the line
+    // (one sequence of 2k tokens: P = 32 beats 64).
+    const int64_t p_by_4_tiles = (tiles + 3) / 4;
+    if (P > kNarrowMergeSplits && p_by_4_tiles <= kNarrowMergeSplits) P = kNarrowMergeSplits;
     if (P > kMaxSplits) P = kMaxSplits;
     if (P < 1) P = 1;
     // the prefill-shaped kernel keeps a partition's tiles in shared memory

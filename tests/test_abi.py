@@ -93,10 +93,12 @@ def test_split_policy(lib, use_kernel, B, Hq, Hkv, D, mb, bs, sms):
     units = _units(B, Hq, Hkv, D)
     if P > 1 and units <= slots:
         assert units * P <= slots              # one wave of resident CTAs
-        assert chunk >= 16 * 4 or chunk * P >= lmax
+        assert chunk >= 16 * 2 or chunk * P >= lmax
+        tiles = (lmax + 15) // 16
+        assert P <= 32 or -(-tiles // 4) > 32  # the wider merge only where 4-tile partitions need it
     if units > slots:   # waves: partitions of about 48 tiles, without empty tails
         tiles = (lmax + 15) // 16
-        p0 = min(-(-tiles // 48), -(-tiles // 4))
+        p0 = min(-(-tiles // 48), -(-tiles // 2))
         assert P == -(-lmax // pa.pa_partition_tokens(mb, bs, max(1, p0)))
 
 
@@ -120,6 +122,16 @@ def test_decode_launches(lib, use_kernel):
     assert L(0, 1, 28, 4, 128, 256, 16, 0, 148) == 0
     assert lib.pa_decode_launches(8, 1, 28, 5, 128, 256, 16, 0, 148) == pa.PA_EINVAL
     assert lib.pa_decode_launches(8, 1, 28, 4, 128, 256, 16, 0, 0) == pa.PA_EINVAL
+
+
+def test_split_policy_short_contexts(lib, use_kernel):
+    use_kernel("auto")
+    # the 7B layer at 256 tokens: partitions of 2 tiles (8 per sequence, 64 CTAs)
+    assert pa.pa_choose_num_splits(8, 28, 4, 128, 16, 16, 152) == 8
+    # one 2k-token sequence: 32 partitions of 4 tiles, not 64 of 2 (the wider merge)
+    assert pa.pa_choose_num_splits(1, 12, 2, 128, 128, 16, 152) == 32
+    # one 4k-token sequence: 4-tile partitions would already be 64, so 2-tile ones
+    assert pa.pa_choose_num_splits(1, 28, 4, 128, 256, 16, 152) == 128
 
 
 def test_split_policy_fills_small_batches(lib, use_kernel):
