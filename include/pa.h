@@ -378,7 +378,7 @@ int pa_decode_mq(void *out, float *lse, const void *q, int32_t q_len, const void
  * log-sum-exp combine of them.  It pays when attending the prefix once per
  * sequence would cost more than that: with PA_OPT_CASCADE at
  * PA_CASCADE_AUTO the call runs the cascade when (B - 1) x the prefix's K/V
- * bytes reach 1 GiB, and pa_decode_splitkv otherwise (the same result).  Requires seq_lens[b] >= n_prefix_blocks *
+ * bytes reach 256 MiB, and pa_decode_splitkv otherwise (the same result).  Requires seq_lens[b] >= n_prefix_blocks *
  * block_size (a shorter sequence sets PA_STATUS_BAD_SEQLEN and its result is
  * undefined); 0 <= n_prefix_blocks < max_blocks_per_seq (0: plain
  * pa_decode_splitkv).  The library reads the prefix's block ids from table

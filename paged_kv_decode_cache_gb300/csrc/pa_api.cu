@@ -810,16 +810,17 @@ static int cascade_splits(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t
 // the same blocks at about the same time, even for a prefix larger than L2),
 // so what they cost is L2 traffic and the SMs' work on the extra rows, against
 // the cascade's extra launch and merge.  Calibrated on this GPU: the cascade
-// pays once the extra reads reach 1 GiB (256 sequences behind a 2048-token
-// prefix of 8 KV heads, 2.1 GB: 3.4x faster; plain decode is faster for 4
-// sequences behind 65536 tokens, 805 MB, for 8 behind 16384, 470 MB, and for
-// 256 behind 8 blocks, 134 MB).
+// pays once the extra reads reach 256 MiB (256 sequences behind a 2048-token
+// prefix of 8 KV heads, 2.1 GB: 3.4x faster; 4 sequences behind 65536
+// tokens, 805 MB: 68.4 against 76.4 us; 8 behind 16384, 470 MB: 36.3
+// against 44.2 us; plain decode is faster for 256 behind 8 blocks, 134 MB:
+// 162.4 against 171.4 us).
 static bool cascade_pays(int32_t B, int32_t Hkv, int32_t D, int32_t n_prefix_blocks,
                          int32_t block_size) {
     const int mode = option(PA_OPT_CASCADE);
     if (mode != PA_CASCADE_AUTO) return mode == PA_CASCADE_ALWAYS;
     const double prefix_bytes = static_cast<double>(n_prefix_blocks) * block_size * Hkv * D * 2 * 2;
-    return (B - 1) * prefix_bytes >= 1024.0 * (1 << 20);
+    return (B - 1) * prefix_bytes >= 256.0 * (1 << 20);
 }
 
 int pa_cascade_pays(int32_t B, int32_t Hkv, int32_t D, int32_t n_prefix_blocks, int32_t block_size) {

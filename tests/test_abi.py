@@ -404,14 +404,16 @@ def test_mq_split_policy_prefill_shape(lib, use_kernel):
 
 def test_cascade_runs_where_it_pays(lib, cascade_mode):
     """The automatic choice: the cascade when (B - 1) x the prefix's K/V bytes
-    reach 1 GiB; the switch forces either path."""
+    reach 256 MiB; the switch forces either path."""
     cascade_mode("auto")
     assert not pa.pa_cascade_pays(256, 8, 128, 8, 16)      # 8 blocks: 255 x 512 KiB = 128 MiB
     assert pa.pa_cascade_pays(256, 8, 128, 128, 16)        # 2048 tokens: 255 x 8 MiB
-    assert not pa.pa_cascade_pays(8, 8, 128, 1024, 16)     # 16384 tokens: 7 x 64 MiB
-    assert not pa.pa_cascade_pays(4, 8, 128, 4096, 16)     # 65536 tokens: 3 x 256 MiB
+    assert pa.pa_cascade_pays(8, 8, 128, 1024, 16)         # 16384 tokens: 7 x 64 MiB
+    assert pa.pa_cascade_pays(4, 8, 128, 4096, 16)         # 65536 tokens: 3 x 256 MiB
+    assert not pa.pa_cascade_pays(2, 8, 128, 1024, 16)     # 16384 tokens read once more: 64 MiB
     assert not pa.pa_cascade_pays(1, 8, 128, 4096, 16)     # one sequence: nothing to share
     assert pa.pa_cascade_pays(9, 8, 128, 2048, 16)         # a 128 MiB prefix read 8 more times
+    assert pa.pa_cascade_pays(3, 8, 128, 2048, 16)         # ... or 2 more times
     assert not pa.pa_cascade_pays(256, 8, 128, 0, 16)
     assert lib.pa_cascade_pays(0, 8, 128, 8, 16) == pa.PA_EINVAL
     cascade_mode("always")

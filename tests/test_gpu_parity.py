@@ -819,8 +819,8 @@ def test_cascade_full_size_qwen3(mode, cascade_mode):
 
 
 @pytest.mark.parametrize("name,npre,pays", [("qwen3-0.6b-B256-prefix2048", 128, True),
-                                            ("qwen3-0.6b-B8-prefix16384", 1024, False),
-                                            ("qwen3-0.6b-B4-prefix65536", 4096, False)])
+                                            ("qwen3-0.6b-B8-prefix16384", 1024, True),
+                                            ("qwen3-0.6b-B4-prefix65536", 4096, True)])
 @pytest.mark.parametrize("cascade", [True, False])
 def test_long_shared_prefix_full_size(name, npre, pays, cascade, cascade_mode):
     """Qwen3-shaped sequences behind one long shared prefix (256 behind 2048
