@@ -390,15 +390,11 @@ def run_ours(args, world, rank, local):
     cascade_runs = cascade and pa.pa_cascade_pays(w.B, w.Hkv, w.D, w.cascade_blocks, w.block_size)
     cascade_kernels = 0   # kernel launches of the cascade proper
     if cascade_runs:
-        # the library's partition counts of the two passes: a split suffix pass merges all
-        # P1 + P2 partials itself when a merge task can hold them (else a combine follows)
+        # prefix pass, suffix pass and, unless the suffix launch merges both passes'
+        # partials, the combine: the library's own count
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
-        p1 = pa.pa_choose_num_splits_mq(1, w.B, w.Hq, w.Hkv, w.D, w.cascade_blocks, w.block_size, sms)
-        p2 = pa.pa_choose_num_splits(w.B, w.Hq, w.Hkv, w.D, w.max_blocks - w.cascade_blocks,
-                                     w.block_size, sms)
-        suffix_merges = pa.pa_decode_launches(w.B, 1, w.Hq, w.Hkv, w.D, w.max_blocks - w.cascade_blocks,
-                                              w.block_size, p2, sms) == 1
-        cascade_kernels = 2 if p2 >= 2 and suffix_merges and p1 + p2 <= 256 else 3
+        cascade_kernels = pa.pa_cascade_launches(w.B, w.Hq, w.Hkv, w.D, w.cascade_blocks, w.max_blocks,
+                                                 w.block_size, sms)
     ws_bytes = (pa.pa_cascade_workspace_bytes(w.B, w.Hq, w.Hkv, w.D, w.cascade_blocks, w.max_blocks,
                                               w.block_size) if cascade
                 else pa.pa_splitkv_workspace_bytes(w.B * w.q_len, w.Hq, w.D, P))

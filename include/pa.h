@@ -398,6 +398,15 @@ int pa_decode_cascade(void *out, float *lse, const void *q, const void *k_cache,
  * arguments.  Host-only. */
 int pa_cascade_pays(int32_t B, int32_t Hkv, int32_t D, int32_t n_prefix_blocks, int32_t block_size);
 
+/* Kernel launches pa_decode_cascade makes for this shape on sm_count SMs
+ * under the current PA_OPT_CASCADE switch: 2 or 3 when it runs the cascade
+ * (prefix pass, suffix pass, and the combine unless the suffix launch merges
+ * both passes' partials), else pa_decode_launches of the plain split decode
+ * with the automatic P.  0 for B = 0; PA_EINVAL on bad arguments.
+ * Host-only. */
+int pa_cascade_launches(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t n_prefix_blocks,
+                        int32_t max_blocks_per_seq, int32_t block_size, int32_t sm_count);
+
 /* Workspace bytes pa_decode_cascade needs on the current device (0 on bad arguments). */
 size_t pa_cascade_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
                                   int32_t n_prefix_blocks, int32_t max_blocks_per_seq,

@@ -793,15 +793,27 @@ int pa_decode_splitkv_fp8(void *out, float *lse, const void *q, const void *k_ca
 
 // Cascade decode: partition counts of the prefix pass (all B sequences' queries
 // as one multi-query call over the shared blocks) and of the suffix pass.
-static int cascade_splits(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t n_prefix_blocks,
-                          int32_t max_blocks_per_seq, int32_t block_size, int *P1, int *P2) {
-    const int sms = sm_count_current();
-    if (sms <= 0) return PA_ECUDA;
+static int cascade_splits_on(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t n_prefix_blocks,
+                             int32_t max_blocks_per_seq, int32_t block_size, int sms, int *P1, int *P2) {
     *P1 = pa_choose_num_splits_mq(1, B, Hq, Hkv, D, n_prefix_blocks, block_size, sms);
     if (*P1 < 0) return *P1;
     *P2 = pa_choose_num_splits(B, Hq, Hkv, D, max_blocks_per_seq - n_prefix_blocks, block_size, sms);
     if (*P2 < 0) return *P2;
     return PA_OK;
+}
+
+static int cascade_splits(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t n_prefix_blocks,
+                          int32_t max_blocks_per_seq, int32_t block_size, int *P1, int *P2) {
+    const int sms = sm_count_current();
+    if (sms <= 0) return PA_ECUDA;
+    return cascade_splits_on(B, Hq, Hkv, D, n_prefix_blocks, max_blocks_per_seq, block_size, sms, P1,
+                             P2);
+}
+
+// Whether the cascade's suffix pass (P2 partitions) merges the P1 + P2
+// partials of its rows in its own launch.
+static bool cascade_suffix_merges(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int P1, int P2, int sms) {
+    return P1 + P2 <= pa::kMaxGridMerge && merge_in_launch(B, 1, Hq, Hkv, D, P2, sms);
 }
 
 // Does attending the shared prefix once for the whole batch pay?  Without the
@@ -821,6 +833,21 @@ static bool cascade_pays(int32_t B, int32_t Hkv, int32_t D, int32_t n_prefix_blo
     if (mode != PA_CASCADE_AUTO) return mode == PA_CASCADE_ALWAYS;
     const double prefix_bytes = static_cast<double>(n_prefix_blocks) * block_size * Hkv * D * 2 * 2;
     return (B - 1) * prefix_bytes >= 256.0 * (1 << 20);
+}
+
+int pa_cascade_launches(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t n_prefix_blocks,
+                        int32_t max_blocks_per_seq, int32_t block_size, int32_t sm_count) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || n_prefix_blocks < 0 ||
+        n_prefix_blocks >= max_blocks_per_seq || block_size <= 0 || sm_count <= 0)
+        return PA_EINVAL;
+    if (B == 0) return 0;
+    if (n_prefix_blocks == 0 || !cascade_pays(B, Hkv, D, n_prefix_blocks, block_size))
+        return pa_decode_launches(B, 1, Hq, Hkv, D, max_blocks_per_seq, block_size, 0, sm_count);
+    int P1 = 0, P2 = 0;
+    const int rc = cascade_splits_on(B, Hq, Hkv, D, n_prefix_blocks, max_blocks_per_seq, block_size,
+                                     sm_count, &P1, &P2);
+    if (rc) return rc;
+    return cascade_suffix_merges(B, Hq, Hkv, D, P1, P2, sm_count) ? 2 : 3;
 }
 
 int pa_cascade_pays(int32_t B, int32_t Hkv, int32_t D, int32_t n_prefix_blocks, int32_t block_size) {
@@ -897,8 +924,7 @@ int pa_decode_cascade(void *out, float *lse, const void *q, const void *k_cache,
     suf.part_stride = PT;
     suf.part_offset = P1;
     suf.table_stride = max_blocks_per_seq;
-    if (PT <= pa::kMaxGridMerge &&
-        merge_in_launch(B, 1, Hq, cache.num_kv_heads, cache.head_dim, P2, sm_count_current())) {
+    if (cascade_suffix_merges(B, Hq, cache.num_kv_heads, cache.head_dim, P1, P2, sm_count_current())) {
         int32_t *counters = reinterpret_cast<int32_t *>(
             ws + round_up(rows * PT * cache.head_dim * 4, 256) + round_up(rows * PT * 4, 256));
         rc = run_decode(true, out, lse, part_o, part_lse, q, k_cache, v_cache, cache,

@@ -72,6 +72,7 @@ _SIGNATURES = {
                            _SZ, _P, _P], ctypes.c_int),
     "pa_cascade_workspace_bytes": ([_I32, _I32, _I32, _I32, _I32, _I32, _I32], _SZ),
     "pa_cascade_pays": ([_I32, _I32, _I32, _I32, _I32], ctypes.c_int),
+    "pa_cascade_launches": ([_I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32], ctypes.c_int),
     "pa_cache_write_fp8": ([_P, _P, _P, _I64, _P, _P, CacheDesc, _F32, _F32, _P, _P], ctypes.c_int),
     "pa_decode_splitkv_fp8": ([_P, _P, _P, _P, _P, CacheDesc, _F32, _F32, _P, _I32, _P, _I32, _I32,
                                _F32, _I32, _P, _SZ, _P, _P], ctypes.c_int),
@@ -388,6 +389,14 @@ def pa_cascade_workspace_bytes(B: int, Hq: int, Hkv: int, D: int, n_prefix_block
                                max_blocks_per_seq: int, block_size: int) -> int:
     return int(lib().pa_cascade_workspace_bytes(B, Hq, Hkv, D, n_prefix_blocks, max_blocks_per_seq,
                                                 block_size))
+
+
+def pa_cascade_launches(B: int, Hq: int, Hkv: int, D: int, n_prefix_blocks: int,
+                        max_blocks_per_seq: int, block_size: int, sm_count: int) -> int:
+    r = lib().pa_cascade_launches(B, Hq, Hkv, D, n_prefix_blocks, max_blocks_per_seq, block_size,
+                                  sm_count)
+    _check("pa_cascade_launches", min(r, 0))
+    return r
 
 
 def pa_cascade_pays(B: int, Hkv: int, D: int, n_prefix_blocks: int, block_size: int) -> bool:

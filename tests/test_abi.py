@@ -134,6 +134,25 @@ def test_split_policy_short_contexts(lib, use_kernel):
     assert pa.pa_choose_num_splits(1, 28, 4, 128, 256, 16, 152) == 128
 
 
+def test_cascade_launches(lib, use_kernel, cascade_mode):
+    use_kernel("auto")
+    cascade_mode("auto")
+    C = pa.pa_cascade_launches
+    # 256 sequences behind 8 shared blocks: no cascade; the plain split runs in
+    # waves (P = 3): partials, then the combine
+    assert C(256, 16, 8, 128, 8, 128, 16, 148) == 2
+    # 256 behind 2048 tokens: prefix pass, unsplit suffix pass, combine
+    assert C(256, 16, 8, 128, 128, 144, 16, 148) == 3
+    # 8 behind 16384 tokens: the split suffix pass merges both passes' partials
+    assert C(8, 16, 8, 128, 1024, 1040, 16, 148) == 2
+    assert C(0, 16, 8, 128, 8, 128, 16, 148) == 0
+    assert lib.pa_cascade_launches(8, 16, 8, 128, 128, 128, 16, 148) == pa.PA_EINVAL  # no own blocks
+    assert lib.pa_cascade_launches(8, 16, 8, 128, 8, 128, 16, 0) == pa.PA_EINVAL
+    cascade_mode("never")
+    assert C(256, 16, 8, 128, 128, 144, 16, 148) == 2    # plain split in waves + combine
+    assert C(8, 16, 8, 128, 1024, 1040, 16, 148) == 1    # plain split, merged in the launch
+
+
 def test_split_policy_fills_small_batches(lib, use_kernel):
     use_kernel("auto")
     # one work unit (B=1, all 4 KV heads in one CTA) at 32k tokens: the split fills every SM

@@ -147,6 +147,54 @@ def test_fused_merge_many_partitions(lens, P, use_kernel):
         assert dev.status_value() == 0
 
 
+@pytest.mark.parametrize("P", [2, 3, 4, 5])
+def test_split_grid_in_waves(P, use_kernel):
+    """A split grid that runs in waves (200 sequences of all 8 KV heads per CTA:
+    200 CTAs per partition on 152 SMs): partials, then the combine kernel.
+    Lengths from 0 to 300 leave some partitions empty; a second call on the
+    same workspace gives the same result, and the fused step and FP8 pools
+    take the same path."""
+    use_kernel("auto")
+    rng = np.random.default_rng(70 + P)
+    lens = [int(x) for x in rng.integers(0, 301, size=200)]
+    w = _small(16, 8, 128, 16, lens, seed=P, poison_unused=True)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert pa.pa_decode_launches(w.B, 1, w.Hq, w.Hkv, w.D, w.max_blocks, w.block_size, P, sms) == 2
+    kc, vc = oracle_after_write(w)
+    ref, ref_lse = oracle.decode(w.q, kc, vc, w.block_tables, w.seq_lens, w.scale)
+    dev = Dev(w)
+    dev.write()
+    ws = torch.zeros(max(1, pa.pa_splitkv_workspace_bytes(w.B, w.Hq, w.D, P)), dtype=torch.uint8,
+                     device="cuda")
+    for rep in range(2):
+        out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device="cuda")
+        pa.pa_decode_splitkv(out, lse, dev.q, dev.k_cache, dev.v_cache, dev.block_tables,
+                             dev.seq_lens, w.scale, num_splits=P, workspace=ws, status=dev.status)
+        assert_close(bf16_dev_to_f64(out), ref, f"P={P} call {rep}")
+        assert_lse_close(lse.cpu().double().numpy(), ref_lse, f"P={P} call {rep}")
+    assert dev.status_value() == 0
+    # the fused write + decode
+    dev2 = Dev(w)
+    so, sl, _ = dev2.step(P)
+    assert_close(bf16_dev_to_f64(so), ref, f"step P={P}")
+    assert_lse_close(sl.cpu().double().numpy(), ref_lse, f"step P={P}")
+    assert dev2.status_value() == 0
+    # FP8 pools
+    w8 = W.with_fp8_pools(w)
+    ref8, ref8_lse = oracle.decode_fp8(w8.q, w8.k_cache8, w8.v_cache8, w8.block_tables, w8.seq_lens,
+                                       w8.scale, w8.k_scale, w8.v_scale)
+    kc8, vc8 = _fp8_dev(w8)
+    ws.zero_()
+    out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device="cuda")
+    pa.pa_decode_splitkv_fp8(out, lse, dev.q, kc8, vc8, w8.k_scale, w8.v_scale, dev.block_tables,
+                             dev.seq_lens, w.scale, num_splits=P, workspace=ws, status=dev.status)
+    assert_close(bf16_dev_to_f64(out), ref8, f"fp8 P={P}")
+    assert_lse_close(lse.cpu().double().numpy(), ref8_lse, f"fp8 P={P}")
+    assert dev.status_value() == 0
+
+
 @pytest.mark.parametrize("Hkv", [1, 2])
 @pytest.mark.parametrize("P", [257, 300])
 def test_more_partitions_than_the_in_launch_merge_holds(P, Hkv, use_kernel):
