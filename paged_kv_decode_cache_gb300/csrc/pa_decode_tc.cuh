@@ -57,7 +57,7 @@
 //   warps 8-11 (FP8 pools only): the producers land the e4m3 codes in 16 KB
 //        stages (so twice the token rows are in flight for the same shared
 //        memory); warp 8 + q widens TMEM lanes 32 q .. 32 q + 31 of each
-//        chunk's K and V^T into fp16 operand buffers in TMEM (two per tensor),
+//        chunk's K and V^T into fp16 operand buffers in TMEM (two or three per tensor),
 //        from which the QK and PV MMAs read their A operand.  k_scale is
 //        folded into the softmax scale and v_scale into the epilogue.
 // With the range split, the CTAs of one (sequence, head group) merge their
@@ -138,17 +138,26 @@ struct TcCfg {
     static constexpr int kNBS = (F8 && kN == 64) ? 2 : kTcNBS;
     // chunk validity masks the producers publish (ring slots)
     static constexpr int kMaskRing = F8 ? 16 : kTcMaskRing;
+    // TMEM: S buffers (NBS x N columns), O^T (hi part N, lo part N), then with
+    // FP8 pools the widened K and V^T operands, NOB buffers of 64 columns each
+    // (128 rows x 128 16-bit values) starting on a 64-column boundary: three
+    // where they fit in the 512 columns (N = 16), else two
+    static constexpr int kColO = kNBS * kN;
+    static constexpr int kColK = (kColO + 2 * kN + 63) / 64 * 64;
+    static constexpr int kNOB = (F8 && kColK + 6 * 64 <= 512) ? 3 : 2;
+    static constexpr int kColV = kColK + 64 * kNOB;
+    static constexpr int kColsUsed = F8 ? kColV + 64 * kNOB : kColO + 2 * kN;
     // A K (V) stage in shared memory: a bf16 chunk (32 KB), or with FP8 pools
     // the chunk's one-byte codes (16 KB), which the converter warps widen into
     // TMEM (the MMAs read their A operands there).
     static constexpr int kStageBytes = F8 ? kTcRows * 128 : kTileBytes;
     // shared memory for nk K stages, nv V stages and nbp P^T buffers, laid out
     // as below (rings, Q, P^T, scratch, barriers, masks, block-id rings, align)
-    // (FP8: the operand buffers' "widened" and "released" barriers, 2 each for
+    // (FP8: the operand buffers' "widened" and "released" barriers, NOB each for
     // K and V, and the V producer's mask ring)
     static constexpr int smem_for(int nk, int nv, int nbp, int gpr = GP) {
         return ((nk + nv) * kStageBytes + kQBytes + nbp * kPBufBytes + red_bytes(gpr) + 7) / 8 * 8 +
-               (2 * nk + 2 * nv + 2 * kNBS + 2 * nbp + (F8 ? 8 : 0) + 2) * 8 +
+               (2 * nk + 2 * nv + 2 * kNBS + 2 * nbp + (F8 ? 4 * kNOB : 0) + 2) * 8 +
                kMaskRing * 8 * (F8 ? 2 : 1) + 2 * (kTcLook + 1) * 32 * 4 + kAlignSlack;
     }
     // bf16: the deepest pipeline that fits: K and V stages first, then P^T buffers
@@ -178,7 +187,7 @@ struct TcCfg {
     static constexpr int kRedOff = kPOff + kNBP * kPBufBytes;
     static constexpr int kBarOff = (kRedOff + kRedBytes + 7) / 8 * 8;
     // (+ 2: the MMA issuers' drain barriers, committed to only by an aborting CTA)
-    static constexpr int kNumBars = 2 * kNK + 2 * kNV + 2 * kNBS + 2 * kNBP + (F8 ? 8 : 0) + 2;
+    static constexpr int kNumBars = 2 * kNK + 2 * kNV + 2 * kNBS + 2 * kNBP + (F8 ? 4 * kNOB : 0) + 2;
     // validity masks [kMaskRing] (u64: chunk << 32 | lane mask), then the two
     // producers' block-id rings [2][kTcLook + 1][32 lanes]
     static constexpr int kMaskOff = kBarOff + kNumBars * 8;
@@ -187,17 +196,11 @@ struct TcCfg {
     static constexpr int kSmemBytes = kLookOff + 2 * (kTcLook + 1) * 32 * 4 + kAlignSlack;
     static_assert(kSmemBytes == smem_for(kNK, kNV, kNBP, kGPr), "layout");
     // the K producer rewrites mask slot c % ring only once softmax c has read it
-    // (FP8: the producer runs at most NK stages, 3 chunks of converter and
-    // operand buffers and NBS S buffers ahead of the softmax)
-    static_assert(kNK + kNBS + (F8 ? 3 : 0) <= kMaskRing, "mask ring");
+    // (FP8: the producer runs at most NK stages, NOB + 1 chunks of converter
+    // and operand buffers and NBS S buffers ahead of the softmax)
+    static_assert(kNK + kNBS + (F8 ? kNOB + 1 : 0) <= kMaskRing, "mask ring");
     static_assert(kSmemBytes <= kTcSmemLimit, "shared memory");
-    // TMEM: S buffers (NBS x N columns), O^T (hi part N, lo part N), then with
-    // FP8 pools the widened K and V^T operands, two buffers of 64 columns each
-    // (128 rows x 128 16-bit values), starting on a 64-column boundary
-    static constexpr int kColO = kNBS * kN;
-    static constexpr int kColK = (kColO + 2 * kN + 63) / 64 * 64;
-    static constexpr int kColV = kColK + 128;
-    static constexpr int kColsUsed = F8 ? kColV + 128 : kColO + 2 * kN;
+
     static constexpr uint32_t kTmemCols = kColsUsed <= 128 ? 128u : kColsUsed <= 256 ? 256u : 512u;
     static_assert(kColsUsed <= 512, "TMEM columns");
 };
@@ -294,8 +297,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     uint64_t *kfull = bars, *kempty = bars + NK, *vfull = bars + 2 * NK, *vempty = vfull + NV;
     uint64_t *sdone = vempty + NV, *sfree = sdone + NBS, *pready = sfree + NBS;
     uint64_t *pfree = pready + NBP;
-    // FP8: operand buffer (chunk c & 1) widened into TMEM, and released by its MMAs
-    uint64_t *kconv = pfree + NBP, *kopfree = kconv + 2, *vconv = kopfree + 2, *vopfree = vconv + 2;
+    // FP8: operand buffer (chunk c % NOB) widened into TMEM, and released by its MMAs
+    constexpr int NOB = C::kNOB;
+    uint64_t *kconv = pfree + NBP, *kopfree = kconv + NOB, *vconv = kopfree + NOB, *vopfree = vconv + NOB;
     // QK and PV issuers: an aborting CTA commits here, so that it frees TMEM
     // only once every MMA it issued has completed
     uint64_t *drain = bars + C::kNumBars - 2;
@@ -594,7 +598,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         mbar_init(&drain[0], 1u);
         mbar_init(&drain[1], 1u);
         if (F8)  // operand buffers: "widened" by the four converter warps, "released" by a commit
-            for (int i = 0; i < 2; ++i) {
+            for (int i = 0; i < NOB; ++i) {
                 mbar_init(&kconv[i], 4u);
                 mbar_init(&vconv[i], 4u);
                 mbar_init(&kopfree[i], 1u);
@@ -643,9 +647,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             int done = 0;
             for (int c = 0; c < nch; ++c) {
                 // S buffer c % NBS is free once softmax c - NBS has read it; K c has
-                // landed (FP8: has been widened into TMEM operand buffer c & 1)
+                // landed (FP8: has been widened into TMEM operand buffer c % NOB)
                 if (c >= NBS && !wait_or_abort(&sfree[c % NBS], ((c / NBS) - 1) & 1)) break;
-                if (!wait_or_abort(F8 ? &kconv[c & 1] : &kfull[c % NK], F8 ? (c >> 1) & 1 : (c / NK) & 1)) break;
+                if (!wait_or_abort(F8 ? &kconv[c % NOB] : &kfull[c % NK], F8 ? (c / NOB) & 1 : (c / NK) & 1)) break;
                 tc5::fence_after_sync();
                 const uint8_t *kt = kring + (c % NK) * C::kStageBytes;
                 const uint32_t dcol = tmem + (c % NBS) * N;
@@ -654,13 +658,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                     const int half = j >> 2, off = (j & 3) * 32;
                     const uint64_t qdesc = tc5::sw128_desc(qs + half * (N * kSubBytes) + off, 16, 1024);
                     if constexpr (F8)  // A: lane m, column d / 2 of the widened chunk
-                        tc5::mma_f16_tmem_a(dcol, tmem + C::kColK + 64 * (c & 1) + 8 * j, qdesc, kIdQK, j > 0);
+                        tc5::mma_f16_tmem_a(dcol, tmem + C::kColK + 64 * (c % NOB) + 8 * j, qdesc, kIdQK, j > 0);
                     else
                         tc5::mma_bf16(dcol, tc5::sw128_desc(kt + half * C::kSubTile + off, 16, 1024), qdesc,
                                       kIdQK, j > 0);
                 }
                 tc5::commit(&sdone[c % NBS]);
-                tc5::commit(F8 ? &kopfree[c & 1] : &kempty[c % NK]);
+                tc5::commit(F8 ? &kopfree[c % NOB] : &kempty[c % NK]);
                 done = c + 1;
             }
             if (*abort_flag && done > 0) {  // let issued MMAs finish before TMEM is freed
@@ -676,7 +680,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             int done = 0;
             for (int c = 0; c < nch; ++c) {
                 if (!wait_or_abort(&pready[c % NBP], (c / NBP) & 1)) break;
-                if (!wait_or_abort(F8 ? &vconv[c & 1] : &vfull[c % NV], F8 ? (c >> 1) & 1 : (c / NV) & 1)) break;
+                if (!wait_or_abort(F8 ? &vconv[c % NOB] : &vfull[c % NV], F8 ? (c / NOB) & 1 : (c / NV) & 1)) break;
                 tc5::fence_after_sync();
                 const uint8_t *vt = vring + (c % NV) * C::kStageBytes;
                 const uint8_t *pt = ps + (c % NBP) * C::kPBufBytes;
@@ -686,14 +690,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                         C::kPMn ? tc5::sw128_desc(pt + j * 16 * kSubBytes, C::kSubTile, 1024)
                                 : tc5::sw128_desc(pt + (j >> 2) * (2 * N * kSubBytes) + (j & 3) * 32, 16, 1024);
                     if constexpr (F8)  // A: V^T widened into TMEM, 16 rows of P^T = 8 columns
-                        tc5::mma_f16_tmem_a(tmem + C::kColO, tmem + C::kColV + 64 * (c & 1) + 8 * j, bdesc,
+                        tc5::mma_f16_tmem_a(tmem + C::kColO, tmem + C::kColV + 64 * (c % NOB) + 8 * j, bdesc,
                                             kIdPV, c > 0 || j > 0);
                     else
                         tc5::mma_bf16(tmem + C::kColO, tc5::sw128_desc(vt + j * 16 * kSubBytes, C::kSubTile, 1024),
                                       bdesc, kIdPV, c > 0 || j > 0);
                 }
                 tc5::commit(&pfree[c % NBP]);
-                tc5::commit(F8 ? &vopfree[c & 1] : &vempty[c % NV]);
+                tc5::commit(F8 ? &vopfree[c % NOB] : &vempty[c % NV]);
                 done = c + 1;
             }
             if (*abort_flag && done > 0) {
@@ -704,7 +708,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     } else if (F8 && warp >= kTcCvtWarp) {
         // ================= FP8 converters: widen each chunk's e4m3 codes into TMEM =================
         // Warp 8 + q4 writes TMEM lanes 32 q4 .. 32 q4 + 31 of both operand
-        // buffers (c & 1) of chunk c:
+        // buffers (c % NOB) of chunk c:
         //   K (QK's A): lane m = row m of the chunk, column d / 2 = fp16 pair
         //     (d, d + 1): thread = row, its 128 codes read whole.
         //   V^T (PV's A): lane L holds head dim vt_dim(L) of the V rows, column
@@ -713,7 +717,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         //     along the contraction; the P^T rows follow the same order).
         //   Rows the V producer did not load, or past the range, widen to zeros,
         //   so 0 * (stale bytes) never reaches O^T.
-        // An operand buffer is rewritten once the MMAs of chunk c - 2 have read
+        // An operand buffer is rewritten once the MMAs of chunk c - NOB have read
         // it; the code stage is released once its codes are widened.  The
         // passes are loops, not unrolled: the warp roles of a CTA run different
         // code at once, and compact loops stay in the instruction cache.
@@ -722,11 +726,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         const bool do_v = C::kCvtWarps == 4 || warp >= kTcCvtWarp + 4;
         const int m = 32 * q4 + lane;  // this thread's K row
         for (int c = 0; c < nch; ++c) {
-            const int ob = c & 1;
+            const int ob = c % NOB;
             // ---- K: 32 columns (64 codes of row m) per pass ----
             if (do_k) {
                 if (!wait_or_abort(&kfull[c % NK], (c / NK) & 1)) break;
-                if (c >= 2 && !wait_or_abort(&kopfree[ob], ((c >> 1) - 1) & 1)) break;
+                if (c >= NOB && !wait_or_abort(&kopfree[ob], ((c / NOB) - 1) & 1)) break;
                 tc5::fence_after_sync();
                 const uint8_t *krow = kring + (c % NK) * C::kStageBytes + m * kSubBytes;
                 const uint32_t kcol = tc5::taddr(tmem, 32 * q4, C::kColK + 64 * ob);
@@ -773,7 +777,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                 }
             }
             if (!wait_or_abort(&vfull[c % NV], (c / NV) & 1)) break;
-            if (c >= 2 && !wait_or_abort(&vopfree[ob], ((c >> 1) - 1) & 1)) break;
+            if (c >= NOB && !wait_or_abort(&vopfree[ob], ((c / NOB) - 1) & 1)) break;
             tc5::fence_after_sync();
             const uint32_t vm = static_cast<uint32_t>(mk);
             const int tok_c = t_begin + c * C::kT;
