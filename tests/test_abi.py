@@ -4,6 +4,7 @@ that reject before any CUDA call) behaves as documented.  No GPU needed."""
 import ctypes
 import subprocess
 
+import numpy as np
 import pytest
 import torch
 
@@ -122,6 +123,34 @@ def test_decode_launches(lib, use_kernel):
     assert L(0, 1, 28, 4, 128, 256, 16, 0, 148) == 0
     assert lib.pa_decode_launches(8, 1, 28, 5, 128, 256, 16, 0, 148) == pa.PA_EINVAL
     assert lib.pa_decode_launches(8, 1, 28, 4, 128, 256, 16, 0, 0) == pa.PA_EINVAL
+
+
+def test_split_policy_properties_on_random_shapes(lib, use_kernel):
+    """The split choice's rules on 300 seeded shapes: 1 <= P <= 256; no empty
+    tail partition; partitions of at least 2 tiles; more than 32 partitions
+    only where 4-tile partitions would already number more than 32; one wave
+    of resident CTAs whenever the units alone fit."""
+    use_kernel("auto")
+    rng = np.random.default_rng(2024)
+    for _ in range(300):
+        Hkv = int(rng.choice([1, 2, 4, 8]))
+        G = int(rng.choice([1, 2, 4, 6, 7, 8]))
+        B = int(rng.integers(1, 300))
+        bs = int(rng.choice([16, 32, 256]))
+        mb = int(rng.integers(1, 4096 // bs + 2))
+        sms = int(rng.choice([132, 148, 152]))
+        Hq = G * Hkv
+        P = pa.pa_choose_num_splits(B, Hq, Hkv, 128, mb, bs, sms)
+        lmax = mb * bs
+        tiles = -(-lmax // 16)
+        assert 1 <= P <= 256
+        chunk = pa.pa_partition_tokens(mb, bs, P)
+        assert chunk * P >= lmax and chunk * (P - 1) < lmax
+        assert P == 1 or chunk >= 32
+        assert P <= 32 or -(-tiles // 4) > 32
+        units = _units(B, Hq, Hkv, 128)
+        if units <= sms and P > 1:
+            assert units * P <= sms
 
 
 def test_split_policy_short_contexts(lib, use_kernel):
